@@ -1,0 +1,203 @@
+/*
+ * moe_route_permute.h -- C ABI of the GB300 (sm_103a) MoE layer hot path.
+ *
+ * The path is the single-GPU Route -> Dispatch -> Compute -> Combine of an MoE
+ * layer, with a local permute in place of the all-to-all (report "Scalable
+ * Training of Mixture-of-Experts Models with Megatron Core": summary page,
+ * "Problem Definition", "Pipeline Flow" and "System Modules"; figures & tables
+ * page, Fig. 1 and Fig. 2), and its training backward.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensors are dense, row-major, in DEVICE memory of the current CUDA
+ *    device, and allocated by the caller. The library allocates nothing on the
+ *    GPU and keeps no per-call state. Pointers must be 16-byte aligned.
+ *  - bf16 tensors are passed as moe_bf16* (IEEE bfloat16 bit patterns).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call only enqueues work on `stream` and returns; nothing synchronises
+ *    the host, and counts/offsets stay on the device.
+ *  - Return value: MOE_OK or a host-detected error (invalid argument,
+ *    unsupported shape, workspace too small, CUDA launch error). On an error
+ *    nothing has been enqueued. Errors detected on the device (a bounded wait
+ *    that ran out, an index out of range) are recorded in a status word in the
+ *    workspace and read back with moe_get_device_status().
+ *  - Sizes: T tokens, H hidden, E experts, k experts per token, F expert FFN
+ *    width, R = T*k routed rows, Fs shared-expert width.
+ *  - Supported shapes: H and F multiples of 64; 1 <= k <= min(E, 16);
+ *    E <= 256; E divisible by n_groups; Fs multiple of 64 (or 0);
+ *    T >= 1 and T*k < 2^30.
+ */
+#ifndef MOE_ROUTE_PERMUTE_H
+#define MOE_ROUTE_PERMUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, k > E, bad enum, ...        */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* outside the supported shapes above        */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+  MOE_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed          */
+  MOE_ERR_DEVICE_TIMEOUT = 5,     /* device: a bounded wait ran out             */
+  MOE_ERR_DEVICE_INDEX = 6        /* device: an expert or row index out of range */
+} moe_status;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+
+/* Layer description. Router options (figures & tables page, Fig. 2: linear
+ * projection, score function, top-k selection, load balancing):
+ *   score        softmax over the E experts, or element-wise sigmoid;
+ *   n_groups,
+ *   topk_groups  group-limited selection: experts split into n_groups
+ *                contiguous groups, a group scored by the sum of its two best
+ *                selection values, only the best topk_groups groups eligible
+ *                (1,1 = plain top-k);
+ *   gate_scale   gates = gate_scale * score_i / sum over the k selected scores;
+ *   aux_coeff    coefficient alpha of the load-balancing loss
+ *                alpha * E * sum_e (c_e / (T k)) * mean_t p[t,e] (training);
+ *   out_fp32     y (forward) and dx (backward) written as fp32 instead of bf16;
+ *   inter_fp32   expert outputs y_perm and the shared-expert output kept in
+ *                fp32 instead of bf16. */
+typedef struct {
+  int T, H, E, k, F;
+  int F_shared;      /* 0 = no shared expert */
+  int score;         /* moe_score_fn */
+  int n_groups, topk_groups;
+  float gate_scale;
+  float aux_coeff;
+  int out_fp32;
+  int inter_fp32;
+} moe_config;
+
+/* Tensors the training forward keeps for the backward (all caller-owned).
+ * Shapes: topk_idx, row_id_map [T,k] int32; topk_gate [T,k] fp32;
+ * logits [T,E] fp32 (router logits incl. logit_bias); counts [E] int32;
+ * offsets [E+1] int32; x_perm [R,H] bf16; h13 [R,2F] bf16 (gate
+ * pre-activation x W1 in columns [0,F), up projection x W3 in [F,2F));
+ * a [R,F] bf16 (SiLU(h1)*h3); y_perm [R,H] bf16 (fp32 if inter_fp32);
+ * aux_partials [4*ceil(T/128), E] fp32 (column sums of the full softmax over
+ * consecutive 32-token slices; only when aux_coeff != 0, else may be NULL). */
+typedef struct {
+  int32_t* topk_idx;
+  float* topk_gate;
+  float* logits;
+  int32_t* row_id_map;
+  int32_t* counts;
+  int32_t* offsets;
+  moe_bf16* x_perm;
+  moe_bf16* h13;
+  moe_bf16* a;
+  void* y_perm;
+  float* aux_partials;
+} moe_fwd_saved;
+
+/* Bytes of device workspace the calls below need (training != 0: the
+ * backward's needs included). The workspace is caller-owned scratch; its first
+ * bytes hold the device status word. It must stay allocated until the enqueued
+ * work has finished; two calls in flight at once must use two workspaces. */
+size_t moe_workspace_bytes(const moe_config* cfg, int training);
+
+/* Router (figures & tables page, Fig. 2; summary page, "System Modules",
+ * Router: a learned linear layer + softmax choosing the top-k experts):
+ *   L = x router_w^T (+ logit_bias),  x [T,H] bf16, router_w [E,H] bf16;
+ *   scores = softmax(L) or sigmoid(L);
+ *   selection on scores (+ expert_bias [E] fp32, selection only), optionally
+ *   group-limited; ties go to the lower expert index; slots ordered by
+ *   descending selection value;
+ *   topk_gate[t,i] = gate_scale * score[e_i] / sum_j score[e_j].
+ * Outputs topk_idx [T,k] int32, topk_gate [T,k] fp32; optional logits_out
+ * [T,E] fp32 and aux_partials [4*ceil(T/128),E] fp32 (softmax column sums per
+ * 32-token slice; rows past the last token are zero). expert_bias, logit_bias, logits_out, aux_partials may be
+ * NULL. The bf16 products are exact and accumulate in fp32 on the tensor
+ * cores. */
+int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                    const float* expert_bias, const float* logit_bias,
+                    int32_t* topk_idx, float* topk_gate, float* logits_out,
+                    float* aux_partials, void* ws, size_t ws_bytes, void* stream);
+
+/* Local dispatch (summary page, "Key Terms", Grouped GEMM; figures & tables
+ * page, Fig. 7 and Fig. 20): counts[e] = number of (t,i) routed to e;
+ * offsets [E+1] = exclusive prefix sum (offsets[E] = T*k); row_id_map[t,i] =
+ * offsets[e] + number of tokens t' < t routed to e (rows grouped by expert, in
+ * token order within an expert; dropless); x_perm[row_id_map[t,i]] = x[t].
+ * Deterministic. Device errors: an index outside [0,E) sets
+ * MOE_ERR_DEVICE_INDEX (that entry is skipped); a bounded wait of the scan sets
+ * MOE_ERR_DEVICE_TIMEOUT. */
+int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx,
+                moe_bf16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped SwiGLU experts (summary page, "Key Terms", Grouped GEMM and
+ * "System Modules", Experts; figures & tables page, Table 4): for each expert
+ * e, rows offsets[e]..offsets[e+1] of x_perm [R,H]:
+ *   h1 = x W1[e], h3 = x W3[e]   (W1, W3 [E,H,F] bf16; W1 is the gate),
+ *   a  = bf16(SiLU(h1) * h3),
+ *   y_perm = a W2[e]             (W2 [E,F,H] bf16), bf16 (fp32 if inter_fp32).
+ * `offsets` is read on the device (no host synchronisation). h13_save [R,2F]
+ * and a_save [R,F] are optional outputs for the backward; without a_save the
+ * activation lives in the workspace. */
+int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const int32_t* offsets,
+                           const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                           moe_bf16* h13_save, moe_bf16* a_save, void* y_perm,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Combine (summary page, "Problem Definition" and "System Modules", Combiner;
+ * figures & tables page, Fig. 40 for the shared expert):
+ *   y[t] = sum_{i=0..k-1} topk_gate[t,i] * y_perm[row_id_map[t,i]] (+ shared_out[t]),
+ * reduced in fp32 in slot order. y_perm and shared_out are bf16 (fp32 if
+ * inter_fp32); y [T,H] is bf16 (fp32 if out_fp32). shared_out may be NULL. */
+int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_id_map,
+                          const float* topk_gate, const void* shared_out, void* y, void* stream);
+
+/* Whole layer forward = router -> permute -> grouped SwiGLU -> (shared
+ * expert) -> combine. Ws1, Ws3 [H,Fs], Ws2 [Fs,H] bf16 when F_shared > 0
+ * (the shared expert processes every token and is added ungated).
+ * saved != NULL (training): every field of *saved must be set and receives
+ * the tensors for moe_layer_bwd; saved == NULL (inference): intermediates live
+ * in the workspace. */
+int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                  const float* expert_bias, const float* logit_bias,
+                  const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                  const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2,
+                  void* y, const moe_fwd_saved* saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Whole layer backward for the loss <dO, y> + L_aux (the chain rule of the
+ * forward; top-k selection and counts carry no gradient). dO [T,H] bf16.
+ * Outputs: dx [T,H] (bf16, fp32 if out_fp32); dW_router [E,H], dW1, dW3
+ * [E,H,F], dW2 [E,F,H] fp32 (overwritten, zero for experts with no tokens);
+ * aux_loss_out (1 fp32, may be NULL; written when aux_coeff != 0). Supported
+ * for F_shared == 0. */
+int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x,
+                  const moe_bf16* router_w, const moe_bf16* W1, const moe_bf16* W3,
+                  const moe_bf16* W2, const moe_fwd_saved* saved,
+                  void* dx, float* dW_router, float* dW1, float* dW3, float* dW2,
+                  float* aux_loss_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns in *status_out the first device-side error
+ * recorded in `ws` since the last read (MOE_OK if none) and clears it. For
+ * tests and debugging; the hot path never calls it. */
+int moe_get_device_status(void* ws, void* stream, int* status_out);
+
+/* Static text for a moe_status value. */
+const char* moe_status_string(int status);
+
+/* Test hooks (not for production use). moe_debug_set_wait_limit_ns sets the
+ * limit of every bounded device wait (default 2e9 ns = 2 s; 0 restores the
+ * default). moe_debug_set_fault(1) makes the permute scan's first token chunk
+ * skip publishing its counts, so that the other chunks' waits run out and the
+ * device status reports MOE_ERR_DEVICE_TIMEOUT; moe_debug_set_fault(0) turns
+ * it off. Both are process-wide. */
+void moe_debug_set_wait_limit_ns(long long ns);
+void moe_debug_set_fault(int fault);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ROUTE_PERMUTE_H */

@@ -1,0 +1,516 @@
+// The C ABI: argument checks, workspace layout, tensor maps and the
+// composition of the kernels into the layer forward and backward.
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "host_util.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// process-wide settings
+// ---------------------------------------------------------------------------
+static unsigned long long g_wait_limit_ns = 2000000000ull;
+static int g_fault = 0;
+unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
+int debug_fault() { return g_fault; }
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps through the driver entry point (no link-time libcuda)
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                   uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t status, lookback;
+  // forward intermediates (inference, or standalone grouped FFN without a_save)
+  size_t topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
+  // backward
+  size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part;
+  size_t total;
+};
+
+static int padded_experts(int E) { return ((E + 63) / 64) * 64; }
+static int router_dw_splits(int T) {
+  const int kbh = (T + kBK - 1) / kBK;
+  int s = 16;
+  if (2 * kbh < s) s = 2 * kbh;
+  return s < 1 ? 1 : s;
+}
+
+static WsLayout ws_layout(const moe_config& c, bool training) {
+  WsLayout L{};
+  const size_t T = c.T, H = c.H, E = c.E, k = c.k, F = c.F, R = T * k;
+  const size_t inter = c.inter_fp32 ? 4 : 2;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  L.status = take(sizeof(DevStatus));
+  L.lookback = take(sizeof(int32_t) * permute_lookback_ints(c.T, c.E));
+  L.topk_idx = take(4 * T * k);
+  L.topk_gate = take(4 * T * k);
+  L.row_id_map = take(4 * T * k);
+  L.counts = take(4 * E);
+  L.offsets = take(4 * (E + 1));
+  L.x_perm = take(2 * R * H);
+  L.a = take(2 * R * F);
+  L.y_perm = take(inter * R * H);
+  L.as = c.F_shared ? take(2 * T * c.F_shared) : 0;
+  L.s_out = c.F_shared ? take(inter * T * H) : 0;
+  if (training) {
+    const size_t Ep = padded_experts(c.E);
+    L.dy_perm = take(2 * R * H);
+    L.dgate = take(4 * T * k);
+    L.dh13 = take(2 * R * 2 * F);
+    L.dx_perm = take(2 * R * H);
+    L.dL_hl = take(2 * T * 2 * Ep);
+    L.dx_r = take(4 * T * H);
+    L.dwr_part = take(4 * static_cast<size_t>(router_dw_splits(c.T)) * E * H);
+  }
+  L.total = o;
+  return L;
+}
+
+template <class P>
+static P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// checks
+// ---------------------------------------------------------------------------
+static int check_cfg(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->H < 1 || c->E < 1 || c->k < 1 || c->F < 1 || c->F_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (!(c->gate_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups < 1 || c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+  if (c->E % c->n_groups != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->n_groups > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->n_groups > 1 && c->topk_groups < c->n_groups && c->k > c->topk_groups * (c->E / c->n_groups))
+    return MOE_ERR_INVALID_ARG;
+  if (c->k > 16 || c->E > 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->H % 64 != 0 || c->F % 64 != 0 || c->F_shared % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(c->T) * c->k >= (1ll << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  fprintf(stderr, "moe: CUDA error %s\n", cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+static GemmParams base_params(const moe_config& c, DevStatus* st) {
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.T = c.T; p.H = c.H; p.E = c.E; p.k = c.k; p.F = c.F;
+  p.bn = 256;
+  p.splits = 1;
+  p.status = st;
+  p.wait_limit_ns = g_wait_limit_ns;
+  p.gate_scale = c.gate_scale;
+  p.score = c.score;
+  p.n_groups = c.n_groups;
+  p.topk_groups = c.topk_groups;
+  return p;
+}
+
+#define MOE_TRY(x)                 \
+  do {                             \
+    int _s = (x);                  \
+    if (_s != MOE_OK) return _s;   \
+  } while (0)
+#define MOE_CUDA(x) MOE_TRY(cuda_status(x))
+#define MOE_MAP(...)                                   \
+  do {                                                 \
+    if (!make_map_bf16(__VA_ARGS__)) return MOE_ERR_CUDA; \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// stages
+// ---------------------------------------------------------------------------
+static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* w_r, const float* eb,
+                      const float* lb, int32_t* idx, float* gate, float* logits, float* aux, DevStatus* st,
+                      cudaStream_t s) {
+  GemmParams p = base_params(c, st);
+  p.bn = ((c.E + 31) / 32) * 32;
+  p.n_tiles = 1;
+  p.ngroups = 1;
+  p.M_total = c.T;
+  p.kb_total = c.H / kBK;
+  p.offsets = nullptr;
+  p.has_expert_bias = eb != nullptr;
+  p.has_logit_bias = lb != nullptr;
+  p.expert_bias = eb;
+  p.logit_bias = lb;
+  p.topk_idx = idx;
+  p.topk_gate = gate;
+  p.logits_out = logits;
+  p.aux_partials = aux;
+  CUtensorMap ma, mb;
+  MOE_MAP(&ma, x, c.H, c.T, 2ull * c.H, 64, 128);
+  MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn);
+  const int tiles = (c.T + kBM - 1) / kBM;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  return cuda_status(launch_gemm(KIND_ROUTER, p, ma, mb, mb, grid, s));
+}
+
+// grouped (offsets != nullptr, rows of x_rows grouped by expert) or single-group
+// (offsets == nullptr, M rows) SwiGLU FFN: a = SiLU(x W1) * (x W3), y = a W2.
+static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offsets, int M,
+                   const __nv_bfloat16* x_rows, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
+                   const __nv_bfloat16* W2, __nv_bfloat16* h13, __nv_bfloat16* a, void* y, bool y_fp32,
+                   DevStatus* st, cudaStream_t s) {
+  GemmParams p = base_params(c, st);
+  p.F = F;
+  p.ngroups = ngroups;
+  p.offsets = offsets;
+  p.M_total = M;
+  // h = x [W1 | W3], 128 gate + 128 up columns per tile
+  p.n_tiles = (F + 127) / 128;
+  p.kb_total = c.H / kBK;
+  p.out0 = a;
+  p.out1 = h13;
+  CUtensorMap ma, m1, m3, m2;
+  MOE_MAP(&ma, x_rows, c.H, M, 2ull * c.H, 64, 128);
+  MOE_MAP(&m1, W1, F, static_cast<uint64_t>(ngroups) * c.H, 2ull * F, 64, 64);
+  MOE_MAP(&m3, W3, F, static_cast<uint64_t>(ngroups) * c.H, 2ull * F, 64, 64);
+  MOE_CUDA(launch_gemm(KIND_FFN1, p, ma, m1, m3, num_sms(), s));
+  // y = a W2
+  GemmParams q = base_params(c, st);
+  q.F = F;
+  q.ngroups = ngroups;
+  q.offsets = offsets;
+  q.M_total = M;
+  q.n_tiles = (c.H + 255) / 256;
+  q.kb_total = F / kBK;
+  q.out0 = y;
+  q.out_fp32 = y_fp32;
+  CUtensorMap mA;
+  MOE_MAP(&mA, a, F, M, 2ull * F, 64, 128);
+  MOE_MAP(&m2, W2, c.H, static_cast<uint64_t>(ngroups) * F, 2ull * c.H, 64, 64);
+  return cuda_status(launch_gemm(KIND_FFN2, q, mA, m2, m2, num_sms(), s));
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+// ---------------------------------------------------------------------------
+// exported C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config* cfg, int training) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg, training != 0).total;
+}
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device: bounded wait ran out";
+    case MOE_ERR_DEVICE_INDEX: return "device: index out of range";
+    default: return "unknown status";
+  }
+}
+
+void moe_debug_set_wait_limit_ns(long long ns) { g_wait_limit_ns = ns > 0 ? static_cast<unsigned long long>(ns) : 2000000000ull; }
+void moe_debug_set_fault(int fault) { g_fault = fault; }
+
+int moe_get_device_status(void* ws, void* stream, int* status_out) {
+  if (ws == nullptr || status_out == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaStreamSynchronize(s));
+  DevStatus h;
+  MOE_CUDA(cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost));
+  *status_out = h.status;
+  MOE_CUDA(cudaMemset(ws, 0, sizeof(DevStatus)));
+  return MOE_OK;
+}
+
+int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w, const float* expert_bias,
+                    const float* logit_bias, int32_t* topk_idx, float* topk_gate, float* logits_out,
+                    float* aux_partials, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (!x || !router_w || !topk_idx || !topk_gate || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(c, false).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return run_router(c, reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(router_w),
+                    expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials,
+                    at<DevStatus>(ws, 0), static_cast<cudaStream_t>(stream));
+}
+
+int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx, moe_bf16* x_perm,
+                int32_t* row_id_map, int32_t* counts, int32_t* offsets, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (!x || !topk_idx || !x_perm || !row_id_map || !counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, false);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_permute(c, reinterpret_cast<const __nv_bfloat16*>(x), topk_idx,
+                                    reinterpret_cast<__nv_bfloat16*>(x_perm), row_id_map, counts, offsets,
+                                    at<int32_t>(ws, L.lookback), at<DevStatus>(ws, 0),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const int32_t* offsets,
+                           const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, moe_bf16* h13_save,
+                           moe_bf16* a_save, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (!x_perm || !offsets || !W1 || !W3 || !W2 || !y_perm || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(y_perm) ||
+      !aligned16(ws) || (h13_save && !aligned16(h13_save)) || (a_save && !aligned16(a_save)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, false);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  __nv_bfloat16* a = a_save ? reinterpret_cast<__nv_bfloat16*>(a_save) : at<__nv_bfloat16>(ws, L.a);
+  return run_ffn(c, c.F, c.E, offsets, c.T * c.k, reinterpret_cast<const __nv_bfloat16*>(x_perm),
+                 reinterpret_cast<const __nv_bfloat16*>(W1), reinterpret_cast<const __nv_bfloat16*>(W3),
+                 reinterpret_cast<const __nv_bfloat16*>(W2), reinterpret_cast<__nv_bfloat16*>(h13_save), a, y_perm,
+                 c.inter_fp32 != 0, at<DevStatus>(ws, 0), static_cast<cudaStream_t>(stream));
+}
+
+int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_id_map,
+                          const float* topk_gate, const void* shared_out, void* y, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (!y_perm || !row_id_map || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(c, y_perm, row_id_map, topk_gate, shared_out, y, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w, const float* expert_bias,
+                  const float* logit_bias, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                  const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2, void* y, const moe_fwd_saved* saved,
+                  void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (!x || !router_w || !W1 || !W3 || !W2 || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (c.F_shared && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) ||
+      !aligned16(y) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, false);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  int32_t *idx, *rows, *counts, *offs;
+  float *gate, *logits = nullptr, *aux = nullptr;
+  __nv_bfloat16 *xp, *a, *h13 = nullptr;
+  void* yp;
+  if (saved != nullptr) {
+    if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
+        !saved->offsets || !saved->x_perm || !saved->h13 || !saved->a || !saved->y_perm)
+      return MOE_ERR_INVALID_ARG;
+    if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+    idx = saved->topk_idx; gate = saved->topk_gate; logits = saved->logits; rows = saved->row_id_map;
+    counts = saved->counts; offs = saved->offsets;
+    xp = reinterpret_cast<__nv_bfloat16*>(saved->x_perm);
+    h13 = reinterpret_cast<__nv_bfloat16*>(saved->h13);
+    a = reinterpret_cast<__nv_bfloat16*>(saved->a);
+    yp = saved->y_perm;
+    aux = c.aux_coeff != 0.0f ? saved->aux_partials : nullptr;
+  } else {
+    idx = at<int32_t>(ws, L.topk_idx); gate = at<float>(ws, L.topk_gate); rows = at<int32_t>(ws, L.row_id_map);
+    counts = at<int32_t>(ws, L.counts); offs = at<int32_t>(ws, L.offsets);
+    xp = at<__nv_bfloat16>(ws, L.x_perm); a = at<__nv_bfloat16>(ws, L.a); yp = at<void>(ws, L.y_perm);
+  }
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
+                     logits, aux, st, s));
+  MOE_CUDA(launch_permute(c, xb, idx, xp, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s));
+  MOE_TRY(run_ffn(c, c.F, c.E, offs, c.T * c.k, xp, reinterpret_cast<const __nv_bfloat16*>(W1),
+                  reinterpret_cast<const __nv_bfloat16*>(W3), reinterpret_cast<const __nv_bfloat16*>(W2), h13, a, yp,
+                  c.inter_fp32 != 0, st, s));
+  void* shared = nullptr;
+  if (c.F_shared) {
+    shared = at<void>(ws, L.s_out);
+    MOE_TRY(run_ffn(c, c.F_shared, 1, nullptr, c.T, xb, reinterpret_cast<const __nv_bfloat16*>(Ws1),
+                    reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), nullptr,
+                    at<__nv_bfloat16>(ws, L.as), shared, c.inter_fp32 != 0, st, s));
+  }
+  return cuda_status(launch_combine(c, yp, rows, gate, shared, y, s));
+}
+
+int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
+                  const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved, void* dx,
+                  float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws,
+                  size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
+      !saved->offsets || !saved->x_perm || !saved->h13 || !saved->a || !saved->y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  const int R = c.T * c.k;
+  const int Ep = padded_experts(c.E);
+  __nv_bfloat16* dy_perm = at<__nv_bfloat16>(ws, L.dy_perm);
+  float* dgate = at<float>(ws, L.dgate);
+  __nv_bfloat16* dh13 = at<__nv_bfloat16>(ws, L.dh13);
+  __nv_bfloat16* dx_perm = at<__nv_bfloat16>(ws, L.dx_perm);
+  __nv_bfloat16* dL_hl = at<__nv_bfloat16>(ws, L.dL_hl);
+  float* dx_r = at<float>(ws, L.dx_r);
+  float* dwr_part = at<float>(ws, L.dwr_part);
+
+  // 1. combine backward
+  MOE_CUDA(launch_combine_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), saved->y_perm, saved->row_id_map,
+                              saved->topk_gate, dy_perm, dgate, s));
+  // 2. router backward (element-wise): dL as bf16 hi/lo
+  MOE_CUDA(launch_router_bwd(c, saved->logits, saved->topk_idx, saved->topk_gate, dgate, saved->counts, Ep, dL_hl, s));
+  // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
+    p.n_tiles = (c.F + 255) / 256; p.kb_total = c.H / kBK;
+    p.out0 = dh13; p.in_aux = saved->h13;
+    CUtensorMap ma, mb;
+    MOE_MAP(&ma, dy_perm, c.H, R, 2ull * c.H, 64, 128);
+    MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 256);
+    MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s));
+  }
+  // 4. dW2_e = a_e^T dy_perm_e
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = c.E; p.offsets = saved->offsets;
+    p.wg_M = c.F; p.wg_N = c.H; p.wg_mode = 0;
+    p.m_tiles_fixed = (c.F + 127) / 128; p.n_tiles = (c.H + 255) / 256;
+    p.out0 = dW2;
+    CUtensorMap ma, mb;
+    MOE_MAP(&ma, saved->a, c.F, R, 2ull * c.F, 64, 64);
+    MOE_MAP(&mb, dy_perm, c.H, R, 2ull * c.H, 64, 64);
+    const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s));
+  }
+  // 5. dx_perm = dh13 [W1_e | W3_e]^T
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
+    p.n_tiles = (c.H + 255) / 256; p.kb_total = 2 * c.F / kBK;
+    p.out0 = dx_perm;
+    CUtensorMap ma, m1, m3;
+    MOE_MAP(&ma, dh13, 2ull * c.F, R, 4ull * c.F, 64, 128);
+    MOE_MAP(&m1, W1, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
+    MOE_MAP(&m3, W3, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
+    MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s));
+  }
+  // 6. dW1_e | dW3_e = x_perm_e^T dh13_e
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = c.E; p.offsets = saved->offsets;
+    p.wg_M = c.H; p.wg_N = 2 * c.F; p.wg_mode = 1;
+    p.m_tiles_fixed = (c.H + 127) / 128; p.n_tiles = (2 * c.F + 255) / 256;
+    p.out0 = dW1; p.out1 = dW3;
+    CUtensorMap ma, mb;
+    MOE_MAP(&ma, saved->x_perm, c.H, R, 2ull * c.H, 64, 64);
+    MOE_MAP(&mb, dh13, 2ull * c.F, R, 4ull * c.F, 64, 64);
+    const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s));
+  }
+  // 7. router part of dx: dx_r = dL W_r (fp32)
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = 1; p.offsets = nullptr; p.M_total = c.T;
+    p.n_tiles = (c.H + 255) / 256; p.kb_total = 2 * Ep / kBK; p.Ep = Ep;
+    p.out0 = dx_r;
+    CUtensorMap ma, mb;
+    MOE_MAP(&ma, dL_hl, 2ull * Ep, c.T, 4ull * Ep, 64, 128);
+    MOE_MAP(&mb, router_w, c.H, c.E, 2ull * c.H, 64, 64);
+    const int tiles = ((c.T + kBM - 1) / kBM) * p.n_tiles;
+    MOE_CUDA(launch_gemm(KIND_ROUTER_DX, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s));
+  }
+  // 8. dx = sum_i dx_perm[row(t,i)] + dx_r
+  MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s));
+  // 9. dW_r = dL^T x, split over K, then reduced in split order
+  {
+    const int splits = router_dw_splits(c.T);
+    const int total_kb = 2 * ((c.T + kBK - 1) / kBK);
+    GemmParams p = base_params(c, st);
+    p.ngroups = splits; p.offsets = nullptr; p.splits = splits;
+    p.kb_total = (total_kb + splits - 1) / splits;
+    p.m_tiles_fixed = (c.E + 127) / 128; p.n_tiles = (c.H + 255) / 256; p.Ep = Ep;
+    p.out0 = dwr_part;
+    CUtensorMap ma, mb;
+    MOE_MAP(&ma, dL_hl, 2ull * Ep, c.T, 4ull * Ep, 64, 64);
+    MOE_MAP(&mb, x, c.H, c.T, 2ull * c.H, 64, 64);
+    const int tiles = splits * p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_gemm(KIND_ROUTER_DW, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s));
+    MOE_CUDA(launch_split_reduce(dwr_part, splits, static_cast<size_t>(c.E) * c.H, dW_router, s));
+  }
+  // 10. aux loss value
+  if (c.aux_coeff != 0.0f && aux_loss_out != nullptr)
+    MOE_CUDA(launch_aux_loss(c, saved->aux_partials, saved->counts, aux_loss_out, s));
+  return MOE_OK;
+}
+
+}  // extern "C"

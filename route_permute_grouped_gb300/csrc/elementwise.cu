@@ -1,0 +1,306 @@
+// Bandwidth-bound kernels of the path: combine (weighted gather-sum), its
+// backward, the permute backward (unweighted gather-sum), the router's
+// element-wise backward, the auxiliary-loss value and the split-K reduction.
+// One warp per token, 16-byte vectors along H, fp32 arithmetic.
+#include "host_util.h"
+
+namespace moe {
+
+template <bool F32>
+struct Vec8 {  // 8 consecutive elements of a bf16 or fp32 row
+  __device__ __forceinline__ static void load(const void* base, size_t elem, float* f) {
+    if constexpr (F32) {
+      const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + elem);
+      const float4 a = __ldg(p), b = __ldg(p + 1);
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + elem));
+      f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+      f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+    }
+  }
+  __device__ __forceinline__ static void store(void* base, size_t elem, const float* f) {
+    if constexpr (F32) {
+      float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + elem);
+      p[0] = make_float4(f[0], f[1], f[2], f[3]);
+      p[1] = make_float4(f[4], f[5], f[6], f[7]);
+    } else {
+      uint4 w;
+      w.x = pack_bf16x2(f[0], f[1]); w.y = pack_bf16x2(f[2], f[3]);
+      w.z = pack_bf16x2(f[4], f[5]); w.w = pack_bf16x2(f[6], f[7]);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + elem) = w;
+    }
+  }
+};
+
+constexpr int kWarpsPerBlock = 8;
+
+// y[t] = shared[t] + sum_i g[t,i] * y_perm[row[t,i]]  (fp32, slot order).
+// With gate == nullptr the weights are 1 (permute backward) and `extra` (fp32,
+// nullable) is added instead of `shared`.
+template <bool YP32, bool SH32, bool OUT32>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    gather_sum_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ row_id_map,
+                      const float* __restrict__ gate, const void* __restrict__ shared, void* __restrict__ y, int T,
+                      int H, int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + warp;
+  if (t >= T) return;
+  int my_r = 0;
+  float my_g = 1.0f;
+  if (lane < k) {
+    my_r = row_id_map[static_cast<size_t>(t) * k + lane];
+    if (gate != nullptr) my_g = gate[static_cast<size_t>(t) * k + lane];
+  }
+  const int nvec = H / 8;
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8];
+    if (shared != nullptr) {
+      Vec8<SH32>::load(shared, static_cast<size_t>(t) * H + v * 8, acc);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    }
+    for (int i = 0; i < k; ++i) {
+      const int r = __shfl_sync(0xffffffffu, my_r, i);
+      const float g = __shfl_sync(0xffffffffu, my_g, i);
+      float f[8];
+      Vec8<YP32>::load(y_perm, static_cast<size_t>(r) * H + v * 8, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(g, f[j], acc[j]);
+    }
+    Vec8<OUT32>::store(y, static_cast<size_t>(t) * H + v * 8, acc);
+  }
+}
+
+// Combine backward: dy_perm[row[t,i]] = bf16(g[t,i] * dO[t]),
+// dgate[t,i] = <dO[t], y_perm[row[t,i]]> (fp32).
+template <bool YP32>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    combine_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ y_perm,
+                       const int32_t* __restrict__ row_id_map, const float* __restrict__ gate,
+                       __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dgate, int T, int H, int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + warp;
+  if (t >= T) return;
+  int my_r = 0;
+  float my_g = 0.0f;
+  if (lane < k) {
+    my_r = row_id_map[static_cast<size_t>(t) * k + lane];
+    my_g = gate[static_cast<size_t>(t) * k + lane];
+  }
+  float dot[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) dot[i] = 0.0f;
+  const int nvec = H / 8;
+  for (int v = lane; v < nvec; v += 32) {
+    float d[8];
+    Vec8<false>::load(dO, static_cast<size_t>(t) * H + v * 8, d);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < k) {
+        const int r = __shfl_sync(0xffffffffu, my_r, i);
+        const float g = __shfl_sync(0xffffffffu, my_g, i);
+        float f[8], o[8];
+        Vec8<YP32>::load(y_perm, static_cast<size_t>(r) * H + v * 8, f);
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          s = fmaf(d[j], f[j], s);
+          o[j] = g * d[j];
+        }
+        dot[i] += s;
+        Vec8<false>::store(dy_perm, static_cast<size_t>(r) * H + v * 8, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (i < k) {
+      float s = dot[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) dgate[static_cast<size_t>(t) * k + i] = s;
+    }
+  }
+}
+
+// Router backward, element-wise part (one warp per token). Gate gradient ->
+// logit gradient:
+//   softmax: g = c q, q = softmax over the selected logits:
+//            dL_sel = c q (dg - <q, dg>), 0 off the selection;
+//   sigmoid: g = c s_sel / S: ds = (c / S)(dg - <dg, s_sel> / S),
+//            dL_sel = ds s (1 - s);
+//   aux (softmax): dL += p (dp - <p, dp>), dp_e = alpha E counts_e / (T k T).
+// Output dL split into bf16 hi = bf16(dL) and lo = bf16(dL - hi), written as
+// row t of dL_hl [T, 2 Ep]: hi at columns [0,E), lo at [Ep, Ep+E), zero padding.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
+                      const float* __restrict__ gate, const float* __restrict__ dgate,
+                      const int32_t* __restrict__ counts, int T, int E, int k, int score, float gate_scale,
+                      float aux_coeff, int Ep, __nv_bfloat16* __restrict__ dL_hl) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + warp;
+  if (t >= T) return;
+  int my_e = -1;
+  float my_dl = 0.0f;
+  const float* Lrow = logits + static_cast<size_t>(t) * E;
+  if (score == MOE_SCORE_SOFTMAX) {
+    float q = 0.0f, dg = 0.0f;
+    if (lane < k) {
+      my_e = topk_idx[static_cast<size_t>(t) * k + lane];
+      q = gate[static_cast<size_t>(t) * k + lane] / gate_scale;
+      dg = dgate[static_cast<size_t>(t) * k + lane];
+    }
+    float inner = q * dg;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, o);
+    my_dl = gate_scale * q * (dg - inner);
+  } else {
+    float s = 0.0f, dg = 0.0f;
+    if (lane < k) {
+      my_e = topk_idx[static_cast<size_t>(t) * k + lane];
+      s = 1.0f / (1.0f + __expf(-Lrow[my_e]));
+      dg = dgate[static_cast<size_t>(t) * k + lane];
+    }
+    float S = s, inner = dg * s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      S += __shfl_xor_sync(0xffffffffu, S, o);
+      inner += __shfl_xor_sync(0xffffffffu, inner, o);
+    }
+    const float ds = (gate_scale / S) * (dg - inner / S);
+    my_dl = ds * s * (1.0f - s);
+  }
+  const bool aux = (score == MOE_SCORE_SOFTMAX) && aux_coeff != 0.0f;
+  float mx = -INFINITY, sum = 0.0f, pdp = 0.0f;
+  const float dp_scale = aux_coeff * static_cast<float>(E) / (static_cast<float>(T) * k * static_cast<float>(T));
+  if (aux) {
+    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, Lrow[e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int e = lane; e < E; e += 32) {
+      const float ex = __expf(Lrow[e] - mx);
+      sum += ex;
+      pdp += ex * (dp_scale * static_cast<float>(counts[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      pdp += __shfl_xor_sync(0xffffffffu, pdp, o);
+    }
+    pdp /= sum;
+  }
+  __nv_bfloat16* out = dL_hl + static_cast<size_t>(t) * 2 * Ep;
+  for (int e = lane; e < Ep; e += 32) {
+    float d = 0.0f;
+    if (e < E) {
+      for (int i = 0; i < k; ++i) {
+        const int ei = __shfl_sync(__activemask(), my_e, i);
+        const float di = __shfl_sync(__activemask(), my_dl, i);
+        if (ei == e) d += di;
+      }
+      if (aux) {
+        const float p = __expf(Lrow[e] - mx) / sum;
+        d += p * (dp_scale * static_cast<float>(counts[e]) - pdp);
+      }
+    }
+    const __nv_bfloat16 hi = __float2bfloat16_rn(d);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(d - __bfloat162float(hi));
+    out[e] = hi;
+    out[Ep + e] = lo;
+  }
+}
+
+// aux loss value: alpha * E * sum_e (c_e / (T k)) * (sum_tiles partial[tile][e] / T)
+__global__ void aux_loss_kernel(const float* __restrict__ partials, int ntiles, const int32_t* __restrict__ counts,
+                                int T, int E, int k, float aux_coeff, float* __restrict__ out) {
+  __shared__ float s[256];
+  const int e = threadIdx.x;
+  float v = 0.0f;
+  if (e < E) {
+    float P = 0.0f;
+    for (int i = 0; i < ntiles; ++i) P += partials[static_cast<size_t>(i) * E + e];
+    v = (static_cast<float>(counts[e]) / (static_cast<float>(T) * k)) * (P / static_cast<float>(T));
+  }
+  s[e] = v;
+  __syncthreads();
+  for (int d = 128; d > 0; d >>= 1) {
+    if (e < d) s[e] += s[e + d];
+    __syncthreads();
+  }
+  if (e == 0) *out = aux_coeff * static_cast<float>(E) * s[0];
+}
+
+// out[i] = sum_s partials[s][i], s in order.
+__global__ void split_reduce_kernel(const float* __restrict__ partials, int splits, size_t n,
+                                    float* __restrict__ out) {
+  const size_t i4 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i4 >= n) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < splits; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(partials + static_cast<size_t>(s) * n + i4);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  *reinterpret_cast<float4*>(out + i4) = acc;
+}
+
+// ---------------------------------------------------------------------------
+static int blocks_for(int T) { return (T + kWarpsPerBlock - 1) / kWarpsPerBlock; }
+
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_id_map, const float* gate,
+                           const void* shared, void* y, cudaStream_t st) {
+  const int b = blocks_for(c.T);
+  const bool yp = c.inter_fp32 != 0, out = c.out_fp32 != 0;
+  // the shared output has the storage type of y_perm
+  if (yp && out) gather_sum_kernel<true, true, true><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
+  else if (yp) gather_sum_kernel<true, true, false><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
+  else if (out) gather_sum_kernel<false, false, true><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
+  else gather_sum_kernel<false, false, false><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
+                                 const float* extra, void* dx, cudaStream_t st) {
+  const int b = blocks_for(c.T);
+  if (c.out_fp32)
+    gather_sum_kernel<false, true, true><<<b, kWarpsPerBlock * 32, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k);
+  else
+    gather_sum_kernel<false, true, false><<<b, kWarpsPerBlock * 32, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
+                               const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
+                               cudaStream_t st) {
+  const int b = blocks_for(c.T);
+  if (c.inter_fp32)
+    combine_bwd_kernel<true><<<b, kWarpsPerBlock * 32, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+  else
+    combine_bwd_kernel<false><<<b, kWarpsPerBlock * 32, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx, const float* gate,
+                              const float* dgate, const int32_t* counts, int Ep, __nv_bfloat16* dL_hl,
+                              cudaStream_t st) {
+  router_bwd_kernel<<<blocks_for(c.T), kWarpsPerBlock * 32, 0, st>>>(logits, topk_idx, gate, dgate, counts, c.T, c.E,
+                                                                     c.k, c.score, c.gate_scale, c.aux_coeff, Ep,
+                                                                     dL_hl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
+                            cudaStream_t st) {
+  aux_loss_kernel<<<1, 256, 0, st>>>(aux_partials, 4 * ((c.T + 127) / 128), counts, c.T, c.E, c.k, c.aux_coeff, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, float* out, cudaStream_t st) {
+  const size_t n4 = (n + 3) / 4;
+  const int blocks = static_cast<int>((n4 + 255) / 256);
+  split_reduce_kernel<<<blocks, 256, 0, st>>>(partials, splits, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

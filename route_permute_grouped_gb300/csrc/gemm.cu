@@ -1,0 +1,645 @@
+// The persistent tcgen05 GEMM kernel and its epilogues (see gemm_tc.cuh for the
+// structure). One template, instantiated once per kind.
+#include <math.h>
+
+#include "gemm_tc.cuh"
+#include "host_util.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// shared-memory layout
+// ---------------------------------------------------------------------------
+template <int KIND>
+struct SmemLayout {
+  static constexpr int kStages = KindTraits<KIND>::kStages;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;           // full, empty, tfull[2], tempty[2], drain
+  static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
+  static constexpr int kCumOff = kTmemSlot + 16;
+  static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
+  static constexpr int kRouterOff = (kOffOff + (kMaxGroups + 1) * 4 + 15) & ~15;
+  // router scratch: aux column sums [128][33], their partials [4][32],
+  // group scores [128][33], expert_bias [256], logit_bias [256]
+  static constexpr int kRouterBytes = (128 * 33 + 128 + 128 * 33 + 256 + 256) * 4;
+  static constexpr int kBytes = kRouterOff + (KIND == KIND_ROUTER ? kRouterBytes : 0);
+  static constexpr int kDynBytes = kBytes + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// ---------------------------------------------------------------------------
+// epilogues (thread = one accumulator row r of the 128-row tile)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* f) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(f[8 * q + 0], f[8 * q + 1]);
+    w.y = pack_bf16x2(f[8 * q + 2], f[8 * q + 3]);
+    w.z = pack_bf16x2(f[8 * q + 4], f[8 * q + 5]);
+    w.w = pack_bf16x2(f[8 * q + 6], f[8 * q + 7]);
+    d[q] = w;
+  }
+}
+__device__ __forceinline__ void store_f32x32(float* dst, const float* f) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+}
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = s[q];
+    f[8 * q + 0] = bf16_lo(w.x); f[8 * q + 1] = bf16_hi(w.x);
+    f[8 * q + 2] = bf16_lo(w.y); f[8 * q + 3] = bf16_hi(w.y);
+    f[8 * q + 4] = bf16_lo(w.z); f[8 * q + 5] = bf16_hi(w.z);
+    f[8 * q + 6] = bf16_lo(w.w); f[8 * q + 7] = bf16_hi(w.w);
+  }
+}
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float* f) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+}
+
+// FFN1: columns [0,128) of the accumulator hold h1 = x W1 for F columns
+// n0..n0+127, columns [128,256) hold h3 = x W3 for the same F columns.
+__device__ __forceinline__ void epi_ffn1(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
+  const int row = ti.m0 + r;
+  const bool valid = row < ti.m_end;
+  __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(p.out0);
+  __nv_bfloat16* h13 = reinterpret_cast<__nv_bfloat16*>(p.out1);
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float g[32], u[32];
+    tmem_ld32f(tacc + c * 32, g);
+    tmem_ld32f(tacc + 128 + c * 32, u);
+    const int col = ti.n0 + c * 32;
+    if (valid && col < p.F) {
+      float o[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = silu_f(g[j]) * u[j];
+      store_bf16x32(a + static_cast<size_t>(row) * p.F + col, o);
+      if (h13 != nullptr) {
+        store_bf16x32(h13 + static_cast<size_t>(row) * 2 * p.F + col, g);
+        store_bf16x32(h13 + static_cast<size_t>(row) * 2 * p.F + p.F + col, u);
+      }
+    }
+  }
+}
+
+// Plain store of a 128 x bn tile: bf16 or fp32, row-major with `ld` columns.
+__device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int r, int nchunks, int ncols,
+                                          int ld, void* out, bool fp32, size_t row_base) {
+  const int row = ti.m0 + r;
+  const bool valid = row < ti.m_end;
+  const bool zero = ti.nkb == 0;  // no k blocks: the product is zero
+#pragma unroll 1
+  for (int c = 0; c < nchunks; ++c) {
+    float f[32];
+    if (!zero) {
+      tmem_ld32f(tacc + c * 32, f);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+    }
+    const int col = ti.n0 + c * 32;
+    if (valid && col < ncols) {
+      const size_t off = (row_base + static_cast<size_t>(row)) * ld + col;
+      if (fp32) store_f32x32(reinterpret_cast<float*>(out) + off, f);
+      else store_bf16x32(reinterpret_cast<__nv_bfloat16*>(out) + off, f);
+    }
+  }
+}
+
+// DGRAD2: accumulator = da for F columns n0..n0+255; SwiGLU backward with the
+// saved bf16 pre-activations h1 (columns [0,F) of h13) and h3 ([F,2F)):
+//   dh1 = da * h3 * SiLU'(h1),  dh3 = da * SiLU(h1).
+__device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
+  const int row = ti.m0 + r;
+  const bool valid = row < ti.m_end;
+  const __nv_bfloat16* h13 = reinterpret_cast<const __nv_bfloat16*>(p.in_aux);
+  __nv_bfloat16* dh13 = reinterpret_cast<__nv_bfloat16*>(p.out0);
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    float da[32];
+    tmem_ld32f(tacc + c * 32, da);
+    const int col = ti.n0 + c * 32;
+    if (valid && col < p.F) {
+      const size_t base = static_cast<size_t>(row) * 2 * p.F;
+      float h1[32], h3[32], d1[32], d3[32];
+      load_bf16x32(h13 + base + col, h1);
+      load_bf16x32(h13 + base + p.F + col, h3);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float s = 1.0f / (1.0f + __expf(-h1[j]));
+        const float si = h1[j] * s;
+        d1[j] = da[j] * h3[j] * (s * (1.0f + h1[j] * (1.0f - s)));
+        d3[j] = da[j] * si;
+      }
+      store_bf16x32(dh13 + base + col, d1);
+      store_bf16x32(dh13 + base + p.F + col, d3);
+    }
+  }
+}
+
+// WGRAD: fp32 gradient tile of expert g, rows m0.., columns n0.. (zero when the
+// expert has no rows).
+__device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
+  const int m = ti.m0 + r;
+  const bool valid = m < p.wg_M;
+  const bool zero = ti.nkb == 0;
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    float f[32];
+    if (!zero) {
+      tmem_ld32f(tacc + c * 32, f);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+    }
+    const int n = ti.n0 + c * 32;
+    if (valid && n < p.wg_N) {
+      float* dst;
+      if (p.wg_mode == 0) {
+        dst = reinterpret_cast<float*>(p.out0) + (static_cast<size_t>(ti.g) * p.wg_M + m) * p.wg_N + n;
+      } else {
+        const int half = p.wg_N / 2;  // F
+        float* base = reinterpret_cast<float*>(n < half ? p.out0 : p.out1);
+        dst = base + (static_cast<size_t>(ti.g) * p.wg_M + m) * half + (n < half ? n : n - half);
+      }
+      store_f32x32(dst, f);
+    }
+  }
+}
+
+// ROUTER: accumulator row = the E logits of token m0 + r.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float z, float sc, int e, float (&tv)[KMAX], float (&ts)[KMAX],
+                                            int (&ti)[KMAX], int k) {
+  if (!(z > tv[k - 1])) return;  // strict: an equal value never displaces a lower index
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k) {
+      const bool gt = z > tv[j];
+      const float ov = tv[j], os = ts[j];
+      const int oi = ti[j];
+      tv[j] = gt ? z : ov;
+      ts[j] = gt ? sc : os;
+      ti[j] = gt ? e : oi;
+      z = gt ? ov : z;
+      sc = gt ? os : sc;
+      e = gt ? oi : e;
+    }
+  }
+}
+
+template <int KMAX>
+__device__ __forceinline__ void epi_router(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r,
+                                           float* s_red, const float* s_eb, const float* s_lb) {
+  const int t = ti.m0 + r;
+  const bool valid = t < ti.m_end;
+  const int E = p.E, k = p.k;
+  const int nch = p.bn / 32;
+  const bool softmax = p.score == MOE_SCORE_SOFTMAX;
+  float* s_aux = s_red;                 // [128][33]
+  float* s_gs = s_red + 128 * 33 + 128;  // [128][33] group scores
+  // pass 1: logits (+ logit bias), row max, optional logits store
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    float L[32];
+    tmem_ld32f(tacc + c * 32, L);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = c * 32 + j;
+      L[j] += s_lb[e];
+      if (e < E) mx = fmaxf(mx, L[j]);
+    }
+    if (valid && p.logits_out != nullptr) {
+      float* dst = p.logits_out + static_cast<size_t>(t) * E + c * 32;
+      if ((E & 3) == 0 && c * 32 + 32 <= E) {
+        store_f32x32(dst, L);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c * 32 + j < E) dst[j] = L[j];
+      }
+    }
+  }
+  // pass 2 (softmax): denominator
+  float inv_sum = 1.0f;
+  if (softmax) {
+    float sum = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+      float L[32];
+      tmem_ld32f(tacc + c * 32, L);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = c * 32 + j;
+        if (e < E) sum += __expf(L[j] + s_lb[e] - mx);
+      }
+    }
+    inv_sum = 1.0f / sum;
+  }
+  // selection value z and gate score sc of expert e from its logit
+  //   softmax, no expert bias: z = logit (same order as the probabilities)
+  //   otherwise: z = score + expert_bias
+  auto score_of = [&](float L) -> float {
+    return softmax ? __expf(L - mx) * inv_sum : 1.0f / (1.0f + __expf(-L));
+  };
+  const bool z_is_logit = softmax && !p.has_expert_bias;
+  // pass 3 (group-limited selection): group score = sum of the two best z
+  uint32_t allowed = 0xffffffffu;
+  const int G = p.n_groups;
+  if (G > 1 && p.topk_groups < G) {
+    const int gsz = E / G;
+    float b1 = -INFINITY, b2 = -INFINITY;
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+      float L[32];
+      tmem_ld32f(tacc + c * 32, L);
+#pragma unroll 1
+      for (int j = 0; j < 32; ++j) {
+        const int e = c * 32 + j;
+        if (e < E) {
+          const float Lb = L[j] + s_lb[e];
+          const float z = z_is_logit ? Lb : score_of(Lb) + s_eb[e];
+          if (z > b1) { b2 = b1; b1 = z; } else if (z > b2) { b2 = z; }
+          if ((e + 1) % gsz == 0) {
+            s_gs[r * 33 + e / gsz] = (gsz >= 2) ? (b1 + b2) : b1;
+            b1 = -INFINITY; b2 = -INFINITY;
+          }
+        }
+      }
+    }
+    // keep the topk_groups best groups (strict >: lower group index wins ties)
+    allowed = 0u;
+#pragma unroll 1
+    for (int s = 0; s < p.topk_groups; ++s) {
+      float best = -INFINITY;
+      int bi = -1;
+#pragma unroll 1
+      for (int g = 0; g < G; ++g) {
+        const float v = s_gs[r * 33 + g];
+        if (!((allowed >> g) & 1u) && (bi < 0 || v > best)) { best = v; bi = g; }
+      }
+      allowed |= 1u << bi;
+    }
+  }
+  // pass 4: top-k (+ aux column sums of the softmax)
+  float tv[KMAX], ts[KMAX];
+  int tix[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) { tv[j] = -INFINITY; ts[j] = 0.0f; tix[j] = 0; }
+  const int gsz = (G > 1) ? E / G : E;
+  const bool want_aux = softmax && p.aux_partials != nullptr;
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    float L[32];
+    tmem_ld32f(tacc + c * 32, L);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = c * 32 + j;
+      const float Lb = L[j] + s_lb[e];
+      const float sc = (want_aux || !z_is_logit) ? score_of(Lb) : 0.0f;
+      if (want_aux) s_aux[r * 33 + j] = (valid && e < E) ? sc : 0.0f;
+      if (e < E && ((allowed >> (e / gsz)) & 1u)) {
+        const float z = z_is_logit ? Lb : sc + s_eb[e];
+        topk_insert<KMAX>(z, z_is_logit ? Lb : sc, e, tv, ts, tix, k);
+      }
+    }
+    if (want_aux) {
+      // column sums over this warp's 32 tokens, in a warp-private slice of
+      // shared memory (no cross-warp barrier): lane j sums column j
+      __syncwarp();
+      float acc = 0.0f;
+      const int w0 = (r >> 5) * 32;
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) acc += s_aux[(w0 + i) * 33 + (r & 31)];
+      if (c * 32 + (r & 31) < E)
+        p.aux_partials[static_cast<size_t>(ti.m0 / 32 + (r >> 5)) * E + c * 32 + (r & 31)] = acc;
+      __syncwarp();
+    }
+  }
+  if (!valid) return;
+  // gates
+  float g[KMAX];
+  float tot = 0.0f;
+  if (z_is_logit) {
+    // renormalised softmax over the selected logits
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      g[j] = (j < k) ? __expf(ts[j] - ts[0]) : 0.0f;
+      tot += g[j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      g[j] = (j < k) ? ts[j] : 0.0f;
+      tot += g[j];
+    }
+  }
+  const float scale = p.gate_scale / tot;
+  int32_t* oi = p.topk_idx + static_cast<size_t>(t) * k;
+  float* og = p.topk_gate + static_cast<size_t>(t) * k;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k) {
+      oi[j] = tix[j];
+      og[j] = g[j] * scale;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int KIND, int KMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap ma,
+                const __grid_constant__ CUtensorMap mb0, const __grid_constant__ CUtensorMap mb1) {
+  using TR = KindTraits<KIND>;
+  using SL = SmemLayout<KIND>;
+  constexpr int NST = TR::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
+  uint64_t* empty = full + NST;
+  uint64_t* tfull = empty + NST;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SL::kTmemSlot + 4);
+  int* s_cum = reinterpret_cast<int*>(smem + SL::kCumOff);
+  int* s_off = reinterpret_cast<int*>(smem + SL::kOffOff);
+
+  const int warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 4);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0) {
+    // tile schedule: s_off = row offsets of the groups, s_cum = prefix of tiles
+    const int ng = p.ngroups;
+    constexpr int PER = (kMaxGroups + 32) / 32;  // groups per lane (ceil(257/32))
+    int cnt[PER];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int g = lane * PER + i;
+      int c = 0;
+      if (g <= ng) {
+        int o;
+        if (p.offsets != nullptr && KIND != KIND_ROUTER_DW) o = p.offsets[g];
+        else o = (g == 0) ? 0 : p.M_total;
+        s_off[g] = o;
+      }
+      if (g < ng) {
+        if constexpr (KIND == KIND_WGRAD || KIND == KIND_ROUTER_DW) {
+          c = p.m_tiles_fixed * p.n_tiles;
+        } else {
+          int lo, hi;
+          if (p.offsets != nullptr) { lo = p.offsets[g]; hi = p.offsets[g + 1]; }
+          else { lo = 0; hi = p.M_total; }
+          const int rows = max(hi - lo, 0);
+          c = ((rows + kBM - 1) / kBM) * p.n_tiles;
+        }
+      }
+      cnt[i] = c;
+      local += c;
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int g = lane * PER + i;
+      if (g <= ng) s_cum[g] = run;
+      run += cnt[i];
+    }
+  }
+  float* s_red = nullptr;
+  float* s_eb = nullptr;
+  float* s_lb = nullptr;
+  if constexpr (KIND == KIND_ROUTER) {
+    s_red = reinterpret_cast<float*>(smem + SL::kRouterOff);
+    s_eb = s_red + 128 * 33 + 128 + 128 * 33;
+    s_lb = s_eb + 256;
+    for (int e = threadIdx.x; e < 256; e += kThreads) {
+      s_eb[e] = (p.has_expert_bias && e < p.E) ? p.expert_bias[e] : 0.0f;
+      s_lb[e] = (p.has_logit_bias && e < p.E) ? p.logit_bias[e] : 0.0f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int ntiles = s_cum[p.ngroups];
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&ma);
+      tma_prefetch_desc(&mb0);
+      if (KIND == KIND_FFN1 || KIND == KIND_DGRAD1) tma_prefetch_desc(&mb1);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_phase[NST];
+#pragma unroll
+      for (int s = 0; s < NST; ++s) issued_phase[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
+          uint8_t* sA = smem + stage * kStageBytes;
+          issue_loads<KIND>(p, ti, kb, sA, sA + kABytes, full + stage, &ma, &mb0, &mb1);
+          issued_phase[stage] = static_cast<int>(phase);
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded, regardless of the abort flag) for copies in flight
+        int zero = 0;
+        for (int s = 0; s < NST; ++s)
+          if (issued_phase[s] >= 0)
+            mbar_wait_bounded(full + s, static_cast<uint32_t>(issued_phase[s]), reinterpret_cast<volatile int*>(&zero),
+                              lim, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kBM, p.bn, TR::A_MN, TR::B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
+      if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, s_abort, lim, p.status, 2)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* sA = smem + stage * kStageBytes;
+        uint8_t* sB = sA + kABytes;
+        if constexpr (KIND == KIND_WGRAD) {
+          // ragged K: zero the rows of the last k block that lie past the
+          // expert's rows (they hold the next expert's data or TMA zero fill)
+          const int valid = ti.krow_end - (ti.krow0 + kb * kBK);
+          if (valid < kBK) {
+            const int nbox = 2 + 4;
+            const int chunks_per_row = 8;  // 16-byte chunks in a 128-byte row
+            const int rows = kBK - valid;
+            for (int idx = lane; idx < nbox * rows * chunks_per_row; idx += 32) {
+              const int box = idx / (rows * chunks_per_row);
+              const int rem = idx - box * rows * chunks_per_row;
+              const int rr = valid + rem / chunks_per_row;
+              const int ch = rem % chunks_per_row;
+              uint8_t* base = (box < 2) ? (sA + box * 8192) : (sB + (box - 2) * 8192);
+              *reinterpret_cast<uint4*>(base + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = TR::A_MN ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
+                                         : smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = TR::B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
+                                         : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(empty + stage);
+        }
+        __syncwarp();
+        if (++stage == NST) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (ti.nkb > 0) umma_commit(tfull + acc);
+        else mbar_arrive(tfull + acc);
+      }
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // drain every MMA issued by this CTA before the TMEM is released
+    if (lane == 0) umma_commit(drain);
+    __syncwarp();
+    int zero = 0;
+    mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int*>(&zero), lim, nullptr, 0);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
+      if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * kAccStride) + (static_cast<uint32_t>(q * 32) << 16);
+      if constexpr (KIND == KIND_FFN1) {
+        epi_ffn1(p, ti, tacc, r);
+      } else if constexpr (KIND == KIND_FFN2) {
+        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
+      } else if constexpr (KIND == KIND_ROUTER) {
+        epi_router<KMAX>(p, ti, tacc, r, s_red, s_eb, s_lb);
+      } else if constexpr (KIND == KIND_DGRAD2) {
+        epi_dgrad2(p, ti, tacc, r);
+      } else if constexpr (KIND == KIND_DGRAD1) {
+        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
+      } else if constexpr (KIND == KIND_WGRAD) {
+        epi_wgrad(p, ti, tacc, r);
+      } else if constexpr (KIND == KIND_ROUTER_DX) {
+        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, true, 0);
+      } else {  // ROUTER_DW partial of split g: rows m < E
+        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, true, static_cast<size_t>(ti.g) * p.E);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty + acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launch
+// ---------------------------------------------------------------------------
+template <int KIND, int KMAX>
+static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
+                               const CUtensorMap& mb1, int grid, cudaStream_t st) {
+  auto kern = gemm_kernel<KIND, KMAX>;
+  const int smem = SmemLayout<KIND>::kDynBytes;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  kern<<<grid, kThreads, smem, st>>>(p, ma, mb0, mb1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
+                        const CUtensorMap& mb1, int grid, cudaStream_t st) {
+  switch (kind) {
+    case KIND_FFN1: return launch_kind<KIND_FFN1, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_FFN2: return launch_kind<KIND_FFN2, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_ROUTER:
+      if (p.k <= 8) return launch_kind<KIND_ROUTER, 8>(p, ma, mb0, mb1, grid, st);
+      return launch_kind<KIND_ROUTER, 16>(p, ma, mb0, mb1, grid, st);
+    case KIND_DGRAD2: return launch_kind<KIND_DGRAD2, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_DGRAD1: return launch_kind<KIND_DGRAD1, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_WGRAD: return launch_kind<KIND_WGRAD, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW, 1>(p, ma, mb0, mb1, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,207 @@
+// Persistent, warp-specialised tcgen05 GEMM for the MoE layer.
+//
+// One CTA per SM (192 threads):
+//   warp 0      TMA producer: 128-byte-swizzled tiles of A and B into a ring of
+//               shared-memory stages (mbarrier full/empty pairs);
+//   warp 1      TMEM owner and UMMA issuer: 128 x BN x 16 bf16 MMAs into one of
+//               two fp32 accumulators in tensor memory (2 x 256 columns), so the
+//               epilogue of tile i overlaps the main loop of tile i+1;
+//   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
+//               reads 32 columns at a time and applies the kind's epilogue.
+//
+// Tiles come from a device-side schedule: every CTA reads the per-expert row
+// offsets produced by the permute (no host synchronisation), builds the
+// prefix of tile counts in shared memory, and walks tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... . Each kind below fixes which global tensors
+// feed A and B, how a tile maps to coordinates, and what the epilogue writes.
+//
+// Operand staging (both operands as 128-byte swizzled boxes of 64 bf16):
+//   K-major operand with R rows: one box {64 (k), R} -> R rows of 128 B;
+//   MN-major operand with R (m or n) extent: R/64 boxes {64 (mn), 64 (k)}, each
+//   64 K-rows of 128 B (8 KB), placed 8 KB apart.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+enum GemmKind : int {
+  KIND_FFN1 = 0,       // h = x_perm [W1_e | W3_e]  -> a = SiLU(h1) h3 (+ h13 save)
+  KIND_FFN2 = 1,       // y_perm = a W2_e
+  KIND_ROUTER = 2,     // L = x W_r^T -> score, top-k, gates (+ logits, aux partials)
+  KIND_DGRAD2 = 3,     // da = dy_perm W2_e^T -> SwiGLU backward -> dh13
+  KIND_DGRAD1 = 4,     // dx_perm = dh13 [W1_e | W3_e]^T
+  KIND_WGRAD = 5,      // dW_e = X_e^T Y_e over the expert's rows (ragged K)
+  KIND_ROUTER_DX = 6,  // dx_r = dL W_r     (dL as bf16 hi + lo parts)
+  KIND_ROUTER_DW = 7,  // dW_r partial = dL^T x over one K split
+};
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kABytes = kBM * 128;        // 16 KB
+constexpr int kBBytesMax = 256 * 128;     // 32 KB
+constexpr int kStageBytes = kABytes + kBBytesMax;
+constexpr int kMaxGroups = 256;
+constexpr int kTmemCols = 512;
+constexpr int kAccStride = 256;           // TMEM column distance of the two accumulators
+
+template <int KIND>
+struct KindTraits {
+  static constexpr bool A_MN = (KIND == KIND_WGRAD || KIND == KIND_ROUTER_DW);
+  static constexpr bool B_MN = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_WGRAD ||
+                                KIND == KIND_ROUTER_DX || KIND == KIND_ROUTER_DW);
+  static constexpr int kStages = (KIND == KIND_ROUTER) ? 3 : 4;
+  static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
+                                        KIND == KIND_DGRAD1);
+};
+
+struct GemmParams {
+  // problem sizes
+  int T, H, E, k, F;
+  int M_total;           // rows of the single group when offsets == nullptr
+  int ngroups;           // groups (experts) in the schedule
+  int bn;                // UMMA N (multiple of 32, <= 256)
+  int n_tiles;           // N tiles per m tile (uniform over groups)
+  int m_tiles_fixed;     // WGRAD / ROUTER_DW: m tiles per group
+  int wg_M, wg_N;        // WGRAD: output rows / columns of one expert's gradient
+  int wg_mode;           // WGRAD: 0 = dW2 [E,F,H]; 1 = dW1|dW3 from N = 2F
+  int kb_total;          // k blocks (non-ragged kinds); ROUTER_DW: per split
+  int splits;            // ROUTER_DW: number of K splits
+  int Ep;                // ROUTER_DX / ROUTER_DW: padded expert count (multiple of 64)
+  const int32_t* offsets;  // [ngroups+1] device row offsets (grouped kinds, WGRAD)
+  // router
+  int score, n_groups, topk_groups, has_expert_bias, has_logit_bias;
+  float gate_scale;
+  const float* expert_bias;
+  const float* logit_bias;
+  int32_t* topk_idx;
+  float* topk_gate;
+  float* logits_out;
+  float* aux_partials;
+  // outputs / epilogue inputs
+  void* out0;            // FFN1: a; FFN2: y_perm; DGRAD2: dh13; DGRAD1: dx_perm;
+                         // WGRAD: dW2 or dW1; ROUTER_DX: dx_r (fp32); ROUTER_DW: partials
+  void* out1;            // FFN1: h13 save (nullable); WGRAD mode 1: dW3
+  const void* in_aux;    // DGRAD2: h13 (saved pre-activations)
+  int out_fp32;          // FFN2: y_perm fp32
+  // status
+  DevStatus* status;
+  unsigned long long wait_limit_ns;
+};
+
+struct TileInfo {
+  int g;       // group (expert) or split
+  int m0;      // first row of the tile (global row for grouped kinds; m offset otherwise)
+  int m_end;   // one past the last valid row
+  int n0;      // first output column of the tile
+  int kb0;     // first k block
+  int nkb;     // k blocks of this tile
+  int krow0;   // WGRAD: first row of the expert (K origin); ROUTER_DW: unused
+  int krow_end;
+};
+
+template <int KIND>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_cum, const int* s_off,
+                                                int tile) {
+  TileInfo ti;
+  int lo = 0, hi = p.ngroups;  // find g with s_cum[g] <= tile < s_cum[g+1]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (s_cum[mid] <= tile) lo = mid; else hi = mid;
+  }
+  ti.g = lo;
+  int local = tile - s_cum[lo];
+  int mb = local / p.n_tiles;
+  int nb = local - mb * p.n_tiles;
+  if constexpr (KindTraits<KIND>::kGroupedRows || KIND == KIND_ROUTER || KIND == KIND_ROUTER_DX) {
+    ti.m0 = s_off[lo] + mb * kBM;
+    ti.m_end = s_off[lo + 1];
+    ti.kb0 = 0;
+    ti.nkb = p.kb_total;
+    ti.krow0 = 0;
+    ti.krow_end = 0;
+  } else if constexpr (KIND == KIND_WGRAD) {
+    ti.m0 = mb * kBM;
+    ti.m_end = p.wg_M;
+    ti.krow0 = s_off[lo];
+    ti.krow_end = s_off[lo + 1];
+    ti.kb0 = 0;
+    ti.nkb = (ti.krow_end - ti.krow0 + kBK - 1) / kBK;
+  } else {  // ROUTER_DW: group = split
+    ti.m0 = mb * kBM;
+    ti.m_end = p.E;
+    int total = 2 * ((p.T + kBK - 1) / kBK);
+    int per = p.kb_total;
+    ti.kb0 = lo * per;
+    ti.nkb = min(per, total - ti.kb0);
+    if (ti.nkb < 0) ti.nkb = 0;
+    ti.krow0 = 0;
+    ti.krow_end = 0;
+  }
+  if constexpr (KIND == KIND_FFN1) {
+    ti.n0 = nb * 128;  // F columns (gate and up halves of the 256-wide tile)
+  } else {
+    ti.n0 = nb * p.bn;
+  }
+  return ti;
+}
+
+// Issue the TMA loads of k block `kb` of tile `ti` into stage buffers sA, sB.
+template <int KIND>
+__device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& ti, int kb, uint8_t* sA,
+                                            uint8_t* sB, uint64_t* bar, const CUtensorMap* ma,
+                                            const CUtensorMap* mb0, const CUtensorMap* mb1) {
+  const int kk = kb * kBK;
+  if constexpr (KIND == KIND_FFN1) {
+    tma_load_2d(sA, ma, bar, kk, ti.m0);
+    const int brow = ti.g * p.H + kk;
+    tma_load_2d(sB + 0 * 8192, mb0, bar, ti.n0, brow);
+    tma_load_2d(sB + 1 * 8192, mb0, bar, ti.n0 + 64, brow);
+    tma_load_2d(sB + 2 * 8192, mb1, bar, ti.n0, brow);
+    tma_load_2d(sB + 3 * 8192, mb1, bar, ti.n0 + 64, brow);
+  } else if constexpr (KIND == KIND_FFN2) {
+    tma_load_2d(sA, ma, bar, kk, ti.m0);
+    const int brow = ti.g * p.F + kk;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, brow);
+  } else if constexpr (KIND == KIND_ROUTER) {
+    tma_load_2d(sA, ma, bar, kk, ti.m0);
+    tma_load_2d(sB, mb0, bar, kk, 0);
+  } else if constexpr (KIND == KIND_DGRAD2) {
+    tma_load_2d(sA, ma, bar, kk, ti.m0);
+    tma_load_2d(sB, mb0, bar, kk, ti.g * p.F + ti.n0);
+  } else if constexpr (KIND == KIND_DGRAD1) {
+    tma_load_2d(sA, ma, bar, kk, ti.m0);
+    if (kk < p.F) tma_load_2d(sB, mb0, bar, kk, ti.g * p.H + ti.n0);
+    else tma_load_2d(sB, mb1, bar, kk - p.F, ti.g * p.H + ti.n0);
+  } else if constexpr (KIND == KIND_WGRAD) {
+    const int r = ti.krow0 + kk;
+    tma_load_2d(sA, ma, bar, ti.m0, r);
+    tma_load_2d(sA + 8192, ma, bar, ti.m0 + 64, r);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, r);
+  } else if constexpr (KIND == KIND_ROUTER_DX) {
+    tma_load_2d(sA, ma, bar, kk, ti.m0);
+    const int erow = kk % p.Ep;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, erow);
+  } else {  // ROUTER_DW
+    const int half = (p.T + kBK - 1) / kBK;
+    const int kbg = ti.kb0 + kb;
+    const int is_lo = kbg >= half ? 1 : 0;
+    const int trow = (kbg - is_lo * half) * kBK;
+    const int col = ti.m0 + is_lo * p.Ep;
+    tma_load_2d(sA, ma, bar, col, trow);
+    tma_load_2d(sA + 8192, ma, bar, col + 64, trow);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, trow);
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
+  if constexpr (KIND == KIND_ROUTER) return kABytes + p.bn * 128;
+  else return kABytes + kBBytesMax;
+}
+
+}  // namespace moe

@@ -1,0 +1,49 @@
+// Host-side helpers shared by the translation units: tensor-map encoding (via
+// the driver entry point, so the library does not link libcuda), device
+// properties, and the launchers each .cu file exports.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gemm_tc.cuh"
+
+namespace moe {
+
+// 2-D bf16 tensor map over a row-major [outer, inner] array with row pitch
+// `row_bytes`, box {box_inner, box_outer}, 128-byte swizzle, zero fill outside
+// the array. Returns false if the driver rejects it.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                   uint32_t box_inner, uint32_t box_outer);
+
+int num_sms();
+unsigned long long wait_limit_ns();
+int debug_fault();
+
+cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
+                        const CUtensorMap& mb1, int grid, cudaStream_t st);
+
+// permute.cu
+cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
+                           __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
+                           int32_t* lookback, DevStatus* st, cudaStream_t stream);
+
+size_t permute_lookback_ints(int T, int E);
+
+// elementwise.cu
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_id_map,
+                           const float* gate, const void* shared, void* y, cudaStream_t st);
+cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
+                               const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
+                               cudaStream_t st);
+cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
+                                 const float* extra, void* dx, cudaStream_t st);
+cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx,
+                              const float* gate, const float* dgate, const int32_t* counts, int Ep,
+                              __nv_bfloat16* dL_hl, cudaStream_t st);
+cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
+                            cudaStream_t st);
+cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, float* out, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,212 @@
+// Local dispatch: per-expert histogram, single-pass decoupled-lookback scan
+// over token chunks, and the 16-byte vectorised row scatter into
+// expert-contiguous rows (dropless; rows of one expert in token order).
+#include "host_util.h"
+
+namespace moe {
+
+constexpr int kChunk = 64;           // tokens per scan chunk (two rank warps)
+constexpr int kScanThreads = 256;
+constexpr uint32_t kFlagP = 0x80000000u;  // inclusive prefix published
+constexpr uint32_t kFlagA = 0x40000000u;  // chunk aggregate published
+constexpr uint32_t kValMask = 0x3fffffffu;
+
+// counts[e] += number of (t,i) with topk_idx[t,i] == e. Warp-aggregated: lanes
+// holding the same expert combine through __match_any_sync, then one shared
+// atomic per group and one global atomic per (block, expert).
+__global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __restrict__ topk_idx, int n, int E,
+                                                           int32_t* __restrict__ counts, DevStatus* st) {
+  __shared__ int s_h[256];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_h[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int stride = gridDim.x * blockDim.x;
+  const int iters = (n + stride - 1) / stride;
+  for (int it = 0; it < iters; ++it) {
+    const int i = it * stride + blockIdx.x * blockDim.x + threadIdx.x;
+    int e = -1;
+    if (i < n) {
+      e = __ldg(topk_idx + i);
+      if (e < 0 || e >= E) {
+        set_status(st, MOE_ERR_DEVICE_INDEX, 10);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_h[e], __popc(peers));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (s_h[e] != 0) atomicAdd(&counts[e], s_h[e]);
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const int32_t* p) {
+  return static_cast<uint32_t>(*reinterpret_cast<const volatile int32_t*>(p));
+}
+__device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
+  *reinterpret_cast<volatile int32_t*>(p) = static_cast<int32_t>(v);
+}
+
+// One CTA per chunk of 64 tokens, chunks taken in ticket order (so every
+// earlier chunk has started when a CTA looks back). For expert e the row of
+// (t,i) is offsets[e] + (rows of e in earlier chunks) + (rank of t among this
+// chunk's tokens routed to e). The earlier-chunk term comes from a decoupled
+// lookback over per-(chunk, expert) words [flag | value].
+__global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx, int T, int H, int E, int k,
+    const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out, int32_t* __restrict__ lookback,
+    __nv_bfloat16* __restrict__ x_perm, int32_t* __restrict__ row_id_map, DevStatus* st,
+    unsigned long long limit_ns, int fault) {
+  __shared__ int s_ticket;
+  __shared__ uint32_t s_mask[2][256];
+  __shared__ int s_base[256];
+  __shared__ int s_scan[256];
+  __shared__ int s_rows[kChunk * 16];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int32_t* ticket_ctr = lookback;  // lookback[0] is the chunk ticket counter
+  int32_t* flags = lookback + 64;  // [nchunks][E]
+  if (tid == 0) s_ticket = atomicAdd(ticket_ctr, 1);
+  for (int e = tid; e < 256; e += kScanThreads) {
+    s_mask[0][e] = 0u;
+    s_mask[1][e] = 0u;
+  }
+  // exclusive scan of the global counts (E <= 256): offsets of the experts
+  const int cnt = (tid < E) ? counts[tid] : 0;
+  s_scan[tid] = cnt;
+  __syncthreads();
+  for (int d = 1; d < 256; d <<= 1) {
+    const int v = (tid >= d) ? s_scan[tid - d] : 0;
+    __syncthreads();
+    s_scan[tid] += v;
+    __syncthreads();
+  }
+  const int b = s_ticket;
+  const int t0 = b * kChunk;
+  if (b == 0) {
+    if (tid < E) offsets_out[tid] = (tid == 0) ? 0 : s_scan[tid - 1];
+    if (tid == 0) offsets_out[E] = s_scan[E - 1];
+  }
+  // per-warp bitmasks: bit `lane` of s_mask[w][e] = token t0 + 32w + lane routes to e
+  int my_e[16];
+  if (warp < 2) {
+    const int t = t0 + warp * 32 + lane;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      my_e[i] = -1;
+      if (i < k && t < T) {
+        int e = topk_idx[static_cast<size_t>(t) * k + i];
+        if (e < 0 || e >= E) {
+          set_status(st, MOE_ERR_DEVICE_INDEX, 11);
+          e = -1;
+        }
+        my_e[i] = e;
+        if (e >= 0) atomicOr(&s_mask[warp][e], 1u << lane);
+      }
+    }
+  }
+  __syncthreads();
+  // publish this chunk's aggregate, look back for the earlier chunks' total
+  for (int e = tid; e < E; e += kScanThreads) {
+    const uint32_t c = __popc(s_mask[0][e]) + __popc(s_mask[1][e]);
+    int32_t* mine = flags + static_cast<size_t>(b) * E + e;
+    uint32_t excl = 0;
+    if (b == 0) {
+      if (!fault) st_volatile_u32(mine, kFlagP | c);
+    } else {
+      st_volatile_u32(mine, kFlagA | c);
+      int bb = b - 1;
+      uint64_t t_start = 0;
+      uint32_t spins = 0;
+      while (bb >= 0) {
+        const uint32_t v = ld_volatile_u32(flags + static_cast<size_t>(bb) * E + e);
+        if (v & kFlagP) {
+          excl += v & kValMask;
+          break;
+        } else if (v & kFlagA) {
+          excl += v & kValMask;
+          --bb;
+        } else {
+          if (spins == 0) t_start = globaltimer();
+          if ((++spins & 31u) == 0 && globaltimer() - t_start > limit_ns) {
+            set_status(st, MOE_ERR_DEVICE_TIMEOUT, 12);
+            break;  // give up: publish what we have so later chunks finish
+          }
+        }
+      }
+      st_volatile_u32(mine, kFlagP | ((excl + c) & kValMask));
+    }
+    s_base[e] = ((e == 0) ? 0 : s_scan[e - 1]) + static_cast<int>(excl);
+  }
+  __syncthreads();
+  // rows of this chunk's (t,i)
+  if (warp < 2) {
+    const int t = t0 + warp * 32 + lane;
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < k && t < T) {
+        const int e = my_e[i];
+        int r = -1;
+        if (e >= 0) {
+          r = s_base[e] + (warp == 1 ? __popc(s_mask[0][e]) : 0) + __popc(s_mask[warp][e] & lt);
+        }
+        row_id_map[static_cast<size_t>(t) * k + i] = r;
+        s_rows[(warp * 32 + lane) * k + i] = r;
+      }
+    }
+  }
+  __syncthreads();
+  // scatter: warp w copies tokens w, w+8, ... of the chunk; 16-byte vectors
+  const int nvec = H / 8;
+  for (int j = warp; j < kChunk; j += kScanThreads / 32) {
+    const int t = t0 + j;
+    if (t >= T) break;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nvec) buf[u] = __ldg(src + v);
+      }
+      for (int i = 0; i < k; ++i) {
+        const int r = s_rows[j * k + i];
+        if (r < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) dst[v] = buf[u];
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
+                           __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
+                           int32_t* lookback, DevStatus* st, cudaStream_t stream) {
+  const int T = c.T, E = c.E, k = c.k;
+  const int nchunks = (T + kChunk - 1) / kChunk;
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(lookback, 0, sizeof(int32_t) * (64 + static_cast<size_t>(nchunks) * E), stream);
+  if (e != cudaSuccess) return e;
+  const int n = T * k;
+  int hb = (n + 1023) / 1024;
+  hb = hb < 4 * num_sms() ? hb : 4 * num_sms();
+  if (hb < 1) hb = 1;
+  permute_hist_kernel<<<hb, 256, 0, stream>>>(topk_idx, n, E, counts, st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  permute_scan_scatter_kernel<<<nchunks, kScanThreads, 0, stream>>>(x, topk_idx, T, c.H, E, k, counts, offsets,
+                                                                    lookback, x_perm, row_id_map, st,
+                                                                    wait_limit_ns(), debug_fault());
+  return cudaGetLastError();
+}
+
+size_t permute_lookback_ints(int T, int E) {
+  return 64 + static_cast<size_t>((T + kChunk - 1) / kChunk) * E;
+}
+
+}  // namespace moe

@@ -1,0 +1,256 @@
+"""Python binding of the C ABI in ``include/moe_route_permute.h``.
+
+Argument marshalling only: tensors are allocated with torch on the current CUDA
+device, their data pointers and torch's current stream are handed to the
+library, and every step of the path runs in the library's kernels. There is no
+fallback: if the compiled library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int, c_int32, c_longlong, c_size_t, c_void_p
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "workspace too small",
+                4: "CUDA error", 5: "device: bounded wait ran out", 6: "device: index out of range"}
+SCORE = {"softmax": 0, "sigmoid": 1}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} (status {status})")
+        self.status = status
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", c_int), ("H", c_int), ("E", c_int), ("k", c_int), ("F", c_int), ("F_shared", c_int),
+                ("score", c_int), ("n_groups", c_int), ("topk_groups", c_int), ("gate_scale", c_float),
+                ("aux_coeff", c_float), ("out_fp32", c_int), ("inter_fp32", c_int)]
+
+
+class MoeFwdSaved(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("topk_idx", "topk_gate", "logits", "row_id_map", "counts", "offsets",
+                                        "x_perm", "h13", "a", "y_perm", "aux_partials")]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing: run route_permute_grouped_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        vp = c_void_p
+        L.moe_workspace_bytes.restype = c_size_t
+        L.moe_workspace_bytes.argtypes = [POINTER(MoeConfig), c_int]
+        L.moe_router_topk.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+        L.moe_permute.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+        L.moe_grouped_swiglu_ffn.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+        L.moe_unpermute_combine.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp]
+        L.moe_layer_fwd.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    POINTER(MoeFwdSaved), vp, c_size_t, vp]
+        L.moe_layer_bwd.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, POINTER(MoeFwdSaved), vp, vp, vp,
+                                    vp, vp, vp, vp, c_size_t, vp]
+        L.moe_get_device_status.argtypes = [vp, vp, POINTER(c_int)]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [c_int]
+        L.moe_debug_set_wait_limit_ns.argtypes = [c_longlong]
+        L.moe_debug_set_wait_limit_ns.restype = None
+        L.moe_debug_set_fault.argtypes = [c_int]
+        L.moe_debug_set_fault.restype = None
+        for n in ("moe_router_topk", "moe_permute", "moe_grouped_swiglu_ffn", "moe_unpermute_combine",
+                  "moe_layer_fwd", "moe_layer_bwd", "moe_get_device_status"):
+            getattr(L, n).restype = c_int
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    assert t.is_contiguous(), "tensors must be contiguous"
+    return c_void_p(t.data_ptr())
+
+
+def _stream():
+    return c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(st, where):
+    if st != MOE_OK:
+        raise MoeError(st, where)
+
+
+def make_config(T, H, E, k, F, F_shared=0, score="softmax", n_groups=1, topk_groups=1, gate_scale=1.0,
+                aux_coeff=0.0, out_fp32=False, inter_fp32=False) -> MoeConfig:
+    return MoeConfig(T, H, E, k, F, F_shared, SCORE[score] if isinstance(score, str) else score, n_groups,
+                     topk_groups, gate_scale, aux_coeff, int(out_fp32), int(inter_fp32))
+
+
+def config_from_shape(ls, **over) -> MoeConfig:
+    d = dict(T=ls.T, H=ls.H, E=ls.E, k=ls.k, F=ls.F, F_shared=ls.F_shared, score=ls.score, n_groups=ls.n_groups,
+             topk_groups=ls.topk_groups, gate_scale=ls.gate_scale, aux_coeff=ls.aux_coeff, out_fp32=ls.out_fp32,
+             inter_fp32=ls.inter_fp32)
+    d.update(over)
+    return make_config(**d)
+
+
+def workspace_bytes(cfg: MoeConfig, training: bool = False) -> int:
+    return int(lib().moe_workspace_bytes(ctypes.byref(cfg), int(training)))
+
+
+def workspace(cfg: MoeConfig, training: bool = False, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(cfg, training)
+    if n == 0:
+        raise MoeError(1, "moe_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()  # device status word
+    return ws
+
+
+def device_status(ws: torch.Tensor) -> int:
+    out = c_int(0)
+    _check(lib().moe_get_device_status(_p(ws), _stream(), ctypes.byref(out)), "moe_get_device_status")
+    return out.value
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().moe_debug_set_wait_limit_ns(int(ns))
+
+
+def set_fault(f: int) -> None:
+    lib().moe_debug_set_fault(int(f))
+
+
+def _inter_dtype(cfg):
+    return torch.float32 if cfg.inter_fp32 else torch.bfloat16
+
+
+def _out_dtype(cfg):
+    return torch.float32 if cfg.out_fp32 else torch.bfloat16
+
+
+def router_topk(cfg, x, router_w, expert_bias=None, logit_bias=None, want_logits=False, want_aux=False, ws=None):
+    dev = x.device
+    T, E, k = cfg.T, cfg.E, cfg.k
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if want_logits else None
+    aux = torch.empty((4 * ((T + 127) // 128), E), dtype=torch.float32, device=dev) if want_aux else None
+    ws = workspace(cfg, False, dev) if ws is None else ws
+    st = lib().moe_router_topk(ctypes.byref(cfg), _p(x), _p(router_w), _p(expert_bias), _p(logit_bias), _p(idx),
+                               _p(gate), _p(logits), _p(aux), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_router_topk")
+    return idx, gate, logits, aux
+
+
+def permute(cfg, x, topk_idx, ws=None):
+    dev = x.device
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    x_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    rows = torch.empty((T, k), dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ws = workspace(cfg, False, dev) if ws is None else ws
+    st = lib().moe_permute(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(x_perm), _p(rows), _p(counts), _p(offsets),
+                           _p(ws), ws.numel(), _stream())
+    _check(st, "moe_permute")
+    return x_perm, rows, counts, offsets
+
+
+def grouped_swiglu_ffn(cfg, x_perm, offsets, W1, W3, W2, save=False, ws=None):
+    dev = x_perm.device
+    R, H, F = cfg.T * cfg.k, cfg.H, cfg.F
+    y_perm = torch.empty((R, H), dtype=_inter_dtype(cfg), device=dev)
+    h13 = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev) if save else None
+    a = torch.empty((R, F), dtype=torch.bfloat16, device=dev) if save else None
+    ws = workspace(cfg, False, dev) if ws is None else ws
+    st = lib().moe_grouped_swiglu_ffn(ctypes.byref(cfg), _p(x_perm), _p(offsets), _p(W1), _p(W3), _p(W2), _p(h13),
+                                      _p(a), _p(y_perm), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_grouped_swiglu_ffn")
+    return y_perm, h13, a
+
+
+def unpermute_combine(cfg, y_perm, row_id_map, topk_gate, shared=None):
+    y = torch.empty((cfg.T, cfg.H), dtype=_out_dtype(cfg), device=y_perm.device)
+    st = lib().moe_unpermute_combine(ctypes.byref(cfg), _p(y_perm), _p(row_id_map), _p(topk_gate), _p(shared),
+                                     _p(y), _stream())
+    _check(st, "moe_unpermute_combine")
+    return y
+
+
+def alloc_saved(cfg, device="cuda"):
+    """Tensors the training forward keeps for the backward."""
+    T, H, E, k, F = cfg.T, cfg.H, cfg.E, cfg.k, cfg.F
+    R = T * k
+    f32, i32, bf = torch.float32, torch.int32, torch.bfloat16
+    return {
+        "topk_idx": torch.empty((T, k), dtype=i32, device=device),
+        "topk_gate": torch.empty((T, k), dtype=f32, device=device),
+        "logits": torch.empty((T, E), dtype=f32, device=device),
+        "row_id_map": torch.empty((T, k), dtype=i32, device=device),
+        "counts": torch.empty(E, dtype=i32, device=device),
+        "offsets": torch.empty(E + 1, dtype=i32, device=device),
+        "x_perm": torch.empty((R, H), dtype=bf, device=device),
+        "h13": torch.empty((R, 2 * F), dtype=bf, device=device),
+        "a": torch.empty((R, F), dtype=bf, device=device),
+        "y_perm": torch.empty((R, H), dtype=_inter_dtype(cfg), device=device),
+        "aux_partials": torch.empty((4 * ((T + 127) // 128), E), dtype=f32, device=device) if cfg.aux_coeff else None,
+    }
+
+
+def _saved_struct(saved):
+    return MoeFwdSaved(*[None if saved.get(n) is None else saved[n].data_ptr() for n, _ in MoeFwdSaved._fields_])
+
+
+def layer_fwd(cfg, x, router_w, W1, W3, W2, expert_bias=None, logit_bias=None, Ws=None, saved=None, ws=None, y=None):
+    """Whole layer forward. ``saved`` (from alloc_saved) makes it a training
+    forward that keeps the tensors the backward needs."""
+    dev = x.device
+    if y is None:
+        y = torch.empty((cfg.T, cfg.H), dtype=_out_dtype(cfg), device=dev)
+    ws = workspace(cfg, saved is not None, dev) if ws is None else ws
+    Ws1, Ws3, Ws2 = Ws if Ws is not None else (None, None, None)
+    sv = ctypes.byref(_saved_struct(saved)) if saved is not None else None
+    st = lib().moe_layer_fwd(ctypes.byref(cfg), _p(x), _p(router_w), _p(expert_bias), _p(logit_bias), _p(W1),
+                             _p(W3), _p(W2), _p(Ws1), _p(Ws3), _p(Ws2), _p(y), sv, _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_fwd")
+    return y
+
+
+def alloc_grads(cfg, device="cuda"):
+    T, H, E, F = cfg.T, cfg.H, cfg.E, cfg.F
+    f32 = torch.float32
+    return {
+        "dx": torch.empty((T, H), dtype=_out_dtype(cfg), device=device),
+        "dW_r": torch.empty((E, H), dtype=f32, device=device),
+        "dW1": torch.empty((E, H, F), dtype=f32, device=device),
+        "dW3": torch.empty((E, H, F), dtype=f32, device=device),
+        "dW2": torch.empty((E, F, H), dtype=f32, device=device),
+        "aux_loss": torch.zeros(1, dtype=f32, device=device),
+    }
+
+
+def layer_bwd(cfg, dO, x, router_w, W1, W3, W2, saved, ws=None, grads=None):
+    dev = x.device
+    g = alloc_grads(cfg, dev) if grads is None else grads
+    ws = workspace(cfg, True, dev) if ws is None else ws
+    sv = _saved_struct(saved)
+    st = lib().moe_layer_bwd(ctypes.byref(cfg), _p(dO), _p(x), _p(router_w), _p(W1), _p(W3), _p(W2),
+                             ctypes.byref(sv), _p(g["dx"]), _p(g["dW_r"]), _p(g["dW1"]), _p(g["dW3"]), _p(g["dW2"]),
+                             _p(g["aux_loss"]), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_bwd")
+    return g

@@ -1,0 +1,68 @@
+"""Comparison helpers for the parity tests."""
+import numpy as np
+import torch
+
+# Floating-point bar of the layer: relative L2 error <= 5e-3 and max-abs error
+# <= 2e-2 against the fp64 oracle, for bf16 inputs with fp32 accumulation.
+REL_L2 = 5e-3
+MAX_ABS = 2e-2
+# Selection margin below which a token's top-k is not compared exactly: the
+# k-th and (k+1)-th selection scores differ by less than this.
+TIE_MARGIN = 1e-6
+
+
+def f64(t):
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def rel_l2(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
+
+
+def assert_close(name, got, ref, rel=REL_L2, atol=MAX_ABS):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, f"{name}: shape {got.shape} vs {ref.shape}"
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    r = rel_l2(got, ref)
+    m = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    assert r <= rel and m <= atol, f"{name}: rel_l2={r:.3e} (<= {rel}), max_abs={m:.3e} (<= {atol})"
+    return r, m
+
+
+def topk_margin(z, k):
+    """Gap between the k-th and (k+1)-th largest selection values per token
+    (inf when k == E)."""
+    zs = -np.sort(-np.where(np.isfinite(z), z, -1e300), axis=1)
+    if zs.shape[1] == k:
+        return np.full(zs.shape[0], np.inf)
+    return zs[:, k - 1] - zs[:, k]
+
+
+def compare_topk(got_idx, ref_idx, z, k, margin=TIE_MARGIN):
+    """Exact comparison of the selected experts on tokens whose selection margin
+    is >= `margin`; the slot order is compared where the selected values are
+    themselves separated by >= margin. Returns the number of excluded tokens;
+    for them only validity (k distinct experts, each within `margin` of the
+    selection threshold) is checked."""
+    got_idx = np.asarray(got_idx, np.int64)
+    ref_idx = np.asarray(ref_idx, np.int64)
+    T = got_idx.shape[0]
+    mg = topk_margin(z, k)
+    excl = mg < margin
+    for t in range(T):
+        g, r = got_idx[t], ref_idx[t]
+        assert len(set(g.tolist())) == k and g.min() >= 0 and g.max() < z.shape[1], f"token {t}: invalid {g}"
+        if excl[t]:
+            thr = np.sort(z[t])[::-1][k - 1]
+            assert np.all(z[t, g] >= thr - margin), f"token {t}: selected value below threshold"
+            continue
+        assert set(g.tolist()) == set(r.tolist()), f"token {t}: got {g} want {r} (margin {mg[t]:.2e})"
+        zr = z[t, r]
+        sep = np.all(np.abs(np.diff(zr)) >= margin) if k > 1 else True
+        if sep:
+            assert np.array_equal(g, r), f"token {t}: slot order {g} want {r}"
+    return int(excl.sum())
