@@ -197,6 +197,23 @@ const char* moe_status_string(int status);
 void moe_debug_set_wait_limit_ns(long long ns);
 void moe_debug_set_fault(int fault);
 
+/* Benchmark support. moe_profile_start(capacity) makes the entry points above
+ * record a CUDA event on the caller's stream at the start of each layer call
+ * and after each of its stages (up to `capacity` events; stage tags: 0 call
+ * start, 1 router, 2 permute, 3/4 expert GEMM 1/2, 5/6 shared expert GEMM 1/2,
+ * 7 combine, 10 combine backward, 11 router backward (element-wise), 12 down
+ * projection data gradient + SwiGLU backward, 13 down projection weight
+ * gradient, 14 gate/up data gradient, 15 gate/up weight gradient, 16 router
+ * data gradient, 17 permute backward, 18 router weight gradient, 19 aux loss).
+ * moe_profile_stop() stops recording. moe_profile_read() waits for the events
+ * and returns their number; ms[i] is the time from event i-1 to event i
+ * (0 for call starts). moe_debug_launch_count() returns the number of kernels
+ * the library has launched in this process. */
+void moe_profile_start(int capacity);
+void moe_profile_stop(void);
+int moe_profile_read(int* tags, float* ms, int max);
+unsigned long long moe_debug_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

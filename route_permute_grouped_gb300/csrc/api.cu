@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "host_util.h"
 
@@ -14,6 +15,37 @@ namespace moe {
 // ---------------------------------------------------------------------------
 static unsigned long long g_wait_limit_ns = 2000000000ull;
 static int g_fault = 0;
+
+// Stage timing log (benchmark support): when enabled, every stage of the
+// layer calls records a CUDA event on the caller's stream, tagged with the
+// stage; the elapsed time between consecutive events is the stage's time.
+struct ProfLog {
+  bool on = false;
+  int n = 0;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> tag;
+};
+static ProfLog g_prof;
+static unsigned long long g_launches = 0;
+
+static void prof_mark(cudaStream_t s, int tag) {
+  if (!g_prof.on || g_prof.n >= static_cast<int>(g_prof.ev.size())) return;
+  cudaEventRecord(g_prof.ev[g_prof.n], s);
+  g_prof.tag[g_prof.n] = tag;
+  ++g_prof.n;
+}
+static void count_launches(int n) { g_launches += static_cast<unsigned long long>(n); }
+
+enum StageTag : int {
+  STAGE_BEGIN = 0, STAGE_ROUTER = 1, STAGE_PERMUTE = 2, STAGE_FFN1 = 3, STAGE_FFN2 = 4, STAGE_SHARED1 = 5,
+  STAGE_SHARED2 = 6, STAGE_COMBINE = 7,
+  STAGE_COMBINE_BWD = 10, STAGE_ROUTER_BWD = 11, STAGE_DGRAD2 = 12, STAGE_WGRAD2 = 13, STAGE_DGRAD1 = 14,
+  STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
+};
+static void stage_done(cudaStream_t s, int tag, int launches) {
+  count_launches(launches);
+  prof_mark(s, tag);
+}
 unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
 int debug_fault() { return g_fault; }
 
@@ -216,7 +248,7 @@ static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bf
 static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offsets, int M,
                    const __nv_bfloat16* x_rows, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
                    const __nv_bfloat16* W2, __nv_bfloat16* h13, __nv_bfloat16* a, void* y, bool y_fp32,
-                   DevStatus* st, cudaStream_t s) {
+                   DevStatus* st, cudaStream_t s, int tag1 = STAGE_FFN1, int tag2 = STAGE_FFN2) {
   GemmParams p = base_params(c, st);
   p.F = F;
   p.ngroups = ngroups;
@@ -232,6 +264,7 @@ static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offse
   MOE_MAP(&m1, W1, F, static_cast<uint64_t>(ngroups) * c.H, 2ull * F, 64, 64);
   MOE_MAP(&m3, W3, F, static_cast<uint64_t>(ngroups) * c.H, 2ull * F, 64, 64);
   MOE_CUDA(launch_gemm(KIND_FFN1, p, ma, m1, m3, num_sms(), s));
+  stage_done(s, tag1, 1);
   // y = a W2
   GemmParams q = base_params(c, st);
   q.F = F;
@@ -245,7 +278,9 @@ static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offse
   CUtensorMap mA;
   MOE_MAP(&mA, a, F, M, 2ull * F, 64, 128);
   MOE_MAP(&m2, W2, c.H, static_cast<uint64_t>(ngroups) * F, 2ull * c.H, 64, 64);
-  return cuda_status(launch_gemm(KIND_FFN2, q, mA, m2, m2, num_sms(), s));
+  MOE_CUDA(launch_gemm(KIND_FFN2, q, mA, m2, m2, num_sms(), s));
+  stage_done(s, tag2, 1);
+  return MOE_OK;
 }
 
 }  // namespace moe
@@ -278,6 +313,30 @@ const char* moe_status_string(int s) {
 void moe_debug_set_wait_limit_ns(long long ns) { g_wait_limit_ns = ns > 0 ? static_cast<unsigned long long>(ns) : 2000000000ull; }
 void moe_debug_set_fault(int fault) { g_fault = fault; }
 
+void moe_profile_start(int capacity) {
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.assign(capacity > 0 ? capacity : 0, nullptr);
+  g_prof.tag.assign(g_prof.ev.size(), -1);
+  for (auto& e : g_prof.ev) cudaEventCreate(&e);
+  g_prof.n = 0;
+  g_prof.on = true;
+}
+
+void moe_profile_stop(void) { g_prof.on = false; }
+
+int moe_profile_read(int* tags, float* ms, int max) {
+  const int n = g_prof.n < max ? g_prof.n : max;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(g_prof.ev[i]) != cudaSuccess) return -1;
+    tags[i] = g_prof.tag[i];
+    ms[i] = 0.0f;
+    if (i > 0 && g_prof.tag[i] != STAGE_BEGIN) cudaEventElapsedTime(&ms[i], g_prof.ev[i - 1], g_prof.ev[i]);
+  }
+  return n;
+}
+
+unsigned long long moe_debug_launch_count(void) { return g_launches; }
+
 int moe_get_device_status(void* ws, void* stream, int* status_out) {
   if (ws == nullptr || status_out == nullptr) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -297,9 +356,11 @@ int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* ro
   if (!x || !router_w || !topk_idx || !topk_gate || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_layout(c, false).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return run_router(c, reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(router_w),
-                    expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials,
-                    at<DevStatus>(ws, 0), static_cast<cudaStream_t>(stream));
+  MOE_TRY(run_router(c, reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(router_w),
+                     expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials, at<DevStatus>(ws, 0),
+                     static_cast<cudaStream_t>(stream)));
+  stage_done(static_cast<cudaStream_t>(stream), STAGE_ROUTER, 1);
+  return MOE_OK;
 }
 
 int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx, moe_bf16* x_perm,
@@ -310,10 +371,11 @@ int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_id
   if (!aligned16(x) || !aligned16(x_perm) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, false);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return cuda_status(launch_permute(c, reinterpret_cast<const __nv_bfloat16*>(x), topk_idx,
-                                    reinterpret_cast<__nv_bfloat16*>(x_perm), row_id_map, counts, offsets,
-                                    at<int32_t>(ws, L.lookback), at<DevStatus>(ws, 0),
-                                    static_cast<cudaStream_t>(stream)));
+  MOE_CUDA(launch_permute(c, reinterpret_cast<const __nv_bfloat16*>(x), topk_idx,
+                          reinterpret_cast<__nv_bfloat16*>(x_perm), row_id_map, counts, offsets,
+                          at<int32_t>(ws, L.lookback), at<DevStatus>(ws, 0), static_cast<cudaStream_t>(stream)));
+  stage_done(static_cast<cudaStream_t>(stream), STAGE_PERMUTE, 2);
+  return MOE_OK;
 }
 
 int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const int32_t* offsets,
@@ -340,7 +402,9 @@ int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32
   const moe_config& c = *cfg;
   if (!y_perm || !row_id_map || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(y) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_combine(c, y_perm, row_id_map, topk_gate, shared_out, y, static_cast<cudaStream_t>(stream)));
+  MOE_CUDA(launch_combine(c, y_perm, row_id_map, topk_gate, shared_out, y, static_cast<cudaStream_t>(stream)));
+  stage_done(static_cast<cudaStream_t>(stream), STAGE_COMBINE, 1);
+  return MOE_OK;
 }
 
 int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w, const float* expert_bias,
@@ -380,20 +444,25 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
     xp = at<__nv_bfloat16>(ws, L.x_perm); a = at<__nv_bfloat16>(ws, L.a); yp = at<void>(ws, L.y_perm);
   }
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  prof_mark(s, STAGE_BEGIN);
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
                      logits, aux, st, s));
+  stage_done(s, STAGE_ROUTER, 1);
   MOE_CUDA(launch_permute(c, xb, idx, xp, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s));
+  stage_done(s, STAGE_PERMUTE, 2);
   MOE_TRY(run_ffn(c, c.F, c.E, offs, c.T * c.k, xp, reinterpret_cast<const __nv_bfloat16*>(W1),
                   reinterpret_cast<const __nv_bfloat16*>(W3), reinterpret_cast<const __nv_bfloat16*>(W2), h13, a, yp,
-                  c.inter_fp32 != 0, st, s));
+                  c.inter_fp32 != 0, st, s, STAGE_FFN1, STAGE_FFN2));
   void* shared = nullptr;
   if (c.F_shared) {
     shared = at<void>(ws, L.s_out);
     MOE_TRY(run_ffn(c, c.F_shared, 1, nullptr, c.T, xb, reinterpret_cast<const __nv_bfloat16*>(Ws1),
                     reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), nullptr,
-                    at<__nv_bfloat16>(ws, L.as), shared, c.inter_fp32 != 0, st, s));
+                    at<__nv_bfloat16>(ws, L.as), shared, c.inter_fp32 != 0, st, s, STAGE_SHARED1, STAGE_SHARED2));
   }
-  return cuda_status(launch_combine(c, yp, rows, gate, shared, y, s));
+  MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
+  stage_done(s, STAGE_COMBINE, 1);
+  return MOE_OK;
 }
 
 int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
@@ -423,11 +492,14 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
   float* dx_r = at<float>(ws, L.dx_r);
   float* dwr_part = at<float>(ws, L.dwr_part);
 
+  prof_mark(s, STAGE_BEGIN);
   // 1. combine backward
   MOE_CUDA(launch_combine_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), saved->y_perm, saved->row_id_map,
                               saved->topk_gate, dy_perm, dgate, s));
+  stage_done(s, STAGE_COMBINE_BWD, 1);
   // 2. router backward (element-wise): dL as bf16 hi/lo
   MOE_CUDA(launch_router_bwd(c, saved->logits, saved->topk_idx, saved->topk_gate, dgate, saved->counts, Ep, dL_hl, s));
+  stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
   {
     GemmParams p = base_params(c, st);
@@ -438,6 +510,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&ma, dy_perm, c.H, R, 2ull * c.H, 64, 128);
     MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 256);
     MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s));
+    stage_done(s, STAGE_DGRAD2, 1);
   }
   // 4. dW2_e = a_e^T dy_perm_e
   {
@@ -451,6 +524,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&mb, dy_perm, c.H, R, 2ull * c.H, 64, 64);
     const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
     MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s));
+    stage_done(s, STAGE_WGRAD2, 1);
   }
   // 5. dx_perm = dh13 [W1_e | W3_e]^T
   {
@@ -463,6 +537,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&m1, W1, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
     MOE_MAP(&m3, W3, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
     MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s));
+    stage_done(s, STAGE_DGRAD1, 1);
   }
   // 6. dW1_e | dW3_e = x_perm_e^T dh13_e
   {
@@ -476,6 +551,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&mb, dh13, 2ull * c.F, R, 4ull * c.F, 64, 64);
     const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
     MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s));
+    stage_done(s, STAGE_WGRAD13, 1);
   }
   // 7. router part of dx: dx_r = dL W_r (fp32)
   {
@@ -488,9 +564,11 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&mb, router_w, c.H, c.E, 2ull * c.H, 64, 64);
     const int tiles = ((c.T + kBM - 1) / kBM) * p.n_tiles;
     MOE_CUDA(launch_gemm(KIND_ROUTER_DX, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s));
+    stage_done(s, STAGE_ROUTER_DX, 1);
   }
   // 8. dx = sum_i dx_perm[row(t,i)] + dx_r
   MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s));
+  stage_done(s, STAGE_UNPERMUTE, 1);
   // 9. dW_r = dL^T x, split over K, then reduced in split order
   {
     const int splits = router_dw_splits(c.T);
@@ -506,10 +584,13 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     const int tiles = splits * p.m_tiles_fixed * p.n_tiles;
     MOE_CUDA(launch_gemm(KIND_ROUTER_DW, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s));
     MOE_CUDA(launch_split_reduce(dwr_part, splits, static_cast<size_t>(c.E) * c.H, dW_router, s));
+    stage_done(s, STAGE_ROUTER_DW, 2);
   }
   // 10. aux loss value
-  if (c.aux_coeff != 0.0f && aux_loss_out != nullptr)
+  if (c.aux_coeff != 0.0f && aux_loss_out != nullptr) {
     MOE_CUDA(launch_aux_loss(c, saved->aux_partials, saved->counts, aux_loss_out, s));
+    stage_done(s, STAGE_AUX, 1);
+  }
   return MOE_OK;
 }
 
