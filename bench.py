@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer hot path on GB300: prints ONE JSON line.
+
+A step is one pass of the whole path over one batch of synthetic input: router
+(GEMM + score + top-k + gates), permute (histogram, scan, scatter), grouped
+SwiGLU experts, combine, and for training workloads the full backward (combine
+backward, SwiGLU backward, data and weight gradients of every GEMM, permute
+backward, router backward with the auxiliary-loss gradient).
+
+The default workload is the Qwen3-235B-shaped layer (T=16384 tokens, H=4096,
+E=128 experts, top-8, F=1536) as a training step, balanced routing. Its
+inputs (x 134 MB, expert weights 4.8 GB) are larger than the 129 MB L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (N>1, one process per GPU under torch.distributed.run): the path
+does not shard across GPUs here; every rank runs an independent replica of the
+layer (weak scaling, no collective on the data path); time is the max over
+ranks and the value is the work of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer TFLOPS (fwd, fwd+bwd) & tokens/s on 1 GB300; % of BF16/HBM roofline"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_train")
+    ap.add_argument("--seed", type=int, default=1234)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# algorithmic FLOPs and bytes
+# ----------------------------------------------------------------------------
+def layer_flops(ls, training):
+    """Active FLOPs: router 2THE, routed experts 6HF per (token, expert) pair,
+    shared expert 6HFs per token; the backward is twice the forward."""
+    T, H, E, k, F = ls.T, ls.H, ls.E, ls.k, ls.F
+    fwd = 2 * T * H * E + 6 * H * F * T * k + 6 * H * ls.F_shared * T
+    return 3 * fwd if training else fwd
+
+
+def stage_model(ls, training):
+    """Per stage: (algorithmic FLOPs, algorithmic bytes) of one launch."""
+    T, H, E, k, F = ls.T, ls.H, ls.E, ls.k, ls.F
+    R = T * k
+    Ep = ((E + 63) // 64) * 64
+    yb = 2  # bf16 storage of y_perm (fp32 when inter_fp32)
+    if ls.inter_fp32:
+        yb = 4
+    m = {
+        "router": (2 * T * H * E, 2 * T * H + 2 * E * H + 8 * T * k + (4 * T * E if training else 0)),
+        "permute": (0, 4 * T * k * 2 + 2 * T * H + 2 * R * H + 4 * T * k),
+        "ffn1_gate_up": (2 * R * H * 2 * F, 2 * R * H + 2 * 2 * E * H * F + 2 * R * F + (4 * R * F if training else 0)),
+        "ffn2_down": (2 * R * F * H, 2 * R * F + 2 * E * F * H + yb * R * H),
+        "combine": (0, yb * R * H + 2 * T * H + 8 * T * k),
+    }
+    if ls.F_shared:
+        Fs = ls.F_shared
+        m["shared_gate_up"] = (2 * T * H * 2 * Fs, 2 * T * H + 4 * H * Fs + 2 * T * Fs)
+        m["shared_down"] = (2 * T * Fs * H, 2 * T * Fs + 2 * Fs * H + yb * T * H)
+    if training:
+        m.update({
+            "combine_bwd": (0, 2 * T * H + yb * R * H + 2 * R * H + 8 * T * k),
+            "router_bwd_elem": (0, 4 * T * E + 12 * T * k + 2 * T * 2 * Ep),
+            "dgrad_down_swiglu": (2 * R * H * F, 2 * R * H + 2 * E * F * H + 4 * R * F + 4 * R * F),
+            "wgrad_down": (2 * R * F * H, 2 * R * F + 2 * R * H + 4 * E * F * H),
+            "dgrad_gate_up": (2 * R * 2 * F * H, 4 * R * F + 4 * E * H * F + 2 * R * H),
+            "wgrad_gate_up": (2 * R * H * 2 * F, 2 * R * H + 4 * R * F + 8 * E * H * F),
+            "router_dgrad": (2 * T * 2 * Ep * H, 2 * T * 2 * Ep + 2 * E * H + 4 * T * H),
+            "permute_bwd": (0, 2 * R * H + 4 * T * H + 2 * T * H + 4 * T * k),
+            "router_wgrad": (2 * T * 2 * Ep * H, 2 * T * 2 * Ep + 2 * T * H + 4 * E * H),
+            "aux_loss": (0, 4 * E * (T // 32 + 2)),
+        })
+    return m
+
+
+TENSOR_STAGES = {"router", "ffn1_gate_up", "ffn2_down", "shared_gate_up", "shared_down", "dgrad_down_swiglu",
+                 "wgrad_down", "dgrad_gate_up", "wgrad_gate_up", "router_dgrad", "router_wgrad"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024):
+    """Prepare a bounded sample of the same workload for the fp64 oracle: the
+    rows of `n_experts` seeded experts (forward + backward of those experts) and
+    the router over `n_router_tokens` tokens. Returns (fn, flops, description):
+    fn() runs the sample once."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+
+    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    x = f64(d["x"])
+    w_r = f64(d["router_w"])
+    lb = None if d["logit_bias"] is None else f64(d["logit_bias"])
+    rt = O.route(x, w_r, ls.k, ls.score, None if d["expert_bias"] is None else f64(d["expert_bias"]), lb,
+                 ls.n_groups, ls.topk_groups, ls.gate_scale)
+    rng = np.random.default_rng(seed)
+    experts = sorted(rng.choice(ls.E, size=min(n_experts, ls.E), replace=False).tolist())
+    data = []
+    rows_total = 0
+    for e in experts:
+        tt, ii = np.nonzero(rt["topk_idx"] == e)
+        W = (f64(d["W1"][e]), f64(d["W3"][e]), f64(d["W2"][e]))
+        xr = x[tt]
+        dO = f64(d["dO"][torch.from_numpy(tt).to(d["dO"].device)]) if d["dO"] is not None else None
+        data.append((xr, W, rt["topk_gate"][tt, ii], dO))
+        rows_total += len(tt)
+    xs = x[:n_router_tokens]
+    training = ls.aux_coeff > 0 or d["dO"] is not None
+
+    def fn():
+        O.route(xs, w_r, ls.k, ls.score, None, lb, ls.n_groups, ls.topk_groups, ls.gate_scale)
+        for xr, W, g, dO in data:
+            h1, h3, a, out = O.swiglu_expert(xr, *W)
+            if training and dO is not None:
+                dyr = O.bf16_rne(g[:, None] * dO)
+                O.expert_backward(xr, O.bf16_rne(h1), O.bf16_rne(h3), a, dyr, *W)
+
+    mult = 3 if training else 1
+    flops = mult * (2 * len(xs) * ls.H * ls.E + 6 * ls.H * ls.F * rows_total)
+    desc = (f"fp64 numpy oracle: router over {len(xs)} tokens + {'fwd+bwd' if training else 'fwd'} of "
+            f"{len(experts)} seeded experts ({rows_total} routed rows) of the {ls.name} layer")
+    return fn, flops, desc
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def time_oracle(fn, flops, reps):
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        fn()
+    dt = (time.perf_counter() - t0) / reps
+    return flops / dt / 1e12, dt
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args, ls):
+    import torch
+
+    from route_permute_grouped_gb300 import synth
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = synth.make_layer(ls, seed=args.seed, device=dev, training=ls.aux_coeff > 0)
+    fn, flops, desc = oracle_sample(ls, d, args.seed)
+    for _ in range(args.warmup):
+        fn()
+    tflops, dt = time_oracle(fn, flops, args.steps)
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tflops, 6), "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(ls),
+        "cpu_baseline": {"value": round(tflops, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(tflops, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(ls):
+    return {"workload": f"{ls.name}: MoE layer T={ls.T} H={ls.H} E={ls.E} k={ls.k} F={ls.F}"
+                        + (f" Fs={ls.F_shared}" if ls.F_shared else "")
+                        + f" {ls.score} top-{ls.k}" + (f" groups {ls.n_groups}/{ls.topk_groups}" if ls.n_groups > 1 else "")
+                        + (f" zipf {ls.skew}" if ls.skew else " balanced")
+                        + (" fwd+bwd" if ls.aux_coeff > 0 else " fwd"),
+            "tokens": ls.T, "hidden": ls.H, "experts": ls.E, "top_k": ls.k, "ffn": ls.F,
+            "l2": "inputs larger than L2 (x 134 MB, expert weights 4.8 GB); no flush"}
+
+
+def run_ours(args, ls, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from route_permute_grouped_gb300 import build, ops, synth
+
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    training = ls.aux_coeff > 0
+    d = synth.make_layer(ls, seed=args.seed + rank, device=dev, training=training)
+    cfg = ops.config_from_shape(ls)
+    ws = ops.workspace(cfg, training, dev)
+    saved = ops.alloc_saved(cfg, dev) if training else None
+    grads = ops.alloc_grads(cfg, dev) if training else None
+    y = torch.empty((ls.T, ls.H), dtype=torch.bfloat16, device=dev)
+    Ws = (d["Ws1"], d["Ws3"], d["Ws2"]) if ls.F_shared else None
+
+    def fwd():
+        ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"], Ws,
+                      saved=saved, ws=ws, y=y)
+
+    def step():
+        fwd()
+        if training:
+            ops.layer_bwd(cfg, d["dO"], d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws, grads=grads)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = ops.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------- timed region: K whole steps
+    cap = args.steps * 32 + 64
+    clocks = Clocks(local_rank)
+    barrier()
+    clocks.start()
+    l0 = ops.launch_count()
+    ops.profile_start(cap)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ops.profile_stop()
+    barrier()
+    clk = clocks.stop()
+    launches = ops.launch_count() - l0
+    ms = e0.elapsed_time(e1) / args.steps
+    stages = ops.profile_read(cap)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert ops.device_status(ws) == 0
+
+    # ---------------- forward-only timing (same inputs)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for _ in range(args.steps):
+        fwd()
+    f1.record()
+    torch.cuda.synchronize()
+    ms_fwd = f0.elapsed_time(f1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_fwd], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_fwd = float(t.item())
+
+    # ---------------- per-stage table and roofline of the dominant kernel
+    peaks = load_peaks()
+    model = stage_model(ls, training)
+    agg = {}
+    for name, t in stages:
+        a = agg.setdefault(name, [0.0, 0])
+        a[0] += t
+        a[1] += 1
+    kernels = {}
+    for name, (tot, n) in agg.items():
+        avg = tot / n
+        fl, by = model.get(name, (0, 0))
+        ent = {"ms": round(avg, 4), "launches": n, "share": None}
+        if name in TENSOR_STAGES and fl:
+            ach = fl / (avg * 1e-3) / 1e12
+            ent.update(bound="tensor", achieved_tflops=round(ach, 1),
+                       frac=round(ach / peaks["bf16_tflops_sustained"], 4))
+        elif by:
+            ach = by / (avg * 1e-3) / 1e9
+            ent.update(bound="hbm", achieved_gbs=round(ach, 1), frac=round(ach / peaks["hbm_gbs"], 4))
+        kernels[name] = ent
+    total_stage = sum(v[0] for v in agg.values())
+    for name in kernels:
+        kernels[name]["share"] = round(agg[name][0] / total_stage, 4) if total_stage else None
+    dom = max(agg, key=lambda n: agg[n][0])
+    dk = kernels[dom]
+    fl, by = model[dom]
+    if dk.get("bound") == "tensor":
+        roof = {"kernel": dom, "bound": "tensor", "achieved": dk["achieved_tflops"],
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": dk["frac"],
+                "traffic": None, "algorithmic_flops_per_launch": fl, "avg_launch_ms": dk["ms"],
+                "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": dk["frac"], "traffic": None, "algorithmic_bytes_per_launch": by,
+                "avg_launch_ms": dk["ms"], "peak_source": f"{peaks['source']} hbm_gbs"}
+    traffic = load_traffic(dom)
+    if traffic is not None:
+        roof["traffic"] = traffic
+
+    flops_step = layer_flops(ls, training)
+    value = world * flops_step / (ms * 1e-3) / 1e12
+    fwd_value = world * layer_flops(ls, False) / (ms_fwd * 1e-3) / 1e12
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = d["x"].cpu().pin_memory()
+        hdO = d["dO"].cpu().pin_memory() if training else None
+        hy = torch.empty((ls.T, ls.H), dtype=torch.bfloat16).pin_memory()
+        hdx = torch.empty((ls.T, ls.H), dtype=torch.bfloat16).pin_memory() if training else None
+        haux = torch.empty(1, dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(d["x"])
+        dOd = torch.empty_like(d["dO"]) if training else None
+
+        def e2e_step():
+            xd.copy_(hx, non_blocking=True)
+            if training:
+                dOd.copy_(hdO, non_blocking=True)
+            ops.layer_fwd(cfg, xd, d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"], Ws,
+                          saved=saved, ws=ws, y=y)
+            if training:
+                ops.layer_bwd(cfg, dOd, xd, d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws, grads=grads)
+                hdx.copy_(grads["dx"], non_blocking=True)
+                haux.copy_(grads["aux_loss"], non_blocking=True)
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        g1.record()
+        torch.cuda.synchronize()
+        ms_e2e = g0.elapsed_time(g1) / args.steps
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        h2d = hx.numel() * 2 + (hdO.numel() * 2 if training else 0)
+        d2h = hy.numel() * 2 + ((hdx.numel() * 2 + 4) if training else 0)
+        e2e = {"value": round(world * flops_step / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)}
+
+    # ---------------- CPU baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fn, fl_s, desc = oracle_sample(ls, d, args.seed)
+        reps = 1
+        t0 = time.perf_counter()
+        fn()
+        one = time.perf_counter() - t0
+        reps = max(1, min(10, int(15.0 / max(one, 1e-3))))
+        tflops, dt = time_oracle(fn, fl_s, reps)
+        cpu = {"value": round(tflops, 6), "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
+               "sample": desc + f"; {reps} repetitions, {dt:.2f} s each"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(ls),
+            "tokens_per_s": round(world * ls.T / (ms * 1e-3), 1),
+            "fwd": {"value": round(fwd_value, 2), "unit": "TFLOPS", "ms_per_step": round(ms_fwd, 4),
+                    "tokens_per_s": round(world * ls.T / (ms_fwd * 1e-3), 1)},
+            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was captured for the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get(kernel)
+        return None if ent is None else ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from route_permute_grouped_gb300 import synth
+    ls = synth.shape(args.workload)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, ls)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, ls, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

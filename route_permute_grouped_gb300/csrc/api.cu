@@ -1,6 +1,7 @@
 // The C ABI: argument checks, workspace layout, tensor maps and the
 // composition of the kernels into the layer forward and backward.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -42,9 +43,23 @@ enum StageTag : int {
   STAGE_COMBINE_BWD = 10, STAGE_ROUTER_BWD = 11, STAGE_DGRAD2 = 12, STAGE_WGRAD2 = 13, STAGE_DGRAD1 = 14,
   STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
 };
+// MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
+// report the first stage whose kernels failed (debugging aid, off by default).
+static bool debug_sync() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MOE_DEBUG_SYNC");
+    v = (e != nullptr && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
 static void stage_done(cudaStream_t s, int tag, int launches) {
   count_launches(launches);
   prof_mark(s, tag);
+  if (debug_sync()) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    fprintf(stderr, "moe: stage %d done: %s\n", tag, cudaGetErrorString(e));
+  }
 }
 unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
 int debug_fault() { return g_fault; }

@@ -52,6 +52,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     my_r = row_id_map[static_cast<size_t>(t) * k + lane];
     if (gate != nullptr) my_g = gate[static_cast<size_t>(t) * k + lane];
   }
+  // every lane takes all k (row, gate) pairs before the H loop, whose trip
+  // count differs between lanes when H/8 is not a multiple of 32
+  int rows[16];
+  float gs[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    rows[i] = __shfl_sync(0xffffffffu, my_r, i < k ? i : 0);
+    gs[i] = __shfl_sync(0xffffffffu, my_g, i < k ? i : 0);
+  }
   const int nvec = H / 8;
   for (int v = lane; v < nvec; v += 32) {
     float acc[8];
@@ -61,13 +70,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
     }
-    for (int i = 0; i < k; ++i) {
-      const int r = __shfl_sync(0xffffffffu, my_r, i);
-      const float g = __shfl_sync(0xffffffffu, my_g, i);
-      float f[8];
-      Vec8<YP32>::load(y_perm, static_cast<size_t>(r) * H + v * 8, f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(g, f[j], acc[j]);
+    for (int i = 0; i < 16; ++i) {
+      if (i < k) {
+        float f[8];
+        Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(gs[i], f[j], acc[j]);
+      }
     }
     Vec8<OUT32>::store(y, static_cast<size_t>(t) * H + v * 8, acc);
   }
@@ -90,8 +100,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     my_g = gate[static_cast<size_t>(t) * k + lane];
   }
   float dot[16];
+  int rows[16];
+  float gs[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) dot[i] = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    dot[i] = 0.0f;
+    rows[i] = __shfl_sync(0xffffffffu, my_r, i < k ? i : 0);  // outside the divergent H loop
+    gs[i] = __shfl_sync(0xffffffffu, my_g, i < k ? i : 0);
+  }
   const int nvec = H / 8;
   for (int v = lane; v < nvec; v += 32) {
     float d[8];
@@ -99,18 +115,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       if (i < k) {
-        const int r = __shfl_sync(0xffffffffu, my_r, i);
-        const float g = __shfl_sync(0xffffffffu, my_g, i);
         float f[8], o[8];
-        Vec8<YP32>::load(y_perm, static_cast<size_t>(r) * H + v * 8, f);
+        Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f);
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           s = fmaf(d[j], f[j], s);
-          o[j] = g * d[j];
+          o[j] = gs[i] * d[j];
         }
         dot[i] += s;
-        Vec8<false>::store(dy_perm, static_cast<size_t>(r) * H + v * 8, o);
+        Vec8<false>::store(dy_perm, static_cast<size_t>(rows[i]) * H + v * 8, o);
       }
     }
   }
@@ -192,14 +206,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     pdp /= sum;
   }
   __nv_bfloat16* out = dL_hl + static_cast<size_t>(t) * 2 * Ep;
+  int sel_e[16];
+  float sel_d[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // all lanes, before any divergence
+    sel_e[i] = __shfl_sync(0xffffffffu, my_e, i < k ? i : 0);
+    sel_d[i] = __shfl_sync(0xffffffffu, my_dl, i < k ? i : 0);
+  }
   for (int e = lane; e < Ep; e += 32) {
     float d = 0.0f;
     if (e < E) {
-      for (int i = 0; i < k; ++i) {
-        const int ei = __shfl_sync(__activemask(), my_e, i);
-        const float di = __shfl_sync(__activemask(), my_dl, i);
-        if (ei == e) d += di;
-      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i < k && sel_e[i] == e) d += sel_d[i];
       if (aux) {
         const float p = __expf(Lrow[e] - mx) / sum;
         d += p * (dp_scale * static_cast<float>(counts[e]) - pdp);

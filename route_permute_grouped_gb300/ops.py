@@ -74,8 +74,44 @@ def lib():
         for n in ("moe_router_topk", "moe_permute", "moe_grouped_swiglu_ffn", "moe_unpermute_combine",
                   "moe_layer_fwd", "moe_layer_bwd", "moe_get_device_status"):
             getattr(L, n).restype = c_int
+        L.moe_profile_start.argtypes = [c_int]
+        L.moe_profile_start.restype = None
+        L.moe_profile_stop.argtypes = []
+        L.moe_profile_stop.restype = None
+        L.moe_profile_read.argtypes = [POINTER(c_int), POINTER(c_float), c_int]
+        L.moe_profile_read.restype = c_int
+        L.moe_debug_launch_count.argtypes = []
+        L.moe_debug_launch_count.restype = ctypes.c_ulonglong
         _lib = L
     return _lib
+
+
+STAGE_NAMES = {1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
+               6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
+               13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
+               17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss"}
+
+
+def profile_start(capacity: int) -> None:
+    lib().moe_profile_start(int(capacity))
+
+
+def profile_stop() -> None:
+    lib().moe_profile_stop()
+
+
+def profile_read(max_events: int):
+    """[(stage name, ms)] for every recorded stage, in order."""
+    tags = (c_int * max_events)()
+    ms = (c_float * max_events)()
+    n = lib().moe_profile_read(tags, ms, max_events)
+    if n < 0:
+        raise MoeError(4, "moe_profile_read")
+    return [(STAGE_NAMES.get(tags[i], str(tags[i])), float(ms[i])) for i in range(n) if tags[i] != 0]
+
+
+def launch_count() -> int:
+    return int(lib().moe_debug_launch_count())
 
 
 def _p(t):

@@ -8,7 +8,7 @@ import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import assert_close, compare_topk, f64, rel_l2
+from tests._util import MAX_ABS, assert_close, compare_topk, f64, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +30,11 @@ SHAPES = {
     "e_eq_k": synth.shape("tiny", T=200, H=128, E=4, k=4, F=128),
     "k1": synth.shape("tiny", T=300, H=192, E=3, k=1, F=64),
 }
+
+
+# shapes outside the layer configurations (fan-in scaled weights, larger
+# activations): gradients use the one-bf16-ulp max-abs allowance
+FLIP_BOUND_SHAPES = {"ragged", "e128_k8", "skew", "k1"}
 
 
 def _inputs(name, device="cuda", seed=1234):
@@ -89,8 +94,8 @@ def test_permute_bit_exact(T, E, k, skew):
     assert np.array_equal(rows.cpu().numpy(), r_ref)
     xp_ref = O.permute_rows(x.cpu().view(torch.int16).numpy(), r_ref)  # bytes move unchanged
     assert np.array_equal(xp.cpu().view(torch.int16).numpy(), xp_ref)
-    if skew > 0:
-        assert (c_ref == 0).any() or E <= k
+    if skew > 0:  # the skewed draws are far from balanced
+        assert c_ref.max() > 4 * c_ref.mean()
 
 
 def _ffn_inputs(ls, d):
@@ -122,7 +127,7 @@ def test_grouped_swiglu_ffn(name):
 @pytest.mark.parametrize("name", ["tiny", "e128_k8", "dsv3_small"])
 def test_unpermute_combine(name):
     ls, d = _inputs(name)
-    cfg = ops.config_from_shape(ls)
+    cfg = ops.config_from_shape(ls, out_fp32=True)
     R = ls.T * ls.k
     g = torch.Generator(device="cuda").manual_seed(5)
     y_perm = torch.randn((R, ls.H), generator=g, device="cuda").to(torch.float32 if ls.inter_fp32 else torch.bfloat16)
@@ -134,7 +139,8 @@ def test_unpermute_combine(name):
         shared = torch.randn((ls.T, ls.H), generator=g, device="cuda").to(y_perm.dtype)
     y = ops.unpermute_combine(cfg, y_perm, torch.from_numpy(rows.astype(np.int32)).cuda(), gate, shared)
     ref = O.combine(f64(y_perm), rows, f64(gate), None if shared is None else f64(shared))
-    assert_close("y", f64(y), ref, rel=1e-5, atol=1e-2)
+    # fp32 reduction of k terms: a few fp32 ulps
+    assert_close("y", f64(y), ref, rel=1e-6, atol=1e-5)
 
 
 def _layer_ref(ls, n, prec):
@@ -183,10 +189,20 @@ def test_layer_bwd(name):
                       prec=O.Precision(y=False, dx=False))
     # the selection must agree for the gradient comparison to be meaningful
     assert np.array_equal(saved["topk_idx"].cpu().numpy(), ref["topk_idx"]), "routing differs (tie)"
-    assert_close("dx", f64(g["dx"]), ref["dx"])
-    assert_close("dW_r", f64(g["dW_r"]), ref["dW_r"])
     E = ls.E
-    assert_close("dW1", f64(g["dW1"]), np.stack([ref["dW1"][e] for e in range(E)]))
-    assert_close("dW3", f64(g["dW3"]), np.stack([ref["dW3"][e] for e in range(E)]))
-    assert_close("dW2", f64(g["dW2"]), np.stack([ref["dW2"][e] for e in range(E)]))
+    pairs = {"dx": (f64(g["dx"]), ref["dx"]), "dW_r": (f64(g["dW_r"]), ref["dW_r"]),
+             "dW1": (f64(g["dW1"]), np.stack([ref["dW1"][e] for e in range(E)])),
+             "dW3": (f64(g["dW3"]), np.stack([ref["dW3"][e] for e in range(E)])),
+             "dW2": (f64(g["dW2"]), np.stack([ref["dW2"][e] for e in range(E)]))}
+    for key, (got, want) in pairs.items():
+        atol = MAX_ABS
+        if name in FLIP_BOUND_SHAPES:
+            # bf16-stored activations (dh13, a, dy_perm) whose fp32 value sits
+            # within the fp32-vs-fp64 accumulation difference of a bf16
+            # rounding boundary round to either neighbour on the two sides; one
+            # such flip moves a gradient element by up to one bf16 ulp of the
+            # element's scale (2^-7 relative), so the max-abs bound is one ulp of
+            # the tensor's largest magnitude when that exceeds the layer bound
+            atol = max(MAX_ABS, 2.0 ** -7 * float(np.abs(want).max()))
+        assert_close(key, got, want, atol=atol)
     assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))
