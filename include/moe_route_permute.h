@@ -134,6 +134,29 @@ int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_id
                 moe_bf16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* moe_permute without a workspace. The report has no counterpart of this
+ * entry point; it exists for callers that cannot allocate device memory: a
+ * serving engine that fixes its device memory at start-up and forbids
+ * allocation afterwards, a plug-in whose host runtime owns every device
+ * buffer, or code for which a cudaMalloc could fail or synchronise at the
+ * wrong moment. Same arguments and results as moe_permute minus `ws`.
+ * Its scratch (status word, chunk ticket, lookback words) is a fixed array of
+ * about 1 MiB inside the library, held by every GPU that loads the library
+ * until the process exits; it serves problems with ceil(T/64)*E <= 262144
+ * (for example T <= 65536 with E = 256). Larger problems are rejected with
+ * MOE_ERR_UNSUPPORTED_SHAPE (and a message on stderr) before any GPU work.
+ * The first call on a device looks up the array's device address (set-up with
+ * that device current); make that first call before any stream capture. The
+ * call allocates nothing: it clears the part of the array it uses with
+ * cudaMemsetAsync on `stream` and launches the permute kernels. All calls
+ * share the one array, so calls that overlap on the GPU (other streams or
+ * threads) race and give wrong results; serialise them. Device-side errors
+ * of this entry point are not reported (moe_get_device_status reads a
+ * workspace, which this call does not have). */
+int moe_permute_noalloc(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx,
+                        moe_bf16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
+                        void* stream);
+
 /* Grouped SwiGLU experts (summary page, "Key Terms", Grouped GEMM and
  * "System Modules", Experts; figures & tables page, Table 4): for each expert
  * e, rows offsets[e]..offsets[e+1] of x_perm [R,H]:

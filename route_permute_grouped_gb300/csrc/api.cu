@@ -195,6 +195,8 @@ static int check_cfg(const moe_config* c) {
   return MOE_OK;
 }
 
+int validate_config(const moe_config* c) { return check_cfg(c); }
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static int cuda_status(cudaError_t e) {

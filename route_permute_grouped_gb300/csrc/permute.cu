@@ -1,11 +1,15 @@
 // Local dispatch: per-expert histogram, single-pass decoupled-lookback scan
 // over token chunks, and the 16-byte vectorised row scatter into
 // expert-contiguous rows (dropless; rows of one expert in token order).
+#include <stdio.h>
+
+#include <mutex>
+
 #include "host_util.h"
 
 namespace moe {
 
-constexpr int kChunk = 64;           // tokens per scan chunk (two rank warps)
+constexpr int kChunk = 64;          // tokens per scan chunk (two rank warps)
 constexpr int kScanThreads = 256;
 constexpr uint32_t kFlagP = 0x80000000u;  // inclusive prefix published
 constexpr uint32_t kFlagA = 0x40000000u;  // chunk aggregate published
@@ -209,4 +213,66 @@ size_t permute_lookback_ints(int T, int E) {
   return 64 + static_cast<size_t>((T + kChunk - 1) / kChunk) * E;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free permute: the same kernels, with their scratch (status word,
+// chunk ticket and the per-(chunk, expert) lookback words) in a fixed
+// file-scope device array instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocStatusInts = sizeof(DevStatus) / sizeof(int32_t);  // 64
+constexpr size_t kNoAllocMaxFlags = size_t(1) << 18;  // chunks x experts words (1 MiB)
+constexpr size_t kNoAllocScratchInts = kNoAllocStatusInts + 64 + kNoAllocMaxFlags;
+
+// Every GPU that loads the library holds this array (about 1 MiB) until exit.
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchInts];
+
+// Device address of g_noalloc_scratch per device (host code cannot use the
+// symbol itself: on the host it names a stand-in, not device memory).
+static int32_t* noalloc_scratch_ptr(int dev) {
+  static std::mutex mu;
+  static int32_t* ptrs[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+int validate_config(const moe_config* c);
+
 }  // namespace moe
+
+extern "C" int moe_permute_noalloc(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx,
+                                   moe_bf16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
+                                   void* stream) {
+  using namespace moe;
+  const int v = validate_config(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  if (!x || !topk_idx || !x_perm || !row_id_map || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
+    return MOE_ERR_INVALID_ARG;
+  const size_t flags = static_cast<size_t>((c.T + kChunk - 1) / kChunk) * c.E;
+  if (flags > kNoAllocMaxFlags) {
+    fprintf(stderr,
+            "moe_permute_noalloc: ceil(T/64)*E = %zu exceeds the static scratch limit %zu "
+            "(use moe_permute with a workspace)\n",
+            flags, kNoAllocMaxFlags);
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t* scratch = noalloc_scratch_ptr(dev);
+  if (scratch == nullptr) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = reinterpret_cast<DevStatus*>(scratch);
+  // the status word keeps the previous call's contents: start from zero
+  if (cudaMemsetAsync(st, 0, sizeof(DevStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+  // launch_permute zeroes the ticket and lookback words itself
+  const cudaError_t e = launch_permute(c, reinterpret_cast<const __nv_bfloat16*>(x), topk_idx,
+                                       reinterpret_cast<__nv_bfloat16*>(x_perm), row_id_map, counts, offsets,
+                                       scratch + kNoAllocStatusInts, st, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
