@@ -258,7 +258,8 @@ def workload_config(ls):
                         + (f" zipf {ls.skew}" if ls.skew else " balanced")
                         + (" fwd+bwd" if ls.aux_coeff > 0 else " fwd"),
             "tokens": ls.T, "hidden": ls.H, "experts": ls.E, "top_k": ls.k, "ffn": ls.F,
-            "l2": "inputs larger than L2 (x 134 MB, expert weights 4.8 GB); no flush"}
+            "l2": (f"inputs larger than the 129 MB L2 (x {2 * ls.T * ls.H / 1e6:.0f} MB, expert weights "
+                   f"{6 * ls.E * ls.H * ls.F / 1e9:.2f} GB); no flush")}
 
 
 def run_ours(args, ls, rank, world, local_rank):

@@ -69,6 +69,10 @@ def shape(name: str, **over) -> LayerShape:
         "qwen3_train": dict(T=16384, H=4096, E=128, k=8, F=1536, w_std=0.02, aux_coeff=1e-2),
         "qwen3_skew_train": dict(T=16384, H=4096, E=128, k=8, F=1536, w_std=0.02,
                                  aux_coeff=1e-2, skew=1.2),
+        # profiling case: the Qwen3 expert shape and rows per expert (1024)
+        # with 32 experts, so the device holds about 2 GB
+        "qwen3_e32": dict(T=4096, H=4096, E=32, k=8, F=1536, w_std=0.02),
+        "qwen3_e32_train": dict(T=4096, H=4096, E=32, k=8, F=1536, w_std=0.02, aux_coeff=1e-2),
     }[name]
     base.update(over)
     return LayerShape(name=name, **base)
