@@ -112,6 +112,19 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 4, inner * mid * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
@@ -539,8 +552,11 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     CUtensorMap ma, mb;
     MOE_MAP(&ma, saved->a, c.F, R, 2ull * c.F, 64, 64);
     MOE_MAP(&mb, dy_perm, c.H, R, 2ull * c.H, 64, 64);
+    CUtensorMap mo;
+    if (!make_map_f32_3d(&mo, dW2, c.H, c.F, c.E)) return MOE_ERR_CUDA;
     const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
-    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s));
+    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s,
+                         &mo, &mo));
     stage_done(s, STAGE_WGRAD2, 1);
   }
   // 5. dx_perm = dh13 [W1_e | W3_e]^T
@@ -566,8 +582,12 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     CUtensorMap ma, mb;
     MOE_MAP(&ma, saved->x_perm, c.H, R, 2ull * c.H, 64, 64);
     MOE_MAP(&mb, dh13, 2ull * c.F, R, 4ull * c.F, 64, 64);
+    CUtensorMap mo1, mo3;
+    if (!make_map_f32_3d(&mo1, dW1, c.F, c.H, c.E) || !make_map_f32_3d(&mo3, dW3, c.F, c.H, c.E))
+      return MOE_ERR_CUDA;
     const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
-    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s));
+    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s,
+                         &mo1, &mo3));
     stage_done(s, STAGE_WGRAD13, 1);
   }
   // 7. router part of dx: dx_r = dL W_r (fp32)

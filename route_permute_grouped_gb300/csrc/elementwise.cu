@@ -84,9 +84,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 }
 
 // Combine backward: dy_perm[row[t,i]] = bf16(g[t,i] * dO[t]),
-// dgate[t,i] = <dO[t], y_perm[row[t,i]]> (fp32).
-template <bool YP32>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+// dgate[t,i] = <dO[t], y_perm[row[t,i]]> (fp32). All k expert-output vectors
+// of a position are loaded before any store is issued, so the loads of the k
+// rows are in flight together.
+template <bool YP32, int KMAX>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     combine_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ y_perm,
                        const int32_t* __restrict__ row_id_map, const float* __restrict__ gate,
                        __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dgate, int T, int H, int k) {
@@ -99,11 +101,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     my_r = row_id_map[static_cast<size_t>(t) * k + lane];
     my_g = gate[static_cast<size_t>(t) * k + lane];
   }
-  float dot[16];
-  int rows[16];
-  float gs[16];
+  float dot[KMAX];
+  int rows[KMAX];
+  float gs[KMAX];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < KMAX; ++i) {
     dot[i] = 0.0f;
     rows[i] = __shfl_sync(0xffffffffu, my_r, i < k ? i : 0);  // outside the divergent H loop
     gs[i] = __shfl_sync(0xffffffffu, my_g, i < k ? i : 0);
@@ -112,15 +114,18 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   for (int v = lane; v < nvec; v += 32) {
     float d[8];
     Vec8<false>::load(dO, static_cast<size_t>(t) * H + v * 8, d);
+    float f[KMAX][8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < KMAX; ++i)
+      if (i < k) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f[i]);
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
       if (i < k) {
-        float f[8], o[8];
-        Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f);
+        float o[8];
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          s = fmaf(d[j], f[j], s);
+          s = fmaf(d[j], f[i][j], s);
           o[j] = gs[i] * d[j];
         }
         dot[i] += s;
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     }
   }
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < KMAX; ++i) {
     if (i < k) {
       float s = dot[i];
 #pragma unroll
@@ -293,10 +298,14 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st) {
   const int b = blocks_for(c.T);
-  if (c.inter_fp32)
-    combine_bwd_kernel<true><<<b, kWarpsPerBlock * 32, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
-  else
-    combine_bwd_kernel<false><<<b, kWarpsPerBlock * 32, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+  const int th = kWarpsPerBlock * 32;
+  if (c.inter_fp32) {
+    if (c.k <= 8) combine_bwd_kernel<true, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+    else combine_bwd_kernel<true, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+  } else {
+    if (c.k <= 8) combine_bwd_kernel<false, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+    else combine_bwd_kernel<false, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+  }
   return cudaGetLastError();
 }
 

@@ -19,10 +19,14 @@ struct SmemLayout {
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
   static constexpr int kRouterOff = (kOffOff + (kMaxGroups + 1) * 4 + 15) & ~15;
-  // router scratch: aux column sums [128][33], their partials [4][32],
-  // group scores [128][33], expert_bias [256], logit_bias [256]
-  static constexpr int kRouterBytes = (128 * 33 + 128 + 128 * 33 + 256 + 256) * 4;
-  static constexpr int kBytes = kRouterOff + (KIND == KIND_ROUTER ? kRouterBytes : 0);
+  // router scratch: per-row staging [128][33] (group scores in pass 3, then
+  // softmax values for the aux column sums in pass 4), expert_bias [256],
+  // logit_bias [256]
+  static constexpr int kRouterBytes = (128 * 33 + 256 + 256) * 4;
+  // output staging for TMA stores (weight gradients): 4 KB per epilogue warp
+  static constexpr int kOutOff = (kRouterOff + (KIND == KIND_ROUTER ? kRouterBytes : 0) + 1023) & ~1023;
+  static constexpr int kOutBytes = (KIND == KIND_WGRAD) ? 4 * 4096 : 0;
+  static constexpr int kBytes = kOutOff + kOutBytes;
   static constexpr int kDynBytes = kBytes + 1024;  // + alignment slack
 };
 
@@ -178,11 +182,53 @@ __device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& t
   }
 }
 
+// WGRAD through TMA stores: each epilogue warp stages its 32 rows x 32 fp32
+// columns in a 4 KB shared-memory buffer laid out with the 128-byte swizzle
+// (16-byte chunk j of row r at chunk j ^ (r & 7), so the warp's writes hit
+// distinct banks) and one lane stores the 32 x 32 box with one bulk tensor copy.
+// The output maps are 3-D {N, M, experts}, so rows past M are clipped per expert.
+__device__ __forceinline__ void epi_wgrad_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int q,
+                                              int lane, uint8_t* buf, const CUtensorMap* mo0,
+                                              const CUtensorMap* mo1) {
+  const bool zero = ti.nkb == 0;
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    float f[32];
+    if (!zero) {
+      tmem_ld32f(tacc + c * 32, f);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+    }
+    const int n = ti.n0 + c * 32;
+    if (n >= p.wg_N) continue;  // uniform over the warp
+    if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+    __syncwarp();
+    uint8_t* row = buf + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+          make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const CUtensorMap* m = mo0;
+      int col = n;
+      if (p.wg_mode == 1 && n >= p.wg_N / 2) {
+        m = mo1;
+        col = n - p.wg_N / 2;
+      }
+      tma_store_3d(m, buf, col, ti.m0 + 32 * q, ti.g);
+      bulk_commit();
+    }
+  }
+}
+
 // ROUTER: accumulator row = the E logits of token m0 + r.
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(float z, float sc, int e, float (&tv)[KMAX], float (&ts)[KMAX],
-                                            int (&ti)[KMAX], int k) {
-  if (!(z > tv[k - 1])) return;  // strict: an equal value never displaces a lower index
+                                            int (&ti)[KMAX], int k, float& thr) {
+  if (!(z > thr)) return;  // strict: an equal value never displaces a lower index
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
     if (j < k) {
@@ -197,6 +243,10 @@ __device__ __forceinline__ void topk_insert(float z, float sc, int e, float (&tv
       e = gt ? oi : e;
     }
   }
+  // the k-th value, selected with static indices so the lists stay in registers
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (j == k - 1) thr = tv[j];
 }
 
 template <int KMAX>
@@ -208,7 +258,7 @@ __device__ __forceinline__ void epi_router(const GemmParams& p, const TileInfo& 
   const int nch = p.bn / 32;
   const bool softmax = p.score == MOE_SCORE_SOFTMAX;
   float* s_aux = s_red;                 // [128][33]
-  float* s_gs = s_red + 128 * 33 + 128;  // [128][33] group scores
+  float* s_gs = s_red;                  // [128][33] group scores (pass 3; same rows as s_aux)
   // pass 1: logits (+ logit bias), row max, optional logits store
   float mx = -INFINITY;
 #pragma unroll 1
@@ -298,7 +348,9 @@ __device__ __forceinline__ void epi_router(const GemmParams& p, const TileInfo& 
   int tix[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) { tv[j] = -INFINITY; ts[j] = 0.0f; tix[j] = 0; }
+  float thr = -INFINITY;
   const int gsz = (G > 1) ? E / G : E;
+  __syncwarp();  // the aux sums below reuse the group-score rows of this warp
   const bool want_aux = softmax && p.aux_partials != nullptr;
 #pragma unroll 1
   for (int c = 0; c < nch; ++c) {
@@ -312,7 +364,7 @@ __device__ __forceinline__ void epi_router(const GemmParams& p, const TileInfo& 
       if (want_aux) s_aux[r * 33 + j] = (valid && e < E) ? sc : 0.0f;
       if (e < E && ((allowed >> (e / gsz)) & 1u)) {
         const float z = z_is_logit ? Lb : sc + s_eb[e];
-        topk_insert<KMAX>(z, z_is_logit ? Lb : sc, e, tv, ts, tix, k);
+        topk_insert<KMAX>(z, z_is_logit ? Lb : sc, e, tv, ts, tix, k, thr);
       }
     }
     if (want_aux) {
@@ -364,7 +416,8 @@ __device__ __forceinline__ void epi_router(const GemmParams& p, const TileInfo& 
 template <int KIND, int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap ma,
-                const __grid_constant__ CUtensorMap mb0, const __grid_constant__ CUtensorMap mb1) {
+                const __grid_constant__ CUtensorMap mb0, const __grid_constant__ CUtensorMap mb1,
+                const __grid_constant__ CUtensorMap mo0, const __grid_constant__ CUtensorMap mo1) {
   using TR = KindTraits<KIND>;
   using SL = SmemLayout<KIND>;
   constexpr int NST = TR::kStages;
@@ -448,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_lb = nullptr;
   if constexpr (KIND == KIND_ROUTER) {
     s_red = reinterpret_cast<float*>(smem + SL::kRouterOff);
-    s_eb = s_red + 128 * 33 + 128 + 128 * 33;
+    s_eb = s_red + 128 * 33;
     s_lb = s_eb + 256;
     for (int e = threadIdx.x; e < 256; e += kThreads) {
       s_eb[e] = (p.has_expert_bias && e < p.E) ? p.expert_bias[e] : 0.0f;
@@ -583,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (KIND == KIND_DGRAD1) {
         epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
       } else if constexpr (KIND == KIND_WGRAD) {
-        epi_wgrad(p, ti, tacc, r);
+        epi_wgrad_tma(p, ti, tacc, q, lane, smem + SL::kOutOff + q * 4096, &mo0, &mo1);
       } else if constexpr (KIND == KIND_ROUTER_DX) {
         epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, true, 0);
       } else {  // ROUTER_DW partial of split g: rows m < E
@@ -594,6 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(tempty + acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (KIND == KIND_WGRAD) {
+      if (lane == 0) bulk_wait_all();  // stores issued by this warp are complete
+      __syncwarp();
     }
   }
 
@@ -610,7 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 template <int KIND, int KMAX>
 static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
-                               const CUtensorMap& mb1, int grid, cudaStream_t st) {
+                               const CUtensorMap& mb1, const CUtensorMap& mo0, const CUtensorMap& mo1, int grid,
+                               cudaStream_t st) {
   auto kern = gemm_kernel<KIND, KMAX>;
   const int smem = SmemLayout<KIND>::kDynBytes;
   static int configured_dev = -1;
@@ -621,23 +679,27 @@ static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  kern<<<grid, kThreads, smem, st>>>(p, ma, mb0, mb1);
+  kern<<<grid, kThreads, smem, st>>>(p, ma, mb0, mb1, mo0, mo1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
-                        const CUtensorMap& mb1, int grid, cudaStream_t st) {
+                        const CUtensorMap& mb1, int grid, cudaStream_t st, const CUtensorMap* out0,
+                        const CUtensorMap* out1) {
+  static const CUtensorMap kNone = {};
+  const CUtensorMap& mo0 = out0 ? *out0 : kNone;
+  const CUtensorMap& mo1 = out1 ? *out1 : kNone;
   switch (kind) {
-    case KIND_FFN1: return launch_kind<KIND_FFN1, 1>(p, ma, mb0, mb1, grid, st);
-    case KIND_FFN2: return launch_kind<KIND_FFN2, 1>(p, ma, mb0, mb1, grid, st);
+    case KIND_FFN1: return launch_kind<KIND_FFN1, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_FFN2: return launch_kind<KIND_FFN2, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_ROUTER:
-      if (p.k <= 8) return launch_kind<KIND_ROUTER, 8>(p, ma, mb0, mb1, grid, st);
-      return launch_kind<KIND_ROUTER, 16>(p, ma, mb0, mb1, grid, st);
-    case KIND_DGRAD2: return launch_kind<KIND_DGRAD2, 1>(p, ma, mb0, mb1, grid, st);
-    case KIND_DGRAD1: return launch_kind<KIND_DGRAD1, 1>(p, ma, mb0, mb1, grid, st);
-    case KIND_WGRAD: return launch_kind<KIND_WGRAD, 1>(p, ma, mb0, mb1, grid, st);
-    case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX, 1>(p, ma, mb0, mb1, grid, st);
-    case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW, 1>(p, ma, mb0, mb1, grid, st);
+      if (p.k <= 8) return launch_kind<KIND_ROUTER, 8>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+      return launch_kind<KIND_ROUTER, 16>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_DGRAD2: return launch_kind<KIND_DGRAD2, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_DGRAD1: return launch_kind<KIND_DGRAD1, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_WGRAD: return launch_kind<KIND_WGRAD, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -50,7 +50,7 @@ struct KindTraits {
   static constexpr bool A_MN = (KIND == KIND_WGRAD || KIND == KIND_ROUTER_DW);
   static constexpr bool B_MN = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_WGRAD ||
                                 KIND == KIND_ROUTER_DX || KIND == KIND_ROUTER_DW);
-  static constexpr int kStages = (KIND == KIND_ROUTER) ? 3 : 4;
+  static constexpr int kStages = 4;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
                                         KIND == KIND_DGRAD1);
 };
@@ -197,6 +197,19 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, trow);
   }
 }
+
+// Bulk tensor store shared -> global (3-D box), tracked by bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until no committed bulk store of this thread still reads shared memory
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until every committed bulk store of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {

@@ -21,8 +21,15 @@ int num_sms();
 unsigned long long wait_limit_ns();
 int debug_fault();
 
+// 3-D fp32 tensor map over [outer2, outer1, inner] (row-major), box
+// {32, 32, 1}, 128-byte swizzle: the output map of the weight-gradient GEMM.
+bool make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer);
+
+// out0/out1: output tensor maps of kinds that store through TMA (weight
+// gradients); nullptr for the others.
 cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
-                        const CUtensorMap& mb1, int grid, cudaStream_t st);
+                        const CUtensorMap& mb1, int grid, cudaStream_t st, const CUtensorMap* out0 = nullptr,
+                        const CUtensorMap* out1 = nullptr);
 
 // permute.cu
 cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
