@@ -125,6 +125,22 @@ bool make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+// Store map of a row-major [rows, cols] output for the TMA-store epilogue:
+// 32-row boxes of 128 bytes (64 bf16 or 32 fp32 columns), 128-byte swizzle.
+static bool make_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, bool fp32) {
+  if (!fp32) return make_map_bf16(m, base, cols, rows, 2 * cols, 64, 32);
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
@@ -133,7 +149,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t status, lookback;
   // forward intermediates (inference, or standalone grouped FFN without a_save)
-  size_t topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
+  size_t logits_raw, topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
   // backward
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part;
   size_t total;
@@ -159,6 +175,7 @@ static WsLayout ws_layout(const moe_config& c, bool training) {
   };
   L.status = take(sizeof(DevStatus));
   L.lookback = take(sizeof(int32_t) * permute_lookback_ints(c.T, c.E));
+  L.logits_raw = take(4 * T * (((E + 31) / 32) * 32));
   L.topk_idx = take(4 * T * k);
   L.topk_gate = take(4 * T * k);
   L.row_id_map = take(4 * T * k);
@@ -226,10 +243,6 @@ static GemmParams base_params(const moe_config& c, DevStatus* st) {
   p.splits = 1;
   p.status = st;
   p.wait_limit_ns = g_wait_limit_ns;
-  p.gate_scale = c.gate_scale;
-  p.score = c.score;
-  p.n_groups = c.n_groups;
-  p.topk_groups = c.topk_groups;
   return p;
 }
 
@@ -248,8 +261,8 @@ static GemmParams base_params(const moe_config& c, DevStatus* st) {
 // stages
 // ---------------------------------------------------------------------------
 static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* w_r, const float* eb,
-                      const float* lb, int32_t* idx, float* gate, float* logits, float* aux, DevStatus* st,
-                      cudaStream_t s) {
+                      const float* lb, int32_t* idx, float* gate, float* logits, float* aux, float* raw,
+                      DevStatus* st, cudaStream_t s) {
   GemmParams p = base_params(c, st);
   p.bn = ((c.E + 31) / 32) * 32;
   p.n_tiles = 1;
@@ -257,20 +270,15 @@ static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bf
   p.M_total = c.T;
   p.kb_total = c.H / kBK;
   p.offsets = nullptr;
-  p.has_expert_bias = eb != nullptr;
-  p.has_logit_bias = lb != nullptr;
-  p.expert_bias = eb;
-  p.logit_bias = lb;
-  p.topk_idx = idx;
-  p.topk_gate = gate;
-  p.logits_out = logits;
-  p.aux_partials = aux;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mo;
   MOE_MAP(&ma, x, c.H, c.T, 2ull * c.H, 64, 128);
   MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn);
+  // raw logits [T, bn] fp32 (columns >= E are zero: router rows past E read as zero)
+  if (!make_map_store(&mo, raw, p.bn, c.T, true)) return MOE_ERR_CUDA;
   const int tiles = (c.T + kBM - 1) / kBM;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  return cuda_status(launch_gemm(KIND_ROUTER, p, ma, mb, mb, grid, s));
+  MOE_CUDA(launch_gemm(KIND_ROUTER, p, ma, mb, mb, grid, s, &mo));
+  return cuda_status(launch_router_select(c, raw, p.bn, eb, lb, idx, gate, logits, aux, s));
 }
 
 // grouped (offsets != nullptr, rows of x_rows grouped by expert) or single-group
@@ -293,7 +301,10 @@ static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offse
   MOE_MAP(&ma, x_rows, c.H, M, 2ull * c.H, 64, 128);
   MOE_MAP(&m1, W1, F, static_cast<uint64_t>(ngroups) * c.H, 2ull * F, 64, 64);
   MOE_MAP(&m3, W3, F, static_cast<uint64_t>(ngroups) * c.H, 2ull * F, 64, 64);
-  MOE_CUDA(launch_gemm(KIND_FFN1, p, ma, m1, m3, num_sms(), s));
+  CUtensorMap oa, oh;
+  if (!make_map_store(&oa, a, F, M, false)) return MOE_ERR_CUDA;
+  if (h13 != nullptr && !make_map_store(&oh, h13, 2ull * F, M, false)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_gemm(KIND_FFN1, p, ma, m1, m3, num_sms(), s, &oa, h13 != nullptr ? &oh : nullptr));
   stage_done(s, tag1, 1);
   // y = a W2
   GemmParams q = base_params(c, st);
@@ -308,7 +319,9 @@ static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offse
   CUtensorMap mA;
   MOE_MAP(&mA, a, F, M, 2ull * F, 64, 128);
   MOE_MAP(&m2, W2, c.H, static_cast<uint64_t>(ngroups) * F, 2ull * c.H, 64, 64);
-  MOE_CUDA(launch_gemm(KIND_FFN2, q, mA, m2, m2, num_sms(), s));
+  CUtensorMap oy;
+  if (!make_map_store(&oy, y, c.H, M, y_fp32)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_gemm(KIND_FFN2, q, mA, m2, m2, num_sms(), s, &oy));
   stage_done(s, tag2, 1);
   return MOE_OK;
 }
@@ -387,9 +400,10 @@ int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* ro
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_layout(c, false).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   MOE_TRY(run_router(c, reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(router_w),
-                     expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials, at<DevStatus>(ws, 0),
+                     expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials,
+                     at<float>(ws, ws_layout(c, false).logits_raw), at<DevStatus>(ws, 0),
                      static_cast<cudaStream_t>(stream)));
-  stage_done(static_cast<cudaStream_t>(stream), STAGE_ROUTER, 1);
+  stage_done(static_cast<cudaStream_t>(stream), STAGE_ROUTER, 2);
   return MOE_OK;
 }
 
@@ -476,8 +490,8 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   prof_mark(s, STAGE_BEGIN);
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
-                     logits, aux, st, s));
-  stage_done(s, STAGE_ROUTER, 1);
+                     logits, aux, at<float>(ws, L.logits_raw), st, s));
+  stage_done(s, STAGE_ROUTER, 2);
   MOE_CUDA(launch_permute(c, xb, idx, xp, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s));
   stage_done(s, STAGE_PERMUTE, 2);
   MOE_TRY(run_ffn(c, c.F, c.E, offs, c.T * c.k, xp, reinterpret_cast<const __nv_bfloat16*>(W1),
@@ -539,7 +553,9 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     CUtensorMap ma, mb;
     MOE_MAP(&ma, dy_perm, c.H, R, 2ull * c.H, 64, 128);
     MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 256);
-    MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s));
+    CUtensorMap od;
+    if (!make_map_store(&od, dh13, 2ull * c.F, R, false)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s, &od));
     stage_done(s, STAGE_DGRAD2, 1);
   }
   // 4. dW2_e = a_e^T dy_perm_e
@@ -569,7 +585,9 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&ma, dh13, 2ull * c.F, R, 4ull * c.F, 64, 128);
     MOE_MAP(&m1, W1, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
     MOE_MAP(&m3, W3, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
-    MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s));
+    CUtensorMap od;
+    if (!make_map_store(&od, dx_perm, c.H, R, false)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s, &od));
     stage_done(s, STAGE_DGRAD1, 1);
   }
   // 6. dW1_e | dW3_e = x_perm_e^T dh13_e
@@ -600,7 +618,9 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&ma, dL_hl, 2ull * Ep, c.T, 4ull * Ep, 64, 128);
     MOE_MAP(&mb, router_w, c.H, c.E, 2ull * c.H, 64, 64);
     const int tiles = ((c.T + kBM - 1) / kBM) * p.n_tiles;
-    MOE_CUDA(launch_gemm(KIND_ROUTER_DX, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s));
+    CUtensorMap od;
+    if (!make_map_store(&od, dx_r, c.H, c.T, true)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_ROUTER_DX, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s, &od));
     stage_done(s, STAGE_ROUTER_DX, 1);
   }
   // 8. dx = sum_i dx_perm[row(t,i)] + dx_r
@@ -619,7 +639,9 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&ma, dL_hl, 2ull * Ep, c.T, 4ull * Ep, 64, 64);
     MOE_MAP(&mb, x, c.H, c.T, 2ull * c.H, 64, 64);
     const int tiles = splits * p.m_tiles_fixed * p.n_tiles;
-    MOE_CUDA(launch_gemm(KIND_ROUTER_DW, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s));
+    CUtensorMap od;
+    if (!make_map_f32_3d(&od, dwr_part, c.H, c.E, splits)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_ROUTER_DW, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s, &od));
     MOE_CUDA(launch_split_reduce(dwr_part, splits, static_cast<size_t>(c.E) * c.H, dW_router, s));
     stage_done(s, STAGE_ROUTER_DW, 2);
   }

@@ -236,24 +236,37 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 }
 
-// aux loss value: alpha * E * sum_e (c_e / (T k)) * (sum_tiles partial[tile][e] / T)
-__global__ void aux_loss_kernel(const float* __restrict__ partials, int ntiles, const int32_t* __restrict__ counts,
-                                int T, int E, int k, float aux_coeff, float* __restrict__ out) {
+// aux loss value: alpha * E * sum_e (c_e / (T k)) * (sum_rows partial[row][e] / T).
+// One block of 1024 threads: thread (part, e) sums every fourth row of column
+// e (coalesced over e), the four parts and then the experts are combined in a
+// fixed order.
+__global__ void __launch_bounds__(1024) aux_loss_kernel(const float* __restrict__ partials, int nrows,
+                                                        const int32_t* __restrict__ counts, int T, int E, int k,
+                                                        float aux_coeff, float* __restrict__ out) {
+  __shared__ float s_part[4][256];
   __shared__ float s[256];
-  const int e = threadIdx.x;
-  float v = 0.0f;
+  const int e = threadIdx.x & 255, part = threadIdx.x >> 8;
+  float P = 0.0f;
   if (e < E) {
-    float P = 0.0f;
-    for (int i = 0; i < ntiles; ++i) P += partials[static_cast<size_t>(i) * E + e];
-    v = (static_cast<float>(counts[e]) / (static_cast<float>(T) * k)) * (P / static_cast<float>(T));
+#pragma unroll 8
+    for (int i = part; i < nrows; i += 4) P += partials[static_cast<size_t>(i) * E + e];
   }
-  s[e] = v;
+  s_part[part][e] = P;
+  __syncthreads();
+  if (threadIdx.x < 256) {
+    float v = 0.0f;
+    if (e < E) {
+      const float Pe = (s_part[0][e] + s_part[1][e]) + (s_part[2][e] + s_part[3][e]);
+      v = (static_cast<float>(counts[e]) / (static_cast<float>(T) * k)) * (Pe / static_cast<float>(T));
+    }
+    s[e] = v;
+  }
   __syncthreads();
   for (int d = 128; d > 0; d >>= 1) {
-    if (e < d) s[e] += s[e + d];
+    if (threadIdx.x < d) s[threadIdx.x] += s[threadIdx.x + d];
     __syncthreads();
   }
-  if (e == 0) *out = aux_coeff * static_cast<float>(E) * s[0];
+  if (threadIdx.x == 0) *out = aux_coeff * static_cast<float>(E) * s[0];
 }
 
 // out[i] = sum_s partials[s][i], s in order.
@@ -320,7 +333,7 @@ cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const in
 
 cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
                             cudaStream_t st) {
-  aux_loss_kernel<<<1, 256, 0, st>>>(aux_partials, 4 * ((c.T + 127) / 128), counts, c.T, c.E, c.k, c.aux_coeff, out);
+  aux_loss_kernel<<<1, 1024, 0, st>>>(aux_partials, 4 * ((c.T + 127) / 128), counts, c.T, c.E, c.k, c.aux_coeff, out);
   return cudaGetLastError();
 }
 

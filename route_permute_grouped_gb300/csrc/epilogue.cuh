@@ -1,0 +1,263 @@
+// GEMM epilogues that leave through the TMA: each epilogue warp owns the 32
+// accumulator rows of its TMEM lane quarter and two 4 KB shared-memory staging
+// buffers. A 32-row x 128-byte box (32 fp32 or 64 bf16 columns) is written to a
+// buffer in the 128-byte swizzled layout (16-byte chunk j of row r lands at
+// chunk j ^ (r & 7), so the 32 lanes' writes spread over all banks), then one
+// lane stores the box with a bulk tensor copy. Two buffers let the copy of one
+// box overlap the staging of the next. Blocks that cross the end of an expert's
+// rows use the per-thread masked stores instead (a box would overwrite the next
+// expert's rows).
+#pragma once
+#include "gemm_tc.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+// wait until at most one committed bulk store of this thread still reads
+// shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+struct Stager {
+  uint8_t* base;  // 8 KB, 1024-byte aligned: two boxes
+  uint32_t n;     // boxes committed so far by this warp
+
+  // a free buffer: the one whose previous box (two boxes ago) has been read
+  __device__ __forceinline__ uint8_t* next(int lane) {
+    if (n >= 2 && lane == 0) bulk_wait_read1();
+    __syncwarp();
+    return base + ((n & 1u) << 12);
+  }
+  // both buffers free (every committed box has been read)
+  __device__ __forceinline__ void both(int lane, uint8_t*& b0, uint8_t*& b1) {
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    b0 = base;
+    b1 = base + 4096;
+  }
+  __device__ __forceinline__ void commit2d(int lane, const CUtensorMap* m, const uint8_t* buf, int c0, int c1) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(m, buf, c0, c1);
+      bulk_commit();
+    }
+    ++n;
+  }
+  __device__ __forceinline__ void commit3d(int lane, const CUtensorMap* m, const uint8_t* buf, int c0, int c1,
+                                           int c2) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(m, buf, c0, c1, c2);
+      bulk_commit();
+    }
+    ++n;
+  }
+  __device__ __forceinline__ void drain(int lane) {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+// row `lane` of a box: 32 fp32 (the whole 128-byte row)
+__device__ __forceinline__ void stage_f32x32(uint8_t* buf, int lane, const float* f) {
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+        make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+}
+// row `lane` of a box: 32 bf16 into half `half` (bytes 64*half..) of the row
+__device__ __forceinline__ void stage_bf16x32(uint8_t* buf, int lane, int half, const float* f) {
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 w;
+    w.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+    w.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+    w.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+    w.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+    *reinterpret_cast<uint4*>(row + (((4 * half + j) ^ (lane & 7)) << 4)) = w;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld32_f(uint32_t taddr, float* f) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+}
+
+__device__ __forceinline__ float silu_fast(float z) { return z / (1.0f + __expf(-z)); }
+
+// FFN1, rows row0..row0+31 all inside the expert: a = SiLU(h1) h3 (and h1, h3
+// when saving) for the 128 F-columns n0.. of the tile, in 64-column boxes.
+__device__ __forceinline__ void epi_ffn1_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
+                                             int row0, Stager& st, const CUtensorMap* map_a,
+                                             const CUtensorMap* map_h13) {
+  const bool save = p.out1 != nullptr;
+#pragma unroll 1
+  for (int cc = 0; cc < 2; ++cc) {
+    const int col = ti.n0 + cc * 64;
+    if (col >= p.F) break;  // uniform over the warp
+    uint8_t* buf = st.next(lane);
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float g[32], u[32];
+      tmem_ld32_f(tacc + (cc * 2 + h) * 32, g);
+      tmem_ld32_f(tacc + 128 + (cc * 2 + h) * 32, u);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = silu_fast(g[j]) * u[j];
+      stage_bf16x32(buf, lane, h, g);
+    }
+    st.commit2d(lane, map_a, buf, col, row0);
+    if (save) {
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {  // h1 then h3
+        uint8_t* b = st.next(lane);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float v[32];
+          tmem_ld32_f(tacc + part * 128 + (cc * 2 + h) * 32, v);
+          stage_bf16x32(b, lane, h, v);
+        }
+        st.commit2d(lane, map_h13, b, part * p.F + col, row0);
+      }
+    }
+  }
+}
+
+// Plain store of the 32 x 256 block of this warp: bf16 in 64-column boxes or
+// fp32 in 32-column boxes. 3-D maps (weight gradients, router partials) take
+// the group as the third coordinate and clip rows per group.
+template <bool F32, bool THREE_D>
+__device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc, int lane, int row0, int ncols,
+                                              Stager& st, const CUtensorMap* map) {
+  const bool zero = ti.nkb == 0;
+  if constexpr (F32) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const int col = ti.n0 + c * 32;
+      if (col >= ncols) break;
+      float f[32];
+      if (!zero) {
+        tmem_ld32_f(tacc + c * 32, f);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+      }
+      uint8_t* buf = st.next(lane);
+      stage_f32x32(buf, lane, f);
+      if (THREE_D) st.commit3d(lane, map, buf, col, row0, ti.g);
+      else st.commit2d(lane, map, buf, col, row0);
+    }
+  } else {
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      const int col = ti.n0 + cc * 64;
+      if (col >= ncols) break;
+      uint8_t* buf = st.next(lane);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float f[32];
+        if (!zero) {
+          tmem_ld32_f(tacc + (cc * 2 + h) * 32, f);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+        }
+        stage_bf16x32(buf, lane, h, f);
+      }
+      if (THREE_D) st.commit3d(lane, map, buf, col, row0, ti.g);
+      else st.commit2d(lane, map, buf, col, row0);
+    }
+  }
+}
+
+// Weight gradient: 32 fp32 columns per box, into dW1 (n < F) or dW3 (n >= F)
+// in mode 1, into dW2 in mode 0; 3-D maps {N, M, experts}.
+__device__ __forceinline__ void epi_wgrad_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
+                                              int row0, Stager& st, const CUtensorMap* mo0,
+                                              const CUtensorMap* mo1) {
+  const bool zero = ti.nkb == 0;
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    const int n = ti.n0 + c * 32;
+    if (n >= p.wg_N) break;
+    float f[32];
+    if (!zero) {
+      tmem_ld32_f(tacc + c * 32, f);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+    }
+    uint8_t* buf = st.next(lane);
+    stage_f32x32(buf, lane, f);
+    const CUtensorMap* m = mo0;
+    int col = n;
+    if (p.wg_mode == 1 && n >= p.wg_N / 2) {
+      m = mo1;
+      col = n - p.wg_N / 2;
+    }
+    st.commit3d(lane, m, buf, col, row0, ti.g);
+  }
+}
+
+// DGRAD2, rows all inside the expert: dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)
+// from the saved bf16 pre-activations; 64-column boxes of dh1 and dh3.
+__device__ __forceinline__ void epi_dgrad2_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
+                                               int row0, Stager& st, const CUtensorMap* map) {
+  const __nv_bfloat16* h13 = reinterpret_cast<const __nv_bfloat16*>(p.in_aux);
+  const size_t base = static_cast<size_t>(row0 + lane) * 2 * p.F;
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    const int col = ti.n0 + cc * 64;
+    if (col >= p.F) break;
+    uint8_t *b1, *b3;
+    st.both(lane, b1, b3);
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float da[32], x1[32], x3[32];
+      tmem_ld32_f(tacc + (cc * 2 + h) * 32, da);
+      const uint4* s1 = reinterpret_cast<const uint4*>(h13 + base + col + 32 * h);
+      const uint4* s3 = reinterpret_cast<const uint4*>(h13 + base + p.F + col + 32 * h);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w1 = s1[q], w3 = s3[q];
+        x1[8 * q + 0] = bf16_lo(w1.x); x1[8 * q + 1] = bf16_hi(w1.x);
+        x1[8 * q + 2] = bf16_lo(w1.y); x1[8 * q + 3] = bf16_hi(w1.y);
+        x1[8 * q + 4] = bf16_lo(w1.z); x1[8 * q + 5] = bf16_hi(w1.z);
+        x1[8 * q + 6] = bf16_lo(w1.w); x1[8 * q + 7] = bf16_hi(w1.w);
+        x3[8 * q + 0] = bf16_lo(w3.x); x3[8 * q + 1] = bf16_hi(w3.x);
+        x3[8 * q + 2] = bf16_lo(w3.y); x3[8 * q + 3] = bf16_hi(w3.y);
+        x3[8 * q + 4] = bf16_lo(w3.z); x3[8 * q + 5] = bf16_hi(w3.z);
+        x3[8 * q + 6] = bf16_lo(w3.w); x3[8 * q + 7] = bf16_hi(w3.w);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float s = 1.0f / (1.0f + __expf(-x1[j]));
+        const float d = da[j];
+        da[j] = d * x3[j] * (s * (1.0f + x1[j] * (1.0f - s)));  // dh1
+        x3[j] = d * x1[j] * s;                                 // dh3
+      }
+      stage_bf16x32(b1, lane, h, da);
+      stage_bf16x32(b3, lane, h, x3);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, b1, col, row0);
+      tma_store_2d(map, b3, p.F + col, row0);
+      bulk_commit();
+    }
+    st.n += 2;
+  }
+}
+
+}  // namespace moe

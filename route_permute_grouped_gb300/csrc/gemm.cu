@@ -2,6 +2,7 @@
 // structure). One template, instantiated once per kind.
 #include <math.h>
 
+#include "epilogue.cuh"
 #include "gemm_tc.cuh"
 #include "host_util.h"
 
@@ -13,21 +14,19 @@ namespace moe {
 template <int KIND>
 struct SmemLayout {
   static constexpr int kStages = KindTraits<KIND>::kStages;
-  static constexpr int kBarOff = kStages * kStageBytes;
+  // output staging for the TMA-store epilogue: 2 x 4 KB per epilogue warp
+  static constexpr int kOutOff = kStages * kStageBytes;
+  static constexpr int kOutBytes = 4 * 8192;
+  static constexpr int kBarOff = kOutOff + kOutBytes;
   static constexpr int kNumBars = 2 * kStages + 5;           // full, empty, tfull[2], tempty[2], drain
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
-  static constexpr int kRouterOff = (kOffOff + (kMaxGroups + 1) * 4 + 15) & ~15;
-  // router scratch: per-row staging [128][33] (group scores in pass 3, then
-  // softmax values for the aux column sums in pass 4), expert_bias [256],
-  // logit_bias [256]
-  static constexpr int kRouterBytes = (128 * 33 + 256 + 256) * 4;
-  // output staging for TMA stores (weight gradients): 4 KB per epilogue warp
-  static constexpr int kOutOff = (kRouterOff + (KIND == KIND_ROUTER ? kRouterBytes : 0) + 1023) & ~1023;
-  static constexpr int kOutBytes = (KIND == KIND_WGRAD) ? 4 * 4096 : 0;
-  static constexpr int kBytes = kOutOff + kOutBytes;
-  static constexpr int kDynBytes = kBytes + 1024;  // + alignment slack
+  static constexpr int kBytes = kOffOff + (kMaxGroups + 1) * 4;
+  // the dynamic shared memory starts 1024-byte aligned (checked at kernel
+  // entry): the 128-byte-swizzled tiles and staging boxes need that alignment
+  static constexpr int kDynBytes = kBytes;
+  static_assert(kDynBytes <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
@@ -152,268 +151,10 @@ __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& 
   }
 }
 
-// WGRAD: fp32 gradient tile of expert g, rows m0.., columns n0.. (zero when the
-// expert has no rows).
-__device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
-  const int m = ti.m0 + r;
-  const bool valid = m < p.wg_M;
-  const bool zero = ti.nkb == 0;
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    float f[32];
-    if (!zero) {
-      tmem_ld32f(tacc + c * 32, f);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = 0.0f;
-    }
-    const int n = ti.n0 + c * 32;
-    if (valid && n < p.wg_N) {
-      float* dst;
-      if (p.wg_mode == 0) {
-        dst = reinterpret_cast<float*>(p.out0) + (static_cast<size_t>(ti.g) * p.wg_M + m) * p.wg_N + n;
-      } else {
-        const int half = p.wg_N / 2;  // F
-        float* base = reinterpret_cast<float*>(n < half ? p.out0 : p.out1);
-        dst = base + (static_cast<size_t>(ti.g) * p.wg_M + m) * half + (n < half ? n : n - half);
-      }
-      store_f32x32(dst, f);
-    }
-  }
-}
-
-// WGRAD through TMA stores: each epilogue warp stages its 32 rows x 32 fp32
-// columns in a 4 KB shared-memory buffer laid out with the 128-byte swizzle
-// (16-byte chunk j of row r at chunk j ^ (r & 7), so the warp's writes hit
-// distinct banks) and one lane stores the 32 x 32 box with one bulk tensor copy.
-// The output maps are 3-D {N, M, experts}, so rows past M are clipped per expert.
-__device__ __forceinline__ void epi_wgrad_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int q,
-                                              int lane, uint8_t* buf, const CUtensorMap* mo0,
-                                              const CUtensorMap* mo1) {
-  const bool zero = ti.nkb == 0;
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    float f[32];
-    if (!zero) {
-      tmem_ld32f(tacc + c * 32, f);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = 0.0f;
-    }
-    const int n = ti.n0 + c * 32;
-    if (n >= p.wg_N) continue;  // uniform over the warp
-    if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
-    __syncwarp();
-    uint8_t* row = buf + lane * 128;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
-          make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      const CUtensorMap* m = mo0;
-      int col = n;
-      if (p.wg_mode == 1 && n >= p.wg_N / 2) {
-        m = mo1;
-        col = n - p.wg_N / 2;
-      }
-      tma_store_3d(m, buf, col, ti.m0 + 32 * q, ti.g);
-      bulk_commit();
-    }
-  }
-}
-
-// ROUTER: accumulator row = the E logits of token m0 + r.
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(float z, float sc, int e, float (&tv)[KMAX], float (&ts)[KMAX],
-                                            int (&ti)[KMAX], int k, float& thr) {
-  if (!(z > thr)) return;  // strict: an equal value never displaces a lower index
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    if (j < k) {
-      const bool gt = z > tv[j];
-      const float ov = tv[j], os = ts[j];
-      const int oi = ti[j];
-      tv[j] = gt ? z : ov;
-      ts[j] = gt ? sc : os;
-      ti[j] = gt ? e : oi;
-      z = gt ? ov : z;
-      sc = gt ? os : sc;
-      e = gt ? oi : e;
-    }
-  }
-  // the k-th value, selected with static indices so the lists stay in registers
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j)
-    if (j == k - 1) thr = tv[j];
-}
-
-template <int KMAX>
-__device__ __forceinline__ void epi_router(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r,
-                                           float* s_red, const float* s_eb, const float* s_lb) {
-  const int t = ti.m0 + r;
-  const bool valid = t < ti.m_end;
-  const int E = p.E, k = p.k;
-  const int nch = p.bn / 32;
-  const bool softmax = p.score == MOE_SCORE_SOFTMAX;
-  float* s_aux = s_red;                 // [128][33]
-  float* s_gs = s_red;                  // [128][33] group scores (pass 3; same rows as s_aux)
-  // pass 1: logits (+ logit bias), row max, optional logits store
-  float mx = -INFINITY;
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    float L[32];
-    tmem_ld32f(tacc + c * 32, L);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = c * 32 + j;
-      L[j] += s_lb[e];
-      if (e < E) mx = fmaxf(mx, L[j]);
-    }
-    if (valid && p.logits_out != nullptr) {
-      float* dst = p.logits_out + static_cast<size_t>(t) * E + c * 32;
-      if ((E & 3) == 0 && c * 32 + 32 <= E) {
-        store_f32x32(dst, L);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c * 32 + j < E) dst[j] = L[j];
-      }
-    }
-  }
-  // pass 2 (softmax): denominator
-  float inv_sum = 1.0f;
-  if (softmax) {
-    float sum = 0.0f;
-#pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-      float L[32];
-      tmem_ld32f(tacc + c * 32, L);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = c * 32 + j;
-        if (e < E) sum += __expf(L[j] + s_lb[e] - mx);
-      }
-    }
-    inv_sum = 1.0f / sum;
-  }
-  // selection value z and gate score sc of expert e from its logit
-  //   softmax, no expert bias: z = logit (same order as the probabilities)
-  //   otherwise: z = score + expert_bias
-  auto score_of = [&](float L) -> float {
-    return softmax ? __expf(L - mx) * inv_sum : 1.0f / (1.0f + __expf(-L));
-  };
-  const bool z_is_logit = softmax && !p.has_expert_bias;
-  // pass 3 (group-limited selection): group score = sum of the two best z
-  uint32_t allowed = 0xffffffffu;
-  const int G = p.n_groups;
-  if (G > 1 && p.topk_groups < G) {
-    const int gsz = E / G;
-    float b1 = -INFINITY, b2 = -INFINITY;
-#pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-      float L[32];
-      tmem_ld32f(tacc + c * 32, L);
-#pragma unroll 1
-      for (int j = 0; j < 32; ++j) {
-        const int e = c * 32 + j;
-        if (e < E) {
-          const float Lb = L[j] + s_lb[e];
-          const float z = z_is_logit ? Lb : score_of(Lb) + s_eb[e];
-          if (z > b1) { b2 = b1; b1 = z; } else if (z > b2) { b2 = z; }
-          if ((e + 1) % gsz == 0) {
-            s_gs[r * 33 + e / gsz] = (gsz >= 2) ? (b1 + b2) : b1;
-            b1 = -INFINITY; b2 = -INFINITY;
-          }
-        }
-      }
-    }
-    // keep the topk_groups best groups (strict >: lower group index wins ties)
-    allowed = 0u;
-#pragma unroll 1
-    for (int s = 0; s < p.topk_groups; ++s) {
-      float best = -INFINITY;
-      int bi = -1;
-#pragma unroll 1
-      for (int g = 0; g < G; ++g) {
-        const float v = s_gs[r * 33 + g];
-        if (!((allowed >> g) & 1u) && (bi < 0 || v > best)) { best = v; bi = g; }
-      }
-      allowed |= 1u << bi;
-    }
-  }
-  // pass 4: top-k (+ aux column sums of the softmax)
-  float tv[KMAX], ts[KMAX];
-  int tix[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) { tv[j] = -INFINITY; ts[j] = 0.0f; tix[j] = 0; }
-  float thr = -INFINITY;
-  const int gsz = (G > 1) ? E / G : E;
-  __syncwarp();  // the aux sums below reuse the group-score rows of this warp
-  const bool want_aux = softmax && p.aux_partials != nullptr;
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    float L[32];
-    tmem_ld32f(tacc + c * 32, L);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = c * 32 + j;
-      const float Lb = L[j] + s_lb[e];
-      const float sc = (want_aux || !z_is_logit) ? score_of(Lb) : 0.0f;
-      if (want_aux) s_aux[r * 33 + j] = (valid && e < E) ? sc : 0.0f;
-      if (e < E && ((allowed >> (e / gsz)) & 1u)) {
-        const float z = z_is_logit ? Lb : sc + s_eb[e];
-        topk_insert<KMAX>(z, z_is_logit ? Lb : sc, e, tv, ts, tix, k, thr);
-      }
-    }
-    if (want_aux) {
-      // column sums over this warp's 32 tokens, in a warp-private slice of
-      // shared memory (no cross-warp barrier): lane j sums column j
-      __syncwarp();
-      float acc = 0.0f;
-      const int w0 = (r >> 5) * 32;
-#pragma unroll 4
-      for (int i = 0; i < 32; ++i) acc += s_aux[(w0 + i) * 33 + (r & 31)];
-      if (c * 32 + (r & 31) < E)
-        p.aux_partials[static_cast<size_t>(ti.m0 / 32 + (r >> 5)) * E + c * 32 + (r & 31)] = acc;
-      __syncwarp();
-    }
-  }
-  if (!valid) return;
-  // gates
-  float g[KMAX];
-  float tot = 0.0f;
-  if (z_is_logit) {
-    // renormalised softmax over the selected logits
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      g[j] = (j < k) ? __expf(ts[j] - ts[0]) : 0.0f;
-      tot += g[j];
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      g[j] = (j < k) ? ts[j] : 0.0f;
-      tot += g[j];
-    }
-  }
-  const float scale = p.gate_scale / tot;
-  int32_t* oi = p.topk_idx + static_cast<size_t>(t) * k;
-  float* og = p.topk_gate + static_cast<size_t>(t) * k;
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    if (j < k) {
-      oi[j] = tix[j];
-      og[j] = g[j] * scale;
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int KIND, int KMAX>
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap ma,
                 const __grid_constant__ CUtensorMap mb0, const __grid_constant__ CUtensorMap mb1,
@@ -421,8 +162,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TR = KindTraits<KIND>;
   using SL = SmemLayout<KIND>;
   constexpr int NST = TR::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // layout assumption broken: report, touch nothing
+    if (threadIdx.x == 0) set_status(p.status, MOE_ERR_CUDA, 99);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
   uint64_t* empty = full + NST;
   uint64_t* tfull = empty + NST;
@@ -496,18 +241,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       run += cnt[i];
     }
   }
-  float* s_red = nullptr;
-  float* s_eb = nullptr;
-  float* s_lb = nullptr;
-  if constexpr (KIND == KIND_ROUTER) {
-    s_red = reinterpret_cast<float*>(smem + SL::kRouterOff);
-    s_eb = s_red + 128 * 33;
-    s_lb = s_eb + 256;
-    for (int e = threadIdx.x; e < 256; e += kThreads) {
-      s_eb[e] = (p.has_expert_bias && e < p.E) ? p.expert_bias[e] : 0.0f;
-      s_lb[e] = (p.has_logit_bias && e < p.E) ? p.logit_bias[e] : 0.0f;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -533,7 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
           mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
           uint8_t* sA = smem + stage * kStageBytes;
-          issue_loads<KIND>(p, ti, kb, sA, sA + kABytes, full + stage, &ma, &mb0, &mb1);
+          // router: every CTA reads the same router weight; start each CTA at a
+          // different k block so the CTAs do not all hit the same L2 lines
+          // at once (the sum runs over all k blocks either way)
+          const int kbl = (KIND == KIND_ROUTER) ? (kb + static_cast<int>(blockIdx.x) * 5) % ti.nkb : kb;
+          issue_loads<KIND>(p, ti, kbl, sA, sA + kABytes, full + stage, &ma, &mb0, &mb1);
           issued_phase[stage] = static_cast<int>(phase);
           if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
@@ -620,27 +357,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    Stager st{smem + SL::kOutOff + q * 8192, 0u};
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
       if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * kAccStride) + (static_cast<uint32_t>(q * 32) << 16);
+      // this warp's 32 rows: a full block leaves through TMA boxes; a block
+      // that crosses the end of the expert's rows uses masked per-thread stores
+      const int row0 = ti.m0 + 32 * q;
+      const bool full_rows = row0 + 32 <= ti.m_end;
+      const bool any_rows = row0 < ti.m_end;
       if constexpr (KIND == KIND_FFN1) {
-        epi_ffn1(p, ti, tacc, r);
+        if (full_rows) epi_ffn1_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
+        else if (any_rows) epi_ffn1(p, ti, tacc, r);
       } else if constexpr (KIND == KIND_FFN2) {
-        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
+        if (full_rows) {
+          if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0);
+          else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
+        } else if (any_rows) {
+          epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
+        }
       } else if constexpr (KIND == KIND_ROUTER) {
-        epi_router<KMAX>(p, ti, tacc, r, s_red, s_eb, s_lb);
+        // raw fp32 logits [T, bn]; the map's row extent T clips the tail
+        epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
       } else if constexpr (KIND == KIND_DGRAD2) {
-        epi_dgrad2(p, ti, tacc, r);
+        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0);
+        else if (any_rows) epi_dgrad2(p, ti, tacc, r);
       } else if constexpr (KIND == KIND_DGRAD1) {
-        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
+        if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
+        else if (any_rows) epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
       } else if constexpr (KIND == KIND_WGRAD) {
-        epi_wgrad_tma(p, ti, tacc, q, lane, smem + SL::kOutOff + q * 4096, &mo0, &mo1);
+        // 3-D output maps clip rows past M per expert
+        epi_wgrad_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
       } else if constexpr (KIND == KIND_ROUTER_DX) {
-        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, true, 0);
-      } else {  // ROUTER_DW partial of split g: rows m < E
-        epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, true, static_cast<size_t>(ti.g) * p.E);
+        // the map's row extent is T: rows past it are clipped
+        epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0);
+      } else {  // ROUTER_DW partial of split g: 3-D map {H, E, splits} clips rows >= E
+        epi_store_tma<true, true>(ti, tacc, lane, row0, p.H, st, &mo0);
       }
       tc_fence_before();
       __syncwarp();
@@ -648,10 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if constexpr (KIND == KIND_WGRAD) {
-      if (lane == 0) bulk_wait_all();  // stores issued by this warp are complete
-      __syncwarp();
-    }
+    st.drain(lane);  // this warp's stores are complete
   }
 
   tc_fence_before();
@@ -665,11 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host launch
 // ---------------------------------------------------------------------------
-template <int KIND, int KMAX>
+template <int KIND>
 static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
                                const CUtensorMap& mb1, const CUtensorMap& mo0, const CUtensorMap& mo1, int grid,
                                cudaStream_t st) {
-  auto kern = gemm_kernel<KIND, KMAX>;
+  auto kern = gemm_kernel<KIND>;
   const int smem = SmemLayout<KIND>::kDynBytes;
   static int configured_dev = -1;
   int dev = 0;
@@ -690,16 +441,14 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
   const CUtensorMap& mo0 = out0 ? *out0 : kNone;
   const CUtensorMap& mo1 = out1 ? *out1 : kNone;
   switch (kind) {
-    case KIND_FFN1: return launch_kind<KIND_FFN1, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_FFN2: return launch_kind<KIND_FFN2, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_ROUTER:
-      if (p.k <= 8) return launch_kind<KIND_ROUTER, 8>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-      return launch_kind<KIND_ROUTER, 16>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_DGRAD2: return launch_kind<KIND_DGRAD2, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_DGRAD1: return launch_kind<KIND_DGRAD1, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_WGRAD: return launch_kind<KIND_WGRAD, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
-    case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW, 1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_FFN1: return launch_kind<KIND_FFN1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_FFN2: return launch_kind<KIND_FFN2>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_ROUTER: return launch_kind<KIND_ROUTER>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_DGRAD2: return launch_kind<KIND_DGRAD2>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_DGRAD1: return launch_kind<KIND_DGRAD1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_WGRAD: return launch_kind<KIND_WGRAD>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

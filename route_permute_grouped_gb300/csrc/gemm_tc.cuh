@@ -27,7 +27,7 @@ namespace moe {
 enum GemmKind : int {
   KIND_FFN1 = 0,       // h = x_perm [W1_e | W3_e]  -> a = SiLU(h1) h3 (+ h13 save)
   KIND_FFN2 = 1,       // y_perm = a W2_e
-  KIND_ROUTER = 2,     // L = x W_r^T -> score, top-k, gates (+ logits, aux partials)
+  KIND_ROUTER = 2,     // raw fp32 router logits L = x W_r^T (selection: router.cu)
   KIND_DGRAD2 = 3,     // da = dy_perm W2_e^T -> SwiGLU backward -> dh13
   KIND_DGRAD1 = 4,     // dx_perm = dh13 [W1_e | W3_e]^T
   KIND_WGRAD = 5,      // dW_e = X_e^T Y_e over the expert's rows (ragged K)
@@ -69,15 +69,6 @@ struct GemmParams {
   int splits;            // ROUTER_DW: number of K splits
   int Ep;                // ROUTER_DX / ROUTER_DW: padded expert count (multiple of 64)
   const int32_t* offsets;  // [ngroups+1] device row offsets (grouped kinds, WGRAD)
-  // router
-  int score, n_groups, topk_groups, has_expert_bias, has_logit_bias;
-  float gate_scale;
-  const float* expert_bias;
-  const float* logit_bias;
-  int32_t* topk_idx;
-  float* topk_gate;
-  float* logits_out;
-  float* aux_partials;
   // outputs / epilogue inputs
   void* out0;            // FFN1: a; FFN2: y_perm; DGRAD2: dh13; DGRAD1: dx_perm;
                          // WGRAD: dW2 or dW1; ROUTER_DX: dx_r (fp32); ROUTER_DW: partials

@@ -31,6 +31,11 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
                         const CUtensorMap& mb1, int grid, cudaStream_t st, const CUtensorMap* out0 = nullptr,
                         const CUtensorMap* out1 = nullptr);
 
+// router.cu: top-k selection from the raw fp32 logits [T, ld] of the router GEMM
+cudaError_t launch_router_select(const moe_config& c, const float* raw, int ld, const float* expert_bias,
+                                 const float* logit_bias, int32_t* topk_idx, float* topk_gate, float* logits_out,
+                                 float* aux_partials, cudaStream_t st);
+
 // permute.cu
 cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
                            __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,

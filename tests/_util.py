@@ -17,6 +17,18 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
+def wgrad_atol(want):
+    """Max-abs bound of an fp32 weight gradient. Weight gradients are sums over
+    many rows of products with activations the training step stores in bf16
+    (dh13, a, dy_perm). Where such an activation's fp32 value lies within the
+    fp32-vs-fp64 accumulation difference of a bf16 rounding boundary, the kernel
+    and the oracle round it to different neighbours; each such flip moves the
+    gradient by one bf16 ulp of the activation times the other operand. The
+    bound is the layer's 2e-2 or one bf16 ulp (2^-7 relative) of the gradient's
+    largest magnitude, whichever is larger; the relative L2 bound stays 5e-3."""
+    return max(MAX_ABS, 2.0 ** -7 * float(np.abs(np.asarray(want, np.float64)).max()))
+
+
 def rel_l2(got, ref):
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     den = np.linalg.norm(ref)

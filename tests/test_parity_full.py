@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import MAX_ABS, assert_close, compare_topk, f64, topk_margin
+from tests._util import assert_close, compare_topk, f64, topk_margin, wgrad_atol
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -153,18 +153,6 @@ def test_full_training_step(name):
     dwr_e = part["dlogits"][:, e] @ x[te] + dL_aux[:, e] @ x[others]
     assert_close(f"dW_r[{e}]", f64(g["dW_r"][e]), dwr_e, atol=wgrad_atol(dwr_e))
     assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-4 * abs(ref["aux_loss"])
-
-
-def wgrad_atol(want):
-    """Max-abs bound of an fp32 weight gradient: a sum over up to ~16K rows of
-    products with bf16-stored activations (dh13, a, dy_perm). Where such an
-    activation's fp32 value lies within the fp32-vs-fp64 accumulation
-    difference of a bf16 rounding boundary, kernel and oracle round it to
-    different neighbours; each such flip moves the sum by one bf16 ulp of the
-    activation times the other operand. The bound is the layer's 2e-2 or one
-    bf16 ulp (2^-7 relative) of the gradient's largest magnitude, whichever is
-    larger; the relative L2 bound stays 5e-3."""
-    return max(MAX_ABS, 2.0 ** -7 * float(np.abs(want).max()))
 
 
 def rt_counts(rt, ls):
