@@ -303,20 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sA = smem + stage * kStageBytes;
         uint8_t* sB = sA + kABytes;
         if constexpr (KIND == KIND_WGRAD) {
-          // ragged K: zero the rows of the last k block that lie past the
-          // expert's rows (they hold the next expert's data or TMA zero fill)
+          // ragged K: the rows of the last k block past the expert's rows hold
+          // the next expert's data (or TMA zero fill). Zeroing them in the A
+          // operand (two 64-row boxes of 128-byte rows) makes their products
+          // zero whatever B holds there (finite values). Lane l clears 16-byte
+          // chunk l&7 of rows valid + l/8, valid + l/8 + 4, ...
           const int valid = ti.krow_end - (ti.krow0 + kb * kBK);
           if (valid < kBK) {
-            const int nbox = 2 + 4;
-            const int chunks_per_row = 8;  // 16-byte chunks in a 128-byte row
-            const int rows = kBK - valid;
-            for (int idx = lane; idx < nbox * rows * chunks_per_row; idx += 32) {
-              const int box = idx / (rows * chunks_per_row);
-              const int rem = idx - box * rows * chunks_per_row;
-              const int rr = valid + rem / chunks_per_row;
-              const int ch = rem % chunks_per_row;
-              uint8_t* base = (box < 2) ? (sA + box * 8192) : (sB + (box - 2) * 8192);
-              *reinterpret_cast<uint4*>(base + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int box = 0; box < 2; ++box) {
+              uint8_t* base = sA + box * 8192 + ((lane & 7) << 4);
+              for (int rr = valid + (lane >> 3); rr < kBK; rr += 4)
+                *reinterpret_cast<uint4*>(base + rr * 128) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
           }
