@@ -453,16 +453,29 @@ def run_ours(args, ls, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def gemm_source_sha():
+    """sha256 prefix of the GEMM kernel sources (the traffic figures in
+    profiles/traffic.json hold only for the sources they were captured on)."""
+    import hashlib
+    d = os.path.join(ROOT, "route_permute_grouped_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "gemm_tc.cuh", "epilogue.cuh", "common.cuh"):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was captured for the current kernel source (else None)."""
+    """DRAM bytes per launch of `kernel` (dram__bytes_read.sum +
+    dram__bytes_write.sum) from the committed ncu summary, or None when it was
+    not captured or the kernel sources changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        d = json.load(open(p))
-        ent = d.get(kernel)
-        return None if ent is None else ent.get("dram_bytes_per_launch")
+        ent = json.load(open(p)).get(kernel)
+        if ent is None or ent.get("source_sha") != gemm_source_sha():
+            return None
+        return ent.get("dram_bytes_per_launch")
     except Exception:
         return None
 
