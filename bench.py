@@ -227,6 +227,23 @@ def time_oracle(fn, flops, reps):
 
 
 # ----------------------------------------------------------------------------
+def max_over_ranks(x, world, device):
+    """The maximum of a per-rank value over all ranks (a step time: the job
+    is as fast as its slowest replica). Identity on one process."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step, ms_per_step, world):
+    """Whole-job TFLOPS: the work of every rank over the max-over-ranks step
+    time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def run_reference(args, ls):
     import torch
 
@@ -320,10 +337,7 @@ def run_ours(args, ls, rank, world, local_rank):
     launches = ops.launch_count() - l0
     ms = e0.elapsed_time(e1) / args.steps
     stages = ops.profile_read(cap)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     assert ops.device_status(ws) == 0
 
     # ---------------- forward-only timing (same inputs)
@@ -335,10 +349,7 @@ def run_ours(args, ls, rank, world, local_rank):
     f1.record()
     torch.cuda.synchronize()
     ms_fwd = f0.elapsed_time(f1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_fwd], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_fwd = float(t.item())
+    ms_fwd = max_over_ranks(ms_fwd, world, dev)
 
     # ---------------- per-stage table and roofline of the dominant kernel
     peaks = load_peaks()
@@ -381,8 +392,8 @@ def run_ours(args, ls, rank, world, local_rank):
         roof["traffic"] = traffic
 
     flops_step = layer_flops(ls, training)
-    value = world * flops_step / (ms * 1e-3) / 1e12
-    fwd_value = world * layer_flops(ls, False) / (ms_fwd * 1e-3) / 1e12
+    value = job_throughput(flops_step, ms, world)
+    fwd_value = job_throughput(layer_flops(ls, False), ms_fwd, world)
 
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
@@ -417,13 +428,10 @@ def run_ours(args, ls, rank, world, local_rank):
         g1.record()
         torch.cuda.synchronize()
         ms_e2e = g0.elapsed_time(g1) / args.steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+        ms_e2e = max_over_ranks(ms_e2e, world, dev)
         h2d = hx.numel() * 2 + (hdO.numel() * 2 if training else 0)
         d2h = hy.numel() * 2 + ((hdx.numel() * 2 + 4) if training else 0)
-        e2e = {"value": round(world * flops_step / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOPS",
+        e2e = {"value": round(job_throughput(flops_step, ms_e2e, world), 3), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)}
 
     # ---------------- CPU baseline (rank 0, N = 1)
