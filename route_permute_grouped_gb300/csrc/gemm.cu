@@ -18,7 +18,7 @@ struct SmemLayout {
   static constexpr int kOutOff = kStages * kStageBytes;
   static constexpr int kOutBytes = 4 * 8192;
   static constexpr int kBarOff = kOutOff + kOutBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;           // full, empty, tfull[2], tempty[2], drain
+  static constexpr int kNumBars = 2 * kStages + 9;  // full, empty, tfull[2], tempty[2], drain, epilogue[4]
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TR = KindTraits<KIND>;
   using SL = SmemLayout<KIND>;
   constexpr int NST = TR::kStages;
+  // This kernel declares no static shared memory: the dynamic region must start
+  // the CTA's shared window (1024-byte aligned) and its layout uses up to the
+  // per-CTA maximum.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // layout assumption broken: report, touch nothing
     if (threadIdx.x == 0) set_status(p.status, MOE_ERR_CUDA, 99);
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty + b, 4);
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(drain + 1 + w, 1);  // epilogue warps' TMA loads
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -356,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     Stager st{smem + SL::kOutOff + q * 8192, 0u};
+    uint32_t epi_phase = 0;  // phase of this warp's load barrier
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
       if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
@@ -380,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // raw fp32 logits [T, bn]; the map's row extent T clips the tail
         epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
       } else if constexpr (KIND == KIND_DGRAD2) {
-        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0);
+        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1, drain + 1 + q, epi_phase, s_abort);
         else if (any_rows) epi_dgrad2(p, ti, tacc, r);
       } else if constexpr (KIND == KIND_DGRAD1) {
         if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
