@@ -354,6 +354,7 @@ def run_ours(args, ls, rank, world, local_rank):
     # ---------------- per-stage table and roofline of the dominant kernel
     peaks = load_peaks()
     model = stage_model(ls, training)
+    ridge = peaks["bf16_tflops_sustained"] * 1e3 / peaks["hbm_gbs"]  # FLOP per byte
     agg = {}
     for name, t in stages:
         a = agg.setdefault(name, [0.0, 0])
@@ -364,13 +365,17 @@ def run_ours(args, ls, rank, world, local_rank):
         avg = tot / n
         fl, by = model.get(name, (0, 0))
         ent = {"ms": round(avg, 4), "launches": n, "share": None}
-        if name in TENSOR_STAGES and fl:
+        # a contraction whose arithmetic intensity (FLOP per algorithmic byte)
+        # is below the ridge point of the two measured peaks is bounded by HBM
+        if name in TENSOR_STAGES and fl and (not by or fl / by >= ridge):
             ach = fl / (avg * 1e-3) / 1e12
             ent.update(bound="tensor", achieved_tflops=round(ach, 1),
                        frac=round(ach / peaks["bf16_tflops_sustained"], 4))
         elif by:
             ach = by / (avg * 1e-3) / 1e9
             ent.update(bound="hbm", achieved_gbs=round(ach, 1), frac=round(ach / peaks["hbm_gbs"], 4))
+            if fl:
+                ent["achieved_tflops"] = round(fl / (avg * 1e-3) / 1e12, 1)
         kernels[name] = ent
     total_stage = sum(v[0] for v in agg.values())
     for name in kernels:

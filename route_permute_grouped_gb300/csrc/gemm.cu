@@ -18,7 +18,8 @@ struct SmemLayout {
   static constexpr int kOutOff = kStages * kStageBytes;
   static constexpr int kOutBytes = 4 * 8192;
   static constexpr int kBarOff = kOutOff + kOutBytes;
-  static constexpr int kNumBars = 2 * kStages + 9;  // full, empty, tfull[2], tempty[2], drain, epilogue[4]
+  static constexpr int kNumBars = 2 * KindTraits<KIND>::kMaxStages + 9;  // full, empty, tfull[2], tempty[2],
+                                                                        // drain, epilogue[4]
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
@@ -161,7 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mo0, const __grid_constant__ CUtensorMap mo1) {
   using TR = KindTraits<KIND>;
   using SL = SmemLayout<KIND>;
-  constexpr int NST = TR::kStages;
+  constexpr int NSTMAX = TR::kMaxStages;
+  const int NST = (KIND == KIND_ROUTER) ? router_stages(p.bn) : TR::kStages;
+  const int SBYTES = (KIND == KIND_ROUTER) ? router_stage_bytes(p.bn) : kStageBytes;
   // This kernel declares no static shared memory: the dynamic region must start
   // the CTA's shared window (1024-byte aligned) and its layout uses up to the
   // per-CTA maximum.
@@ -172,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint8_t* smem = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
-  uint64_t* empty = full + NST;
-  uint64_t* tfull = empty + NST;
+  uint64_t* empty = full + NSTMAX;
+  uint64_t* tfull = empty + NSTMAX;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
@@ -260,16 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (KIND == KIND_FFN1 || KIND == KIND_DGRAD1) tma_prefetch_desc(&mb1);
       int stage = 0;
       uint32_t phase = 0;
-      int issued_phase[NST];
+      int issued_phase[NSTMAX];
 #pragma unroll
-      for (int s = 0; s < NST; ++s) issued_phase[s] = -1;
+      for (int s = 0; s < NSTMAX; ++s) issued_phase[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
           mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
-          uint8_t* sA = smem + stage * kStageBytes;
+          uint8_t* sA = smem + stage * SBYTES;
           // router: every CTA reads the same router weight; start each CTA at a
           // different k block so the CTAs do not all hit the same L2 lines
           // at once (the sum runs over all k blocks either way)
@@ -282,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // drain: wait (bounded, regardless of the abort flag) for copies in flight
         int zero = 0;
-        for (int s = 0; s < NST; ++s)
+#pragma unroll
+        for (int s = 0; s < NSTMAX; ++s)
           if (issued_phase[s] >= 0)
             mbar_wait_bounded(full + s, static_cast<uint32_t>(issued_phase[s]), reinterpret_cast<volatile int*>(&zero),
                               lim, nullptr, 0);
@@ -291,6 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(kBM, p.bn, TR::A_MN, TR::B_MN);
+    // operand descriptors: stage 0's low words, advanced per stage and per
+    // 16-deep k step (K-major: 32 bytes; MN-major: 16 rows of 128 bytes)
+    const uint32_t d_hi = sdesc_hi_sw128(1024);
+    const uint32_t a_lo0 = sdesc_lo(smem_u32(smem), TR::A_MN ? 8192u : 16u);
+    const uint32_t b_lo0 = sdesc_lo(smem_u32(smem) + kABytes, TR::B_MN ? 8192u : 16u);
+    constexpr uint32_t kAStep = TR::A_MN ? (2048u >> 4) : (32u >> 4);
+    constexpr uint32_t kBStep = TR::B_MN ? (2048u >> 4) : (32u >> 4);
+    const uint32_t stage_lo = static_cast<uint32_t>(SBYTES) >> 4;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -304,9 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < ti.nkb; ++kb) {
         if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
         tc_fence_after();
-        uint8_t* sA = smem + stage * kStageBytes;
-        uint8_t* sB = sA + kABytes;
         if constexpr (KIND == KIND_WGRAD) {
+          uint8_t* sA = smem + stage * SBYTES;
           // ragged K: the rows of the last k block past the expert's rows hold
           // the next expert's data (or TMA zero fill). Zeroing them in the A
           // operand (two 64-row boxes of 128-byte rows) makes their products
@@ -325,15 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         if (lane == 0) {
-          const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+          const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
+          const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = TR::A_MN ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
-                                         : smem_desc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = TR::B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
-                                         : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           umma_commit(empty + stage);
         }
         __syncwarp();

@@ -50,7 +50,10 @@ struct KindTraits {
   static constexpr bool A_MN = (KIND == KIND_WGRAD || KIND == KIND_ROUTER_DW);
   static constexpr bool B_MN = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_WGRAD ||
                                 KIND == KIND_ROUTER_DX || KIND == KIND_ROUTER_DW);
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 4;  // stages of kStageBytes: the ring's size
+  // the router's B tile is bn x 64 (bn <= 256): its stages are packed at
+  // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
+  static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
                                         KIND == KIND_DGRAD1);
 };
@@ -201,6 +204,14 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // wait until every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// router stage stride (a multiple of 1024 bytes: bn is a multiple of 32) and
+// the number of such stages in the ring
+__host__ __device__ __forceinline__ int router_stage_bytes(int bn) { return kABytes + bn * 128; }
+__host__ __device__ __forceinline__ int router_stages(int bn) {
+  const int n = (4 * kStageBytes) / router_stage_bytes(bn);
+  return n < 8 ? n : 8;
+}
 
 template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
