@@ -552,7 +552,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     p.out0 = dh13; p.in_aux = saved->h13;
     CUtensorMap ma, mb;
     MOE_MAP(&ma, dy_perm, c.H, R, 2ull * c.H, 64, 128);
-    MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 256);
+    MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 128);  // CTA pairs: 128 rows each
     CUtensorMap od;
     if (!make_map_store(&od, dh13, 2ull * c.F, R, false)) return MOE_ERR_CUDA;
     CUtensorMap oh;  // saved pre-activations, read by the epilogue in 32 x 64 boxes
@@ -585,8 +585,8 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     p.out0 = dx_perm;
     CUtensorMap ma, m1, m3;
     MOE_MAP(&ma, dh13, 2ull * c.F, R, 4ull * c.F, 64, 128);
-    MOE_MAP(&m1, W1, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
-    MOE_MAP(&m3, W3, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 256);
+    MOE_MAP(&m1, W1, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 128);  // CTA pairs: 128 rows each
+    MOE_MAP(&m3, W3, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 128);
     CUtensorMap od;
     if (!make_map_store(&od, dx_perm, c.H, R, false)) return MOE_ERR_CUDA;
     MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s, &od));

@@ -15,7 +15,7 @@ template <int KIND>
 struct SmemLayout {
   static constexpr int kStages = KindTraits<KIND>::kStages;
   // output staging for the TMA-store epilogue: 2 x 4 KB per epilogue warp
-  static constexpr int kOutOff = kStages * kStageBytes;
+  static constexpr int kOutOff = kRingBytes;
   static constexpr int kOutBytes = 4 * 8192;
   static constexpr int kBarOff = kOutOff + kOutBytes;
   static constexpr int kNumBars = 2 * KindTraits<KIND>::kMaxStages + 9;  // full, empty, tfull[2], tempty[2],
@@ -163,8 +163,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TR = KindTraits<KIND>;
   using SL = SmemLayout<KIND>;
   constexpr int NSTMAX = TR::kMaxStages;
+  constexpr bool PAIR = TR::kPair;
   const int NST = (KIND == KIND_ROUTER) ? router_stages(p.bn) : TR::kStages;
-  const int SBYTES = (KIND == KIND_ROUTER) ? router_stage_bytes(p.bn) : kStageBytes;
+  const int SBYTES = (KIND == KIND_ROUTER) ? router_stage_bytes(p.bn) : TR::kStageBytesK;
+  // CTA pairs: rank in the cluster (the even CTA issues the MMAs); tiles are
+  // walked per cluster
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int tile_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   // This kernel declares no static shared memory: the dynamic region must start
   // the CTA's shared window (1024-byte aligned) and its layout uses up to the
   // per-CTA maximum.
@@ -193,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, 4);
+      mbar_init(tempty + b, PAIR ? 8 : 4);  // pairs: the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
     for (int w = 0; w < 4; ++w) mbar_init(drain + 1 + w, 1);  // epilogue warps' TMA loads
@@ -201,8 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(s_tmem, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc2(s_tmem, kTmemCols);
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(s_tmem, kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == 0) {
     // tile schedule: s_off = row offsets of the groups, s_cum = prefix of tiles
@@ -228,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.offsets != nullptr) { lo = p.offsets[g]; hi = p.offsets[g + 1]; }
           else { lo = 0; hi = p.M_total; }
           const int rows = max(hi - lo, 0);
-          c = ((rows + kBM - 1) / kBM) * p.n_tiles;
+          c = ((rows + TR::kTileM - 1) / TR::kTileM) * p.n_tiles;
         }
       }
       cnt[i] = c;
@@ -250,6 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // pairs: the peer's barriers are initialised before any signal crosses over
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int ntiles = s_cum[p.ngroups];
@@ -267,10 +281,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int s = 0; s < NSTMAX; ++s) issued_phase[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
+      for (int tile = tile_first; tile < ntiles && ok; tile += tile_step) {
+        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
+          if constexpr (PAIR) {
+            // both CTAs' shares complete on the even CTA's barrier, which
+            // expects them; a share may land before the expectation (the
+            // transaction count goes below zero meanwhile)
+            uint8_t* sA = smem + stage * SBYTES;
+            if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
+            issue_loads_pair<KIND>(p, ti, kb, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
+                                   &mb0, &mb1);
+            issued_phase[stage] = static_cast<int>(phase);
+            if (++stage == NST) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
           uint8_t* sA = smem + stage * SBYTES;
           // router: every CTA reads the same router weight; start each CTA at a
@@ -282,7 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok && PAIR) {
+        // drain: pair shares complete on the even CTA's barriers, out of this
+        // thread's sight; give copies in flight time to land
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+      } else if (!ok) {
         // drain: wait (bounded, regardless of the abort flag) for copies in flight
         int zero = 0;
 #pragma unroll
@@ -294,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(kBM, p.bn, TR::A_MN, TR::B_MN);
+    const uint32_t idesc = idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
     // operand descriptors: stage 0's low words, advanced per stage and per
     // 16-deep k step (K-major: 32 bytes; MN-major: 16 rows of 128 bytes)
     const uint32_t d_hi = sdesc_hi_sw128(1024);
@@ -308,9 +339,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
-      if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, s_abort, lim, p.status, 2)) { ok = false; break; }
+    // pairs: only the even CTA issues MMAs; its peer's MMA warp holds the
+    // tensor memory allocation and waits at the end
+    for (int tile = tile_first; tile < ntiles && ok && leader; tile += tile_step) {
+      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
+      if constexpr (PAIR) {
+        // the accumulator is free once the epilogue warps of both CTAs are done
+        // with it (the odd CTA's arrive from across the cluster)
+        const uint64_t t0 = globaltimer();
+        bool got = mbar_try_wait_cluster(tempty + acc, acc_phase ^ 1u);
+        while (!got && !*s_abort) {
+          got = mbar_try_wait_cluster(tempty + acc, acc_phase ^ 1u);
+          if (!got && globaltimer() - t0 > lim) {
+            *s_abort = 1;
+            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT, 2);
+          }
+        }
+        if (!got) { ok = false; break; }
+      } else if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, s_abort, lim, p.status, 2)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
       for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -339,16 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(empty + stage);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            if constexpr (PAIR)
+              umma2_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            else
+              umma_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (PAIR) umma2_commit_mc(empty + stage, 3);  // frees the stage in both CTAs
+          else umma_commit(empty + stage);
         }
         __syncwarp();
         if (++stage == NST) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
       if (lane == 0) {
-        if (ti.nkb > 0) umma_commit(tfull + acc);
+        if constexpr (PAIR) umma2_commit_mc(tfull + acc, 3);  // nkb > 0: K is fixed
+        else if (ti.nkb > 0) umma_commit(tfull + acc);
         else mbar_arrive(tfull + acc);
       }
       __syncwarp();
@@ -356,10 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
     // drain every MMA issued by this CTA before the TMEM is released
-    if (lane == 0) umma_commit(drain);
-    __syncwarp();
-    int zero = 0;
-    mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int*>(&zero), lim, nullptr, 0);
+    if (leader) {
+      if (lane == 0) {
+        if constexpr (PAIR) umma2_commit_mc(drain, 1);
+        else umma_commit(drain);
+      }
+      __syncwarp();
+      int zero = 0;
+      mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int*>(&zero), lim, nullptr, 0);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -368,8 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     Stager st{smem + SL::kOutOff + q * 8192, 0u};
     uint32_t epi_phase = 0;  // phase of this warp's load barrier
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile);
+    // pairs: the odd CTA's epilogue frees the even CTA's accumulator slot
+    const uint32_t tempty_even = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
+    for (int tile = tile_first; tile < ntiles; tile += tile_step) {
+      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
       if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * kAccStride) + (static_cast<uint32_t>(q * 32) << 16);
@@ -408,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty + acc);
+      if (lane == 0) {
+        if (PAIR && !leader) mbar_arrive_cluster(tempty_even + 8u * acc);
+        else mbar_arrive(tempty + acc);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -417,9 +482,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // neither CTA leaves (or frees the pair's tensor memory) while its peer may
+    // still read its shared memory or signal its barriers
+    if (*s_abort) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+    }
+    cluster_sync_all();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc2(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -433,15 +508,40 @@ static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const
   auto kern = gemm_kernel<KIND>;
   const int smem = SmemLayout<KIND>::kDynBytes;
   static int configured_dev = -1;
+  static int max_pairs = 0;  // clusters of two CTAs resident at once (pair kinds)
   int dev = 0;
   cudaGetDevice(&dev);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  if (KindTraits<KIND>::kPair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   if (configured_dev != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (KindTraits<KIND>::kPair) {
+      cfg.gridDim = dim3(2 * (num_sms() / 2));
+      e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (max_pairs < 1) return cudaErrorInvalidConfiguration;
+    }
     configured_dev = dev;
   }
-  kern<<<grid, kThreads, smem, st>>>(p, ma, mb0, mb1, mo0, mo1);
-  return cudaGetLastError();
+  if (KindTraits<KIND>::kPair) {
+    // a persistent grid of resident pairs (tiles are walked per cluster)
+    const int pairs = (grid + 1) / 2;
+    grid = 2 * (pairs < max_pairs ? pairs : max_pairs);
+  }
+  cfg.gridDim = dim3(grid);
+  return cudaLaunchKernelEx(&cfg, kern, p, ma, mb0, mb1, mo0, mo1);
 }
 
 cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,

@@ -41,6 +41,7 @@ constexpr int kThreads = 192;
 constexpr int kABytes = kBM * 128;        // 16 KB
 constexpr int kBBytesMax = 256 * 128;     // 32 KB
 constexpr int kStageBytes = kABytes + kBBytesMax;
+constexpr int kRingBytes = 4 * kStageBytes;  // shared memory of the operand stage ring
 constexpr int kMaxGroups = 256;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;           // TMEM column distance of the two accumulators
@@ -50,7 +51,15 @@ struct KindTraits {
   static constexpr bool A_MN = (KIND == KIND_WGRAD || KIND == KIND_ROUTER_DW);
   static constexpr bool B_MN = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_WGRAD ||
                                 KIND == KIND_ROUTER_DX || KIND == KIND_ROUTER_DW);
-  static constexpr int kStages = 4;  // stages of kStageBytes: the ring's size
+  // CTA pairs: the expert GEMMs with a fixed K run as M=256 tiles on two SMs
+  // (cta_group::2); each CTA stages its own 128 rows of A and half of B
+  static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
+                                 KIND == KIND_DGRAD1);
+  static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
+  // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
+  // 16 KB of A + 16 KB of B
+  static constexpr int kStageBytesK = kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
+  static constexpr int kStages = kPair ? 6 : 4;
   // the router's B tile is bn x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
@@ -96,7 +105,7 @@ struct TileInfo {
 
 template <int KIND>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_cum, const int* s_off,
-                                                int tile) {
+                                                int tile, int rank = 0) {
   TileInfo ti;
   int lo = 0, hi = p.ngroups;  // find g with s_cum[g] <= tile < s_cum[g+1]
   while (hi - lo > 1) {
@@ -108,7 +117,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
   int mb = local / p.n_tiles;
   int nb = local - mb * p.n_tiles;
   if constexpr (KindTraits<KIND>::kGroupedRows || KIND == KIND_ROUTER || KIND == KIND_ROUTER_DX) {
-    ti.m0 = s_off[lo] + mb * kBM;
+    // a pair tile spans 256 rows: this CTA's 128 start at rank * 128
+    ti.m0 = s_off[lo] + mb * KindTraits<KIND>::kTileM + rank * kBM;
     ti.m_end = s_off[lo + 1];
     ti.kb0 = 0;
     ti.nkb = p.kb_total;
@@ -138,6 +148,35 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     ti.n0 = nb * p.bn;
   }
   return ti;
+}
+
+// CTA pairs: this CTA's share of k block `kb`: its 128 rows of A and half of B
+// (FFN1: the W1 (even CTA) or W3 (odd CTA) columns of the tile; FFN2: columns
+// n0 + 128 rank ..; DGRAD2 / DGRAD1: B rows n0 + 128 rank .., boxes of 128
+// rows), completing on the even CTA's barrier `bar_cluster`.
+template <int KIND>
+__device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const TileInfo& ti, int kb, int rank,
+                                                 uint8_t* sA, uint8_t* sB, uint32_t bar_cluster, const CUtensorMap* ma,
+                                                 const CUtensorMap* mb0, const CUtensorMap* mb1) {
+  const int kk = kb * kBK;
+  tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
+  if constexpr (KIND == KIND_FFN1) {
+    const int brow = ti.g * p.H + kk;
+    const CUtensorMap* m = rank == 0 ? mb0 : mb1;
+    tma_load_2d_pair(sB, m, bar_cluster, ti.n0, brow);
+    tma_load_2d_pair(sB + 8192, m, bar_cluster, ti.n0 + 64, brow);
+  } else if constexpr (KIND == KIND_FFN2) {
+    const int brow = ti.g * p.F + kk;
+    const int n = ti.n0 + 128 * rank;
+    tma_load_2d_pair(sB, mb0, bar_cluster, n, brow);
+    tma_load_2d_pair(sB + 8192, mb0, bar_cluster, n + 64, brow);
+  } else if constexpr (KIND == KIND_DGRAD2) {
+    tma_load_2d_pair(sB, mb0, bar_cluster, kk, ti.g * p.F + ti.n0 + 128 * rank);
+  } else {  // DGRAD1
+    const int brow = ti.g * p.H + ti.n0 + 128 * rank;
+    if (kk < p.F) tma_load_2d_pair(sB, mb0, bar_cluster, kk, brow);
+    else tma_load_2d_pair(sB, mb1, bar_cluster, kk - p.F, brow);
+  }
 }
 
 // Issue the TMA loads of k block `kb` of tile `ti` into stage buffers sA, sB.
@@ -209,13 +248,14 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // the number of such stages in the ring
 __host__ __device__ __forceinline__ int router_stage_bytes(int bn) { return kABytes + bn * 128; }
 __host__ __device__ __forceinline__ int router_stages(int bn) {
-  const int n = (4 * kStageBytes) / router_stage_bytes(bn);
+  const int n = kRingBytes / router_stage_bytes(bn);
   return n < 8 ? n : 8;
 }
 
 template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
-  if constexpr (KIND == KIND_ROUTER) return kABytes + p.bn * 128;
+  if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
+  else if constexpr (KIND == KIND_ROUTER) return kABytes + p.bn * 128;
   else return kABytes + kBBytesMax;
 }
 
