@@ -565,7 +565,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets;
     p.wg_M = c.F; p.wg_N = c.H; p.wg_mode = 0;
-    p.m_tiles_fixed = (c.F + 127) / 128; p.n_tiles = (c.H + 255) / 256;
+    p.m_tiles_fixed = (c.F + 255) / 256; p.n_tiles = (c.H + 255) / 256;  // CTA-pair tiles of 256 rows
     p.out0 = dW2;
     CUtensorMap ma, mb;
     MOE_MAP(&ma, saved->a, c.F, R, 2ull * c.F, 64, 64);
@@ -597,7 +597,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets;
     p.wg_M = c.H; p.wg_N = 2 * c.F; p.wg_mode = 1;
-    p.m_tiles_fixed = (c.H + 127) / 128; p.n_tiles = (2 * c.F + 255) / 256;
+    p.m_tiles_fixed = (c.H + 255) / 256; p.n_tiles = (2 * c.F + 255) / 256;  // CTA-pair tiles of 256 rows
     p.out0 = dW1; p.out1 = dW3;
     CUtensorMap ma, mb;
     MOE_MAP(&ma, saved->x_perm, c.H, R, 2ull * c.H, 64, 64);

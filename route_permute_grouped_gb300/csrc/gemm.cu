@@ -18,8 +18,8 @@ struct SmemLayout {
   static constexpr int kOutOff = kRingBytes;
   static constexpr int kOutBytes = 4 * 8192;
   static constexpr int kBarOff = kOutOff + kOutBytes;
-  static constexpr int kNumBars = 2 * KindTraits<KIND>::kMaxStages + 9;  // full, empty, tfull[2], tempty[2],
-                                                                        // drain, epilogue[4]
+  static constexpr int kNumBars = 3 * KindTraits<KIND>::kMaxStages + 9;  // full, empty, peer, tfull[2],
+                                                                        // tempty[2], drain, epilogue[4]
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
   uint64_t* empty = full + NSTMAX;
-  uint64_t* tfull = empty + NSTMAX;
+  uint64_t* peer = empty + NSTMAX;  // WGRAD pairs: the odd CTA's ragged k block is ready
+  uint64_t* tfull = peer + NSTMAX;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NST; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
+      mbar_init(peer + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
@@ -286,13 +288,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
           if constexpr (PAIR) {
-            // both CTAs' shares complete on the even CTA's barrier, which
-            // expects them; a share may land before the expectation (the
-            // transaction count goes below zero meanwhile)
             uint8_t* sA = smem + stage * SBYTES;
-            if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
-            issue_loads_pair<KIND>(p, ti, kb, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
-                                   &mb0, &mb1);
+            const bool ragged = KIND == KIND_WGRAD && ti.krow_end - (ti.krow0 + kb * kBK) < kBK;
+            if (ragged) {
+              // WGRAD's partial last k block: each CTA's share completes on
+              // its own barrier, so that each can zero its rows past the
+              // expert before the MMA (the odd CTA then relays)
+              mbar_arrive_expect_tx(full + stage, TR::kStageBytesK);
+              issue_loads_pair<KIND>(p, ti, kb, rank, sA, sA + kABytes, 0u, &ma, &mb0, &mb1, full + stage);
+            } else {
+              // both CTAs' shares complete on the even CTA's barrier, which
+              // expects them; a share may land before the expectation (the
+              // transaction count goes below zero meanwhile)
+              if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
+              issue_loads_pair<KIND>(p, ti, kb, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
+                                     &mb0, &mb1);
+            }
             issued_phase[stage] = static_cast<int>(phase);
             if (++stage == NST) { stage = 0; phase ^= 1u; }
             continue;
@@ -339,6 +350,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    uint32_t rag_bits = 0;  // WGRAD pairs: phase of each stage's ragged-block barrier
+    if (PAIR && KIND == KIND_WGRAD && !leader) {
+      // the odd CTA of a WGRAD pair: for each ragged k block, wait for this
+      // CTA's share, zero its A rows past the expert, and tell the even CTA
+      const uint32_t peer_even = mapa_shared(smem_u32(peer), 0);
+      for (int tile = tile_first; tile < ntiles && ok; tile += tile_step) {
+        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          const int valid = ti.krow_end - (ti.krow0 + kb * kBK);
+          if (valid < kBK) {
+            if (!mbar_wait_bounded(full + stage, (rag_bits >> stage) & 1u, s_abort, lim, p.status, 5)) {
+              ok = false;
+              break;
+            }
+            rag_bits ^= 1u << stage;
+            uint8_t* sA = smem + stage * SBYTES;
+#pragma unroll
+            for (int box = 0; box < 2; ++box) {
+              uint8_t* base = sA + box * 8192 + ((lane & 7) << 4);
+              for (int rr = valid + (lane >> 3); rr < kBK; rr += 4)
+                *reinterpret_cast<uint4*>(base + rr * 128) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(peer_even + 8u * static_cast<uint32_t>(stage));
+          }
+          if (++stage == NST) stage = 0;
+        }
+      }
+    }
     // pairs: only the even CTA issues MMAs; its peer's MMA warp holds the
     // tensor memory allocation and waits at the end
     for (int tile = tile_first; tile < ntiles && ok && leader; tile += tile_step) {
@@ -381,6 +422,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(base + rr * 128) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
+            if constexpr (PAIR) {
+              // the odd CTA's share of this block is zeroed likewise: wait for
+              // its relay (cluster-scope acquire)
+              const uint32_t par = (rag_bits >> stage) & 1u;
+              rag_bits ^= 1u << stage;
+              const uint64_t t0 = globaltimer();
+              bool got = mbar_try_wait_cluster(peer + stage, par);
+              while (!got && !*s_abort) {
+                got = mbar_try_wait_cluster(peer + stage, par);
+                if (!got && globaltimer() - t0 > lim) {
+                  *s_abort = 1;
+                  set_status(p.status, MOE_ERR_DEVICE_TIMEOUT, 6);
+                }
+              }
+              if (!got) { ok = false; break; }
+              tc_fence_after();
+            }
           }
           __syncwarp();
         }
@@ -402,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (lane == 0) {
-        if constexpr (PAIR) umma2_commit_mc(tfull + acc, 3);  // nkb > 0: K is fixed
+        if constexpr (PAIR) umma2_commit_mc(tfull + acc, 3);  // with no MMA (nkb = 0) it arrives at once
         else if (ti.nkb > 0) umma_commit(tfull + acc);
         else mbar_arrive(tfull + acc);
       }

@@ -54,7 +54,7 @@ struct KindTraits {
   // CTA pairs: the expert GEMMs with a fixed K run as M=256 tiles on two SMs
   // (cta_group::2); each CTA stages its own 128 rows of A and half of B
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                 KIND == KIND_DGRAD1);
+                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
@@ -125,7 +125,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     ti.krow0 = 0;
     ti.krow_end = 0;
   } else if constexpr (KIND == KIND_WGRAD) {
-    ti.m0 = mb * kBM;
+    ti.m0 = mb * KindTraits<KIND>::kTileM + rank * kBM;
     ti.m_end = p.wg_M;
     ti.krow0 = s_off[lo];
     ti.krow_end = s_off[lo + 1];
@@ -153,12 +153,31 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
 // CTA pairs: this CTA's share of k block `kb`: its 128 rows of A and half of B
 // (FFN1: the W1 (even CTA) or W3 (odd CTA) columns of the tile; FFN2: columns
 // n0 + 128 rank ..; DGRAD2 / DGRAD1: B rows n0 + 128 rank .., boxes of 128
-// rows), completing on the even CTA's barrier `bar_cluster`.
+// rows; WGRAD: A columns m0 .. m0 + 127 and B columns n0 + 128 rank .. of the
+// expert's rows kb*64 ..), completing on the even CTA's barrier `bar_cluster`,
+// or (WGRAD, `local_bar` != nullptr) on this CTA's own barrier.
 template <int KIND>
 __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const TileInfo& ti, int kb, int rank,
                                                  uint8_t* sA, uint8_t* sB, uint32_t bar_cluster, const CUtensorMap* ma,
-                                                 const CUtensorMap* mb0, const CUtensorMap* mb1) {
+                                                 const CUtensorMap* mb0, const CUtensorMap* mb1,
+                                                 uint64_t* local_bar = nullptr) {
   const int kk = kb * kBK;
+  if constexpr (KIND == KIND_WGRAD) {
+    const int r = ti.krow0 + kk;
+    const int n = ti.n0 + 128 * rank;
+    if (local_bar != nullptr) {
+      tma_load_2d(sA, ma, local_bar, ti.m0, r);
+      tma_load_2d(sA + 8192, ma, local_bar, ti.m0 + 64, r);
+      tma_load_2d(sB, mb0, local_bar, n, r);
+      tma_load_2d(sB + 8192, mb0, local_bar, n + 64, r);
+    } else {
+      tma_load_2d_pair(sA, ma, bar_cluster, ti.m0, r);
+      tma_load_2d_pair(sA + 8192, ma, bar_cluster, ti.m0 + 64, r);
+      tma_load_2d_pair(sB, mb0, bar_cluster, n, r);
+      tma_load_2d_pair(sB + 8192, mb0, bar_cluster, n + 64, r);
+    }
+    return;
+  }
   tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
   if constexpr (KIND == KIND_FFN1) {
     const int brow = ti.g * p.H + kk;
