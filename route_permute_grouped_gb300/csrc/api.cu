@@ -555,9 +555,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 128);  // CTA pairs: 128 rows each
     CUtensorMap od;
     if (!make_map_store(&od, dh13, 2ull * c.F, R, false)) return MOE_ERR_CUDA;
-    CUtensorMap oh;  // saved pre-activations, read by the epilogue in 32 x 64 boxes
-    if (!make_map_store(&oh, saved->h13, 2ull * c.F, R, false)) return MOE_ERR_CUDA;
-    MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s, &od, &oh));
+    MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s, &od));
     stage_done(s, STAGE_DGRAD2, 1);
   }
   // 4. dW2_e = a_e^T dy_perm_e

@@ -210,62 +210,60 @@ __device__ __forceinline__ void epi_wgrad_tma(const GemmParams& p, const TileInf
 }
 
 // DGRAD2, rows all inside the expert: dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1).
-// Per 64-column chunk the warp loads its 32 x 64 boxes of the saved h1 and h3
-// with the TMA into its two staging buffers (completion on the warp's own
-// mbarrier), reads da from TMEM meanwhile, rewrites both boxes in place with
-// dh1 and dh3, and stores them with the TMA. Returns false if the bounded
-// wait ran out (the tile is then left incomplete and the CTA aborts).
-__device__ __forceinline__ bool epi_dgrad2_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
-                                               int row0, Stager& st, const CUtensorMap* map_out,
-                                               const CUtensorMap* map_h13, uint64_t* bar, uint32_t& phase,
-                                               volatile int* abort_flag) {
+// Per 64-column chunk each thread reads its row's 64 values of the saved h1
+// and h3 with vector loads (not through the TMA unit, whose queue holds the
+// operand loads of the main loop), reads da from TMEM, writes dh1 and dh3 into
+// the warp's two staging boxes and stores them with the TMA.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ void epi_dgrad2_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
+                                               int row0, Stager& st, const CUtensorMap* map_out) {
+  const __nv_bfloat16* hrow =
+      reinterpret_cast<const __nv_bfloat16*>(p.in_aux) + static_cast<size_t>(row0 + lane) * (2 * p.F);
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
     const int col = ti.n0 + cc * 64;
     if (col >= p.F) break;
-    uint8_t *b1, *b3;
-    st.both(lane, b1, b3);  // the previous boxes have left both buffers
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar, 2 * 4096);
-      tma_load_2d(b1, map_h13, bar, col, row0);
-      tma_load_2d(b3, map_h13, bar, p.F + col, row0);
+    uint4 v1[8], v3[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v1[j] = ldg_nc_v4(hrow + col + 8 * j);
+      v3[j] = ldg_nc_v4(hrow + p.F + col + 8 * j);
     }
     float da0[32], da1[32];
     tmem_ld32_f(tacc + (cc * 2) * 32, da0);
     tmem_ld32_f(tacc + (cc * 2 + 1) * 32, da1);
-    const bool ok = mbar_wait_bounded(bar, phase, abort_flag, p.wait_limit_ns, p.status, 5);
-    phase ^= 1u;
-    if (!ok) return false;
+    uint8_t *b1, *b3;
+    st.both(lane, b1, b3);  // the previous boxes have left both buffers
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float* da = h ? da1 : da0;
+    for (int j = 0; j < 8; ++j) {
+      const float* da = j < 4 ? da0 : da1;
+      const uint32_t a1[4] = {v1[j].x, v1[j].y, v1[j].z, v1[j].w};
+      const uint32_t a3[4] = {v3[j].x, v3[j].y, v3[j].z, v3[j].w};
+      uint32_t o1[4], o3[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int off = lane * 128 + (((4 * h + j) ^ (lane & 7)) << 4);
-        uint4* p1 = reinterpret_cast<uint4*>(b1 + off);
-        uint4* p3 = reinterpret_cast<uint4*>(b3 + off);
-        const uint4 w1 = *p1, w3 = *p3;
-        const uint32_t a1[4] = {w1.x, w1.y, w1.z, w1.w};
-        const uint32_t a3[4] = {w3.x, w3.y, w3.z, w3.w};
-        uint32_t o1[4], o3[4];
+      for (int q = 0; q < 4; ++q) {
+        float d1v[2], d3v[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float d1v[2], d3v[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float x1 = e ? bf16_hi(a1[q]) : bf16_lo(a1[q]);
-            const float x3 = e ? bf16_hi(a3[q]) : bf16_lo(a3[q]);
-            const float d = da[8 * j + 2 * q + e];
-            const float s = 1.0f / (1.0f + __expf(-x1));
-            d1v[e] = d * x3 * (s * (1.0f + x1 * (1.0f - s)));
-            d3v[e] = d * x1 * s;
-          }
-          o1[q] = pack_bf16x2(d1v[0], d1v[1]);
-          o3[q] = pack_bf16x2(d3v[0], d3v[1]);
+        for (int e = 0; e < 2; ++e) {
+          const float x1 = e ? bf16_hi(a1[q]) : bf16_lo(a1[q]);
+          const float x3 = e ? bf16_hi(a3[q]) : bf16_lo(a3[q]);
+          const float d = da[8 * (j & 3) + 2 * q + e];
+          const float s = 1.0f / (1.0f + __expf(-x1));
+          d1v[e] = d * x3 * (s * (1.0f + x1 * (1.0f - s)));
+          d3v[e] = d * x1 * s;
         }
-        *p1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-        *p3 = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+        o1[q] = pack_bf16x2(d1v[0], d1v[1]);
+        o3[q] = pack_bf16x2(d3v[0], d3v[1]);
       }
+      const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
+      *reinterpret_cast<uint4*>(b1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      *reinterpret_cast<uint4*>(b3 + off) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -276,7 +274,6 @@ __device__ __forceinline__ bool epi_dgrad2_tma(const GemmParams& p, const TileIn
     }
     st.n += 2;
   }
-  return true;
 }
 
 }  // namespace moe

@@ -18,8 +18,8 @@ struct SmemLayout {
   static constexpr int kOutOff = kRingBytes;
   static constexpr int kOutBytes = 4 * 8192;
   static constexpr int kBarOff = kOutOff + kOutBytes;
-  static constexpr int kNumBars = 3 * KindTraits<KIND>::kMaxStages + 9;  // full, empty, peer, tfull[2],
-                                                                        // tempty[2], drain, epilogue[4]
+  static constexpr int kNumBars = 3 * KindTraits<KIND>::kMaxStages + 5;  // full, empty, peer, tfull[2],
+                                                                        // tempty[2], drain
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
@@ -205,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty + b, PAIR ? 8 : 4);  // pairs: the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
-    for (int w = 0; w < 4; ++w) mbar_init(drain + 1 + w, 1);  // epilogue warps' TMA loads
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -485,19 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     Stager st{smem + SL::kOutOff + q * 8192, 0u};
-    uint32_t epi_phase = 0;  // phase of this warp's load barrier
     // pairs: the odd CTA's epilogue frees the even CTA's accumulator slot
     const uint32_t tempty_even = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
     for (int tile = tile_first; tile < ntiles; tile += tile_step) {
       const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
-      if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
-      tc_fence_after();
-      const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * kAccStride) + (static_cast<uint32_t>(q * 32) << 16);
       // this warp's 32 rows: a full block leaves through TMA boxes; a block
       // that crosses the end of the expert's rows uses masked per-thread stores
       const int row0 = ti.m0 + 32 * q;
       const bool full_rows = row0 + 32 <= ti.m_end;
       const bool any_rows = row0 < ti.m_end;
+      if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * kAccStride) + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (KIND == KIND_FFN1) {
         if (full_rows) epi_ffn1_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
         else if (any_rows) epi_ffn1(p, ti, tacc, r);
@@ -512,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // raw fp32 logits [T, bn]; the map's row extent T clips the tail
         epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
       } else if constexpr (KIND == KIND_DGRAD2) {
-        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1, drain + 1 + q, epi_phase, s_abort);
+        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0);
         else if (any_rows) epi_dgrad2(p, ti, tacc, r);
       } else if constexpr (KIND == KIND_DGRAD1) {
         if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
