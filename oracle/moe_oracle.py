@@ -43,7 +43,7 @@ import numpy as np
 
 __all__ = [
     "Precision", "EXACT", "CONTRACT", "bf16_rne", "router_logits", "softmax",
-    "sigmoid", "group_limit_mask", "topk_select", "route", "permute_plan",
+    "sigmoid", "group_limit_mask", "topk_select", "balanced_assignment", "route", "permute_plan",
     "permute_rows", "silu", "silu_grad", "swiglu_expert", "grouped_swiglu",
     "combine", "layer_fwd", "aux_loss", "router_backward", "layer_bwd",
     "expert_backward",
@@ -149,14 +149,26 @@ def group_limit_mask(z, n_groups, topk_groups):
     return out.reshape(T, E)
 
 
+def balanced_assignment(T, E, k):
+    """Force-balanced routing (throughput page, Table 11: every configuration
+    of the unified benchmark uses force-balanced routing; the page gives no
+    rule). Reading: slot i of token t goes to expert (t k + i) mod E, so the
+    T k assignments cycle through the experts and every expert receives
+    floor(T k / E) or one more; a token's k experts are distinct when k <= E."""
+    t = np.arange(T)[:, None]
+    i = np.arange(k)[None, :]
+    return (t * k + i) % E
+
+
 def route(x, w_r, k, score="softmax", expert_bias=None, logit_bias=None,
-          n_groups=1, topk_groups=1, gate_scale=1.0):
+          n_groups=1, topk_groups=1, gate_scale=1.0, force_balanced=False):
     """The router of the MoE layer.
 
     1. logits L = x w_r^T (+ logit_bias);
     2. scores: softmax over all E experts, or element-wise sigmoid;
     3. selection value z = scores (+ expert_bias, selection only), optionally
-       group-limited, then top-k;
+       group-limited, then top-k (force_balanced: the fixed assignment of
+       ``balanced_assignment`` instead of the top-k);
     4. gates g_i = gate_scale * score[e_i] / sum_j score[e_j] over the k
        selected experts (renormalised; for sigmoid the unbiased score).
 
@@ -171,7 +183,10 @@ def route(x, w_r, k, score="softmax", expert_bias=None, logit_bias=None,
         raise ValueError(score)
     z = s if expert_bias is None else s + np.asarray(expert_bias, np.float64)[None, :]
     z = group_limit_mask(z, n_groups, topk_groups)
-    idx = topk_select(z, k)
+    if force_balanced:
+        idx = balanced_assignment(L.shape[0], L.shape[1], k)
+    else:
+        idx = topk_select(z, k)
     sel = np.take_along_axis(s, idx, axis=1)
     gate = gate_scale * sel / sel.sum(axis=1, keepdims=True)
     return {"logits": L, "scores": s, "z": z, "topk_idx": idx, "topk_gate": gate}
@@ -286,7 +301,7 @@ def combine(y_perm, row_id_map, topk_gate, shared=None):
 
 def layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None,
               logit_bias=None, n_groups=1, topk_groups=1, gate_scale=1.0,
-              Ws=None, prec=CONTRACT, tokens=None):
+              Ws=None, prec=CONTRACT, tokens=None, force_balanced=False):
     """Forward of the whole layer.
 
     ``tokens`` (optional) restricts the expert and combine stages to a token
@@ -296,7 +311,7 @@ def layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None,
     """
     x = np.asarray(x, np.float64)
     T, H = x.shape
-    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale)
+    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
     E = np.asarray(w_r).shape[0]
     counts, offsets, row = permute_plan(rt["topk_idx"], E)
     get = _weights_getter(W1, W3, W2)
@@ -394,7 +409,8 @@ def expert_backward(xr, h1, h3, a, dyr, W1e, W3e, W2e, prec=CONTRACT):
 
 def layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None,
               logit_bias=None, n_groups=1, topk_groups=1, gate_scale=1.0,
-              aux_coeff=0.0, Ws=None, prec=CONTRACT, experts=None, tokens=None):
+              aux_coeff=0.0, Ws=None, prec=CONTRACT, experts=None, tokens=None,
+              force_balanced=False):
     """Forward and backward of the layer for the loss <dO, y> + L_aux.
 
     Returns a dict with the forward results plus dx [T,H], dW_r [E,H],
@@ -407,7 +423,7 @@ def layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None,
     T, H = x.shape
     w_r = np.asarray(w_r, np.float64)
     E = w_r.shape[0]
-    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale)
+    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
     idx, gate = rt["topk_idx"], rt["topk_gate"]
     counts, offsets, row = permute_plan(idx, E)
     get = _weights_getter(W1, W3, W2)

@@ -85,6 +85,11 @@ def _router_bwd_no_inner(logits, topk_idx, topk_gate, dgate, score="softmax", ga
     return dL
 
 
+def _balanced_by_token(T, E, k):
+    t = np.arange(T)[:, None]
+    return (t + np.arange(k)[None, :]) % E  # the token's slots start at t, not at t k
+
+
 MUTATIONS = [
     ("route", _route_unnormalised, [P.test_gates_sum_and_closed_form]),
     ("topk_select", _topk_high_index_wins, [P.test_topk_tie_rule]),
@@ -93,6 +98,7 @@ MUTATIONS = [
     ("aux_loss", _aux_without_E, [P.test_aux_loss_uniform_balanced_equals_alpha]),
     ("group_limit_mask", _group_limit_top1, [P.test_group_limit_against_enumeration]),
     ("swiglu_expert", _swiglu_gate_on_w3, [P.test_single_expert_is_textbook_swiglu_mlp]),
+    ("balanced_assignment", _balanced_by_token, [P.test_force_balanced_assignment]),
     ("router_backward", _router_bwd_no_inner,
      [lambda: P.test_backward_against_central_differences("softmax_aux")]),
 ]

@@ -162,6 +162,36 @@ def test_gates_sum_and_closed_form():
     np.testing.assert_allclose(rs["topk_gate"].sum(1), 2.5, rtol=0, atol=1e-14)
 
 
+def test_force_balanced_assignment():
+    """Force-balanced routing: the T k assignments cycle through the experts
+    (counted here with a running counter, one assignment at a time), every
+    expert gets floor(T k / E) or one more, a token's experts are distinct, and
+    the gates are the renormalised scores of the assigned experts."""
+    rng = np.random.default_rng(21)
+    for T, E, k in ((37, 8, 3), (64, 16, 4), (5, 4, 4), (9, 7, 1)):
+        idx = O.balanced_assignment(T, E, k)
+        c = 0
+        for t in range(T):
+            for i in range(k):
+                assert idx[t, i] == c % E
+                c += 1
+        counts = np.bincount(idx.ravel(), minlength=E)
+        assert counts.min() == (T * k) // E and counts.max() <= (T * k + E - 1) // E
+        assert all(len(set(row)) == k for row in idx.tolist())
+        x = rng.standard_normal((T, 8)); w = rng.standard_normal((E, 8)) / 3
+        rt = O.route(x, w, k, force_balanced=True)
+        assert np.array_equal(rt["topk_idx"], idx)
+        Lsel = np.take_along_axis(rt["logits"], idx, 1)
+        q = np.exp(Lsel - Lsel.max(1, keepdims=True)); q /= q.sum(1, keepdims=True)
+        np.testing.assert_allclose(rt["topk_gate"], q, rtol=1e-13, atol=0)
+        rs = O.route(x, w, k, "sigmoid", gate_scale=2.5, force_balanced=True)
+        ssel = 1.0 / (1.0 + np.exp(-np.take_along_axis(rs["logits"], idx, 1)))
+        np.testing.assert_allclose(rs["topk_gate"], 2.5 * ssel / ssel.sum(1, keepdims=True), rtol=1e-13, atol=0)
+        if (T * k) % E == 0:
+            # every f_e = 1/E, and the mean probabilities sum to one: L_aux = alpha
+            assert abs(O.aux_loss(rt["scores"], counts, k, 0.01) - 0.01) < 1e-15
+
+
 def test_router_logits_against_python_loop():
     rng = np.random.default_rng(5)
     x = rng.standard_normal((3, 5)); w = rng.standard_normal((4, 5)); b = rng.standard_normal(4)
@@ -373,15 +403,18 @@ def _margins_ok(x, w_r, k, kw, step):
     return np.min(zz[:, k - 1] - zz[:, k]) > 100 * step
 
 
-@pytest.mark.parametrize("variant", ["softmax_aux", "sigmoid_groups_shared"])
+@pytest.mark.parametrize("variant", ["softmax_aux", "sigmoid_groups_shared", "force_balanced_aux"])
 def test_backward_against_central_differences(variant):
-    rng = np.random.default_rng(14 if variant == "softmax_aux" else 15)
+    rng = np.random.default_rng({"softmax_aux": 14, "sigmoid_groups_shared": 15}.get(variant, 16))
     T, H, E, k, F = 8, 6, 4, 2, 5
     kw = {}
     aux = 0.0
     Ws = None
     if variant == "softmax_aux":
         aux = 1e-1
+    elif variant == "force_balanced_aux":
+        aux = 1e-1
+        kw = dict(force_balanced=True)
     else:
         kw = dict(score="sigmoid", expert_bias=rng.uniform(-.1, .1, E), n_groups=2,
                   topk_groups=1, gate_scale=2.5)
@@ -430,7 +463,7 @@ def test_backward_against_central_differences(variant):
         close(g["dWs1"], fd(Ws[0], lambda: L(x, w_r, W1, W3, W2)))
         close(g["dWs2"], fd(Ws[2], lambda: L(x, w_r, W1, W3, W2)))
     if aux:
-        out = O.layer_fwd(x, w_r, W1, W3, W2, k, prec=O.EXACT)
+        out = O.layer_fwd(x, w_r, W1, W3, W2, k, prec=O.EXACT, **kw)
         assert abs(g["aux_loss"] - O.aux_loss(out["scores"], out["counts"], k, aux)) < 1e-15
 
 
