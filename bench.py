@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay timing")
+    ap.add_argument("--force-balanced", action="store_true", help="force-balanced routing (cyclic assignment)")
     return ap.parse_args()
 
 
@@ -177,7 +179,7 @@ def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024):
     w_r = f64(d["router_w"])
     lb = None if d["logit_bias"] is None else f64(d["logit_bias"])
     rt = O.route(x, w_r, ls.k, ls.score, None if d["expert_bias"] is None else f64(d["expert_bias"]), lb,
-                 ls.n_groups, ls.topk_groups, ls.gate_scale)
+                 ls.n_groups, ls.topk_groups, ls.gate_scale, force_balanced=ls.force_balanced)
     rng = np.random.default_rng(seed)
     experts = sorted(rng.choice(ls.E, size=min(n_experts, ls.E), replace=False).tolist())
     data = []
@@ -193,7 +195,8 @@ def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024):
     training = ls.aux_coeff > 0 or d["dO"] is not None
 
     def fn():
-        O.route(xs, w_r, ls.k, ls.score, None, lb, ls.n_groups, ls.topk_groups, ls.gate_scale)
+        O.route(xs, w_r, ls.k, ls.score, None, lb, ls.n_groups, ls.topk_groups, ls.gate_scale,
+                force_balanced=ls.force_balanced)
         for xr, W, g, dO in data:
             h1, h3, a, out = O.swiglu_expert(xr, *W)
             if training and dO is not None:
@@ -272,7 +275,7 @@ def workload_config(ls):
     return {"workload": f"{ls.name}: MoE layer T={ls.T} H={ls.H} E={ls.E} k={ls.k} F={ls.F}"
                         + (f" Fs={ls.F_shared}" if ls.F_shared else "")
                         + f" {ls.score} top-{ls.k}" + (f" groups {ls.n_groups}/{ls.topk_groups}" if ls.n_groups > 1 else "")
-                        + (f" zipf {ls.skew}" if ls.skew else " balanced")
+                        + (" force-balanced" if ls.force_balanced else (f" zipf {ls.skew}" if ls.skew else " balanced"))
                         + (" fwd+bwd" if ls.aux_coeff > 0 else " fwd"),
             "tokens": ls.T, "hidden": ls.H, "experts": ls.E, "top_k": ls.k, "ffn": ls.F,
             "l2": (f"inputs larger than the 129 MB L2 (x {2 * ls.T * ls.H / 1e6:.0f} MB, expert weights "
@@ -350,6 +353,30 @@ def run_ours(args, ls, rank, world, local_rank):
     torch.cuda.synchronize()
     ms_fwd = f0.elapsed_time(f1) / args.steps
     ms_fwd = max_over_ranks(ms_fwd, world, dev)
+
+    # ---------------- the same step captured once as a CUDA graph and replayed
+    # (device-side offsets: no host synchronisation inside a step)
+    graph = None
+    if not args.no_graph:
+        gs = torch.cuda.Stream(device=dev)
+        gs.wait_stream(torch.cuda.current_stream())
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gs):
+            step()
+        torch.cuda.current_stream().wait_stream(gs)
+        for _ in range(2):
+            cg.replay()
+        barrier()
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0.record()
+        for _ in range(args.steps):
+            cg.replay()
+        q1.record()
+        torch.cuda.synchronize()
+        assert ops.device_status(ws) == 0
+        ms_graph = max_over_ranks(q0.elapsed_time(q1) / args.steps, world, dev)
+        graph = {"value": round(job_throughput(layer_flops(ls, training), ms_graph, world), 2), "unit": "TFLOPS",
+                 "ms_per_step": round(ms_graph, 4)}
 
     # ---------------- per-stage table and roofline of the dominant kernel
     peaks = load_peaks()
@@ -460,7 +487,7 @@ def run_ours(args, ls, rank, world, local_rank):
             "tokens_per_s": round(world * ls.T / (ms * 1e-3), 1),
             "fwd": {"value": round(fwd_value, 2), "unit": "TFLOPS", "ms_per_step": round(ms_fwd, 4),
                     "tokens_per_s": round(world * ls.T / (ms_fwd * 1e-3), 1)},
-            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "graph": graph, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -499,7 +526,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     from route_permute_grouped_gb300 import synth
-    ls = synth.shape(args.workload)
+    ls = synth.shape(args.workload, force_balanced=bool(getattr(args, "force_balanced", False)))
     if args.impl == "reference":
         if rank != 0:
             return

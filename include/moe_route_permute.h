@@ -64,7 +64,14 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
  *                alpha * E * sum_e (c_e / (T k)) * mean_t p[t,e] (training);
  *   out_fp32     y (forward) and dx (backward) written as fp32 instead of bf16;
  *   inter_fp32   expert outputs y_perm and the shared-expert output kept in
- *                fp32 instead of bf16. */
+ *                fp32 instead of bf16;
+ *   force_balanced  force-balanced routing (throughput page, Table 11, where
+ *                every benchmark configuration uses it): slot i of token t goes
+ *                to expert (t k + i) mod E instead of the top-k, so each expert
+ *                receives floor(T k / E) or one more rows; the scores, gates
+ *                (renormalised over the assigned experts), aux statistics and
+ *                the backward are computed as usual; the group limit and the
+ *                expert bias do not apply. 0 or 1. */
 typedef struct {
   int T, H, E, k, F;
   int F_shared;      /* 0 = no shared expert */
@@ -74,6 +81,7 @@ typedef struct {
   float aux_coeff;
   int out_fp32;
   int inter_fp32;
+  int force_balanced;
 } moe_config;
 
 /* Tensors the training forward keeps for the backward (all caller-owned).

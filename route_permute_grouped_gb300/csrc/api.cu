@@ -215,6 +215,7 @@ static int check_cfg(const moe_config* c) {
   if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (!(c->gate_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
   if (c->n_groups < 1 || c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+  if (c->force_balanced != 0 && c->force_balanced != 1) return MOE_ERR_INVALID_ARG;
   if (c->E % c->n_groups != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->n_groups > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->n_groups > 1 && c->topk_groups < c->n_groups && c->k > c->topk_groups * (c->E / c->n_groups))

@@ -57,7 +57,7 @@ enum SelMode : int { SEL_SOFTMAX_LOGIT = 0, SEL_SOFTMAX_BIAS = 1, SEL_SIGMOID = 
 // lane drops its head. NaN values of z are taken as -inf.
 template <int NJ, int MODE>
 __device__ __forceinline__ void select_token(const float (&L)[NJ], int t, bool valid, int lane, int E, int k,
-                                             int n_groups, int topk_groups, float gate_scale,
+                                             bool force, int n_groups, int topk_groups, float gate_scale,
                                              const float* __restrict__ expert_bias, int32_t* __restrict__ topk_idx,
                                              float* __restrict__ topk_gate, float* __restrict__ logits_out,
                                              float* p_row) {
@@ -112,8 +112,21 @@ __device__ __forceinline__ void select_token(const float (&L)[NJ], int t, bool v
       if (e < E) p_row[e] = sc[j];  // 0 for tokens past T
     }
   }
+  int my_e = 0;
+  float my_sc = 0.0f;
+  if (force) {
+    // force-balanced routing: slot `lane` takes expert (t k + lane) mod E; its
+    // score comes from the lane that holds that expert
+    const int ei = static_cast<int>((static_cast<long long>(t) * k + lane) % E);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const float v = __shfl_sync(0xffffffffu, kZL ? L[j] : sc[j], ei & 31);
+      if ((ei >> 5) == j) my_sc = v;
+    }
+    my_e = ei;
+  }
   // group-limited selection
-  if (n_groups > 1 && topk_groups < n_groups) {
+  if (!force && n_groups > 1 && topk_groups < n_groups) {
     const int gsz = E / n_groups;
     uint32_t keep = 0u;
     float gscore[32];
@@ -179,10 +192,8 @@ __device__ __forceinline__ void select_token(const float (&L)[NJ], int t, bool v
     }
   }
   // k rounds; lane i keeps slot i
-  int my_e = 0;
-  float my_sc = 0.0f;
 #pragma unroll 1
-  for (int i = 0; i < k; ++i) {
+  for (int i = 0; i < (force ? 0 : k); ++i) {
     const float m = warp_max(cz[0]);
     const int e = static_cast<int>(warp_min_u32(cz[0] == m ? static_cast<uint32_t>(ce[0]) : 0xffffffffu));
     const float sel = kZL ? m : __shfl_sync(0xffffffffu, cv[0], e & 31);
@@ -204,7 +215,7 @@ __device__ __forceinline__ void select_token(const float (&L)[NJ], int t, bool v
   // gates over the k slots (lanes 0..k-1)
   float w;
   if (kZL) {
-    const float top = __shfl_sync(0xffffffffu, my_sc, 0);
+    const float top = warp_max(lane < k ? my_sc : -INFINITY);
     w = lane < k ? __expf(my_sc - top) : 0.0f;
   } else {
     w = lane < k ? my_sc : 0.0f;
@@ -220,7 +231,8 @@ __device__ __forceinline__ void select_token(const float (&L)[NJ], int t, bool v
 // slice, loading all four tokens' logits before working on the first.
 template <int NJ, int MODE>
 __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(
-    const float* __restrict__ raw, int ld, int T, int E, int k, int n_groups, int topk_groups, float gate_scale,
+    const float* __restrict__ raw, int ld, int T, int E, int k, int force, int n_groups, int topk_groups,
+    float gate_scale,
     const float* __restrict__ expert_bias, const float* __restrict__ logit_bias, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_gate, float* __restrict__ logits_out, float* __restrict__ aux_partials) {
   extern __shared__ float s_p[];  // [kSel][E] softmax values (aux only)
@@ -246,8 +258,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(
   for (int i = 0; i < kTokPerWarp; ++i) {
     const int r = warp * kTokPerWarp + i;
     const int t = blockIdx.x * kSel + r;
-    select_token<NJ, MODE>(Ls[i], t, t < T, lane, E, k, n_groups, topk_groups, gate_scale, expert_bias, topk_idx,
-                           topk_gate, logits_out, want_aux ? s_p + r * E : nullptr);
+    select_token<NJ, MODE>(Ls[i], t, t < T, lane, E, k, force != 0, n_groups, topk_groups, gate_scale, expert_bias,
+                           topk_idx, topk_gate, logits_out, want_aux ? s_p + r * E : nullptr);
   }
   if (want_aux) {
     __syncthreads();
@@ -260,8 +272,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(
 }
 
 template <int MODE>
-using SelKernel = void (*)(const float*, int, int, int, int, int, int, float, const float*, const float*, int32_t*,
-                           float*, float*, float*);
+using SelKernel = void (*)(const float*, int, int, int, int, int, int, int, float, const float*, const float*,
+                           int32_t*, float*, float*, float*);
 
 template <int MODE>
 static SelKernel<MODE> pick_select_kernel(int nj) {
@@ -288,16 +300,16 @@ cudaError_t launch_router_select(const moe_config& c, const float* raw, int ld, 
   const bool softmax = c.score == MOE_SCORE_SOFTMAX;
   if (softmax && expert_bias == nullptr) {
     pick_select_kernel<SEL_SOFTMAX_LOGIT>(nj)<<<blocks, kSelWarps * 32, smem, st>>>(
-        raw, ld, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias, topk_idx, topk_gate,
-        logits_out, aux_partials);
+        raw, ld, c.T, c.E, c.k, c.force_balanced, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias,
+        topk_idx, topk_gate, logits_out, aux_partials);
   } else if (softmax) {
     pick_select_kernel<SEL_SOFTMAX_BIAS>(nj)<<<blocks, kSelWarps * 32, smem, st>>>(
-        raw, ld, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias, topk_idx, topk_gate,
-        logits_out, aux_partials);
+        raw, ld, c.T, c.E, c.k, c.force_balanced, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias,
+        topk_idx, topk_gate, logits_out, aux_partials);
   } else {
     pick_select_kernel<SEL_SIGMOID>(nj)<<<blocks, kSelWarps * 32, smem, st>>>(
-        raw, ld, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias, topk_idx, topk_gate,
-        logits_out, aux_partials);
+        raw, ld, c.T, c.E, c.k, c.force_balanced, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias,
+        topk_idx, topk_gate, logits_out, aux_partials);
   }
   return cudaGetLastError();
 }

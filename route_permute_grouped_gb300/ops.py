@@ -30,7 +30,7 @@ class MoeError(RuntimeError):
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", c_int), ("H", c_int), ("E", c_int), ("k", c_int), ("F", c_int), ("F_shared", c_int),
                 ("score", c_int), ("n_groups", c_int), ("topk_groups", c_int), ("gate_scale", c_float),
-                ("aux_coeff", c_float), ("out_fp32", c_int), ("inter_fp32", c_int)]
+                ("aux_coeff", c_float), ("out_fp32", c_int), ("inter_fp32", c_int), ("force_balanced", c_int)]
 
 
 class MoeFwdSaved(ctypes.Structure):
@@ -131,15 +131,15 @@ def _check(st, where):
 
 
 def make_config(T, H, E, k, F, F_shared=0, score="softmax", n_groups=1, topk_groups=1, gate_scale=1.0,
-                aux_coeff=0.0, out_fp32=False, inter_fp32=False) -> MoeConfig:
+                aux_coeff=0.0, out_fp32=False, inter_fp32=False, force_balanced=False) -> MoeConfig:
     return MoeConfig(T, H, E, k, F, F_shared, SCORE[score] if isinstance(score, str) else score, n_groups,
-                     topk_groups, gate_scale, aux_coeff, int(out_fp32), int(inter_fp32))
+                     topk_groups, gate_scale, aux_coeff, int(out_fp32), int(inter_fp32), int(force_balanced))
 
 
 def config_from_shape(ls, **over) -> MoeConfig:
     d = dict(T=ls.T, H=ls.H, E=ls.E, k=ls.k, F=ls.F, F_shared=ls.F_shared, score=ls.score, n_groups=ls.n_groups,
              topk_groups=ls.topk_groups, gate_scale=ls.gate_scale, aux_coeff=ls.aux_coeff, out_fp32=ls.out_fp32,
-             inter_fp32=ls.inter_fp32)
+             inter_fp32=ls.inter_fp32, force_balanced=getattr(ls, "force_balanced", False))
     d.update(over)
     return make_config(**d)
 

@@ -43,6 +43,7 @@ class LayerShape:
     w_std: float | None = None      # expert weight std (None: 1/sqrt(fan_in))
     inter_fp32: bool = False        # expert outputs / shared output kept in fp32
     out_fp32: bool = False          # layer output y (and dx) in fp32
+    force_balanced: bool = False    # force-balanced routing (cyclic slot assignment)
     extra: dict = field(default_factory=dict)
 
     def as_dict(self):
