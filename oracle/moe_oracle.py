@@ -410,8 +410,16 @@ def expert_backward(xr, h1, h3, a, dyr, W1e, W3e, W2e, prec=CONTRACT):
 def layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None,
               logit_bias=None, n_groups=1, topk_groups=1, gate_scale=1.0,
               aux_coeff=0.0, Ws=None, prec=CONTRACT, experts=None, tokens=None,
-              force_balanced=False):
+              force_balanced=False, recompute=False):
     """Forward and backward of the layer for the loss <dO, y> + L_aux.
+
+    ``recompute`` is the memory-saving variant (captions page, Fig. 7 and
+    Table 4 "SwiGLU recompute"): the forward keeps neither a nor y_perm; the
+    backward recomputes a = SiLU(h1) h3 from the stored pre-activations (and
+    stores it per prec.a) and takes the gate gradient from the dgrad of the
+    down projection, dg = <da, a> / g with da = dy W2^T and dy = g dO, which
+    equals <dO, y_perm> in exact arithmetic (0 where g = 0, whose dg carries
+    no weight in the router backward).
 
     Returns a dict with the forward results plus dx [T,H], dW_r [E,H],
     dW1/dW3 [E,H,F], dW2 [E,F,H], aux_loss (and dWs1/dWs3/dWs2 with a shared
@@ -451,10 +459,16 @@ def layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None,
         W1e, W3e, W2e = get(e)
         h1, h3, a, out = swiglu_expert(x[tt], W1e, W3e, W2e, prec)
         out = prec.r("y_perm", out)
-        dgate[tt, ii] = np.sum(dO[tt] * out, axis=1)
-        dyr = prec.r("dy_perm", gate[tt, ii][:, None] * dO[tt])
-        dxr, g1, g3, g2 = expert_backward(x[tt], prec.r("h13", h1), prec.r("h13", h3), a,
-                                          dyr, W1e, W3e, W2e, prec)
+        h1s, h3s = prec.r("h13", h1), prec.r("h13", h3)
+        gsel = gate[tt, ii]
+        dyr = prec.r("dy_perm", gsel[:, None] * dO[tt])
+        if recompute:
+            a = prec.r("a", silu(h1s) * h3s)
+            dot = np.sum((dyr @ W2e.T) * a, axis=1)
+            dgate[tt, ii] = np.where(gsel != 0, dot / np.where(gsel != 0, gsel, 1.0), 0.0)
+        else:
+            dgate[tt, ii] = np.sum(dO[tt] * out, axis=1)
+        dxr, g1, g3, g2 = expert_backward(x[tt], h1s, h3s, a, dyr, W1e, W3e, W2e, prec)
         np.add.at(dx, tt, dxr)
         if e in exp_set:
             dW1[e] += g1

@@ -192,6 +192,27 @@ def test_force_balanced_assignment():
             assert abs(O.aux_loss(rt["scores"], counts, k, 0.01) - 0.01) < 1e-15
 
 
+def test_recompute_variant_equals_standard_in_exact_arithmetic():
+    """The memory-saving backward (a recomputed from h1, h3; gate gradient
+    <da, a> / g instead of <dO, y_perm>) is the same function as the standard
+    backward when nothing is rounded."""
+    rng = np.random.default_rng(22)
+    T, H, E, k, F = 40, 12, 6, 3, 10
+    x = rng.standard_normal((T, H)); w_r = rng.standard_normal((E, H)) / 2
+    W1, W3, W2 = _experts(rng, E, H, F)
+    dO = rng.standard_normal((T, H))
+    for kw in (dict(aux_coeff=0.05), dict(score="sigmoid", gate_scale=2.5, n_groups=3, topk_groups=2),
+               dict(force_balanced=True, aux_coeff=0.05)):
+        a = O.layer_bwd(x, w_r, W1, W3, W2, dO, k, prec=O.EXACT, **kw)
+        b = O.layer_bwd(x, w_r, W1, W3, W2, dO, k, prec=O.EXACT, recompute=True, **kw)
+        np.testing.assert_allclose(b["dgate"], a["dgate"], rtol=1e-11, atol=1e-12)
+        for key in ("dx", "dW_r"):
+            np.testing.assert_allclose(b[key], a[key], rtol=1e-11, atol=1e-12)
+        for key in ("dW1", "dW3", "dW2"):
+            for e in range(E):
+                np.testing.assert_allclose(b[key][e], a[key][e], rtol=1e-11, atol=1e-12)
+
+
 def test_router_logits_against_python_loop():
     rng = np.random.default_rng(5)
     x = rng.standard_normal((3, 5)); w = rng.standard_normal((4, 5)); b = rng.standard_normal(4)
