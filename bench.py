@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay timing")
     ap.add_argument("--force-balanced", action="store_true", help="force-balanced routing (cyclic assignment)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="memory-saving training step (a and y_perm not kept; recomputed in the backward)")
     return ap.parse_args()
 
 
@@ -84,10 +86,12 @@ def stage_model(ls, training):
         m["shared_gate_up"] = (2 * T * H * 2 * Fs, 2 * T * H + 4 * H * Fs + 2 * T * Fs)
         m["shared_down"] = (2 * T * Fs * H, 2 * T * Fs + 2 * Fs * H + yb * T * H)
     if training:
+        rec = bool(ls.extra.get("recompute", False))  # memory-saving backward: no y_perm read, a re-written
         m.update({
-            "combine_bwd": (0, 2 * T * H + yb * R * H + 2 * R * H + 8 * T * k),
+            "combine_bwd": (0, 2 * T * H + (0 if rec else yb * R * H) + 2 * R * H + 8 * T * k),
             "router_bwd_elem": (0, 4 * T * E + 12 * T * k + 2 * T * 2 * Ep),
-            "dgrad_down_swiglu": (2 * R * H * F, 2 * R * H + 2 * E * F * H + 4 * R * F + 4 * R * F),
+            "dgrad_down_swiglu": (2 * R * H * F, 2 * R * H + 2 * E * F * H + 4 * R * F + 4 * R * F
+                                  + (2 * R * F if rec else 0)),
             "wgrad_down": (2 * R * F * H, 2 * R * F + 2 * R * H + 4 * E * F * H),
             "dgrad_gate_up": (2 * R * 2 * F * H, 4 * R * F + 4 * E * H * F + 2 * R * H),
             "wgrad_gate_up": (2 * R * H * 2 * F, 2 * R * H + 4 * R * F + 8 * E * H * F),
@@ -278,6 +282,7 @@ def workload_config(ls):
                         + (" force-balanced" if ls.force_balanced else (f" zipf {ls.skew}" if ls.skew else " balanced"))
                         + (" fwd+bwd" if ls.aux_coeff > 0 else " fwd"),
             "tokens": ls.T, "hidden": ls.H, "experts": ls.E, "top_k": ls.k, "ffn": ls.F,
+            "memory_saving": bool(ls.extra.get("recompute", False)),
             "l2": (f"inputs larger than the 129 MB L2 (x {2 * ls.T * ls.H / 1e6:.0f} MB, expert weights "
                    f"{6 * ls.E * ls.H * ls.F / 1e9:.2f} GB); no flush")}
 
@@ -295,7 +300,7 @@ def run_ours(args, ls, rank, world, local_rank):
     d = synth.make_layer(ls, seed=args.seed + rank, device=dev, training=training)
     cfg = ops.config_from_shape(ls)
     ws = ops.workspace(cfg, training, dev)
-    saved = ops.alloc_saved(cfg, dev) if training else None
+    saved = ops.alloc_saved(cfg, dev, recompute=args.recompute) if training else None
     grads = ops.alloc_grads(cfg, dev) if training else None
     y = torch.empty((ls.T, ls.H), dtype=torch.bfloat16, device=dev)
     Ws = (d["Ws1"], d["Ws3"], d["Ws2"]) if ls.F_shared else None
@@ -527,6 +532,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     from route_permute_grouped_gb300 import synth
     ls = synth.shape(args.workload, force_balanced=bool(getattr(args, "force_balanced", False)))
+    if getattr(args, "recompute", False):
+        ls.extra["recompute"] = True
     if args.impl == "reference":
         if rank != 0:
             return

@@ -91,7 +91,14 @@ typedef struct {
  * pre-activation x W1 in columns [0,F), up projection x W3 in [F,2F));
  * a [R,F] bf16 (SiLU(h1)*h3); y_perm [R,H] bf16 (fp32 if inter_fp32);
  * aux_partials [4*ceil(T/128), E] fp32 (column sums of the full softmax over
- * consecutive 32-token slices; only when aux_coeff != 0, else may be NULL). */
+ * consecutive 32-token slices; only when aux_coeff != 0, else may be NULL).
+ * Memory-saving mode (captions page, Fig. 7 memory-efficient permutation and
+ * Table 4 SwiGLU recompute): a and y_perm both NULL (one NULL alone is
+ * MOE_ERR_INVALID_ARG). The forward then keeps them in the workspace only; the
+ * backward, given the same NULLs, recomputes a = bf16(SiLU(h1) h3) from h13 in
+ * the epilogue of the down-projection dgrad and takes the gate gradient there
+ * as <da, a> / g (da = dy_perm W2^T, dy_perm = g dO; 0 where g = 0), which
+ * equals <dO, y_perm> in exact arithmetic. Saves 2 R (F + H) bytes (bf16). */
 typedef struct {
   int32_t* topk_idx;
   float* topk_gate;
@@ -190,9 +197,10 @@ int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32
 /* Whole layer forward = router -> permute -> grouped SwiGLU -> (shared
  * expert) -> combine. Ws1, Ws3 [H,Fs], Ws2 [Fs,H] bf16 when F_shared > 0
  * (the shared expert processes every token and is added ungated).
- * saved != NULL (training): every field of *saved must be set and receives
- * the tensors for moe_layer_bwd; saved == NULL (inference): intermediates live
- * in the workspace. */
+ * saved != NULL (training): every field of *saved must be set (except a and
+ * y_perm together, the memory-saving mode, and aux_partials when aux_coeff is
+ * 0) and receives the tensors for moe_layer_bwd; saved == NULL (inference):
+ * intermediates live in the workspace. */
 int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
                   const float* expert_bias, const float* logit_bias,
                   const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
@@ -204,7 +212,9 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
  * Outputs: dx [T,H] (bf16, fp32 if out_fp32); dW_router [E,H], dW1, dW3
  * [E,H,F], dW2 [E,F,H] fp32 (overwritten, zero for experts with no tokens);
  * aux_loss_out (1 fp32, may be NULL; written when aux_coeff != 0). Supported
- * for F_shared == 0. */
+ * for F_shared == 0. With saved->a and saved->y_perm NULL it runs the
+ * memory-saving backward (see moe_fwd_saved); the workspace must be the
+ * training size either way. */
 int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x,
                   const moe_bf16* router_w, const moe_bf16* W1, const moe_bf16* W3,
                   const moe_bf16* W2, const moe_fwd_saved* saved,

@@ -151,7 +151,7 @@ struct WsLayout {
   // forward intermediates (inference, or standalone grouped FFN without a_save)
   size_t logits_raw, topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
   // backward
-  size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part;
+  size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
   size_t total;
 };
 
@@ -190,6 +190,7 @@ static WsLayout ws_layout(const moe_config& c, bool training) {
     const size_t Ep = padded_experts(c.E);
     L.dy_perm = take(2 * R * H);
     L.dgate = take(4 * T * k);
+    L.dg_part = take(4 * R * ((F + 255) / 256));  // memory-saving backward: gate-gradient partials
     L.dh13 = take(2 * R * 2 * F);
     L.dx_perm = take(2 * R * H);
     L.dL_hl = take(2 * T * 2 * Ep);
@@ -473,15 +474,16 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
   void* yp;
   if (saved != nullptr) {
     if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
-        !saved->offsets || !saved->x_perm || !saved->h13 || !saved->a || !saved->y_perm)
+        !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
       return MOE_ERR_INVALID_ARG;
     if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
     idx = saved->topk_idx; gate = saved->topk_gate; logits = saved->logits; rows = saved->row_id_map;
     counts = saved->counts; offs = saved->offsets;
     xp = reinterpret_cast<__nv_bfloat16*>(saved->x_perm);
     h13 = reinterpret_cast<__nv_bfloat16*>(saved->h13);
-    a = reinterpret_cast<__nv_bfloat16*>(saved->a);
-    yp = saved->y_perm;
+    // memory-saving mode (a and y_perm NULL): both stay in the workspace
+    a = saved->a ? reinterpret_cast<__nv_bfloat16*>(saved->a) : at<__nv_bfloat16>(ws, L.a);
+    yp = saved->y_perm ? saved->y_perm : at<void>(ws, L.y_perm);
     aux = c.aux_coeff != 0.0f ? saved->aux_partials : nullptr;
   } else {
     idx = at<int32_t>(ws, L.topk_idx); gate = at<float>(ws, L.topk_gate); rows = at<int32_t>(ws, L.row_id_map);
@@ -520,9 +522,11 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
   if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
     return MOE_ERR_INVALID_ARG;
   if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
-      !saved->offsets || !saved->x_perm || !saved->h13 || !saved->a || !saved->y_perm)
+      !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
     return MOE_ERR_INVALID_ARG;
   if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+  // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
+  const bool recompute = saved->a == nullptr;
   const WsLayout L = ws_layout(c, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -538,15 +542,35 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
   float* dwr_part = at<float>(ws, L.dwr_part);
 
   prof_mark(s, STAGE_BEGIN);
-  // 1. combine backward
+  // 1. combine backward (memory-saving: dy_perm only)
   MOE_CUDA(launch_combine_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), saved->y_perm, saved->row_id_map,
                               saved->topk_gate, dy_perm, dgate, s));
   stage_done(s, STAGE_COMBINE_BWD, 1);
+  const int n_part = (c.F + 255) / 256;
+  float* dg_part = at<float>(ws, L.dg_part);
+  __nv_bfloat16* a_used = recompute ? at<__nv_bfloat16>(ws, L.a) : reinterpret_cast<__nv_bfloat16*>(saved->a);
+  if (recompute) {
+    // 3'. da = dy_perm W2_e^T: SwiGLU backward -> dh13, recomputed a -> workspace,
+    //     gate-gradient partials <da, a> per row and 256-column tile
+    GemmParams p = base_params(c, st);
+    p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
+    p.n_tiles = n_part; p.kb_total = c.H / kBK;
+    p.out0 = dh13; p.in_aux = saved->h13; p.out1 = a_used; p.dg_part = dg_part; p.n_part = n_part;
+    CUtensorMap ma, mb;
+    MOE_MAP(&ma, dy_perm, c.H, R, 2ull * c.H, 64, 128);
+    MOE_MAP(&mb, W2, c.H, static_cast<uint64_t>(c.E) * c.F, 2ull * c.H, 64, 128);  // CTA pairs: 128 rows each
+    CUtensorMap od, oa;
+    if (!make_map_store(&od, dh13, 2ull * c.F, R, false) || !make_map_store(&oa, a_used, c.F, R, false))
+      return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_DGRAD2R, p, ma, mb, mb, num_sms(), s, &od, &oa));
+    stage_done(s, STAGE_DGRAD2, 1);
+  }
   // 2. router backward (element-wise): dL as bf16 hi/lo
-  MOE_CUDA(launch_router_bwd(c, saved->logits, saved->topk_idx, saved->topk_gate, dgate, saved->counts, Ep, dL_hl, s));
+  MOE_CUDA(launch_router_bwd(c, saved->logits, saved->topk_idx, saved->topk_gate, dgate, recompute ? dg_part : nullptr,
+                             n_part, saved->row_id_map, saved->counts, Ep, dL_hl, s));
   stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
-  {
+  if (!recompute) {
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
     p.n_tiles = (c.F + 255) / 256; p.kb_total = c.H / kBK;
@@ -567,7 +591,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     p.m_tiles_fixed = (c.F + 255) / 256; p.n_tiles = (c.H + 255) / 256;  // CTA-pair tiles of 256 rows
     p.out0 = dW2;
     CUtensorMap ma, mb;
-    MOE_MAP(&ma, saved->a, c.F, R, 2ull * c.F, 64, 64);
+    MOE_MAP(&ma, a_used, c.F, R, 2ull * c.F, 64, 64);
     MOE_MAP(&mb, dy_perm, c.H, R, 2ull * c.H, 64, 64);
     CUtensorMap mo;
     if (!make_map_f32_3d(&mo, dW2, c.H, c.F, c.E)) return MOE_ERR_CUDA;

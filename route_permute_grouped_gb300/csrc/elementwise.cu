@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // Combine backward: dy_perm[row[t,i]] = bf16(g[t,i] * dO[t]),
 // dgate[t,i] = <dO[t], y_perm[row[t,i]]> (fp32). All k expert-output vectors
 // of a position are loaded before any store is issued, so the loads of the k
-// rows are in flight together.
-template <bool YP32, int KMAX>
+// rows are in flight together. DG = false (memory-saving backward, no y_perm):
+// dy_perm only; the gate gradient comes from the down-projection dgrad.
+template <bool YP32, int KMAX, bool DG = true>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     combine_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ y_perm,
                        const int32_t* __restrict__ row_id_map, const float* __restrict__ gate,
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     float f[KMAX][8];
 #pragma unroll
     for (int i = 0; i < KMAX; ++i)
-      if (i < k) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f[i]);
+      if (DG && i < k) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f[i]);
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
       if (i < k) {
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          s = fmaf(d[j], f[i][j], s);
+          if (DG) s = fmaf(d[j], f[i][j], s);
           o[j] = gs[i] * d[j];
         }
         dot[i] += s;
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
       }
     }
   }
+  if (!DG) return;
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) {
     if (i < k) {
@@ -153,9 +155,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
 //   aux (softmax): dL += p (dp - <p, dp>), dp_e = alpha E counts_e / (T k T).
 // Output dL split into bf16 hi = bf16(dL) and lo = bf16(dL - hi), written as
 // row t of dL_hl [T, 2 Ep]: hi at columns [0,E), lo at [Ep, Ep+E), zero padding.
+// Memory-saving backward (dg_part != nullptr): the gate gradient of slot i is
+// (sum over the n_part tile partials of its permuted row) / g, 0 where g = 0.
+__device__ __forceinline__ float slot_dgate(const float* dgate, const float* dg_part, int n_part,
+                                            const int32_t* row_id_map, const float* gate, size_t slot) {
+  if (dg_part == nullptr) return dgate[slot];
+  const float* pr = dg_part + static_cast<size_t>(row_id_map[slot]) * n_part;
+  float s = 0.0f;
+  for (int j = 0; j < n_part; ++j) s += pr[j];
+  const float g = gate[slot];
+  return g != 0.0f ? s / g : 0.0f;
+}
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                       const float* __restrict__ gate, const float* __restrict__ dgate,
+                      const float* __restrict__ dg_part, int n_part, const int32_t* __restrict__ row_id_map,
                       const int32_t* __restrict__ counts, int T, int E, int k, int score, float gate_scale,
                       float aux_coeff, int Ep, __nv_bfloat16* __restrict__ dL_hl) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -169,7 +183,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     if (lane < k) {
       my_e = topk_idx[static_cast<size_t>(t) * k + lane];
       q = gate[static_cast<size_t>(t) * k + lane] / gate_scale;
-      dg = dgate[static_cast<size_t>(t) * k + lane];
+      dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, static_cast<size_t>(t) * k + lane);
     }
     float inner = q * dg;
 #pragma unroll
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     if (lane < k) {
       my_e = topk_idx[static_cast<size_t>(t) * k + lane];
       s = 1.0f / (1.0f + __expf(-Lrow[my_e]));
-      dg = dgate[static_cast<size_t>(t) * k + lane];
+      dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, static_cast<size_t>(t) * k + lane);
     }
     float S = s, inner = dg * s;
 #pragma unroll
@@ -312,7 +326,10 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
                                cudaStream_t st) {
   const int b = blocks_for(c.T);
   const int th = kWarpsPerBlock * 32;
-  if (c.inter_fp32) {
+  if (y_perm == nullptr) {  // memory-saving backward: dy_perm only
+    if (c.k <= 8) combine_bwd_kernel<false, 8, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k);
+    else combine_bwd_kernel<false, 16, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k);
+  } else if (c.inter_fp32) {
     if (c.k <= 8) combine_bwd_kernel<true, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
     else combine_bwd_kernel<true, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
   } else {
@@ -323,11 +340,11 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
 }
 
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx, const float* gate,
-                              const float* dgate, const int32_t* counts, int Ep, __nv_bfloat16* dL_hl,
-                              cudaStream_t st) {
-  router_bwd_kernel<<<blocks_for(c.T), kWarpsPerBlock * 32, 0, st>>>(logits, topk_idx, gate, dgate, counts, c.T, c.E,
-                                                                     c.k, c.score, c.gate_scale, c.aux_coeff, Ep,
-                                                                     dL_hl);
+                              const float* dgate, const float* dg_part, int n_part, const int32_t* row_id_map,
+                              const int32_t* counts, int Ep, __nv_bfloat16* dL_hl, cudaStream_t st) {
+  router_bwd_kernel<<<blocks_for(c.T), kWarpsPerBlock * 32, 0, st>>>(logits, topk_idx, gate, dgate, dg_part, n_part,
+                                                                     row_id_map, counts, c.T, c.E, c.k, c.score,
+                                                                     c.gate_scale, c.aux_coeff, Ep, dL_hl);
   return cudaGetLastError();
 }
 

@@ -276,4 +276,74 @@ __device__ __forceinline__ void epi_dgrad2_tma(const GemmParams& p, const TileIn
   }
 }
 
+// DGRAD2R (memory-saving backward), rows all inside the expert: as
+// epi_dgrad2_tma, and also a = bf16(SiLU(h1) h3) recomputed from the saved
+// pre-activations into a third staging box (TMA store through map_a), and this
+// row's partial of the gate gradient, sum over the tile's columns of da * a
+// (with a as stored), into dg_part[row, n0 / 256].
+__device__ __forceinline__ void epi_dgrad2r_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
+                                                int row0, Stager& st, const CUtensorMap* map_out,
+                                                const CUtensorMap* map_a) {
+  const __nv_bfloat16* hrow =
+      reinterpret_cast<const __nv_bfloat16*>(p.in_aux) + static_cast<size_t>(row0 + lane) * (2 * p.F);
+  float dg = 0.0f;
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    const int col = ti.n0 + cc * 64;
+    if (col >= p.F) break;
+    uint4 v1[8], v3[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v1[j] = ldg_nc_v4(hrow + col + 8 * j);
+      v3[j] = ldg_nc_v4(hrow + p.F + col + 8 * j);
+    }
+    float da0[32], da1[32];
+    tmem_ld32_f(tacc + (cc * 2) * 32, da0);
+    tmem_ld32_f(tacc + (cc * 2 + 1) * 32, da1);
+    uint8_t *b1, *b3;
+    st.both(lane, b1, b3);  // every previous box has left the three buffers
+    uint8_t* ba = b1 + 8192;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float* da = j < 4 ? da0 : da1;
+      const uint32_t a1[4] = {v1[j].x, v1[j].y, v1[j].z, v1[j].w};
+      const uint32_t a3[4] = {v3[j].x, v3[j].y, v3[j].z, v3[j].w};
+      uint32_t o1[4], o3[4], oa[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float d1v[2], d3v[2], av[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x1 = e ? bf16_hi(a1[q]) : bf16_lo(a1[q]);
+          const float x3 = e ? bf16_hi(a3[q]) : bf16_lo(a3[q]);
+          const float d = da[8 * (j & 3) + 2 * q + e];
+          const float s = 1.0f / (1.0f + __expf(-x1));
+          const float si = x1 * s;
+          d1v[e] = d * x3 * (s * (1.0f + x1 * (1.0f - s)));
+          d3v[e] = d * si;
+          av[e] = __bfloat162float(__float2bfloat16_rn(si * x3));
+          dg = fmaf(d, av[e], dg);
+        }
+        o1[q] = pack_bf16x2(d1v[0], d1v[1]);
+        o3[q] = pack_bf16x2(d3v[0], d3v[1]);
+        oa[q] = pack_bf16x2(av[0], av[1]);
+      }
+      const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
+      *reinterpret_cast<uint4*>(b1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      *reinterpret_cast<uint4*>(b3 + off) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+      *reinterpret_cast<uint4*>(ba + off) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map_out, b1, col, row0);
+      tma_store_2d(map_out, b3, p.F + col, row0);
+      tma_store_2d(map_a, ba, col, row0);
+      bulk_commit();
+    }
+    st.n += 3;
+  }
+  p.dg_part[static_cast<size_t>(row0 + lane) * p.n_part + ti.n0 / 256] = dg;
+}
+
 }  // namespace moe

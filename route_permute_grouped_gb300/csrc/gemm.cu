@@ -14,9 +14,9 @@ namespace moe {
 template <int KIND>
 struct SmemLayout {
   static constexpr int kStages = KindTraits<KIND>::kStages;
-  // output staging for the TMA-store epilogue: 2 x 4 KB per epilogue warp
-  static constexpr int kOutOff = kRingBytes;
-  static constexpr int kOutBytes = 4 * 8192;
+  // output staging for the TMA-store epilogue: 2 (DGRAD2R: 3) x 4 KB per epilogue warp
+  static constexpr int kOutOff = KindTraits<KIND>::kStages * KindTraits<KIND>::kStageBytesK;
+  static constexpr int kOutBytes = 4 * KindTraits<KIND>::kOutWarpBytes;
   static constexpr int kBarOff = kOutOff + kOutBytes;
   static constexpr int kNumBars = 3 * KindTraits<KIND>::kMaxStages + 5;  // full, empty, peer, tfull[2],
                                                                         // tempty[2], drain
@@ -124,11 +124,16 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
 // DGRAD2: accumulator = da for F columns n0..n0+255; SwiGLU backward with the
 // saved bf16 pre-activations h1 (columns [0,F) of h13) and h3 ([F,2F)):
 //   dh1 = da * h3 * SiLU'(h1),  dh3 = da * SiLU(h1).
-__device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
+// `recompute` (DGRAD2R): also a = bf16(SiLU(h1) h3) into out1 [rows, F] and
+// this row's partial <da, a> over the tile into dg_part[row, n0 / 256].
+__device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r,
+                                           bool recompute) {
   const int row = ti.m0 + r;
   const bool valid = row < ti.m_end;
   const __nv_bfloat16* h13 = reinterpret_cast<const __nv_bfloat16*>(p.in_aux);
   __nv_bfloat16* dh13 = reinterpret_cast<__nv_bfloat16*>(p.out0);
+  __nv_bfloat16* aout = reinterpret_cast<__nv_bfloat16*>(p.out1);
+  float dg = 0.0f;
 #pragma unroll 1
   for (int c = 0; c < 8; ++c) {
     float da[32];
@@ -136,7 +141,7 @@ __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& 
     const int col = ti.n0 + c * 32;
     if (valid && col < p.F) {
       const size_t base = static_cast<size_t>(row) * 2 * p.F;
-      float h1[32], h3[32], d1[32], d3[32];
+      float h1[32], h3[32], d1[32], d3[32], av[32];
       load_bf16x32(h13 + base + col, h1);
       load_bf16x32(h13 + base + p.F + col, h3);
 #pragma unroll
@@ -145,11 +150,15 @@ __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& 
         const float si = h1[j] * s;
         d1[j] = da[j] * h3[j] * (s * (1.0f + h1[j] * (1.0f - s)));
         d3[j] = da[j] * si;
+        av[j] = __bfloat162float(__float2bfloat16_rn(si * h3[j]));
+        dg = fmaf(da[j], av[j], dg);
       }
       store_bf16x32(dh13 + base + col, d1);
       store_bf16x32(dh13 + base + p.F + col, d3);
+      if (recompute) store_bf16x32(aout + static_cast<size_t>(row) * p.F + col, av);
     }
   }
+  if (recompute && valid) p.dg_part[static_cast<size_t>(row) * p.n_part + ti.n0 / 256] = dg;
 }
 
 // ---------------------------------------------------------------------------
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    Stager st{smem + SL::kOutOff + q * 8192, 0u};
+    Stager st{smem + SL::kOutOff + q * TR::kOutWarpBytes, 0u};
     // pairs: the odd CTA's epilogue frees the even CTA's accumulator slot
     const uint32_t tempty_even = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
     for (int tile = tile_first; tile < ntiles; tile += tile_step) {
@@ -509,9 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (KIND == KIND_ROUTER) {
         // raw fp32 logits [T, bn]; the map's row extent T clips the tail
         epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
+      } else if constexpr (KIND == KIND_DGRAD2R) {
+        if (full_rows) epi_dgrad2r_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
+        else if (any_rows) epi_dgrad2(p, ti, tacc, r, true);
       } else if constexpr (KIND == KIND_DGRAD2) {
         if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0);
-        else if (any_rows) epi_dgrad2(p, ti, tacc, r);
+        else if (any_rows) epi_dgrad2(p, ti, tacc, r, false);
       } else if constexpr (KIND == KIND_DGRAD1) {
         if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
         else if (any_rows) epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
@@ -611,6 +623,7 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
     case KIND_FFN2: return launch_kind<KIND_FFN2>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_ROUTER: return launch_kind<KIND_ROUTER>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_DGRAD2: return launch_kind<KIND_DGRAD2>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_DGRAD2R: return launch_kind<KIND_DGRAD2R>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_DGRAD1: return launch_kind<KIND_DGRAD1>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_WGRAD: return launch_kind<KIND_WGRAD>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX>(p, ma, mb0, mb1, mo0, mo1, grid, st);

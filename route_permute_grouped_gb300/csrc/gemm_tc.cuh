@@ -33,6 +33,8 @@ enum GemmKind : int {
   KIND_WGRAD = 5,      // dW_e = X_e^T Y_e over the expert's rows (ragged K)
   KIND_ROUTER_DX = 6,  // dx_r = dL W_r     (dL as bf16 hi + lo parts)
   KIND_ROUTER_DW = 7,  // dW_r partial = dL^T x over one K split
+  KIND_DGRAD2R = 8,    // DGRAD2 of the memory-saving backward: also stores a = SiLU(h1) h3 recomputed from
+                       // h13 and the per-row partials of the gate gradient <da, a> over each 256-column tile
 };
 
 constexpr int kBM = 128;
@@ -54,17 +56,19 @@ struct KindTraits {
   // CTA pairs: the expert GEMMs with a fixed K run as M=256 tiles on two SMs
   // (cta_group::2); each CTA stages its own 128 rows of A and half of B
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD);
+                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
   static constexpr int kStageBytesK = kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
-  static constexpr int kStages = kPair ? 6 : 4;
+  // DGRAD2R gives one stage to a third staging box per epilogue warp
+  static constexpr int kStages = (KIND == KIND_DGRAD2R) ? 5 : (kPair ? 6 : 4);
+  static constexpr int kOutWarpBytes = (KIND == KIND_DGRAD2R) ? 3 * 4096 : 2 * 4096;  // epilogue staging
   // the router's B tile is bn x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                        KIND == KIND_DGRAD1);
+                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R);
 };
 
 struct GemmParams {
@@ -85,7 +89,9 @@ struct GemmParams {
   void* out0;            // FFN1: a; FFN2: y_perm; DGRAD2: dh13; DGRAD1: dx_perm;
                          // WGRAD: dW2 or dW1; ROUTER_DX: dx_r (fp32); ROUTER_DW: partials
   void* out1;            // FFN1: h13 save (nullable); WGRAD mode 1: dW3
-  const void* in_aux;    // DGRAD2: h13 (saved pre-activations)
+  const void* in_aux;    // DGRAD2, DGRAD2R: h13 (saved pre-activations)
+  float* dg_part;        // DGRAD2R: gate-gradient partials [rows, n_part] (DGRAD2R also stores a in out1)
+  int n_part;            // DGRAD2R: 256-column tiles of F
   int out_fp32;          // FFN2: y_perm fp32
   // status
   DevStatus* status;
@@ -189,7 +195,7 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
     const int n = ti.n0 + 128 * rank;
     tma_load_2d_pair(sB, mb0, bar_cluster, n, brow);
     tma_load_2d_pair(sB + 8192, mb0, bar_cluster, n + 64, brow);
-  } else if constexpr (KIND == KIND_DGRAD2) {
+  } else if constexpr (KIND == KIND_DGRAD2 || KIND == KIND_DGRAD2R) {
     tma_load_2d_pair(sB, mb0, bar_cluster, kk, ti.g * p.F + ti.n0 + 128 * rank);
   } else {  // DGRAD1
     const int brow = ti.g * p.H + ti.n0 + 128 * rank;

@@ -52,8 +52,9 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
 cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
                                  const float* extra, void* dx, cudaStream_t st);
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx,
-                              const float* gate, const float* dgate, const int32_t* counts, int Ep,
-                              __nv_bfloat16* dL_hl, cudaStream_t st);
+                              const float* gate, const float* dgate, const float* dg_part, int n_part,
+                              const int32_t* row_id_map, const int32_t* counts, int Ep, __nv_bfloat16* dL_hl,
+                              cudaStream_t st);
 cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
                             cudaStream_t st);
 cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, float* out, cudaStream_t st);

@@ -228,8 +228,11 @@ def unpermute_combine(cfg, y_perm, row_id_map, topk_gate, shared=None):
     return y
 
 
-def alloc_saved(cfg, device="cuda"):
-    """Tensors the training forward keeps for the backward."""
+def alloc_saved(cfg, device="cuda", recompute=False):
+    """Tensors the training forward keeps for the backward. ``recompute``:
+    the memory-saving mode, which keeps neither ``a`` nor ``y_perm`` (the
+    backward recomputes ``a`` from ``h13`` and takes the gate gradient from
+    the down-projection dgrad)."""
     T, H, E, k, F = cfg.T, cfg.H, cfg.E, cfg.k, cfg.F
     R = T * k
     f32, i32, bf = torch.float32, torch.int32, torch.bfloat16
@@ -242,8 +245,8 @@ def alloc_saved(cfg, device="cuda"):
         "offsets": torch.empty(E + 1, dtype=i32, device=device),
         "x_perm": torch.empty((R, H), dtype=bf, device=device),
         "h13": torch.empty((R, 2 * F), dtype=bf, device=device),
-        "a": torch.empty((R, F), dtype=bf, device=device),
-        "y_perm": torch.empty((R, H), dtype=_inter_dtype(cfg), device=device),
+        "a": None if recompute else torch.empty((R, F), dtype=bf, device=device),
+        "y_perm": None if recompute else torch.empty((R, H), dtype=_inter_dtype(cfg), device=device),
         "aux_partials": torch.empty((4 * ((T + 127) // 128), E), dtype=f32, device=device) if cfg.aux_coeff else None,
     }
 
