@@ -274,7 +274,7 @@ static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bf
   p.offsets = nullptr;
   CUtensorMap ma, mb, mo;
   MOE_MAP(&ma, x, c.H, c.T, 2ull * c.H, 64, 128);
-  MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn);
+  MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn / 2);  // CTA pairs: bn/2 router rows each
   // raw logits [T, bn] fp32 (columns >= E are zero: router rows past E read as zero)
   if (!make_map_store(&mo, raw, p.bn, c.T, true)) return MOE_ERR_CUDA;
   const int tiles = (c.T + kBM - 1) / kBM;

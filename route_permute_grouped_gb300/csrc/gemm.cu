@@ -298,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (PAIR) {
             uint8_t* sA = smem + stage * SBYTES;
             const bool ragged = KIND == KIND_WGRAD && ti.krow_end - (ti.krow0 + kb * kBK) < kBK;
+            // router: every pair reads the same router weight; start each pair at
+            // a different k block (the sum runs over all k blocks either way)
+            const int kbp = (KIND == KIND_ROUTER) ? (kb + tile_first * 5) % ti.nkb : kb;
             if (ragged) {
               // WGRAD's partial last k block: each CTA's share completes on
               // its own barrier, so that each can zero its rows past the
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // expects them; a share may land before the expectation (the
               // transaction count goes below zero meanwhile)
               if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
-              issue_loads_pair<KIND>(p, ti, kb, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
+              issue_loads_pair<KIND>(p, ti, kbp, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
                                      &mb0, &mb1);
             }
             issued_phase[stage] = static_cast<int>(phase);

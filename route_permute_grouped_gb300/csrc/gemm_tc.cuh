@@ -56,7 +56,8 @@ struct KindTraits {
   // CTA pairs: the expert GEMMs with a fixed K run as M=256 tiles on two SMs
   // (cta_group::2); each CTA stages its own 128 rows of A and half of B
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R);
+                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R ||
+                                 KIND == KIND_ROUTER);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
@@ -64,7 +65,7 @@ struct KindTraits {
   // DGRAD2R gives one stage to a third staging box per epilogue warp
   static constexpr int kStages = (KIND == KIND_DGRAD2R) ? 5 : (kPair ? 6 : 4);
   static constexpr int kOutWarpBytes = (KIND == KIND_DGRAD2R) ? 3 * 4096 : 2 * 4096;  // epilogue staging
-  // the router's B tile is bn x 64 (bn <= 256): its stages are packed at
+  // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
@@ -168,6 +169,12 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
                                                  const CUtensorMap* mb0, const CUtensorMap* mb1,
                                                  uint64_t* local_bar = nullptr) {
   const int kk = kb * kBK;
+  if constexpr (KIND == KIND_ROUTER) {
+    // 128 token rows of x; router-weight rows rank * bn/2 .. (box of bn/2 rows)
+    tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
+    tma_load_2d_pair(sB, mb0, bar_cluster, kk, rank * (p.bn / 2));
+    return;
+  }
   if constexpr (KIND == KIND_WGRAD) {
     const int r = ti.krow0 + kk;
     const int n = ti.n0 + 128 * rank;
@@ -269,9 +276,10 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 // wait until every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// router stage stride (a multiple of 1024 bytes: bn is a multiple of 32) and
-// the number of such stages in the ring
-__host__ __device__ __forceinline__ int router_stage_bytes(int bn) { return kABytes + bn * 128; }
+// router stage stride (a CTA-pair share: 128 x 64 of x and bn/2 x 64 of the
+// router weight; a multiple of 1024 bytes: bn is a multiple of 32) and the
+// number of such stages in the ring
+__host__ __device__ __forceinline__ int router_stage_bytes(int bn) { return kABytes + (bn / 2) * 128; }
 __host__ __device__ __forceinline__ int router_stages(int bn) {
   const int n = kRingBytes / router_stage_bytes(bn);
   return n < 8 ? n : 8;
@@ -279,8 +287,8 @@ __host__ __device__ __forceinline__ int router_stages(int bn) {
 
 template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
-  if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
-  else if constexpr (KIND == KIND_ROUTER) return kABytes + p.bn * 128;
+  if constexpr (KIND == KIND_ROUTER) return 2 * router_stage_bytes(p.bn);        // both CTAs' shares
+  else if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
   else return kABytes + kBBytesMax;
 }
 
