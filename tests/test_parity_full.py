@@ -181,3 +181,60 @@ def test_full_permute_bit_exact(skew):
     for i in range(k):
         r = torch.from_numpy(r_ref[ts, i]).cuda()
         assert torch.equal(xpb[r], xb[torch.from_numpy(ts).cuda()])
+
+
+@pytest.mark.parametrize("mode", ["memory_saving", "force_balanced"])
+def test_full_training_step_modes(mode):
+    """The two optional training modes at the full Qwen3 size, as
+    `bench.py --recompute` / `--force-balanced` time them: the memory-saving
+    backward (a and y_perm not kept) against the oracle's recompute variant,
+    and force-balanced routing (assignment and counts bit for bit)."""
+    force = mode == "force_balanced"
+    rec = mode == "memory_saving"
+    ls = synth.shape("qwen3_train", force_balanced=force)
+    d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
+    cfg = ops.config_from_shape(ls)
+    ws = ops.workspace(cfg, True)
+    saved = ops.alloc_saved(cfg, recompute=rec)
+    ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"],
+                  saved=saved, ws=ws)
+    g = ops.layer_bwd(cfg, d["dO"], d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    x = f64(d["x"])
+    rt = O.route(x, f64(d["router_w"]), ls.k, ls.score, None, None, ls.n_groups, ls.topk_groups, ls.gate_scale,
+                 force_balanced=force)
+    gidx = saved["topk_idx"].cpu().numpy()
+    counts = saved["counts"].cpu().numpy()
+    if force:
+        assert np.array_equal(gidx, rt["topk_idx"])
+        assert np.all(counts == ls.T * ls.k // ls.E)
+        keep = np.ones(ls.T, bool)
+    else:
+        assert compare_topk(gidx, rt["topk_idx"], rt["z"], ls.k) <= ls.T // 200
+        keep = topk_margin(rt["z"], ls.k) >= 1e-6
+    same = [e for e in range(ls.E)
+            if np.array_equal(np.nonzero((gidx == e).any(1))[0], np.nonzero((rt["topk_idx"] == e).any(1))[0])]
+    assert len(same) >= ls.E // 2
+    rng = np.random.default_rng(13)
+    experts = sorted(rng.choice(same, size=3, replace=False).tolist())
+    tok = _sample(rng, keep, 128)
+    prec = O.Precision(y=True, dx=True)
+    kw = dict(force_balanced=force, recompute=rec)
+    ref = O.layer_bwd(x, f64(d["router_w"]), _getter(d), None, None, f64(d["dO"]), ls.k, ls.score, None, None,
+                      aux_coeff=ls.aux_coeff, prec=prec, experts=experts, tokens=tok, **kw)
+    assert_close("dx", f64(g["dx"][torch.from_numpy(tok).cuda()]), ref["dx"][tok])
+    for e in experts:
+        for key in ("dW1", "dW3", "dW2"):
+            want = ref[key][e]
+            assert_close(f"{key}[{e}]", f64(g[key][e]), want, atol=wgrad_atol(want))
+    e = experts[0]
+    te = np.nonzero(rt["topk_idx"] == e)[0]
+    part = O.layer_bwd(x, f64(d["router_w"]), _getter(d), None, None, f64(d["dO"]), ls.k, ls.score, None, None,
+                       aux_coeff=ls.aux_coeff, prec=prec, experts=[], tokens=te, **kw)
+    others = np.setdiff1d(np.arange(ls.T), te)
+    dL_aux = O.router_backward(rt["logits"][others], rt["topk_idx"][others], rt["topk_gate"][others],
+                               np.zeros((len(others), ls.k)), ls.score, ls.gate_scale, rt_counts(rt, ls), ls.k,
+                               ls.aux_coeff, T_total=ls.T)
+    dwr_e = part["dlogits"][:, e] @ x[te] + dL_aux[:, e] @ x[others]
+    assert_close(f"dW_r[{e}]", f64(g["dW_r"][e]), dwr_e, atol=wgrad_atol(dwr_e))
