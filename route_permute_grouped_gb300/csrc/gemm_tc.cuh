@@ -3,17 +3,28 @@
 // One CTA per SM (192 threads):
 //   warp 0      TMA producer: 128-byte-swizzled tiles of A and B into a ring of
 //               shared-memory stages (mbarrier full/empty pairs);
-//   warp 1      TMEM owner and UMMA issuer: 128 x BN x 16 bf16 MMAs into one of
-//               two fp32 accumulators in tensor memory (2 x 256 columns), so the
-//               epilogue of tile i overlaps the main loop of tile i+1;
+//   warp 1      TMEM owner and MMA issuer: 128 (pairs: 256) x BN x 16 bf16 MMAs
+//               into one of two fp32 accumulators in tensor memory (2 x 256
+//               columns), so the epilogue of tile i overlaps the main loop of
+//               tile i+1;
 //   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
 //               reads 32 columns at a time and applies the kind's epilogue.
 //
+// CTA pairs (every kind but the router gradients): clusters of two CTAs run
+// M=256 tiles with tcgen05.mma.cta_group::2. Each CTA stages its own 128 rows
+// of A and one half of B; both CTAs' loads complete on the even CTA's full
+// barrier; the even CTA issues the MMAs and signals stage release, accumulator
+// ready and drain to both CTAs with multicast commits; the odd CTA's epilogue
+// frees the accumulator with cluster-scope arrivals on the even CTA's barrier.
+// An SM then receives 32 KB per 64-deep k block instead of 48 KB, which keeps
+// the operand stream within the L2-to-SM bandwidth.
+//
 // Tiles come from a device-side schedule: every CTA reads the per-expert row
 // offsets produced by the permute (no host synchronisation), builds the
-// prefix of tile counts in shared memory, and walks tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... . Each kind below fixes which global tensors
-// feed A and B, how a tile maps to coordinates, and what the epilogue writes.
+// prefix of tile counts in shared memory, and walks tiles blockIdx.x (pairs:
+// its cluster's index), + gridDim.x (pairs: the number of clusters), ... .
+// Each kind below fixes which global tensors feed A and B, how a tile maps to
+// coordinates, and what the epilogue writes.
 //
 // Operand staging (both operands as 128-byte swizzled boxes of 64 bf16):
 //   K-major operand with R rows: one box {64 (k), R} -> R rows of 128 B;
