@@ -2,7 +2,7 @@
 // experts and gates of every token (figures & tables page of the report,
 // Fig. 2: score function, top-k selection, load balancing).
 //
-// One warp per token (a warp takes four tokens of its CTA's 32-token slice).
+// One warp per token (a warp takes two tokens of its CTA's 32-token slice).
 // Lane l holds the experts e = l + 32 j (j < 8, E <= 256) in registers. Per
 // token:
 //   L = logit + logit_bias; score = softmax(L) or sigmoid(L);
@@ -37,8 +37,8 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 __device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) { return __reduce_min_sync(0xffffffffu, v); }
 
-constexpr int kSelWarps = 8;                   // warps per CTA
-constexpr int kTokPerWarp = kSel / kSelWarps;  // tokens per warp (4)
+constexpr int kSelWarps = 16;                  // warps per CTA
+constexpr int kTokPerWarp = kSel / kSelWarps;  // tokens per warp (2)
 
 // Score modes of the selection kernel (compile-time):
 //   SEL_SOFTMAX_LOGIT  softmax scores, no expert bias: z = L (the logits order
@@ -227,8 +227,8 @@ __device__ __forceinline__ void select_token(const float (&L)[NJ], int t, bool v
   }
 }
 
-// One CTA of 8 warps per 32-token slice; warp w takes tokens 4w..4w+3 of the
-// slice, loading all four tokens' logits before working on the first.
+// One CTA of 16 warps per 32-token slice; warp w takes tokens 2w and 2w+1 of
+// the slice, loading both tokens' logits before working on the first.
 template <int NJ, int MODE>
 __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(
     const float* __restrict__ raw, int ld, int T, int E, int k, int force, int n_groups, int topk_groups,
