@@ -229,6 +229,11 @@ int moe_get_device_status(void* ws, void* stream, int* status_out);
 /* Static text for a moe_status value. */
 const char* moe_status_string(int status);
 
+/* Size in bytes of the ABI structs as this library was compiled:
+ * which = 0 -> sizeof(moe_config), 1 -> sizeof(moe_fwd_saved), else 0.
+ * For bindings that mirror the structs to check their layout. */
+size_t moe_abi_struct_bytes(int which);
+
 /* Test hooks (not for production use). moe_debug_set_wait_limit_ns sets the
  * limit of every bounded device wait (default 2e9 ns = 2 s; 0 restores the
  * default). moe_debug_set_fault(1) makes the permute scan's first token chunk

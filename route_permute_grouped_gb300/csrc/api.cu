@@ -342,6 +342,10 @@ size_t moe_workspace_bytes(const moe_config* cfg, int training) {
   return ws_layout(*cfg, training != 0).total;
 }
 
+size_t moe_abi_struct_bytes(int which) {
+  return which == 0 ? sizeof(moe_config) : (which == 1 ? sizeof(moe_fwd_saved) : 0);
+}
+
 const char* moe_status_string(int s) {
   switch (s) {
     case MOE_OK: return "ok";

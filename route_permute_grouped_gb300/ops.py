@@ -54,6 +54,11 @@ def lib():
             raise RuntimeError(f"CUDA library {path} is missing: run route_permute_grouped_gb300.build.build()")
         L = ctypes.CDLL(path)
         vp = c_void_p
+        L.moe_abi_struct_bytes.restype = c_size_t
+        L.moe_abi_struct_bytes.argtypes = [c_int]
+        if (L.moe_abi_struct_bytes(0) != ctypes.sizeof(MoeConfig)
+                or L.moe_abi_struct_bytes(1) != ctypes.sizeof(MoeFwdSaved)):
+            raise RuntimeError("moe_config / moe_fwd_saved layout of the binding differs from the library")
         L.moe_workspace_bytes.restype = c_size_t
         L.moe_workspace_bytes.argtypes = [POINTER(MoeConfig), c_int]
         L.moe_router_topk.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]

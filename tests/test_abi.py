@@ -54,6 +54,7 @@ def test_workspace_bytes_and_status_strings(lib):
     (dict(E=512, k=8), 2),                  # E > 256
     (dict(score=7), 1),
     (dict(gate_scale=0.0), 1),
+    (dict(force_balanced=2), 1),
 ])
 def test_host_rejects_bad_config(lib, over, code):
     d = dict(T=256, H=128, E=8, k=2, F=256)
@@ -74,3 +75,10 @@ def test_host_rejects_null_and_small_workspace(lib):
                              None, fake, 16, None) == 3
     misaligned = ctypes.c_void_p(256 + 8)
     assert lib.moe_permute(ctypes.byref(cfg), misaligned, fake, fake, fake, fake, fake, fake, 1 << 30, None) == 1
+
+
+def test_binding_structs_match_the_library(lib):
+    lib.moe_abi_struct_bytes.restype = ctypes.c_size_t
+    assert lib.moe_abi_struct_bytes(0) == ctypes.sizeof(ops.MoeConfig)
+    assert lib.moe_abi_struct_bytes(1) == ctypes.sizeof(ops.MoeFwdSaved)
+    assert lib.moe_abi_struct_bytes(2) == 0
