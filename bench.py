@@ -22,6 +22,7 @@ ranks and the value is the work of all ranks over that time.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -120,14 +121,18 @@ def load_peaks():
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 class Clocks:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """nvidia-smi samples (every 50 ms) of the SM clock, its maximum, the power
+    draw and the throttle reasons; only samples stamped inside the timed region
+    (between mark_begin and mark_end) are kept."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -135,10 +140,17 @@ class Clocks:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)  # the sampler is running before the timed region starts
         except Exception:
             self.proc = None
+
+    def mark_begin(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def stop(self):
         if self.proc is None:
@@ -149,18 +161,27 @@ class Clocks:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
+        rows, every = [], []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
+            if len(parts) < 10:
+                continue
+            every.append(parts)
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            if self.t0 is not None and self.t1 is not None and not (self.t0 <= ts <= self.t1):
+                continue
+            rows.append(parts)
         os.unlink(self.path)
+        rows = rows or every  # unparsable stamps: keep every sample
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[6 + j].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
 
@@ -331,6 +352,7 @@ def run_ours(args, ls, rank, world, local_rank):
     clocks = Clocks(local_rank)
     barrier()
     clocks.start()
+    clocks.mark_begin()
     l0 = ops.launch_count()
     ops.profile_start(cap)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -339,6 +361,7 @@ def run_ours(args, ls, rank, world, local_rank):
         step()
     e1.record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     ops.profile_stop()
     barrier()
     clk = clocks.stop()
