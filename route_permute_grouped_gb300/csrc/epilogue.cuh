@@ -221,12 +221,14 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
                : "l"(ptr));
   return v;
 }
+// chunks cc_begin .. cc_end - 1 of the tile's four 64-column chunks
 __device__ __forceinline__ void epi_dgrad2_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
-                                               int row0, Stager& st, const CUtensorMap* map_out) {
+                                               int row0, Stager& st, const CUtensorMap* map_out, int cc_begin,
+                                               int cc_end) {
   const __nv_bfloat16* hrow =
       reinterpret_cast<const __nv_bfloat16*>(p.in_aux) + static_cast<size_t>(row0 + lane) * (2 * p.F);
 #pragma unroll 1
-  for (int cc = 0; cc < 4; ++cc) {
+  for (int cc = cc_begin; cc < cc_end; ++cc) {
     const int col = ti.n0 + cc * 64;
     if (col >= p.F) break;
     uint4 v1[8], v3[8];

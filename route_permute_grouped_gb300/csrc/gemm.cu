@@ -16,7 +16,7 @@ struct SmemLayout {
   static constexpr int kStages = KindTraits<KIND>::kStages;
   // output staging for the TMA-store epilogue: 2 (DGRAD2R: 3) x 4 KB per epilogue warp
   static constexpr int kOutOff = KindTraits<KIND>::kStages * KindTraits<KIND>::kStageBytesK;
-  static constexpr int kOutBytes = 4 * KindTraits<KIND>::kOutWarpBytes;
+  static constexpr int kOutBytes = KindTraits<KIND>::kEpiWarps * KindTraits<KIND>::kOutWarpBytes;
   static constexpr int kBarOff = kOutOff + kOutBytes;
   static constexpr int kNumBars = 3 * KindTraits<KIND>::kMaxStages + 5;  // full, empty, peer, tfull[2],
                                                                         // tempty[2], drain
@@ -127,7 +127,7 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
 // `recompute` (DGRAD2R): also a = bf16(SiLU(h1) h3) into out1 [rows, F] and
 // this row's partial <da, a> over the tile into dg_part[row, n0 / 256].
 __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r,
-                                           bool recompute) {
+                                           bool recompute, int c_begin, int c_end) {
   const int row = ti.m0 + r;
   const bool valid = row < ti.m_end;
   const __nv_bfloat16* h13 = reinterpret_cast<const __nv_bfloat16*>(p.in_aux);
@@ -135,7 +135,7 @@ __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& 
   __nv_bfloat16* aout = reinterpret_cast<__nv_bfloat16*>(p.out1);
   float dg = 0.0f;
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     float da[32];
     tmem_ld32f(tacc + c * 32, da);
     const int col = ti.n0 + c * 32;
@@ -165,7 +165,7 @@ __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& 
 // the kernel
 // ---------------------------------------------------------------------------
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap ma,
                 const __grid_constant__ CUtensorMap mb0, const __grid_constant__ CUtensorMap mb1,
                 const __grid_constant__ CUtensorMap mo0, const __grid_constant__ CUtensorMap mo1) {
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, PAIR ? 8 : 4);  // pairs: the epilogue warps of both CTAs
+      mbar_init(tempty + b, (PAIR ? 2 : 1) * TR::kEpiWarps);  // pairs: the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
     *s_abort = 0;
@@ -491,11 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int part = (warp - 2) >> 2;  // DGRAD2: which half of the tile's columns
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    Stager st{smem + SL::kOutOff + q * TR::kOutWarpBytes, 0u};
+    Stager st{smem + SL::kOutOff + (warp - 2) * TR::kOutWarpBytes, 0u};
     // pairs: the odd CTA's epilogue frees the even CTA's accumulator slot
     const uint32_t tempty_even = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
     for (int tile = tile_first; tile < ntiles; tile += tile_step) {
@@ -523,10 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
       } else if constexpr (KIND == KIND_DGRAD2R) {
         if (full_rows) epi_dgrad2r_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
-        else if (any_rows) epi_dgrad2(p, ti, tacc, r, true);
+        else if (any_rows) epi_dgrad2(p, ti, tacc, r, true, 0, 8);
       } else if constexpr (KIND == KIND_DGRAD2) {
-        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0);
-        else if (any_rows) epi_dgrad2(p, ti, tacc, r, false);
+        if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0, 2 * part, 2 * part + 2);
+        else if (any_rows) epi_dgrad2(p, ti, tacc, r, false, 4 * part, 4 * part + 4);
       } else if constexpr (KIND == KIND_DGRAD1) {
         if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
         else if (any_rows) epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
@@ -584,7 +585,7 @@ static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(KindTraits<KIND>::kThreadsK);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   if (KindTraits<KIND>::kPair) {

@@ -73,8 +73,12 @@ struct KindTraits {
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
   static constexpr int kStageBytesK = kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
-  // DGRAD2R gives one stage to a third staging box per epilogue warp
-  static constexpr int kStages = (KIND == KIND_DGRAD2R) ? 5 : (kPair ? 6 : 4);
+  // DGRAD2 runs eight epilogue warps (two per TMEM lane quadrant, each taking
+  // half of the tile's columns) to hide the latency of its loads of the saved
+  // pre-activations; it and DGRAD2R (third staging box) give up one stage
+  static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : 4;
+  static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
+  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2) ? 5 : (kPair ? 6 : 4);
   static constexpr int kOutWarpBytes = (KIND == KIND_DGRAD2R) ? 3 * 4096 : 2 * 4096;  // epilogue staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
