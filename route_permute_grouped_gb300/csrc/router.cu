@@ -6,8 +6,8 @@
 // Lane l holds the experts e = l + 32 j (j < 8, E <= 256) in registers. Per
 // token:
 //   L = logit + logit_bias; score = softmax(L) or sigmoid(L);
-//   z = L (softmax without expert bias: same order as the probabilities) or
-//       score + expert_bias;
+//   z = L (softmax without expert bias or group limit: the same order as the
+//       probabilities) or score + expert_bias;
 //   group limit: group score = sum of its two largest z, keep the best
 //       topk_groups groups (lower group index wins ties), z = -inf elsewhere;
 //   top-k of (z, -e) from per-lane sorted candidates and k rounds of warp
@@ -41,9 +41,11 @@ constexpr int kSelWarps = 16;                  // warps per CTA
 constexpr int kTokPerWarp = kSel / kSelWarps;  // tokens per warp (2)
 
 // Score modes of the selection kernel (compile-time):
-//   SEL_SOFTMAX_LOGIT  softmax scores, no expert bias: z = L (the logits order
-//                      the probabilities), gates from the selected logits;
-//   SEL_SOFTMAX_BIAS   softmax scores + expert bias: z = p + b;
+//   SEL_SOFTMAX_LOGIT  softmax scores, no expert bias, no group limit: z = L
+//                      (the logits order the probabilities), gates from the
+//                      selected logits;
+//   SEL_SOFTMAX_BIAS   softmax scores, with expert bias (z = p + b) or group
+//                      limit (z = p);
 //   SEL_SIGMOID        sigmoid scores (+ expert bias if given): z = s + b.
 enum SelMode : int { SEL_SOFTMAX_LOGIT = 0, SEL_SOFTMAX_BIAS = 1, SEL_SIGMOID = 2 };
 
@@ -298,7 +300,9 @@ cudaError_t launch_router_select(const moe_config& c, const float* raw, int ld, 
   const size_t smem = aux ? sizeof(float) * kSel * c.E : 0;
   const int nj = (c.E + 31) / 32;
   const bool softmax = c.score == MOE_SCORE_SOFTMAX;
-  if (softmax && expert_bias == nullptr) {
+  // a group limit ranks groups by sums of scores, which logits do not order
+  const bool grouped = !c.force_balanced && c.n_groups > 1 && c.topk_groups < c.n_groups;
+  if (softmax && expert_bias == nullptr && !grouped) {
     pick_select_kernel<SEL_SOFTMAX_LOGIT>(nj)<<<blocks, kSelWarps * 32, smem, st>>>(
         raw, ld, c.T, c.E, c.k, c.force_balanced, c.n_groups, c.topk_groups, c.gate_scale, expert_bias, logit_bias,
         topk_idx, topk_gate, logits_out, aux_partials);

@@ -29,6 +29,9 @@ SHAPES = {
     "dsv3_small": synth.shape("dsv3", T=333, H=256, E=64, k=8, F=128, F_shared=192),
     "e_eq_k": synth.shape("tiny", T=200, H=128, E=4, k=4, F=128),
     "k1": synth.shape("tiny", T=300, H=192, E=3, k=1, F=64),
+    # softmax scores with a group limit and no expert bias: groups are ranked
+    # by sums of probabilities (not of logits)
+    "softmax_groups": synth.shape("tiny", T=450, H=256, E=64, k=6, F=128, n_groups=8, topk_groups=3, w_std=0.1),
 }
 
 
