@@ -9,3 +9,4 @@ Method source: "Scalable Training of Mixture-of-Experts Models with Megatron
 Core" (paper summary page and the figures & tables page of the same report).
 """
 from .moe_oracle import *  # noqa: F401,F403
+from .mx_oracle import *  # noqa: F401,F403
