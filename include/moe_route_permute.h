@@ -221,6 +221,61 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x,
                   void* dx, float* dW_router, float* dW1, float* dW3, float* dW2,
                   float* aux_loss_out, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * MXFP8 expert GEMMs (forward). The report benchmarks its Blackwell runs with
+ * MXFP8, microscaling FP8 (figures & tables page, Table 11 "Dtype" and
+ * Fig. 30) without defining it; the format here is the OCP Microscaling (MX)
+ * v1.0 MXFP8: blocks of 32 consecutive elements along a GEMM operand's K share
+ * one E8M0 scale 2^s (byte s + 127), s = floor(log2 max|v|) - 8 clamped to
+ * [-127, 127] (-127 for an all-zero block); elements are E4M3 (bias 7, no
+ * infinities) v / 2^s rounded to nearest, ties to even, saturating at +-448.
+ * Requires H and F multiples of 128.
+ * ------------------------------------------------------------------------- */
+
+/* Quantised expert weights, device buffers owned by the caller (sizes from
+ * moe_mx_weight_bytes), written by moe_mx_quantize_weights:
+ *   w13  [E][2][F][H] E4M3: per expert W1[e]^T then W3[e]^T (K = H contiguous);
+ *   w2   [E][H][F]    E4M3: W2[e]^T (K = F contiguous);
+ *   sf13, sf2: their E8M0 scales in the tile-ready layout of the FP8 GEMMs
+ *   (opaque: blocks of 2 x 512 bytes per expert, 96-column (w13: 96 W1 +
+ *   96 W3 rows) or 192-column (w2) tile and 128-element k block; byte
+ *   512 b + 16 r + 4 c + s holds the scale of tile row 128 b + 32 c + r,
+ *   32-element K block 4 kb + s; unused bytes zero). */
+typedef struct {
+  uint8_t* w13;
+  uint8_t* sf13;
+  uint8_t* w2;
+  uint8_t* sf2;
+} moe_mx_weights;
+
+/* Bytes of the moe_mx_weights buffers: which = 0 w13, 1 sf13, 2 w2, 3 sf2
+ * (0 for an invalid config or shape). */
+size_t moe_mx_weight_bytes(const moe_config* cfg, int which);
+
+/* Quantise the bf16 expert weights W1, W3 [E,H,F] (blocks along H) and W2
+ * [E,F,H] (blocks along F) into *w. Enqueues on `stream`. */
+int moe_mx_quantize_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3,
+                            const moe_bf16* W2, const moe_mx_weights* w, void* stream);
+
+/* Row-major MXFP8 quantisation of x [M,K] bf16 (K a multiple of 32, blocks
+ * along K): q [M,K] E4M3 codes, scales [M,K/32] E8M0 bytes. */
+int moe_mx_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, void* stream);
+
+/* Workspace bytes of moe_layer_fwd_mxfp8. */
+size_t moe_mx_workspace_bytes(const moe_config* cfg);
+
+/* Whole layer forward with MXFP8 expert GEMMs: router and combine as in
+ * moe_layer_fwd; the permute quantises x's rows (blocks along H) as it
+ * scatters them; gate/up GEMM h = Q(x_perm) [Q(W1_e) | Q(W3_e)] (fp32
+ * accumulation) with a = SiLU(h1) h3 quantised in its epilogue (blocks along
+ * F); down GEMM y_perm = Q(a) Q(W2_e), stored bf16 (fp32 if inter_fp32); the
+ * shared expert (F_shared > 0) runs in bf16. y [T,H] bf16 (fp32 if out_fp32).
+ * Inference: intermediates live in the workspace. */
+int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                        const float* expert_bias, const float* logit_bias, const moe_mx_weights* w,
+                        const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2, void* y,
+                        void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, returns in *status_out the first device-side error
  * recorded in `ws` since the last read (MOE_OK if none) and clears it. For
  * tests and debugging; the hot path never calls it. */

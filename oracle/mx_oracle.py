@@ -29,7 +29,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import CONTRACT, permute_plan, route, silu
+from .moe_oracle import CONTRACT, permute_plan, route, silu, swiglu_expert
 
 __all__ = ["E4M3_MAX", "e4m3_round", "e4m3_encode", "e4m3_decode", "e8m0_exponent", "mx_quantize",
            "mx_dequantize", "mx_roundtrip", "mx_layer_fwd"]
@@ -121,7 +121,7 @@ def mx_roundtrip(v, axis=-1):
 
 
 def mx_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
-                 topk_groups=1, gate_scale=1.0, prec=CONTRACT, tokens=None, force_balanced=False):
+                 topk_groups=1, gate_scale=1.0, Ws=None, prec=CONTRACT, tokens=None, force_balanced=False):
     """Forward of the layer with MXFP8 expert GEMMs.
 
     Routing and combine are those of the bf16 layer (fp64). Per expert e on its
@@ -129,6 +129,7 @@ def mx_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
     along H; a = SiLU(h1) h3; out = Q(a) Q(W2e) along F, stored per
     ``prec.y_perm``. W1/W3 [E,H,F] and W2 [E,F,H] are the bf16 layer's
     weights; ``tokens`` restricts the expert and combine stages as in
+    ``layer_fwd``. The optional shared expert ``Ws`` runs unquantised, as in
     ``layer_fwd``."""
     x = np.asarray(x, np.float64)
     T, H = x.shape
@@ -153,6 +154,9 @@ def mx_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
             yp[(int(t_e[j]), int(sel_i[j]))] = out[j]
     y = np.full((T, H), np.nan)
     acc = np.zeros((len(tok), H))
+    if Ws is not None:
+        Ws1, Ws3, Ws2 = (np.asarray(w, np.float64) for w in Ws)
+        acc = acc + prec.r("shared", swiglu_expert(x[tok], Ws1, Ws3, Ws2, prec)[3])
     for i in range(k):
         rows = np.stack([yp[(int(t), i)] for t in tok]) if len(tok) else np.zeros((0, H))
         acc = acc + rt["topk_gate"][tok, i:i + 1] * rows

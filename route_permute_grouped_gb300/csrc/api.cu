@@ -112,6 +112,22 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major [outer, inner] array of bytes (E4M3 codes), box
+// {box_inner, box_outer}, 128-byte swizzle, zero fill outside the array.
+static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                        uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
@@ -152,6 +168,8 @@ struct WsLayout {
   size_t logits_raw, topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
   // backward
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
+  // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
+  size_t x_q, sfa1, a_q, sfa2;
   size_t total;
 };
 
@@ -163,7 +181,7 @@ static int router_dw_splits(int T) {
   return s < 1 ? 1 : s;
 }
 
-static WsLayout ws_layout(const moe_config& c, bool training) {
+static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false) {
   WsLayout L{};
   const size_t T = c.T, H = c.H, E = c.E, k = c.k, F = c.F, R = T * k;
   const size_t inter = c.inter_fp32 ? 4 : 2;
@@ -181,8 +199,15 @@ static WsLayout ws_layout(const moe_config& c, bool training) {
   L.row_id_map = take(4 * T * k);
   L.counts = take(4 * E);
   L.offsets = take(4 * (E + 1));
-  L.x_perm = take(2 * R * H);
-  L.a = take(2 * R * F);
+  if (mx) {
+    L.x_q = take(R * H);
+    L.sfa1 = take(mx_sfa_bytes(c.T * c.k, c.E, c.H));
+    L.a_q = take(R * F);
+    L.sfa2 = take(mx_sfa_bytes(c.T * c.k, c.E, c.F));
+  } else {
+    L.x_perm = take(2 * R * H);
+    L.a = take(2 * R * F);
+  }
   L.y_perm = take(inter * R * H);
   L.as = c.F_shared ? take(2 * T * c.F_shared) : 0;
   L.s_out = c.F_shared ? take(inter * T * H) : 0;
@@ -325,6 +350,57 @@ static int run_ffn(const moe_config& c, int F, int ngroups, const int32_t* offse
   if (!make_map_store(&oy, y, c.H, M, y_fp32)) return MOE_ERR_CUDA;
   MOE_CUDA(launch_gemm(KIND_FFN2, q, mA, m2, m2, num_sms(), s, &oy));
   stage_done(s, tag2, 1);
+  return MOE_OK;
+}
+
+static int check_mx_shape(const moe_config& c) {
+  // k blocks of 128 codes along H (gate/up GEMM) and F (down GEMM)
+  if (c.H % kMxKB != 0 || c.F % kMxKB != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+// MXFP8 grouped SwiGLU FFN over the permuted rows: a = SiLU(Q(x) Q(W1)) * (Q(x)
+// Q(W3)) quantised in the epilogue, y_perm = Q(a) Q(W2).
+static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const uint8_t* x_q, const uint8_t* sfa1,
+                      const moe_mx_weights& w, uint8_t* a_q, uint8_t* sfa2, void* y, bool y_fp32, DevStatus* st,
+                      cudaStream_t s) {
+  GemmParams p = base_params(c, st);
+  p.F = c.F;
+  p.ngroups = c.E;
+  p.offsets = offsets;
+  p.M_total = R;
+  p.bn = kMxBN;
+  p.n_tiles = mx_ntiles1(c);
+  p.nt_w = mx_ntiles1(c);
+  p.kb_total = c.H / kMxKB;
+  p.out0 = a_q;
+  p.sfa = sfa1;
+  p.sfb = w.sf13;
+  p.sfa_out = sfa2;
+  CUtensorMap ma, mb;
+  if (!make_map_u8(&ma, x_q, c.H, R, kMxKB, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb, w.w13, c.H, 2ull * c.E * c.F, kMxKB, kMxTileF1)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_gemm(KIND_FFN1_MX, p, ma, mb, mb, num_sms(), s, nullptr));
+  stage_done(s, STAGE_FFN1, 1);
+  GemmParams q = base_params(c, st);
+  q.F = c.F;
+  q.ngroups = c.E;
+  q.offsets = offsets;
+  q.M_total = R;
+  q.bn = kMxBN;
+  q.n_tiles = mx_ntiles2(c);
+  q.nt_w = mx_ntiles2(c);
+  q.kb_total = c.F / kMxKB;
+  q.out0 = y;
+  q.out_fp32 = y_fp32;
+  q.sfa = sfa2;
+  q.sfb = w.sf2;
+  CUtensorMap ma2, mb2, oy;
+  if (!make_map_u8(&ma2, a_q, c.F, R, kMxKB, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb2, w.w2, c.F, static_cast<uint64_t>(c.E) * c.H, kMxKB, kMxTileN2)) return MOE_ERR_CUDA;
+  if (!make_map_store(&oy, y, c.H, R, y_fp32)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_gemm(KIND_FFN2_MX, q, ma2, mb2, mb2, num_sms(), s, &oy));
+  stage_done(s, STAGE_FFN2, 1);
   return MOE_OK;
 }
 
@@ -679,6 +755,96 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     MOE_CUDA(launch_aux_loss(c, saved->aux_partials, saved->counts, aux_loss_out, s));
     stage_done(s, STAGE_AUX, 1);
   }
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 forward
+// ---------------------------------------------------------------------------
+size_t moe_mx_weight_bytes(const moe_config* cfg, int which) {
+  if (check_cfg(cfg) != MOE_OK || check_mx_shape(*cfg) != MOE_OK) return 0;
+  const moe_config& c = *cfg;
+  switch (which) {
+    case 0: return 2ull * c.E * c.F * c.H;
+    case 1: return mx_sf13_bytes(c);
+    case 2: return static_cast<size_t>(c.E) * c.H * c.F;
+    case 3: return mx_sf2_bytes(c);
+    default: return 0;
+  }
+}
+
+int moe_mx_quantize_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                            const moe_mx_weights* w, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_mx_shape(*cfg));
+  if (!W1 || !W3 || !W2 || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w13) || !aligned16(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_mx_quantize_weights(*cfg, reinterpret_cast<const __nv_bfloat16*>(W1),
+                                      reinterpret_cast<const __nv_bfloat16*>(W3),
+                                      reinterpret_cast<const __nv_bfloat16*>(W2), w->w13, w->sf13, w->w2, w->sf2,
+                                      static_cast<cudaStream_t>(stream)));
+  count_launches(3);
+  return MOE_OK;
+}
+
+int moe_mx_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, void* stream) {
+  if (!x || !q || !scales || M < 0 || K < kMxBlock || K % kMxBlock != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_mx_quantize_rows(reinterpret_cast<const __nv_bfloat16*>(x), M, K, q, scales,
+                                   static_cast<cudaStream_t>(stream)));
+  count_launches(M > 0 ? 1 : 0);
+  return MOE_OK;
+}
+
+size_t moe_mx_workspace_bytes(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK || check_mx_shape(*cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg, false, true).total;
+}
+
+int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                        const float* expert_bias, const float* logit_bias, const moe_mx_weights* w,
+                        const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2, void* y, void* ws,
+                        size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_mx_shape(c));
+  if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2 || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (c.F_shared && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
+      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, false, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  int32_t* idx = at<int32_t>(ws, L.topk_idx);
+  float* gate = at<float>(ws, L.topk_gate);
+  int32_t* rows = at<int32_t>(ws, L.row_id_map);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offs = at<int32_t>(ws, L.offsets);
+  uint8_t* x_q = at<uint8_t>(ws, L.x_q);
+  uint8_t* sfa1 = at<uint8_t>(ws, L.sfa1);
+  uint8_t* a_q = at<uint8_t>(ws, L.a_q);
+  uint8_t* sfa2 = at<uint8_t>(ws, L.sfa2);
+  void* yp = at<void>(ws, L.y_perm);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  prof_mark(s, STAGE_BEGIN);
+  MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
+                     nullptr, nullptr, at<float>(ws, L.logits_raw), st, s));
+  stage_done(s, STAGE_ROUTER, 2);
+  MOE_CUDA(launch_permute(c, xb, idx, nullptr, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s, x_q, sfa1));
+  stage_done(s, STAGE_PERMUTE, 2);
+  MOE_TRY(run_ffn_mx(c, offs, c.T * c.k, x_q, sfa1, *w, a_q, sfa2, yp, c.inter_fp32 != 0, st, s));
+  void* shared = nullptr;
+  if (c.F_shared) {
+    shared = at<void>(ws, L.s_out);
+    MOE_TRY(run_ffn(c, c.F_shared, 1, nullptr, c.T, xb, reinterpret_cast<const __nv_bfloat16*>(Ws1),
+                    reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), nullptr,
+                    at<__nv_bfloat16>(ws, L.as), shared, c.inter_fp32 != 0, st, s, STAGE_SHARED1, STAGE_SHARED2));
+  }
+  MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
+  stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
 }
 

@@ -272,6 +272,43 @@ __device__ __forceinline__ void umma2_commit_mc(uint64_t* bar, uint16_t cta_mask
       : "memory");
 }
 
+// Block-scaled FP8 MMA (kind::mxf8f6f4, scale_vec::1X: one E8M0 scale per row
+// and K=32 step): D[tmem] (+)= (A * scale_A) (B * scale_B), E4M3 inputs from
+// shared memory, scales from tensor memory (`sfa`, `sfb`: columns of the scale
+// cells; the byte chosen by the instruction descriptor's scale ids).
+__device__ __forceinline__ void umma_mx_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], da, db, %4, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Copy 32 rows x 16 bytes of shared memory (descriptor `desc`) to four TMEM
+// columns of lanes 0-31, replicated into all four lane quarters. Executed in
+// issue order with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+// Bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B (K-major), fp32 D and
+// E8M0 scales (bit 23); scale ids (bits 29-30 for A, 4-5 for B) are or-ed in
+// per K step.
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N) {
+  return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |

@@ -138,11 +138,11 @@ __device__ __forceinline__ void epi_ffn1_tma(const GemmParams& p, const TileInfo
 // the group as the third coordinate and clip rows per group.
 template <bool F32, bool THREE_D>
 __device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc, int lane, int row0, int ncols,
-                                              Stager& st, const CUtensorMap* map) {
+                                              Stager& st, const CUtensorMap* map, int nch64 = 4) {
   const bool zero = ti.nkb == 0;
   if constexpr (F32) {
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 2 * nch64; ++c) {
       const int col = ti.n0 + c * 32;
       if (col >= ncols) break;
       float f[32];
@@ -159,7 +159,7 @@ __device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc,
     }
   } else {
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < nch64; ++cc) {
       const int col = ti.n0 + cc * 64;
       if (col >= ncols) break;
       uint8_t* buf = st.next(lane);

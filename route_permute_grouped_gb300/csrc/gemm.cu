@@ -121,6 +121,40 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
   }
 }
 
+// MXFP8 gate/up epilogue, thread = row r of the tile: for each 32-column block
+// of the tile's 96 F columns a = SiLU(h1) h3 (h1 from accumulator columns
+// 32 b.., h3 from 96 + 32 b..) is quantised as one MXFP8 block of the down
+// GEMM's K: codes to a_q[row, col..] (rows of this expert only) and the scale
+// to the down GEMM's tile-ready A scale block of this m tile (every row of the
+// tile, so rows past the expert carry a valid scale too).
+__device__ __forceinline__ void epi_ffn1_mx(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
+  const int row = ti.m0 + r;
+  const bool valid = row < ti.m_end;
+  uint8_t* aq = reinterpret_cast<uint8_t*>(p.out0);
+  const int nkb2 = p.F / kMxKB;
+#pragma unroll 1
+  for (int b = 0; b < kMxTileF1 / 32; ++b) {
+    const int col = ti.n0 + 32 * b;
+    if (col >= p.F) break;  // uniform: the last tile of a ragged F
+    float h1[32], h3[32];
+    tmem_ld32f(tacc + 32 * b, h1);
+    tmem_ld32f(tacc + kMxTileF1 + 32 * b, h3);
+    float a[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = silu_f(h1[j]) * h3[j];
+    uint32_t w[8];
+    const uint32_t sb = mx_quant32(a, w);
+    if (valid) {
+      uint4* d = reinterpret_cast<uint4*>(aq + static_cast<size_t>(row) * p.F + col);
+      d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    const int fb = col / 32;
+    p.sfa_out[(static_cast<size_t>(ti.mt) * nkb2 + fb / 4) * kMxSfBytes + mx_sf_pos(r, fb & 3)] =
+        static_cast<uint8_t>(sb);
+  }
+}
+
 // DGRAD2: accumulator = da for F columns n0..n0+255; SwiGLU backward with the
 // saved bf16 pre-activations h1 (columns [0,F) of h13) and h3 ([F,2F)):
 //   dh1 = da * h3 * SiLU'(h1),  dh3 = da * SiLU(h1).
@@ -347,7 +381,11 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
+    const uint32_t idesc = TR::kMx ? idesc_mxf8_f32(kBM, kMxBN) : idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
+    // MXFP8: descriptors of the stage's scale blocks (32 rows of 16 bytes,
+    // no swizzle, 8-row groups 128 bytes apart) for the copies into TMEM
+    const uint32_t sf_lo0 = sdesc_lo(smem_u32(smem) + kMxSfOff, 128);
+    const uint64_t sf_hi = static_cast<uint64_t>((128u >> 4) | (1u << 14)) << 32;
     // operand descriptors: stage 0's low words, advanced per stage and per
     // 16-deep k step (K-major: 32 bytes; MN-major: 16 rows of 128 bytes)
     const uint32_t d_hi = sdesc_hi_sw128(1024);
@@ -453,7 +491,23 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           }
           __syncwarp();
         }
-        if (lane == 0) {
+        if (TR::kMx && lane == 0) {
+          // scales of this k block into TMEM (in issue order with the MMAs,
+          // after the previous block's MMAs), then four K=32 steps, step kk
+          // taking byte kk of the scale cells
+          const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
+          const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
+          const uint32_t sf_lo = sf_lo0 + static_cast<uint32_t>(stage) * stage_lo;
+          tmem_cp_32x128b_x4(tmem_base + kMxSfaCol, sf_hi | sf_lo);
+          tmem_cp_32x128b_x4(tmem_base + kMxSfbCol, sf_hi | (sf_lo + (kMxSfBytes >> 4)));
+          tmem_cp_32x128b_x4(tmem_base + kMxSfbCol + 4, sf_hi | (sf_lo + (2 * kMxSfBytes >> 4)));
+#pragma unroll
+          for (int kk = 0; kk < kMxKB / 32; ++kk)
+            umma_mx_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi,
+                      idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
+                      tmem_base + kMxSfaCol, tmem_base + kMxSfbCol, (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(empty + stage);
+        } else if (lane == 0) {
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
 #pragma unroll
@@ -518,6 +572,15 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
         } else if (any_rows) {
           epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
+        }
+      } else if constexpr (KIND == KIND_FFN1_MX) {
+        epi_ffn1_mx(p, ti, tacc, r);
+      } else if constexpr (KIND == KIND_FFN2_MX) {
+        if (full_rows) {
+          if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0, kMxBN / 64);
+          else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0, kMxBN / 64);
+        } else if (any_rows) {
+          epi_store(ti, tacc, r, kMxBN / 32, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
         }
       } else if constexpr (KIND == KIND_ROUTER) {
         // raw fp32 logits [T, bn]; the map's row extent T clips the tail
@@ -632,6 +695,8 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
     case KIND_WGRAD: return launch_kind<KIND_WGRAD>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_ROUTER_DX: return launch_kind<KIND_ROUTER_DX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_FFN1_MX: return launch_kind<KIND_FFN1_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_FFN2_MX: return launch_kind<KIND_FFN2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

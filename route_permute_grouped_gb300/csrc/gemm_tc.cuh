@@ -32,6 +32,7 @@
 //   64 K-rows of 128 B (8 KB), placed 8 KB apart.
 #pragma once
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -46,6 +47,9 @@ enum GemmKind : int {
   KIND_ROUTER_DW = 7,  // dW_r partial = dL^T x over one K split
   KIND_DGRAD2R = 8,    // DGRAD2 of the memory-saving backward: also stores a = SiLU(h1) h3 recomputed from
                        // h13 and the per-row partials of the gate gradient <da, a> over each 256-column tile
+  KIND_FFN1_MX = 9,    // MXFP8 gate/up: h = Q(x_perm) [Q(W1_e) | Q(W3_e)] -> a = SiLU(h1) h3, stored as MXFP8
+                       // (codes + the down GEMM's tile-ready scales); tiles of 96 gate + 96 up columns
+  KIND_FFN2_MX = 10,   // MXFP8 down: y_perm = Q(a) Q(W2_e), bf16 out; tiles of 192 columns
 };
 
 constexpr int kBM = 128;
@@ -57,6 +61,14 @@ constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kRingBytes = 4 * kStageBytes;  // shared memory of the operand stage ring
 constexpr int kMaxGroups = 256;
 constexpr int kTmemCols = 512;
+// MXFP8 stage: A 16 KB at 0, B (192 rows x 128 B) at 16 KB, scale blocks of A
+// (512 B) and B (1 KB) at 40 KB; 42 KB keeps every stage 1024-byte aligned
+constexpr int kMxSfOff = 40960;
+constexpr int kMxStageBytes = 43008;
+constexpr uint32_t kMxStageTx = 16384 + kMxBN * 128 + 3 * kMxSfBytes;
+// TMEM columns of the scale cells (past both 192-column accumulators)
+constexpr uint32_t kMxSfaCol = 448;
+constexpr uint32_t kMxSfbCol = 452;
 constexpr int kAccStride = 256;           // TMEM column distance of the two accumulators
 
 template <int KIND>
@@ -66,25 +78,28 @@ struct KindTraits {
                                 KIND == KIND_ROUTER_DX || KIND == KIND_ROUTER_DW);
   // CTA pairs: the expert GEMMs with a fixed K run as M=256 tiles on two SMs
   // (cta_group::2); each CTA stages its own 128 rows of A and half of B
+  // MXFP8 kinds: one CTA per 128 x 192 tile; a stage holds 128 k elements (one
+  // byte each) of A (16 KB) and B (24 KB) and their scale blocks (0.5 + 1 KB)
+  static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX);
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
                                  KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R ||
                                  KIND == KIND_ROUTER);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
-  static constexpr int kStageBytesK = kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
+  static constexpr int kStageBytesK = kMx ? kMxStageBytes : kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
   // DGRAD2 runs eight epilogue warps (two per TMEM lane quadrant, each taking
   // half of the tile's columns) to hide the latency of its loads of the saved
   // pre-activations; it and DGRAD2R (third staging box) give up one stage
   static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
-  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2) ? 5 : (kPair ? 6 : 4);
+  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2) ? 5 : (kPair ? 6 : 4);  // MX: 4
   static constexpr int kOutWarpBytes = (KIND == KIND_DGRAD2R) ? 3 * 4096 : 2 * 4096;  // epilogue staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R);
+                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R || kMx);
 };
 
 struct GemmParams {
@@ -109,6 +124,13 @@ struct GemmParams {
   float* dg_part;        // DGRAD2R: gate-gradient partials [rows, n_part] (DGRAD2R also stores a in out1)
   int n_part;            // DGRAD2R: 256-column tiles of F
   int out_fp32;          // FFN2: y_perm fp32
+  // MXFP8 kinds: tile-ready scale blocks of A (per global m tile and k block)
+  // and B (per expert, n tile and k block); FFN1_MX writes the down GEMM's A
+  // scales to sfa_out; nt_w = n tiles per expert of the weight scales
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  uint8_t* sfa_out;
+  int nt_w;
   // status
   DevStatus* status;
   unsigned long long wait_limit_ns;
@@ -123,6 +145,8 @@ struct TileInfo {
   int nkb;     // k blocks of this tile
   int krow0;   // WGRAD: first row of the expert (K origin); ROUTER_DW: unused
   int krow_end;
+  int mt;      // grouped kinds: global m tile (tiles of all earlier groups + this group's)
+  int nb;      // n tile within the group
 };
 
 template <int KIND>
@@ -138,6 +162,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
   int local = tile - s_cum[lo];
   int mb = local / p.n_tiles;
   int nb = local - mb * p.n_tiles;
+  ti.mt = s_cum[lo] / p.n_tiles + mb;
+  ti.nb = nb;
   if constexpr (KindTraits<KIND>::kGroupedRows || KIND == KIND_ROUTER || KIND == KIND_ROUTER_DX) {
     // a pair tile spans 256 rows: this CTA's 128 start at rank * 128
     ti.m0 = s_off[lo] + mb * KindTraits<KIND>::kTileM + rank * kBM;
@@ -166,6 +192,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
   }
   if constexpr (KIND == KIND_FFN1) {
     ti.n0 = nb * 128;  // F columns (gate and up halves of the 256-wide tile)
+  } else if constexpr (KIND == KIND_FFN1_MX) {
+    ti.n0 = nb * kMxTileF1;  // F columns (gate and up halves of the 192-wide tile)
   } else {
     ti.n0 = nb * p.bn;
   }
@@ -231,6 +259,27 @@ template <int KIND>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& ti, int kb, uint8_t* sA,
                                             uint8_t* sB, uint64_t* bar, const CUtensorMap* ma,
                                             const CUtensorMap* mb0, const CUtensorMap* mb1) {
+  if constexpr (KindTraits<KIND>::kMx) {
+    // 128 k elements (bytes) of the tile's A rows and B rows, and the scale
+    // blocks of both (A: global m tile; B: expert, n tile)
+    const int kc = kb * kMxKB;
+    tma_load_2d(sA, ma, bar, kc, ti.m0);
+    if constexpr (KIND == KIND_FFN1_MX) {
+      // W1 rows n0.. then W3 rows n0.. of expert g ([E][2][F] rows of H codes)
+      const int wrow = ti.g * 2 * p.F + ti.n0;
+      tma_load_2d(sB, mb0, bar, kc, wrow);
+      tma_load_2d(sB + kMxTileF1 * 128, mb0, bar, kc, wrow + p.F);
+    } else {
+      // W2 rows (H index) n0.. of expert g ([E][H] rows of F codes)
+      tma_load_2d(sB, mb0, bar, kc, ti.g * p.H + ti.n0);
+    }
+    uint8_t* sSF = sA + kMxSfOff;
+    bulk_load(sSF, p.sfa + (static_cast<size_t>(ti.mt) * p.kb_total + kb) * kMxSfBytes, kMxSfBytes, bar);
+    bulk_load(sSF + kMxSfBytes,
+              p.sfb + ((static_cast<size_t>(ti.g) * p.nt_w + ti.nb) * p.kb_total + kb) * (2 * kMxSfBytes),
+              2 * kMxSfBytes, bar);
+    return;
+  }
   const int kk = kb * kBK;
   if constexpr (KIND == KIND_FFN1) {
     tma_load_2d(sA, ma, bar, kk, ti.m0);
@@ -304,6 +353,7 @@ template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
   if constexpr (KIND == KIND_ROUTER) return 2 * router_stage_bytes(p.bn);        // both CTAs' shares
   else if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
+  else if constexpr (KindTraits<KIND>::kMx) return kMxStageTx;
   else return kABytes + kBBytesMax;
 }
 

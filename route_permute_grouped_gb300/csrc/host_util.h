@@ -37,9 +37,12 @@ cudaError_t launch_router_select(const moe_config& c, const float* raw, int ld, 
                                  float* aux_partials, cudaStream_t st);
 
 // permute.cu
+// With x_q != nullptr the permute writes MXFP8 rows (x_q [R, H] codes and the
+// tile-ready scales sfa, mx_sfa_bytes(R, E, H) bytes) instead of bf16 x_perm.
 cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
                            __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
-                           int32_t* lookback, DevStatus* st, cudaStream_t stream);
+                           int32_t* lookback, DevStatus* st, cudaStream_t stream, uint8_t* x_q = nullptr,
+                           uint8_t* sfa = nullptr);
 
 size_t permute_lookback_ints(int T, int E);
 
@@ -58,5 +61,26 @@ cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const in
 cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
                             cudaStream_t st);
 cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, float* out, cudaStream_t st);
+
+// mx.cu: MXFP8 quantisers and the sizes of the tile-ready scale buffers
+inline int mx_ntiles1(const moe_config& c) { return (c.F + kMxTileF1 - 1) / kMxTileF1; }
+inline int mx_ntiles2(const moe_config& c) { return (c.H + kMxTileN2 - 1) / kMxTileN2; }
+inline size_t mx_sf13_bytes(const moe_config& c) {
+  return static_cast<size_t>(c.E) * mx_ntiles1(c) * (c.H / kMxKB) * 2 * kMxSfBytes;
+}
+inline size_t mx_sf2_bytes(const moe_config& c) {
+  return static_cast<size_t>(c.E) * mx_ntiles2(c) * (c.F / kMxKB) * 2 * kMxSfBytes;
+}
+// scale blocks of the activations of a grouped GEMM with K = `K`: one per
+// (m tile of 128 rows, k block); an expert's rows start a new m tile, so there
+// are at most ceil(R / 128) + E m tiles
+inline size_t mx_sfa_bytes(long long R, int E, int K) {
+  return static_cast<size_t>((R + kBM - 1) / kBM + E) * (K / kMxKB) * kMxSfBytes;
+}
+cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,
+                                    cudaStream_t st);
+cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
+                                       const __nv_bfloat16* W2, uint8_t* w13q, uint8_t* sf13, uint8_t* w2q,
+                                       uint8_t* sf2, cudaStream_t st);
 
 }  // namespace moe

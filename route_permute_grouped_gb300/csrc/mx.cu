@@ -1,0 +1,112 @@
+// MXFP8 quantisers: row-major blocks of a bf16 matrix, and the expert weights
+// transposed to K-major E4M3 with their scales in the tile-ready layout of the
+// FP8 expert GEMMs (see mx.cuh for the format and the scale layout).
+#include "host_util.h"
+#include "mx.cuh"
+
+namespace moe {
+
+// q[M, K] codes and s[M, K/32] scales of x[M, K] (row-major, blocks along K).
+// Thread = one block of 32 elements: four 16-byte loads, two 16-byte stores.
+__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, long long M,
+                                                               int K, uint8_t* __restrict__ q,
+                                                               uint8_t* __restrict__ s) {
+  const int nb = K / kMxBlock;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= M * nb) return;
+  const long long row = i / nb;
+  const int b = static_cast<int>(i - row * nb);
+  const uint4* src = reinterpret_cast<const uint4*>(x + row * K + b * kMxBlock);
+  float v[32];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint4 w = __ldg(src + u);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * u + 2 * j] = bf16_lo(ww[j]);
+      v[8 * u + 2 * j + 1] = bf16_hi(ww[j]);
+    }
+  }
+  uint32_t c[8];
+  s[i] = static_cast<uint8_t>(mx_quant32(v, c));
+  uint4* dst = reinterpret_cast<uint4*>(q + row * K + b * kMxBlock);
+  dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+  dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+}
+
+// Weight W[E][K][N] bf16 (K rows, N contiguous) -> codes Wq (expert e at
+// wq + e * wq_estride, row n of K contiguous codes) and the scale of
+// (e, n, 32-element K block kb32) in expert e's tile-ready scale blocks
+// (sf + e * sf_estride): tile n / tile_n, k block kb32 / 4, B row of the tile
+// b = n % tile_n + row_off (row_off: 0 for W1 and W2, tile_n for W3, whose
+// rows follow W1's in a gate/up tile); every (tile, k block) owns two 512-byte
+// blocks (B rows 0..127, 128..255). Thread = one (e, n, kb32): 32 strided
+// loads (coalesced over n across the warp), one 32-byte store.
+__global__ void __launch_bounds__(256) mx_quantize_weight_kernel(const __nv_bfloat16* __restrict__ w, int E, int K,
+                                                                 int N, uint8_t* __restrict__ wq, size_t wq_estride,
+                                                                 uint8_t* __restrict__ sf, size_t sf_estride,
+                                                                 int tile_n, int row_off) {
+  const int nkb32 = K / kMxBlock;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(E) * nkb32 * N;
+  if (i >= total) return;
+  const int n = static_cast<int>(i % N);
+  const long long r = i / N;
+  const int kb32 = static_cast<int>(r % nkb32);
+  const int e = static_cast<int>(r / nkb32);
+  const __nv_bfloat16* src = w + (static_cast<size_t>(e) * K + static_cast<size_t>(kb32) * kMxBlock) * N + n;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(src[static_cast<size_t>(j) * N]);
+  uint32_t c[8];
+  const uint32_t sb = mx_quant32(v, c);
+  uint4* dst = reinterpret_cast<uint4*>(wq + e * wq_estride + static_cast<size_t>(n) * K +
+                                        static_cast<size_t>(kb32) * kMxBlock);
+  dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+  dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+  const int tile = n / tile_n;
+  const int b = n % tile_n + row_off;  // B row of the tile
+  const size_t blk = static_cast<size_t>(tile) * (K / kMxKB) + kb32 / 4;
+  sf[e * sf_estride + blk * 2 * kMxSfBytes + (b >> 7) * kMxSfBytes + mx_sf_pos(b & 127, kb32 & 3)] =
+      static_cast<uint8_t>(sb);
+}
+
+cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,
+                                    cudaStream_t st) {
+  const long long n = M * (K / kMxBlock);
+  if (n == 0) return cudaSuccess;
+  mx_quantize_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(x, M, K, q, s);
+  return cudaGetLastError();
+}
+
+// W1/W3 [E, H, F] -> w13q [E][2][F][H] (W1 then W3 per expert) and sf13; W2
+// [E, F, H] -> w2q [E][H][F] and sf2. The scale buffers are zeroed first (the
+// unused half of each tile's second scale block stays zero).
+cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
+                                       const __nv_bfloat16* W2, uint8_t* w13q, uint8_t* sf13, uint8_t* w2q,
+                                       uint8_t* sf2, cudaStream_t st) {
+  const int E = c.E, H = c.H, F = c.F;
+  const int nt1 = mx_ntiles1(c), nt2 = mx_ntiles2(c);
+  cudaError_t err = cudaMemsetAsync(sf13, 0, mx_sf13_bytes(c), st);
+  if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(sf2, 0, mx_sf2_bytes(c), st);
+  if (err != cudaSuccess) return err;
+  // W1 and W3 of expert e land in w13q[e][0] and w13q[e][1]
+  const long long n1 = static_cast<long long>(E) * (H / kMxBlock) * F;
+  const size_t sf13_e = static_cast<size_t>(nt1) * (H / kMxKB) * 2 * kMxSfBytes;
+  for (int which = 0; which < 2; ++which) {
+    mx_quantize_weight_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, st>>>(
+        which == 0 ? W1 : W3, E, H, F, w13q + static_cast<size_t>(which) * F * H, 2ull * F * H, sf13, sf13_e,
+        kMxTileF1, which * kMxTileF1);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  const long long n2 = static_cast<long long>(E) * (F / kMxBlock) * H;
+  const size_t sf2_e = static_cast<size_t>(nt2) * (F / kMxKB) * 2 * kMxSfBytes;
+  mx_quantize_weight_kernel<<<static_cast<unsigned>((n2 + 255) / 256), 256, 0, st>>>(
+      W2, E, F, H, w2q, static_cast<size_t>(H) * F, sf2, sf2_e, kMxTileN2, 0);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

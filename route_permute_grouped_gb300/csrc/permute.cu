@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "host_util.h"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -56,16 +57,25 @@ __device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
 // (t,i) is offsets[e] + (rows of e in earlier chunks) + (rank of t among this
 // chunk's tokens routed to e). The earlier-chunk term comes from a decoupled
 // lookback over per-(chunk, expert) words [flag | value].
+//
+// MX: the scattered rows are MXFP8 instead of bf16: each token's row is
+// quantised once (32-element blocks along H) and its codes written to every
+// destination row of x_q; the scale of row r, block j goes to the tile-ready
+// scale block of r's m tile (tile base of its expert + (r - offset) / 128) and
+// k block j / 4 in sfa (row (r - offset) % 128, K step j % 4).
+template <bool MX>
 __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx, int T, int H, int E, int k,
     const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out, int32_t* __restrict__ lookback,
     __nv_bfloat16* __restrict__ x_perm, int32_t* __restrict__ row_id_map, DevStatus* st,
-    unsigned long long limit_ns, int fault) {
+    unsigned long long limit_ns, int fault, uint8_t* __restrict__ x_q, uint8_t* __restrict__ sfa) {
   __shared__ int s_ticket;
   __shared__ uint32_t s_mask[2][256];
   __shared__ int s_base[256];
   __shared__ int s_scan[256];
+  __shared__ int s_tscan[MX ? 256 : 1];
   __shared__ int s_rows[kChunk * 16];
+  __shared__ int s_exp[MX ? kChunk * 16 : 1];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int32_t* ticket_ctr = lookback;  // lookback[0] is the chunk ticket counter
   int32_t* flags = lookback + 64;  // [nchunks][E]
@@ -77,11 +87,14 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
   // exclusive scan of the global counts (E <= 256): offsets of the experts
   const int cnt = (tid < E) ? counts[tid] : 0;
   s_scan[tid] = cnt;
+  if (MX) s_tscan[tid] = (cnt + kBM - 1) / kBM;  // m tiles of 128 rows per expert
   __syncthreads();
   for (int d = 1; d < 256; d <<= 1) {
     const int v = (tid >= d) ? s_scan[tid - d] : 0;
+    const int vt = (MX && tid >= d) ? s_tscan[tid - d] : 0;
     __syncthreads();
     s_scan[tid] += v;
+    if (MX) s_tscan[tid] += vt;
     __syncthreads();
   }
   const int b = s_ticket;
@@ -156,10 +169,48 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
         }
         row_id_map[static_cast<size_t>(t) * k + i] = r;
         s_rows[(warp * 32 + lane) * k + i] = r;
+        if (MX) s_exp[(warp * 32 + lane) * k + i] = e;
       }
     }
   }
   __syncthreads();
+  if constexpr (MX) {
+    // quantise and scatter: warp w takes tokens w, w+8, ...; lane l the
+    // 32-element blocks l, l+32, ... of the row (64 contiguous bytes each)
+    const int nblk = H / kMxBlock, nkb = H / kMxKB;
+    for (int j = warp; j < kChunk; j += kScanThreads / 32) {
+      const int t = t0 + j;
+      if (t >= T) break;
+      for (int b = lane; b < nblk; b += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + b * kMxBlock);
+        float v[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 w = __ldg(src + u);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            v[8 * u + 2 * q] = bf16_lo(ww[q]);
+            v[8 * u + 2 * q + 1] = bf16_hi(ww[q]);
+          }
+        }
+        uint32_t c[8];
+        const uint8_t sb = static_cast<uint8_t>(mx_quant32(v, c));
+        for (int i = 0; i < k; ++i) {
+          const int r = s_rows[j * k + i];
+          if (r < 0) continue;
+          uint4* dst = reinterpret_cast<uint4*>(x_q + static_cast<size_t>(r) * H + b * kMxBlock);
+          dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+          dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+          const int e = s_exp[j * k + i];
+          const int rel = r - (e == 0 ? 0 : s_scan[e - 1]);
+          const int mt = (e == 0 ? 0 : s_tscan[e - 1]) + rel / kBM;
+          sfa[(static_cast<size_t>(mt) * nkb + b / 4) * kMxSfBytes + mx_sf_pos(rel % kBM, b & 3)] = sb;
+        }
+      }
+    }
+    return;
+  }
   // scatter: warp w copies tokens w, w+8, ... of the chunk; 16-byte vectors
   const int nvec = H / 8;
   for (int j = warp; j < kChunk; j += kScanThreads / 32) {
@@ -189,7 +240,7 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
 
 cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
                            __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
-                           int32_t* lookback, DevStatus* st, cudaStream_t stream) {
+                           int32_t* lookback, DevStatus* st, cudaStream_t stream, uint8_t* x_q, uint8_t* sfa) {
   const int T = c.T, E = c.E, k = c.k;
   const int nchunks = (T + kChunk - 1) / kChunk;
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
@@ -203,9 +254,19 @@ cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const in
   permute_hist_kernel<<<hb, 256, 0, stream>>>(topk_idx, n, E, counts, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  permute_scan_scatter_kernel<<<nchunks, kScanThreads, 0, stream>>>(x, topk_idx, T, c.H, E, k, counts, offsets,
-                                                                    lookback, x_perm, row_id_map, st,
-                                                                    wait_limit_ns(), debug_fault());
+  if (x_q != nullptr) {
+    // scale blocks of rows past an expert's count (the tail of its last m
+    // tile) are not written by the scatter: zero scales
+    e = cudaMemsetAsync(sfa, 0, mx_sfa_bytes(T * k, E, c.H), stream);
+    if (e != cudaSuccess) return e;
+    permute_scan_scatter_kernel<true><<<nchunks, kScanThreads, 0, stream>>>(
+        x, topk_idx, T, c.H, E, k, counts, offsets, lookback, x_perm, row_id_map, st, wait_limit_ns(),
+        debug_fault(), x_q, sfa);
+  } else {
+    permute_scan_scatter_kernel<false><<<nchunks, kScanThreads, 0, stream>>>(
+        x, topk_idx, T, c.H, E, k, counts, offsets, lookback, x_perm, row_id_map, st, wait_limit_ns(),
+        debug_fault(), nullptr, nullptr);
+  }
   return cudaGetLastError();
 }
 

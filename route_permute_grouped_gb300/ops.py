@@ -87,6 +87,16 @@ def lib():
         L.moe_profile_read.restype = c_int
         L.moe_debug_launch_count.argtypes = []
         L.moe_debug_launch_count.restype = ctypes.c_ulonglong
+        L.moe_mx_weight_bytes.restype = c_size_t
+        L.moe_mx_weight_bytes.argtypes = [POINTER(MoeConfig), c_int]
+        L.moe_mx_workspace_bytes.restype = c_size_t
+        L.moe_mx_workspace_bytes.argtypes = [POINTER(MoeConfig)]
+        L.moe_mx_quantize_weights.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeMxWeights), vp]
+        L.moe_mx_quantize.argtypes = [vp, c_longlong, c_int, vp, vp, vp]
+        L.moe_layer_fwd_mxfp8.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, POINTER(MoeMxWeights), vp, vp, vp, vp,
+                                          vp, c_size_t, vp]
+        for n in ("moe_mx_quantize_weights", "moe_mx_quantize", "moe_layer_fwd_mxfp8"):
+            getattr(L, n).restype = c_int
         _lib = L
     return _lib
 
@@ -298,3 +308,70 @@ def layer_bwd(cfg, dO, x, router_w, W1, W3, W2, saved, ws=None, grads=None):
                              _p(g["aux_loss"]), _p(ws), ws.numel(), _stream())
     _check(st, "moe_layer_bwd")
     return g
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 expert GEMMs (forward)
+# ---------------------------------------------------------------------------
+class MoeMxWeights(ctypes.Structure):
+    """Mirror of moe_mx_weights (four device pointers)."""
+    _fields_ = [("w13", c_void_p), ("sf13", c_void_p), ("w2", c_void_p), ("sf2", c_void_p)]
+
+
+MX_WEIGHT_FIELDS = ("w13", "sf13", "w2", "sf2")
+
+
+def mx_quantize_weights(cfg, W1, W3, W2):
+    """Quantise the bf16 expert weights into new uint8 device tensors (dict
+    with keys w13 [E,2,F,H], sf13, w2 [E,H,F], sf2)."""
+    dev = W1.device
+    out = {}
+    for i, n in enumerate(MX_WEIGHT_FIELDS):
+        nb = int(lib().moe_mx_weight_bytes(ctypes.byref(cfg), i))
+        if nb == 0:
+            raise MoeError(2, "moe_mx_weight_bytes")
+        out[n] = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out["w13"] = out["w13"].view(cfg.E, 2, cfg.F, cfg.H)
+    out["w2"] = out["w2"].view(cfg.E, cfg.H, cfg.F)
+    st = lib().moe_mx_quantize_weights(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2), ctypes.byref(_mx_struct(out)),
+                                       _stream())
+    _check(st, "moe_mx_quantize_weights")
+    return out
+
+
+def _mx_struct(w):
+    return MoeMxWeights(*[w[n].data_ptr() for n in MX_WEIGHT_FIELDS])
+
+
+def mx_quantize(x):
+    """Row-major MXFP8 quantisation of a bf16 [M, K] tensor: (codes uint8
+    [M, K], scales uint8 [M, K/32])."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((M, K // 32), dtype=torch.uint8, device=x.device)
+    _check(lib().moe_mx_quantize(_p(x), M, K, _p(q), _p(s), _stream()), "moe_mx_quantize")
+    return q, s
+
+
+def mx_workspace(cfg, device="cuda"):
+    n = int(lib().moe_mx_workspace_bytes(ctypes.byref(cfg)))
+    if n == 0:
+        raise MoeError(2, "moe_mx_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def layer_fwd_mxfp8(cfg, x, router_w, mxw, expert_bias=None, logit_bias=None, Ws=None, ws=None, y=None):
+    """Whole layer forward with MXFP8 expert GEMMs (``mxw`` from
+    mx_quantize_weights)."""
+    dev = x.device
+    if y is None:
+        y = torch.empty((cfg.T, cfg.H), dtype=_out_dtype(cfg), device=dev)
+    ws = mx_workspace(cfg, dev) if ws is None else ws
+    Ws1, Ws3, Ws2 = Ws if Ws is not None else (None, None, None)
+    st = lib().moe_layer_fwd_mxfp8(ctypes.byref(cfg), _p(x), _p(router_w), _p(expert_bias), _p(logit_bias),
+                                   ctypes.byref(_mx_struct(mxw)), _p(Ws1), _p(Ws3), _p(Ws2), _p(y), _p(ws),
+                                   ws.numel(), _stream())
+    _check(st, "moe_layer_fwd_mxfp8")
+    return y
