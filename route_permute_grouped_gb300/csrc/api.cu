@@ -113,9 +113,10 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
 }
 
 // 2-D map over a row-major [outer, inner] array of bytes (E4M3 codes), box
-// {box_inner, box_outer}, 128-byte swizzle, zero fill outside the array.
+// {box_inner, box_outer}, 128-byte swizzle (or none: scale blocks as rows of
+// 256 bytes), zero fill outside the array.
 static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                        uint32_t box_outer) {
+                        uint32_t box_outer, bool swizzle = true) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -123,8 +124,8 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -360,7 +361,8 @@ static int check_mx_shape(const moe_config& c) {
 }
 
 // MXFP8 grouped SwiGLU FFN over the permuted rows: a = SiLU(Q(x) Q(W1)) * (Q(x)
-// Q(W3)) quantised in the epilogue, y_perm = Q(a) Q(W2).
+// Q(W3)) quantised in the epilogue, y_perm = Q(a) Q(W2). Scale blocks are read
+// as rows of 256 bytes (A: 2 per block, B: 4 per tile's pair of blocks).
 static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const uint8_t* x_q, const uint8_t* sfa1,
                       const moe_mx_weights& w, uint8_t* a_q, uint8_t* sfa2, void* y, bool y_fp32, DevStatus* st,
                       cudaStream_t s) {
@@ -374,13 +376,13 @@ static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const 
   p.nt_w = mx_ntiles1(c);
   p.kb_total = c.H / kMxKB;
   p.out0 = a_q;
-  p.sfa = sfa1;
-  p.sfb = w.sf13;
   p.sfa_out = sfa2;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, msa, msb;
   if (!make_map_u8(&ma, x_q, c.H, R, kMxKB, kBM)) return MOE_ERR_CUDA;
   if (!make_map_u8(&mb, w.w13, c.H, 2ull * c.E * c.F, kMxKB, kMxTileF1)) return MOE_ERR_CUDA;
-  MOE_CUDA(launch_gemm(KIND_FFN1_MX, p, ma, mb, mb, num_sms(), s, nullptr));
+  if (!make_map_u8(&msa, sfa1, 256, mx_sfa_bytes(R, c.E, c.H) / 256, 256, 2, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb, w.sf13, 256, mx_sf13_bytes(c) / 256, 256, 4, false)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_gemm(KIND_FFN1_MX, p, ma, mb, msa, num_sms(), s, nullptr, &msb));
   stage_done(s, STAGE_FFN1, 1);
   GemmParams q = base_params(c, st);
   q.F = c.F;
@@ -393,13 +395,13 @@ static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const 
   q.kb_total = c.F / kMxKB;
   q.out0 = y;
   q.out_fp32 = y_fp32;
-  q.sfa = sfa2;
-  q.sfb = w.sf2;
-  CUtensorMap ma2, mb2, oy;
+  CUtensorMap ma2, mb2, msa2, msb2, oy;
   if (!make_map_u8(&ma2, a_q, c.F, R, kMxKB, kBM)) return MOE_ERR_CUDA;
-  if (!make_map_u8(&mb2, w.w2, c.F, static_cast<uint64_t>(c.E) * c.H, kMxKB, kMxTileN2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb2, w.w2, c.F, static_cast<uint64_t>(c.E) * c.H, kMxKB, kMxBN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msa2, sfa2, 256, mx_sfa_bytes(R, c.E, c.F) / 256, 256, 2, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb2, w.sf2, 256, mx_sf2_bytes(c) / 256, 256, 4, false)) return MOE_ERR_CUDA;
   if (!make_map_store(&oy, y, c.H, R, y_fp32)) return MOE_ERR_CUDA;
-  MOE_CUDA(launch_gemm(KIND_FFN2_MX, q, ma2, mb2, mb2, num_sms(), s, &oy));
+  MOE_CUDA(launch_gemm(KIND_FFN2_MX, q, ma2, mb2, msa2, num_sms(), s, &oy, &msb2));
   stage_done(s, STAGE_FFN2, 1);
   return MOE_OK;
 }

@@ -294,6 +294,24 @@ __device__ __forceinline__ void umma_mx_w(uint32_t d_tmem, uint32_t a_lo, uint32
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
+// CTA-pair forms: the even CTA issues them; each CTA's scale cells come from
+// its own shared memory at the same offset (cp), and the M=256 MMA reads each
+// CTA's cells for its own 128 rows and the B scales replicated in both.
+__device__ __forceinline__ void umma2_mx_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi,
+                                           uint32_t idesc, uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], da, db, %4, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_cp2_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
 // Bulk copy global -> shared (16-byte aligned, size a multiple of 16),
 // completing on an mbarrier's transaction count.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -121,38 +121,37 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
   }
 }
 
-// MXFP8 gate/up epilogue, thread = row r of the tile: for each 32-column block
-// of the tile's 96 F columns a = SiLU(h1) h3 (h1 from accumulator columns
-// 32 b.., h3 from 96 + 32 b..) is quantised as one MXFP8 block of the down
-// GEMM's K: codes to a_q[row, col..] (rows of this expert only) and the scale
-// to the down GEMM's tile-ready A scale block of this m tile (every row of the
-// tile, so rows past the expert carry a valid scale too).
-__device__ __forceinline__ void epi_ffn1_mx(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
+// MXFP8 gate/up epilogue, thread = row r of this CTA's 128 rows of the pair
+// tile, block b (0..2) of the tile's 96 F columns: a = SiLU(h1) h3 (h1 from
+// accumulator columns 32 b.., h3 from 96 + 32 b..) is quantised as one MXFP8
+// block of the down GEMM's K: codes to a_q[row, col..] (rows of this expert
+// only) and the scale to the down GEMM's A scale block 2 * pair tile + rank
+// (every row of the tile, so rows past the expert carry a valid scale).
+__device__ __forceinline__ void epi_ffn1_mx(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r,
+                                            int rank, int b) {
+  const int col = ti.n0 + 32 * b;
+  if (col >= p.F) return;  // uniform: the last tile of a ragged F
   const int row = ti.m0 + r;
-  const bool valid = row < ti.m_end;
-  uint8_t* aq = reinterpret_cast<uint8_t*>(p.out0);
-  const int nkb2 = p.F / kMxKB;
-#pragma unroll 1
-  for (int b = 0; b < kMxTileF1 / 32; ++b) {
-    const int col = ti.n0 + 32 * b;
-    if (col >= p.F) break;  // uniform: the last tile of a ragged F
-    float h1[32], h3[32];
-    tmem_ld32f(tacc + 32 * b, h1);
-    tmem_ld32f(tacc + kMxTileF1 + 32 * b, h3);
-    float a[32];
+  uint32_t v1[32], v3[32];
+  tmem_ld32(tacc + 32 * b, v1);
+  tmem_ld32(tacc + kMxTileF1 + 32 * b, v3);
+  tmem_ld_wait();
+  float a[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) a[j] = silu_f(h1[j]) * h3[j];
-    uint32_t w[8];
-    const uint32_t sb = mx_quant32(a, w);
-    if (valid) {
-      uint4* d = reinterpret_cast<uint4*>(aq + static_cast<size_t>(row) * p.F + col);
-      d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-    const int fb = col / 32;
-    p.sfa_out[(static_cast<size_t>(ti.mt) * nkb2 + fb / 4) * kMxSfBytes + mx_sf_pos(r, fb & 3)] =
-        static_cast<uint8_t>(sb);
+  for (int j = 0; j < 32; ++j) {
+    const float h1 = __uint_as_float(v1[j]);
+    a[j] = __fdividef(h1, 1.0f + __expf(-h1)) * __uint_as_float(v3[j]);
   }
+  uint32_t w[8];
+  const uint32_t sb = mx_quant32(a, w);
+  if (row < ti.m_end) {
+    uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out0) + static_cast<size_t>(row) * p.F + col);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  const int fb = col / 32;
+  p.sfa_out[(static_cast<size_t>(2 * ti.mt + rank) * (p.F / kMxKB) + fb / 4) * kMxSfBytes + mx_sf_pos(r, fb & 3)] =
+      static_cast<uint8_t>(sb);
 }
 
 // DGRAD2: accumulator = da for F columns n0..n0+255; SwiGLU backward with the
@@ -347,7 +346,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
               // transaction count goes below zero meanwhile)
               if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
               issue_loads_pair<KIND>(p, ti, kbp, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
-                                     &mb0, &mb1);
+                                     &mb0, &mb1, nullptr, &mo1);
             }
             issued_phase[stage] = static_cast<int>(phase);
             if (++stage == NST) { stage = 0; phase ^= 1u; }
@@ -381,7 +380,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = TR::kMx ? idesc_mxf8_f32(kBM, kMxBN) : idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
+    const uint32_t idesc =
+        TR::kMx ? idesc_mxf8_f32(TR::kTileM, kMxBN) : idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
     // MXFP8: descriptors of the stage's scale blocks (32 rows of 16 bytes,
     // no swizzle, 8-row groups 128 bytes apart) for the copies into TMEM
     const uint32_t sf_lo0 = sdesc_lo(smem_u32(smem) + kMxSfOff, 128);
@@ -452,7 +452,49 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
-      for (int kb = 0; kb < ti.nkb; ++kb) {
+      if constexpr (TR::kMx) {
+        // MXFP8: the scale copy of k block kb+1 (into the other of two scale
+        // regions) is issued before the MMAs of block kb, so no MMA waits for
+        // the copy its scales come from (a copy takes about as long as a
+        // quarter of a block's MMAs); region r holds the scales of the blocks
+        // kb with kb % 2 == r
+        auto copy_scales = [&](int st_, uint32_t region) {
+          const uint32_t sf_lo = sf_lo0 + static_cast<uint32_t>(st_) * stage_lo;
+          const uint32_t col = region * kMxSfRegion;
+          tmem_cp2_32x128b_x4(tmem_base + kMxSfaCol + col, sf_hi | sf_lo);
+          tmem_cp2_32x128b_x4(tmem_base + kMxSfbCol + col, sf_hi | (sf_lo + (kMxSfBytes >> 4)));
+          tmem_cp2_32x128b_x4(tmem_base + kMxSfbCol + 4 + col, sf_hi | (sf_lo + (2 * kMxSfBytes >> 4)));
+        };
+        if (ti.nkb > 0) {
+          if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) copy_scales(stage, 0u);
+          __syncwarp();
+        }
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          const int cur = stage;
+          const uint32_t region = static_cast<uint32_t>(kb & 1);
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+          if (kb + 1 < ti.nkb) {
+            if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) copy_scales(stage, region ^ 1u);
+          }
+          if (lane == 0) {
+            const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(cur) * stage_lo;
+            const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cur) * stage_lo;
+            const uint32_t col = region * kMxSfRegion;
+#pragma unroll
+            for (int kk = 0; kk < kMxKB / 32; ++kk)
+              umma2_mx_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi,
+                         idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
+                         tmem_base + kMxSfaCol + col, tmem_base + kMxSfbCol + col, (kb > 0 || kk > 0) ? 1u : 0u);
+            umma2_commit_mc(empty + cur, 3);  // frees the stage in both CTAs
+          }
+          __syncwarp();
+        }
+      }
+      for (int kb = 0; kb < (TR::kMx ? 0 : ti.nkb); ++kb) {
         if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
         tc_fence_after();
         if constexpr (KIND == KIND_WGRAD) {
@@ -491,23 +533,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           }
           __syncwarp();
         }
-        if (TR::kMx && lane == 0) {
-          // scales of this k block into TMEM (in issue order with the MMAs,
-          // after the previous block's MMAs), then four K=32 steps, step kk
-          // taking byte kk of the scale cells
-          const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
-          const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
-          const uint32_t sf_lo = sf_lo0 + static_cast<uint32_t>(stage) * stage_lo;
-          tmem_cp_32x128b_x4(tmem_base + kMxSfaCol, sf_hi | sf_lo);
-          tmem_cp_32x128b_x4(tmem_base + kMxSfbCol, sf_hi | (sf_lo + (kMxSfBytes >> 4)));
-          tmem_cp_32x128b_x4(tmem_base + kMxSfbCol + 4, sf_hi | (sf_lo + (2 * kMxSfBytes >> 4)));
-#pragma unroll
-          for (int kk = 0; kk < kMxKB / 32; ++kk)
-            umma_mx_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi,
-                      idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
-                      tmem_base + kMxSfaCol, tmem_base + kMxSfbCol, (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(empty + stage);
-        } else if (lane == 0) {
+        if (lane == 0) {
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
 #pragma unroll
@@ -574,7 +600,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
         }
       } else if constexpr (KIND == KIND_FFN1_MX) {
-        epi_ffn1_mx(p, ti, tacc, r);
+        epi_ffn1_mx(p, ti, tacc, r, rank, part);
       } else if constexpr (KIND == KIND_FFN2_MX) {
         if (full_rows) {
           if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0, kMxBN / 64);

@@ -48,8 +48,8 @@ enum GemmKind : int {
   KIND_DGRAD2R = 8,    // DGRAD2 of the memory-saving backward: also stores a = SiLU(h1) h3 recomputed from
                        // h13 and the per-row partials of the gate gradient <da, a> over each 256-column tile
   KIND_FFN1_MX = 9,    // MXFP8 gate/up: h = Q(x_perm) [Q(W1_e) | Q(W3_e)] -> a = SiLU(h1) h3, stored as MXFP8
-                       // (codes + the down GEMM's tile-ready scales); tiles of 96 gate + 96 up columns
-  KIND_FFN2_MX = 10,   // MXFP8 down: y_perm = Q(a) Q(W2_e), bf16 out; tiles of 192 columns
+                       // (codes + the down GEMM's tile-ready scales); 256 x (96 gate + 96 up) pair tiles
+  KIND_FFN2_MX = 10,   // MXFP8 down: y_perm = Q(a) Q(W2_e), bf16 out; 256 x 192 pair tiles
 };
 
 constexpr int kBM = 128;
@@ -61,14 +61,17 @@ constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kRingBytes = 4 * kStageBytes;  // shared memory of the operand stage ring
 constexpr int kMaxGroups = 256;
 constexpr int kTmemCols = 512;
-// MXFP8 stage: A 16 KB at 0, B (192 rows x 128 B) at 16 KB, scale blocks of A
-// (512 B) and B (1 KB) at 40 KB; 42 KB keeps every stage 1024-byte aligned
-constexpr int kMxSfOff = 40960;
-constexpr int kMxStageBytes = 43008;
-constexpr uint32_t kMxStageTx = 16384 + kMxBN * 128 + 3 * kMxSfBytes;
-// TMEM columns of the scale cells (past both 192-column accumulators)
+// MXFP8 pair stage (per CTA): A 16 KB at 0, B (96 rows x 128 B) at 16 KB, scale
+// blocks of A (512 B) and B (1 KB) at 28 KB; 31 KB keeps every stage
+// 1024-byte aligned
+constexpr int kMxSfOff = 28672;
+constexpr int kMxStageBytes = 31744;
+constexpr uint32_t kMxStageTx = 16384 + (kMxBN / 2) * 128 + 3 * kMxSfBytes;  // one CTA's share
+// TMEM columns of the scale cells (past both 192-column accumulators): two
+// regions of 12 columns (A: 4, B: 8), alternating per k block
 constexpr uint32_t kMxSfaCol = 448;
 constexpr uint32_t kMxSfbCol = 452;
+constexpr uint32_t kMxSfRegion = 12;
 constexpr int kAccStride = 256;           // TMEM column distance of the two accumulators
 
 template <int KIND>
@@ -78,12 +81,13 @@ struct KindTraits {
                                 KIND == KIND_ROUTER_DX || KIND == KIND_ROUTER_DW);
   // CTA pairs: the expert GEMMs with a fixed K run as M=256 tiles on two SMs
   // (cta_group::2); each CTA stages its own 128 rows of A and half of B
-  // MXFP8 kinds: one CTA per 128 x 192 tile; a stage holds 128 k elements (one
-  // byte each) of A (16 KB) and B (24 KB) and their scale blocks (0.5 + 1 KB)
+  // MXFP8 kinds: CTA pairs on 256 x 192 tiles; a CTA's stage holds 128 k
+  // elements (one byte each) of its 128 A rows (16 KB) and 96 B rows (12 KB),
+  // its A scale block (0.5 KB) and the tile's B scale blocks (1 KB)
   static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX);
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
                                  KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R ||
-                                 KIND == KIND_ROUTER);
+                                 KIND == KIND_ROUTER || kMx);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
@@ -91,10 +95,14 @@ struct KindTraits {
   // DGRAD2 runs eight epilogue warps (two per TMEM lane quadrant, each taking
   // half of the tile's columns) to hide the latency of its loads of the saved
   // pre-activations; it and DGRAD2R (third staging box) give up one stage
-  static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : 4;
+  // FFN1_MX runs twelve (three per TMEM lane quadrant, one 32-column block of
+  // the 96 SwiGLU columns each): its tiles are short (K / 128 blocks of
+  // 128) and its epilogue (SiLU, quantisation) long
+  static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX) ? 12 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
   static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2) ? 5 : (kPair ? 6 : 4);  // MX: 4
-  static constexpr int kOutWarpBytes = (KIND == KIND_DGRAD2R) ? 3 * 4096 : 2 * 4096;  // epilogue staging
+  static constexpr int kOutWarpBytes =
+      (KIND == KIND_DGRAD2R) ? 3 * 4096 : (KIND == KIND_FFN1_MX) ? 0 : 2 * 4096;  // epilogue staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
@@ -124,11 +132,9 @@ struct GemmParams {
   float* dg_part;        // DGRAD2R: gate-gradient partials [rows, n_part] (DGRAD2R also stores a in out1)
   int n_part;            // DGRAD2R: 256-column tiles of F
   int out_fp32;          // FFN2: y_perm fp32
-  // MXFP8 kinds: tile-ready scale blocks of A (per global m tile and k block)
-  // and B (per expert, n tile and k block); FFN1_MX writes the down GEMM's A
-  // scales to sfa_out; nt_w = n tiles per expert of the weight scales
-  const uint8_t* sfa;
-  const uint8_t* sfb;
+  // MXFP8 kinds: the activations' scale blocks are read through a tensor map;
+  // FFN1_MX writes the down GEMM's A scale blocks to sfa_out; nt_w = n tiles
+  // per expert of the weight scales (the weight scales: map msfb)
   uint8_t* sfa_out;
   int nt_w;
   // status
@@ -210,7 +216,27 @@ template <int KIND>
 __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const TileInfo& ti, int kb, int rank,
                                                  uint8_t* sA, uint8_t* sB, uint32_t bar_cluster, const CUtensorMap* ma,
                                                  const CUtensorMap* mb0, const CUtensorMap* mb1,
-                                                 uint64_t* local_bar = nullptr) {
+                                                 uint64_t* local_bar = nullptr, const CUtensorMap* msfb = nullptr) {
+  if constexpr (KindTraits<KIND>::kMx) {
+    // 128 k elements (bytes) of this CTA's 128 A rows and its 96 B rows, its A
+    // scale block (block 2 * pair tile + rank of the activations' scales: map
+    // mb1, 256-byte rows) and the tile's two B scale blocks (map msfb)
+    const int kc = kb * kMxKB;
+    tma_load_2d_pair(sA, ma, bar_cluster, kc, ti.m0);
+    if constexpr (KIND == KIND_FFN1_MX) {
+      // W1 rows n0.. (even CTA) or W3 rows n0.. (odd CTA) of expert g
+      tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * 2 * p.F + rank * p.F + ti.n0);
+    } else {
+      // W2 rows (H index) n0 + 96 rank .. of expert g
+      tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * p.H + ti.n0 + rank * (kMxBN / 2));
+    }
+    uint8_t* sSF = sA + kMxSfOff;
+    const int ablk = (2 * ti.mt + rank) * p.kb_total + kb;
+    tma_load_2d_pair(sSF, mb1, bar_cluster, 0, 2 * ablk);
+    const int bblk = (ti.g * p.nt_w + ti.nb) * p.kb_total + kb;
+    tma_load_2d_pair(sSF + kMxSfBytes, msfb, bar_cluster, 0, 4 * bblk);
+    return;
+  }
   const int kk = kb * kBK;
   if constexpr (KIND == KIND_ROUTER) {
     // 128 token rows of x; router-weight rows rank * bn/2 .. (box of bn/2 rows)
@@ -259,27 +285,6 @@ template <int KIND>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& ti, int kb, uint8_t* sA,
                                             uint8_t* sB, uint64_t* bar, const CUtensorMap* ma,
                                             const CUtensorMap* mb0, const CUtensorMap* mb1) {
-  if constexpr (KindTraits<KIND>::kMx) {
-    // 128 k elements (bytes) of the tile's A rows and B rows, and the scale
-    // blocks of both (A: global m tile; B: expert, n tile)
-    const int kc = kb * kMxKB;
-    tma_load_2d(sA, ma, bar, kc, ti.m0);
-    if constexpr (KIND == KIND_FFN1_MX) {
-      // W1 rows n0.. then W3 rows n0.. of expert g ([E][2][F] rows of H codes)
-      const int wrow = ti.g * 2 * p.F + ti.n0;
-      tma_load_2d(sB, mb0, bar, kc, wrow);
-      tma_load_2d(sB + kMxTileF1 * 128, mb0, bar, kc, wrow + p.F);
-    } else {
-      // W2 rows (H index) n0.. of expert g ([E][H] rows of F codes)
-      tma_load_2d(sB, mb0, bar, kc, ti.g * p.H + ti.n0);
-    }
-    uint8_t* sSF = sA + kMxSfOff;
-    bulk_load(sSF, p.sfa + (static_cast<size_t>(ti.mt) * p.kb_total + kb) * kMxSfBytes, kMxSfBytes, bar);
-    bulk_load(sSF + kMxSfBytes,
-              p.sfb + ((static_cast<size_t>(ti.g) * p.nt_w + ti.nb) * p.kb_total + kb) * (2 * kMxSfBytes),
-              2 * kMxSfBytes, bar);
-    return;
-  }
   const int kk = kb * kBK;
   if constexpr (KIND == KIND_FFN1) {
     tma_load_2d(sA, ma, bar, kk, ti.m0);
@@ -351,9 +356,9 @@ __host__ __device__ __forceinline__ int router_stages(int bn) {
 
 template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
-  if constexpr (KIND == KIND_ROUTER) return 2 * router_stage_bytes(p.bn);        // both CTAs' shares
+  if constexpr (KindTraits<KIND>::kMx) return 2 * kMxStageTx;                    // both CTAs' shares
+  else if constexpr (KIND == KIND_ROUTER) return 2 * router_stage_bytes(p.bn);   // both CTAs' shares
   else if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
-  else if constexpr (KindTraits<KIND>::kMx) return kMxStageTx;
   else return kABytes + kBBytesMax;
 }
 

@@ -71,11 +71,11 @@ inline size_t mx_sf13_bytes(const moe_config& c) {
 inline size_t mx_sf2_bytes(const moe_config& c) {
   return static_cast<size_t>(c.E) * mx_ntiles2(c) * (c.F / kMxKB) * 2 * kMxSfBytes;
 }
-// scale blocks of the activations of a grouped GEMM with K = `K`: one per
-// (m tile of 128 rows, k block); an expert's rows start a new m tile, so there
-// are at most ceil(R / 128) + E m tiles
+// scale blocks of the activations of a grouped GEMM with K = `K`: two per
+// (256-row pair tile, k block); an expert's rows start a new pair tile, so
+// there are at most ceil(R / 256) + E pair tiles
 inline size_t mx_sfa_bytes(long long R, int E, int K) {
-  return static_cast<size_t>((R + kBM - 1) / kBM + E) * (K / kMxKB) * kMxSfBytes;
+  return 2 * static_cast<size_t>((R + 2 * kBM - 1) / (2 * kBM) + E) * (K / kMxKB) * kMxSfBytes;
 }
 cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,
                                     cudaStream_t st);

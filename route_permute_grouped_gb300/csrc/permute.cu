@@ -60,9 +60,10 @@ __device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
 //
 // MX: the scattered rows are MXFP8 instead of bf16: each token's row is
 // quantised once (32-element blocks along H) and its codes written to every
-// destination row of x_q; the scale of row r, block j goes to the tile-ready
-// scale block of r's m tile (tile base of its expert + (r - offset) / 128) and
-// k block j / 4 in sfa (row (r - offset) % 128, K step j % 4).
+// destination row of x_q; the scale of row r (rel = r - offset of its expert),
+// block j goes to scale block 2 P + h, P = the expert's first 256-row pair tile
+// + rel / 256, h = (rel / 128) % 2, k block j / 4 in sfa (row rel % 128, K
+// step j % 4): the blocks the CTA pairs of the expert GEMM read.
 template <bool MX>
 __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx, int T, int H, int E, int k,
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
   // exclusive scan of the global counts (E <= 256): offsets of the experts
   const int cnt = (tid < E) ? counts[tid] : 0;
   s_scan[tid] = cnt;
-  if (MX) s_tscan[tid] = (cnt + kBM - 1) / kBM;  // m tiles of 128 rows per expert
+  if (MX) s_tscan[tid] = (cnt + 2 * kBM - 1) / (2 * kBM);  // 256-row pair tiles per expert
   __syncthreads();
   for (int d = 1; d < 256; d <<= 1) {
     const int v = (tid >= d) ? s_scan[tid - d] : 0;
@@ -204,8 +205,8 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
           dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
           const int e = s_exp[j * k + i];
           const int rel = r - (e == 0 ? 0 : s_scan[e - 1]);
-          const int mt = (e == 0 ? 0 : s_tscan[e - 1]) + rel / kBM;
-          sfa[(static_cast<size_t>(mt) * nkb + b / 4) * kMxSfBytes + mx_sf_pos(rel % kBM, b & 3)] = sb;
+          const int blk = 2 * ((e == 0 ? 0 : s_tscan[e - 1]) + rel / (2 * kBM)) + ((rel / kBM) & 1);
+          sfa[(static_cast<size_t>(blk) * nkb + b / 4) * kMxSfBytes + mx_sf_pos(rel % kBM, b & 3)] = sb;
         }
       }
     }
