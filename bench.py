@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay timing")
     ap.add_argument("--force-balanced", action="store_true", help="force-balanced routing (cyclic assignment)")
+    ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
     ap.add_argument("--recompute", action="store_true",
                     help="memory-saving training step (a and y_perm not kept; recomputed in the backward)")
     return ap.parse_args()
@@ -406,8 +407,57 @@ def run_ours(args, ls, rank, world, local_rank):
         graph = {"value": round(job_throughput(layer_flops(ls, training), ms_graph, world), 2), "unit": "TFLOPS",
                  "ms_per_step": round(ms_graph, 4)}
 
-    # ---------------- per-stage table and roofline of the dominant kernel
+    # ---------------- the forward with MXFP8 expert GEMMs (same inputs; the
+    # weights quantised once, outside the timed region, as a trained model's
+    # would be)
     peaks = load_peaks()
+    mx = None
+    if not args.no_mxfp8 and ls.H % 128 == 0 and ls.F % 128 == 0:
+        mxw = ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"])
+        wsm = ops.mx_workspace(cfg, dev)
+        ym = torch.empty_like(y)
+
+        def fwd_mx():
+            ops.layer_fwd_mxfp8(cfg, d["x"], d["router_w"], mxw, d["expert_bias"], d["logit_bias"], Ws=Ws, ws=wsm,
+                                y=ym)
+
+        for _ in range(max(3, args.warmup)):
+            fwd_mx()
+        barrier()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ops.profile_start(args.steps * 8 + 8)
+        m0.record()
+        for _ in range(args.steps):
+            fwd_mx()
+        m1.record()
+        torch.cuda.synchronize()
+        ops.profile_stop()
+        assert ops.device_status(wsm) == 0
+        ms_mx = max_over_ranks(m0.elapsed_time(m1) / args.steps, world, dev)
+        mx_stages = {}
+        for name, t in ops.profile_read(args.steps * 8 + 8):
+            mx_stages.setdefault(name, []).append(t)
+        # FP8 dense peak: the measured sustained bf16 peak times the nominal
+        # fp8 : bf16 ratio of the tensor cores (2)
+        peak8 = 2 * peaks["bf16_tflops_sustained"]
+        R = ls.T * ls.k
+        mk = {}
+        for name, fl in (("ffn1_gate_up", 2 * R * ls.H * 2 * ls.F), ("ffn2_down", 2 * R * ls.F * ls.H)):
+            if name in mx_stages:
+                avg = sum(mx_stages[name]) / len(mx_stages[name])
+                ach = fl / (avg * 1e-3) / 1e12
+                mk[name] = {"ms": round(avg, 4), "bound": "tensor", "achieved_tflops": round(ach, 1),
+                            "frac": round(ach / peak8, 4)}
+        for name in ("router", "permute", "combine"):
+            if name in mx_stages:
+                mk[name] = {"ms": round(sum(mx_stages[name]) / len(mx_stages[name]), 4)}
+        mx = {"value": round(job_throughput(layer_flops(ls, False), ms_mx, world), 2), "unit": "TFLOPS",
+              "ms_per_step": round(ms_mx, 4), "dtype": "mxfp8 (e4m3, e8m0 scale per 32 along K)",
+              "vs_bf16_fwd": round(ms_fwd / ms_mx, 3), "kernels": mk, "peak_fp8_tflops": round(peak8, 1),
+              "peak_source": f"{peaks['source']} bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"}
+        del mxw, wsm, ym
+
+    # ---------------- per-stage table and roofline of the dominant kernel
     model = stage_model(ls, training)
     ridge = peaks["bf16_tflops_sustained"] * 1e3 / peaks["hbm_gbs"]  # FLOP per byte
     agg = {}
@@ -554,7 +604,7 @@ def run_ours(args, ls, rank, world, local_rank):
             "tokens_per_s": round(world * ls.T / (ms * 1e-3), 1),
             "fwd": {"value": round(fwd_value, 2), "unit": "TFLOPS", "ms_per_step": round(ms_fwd, 4),
                     "tokens_per_s": round(world * ls.T / (ms_fwd * 1e-3), 1)},
-            "graph": graph, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "graph": graph, "mxfp8_fwd": mx, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
