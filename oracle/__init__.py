@@ -10,3 +10,4 @@ Core" (paper summary page and the figures & tables page of the same report).
 """
 from .moe_oracle import *  # noqa: F401,F403
 from .mx_oracle import *  # noqa: F401,F403
+from .nv_oracle import *  # noqa: F401,F403
