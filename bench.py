@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay timing")
     ap.add_argument("--force-balanced", action="store_true", help="force-balanced routing (cyclic assignment)")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
+    ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 grouped GEMM timing")
     ap.add_argument("--recompute", action="store_true",
                     help="memory-saving training step (a and y_perm not kept; recomputed in the backward)")
     return ap.parse_args()
@@ -457,6 +458,51 @@ def run_ours(args, ls, rank, world, local_rank):
               "peak_source": f"{peaks['source']} bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"}
         del mxw, wsm, ym
 
+    # ---------------- the NVFP4 grouped expert GEMM on the down projection's
+    # shape: rows grouped by expert as the forward grouped them (its offsets),
+    # the layer's W2 (quantised beforehand), activations quantised per call
+    nv = None
+    if not args.no_nvfp4 and ls.F % 256 == 0 and ls.H % 8 == 0 and training:
+        R = ls.T * ls.k
+        nvw = ops.nv_quantize_weights(d["W2"])
+        gen = torch.Generator(device=dev).manual_seed(args.seed + 7)
+        a_in = torch.randn((R, ls.F), generator=gen, device=dev).to(torch.bfloat16)
+        wsn = ops.nv_workspace(ls.E, R, ls.F, dev)
+        yn = torch.empty((R, ls.H), dtype=torch.bfloat16, device=dev)
+        offs = saved["offsets"]
+
+        def gemm_nv():
+            ops.nv_grouped_gemm(a_in, offs, nvw, ws=wsn, y=yn)
+
+        for _ in range(max(3, args.warmup)):
+            gemm_nv()
+        barrier()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ops.profile_start(args.steps * 4 + 4)
+        n0.record()
+        for _ in range(args.steps):
+            gemm_nv()
+        n1.record()
+        torch.cuda.synchronize()
+        ops.profile_stop()
+        assert ops.device_status(wsn) == 0
+        ms_nv = max_over_ranks(n0.elapsed_time(n1) / args.steps, world, dev)
+        st_nv = {}
+        for name, t in ops.profile_read(args.steps * 4 + 4):
+            st_nv.setdefault(name, []).append(t)
+        fl = 2 * R * ls.F * ls.H
+        peak4 = 6 * peaks["bf16_tflops_sustained"]
+        g_ms = sum(st_nv.get("nv_gemm", [0])) / max(1, len(st_nv.get("nv_gemm", [0])))
+        q_ms = sum(st_nv.get("nv_quantize", [0])) / max(1, len(st_nv.get("nv_quantize", [0])))
+        nv = {"shape": f"grouped {R} x {ls.F} x {ls.H} (down projection, {ls.E} experts)",
+              "ms_per_call": round(ms_nv, 4), "value": round(fl / (ms_nv * 1e-3) / 1e12, 1), "unit": "TFLOPS",
+              "gemm_ms": round(g_ms, 4), "quantize_ms": round(q_ms, 4),
+              "gemm": {"bound": "tensor", "achieved_tflops": round(fl / (g_ms * 1e-3) / 1e12, 1) if g_ms else None,
+                       "frac": round(fl / (g_ms * 1e-3) / 1e12 / peak4, 4) if g_ms else None},
+              "dtype": "nvfp4 (e2m1, e4m3 scale per 16 along K, fp32 tensor scale)", "peak_fp4_tflops": round(peak4, 1),
+              "peak_source": f"{peaks['source']} bf16_tflops_sustained x 6 (nominal fp4:bf16 ratio 13.5/2.25)"}
+        del nvw, a_in, wsn, yn
+
     # ---------------- per-stage table and roofline of the dominant kernel
     model = stage_model(ls, training)
     ridge = peaks["bf16_tflops_sustained"] * 1e3 / peaks["hbm_gbs"]  # FLOP per byte
@@ -604,7 +650,7 @@ def run_ours(args, ls, rank, world, local_rank):
             "tokens_per_s": round(world * ls.T / (ms * 1e-3), 1),
             "fwd": {"value": round(fwd_value, 2), "unit": "TFLOPS", "ms_per_step": round(ms_fwd, 4),
                     "tokens_per_s": round(world * ls.T / (ms_fwd * 1e-3), 1)},
-            "graph": graph, "mxfp8_fwd": mx, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "graph": graph, "mxfp8_fwd": mx, "nvfp4_grouped_gemm": nv, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -276,6 +276,45 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
                         const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2, void* y,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * NVFP4 grouped expert GEMM. The report lists NVFP4 among its precisions
+ * (summary page, "Modeling" and "Key Terms") without defining it; the format
+ * here is NVIDIA's NVFP4: E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6,
+ * round to nearest even, saturating), a positive E4M3 scale per 16 consecutive
+ * elements along K and an fp32 tensor scale g = amax / (6 * 448) (1 for a zero
+ * tensor); in fp32: s_b = E4M3(fp32(amax_b / 6) / g), q = E2M1(v / fp32(s_b g)).
+ * Codes are packed two per byte, element 2j in the low nibble.
+ * Requires K a multiple of 256, N a multiple of 8, E <= 256.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the quantised weights of E experts W[E][K][N]: which = 0 codes
+ * [E][N][K/2] (K-major), 1 tile-ready scales (opaque: per expert, 192-row n
+ * tile and 256-element k block, two blocks of 4 x 512 bytes; byte
+ * 2048 b + 512 s + 16 r + 4 c + j = scale of tile row 128 b + 32 c + r,
+ * 16-element block 4 s + j; unused bytes zero), 2 tensor scales [E] fp32. */
+size_t moe_nv_weight_bytes(int E, int K, int N, int which);
+
+/* Quantise W [E][K][N] bf16 (each expert a tensor of its own, blocks along K)
+ * into wq, sf and g. */
+int moe_nv_quantize_weights(int E, int K, int N, const moe_bf16* W, uint8_t* wq, uint8_t* sf, float* g,
+                            void* stream);
+
+/* Row-major NVFP4 quantisation of x [M,K] bf16 as one tensor (blocks along K):
+ * q [M][K/2] codes, scales [M][K/16] E4M3 bytes, *g the tensor scale. */
+int moe_nv_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, float* g, void* stream);
+
+/* Workspace bytes of moe_nv_grouped_gemm. */
+size_t moe_nv_workspace_bytes(int E, long long R, int K);
+
+/* Grouped expert GEMM on NVFP4 operands: rows offsets[e]..offsets[e+1] of
+ * x [R,K] bf16 (quantised here as one tensor, blocks along K) times expert
+ * e's quantised weights (moe_nv_quantize_weights): y [R,N] bf16 =
+ * g_x g_e sum_k Q(x)[r,k] Q(W_e)[k,n], fp32 accumulation. offsets [E+1] is
+ * read on the device. */
+int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, const int32_t* offsets,
+                        const uint8_t* wq, const uint8_t* sf, const float* g, moe_bf16* y, void* ws,
+                        size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, returns in *status_out the first device-side error
  * recorded in `ws` since the last read (MOE_OK if none) and clears it. For
  * tests and debugging; the hot path never calls it. */

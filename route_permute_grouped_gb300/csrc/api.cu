@@ -42,6 +42,7 @@ enum StageTag : int {
   STAGE_SHARED2 = 6, STAGE_COMBINE = 7,
   STAGE_COMBINE_BWD = 10, STAGE_ROUTER_BWD = 11, STAGE_DGRAD2 = 12, STAGE_WGRAD2 = 13, STAGE_DGRAD1 = 14,
   STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
+  STAGE_NV_QUANT = 20, STAGE_NV_GEMM = 21,
 };
 // MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
 // report the first stage whose kernels failed (debugging aid, off by default).
@@ -847,6 +848,117 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   }
   MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
   stage_done(s, STAGE_COMBINE, 1);
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 grouped expert GEMM
+// ---------------------------------------------------------------------------
+static int check_nv_shape(int E, long long R, int K, int N) {
+  if (E < 1 || R < 0 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxGroups || K % kNvKB != 0 || N % 8 != 0 || R >= (1ll << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+size_t moe_nv_weight_bytes(int E, int K, int N, int which) {
+  if (check_nv_shape(E, 0, K, N) != MOE_OK) return 0;
+  switch (which) {
+    case 0: return static_cast<size_t>(E) * N * (K / 2);
+    case 1: return nv_weight_sf_bytes(E, K, N);
+    case 2: return sizeof(float) * E;
+    default: return 0;
+  }
+}
+
+int moe_nv_quantize_weights(int E, int K, int N, const moe_bf16* W, uint8_t* wq, uint8_t* sf, float* g,
+                            void* stream) {
+  MOE_TRY(check_nv_shape(E, 0, K, N));
+  if (!W || !wq || !sf || !g || !aligned16(W) || !aligned16(wq) || !aligned16(sf)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(W);
+  MOE_CUDA(launch_nv_amax(w, static_cast<long long>(K) * N, E, g, s));
+  MOE_CUDA(launch_nv_quantize_weights(w, E, K, N, g, wq, sf, s));
+  count_launches(3);
+  return MOE_OK;
+}
+
+int moe_nv_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, float* g, void* stream) {
+  if (!x || !q || !scales || !g || M < 1 || K < kNvBlock || K % kNvBlock != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (M * K) % 8 != 0) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  MOE_CUDA(launch_nv_amax(xb, M * K, 1, g, s));
+  MOE_CUDA(launch_nv_quantize_rows(xb, M, K, g, q, scales, s));
+  count_launches(3);
+  return MOE_OK;
+}
+
+struct NvWs {
+  size_t status, g, xq, sf, total;
+};
+static NvWs nv_ws_layout(int E, long long R, int K) {
+  NvWs L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  L.status = take(sizeof(DevStatus));
+  L.g = take(sizeof(float));
+  L.xq = take(static_cast<size_t>(R) * (K / 2));
+  L.sf = take(nv_act_sf_bytes(R, E, K));
+  L.total = o;
+  return L;
+}
+
+size_t moe_nv_workspace_bytes(int E, long long R, int K) {
+  if (check_nv_shape(E, R, K, 8) != MOE_OK) return 0;
+  return nv_ws_layout(E, R, K).total;
+}
+
+int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, const int32_t* offsets,
+                        const uint8_t* wq, const uint8_t* sf, const float* g, moe_bf16* y, void* ws,
+                        size_t ws_bytes, void* stream) {
+  MOE_TRY(check_nv_shape(E, R, K, N));
+  if (!x || !offsets || !wq || !sf || !g || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(wq) || !aligned16(sf) || !aligned16(y) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const NvWs L = nv_ws_layout(E, R, K);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (R == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, L.status);
+  float* gx = at<float>(ws, L.g);
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  uint8_t* sfx = at<uint8_t>(ws, L.sf);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  prof_mark(s, STAGE_BEGIN);
+  MOE_CUDA(launch_nv_amax(xb, R * K, 1, gx, s));
+  MOE_CUDA(launch_nv_quantize_grouped(xb, static_cast<int>(R), K, E, offsets, gx, xq, sfx, s));
+  stage_done(s, STAGE_NV_QUANT, 3);
+  moe_config c{};
+  c.T = 1; c.H = N; c.E = E; c.k = 1; c.F = K;
+  GemmParams p = base_params(c, st);
+  p.H = N;
+  p.ngroups = E;
+  p.offsets = offsets;
+  p.M_total = static_cast<int>(R);
+  p.bn = kNvTileN;
+  p.n_tiles = (N + kNvTileN - 1) / kNvTileN;
+  p.nt_w = p.n_tiles;
+  p.kb_total = K / kNvKB;
+  p.out0 = y;
+  p.nv_ga = gx;
+  p.nv_gb = g;
+  CUtensorMap ma, mb, msa, msb, oy;
+  if (!make_map_u8(&ma, xq, K / 2, R, 128, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb, wq, K / 2, static_cast<uint64_t>(E) * N, 128, kNvTileN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msa, sfx, 256, nv_act_sf_bytes(R, E, K) / 256, 256, 8, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb, sf, 256, nv_weight_sf_bytes(E, K, N) / 256, 256, 16, false)) return MOE_ERR_CUDA;
+  if (!make_map_store(&oy, y, N, R, false)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_gemm(KIND_GEMM_NV, p, ma, mb, msa, num_sms(), s, &oy, &msb));
+  stage_done(s, STAGE_NV_GEMM, 1);
   return MOE_OK;
 }
 

@@ -309,6 +309,25 @@ __device__ __forceinline__ void umma2_mx_w(uint32_t d_tmem, uint32_t a_lo, uint3
       "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
+// NVFP4 CTA-pair MMA (kind::mxf4nvf4, scale_vec::4X: four E4M3 scales per row
+// and K=64 step, the bytes of one cell; E2M1 operands two per byte).
+__device__ __forceinline__ void umma2_nv_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi,
+                                           uint32_t idesc, uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %4, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of kind::mxf4nvf4 with E2M1 A/B (K-major, format 1),
+// fp32 D and E4M3 scales (bit 23 clear), K = 64 per MMA.
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __device__ __forceinline__ void tmem_cp2_32x128b_x4(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }

@@ -138,7 +138,7 @@ __device__ __forceinline__ void epi_ffn1_tma(const GemmParams& p, const TileInfo
 // the group as the third coordinate and clip rows per group.
 template <bool F32, bool THREE_D>
 __device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc, int lane, int row0, int ncols,
-                                              Stager& st, const CUtensorMap* map, int nch64 = 4) {
+                                              Stager& st, const CUtensorMap* map, int nch64 = 4, float alpha = 1.0f) {
   const bool zero = ti.nkb == 0;
   if constexpr (F32) {
 #pragma unroll 1
@@ -171,6 +171,10 @@ __device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc,
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+        }
+        if (alpha != 1.0f) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] *= alpha;
         }
         stage_bf16x32(buf, lane, h, f);
       }

@@ -99,7 +99,7 @@ __device__ __forceinline__ void epi_ffn1(const GemmParams& p, const TileInfo& ti
 
 // Plain store of a 128 x bn tile: bf16 or fp32, row-major with `ld` columns.
 __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int r, int nchunks, int ncols,
-                                          int ld, void* out, bool fp32, size_t row_base) {
+                                          int ld, void* out, bool fp32, size_t row_base, float alpha = 1.0f) {
   const int row = ti.m0 + r;
   const bool valid = row < ti.m_end;
   const bool zero = ti.nkb == 0;  // no k blocks: the product is zero
@@ -113,10 +113,25 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
       for (int j = 0; j < 32; ++j) f[j] = 0.0f;
     }
     const int col = ti.n0 + c * 32;
+    if (alpha != 1.0f) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] *= alpha;
+    }
     if (valid && col < ncols) {
       const size_t off = (row_base + static_cast<size_t>(row)) * ld + col;
-      if (fp32) store_f32x32(reinterpret_cast<float*>(out) + off, f);
-      else store_bf16x32(reinterpret_cast<__nv_bfloat16*>(out) + off, f);
+      if (col + 32 <= ncols) {
+        if (fp32) store_f32x32(reinterpret_cast<float*>(out) + off, f);
+        else store_bf16x32(reinterpret_cast<__nv_bfloat16*>(out) + off, f);
+      } else {
+        // the matrix ends inside this chunk: columns past it belong to the
+        // next row
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j >= ncols - col) break;
+          if (fp32) reinterpret_cast<float*>(out)[off + j] = f[j];
+          else reinterpret_cast<__nv_bfloat16*>(out)[off + j] = __float2bfloat16_rn(f[j]);
+        }
+      }
     }
   }
 }
@@ -380,11 +395,12 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc =
-        TR::kMx ? idesc_mxf8_f32(TR::kTileM, kMxBN) : idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
+    const uint32_t idesc = TR::kNv ? idesc_nvf4_f32(TR::kTileM, kNvTileN)
+                           : TR::kMx ? idesc_mxf8_f32(TR::kTileM, kMxBN)
+                                     : idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
     // MXFP8: descriptors of the stage's scale blocks (32 rows of 16 bytes,
     // no swizzle, 8-row groups 128 bytes apart) for the copies into TMEM
-    const uint32_t sf_lo0 = sdesc_lo(smem_u32(smem) + kMxSfOff, 128);
+    const uint32_t sf_lo0 = sdesc_lo(smem_u32(smem) + (TR::kNv ? kNvSfOff : kMxSfOff), 128);
     const uint64_t sf_hi = static_cast<uint64_t>((128u >> 4) | (1u << 14)) << 32;
     // operand descriptors: stage 0's low words, advanced per stage and per
     // 16-deep k step (K-major: 32 bytes; MN-major: 16 rows of 128 bytes)
@@ -452,6 +468,47 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+      if constexpr (TR::kNv) {
+        // NVFP4: four K=64 steps per 256-element k block, each with its own
+        // scale cells (A: 4 columns, B: 8); the twelve copies of block kb+1
+        // go to the other scale region before the MMAs of block kb
+        auto copy_scales = [&](int st_, uint32_t region) {
+          const uint32_t sf_lo = sf_lo0 + static_cast<uint32_t>(st_) * stage_lo;
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) {
+            tmem_cp2_32x128b_x4(tmem_base + region + 4 * s4, sf_hi | (sf_lo + (512u * s4 >> 4)));
+            tmem_cp2_32x128b_x4(tmem_base + region + 16 + 8 * s4, sf_hi | (sf_lo + ((kNvSfBytes + 512u * s4) >> 4)));
+            tmem_cp2_32x128b_x4(tmem_base + region + 20 + 8 * s4,
+                                sf_hi | (sf_lo + ((2 * kNvSfBytes + 512u * s4) >> 4)));
+          }
+        };
+        if (ti.nkb > 0) {
+          if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) copy_scales(stage, kNvSfRegion0);
+          __syncwarp();
+        }
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          const int cur = stage;
+          const uint32_t region = (kb & 1) ? kNvSfRegion1 : kNvSfRegion0;
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+          if (kb + 1 < ti.nkb) {
+            if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) copy_scales(stage, (kb & 1) ? kNvSfRegion0 : kNvSfRegion1);
+          }
+          if (lane == 0) {
+            const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(cur) * stage_lo;
+            const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cur) * stage_lo;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+              umma2_nv_w(d_tmem, a_lo + s4 * kAStep, b_lo + s4 * kBStep, d_hi, idesc, tmem_base + region + 4 * s4,
+                         tmem_base + region + 16 + 8 * s4, (kb > 0 || s4 > 0) ? 1u : 0u);
+            umma2_commit_mc(empty + cur, 3);  // frees the stage in both CTAs
+          }
+          __syncwarp();
+        }
+      }
       if constexpr (TR::kMx) {
         // MXFP8: the scale copy of k block kb+1 (into the other of two scale
         // regions) is issued before the MMAs of block kb, so no MMA waits for
@@ -494,7 +551,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           __syncwarp();
         }
       }
-      for (int kb = 0; kb < (TR::kMx ? 0 : ti.nkb); ++kb) {
+      for (int kb = 0; kb < ((TR::kMx || TR::kNv) ? 0 : ti.nkb); ++kb) {
         if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
         tc_fence_after();
         if constexpr (KIND == KIND_WGRAD) {
@@ -608,6 +665,11 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         } else if (any_rows) {
           epi_store(ti, tacc, r, kMxBN / 32, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
         }
+      } else if constexpr (KIND == KIND_GEMM_NV) {
+        // y = g_x g_e (sum of the block-scaled products)
+        const float alpha = __ldg(p.nv_ga) * __ldg(p.nv_gb + ti.g);
+        if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0, kNvTileN / 64, alpha);
+        else if (any_rows) epi_store(ti, tacc, r, kNvTileN / 32, p.H, p.H, p.out0, false, 0, alpha);
       } else if constexpr (KIND == KIND_ROUTER) {
         // raw fp32 logits [T, bn]; the map's row extent T clips the tail
         epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
@@ -723,6 +785,7 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
     case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN1_MX: return launch_kind<KIND_FFN1_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN2_MX: return launch_kind<KIND_FFN2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_GEMM_NV: return launch_kind<KIND_GEMM_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

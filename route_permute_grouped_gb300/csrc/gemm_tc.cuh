@@ -33,6 +33,7 @@
 #pragma once
 #include "common.cuh"
 #include "mx.cuh"
+#include "nv.cuh"
 
 namespace moe {
 
@@ -50,6 +51,7 @@ enum GemmKind : int {
   KIND_FFN1_MX = 9,    // MXFP8 gate/up: h = Q(x_perm) [Q(W1_e) | Q(W3_e)] -> a = SiLU(h1) h3, stored as MXFP8
                        // (codes + the down GEMM's tile-ready scales); 256 x (96 gate + 96 up) pair tiles
   KIND_FFN2_MX = 10,   // MXFP8 down: y_perm = Q(a) Q(W2_e), bf16 out; 256 x 192 pair tiles
+  KIND_GEMM_NV = 11,   // NVFP4 grouped expert GEMM: y = g_x g_e Q(x_e) Q(W_e), bf16 out; 256 x 192 pair tiles
 };
 
 constexpr int kBM = 128;
@@ -72,6 +74,14 @@ constexpr uint32_t kMxStageTx = 16384 + (kMxBN / 2) * 128 + 3 * kMxSfBytes;  // 
 constexpr uint32_t kMxSfaCol = 448;
 constexpr uint32_t kMxSfbCol = 452;
 constexpr uint32_t kMxSfRegion = 12;
+// NVFP4 pair stage (per CTA): A 16 KB, B 12 KB at 16 KB, A scales (2 KB) and
+// B scales (4 KB) at 28 KB. TMEM scale regions of 48 columns (A: 4 steps x 4,
+// B: 4 steps x 8) in the gaps after the two 192-column accumulators.
+constexpr int kNvSfOff = 28672;
+constexpr int kNvStageBytes = 34816;
+constexpr uint32_t kNvStageTx = kNvStageBytes;  // one CTA's share
+constexpr uint32_t kNvSfRegion0 = 192;
+constexpr uint32_t kNvSfRegion1 = 448;
 constexpr int kAccStride = 256;           // TMEM column distance of the two accumulators
 
 template <int KIND>
@@ -85,13 +95,17 @@ struct KindTraits {
   // elements (one byte each) of its 128 A rows (16 KB) and 96 B rows (12 KB),
   // its A scale block (0.5 KB) and the tile's B scale blocks (1 KB)
   static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX);
+  // NVFP4: like MXFP8 with 256-element k blocks (128 bytes of codes per row)
+  // and four scale blocks per operand block (2 KB of A, 4 KB of B scales)
+  static constexpr bool kNv = (KIND == KIND_GEMM_NV);
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
                                  KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R ||
-                                 KIND == KIND_ROUTER || kMx);
+                                 KIND == KIND_ROUTER || kMx || kNv);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
-  static constexpr int kStageBytesK = kMx ? kMxStageBytes : kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
+  static constexpr int kStageBytesK =
+      kNv ? kNvStageBytes : kMx ? kMxStageBytes : kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
   // DGRAD2 runs eight epilogue warps (two per TMEM lane quadrant, each taking
   // half of the tile's columns) to hide the latency of its loads of the saved
   // pre-activations; it and DGRAD2R (third staging box) give up one stage
@@ -100,14 +114,14 @@ struct KindTraits {
   // 128) and its epilogue (SiLU, quantisation) long
   static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX) ? 12 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
-  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2) ? 5 : (kPair ? 6 : 4);  // MX: 4
+  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (kPair ? 6 : 4);
   static constexpr int kOutWarpBytes =
       (KIND == KIND_DGRAD2R) ? 3 * 4096 : (KIND == KIND_FFN1_MX) ? 0 : 2 * 4096;  // epilogue staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R || kMx);
+                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R || kMx || kNv);
 };
 
 struct GemmParams {
@@ -137,6 +151,8 @@ struct GemmParams {
   // per expert of the weight scales (the weight scales: map msfb)
   uint8_t* sfa_out;
   int nt_w;
+  const float* nv_ga;    // GEMM_NV: tensor scale of the activations (one value)
+  const float* nv_gb;    // GEMM_NV: tensor scales of the experts' weights [ngroups]
   // status
   DevStatus* status;
   unsigned long long wait_limit_ns;
@@ -217,6 +233,19 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
                                                  uint8_t* sA, uint8_t* sB, uint32_t bar_cluster, const CUtensorMap* ma,
                                                  const CUtensorMap* mb0, const CUtensorMap* mb1,
                                                  uint64_t* local_bar = nullptr, const CUtensorMap* msfb = nullptr) {
+  if constexpr (KindTraits<KIND>::kNv) {
+    // 256 k elements (128 bytes) of this CTA's 128 A rows and its 96 B rows
+    // (rows n0 + 96 rank .. of expert g's [N] weight rows), its A scale block
+    // (2 KB = 8 rows of the activations' scale map) and the tile's two B scale
+    // blocks (4 KB = 16 rows of msfb)
+    const int kc = kb * (kNvKB / 2);
+    tma_load_2d_pair(sA, ma, bar_cluster, kc, ti.m0);
+    tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * p.H + ti.n0 + rank * (kNvTileN / 2));
+    uint8_t* sSF = sA + kNvSfOff;
+    tma_load_2d_pair(sSF, mb1, bar_cluster, 0, 8 * ((2 * ti.mt + rank) * p.kb_total + kb));
+    tma_load_2d_pair(sSF + kNvSfBytes, msfb, bar_cluster, 0, 16 * ((ti.g * p.nt_w + ti.nb) * p.kb_total + kb));
+    return;
+  }
   if constexpr (KindTraits<KIND>::kMx) {
     // 128 k elements (bytes) of this CTA's 128 A rows and its 96 B rows, its A
     // scale block (block 2 * pair tile + rank of the activations' scales: map
@@ -356,7 +385,8 @@ __host__ __device__ __forceinline__ int router_stages(int bn) {
 
 template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
-  if constexpr (KindTraits<KIND>::kMx) return 2 * kMxStageTx;                    // both CTAs' shares
+  if constexpr (KindTraits<KIND>::kNv) return 2 * kNvStageTx;                    // both CTAs' shares
+  else if constexpr (KindTraits<KIND>::kMx) return 2 * kMxStageTx;               // both CTAs' shares
   else if constexpr (KIND == KIND_ROUTER) return 2 * router_stage_bytes(p.bn);   // both CTAs' shares
   else if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
   else return kABytes + kBBytesMax;

@@ -77,6 +77,20 @@ inline size_t mx_sf2_bytes(const moe_config& c) {
 inline size_t mx_sfa_bytes(long long R, int E, int K) {
   return 2 * static_cast<size_t>((R + 2 * kBM - 1) / (2 * kBM) + E) * (K / kMxKB) * kMxSfBytes;
 }
+// nv.cu: NVFP4 quantisers and the sizes of the tile-ready scale buffers
+inline size_t nv_weight_sf_bytes(int E, int K, int N) {
+  return static_cast<size_t>(E) * ((N + kNvTileN - 1) / kNvTileN) * (K / kNvKB) * 2 * kNvSfBytes;
+}
+inline size_t nv_act_sf_bytes(long long R, int E, int K) {
+  return 2 * static_cast<size_t>((R + 2 * kBM - 1) / (2 * kBM) + E) * (K / kNvKB) * kNvSfBytes;
+}
+cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, float* out_g, cudaStream_t st);
+cudaError_t launch_nv_quantize_rows(const __nv_bfloat16* x, long long M, int K, const float* g, uint8_t* q,
+                                    uint8_t* s, cudaStream_t st);
+cudaError_t launch_nv_quantize_weights(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,
+                                       uint8_t* sf, cudaStream_t st);
+cudaError_t launch_nv_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
+                                       const float* g, uint8_t* xq, uint8_t* sf, cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,
                                     cudaStream_t st);
 cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,

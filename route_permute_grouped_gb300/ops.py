@@ -97,11 +97,20 @@ def lib():
                                           vp, c_size_t, vp]
         for n in ("moe_mx_quantize_weights", "moe_mx_quantize", "moe_layer_fwd_mxfp8"):
             getattr(L, n).restype = c_int
+        L.moe_nv_weight_bytes.restype = c_size_t
+        L.moe_nv_weight_bytes.argtypes = [c_int, c_int, c_int, c_int]
+        L.moe_nv_workspace_bytes.restype = c_size_t
+        L.moe_nv_workspace_bytes.argtypes = [c_int, c_longlong, c_int]
+        L.moe_nv_quantize_weights.argtypes = [c_int, c_int, c_int, vp, vp, vp, vp, vp]
+        L.moe_nv_quantize.argtypes = [vp, c_longlong, c_int, vp, vp, vp, vp]
+        L.moe_nv_grouped_gemm.argtypes = [c_int, c_longlong, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+        for n in ("moe_nv_quantize_weights", "moe_nv_quantize", "moe_nv_grouped_gemm"):
+            getattr(L, n).restype = c_int
         _lib = L
     return _lib
 
 
-STAGE_NAMES = {1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
+STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
                17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss"}
@@ -374,4 +383,55 @@ def layer_fwd_mxfp8(cfg, x, router_w, mxw, expert_bias=None, logit_bias=None, Ws
                                    ctypes.byref(_mx_struct(mxw)), _p(Ws1), _p(Ws3), _p(Ws2), _p(y), _p(ws),
                                    ws.numel(), _stream())
     _check(st, "moe_layer_fwd_mxfp8")
+    return y
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 grouped expert GEMM
+# ---------------------------------------------------------------------------
+def nv_quantize_weights(W):
+    """Quantise expert weights W [E, K, N] bf16: dict with wq [E, N, K/2]
+    (codes, two per byte), sf (tile-ready E4M3 scales), g [E] fp32."""
+    E, K, N = W.shape
+    nb = [int(lib().moe_nv_weight_bytes(E, K, N, i)) for i in range(3)]
+    if 0 in nb:
+        raise MoeError(2, "moe_nv_weight_bytes")
+    wq = torch.empty((E, N, K // 2), dtype=torch.uint8, device=W.device)
+    sf = torch.empty(nb[1], dtype=torch.uint8, device=W.device)
+    g = torch.empty(E, dtype=torch.float32, device=W.device)
+    _check(lib().moe_nv_quantize_weights(E, K, N, _p(W), _p(wq), _p(sf), _p(g), _stream()), "moe_nv_quantize_weights")
+    return {"wq": wq, "sf": sf, "g": g, "E": E, "K": K, "N": N}
+
+
+def nv_quantize(x):
+    """Row-major NVFP4 quantisation of x [M, K] bf16 as one tensor: (codes
+    [M, K/2], scales [M, K/16], tensor scale [1])."""
+    M, K = x.shape
+    q = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty((M, K // 16), dtype=torch.uint8, device=x.device)
+    g = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().moe_nv_quantize(_p(x), M, K, _p(q), _p(s), _p(g), _stream()), "moe_nv_quantize")
+    return q, s, g
+
+
+def nv_workspace(E, R, K, device="cuda"):
+    n = int(lib().moe_nv_workspace_bytes(E, R, K))
+    if n == 0:
+        raise MoeError(2, "moe_nv_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def nv_grouped_gemm(x, offsets, w, ws=None, y=None):
+    """y [R, N] bf16 = grouped NVFP4 GEMM of x [R, K] (rows grouped by
+    ``offsets``, [E+1] int32 on the device) with quantised weights ``w``."""
+    R, K = x.shape
+    E, N = w["E"], w["N"]
+    if y is None:
+        y = torch.empty((R, N), dtype=torch.bfloat16, device=x.device)
+    ws = nv_workspace(E, R, K, x.device) if ws is None else ws
+    st = lib().moe_nv_grouped_gemm(E, R, K, N, _p(x), _p(offsets), _p(w["wq"]), _p(w["sf"]), _p(w["g"]), _p(y),
+                                   _p(ws), ws.numel(), _stream())
+    _check(st, "moe_nv_grouped_gemm")
     return y

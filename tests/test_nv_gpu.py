@@ -1,0 +1,101 @@
+"""NVFP4 grouped expert GEMM (GPU) against the NVFP4 oracle: the quantisers
+bit for bit (codes, block scales, tensor scales, the tile-ready weight-scale
+layout), and the grouped GEMM within the layer's tolerance on expert segments
+that span several tiles, end mid-tile, are empty, and a ragged last n tile."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from route_permute_grouped_gb300 import ops
+from tests._util import assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from route_permute_grouped_gb300 import build
+    build.build()
+    ops.lib()
+
+
+def _unpack(q):
+    q = np.asarray(q, np.uint8)
+    out = np.empty(q.shape[:-1] + (2 * q.shape[-1],), np.uint8)
+    out[..., 0::2] = q & 15
+    out[..., 1::2] = q >> 4
+    return out
+
+
+def _bf16(shape, std, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+
+
+def test_nv_quantize_rows_bit_exact():
+    x = _bf16((300, 256), 1.0, 3) * torch.exp(_bf16((300, 1), 1.5, 4).float()).to(torch.bfloat16)
+    x[4, 16:32] = 0.0
+    x[5, :16] = torch.linspace(-7, 7, 16).to(torch.bfloat16)
+    q, s, g = ops.nv_quantize(x.cuda())
+    torch.cuda.synchronize()
+    rq, rs, rg = O.nv_quantize(f64(x).astype(np.float32), axis=1)
+    assert g.item() == float(rg)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(_unpack(q.cpu().numpy()), rq)
+
+
+@pytest.mark.parametrize("E,K,N", [(3, 512, 200), (2, 256, 384)])
+def test_nv_weight_quantization_bit_exact(E, K, N):
+    W = _bf16((E, K, N), K ** -0.5, 11)
+    w = ops.nv_quantize_weights(W.cuda())
+    torch.cuda.synchronize()
+    Wn = f64(W).astype(np.float32)
+    nt = -(-N // 192)
+    sf = w["sf"].cpu().numpy().reshape(E, nt, K // 256, 2, 4, 32, 4, 4)  # [e][tile][kb][blk][step][r][c][j]
+    wq = _unpack(w["wq"].cpu().numpy())
+    for e in range(E):
+        rq, rs, rg = O.nv_quantize(Wn[e].T, axis=1)  # [N, K] blocks along K
+        assert w["g"][e].item() == float(rg)
+        assert np.array_equal(wq[e], rq), e
+        got = np.zeros((N, K // 16), np.uint8)
+        for n in range(N):
+            j, b = divmod(n, 192)
+            blk, rr = divmod(b, 128)
+            c, r = divmod(rr, 32)
+            got[n] = sf[e, j, :, blk, :, r, c, :].reshape(-1)
+        assert np.array_equal(got, rs), e
+        # rows of the last tile past N keep zero scales
+        for b in range(N - 192 * (nt - 1), 256):
+            blk, rr = divmod(b, 128)
+            c, r = divmod(rr, 32)
+            assert not sf[e, nt - 1, :, blk, :, r, c, :].any()
+
+
+@pytest.mark.parametrize("counts,K,N", [([300, 0, 41, 513, 256, 7], 512, 200), ([1000, 24], 256, 384)])
+def test_nv_grouped_gemm(counts, K, N):
+    E = len(counts)
+    R = sum(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = _bf16((R, K), 1.0, 21)
+    W = _bf16((E, K, N), K ** -0.5, 22)
+    w = ops.nv_quantize_weights(W.cuda())
+    ws = ops.nv_workspace(E, R, K)
+    y = ops.nv_grouped_gemm(x.cuda(), torch.from_numpy(offsets).cuda(), w, ws=ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    ref = O.nv_grouped_gemm(f64(x).astype(np.float32), offsets, f64(W).astype(np.float32))
+    # bf16 outputs: one bf16 ulp of the largest value where the fp32 sum sits
+    # at a rounding boundary
+    assert_close("y", f64(y), ref, atol=max(2e-2, 2.0 ** -7 * float(np.abs(ref).max())))
+    # the NVFP4 GEMM differs from the exact product by FP4 rounding, not more
+    exact = np.zeros((R, N))
+    for e in range(E):
+        exact[offsets[e]:offsets[e + 1]] = f64(x)[offsets[e]:offsets[e + 1]] @ f64(W)[e]
+    rel = np.linalg.norm(f64(y) - exact) / np.linalg.norm(exact)
+    assert 0.03 < rel < 0.3, rel
+
+
+def test_nv_rejects_unaligned_shapes():
+    assert ops.lib().moe_nv_workspace_bytes(4, 100, 128) == 0   # K not a multiple of 256
+    assert ops.lib().moe_nv_weight_bytes(4, 256, 12, 0) == 0     # N not a multiple of 8
