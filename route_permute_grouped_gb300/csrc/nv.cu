@@ -12,13 +12,20 @@ namespace moe {
 __global__ void __launch_bounds__(256) nv_amax_kernel(const __nv_bfloat16* __restrict__ x, long long n_per,
                                                       unsigned* __restrict__ out) {
   const uint4* base = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.y) * n_per);
+  const long long nv = n_per / 8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   float m = 0.0f;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_per / 8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldg(base + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // four independent 16-byte loads in flight per thread
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nv; i += 4 * stride) {
+    uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    for (int u = 0; u < 4; ++u) v[u] = i + u * stride < nv ? __ldg(base + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -155,7 +162,7 @@ cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, 
   cudaError_t e = cudaMemsetAsync(out_bits, 0, sizeof(float) * groups, st);
   if (e != cudaSuccess) return e;
   long long blocks = (n_per / 8 + 255) / 256;
-  if (blocks > 1024) blocks = 1024;
+  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
   if (blocks < 1) blocks = 1;
   nv_amax_kernel<<<dim3(static_cast<unsigned>(blocks), groups), 256, 0, st>>>(x, n_per,
                                                                               reinterpret_cast<unsigned*>(out_bits));
