@@ -273,27 +273,12 @@ __device__ __forceinline__ void umma2_commit_mc(uint64_t* bar, uint16_t cta_mask
 }
 
 // Block-scaled FP8 MMA (kind::mxf8f6f4, scale_vec::1X: one E8M0 scale per row
-// and K=32 step): D[tmem] (+)= (A * scale_A) (B * scale_B), E4M3 inputs from
-// shared memory, scales from tensor memory (`sfa`, `sfb`: columns of the scale
-// cells; the byte chosen by the instruction descriptor's scale ids).
-__device__ __forceinline__ void umma_mx_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "setp.ne.b32 p, %7, 0;\n\t"
-      "mov.b64 da, {%1, %3};\n\t"
-      "mov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], da, db, %4, [%5], [%6], p;\n\t}" ::"r"(
-          d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-      : "memory");
-}
-// Copy 32 rows x 16 bytes of shared memory (descriptor `desc`) to four TMEM
-// columns of lanes 0-31, replicated into all four lane quarters. Executed in
-// issue order with this thread's MMAs.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
+// and K=32 step) with E4M3 inputs from shared memory and scales from tensor
+// memory (`sfa`, `sfb`: columns of the scale cells; the byte chosen by the
+// instruction descriptor's scale ids). tcgen05.cp 32x128b.warpx4 copies 32
+// rows x 16 bytes of shared memory (a no-swizzle descriptor) to four TMEM
+// columns of lanes 0-31, replicated into all four lane quarters; copies and
+// MMAs issued by one thread execute in issue order.
 // CTA-pair forms: the even CTA issues them; each CTA's scale cells come from
 // its own shared memory at the same offset (cp), and the M=256 MMA reads each
 // CTA's cells for its own 128 rows and the B scales replicated in both.
