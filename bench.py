@@ -502,6 +502,22 @@ def run_ours(args, ls, rank, world, local_rank):
               "dtype": "nvfp4 (e2m1, e4m3 scale per 16 along K, fp32 tensor scale)", "peak_fp4_tflops": round(peak4, 1),
               "peak_source": f"{peaks['source']} bf16_tflops_sustained x 6 (nominal fp4:bf16 ratio 13.5/2.25)"}
         del nvw, a_in, wsn, yn
+        # the layer forward with NVFP4 expert GEMMs (same inputs)
+        nlw = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
+        yl = torch.empty_like(y)
+        for _ in range(max(3, args.warmup)):
+            ops.layer_fwd_nvfp4(cfg, d["x"], d["router_w"], nlw, d["expert_bias"], d["logit_bias"], y=yl)
+        barrier()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record()
+        for _ in range(args.steps):
+            ops.layer_fwd_nvfp4(cfg, d["x"], d["router_w"], nlw, d["expert_bias"], d["logit_bias"], y=yl)
+        l1.record()
+        torch.cuda.synchronize()
+        ms_nl = max_over_ranks(l0.elapsed_time(l1) / args.steps, world, dev)
+        nv["layer_fwd"] = {"value": round(job_throughput(layer_flops(ls, False), ms_nl, world), 2), "unit": "TFLOPS",
+                           "ms_per_step": round(ms_nl, 4), "vs_bf16_fwd": round(ms_fwd / ms_nl, 3)}
+        del nlw, yl
 
     # ---------------- per-stage table and roofline of the dominant kernel
     model = stage_model(ls, training)

@@ -315,6 +315,39 @@ int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, con
                         const uint8_t* wq, const uint8_t* sf, const float* g, moe_bf16* y, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* NVFP4 layer forward. Quantised weights (device buffers owned by the caller,
+ * sizes from moe_nv_layer_weight_bytes, which = 0..5 in field order): w13 /
+ * sf13 / g13 are [W1_e | W3_e] (H x 2F, one tensor per expert) in the layout
+ * of moe_nv_quantize_weights with N = 2F; w2 / sf2 / g2 are W2 (K = F, N = H). */
+typedef struct {
+  uint8_t* w13;
+  uint8_t* sf13;
+  float* g13;
+  uint8_t* w2;
+  uint8_t* sf2;
+  float* g2;
+} moe_nv_weights;
+
+size_t moe_nv_layer_weight_bytes(const moe_config* cfg, int which);
+
+/* Quantise W1, W3 [E,H,F] and W2 [E,F,H] bf16 into *w. */
+int moe_nv_quantize_layer_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                                  const moe_nv_weights* w, void* stream);
+
+/* Workspace bytes of moe_layer_fwd_nvfp4. */
+size_t moe_nv_workspace_bytes_layer(const moe_config* cfg);
+
+/* Whole layer forward with NVFP4 expert GEMMs: router, permute and combine as
+ * in moe_layer_fwd; the routed rows x_perm (one tensor: x's maximum) are
+ * quantised, the gate/up GEMM writes h = bf16(g_x g_e Q(x_perm) Q([W1|W3]))
+ * [R, 2F], a = bf16(SiLU(h1) h3) is formed with its maximum, quantised as one
+ * tensor, and the down GEMM writes y_perm = bf16(g_a g_e Q(a) Q(W2)). y [T,H]
+ * bf16 (fp32 if out_fp32). Requires H and F multiples of 256, F_shared = 0 and
+ * inter_fp32 = 0. Inference: intermediates live in the workspace. */
+int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                        const float* expert_bias, const float* logit_bias, const moe_nv_weights* w, void* y, void* ws,
+                        size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, returns in *status_out the first device-side error
  * recorded in `ws` since the last read (MOE_OK if none) and clears it. For
  * tests and debugging; the hot path never calls it. */

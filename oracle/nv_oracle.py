@@ -31,11 +31,11 @@ from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import bf16_rne
+from .moe_oracle import bf16_rne, permute_plan, route, silu
 from .mx_oracle import e4m3_encode, e4m3_round
 
 __all__ = ["E2M1_MAX", "e2m1_round", "e2m1_encode", "e2m1_decode", "nv_tensor_scale", "nv_quantize",
-           "nv_dequantize", "nv_roundtrip", "nv_grouped_gemm"]
+           "nv_dequantize", "nv_roundtrip", "nv_grouped_gemm", "nv_layer_fwd"]
 
 E2M1_MAX = 6.0
 NV_BLOCK = 16
@@ -135,3 +135,52 @@ def nv_grouped_gemm(x, offsets, W, out_bf16=True):
         We = nv_roundtrip(np.asarray(W[e], np.float32), axis=0)
         y[lo:hi] = xq[lo:hi] @ We
     return bf16_rne(y) if out_bf16 else y
+
+
+def nv_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
+                 topk_groups=1, gate_scale=1.0, tokens=None, force_balanced=False):
+    """Forward of the layer with NVFP4 expert GEMMs.
+
+    Routing and combine as in the bf16 layer (fp64). The routed rows x_perm
+    form one tensor; expert e's [W1_e | W3_e] (H x 2F, blocks along H) one
+    tensor and W2_e (blocks along F) another. Per expert:
+      h  = bf16(Q(x_e) Q([W1_e | W3_e]))        (the gate/up GEMM, stored bf16)
+      a  = bf16(SiLU(h1) h3)                    (stored bf16)
+      out = bf16(Q(a_e) Q(W2_e))                (a quantised as one tensor over all rows)
+    with Q = ``nv_roundtrip``. The tensor scale of a comes from the maximum of
+    a over every routed row, so a is formed for all rows; ``tokens`` restricts
+    the combine."""
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
+    E = np.asarray(w_r).shape[0]
+    counts, offsets, row = permute_plan(rt["topk_idx"], E)
+    R = T * k
+    x_perm = np.zeros((R, H), np.float32)
+    x_perm[row.reshape(-1)] = np.repeat(x.astype(np.float32), k, axis=0)
+    gx = nv_tensor_scale(np.abs(x_perm).max() if R else 0.0)
+    xq = nv_roundtrip(x_perm, axis=1, g=gx)
+    F = np.asarray(W1[0]).shape[1]
+    a = np.zeros((R, F))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        W13 = np.concatenate([np.asarray(W1[e], np.float32), np.asarray(W3[e], np.float32)], axis=1)
+        h = bf16_rne(xq[lo:hi] @ nv_roundtrip(W13, axis=0))
+        a[lo:hi] = bf16_rne(silu(h[:, :F]) * h[:, F:])
+    ga = nv_tensor_scale(np.abs(a).max() if R else 0.0)
+    aq = nv_roundtrip(a.astype(np.float32), axis=1, g=ga)
+    y_perm = np.zeros((R, H))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        y_perm[lo:hi] = bf16_rne(aq[lo:hi] @ nv_roundtrip(np.asarray(W2[e], np.float32), axis=0))
+    tok = np.arange(T) if tokens is None else np.asarray(tokens)
+    y = np.full((T, H), np.nan)
+    acc = np.zeros((len(tok), H))
+    for i in range(k):
+        acc = acc + rt["topk_gate"][tok, i:i + 1] * y_perm[row[tok, i]]
+    y[tok] = acc
+    return {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": y}

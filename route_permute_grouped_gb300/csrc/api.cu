@@ -172,6 +172,9 @@ struct WsLayout {
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
+  // NVFP4 forward: gate/up output h [R, 2F] bf16, codes and scales of the
+  // current GEMM's activations (x_perm, then a), their two tensor scales
+  size_t nv_h, nv_q, nv_sf, nv_g;
   size_t total;
 };
 
@@ -183,7 +186,7 @@ static int router_dw_splits(int T) {
   return s < 1 ? 1 : s;
 }
 
-static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false) {
+static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, bool nv = false) {
   WsLayout L{};
   const size_t T = c.T, H = c.H, E = c.E, k = c.k, F = c.F, R = T * k;
   const size_t inter = c.inter_fp32 ? 4 : 2;
@@ -209,6 +212,14 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false) {
   } else {
     L.x_perm = take(2 * R * H);
     L.a = take(2 * R * F);
+  }
+  if (nv) {
+    L.nv_h = take(2 * R * 2 * F);
+    L.nv_q = take(R * (H > F ? H : F) / 2);
+    const size_t sx = nv_act_sf_bytes(static_cast<long long>(R), c.E, c.H);
+    const size_t sa = nv_act_sf_bytes(static_cast<long long>(R), c.E, c.F);
+    L.nv_sf = take(sx > sa ? sx : sa);
+    L.nv_g = take(2 * sizeof(float));
   }
   L.y_perm = take(inter * R * H);
   L.as = c.F_shared ? take(2 * T * c.F_shared) : 0;
@@ -404,6 +415,40 @@ static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const 
   if (!make_map_store(&oy, y, c.H, R, y_fp32)) return MOE_ERR_CUDA;
   MOE_CUDA(launch_gemm(KIND_FFN2_MX, q, ma2, mb2, msa2, num_sms(), s, &oy, &msb2));
   stage_done(s, STAGE_FFN2, 1);
+  return MOE_OK;
+}
+
+// NVFP4 grouped GEMM on quantised activations: y [R, N] bf16 = g_x g_e (Q(x) Q(W_e))
+static int run_gemm_nv(int E, long long R, int K, int N, const int32_t* offsets, const uint8_t* xq,
+                       const uint8_t* sfx, const float* gx, const uint8_t* wq, const uint8_t* sf, const float* g,
+                       __nv_bfloat16* y, DevStatus* st, cudaStream_t s) {
+  moe_config c{};
+  c.T = 1; c.H = N; c.E = E; c.k = 1; c.F = K;
+  GemmParams p = base_params(c, st);
+  p.H = N;
+  p.ngroups = E;
+  p.offsets = offsets;
+  p.M_total = static_cast<int>(R);
+  p.bn = kNvTileN;
+  p.n_tiles = (N + kNvTileN - 1) / kNvTileN;
+  p.nt_w = p.n_tiles;
+  p.kb_total = K / kNvKB;
+  p.out0 = y;
+  p.nv_ga = gx;
+  p.nv_gb = g;
+  CUtensorMap ma, mb, msa, msb, oy;
+  if (!make_map_u8(&ma, xq, K / 2, R, 128, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb, wq, K / 2, static_cast<uint64_t>(E) * N, 128, kNvTileN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msa, sfx, 256, nv_act_sf_bytes(R, E, K) / 256, 256, 8, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb, sf, 256, nv_weight_sf_bytes(E, K, N) / 256, 256, 16, false)) return MOE_ERR_CUDA;
+  if (!make_map_store(&oy, y, N, R, false)) return MOE_ERR_CUDA;
+  return cuda_status(launch_gemm(KIND_GEMM_NV, p, ma, mb, msa, num_sms(), s, &oy, &msb));
+}
+
+// NVFP4 layer: k blocks of 256 along H and F; bf16 intermediates (y_perm
+// too); no shared expert
+static int check_nv_layer_shape(const moe_config& c) {
+  if (c.H % kNvKB != 0 || c.F % kNvKB != 0 || c.F_shared != 0 || c.inter_fp32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
@@ -937,28 +982,107 @@ int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, con
   MOE_CUDA(launch_nv_amax(xb, R * K, 1, gx, s));
   MOE_CUDA(launch_nv_quantize_grouped(xb, static_cast<int>(R), K, E, offsets, gx, xq, sfx, s));
   stage_done(s, STAGE_NV_QUANT, 3);
-  moe_config c{};
-  c.T = 1; c.H = N; c.E = E; c.k = 1; c.F = K;
-  GemmParams p = base_params(c, st);
-  p.H = N;
-  p.ngroups = E;
-  p.offsets = offsets;
-  p.M_total = static_cast<int>(R);
-  p.bn = kNvTileN;
-  p.n_tiles = (N + kNvTileN - 1) / kNvTileN;
-  p.nt_w = p.n_tiles;
-  p.kb_total = K / kNvKB;
-  p.out0 = y;
-  p.nv_ga = gx;
-  p.nv_gb = g;
-  CUtensorMap ma, mb, msa, msb, oy;
-  if (!make_map_u8(&ma, xq, K / 2, R, 128, kBM)) return MOE_ERR_CUDA;
-  if (!make_map_u8(&mb, wq, K / 2, static_cast<uint64_t>(E) * N, 128, kNvTileN / 2)) return MOE_ERR_CUDA;
-  if (!make_map_u8(&msa, sfx, 256, nv_act_sf_bytes(R, E, K) / 256, 256, 8, false)) return MOE_ERR_CUDA;
-  if (!make_map_u8(&msb, sf, 256, nv_weight_sf_bytes(E, K, N) / 256, 256, 16, false)) return MOE_ERR_CUDA;
-  if (!make_map_store(&oy, y, N, R, false)) return MOE_ERR_CUDA;
-  MOE_CUDA(launch_gemm(KIND_GEMM_NV, p, ma, mb, msa, num_sms(), s, &oy, &msb));
+  MOE_TRY(run_gemm_nv(E, R, K, N, offsets, xq, sfx, gx, wq, sf, g, reinterpret_cast<__nv_bfloat16*>(y), st, s));
   stage_done(s, STAGE_NV_GEMM, 1);
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 layer forward
+// ---------------------------------------------------------------------------
+size_t moe_nv_layer_weight_bytes(const moe_config* cfg, int which) {
+  if (check_cfg(cfg) != MOE_OK || check_nv_layer_shape(*cfg) != MOE_OK) return 0;
+  const moe_config& c = *cfg;
+  switch (which) {
+    case 0: return moe_nv_weight_bytes(c.E, c.H, 2 * c.F, 0);
+    case 1: return moe_nv_weight_bytes(c.E, c.H, 2 * c.F, 1);
+    case 2: return moe_nv_weight_bytes(c.E, c.H, 2 * c.F, 2);
+    case 3: return moe_nv_weight_bytes(c.E, c.F, c.H, 0);
+    case 4: return moe_nv_weight_bytes(c.E, c.F, c.H, 1);
+    case 5: return moe_nv_weight_bytes(c.E, c.F, c.H, 2);
+    default: return 0;
+  }
+}
+
+int moe_nv_quantize_layer_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                                  const moe_nv_weights* w, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_nv_layer_shape(c));
+  if (!W1 || !W3 || !W2 || !w || !w->w13 || !w->sf13 || !w->g13 || !w->w2 || !w->sf2 || !w->g2)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w13) || !aligned16(w->sf13) ||
+      !aligned16(w->w2) || !aligned16(w->sf2))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* w1 = reinterpret_cast<const __nv_bfloat16*>(W1);
+  const __nv_bfloat16* w3 = reinterpret_cast<const __nv_bfloat16*>(W3);
+  const __nv_bfloat16* w2 = reinterpret_cast<const __nv_bfloat16*>(W2);
+  // gate/up: [W1_e | W3_e] (H x 2F) is one tensor per expert
+  MOE_CUDA(launch_nv_amax(w1, static_cast<long long>(c.H) * c.F, c.E, w->g13, s, w3));
+  MOE_CUDA(launch_nv_quantize_weights(w1, c.E, c.H, 2 * c.F, w->g13, w->w13, w->sf13, s, w3, c.F));
+  MOE_CUDA(launch_nv_amax(w2, static_cast<long long>(c.F) * c.H, c.E, w->g2, s));
+  MOE_CUDA(launch_nv_quantize_weights(w2, c.E, c.F, c.H, w->g2, w->w2, w->sf2, s));
+  count_launches(7);
+  return MOE_OK;
+}
+
+static WsLayout nv_layer_ws(const moe_config& c) { return ws_layout(c, false, false, true); }
+
+size_t moe_nv_workspace_bytes_layer(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK || check_nv_layer_shape(*cfg) != MOE_OK) return 0;
+  return nv_layer_ws(*cfg).total;
+}
+
+int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                        const float* expert_bias, const float* logit_bias, const moe_nv_weights* w, void* y, void* ws,
+                        size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_nv_layer_shape(c));
+  if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->g13 || !w->w2 || !w->sf2 || !w->g2 || !y || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
+      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = nv_layer_ws(c);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  const long long R = static_cast<long long>(c.T) * c.k;
+  int32_t* idx = at<int32_t>(ws, L.topk_idx);
+  float* gate = at<float>(ws, L.topk_gate);
+  int32_t* rows = at<int32_t>(ws, L.row_id_map);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offs = at<int32_t>(ws, L.offsets);
+  __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.x_perm);
+  __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.nv_h);
+  __nv_bfloat16* a = at<__nv_bfloat16>(ws, L.a);
+  uint8_t* q = at<uint8_t>(ws, L.nv_q);
+  uint8_t* sfq = at<uint8_t>(ws, L.nv_sf);
+  float* gq = at<float>(ws, L.nv_g);
+  void* yp = at<void>(ws, L.y_perm);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  prof_mark(s, STAGE_BEGIN);
+  MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
+                     nullptr, nullptr, at<float>(ws, L.logits_raw), st, s));
+  stage_done(s, STAGE_ROUTER, 2);
+  MOE_CUDA(launch_permute(c, xb, idx, xp, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s));
+  stage_done(s, STAGE_PERMUTE, 2);
+  // the routed rows are copies of x's rows: the same tensor maximum
+  MOE_CUDA(launch_nv_amax(xb, static_cast<long long>(c.T) * c.H, 1, gq, s));
+  MOE_CUDA(launch_nv_quantize_grouped(xp, static_cast<int>(R), c.H, c.E, offs, gq, q, sfq, s));
+  stage_done(s, STAGE_NV_QUANT, 3);
+  MOE_TRY(run_gemm_nv(c.E, R, c.H, 2 * c.F, offs, q, sfq, gq, w->w13, w->sf13, w->g13, h, st, s));
+  stage_done(s, STAGE_FFN1, 1);
+  MOE_CUDA(launch_nv_swiglu_amax(h, R, c.F, a, gq + 1, s));
+  MOE_CUDA(launch_nv_quantize_grouped(a, static_cast<int>(R), c.F, c.E, offs, gq + 1, q, sfq, s));
+  stage_done(s, STAGE_NV_QUANT, 3);
+  MOE_TRY(run_gemm_nv(c.E, R, c.F, c.H, offs, q, sfq, gq + 1, w->w2, w->sf2, w->g2,
+                      reinterpret_cast<__nv_bfloat16*>(yp), st, s));
+  stage_done(s, STAGE_FFN2, 1);
+  MOE_CUDA(launch_combine(c, yp, rows, gate, nullptr, y, s));
+  stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
 }
 

@@ -84,11 +84,17 @@ inline size_t nv_weight_sf_bytes(int E, int K, int N) {
 inline size_t nv_act_sf_bytes(long long R, int E, int K) {
   return 2 * static_cast<size_t>((R + 2 * kBM - 1) / (2 * kBM) + E) * (K / kNvKB) * kNvSfBytes;
 }
-cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, float* out_g, cudaStream_t st);
+// tensor scales of `groups` tensors of n_per elements (x2: a second tensor of
+// the same shape whose elements count too)
+cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, float* out_g, cudaStream_t st,
+                           const __nv_bfloat16* x2 = nullptr);
+cudaError_t launch_nv_swiglu_amax(const __nv_bfloat16* h, long long R, int F, __nv_bfloat16* a, float* g,
+                                  cudaStream_t st);
 cudaError_t launch_nv_quantize_rows(const __nv_bfloat16* x, long long M, int K, const float* g, uint8_t* q,
                                     uint8_t* s, cudaStream_t st);
 cudaError_t launch_nv_quantize_weights(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,
-                                       uint8_t* sf, cudaStream_t st);
+                                       uint8_t* sf, cudaStream_t st, const __nv_bfloat16* w_hi = nullptr,
+                                       int split = 0);
 cudaError_t launch_nv_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
                                        const float* g, uint8_t* xq, uint8_t* sf, cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,

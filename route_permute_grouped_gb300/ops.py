@@ -106,6 +106,15 @@ def lib():
         L.moe_nv_grouped_gemm.argtypes = [c_int, c_longlong, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
         for n in ("moe_nv_quantize_weights", "moe_nv_quantize", "moe_nv_grouped_gemm"):
             getattr(L, n).restype = c_int
+        L.moe_nv_layer_weight_bytes.restype = c_size_t
+        L.moe_nv_layer_weight_bytes.argtypes = [POINTER(MoeConfig), c_int]
+        L.moe_nv_workspace_bytes_layer.restype = c_size_t
+        L.moe_nv_workspace_bytes_layer.argtypes = [POINTER(MoeConfig)]
+        L.moe_nv_quantize_layer_weights.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeNvWeights), vp]
+        L.moe_layer_fwd_nvfp4.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, POINTER(MoeNvWeights), vp, vp,
+                                          c_size_t, vp]
+        for n in ("moe_nv_quantize_layer_weights", "moe_layer_fwd_nvfp4"):
+            getattr(L, n).restype = c_int
         _lib = L
     return _lib
 
@@ -434,4 +443,46 @@ def nv_grouped_gemm(x, offsets, w, ws=None, y=None):
     st = lib().moe_nv_grouped_gemm(E, R, K, N, _p(x), _p(offsets), _p(w["wq"]), _p(w["sf"]), _p(w["g"]), _p(y),
                                    _p(ws), ws.numel(), _stream())
     _check(st, "moe_nv_grouped_gemm")
+    return y
+
+
+class MoeNvWeights(ctypes.Structure):
+    """Mirror of moe_nv_weights (six device pointers)."""
+    _fields_ = [(n, c_void_p) for n in ("w13", "sf13", "g13", "w2", "sf2", "g2")]
+
+
+def nv_quantize_layer_weights(cfg, W1, W3, W2):
+    """NVFP4 weights of the layer (dict of uint8 / fp32 device tensors)."""
+    out = {}
+    for i, n in enumerate(MoeNvWeights._fields_):
+        nb = int(lib().moe_nv_layer_weight_bytes(ctypes.byref(cfg), i))
+        if nb == 0:
+            raise MoeError(2, "moe_nv_layer_weight_bytes")
+        dt = torch.float32 if n[0].startswith("g") else torch.uint8
+        out[n[0]] = torch.empty(nb // (4 if dt == torch.float32 else 1), dtype=dt, device=W1.device)
+    st = lib().moe_nv_quantize_layer_weights(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2), ctypes.byref(_nv_struct(out)),
+                                             _stream())
+    _check(st, "moe_nv_quantize_layer_weights")
+    return out
+
+
+def _nv_struct(w):
+    return MoeNvWeights(*[w[n[0]].data_ptr() for n in MoeNvWeights._fields_])
+
+
+def layer_fwd_nvfp4(cfg, x, router_w, nvw, expert_bias=None, logit_bias=None, ws=None, y=None):
+    """Whole layer forward with NVFP4 expert GEMMs (``nvw`` from
+    nv_quantize_layer_weights)."""
+    dev = x.device
+    if y is None:
+        y = torch.empty((cfg.T, cfg.H), dtype=_out_dtype(cfg), device=dev)
+    if ws is None:
+        n = int(lib().moe_nv_workspace_bytes_layer(ctypes.byref(cfg)))
+        if n == 0:
+            raise MoeError(2, "moe_nv_workspace_bytes_layer")
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        ws[:256].zero_()
+    st = lib().moe_layer_fwd_nvfp4(ctypes.byref(cfg), _p(x), _p(router_w), _p(expert_bias), _p(logit_bias),
+                                   ctypes.byref(_nv_struct(nvw)), _p(y), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_fwd_nvfp4")
     return y

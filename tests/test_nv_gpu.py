@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle as O
-from route_permute_grouped_gb300 import ops
+from route_permute_grouped_gb300 import ops, synth
 from tests._util import assert_close, f64
 
 pytestmark = pytest.mark.gpu
@@ -99,3 +99,25 @@ def test_nv_grouped_gemm(counts, K, N):
 def test_nv_rejects_unaligned_shapes():
     assert ops.lib().moe_nv_workspace_bytes(4, 100, 128) == 0   # K not a multiple of 256
     assert ops.lib().moe_nv_weight_bytes(4, 256, 12, 0) == 0     # N not a multiple of 8
+
+
+NV_LAYER_SHAPES = {
+    "tiny": synth.shape("tiny", T=300, H=256, E=8, k=2, F=256),
+    "ragged_skew": synth.shape("tiny", T=777, H=512, E=32, k=4, F=256, skew=1.2),
+    "sigmoid_groups": synth.shape("tiny", T=333, H=256, E=64, k=8, F=256, score="sigmoid", n_groups=8, topk_groups=4,
+                                  gate_scale=2.5, expert_bias_range=0.1),
+}
+
+
+@pytest.mark.parametrize("name", list(NV_LAYER_SHAPES))
+def test_layer_fwd_nvfp4(name):
+    ls = NV_LAYER_SHAPES[name]
+    d = synth.make_layer(ls, seed=1234, device="cuda", training=False)
+    cfg = ops.config_from_shape(ls)
+    w = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
+    y = ops.layer_fwd_nvfp4(cfg, d["x"], d["router_w"], w, d["expert_bias"], d["logit_bias"])
+    torch.cuda.synchronize()
+    n = {k_: (None if v is None else f64(v)) for k_, v in d.items()}
+    ref = O.nv_layer_fwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], ls.k, ls.score, n["expert_bias"],
+                         n["logit_bias"], ls.n_groups, ls.topk_groups, ls.gate_scale)
+    assert_close("y", f64(y), ref["y"], atol=max(2e-2, 2.0 ** -7 * float(np.abs(ref["y"]).max())))

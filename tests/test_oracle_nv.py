@@ -112,3 +112,23 @@ def test_planted_nv_mistake_is_caught(monkeypatch, name, fn, pins):
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+def test_nv_layer_routing_and_fp4_closeness():
+    # routing, counts and the permutation are the bf16 layer's; the output
+    # differs from the exact layer by FP4 rounding (present, and of FP4 size)
+    rng = np.random.default_rng(12)
+    T, H, E, k, F = 64, 256, 4, 2, 256
+    x = rng.normal(size=(T, H))
+    w_r = rng.normal(size=(E, H)) / 16
+    W1 = rng.normal(size=(E, H, F)) / 16
+    W3 = rng.normal(size=(E, H, F)) / 16
+    W2 = rng.normal(size=(E, F, H)) / 16
+    out = O.nv_layer_fwd(x, w_r, W1, W3, W2, k)
+    ref = O.layer_fwd(x, w_r, W1, W3, W2, k, prec=O.EXACT)
+    assert np.array_equal(out["topk_idx"], ref["topk_idx"]) and np.array_equal(out["row_id_map"], ref["row_id_map"])
+    rel = np.linalg.norm(out["y"] - ref["y"]) / np.linalg.norm(ref["y"])
+    assert 0.02 < rel < 0.5, rel
+    # the tokens argument restricts the combine only
+    sub = O.nv_layer_fwd(x, w_r, W1, W3, W2, k, tokens=np.array([3, 7]))
+    np.testing.assert_array_equal(sub["y"][[3, 7]], out["y"][[3, 7]])
