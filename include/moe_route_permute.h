@@ -317,8 +317,11 @@ int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, con
 
 /* NVFP4 layer forward. Quantised weights (device buffers owned by the caller,
  * sizes from moe_nv_layer_weight_bytes, which = 0..5 in field order): w13 /
- * sf13 / g13 are [W1_e | W3_e] (H x 2F, one tensor per expert) in the layout
- * of moe_nv_quantize_weights with N = 2F; w2 / sf2 / g2 are W2 (K = F, N = H). */
+ * g13 are [W1_e | W3_e] (H x 2F, one tensor per expert: codes [E][2F][H/2],
+ * W1's columns then W3's) and sf13 their scales in the gate/up GEMM's tiles
+ * (opaque: tile t = 96 W1 columns 96 t .. then the same W3 columns, blocks as
+ * in moe_nv_quantize_weights); w2 / sf2 / g2 are W2 (K = F, N = H) in the
+ * layout of moe_nv_quantize_weights. */
 typedef struct {
   uint8_t* w13;
   uint8_t* sf13;
@@ -339,9 +342,9 @@ size_t moe_nv_workspace_bytes_layer(const moe_config* cfg);
 
 /* Whole layer forward with NVFP4 expert GEMMs: router, permute and combine as
  * in moe_layer_fwd; the routed rows x_perm (one tensor: x's maximum) are
- * quantised, the gate/up GEMM writes h = bf16(g_x g_e Q(x_perm) Q([W1|W3]))
- * [R, 2F], a = bf16(SiLU(h1) h3) is formed with its maximum, quantised as one
- * tensor, and the down GEMM writes y_perm = bf16(g_a g_e Q(a) Q(W2)). y [T,H]
+ * quantised, the gate/up GEMM forms h = bf16(g_x g_e Q(x_perm) Q([W1|W3]))
+ * and writes a = bf16(SiLU(h1) h3) [R, F] with its maximum, a is quantised as
+ * one tensor, and the down GEMM writes y_perm = bf16(g_a g_e Q(a) Q(W2)). y [T,H]
  * bf16 (fp32 if out_fp32). Requires H and F multiples of 256, F_shared = 0 and
  * inter_fp32 = 0. Inference: intermediates live in the workspace. */
 int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,

@@ -172,9 +172,9 @@ struct WsLayout {
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
-  // NVFP4 forward: gate/up output h [R, 2F] bf16, codes and scales of the
-  // current GEMM's activations (x_perm, then a), their two tensor scales
-  size_t nv_h, nv_q, nv_sf, nv_g;
+  // NVFP4 forward: codes and scales of the current GEMM's activations
+  // (x_perm, then a), their two tensor scales
+  size_t nv_q, nv_sf, nv_g;
   size_t total;
 };
 
@@ -214,7 +214,6 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.a = take(2 * R * F);
   }
   if (nv) {
-    L.nv_h = take(2 * R * 2 * F);
     L.nv_q = take(R * (H > F ? H : F) / 2);
     const size_t sx = nv_act_sf_bytes(static_cast<long long>(R), c.E, c.H);
     const size_t sa = nv_act_sf_bytes(static_cast<long long>(R), c.E, c.F);
@@ -995,7 +994,7 @@ size_t moe_nv_layer_weight_bytes(const moe_config* cfg, int which) {
   const moe_config& c = *cfg;
   switch (which) {
     case 0: return moe_nv_weight_bytes(c.E, c.H, 2 * c.F, 0);
-    case 1: return moe_nv_weight_bytes(c.E, c.H, 2 * c.F, 1);
+    case 1: return nv_weight_sf_bytes_gu(c.E, c.H, c.F);
     case 2: return moe_nv_weight_bytes(c.E, c.H, 2 * c.F, 2);
     case 3: return moe_nv_weight_bytes(c.E, c.F, c.H, 0);
     case 4: return moe_nv_weight_bytes(c.E, c.F, c.H, 1);
@@ -1056,7 +1055,6 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   int32_t* counts = at<int32_t>(ws, L.counts);
   int32_t* offs = at<int32_t>(ws, L.offsets);
   __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.x_perm);
-  __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.nv_h);
   __nv_bfloat16* a = at<__nv_bfloat16>(ws, L.a);
   uint8_t* q = at<uint8_t>(ws, L.nv_q);
   uint8_t* sfq = at<uint8_t>(ws, L.nv_sf);
@@ -1073,9 +1071,32 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_CUDA(launch_nv_amax(xb, static_cast<long long>(c.T) * c.H, 1, gq, s));
   MOE_CUDA(launch_nv_quantize_grouped(xp, static_cast<int>(R), c.H, c.E, offs, gq, q, sfq, s));
   stage_done(s, STAGE_NV_QUANT, 3);
-  MOE_TRY(run_gemm_nv(c.E, R, c.H, 2 * c.F, offs, q, sfq, gq, w->w13, w->sf13, w->g13, h, st, s));
-  stage_done(s, STAGE_FFN1, 1);
-  MOE_CUDA(launch_nv_swiglu_amax(h, R, c.F, a, gq + 1, s));
+  // gate/up GEMM with SiLU * up and the maximum of a in its epilogue
+  MOE_CUDA(cudaMemsetAsync(gq + 1, 0, sizeof(float), s));
+  {
+    GemmParams p = base_params(c, st);
+    p.F = c.F;
+    p.ngroups = c.E;
+    p.offsets = offs;
+    p.M_total = static_cast<int>(R);
+    p.bn = kNvTileN;
+    p.n_tiles = (c.F + kMxTileF1 - 1) / kMxTileF1;
+    p.nt_w = p.n_tiles;
+    p.kb_total = c.H / kNvKB;
+    p.out0 = a;
+    p.nv_ga = gq;
+    p.nv_gb = w->g13;
+    p.nv_amax = reinterpret_cast<unsigned*>(gq + 1);
+    CUtensorMap ma, mb, msa, msb;
+    if (!make_map_u8(&ma, q, c.H / 2, R, 128, kBM)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&mb, w->w13, c.H / 2, 2ull * c.E * c.F, 128, kMxTileF1)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&msa, sfq, 256, nv_act_sf_bytes(R, c.E, c.H) / 256, 256, 8, false)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&msb, w->sf13, 256, nv_weight_sf_bytes_gu(c.E, c.H, c.F) / 256, 256, 16, false))
+      return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_FFN1_NV, p, ma, mb, msa, num_sms(), s, nullptr, &msb));
+  }
+  MOE_CUDA(launch_nv_scale_from_amax(gq + 1, 1, s));
+  stage_done(s, STAGE_FFN1, 2);
   MOE_CUDA(launch_nv_quantize_grouped(a, static_cast<int>(R), c.F, c.E, offs, gq + 1, q, sfq, s));
   stage_done(s, STAGE_NV_QUANT, 3);
   MOE_TRY(run_gemm_nv(c.E, R, c.F, c.H, offs, q, sfq, gq + 1, w->w2, w->sf2, w->g2,

@@ -136,6 +136,47 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
   }
 }
 
+// NVFP4 gate/up epilogue, thread = row r of this CTA's 128 rows of the pair
+// tile, block b (0..2) of the tile's 96 F columns: h = bf16(g_x g_e acc) for
+// the gate (columns 32 b..) and up (96 + 32 b..) halves, a = bf16(SiLU(h1) h3)
+// stored to a[row, col..] (rows of this expert only), and max |a| of the
+// warp's rows into *nv_amax.
+__device__ __forceinline__ void epi_ffn1_nv(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r, int b) {
+  const int col = ti.n0 + 32 * b;
+  if (col >= p.F) return;  // uniform: the last tile of a ragged F
+  const int row = ti.m0 + r;
+  const bool valid = row < ti.m_end;
+  const float alpha = __ldg(p.nv_ga) * __ldg(p.nv_gb + ti.g);
+  uint32_t v1[32], v3[32];
+  tmem_ld32(tacc + 32 * b, v1);
+  tmem_ld32(tacc + kMxTileF1 + 32 * b, v3);
+  tmem_ld_wait();
+  uint32_t o[16];
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float a2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float h1 = __bfloat162float(__float2bfloat16_rn(alpha * __uint_as_float(v1[2 * j + u])));
+      const float h3 = __bfloat162float(__float2bfloat16_rn(alpha * __uint_as_float(v3[2 * j + u])));
+      a2[u] = h1 / (1.0f + expf(-h1)) * h3;
+    }
+    o[j] = pack_bf16x2(a2[0], a2[1]);
+    m = fmaxf(m, fmaxf(fabsf(bf16_lo(o[j])), fabsf(bf16_hi(o[j]))));
+  }
+  if (valid) {
+    uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(row) * p.F + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  } else {
+    m = 0.0f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(p.nv_amax, __float_as_uint(m));
+}
+
 // MXFP8 gate/up epilogue, thread = row r of this CTA's 128 rows of the pair
 // tile, block b (0..2) of the tile's 96 F columns: a = SiLU(h1) h3 (h1 from
 // accumulator columns 32 b.., h3 from 96 + 32 b..) is quantised as one MXFP8
@@ -665,6 +706,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         } else if (any_rows) {
           epi_store(ti, tacc, r, kMxBN / 32, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
         }
+      } else if constexpr (KIND == KIND_FFN1_NV) {
+        epi_ffn1_nv(p, ti, tacc, r, part);
       } else if constexpr (KIND == KIND_GEMM_NV) {
         // y = g_x g_e (sum of the block-scaled products)
         const float alpha = __ldg(p.nv_ga) * __ldg(p.nv_gb + ti.g);
@@ -786,6 +829,7 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
     case KIND_FFN1_MX: return launch_kind<KIND_FFN1_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN2_MX: return launch_kind<KIND_FFN2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_GEMM_NV: return launch_kind<KIND_GEMM_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_FFN1_NV: return launch_kind<KIND_FFN1_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -52,6 +52,8 @@ enum GemmKind : int {
                        // (codes + the down GEMM's tile-ready scales); 256 x (96 gate + 96 up) pair tiles
   KIND_FFN2_MX = 10,   // MXFP8 down: y_perm = Q(a) Q(W2_e), bf16 out; 256 x 192 pair tiles
   KIND_GEMM_NV = 11,   // NVFP4 grouped expert GEMM: y = g_x g_e Q(x_e) Q(W_e), bf16 out; 256 x 192 pair tiles
+  KIND_FFN1_NV = 12,   // NVFP4 gate/up: h = g_x g_e Q(x_perm) Q([W1_e | W3_e]) -> a = bf16(SiLU(h1) h3) and max |a|;
+                       // 256 x (96 gate + 96 up) pair tiles
 };
 
 constexpr int kBM = 128;
@@ -97,7 +99,7 @@ struct KindTraits {
   static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX);
   // NVFP4: like MXFP8 with 256-element k blocks (128 bytes of codes per row)
   // and four scale blocks per operand block (2 KB of A, 4 KB of B scales)
-  static constexpr bool kNv = (KIND == KIND_GEMM_NV);
+  static constexpr bool kNv = (KIND == KIND_GEMM_NV || KIND == KIND_FFN1_NV);
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
                                  KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R ||
                                  KIND == KIND_ROUTER || kMx || kNv);
@@ -112,11 +114,11 @@ struct KindTraits {
   // FFN1_MX runs twelve (three per TMEM lane quadrant, one 32-column block of
   // the 96 SwiGLU columns each): its tiles are short (K / 128 blocks of
   // 128) and its epilogue (SiLU, quantisation) long
-  static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX) ? 12 : 4;
+  static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV) ? 12 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
   static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (kPair ? 6 : 4);
   static constexpr int kOutWarpBytes =
-      (KIND == KIND_DGRAD2R) ? 3 * 4096 : (KIND == KIND_FFN1_MX) ? 0 : 2 * 4096;  // epilogue staging
+      (KIND == KIND_DGRAD2R) ? 3 * 4096 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV) ? 0 : 2 * 4096;  // staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
@@ -153,6 +155,7 @@ struct GemmParams {
   int nt_w;
   const float* nv_ga;    // GEMM_NV: tensor scale of the activations (one value)
   const float* nv_gb;    // GEMM_NV: tensor scales of the experts' weights [ngroups]
+  unsigned* nv_amax;     // FFN1_NV: running max |a| (fp32 bits)
   // status
   DevStatus* status;
   unsigned long long wait_limit_ns;
@@ -214,7 +217,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
   }
   if constexpr (KIND == KIND_FFN1) {
     ti.n0 = nb * 128;  // F columns (gate and up halves of the 256-wide tile)
-  } else if constexpr (KIND == KIND_FFN1_MX) {
+  } else if constexpr (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV) {
     ti.n0 = nb * kMxTileF1;  // F columns (gate and up halves of the 192-wide tile)
   } else {
     ti.n0 = nb * p.bn;
@@ -240,7 +243,12 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
     // blocks (4 KB = 16 rows of msfb)
     const int kc = kb * (kNvKB / 2);
     tma_load_2d_pair(sA, ma, bar_cluster, kc, ti.m0);
-    tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * p.H + ti.n0 + rank * (kNvTileN / 2));
+    if constexpr (KIND == KIND_FFN1_NV) {
+      // W1 rows n0.. (even CTA) or W3 rows n0.. (odd CTA) of expert g ([E][2F] rows)
+      tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * 2 * p.F + rank * p.F + ti.n0);
+    } else {
+      tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * p.H + ti.n0 + rank * (kNvTileN / 2));
+    }
     uint8_t* sSF = sA + kNvSfOff;
     tma_load_2d_pair(sSF, mb1, bar_cluster, 0, 8 * ((2 * ti.mt + rank) * p.kb_total + kb));
     tma_load_2d_pair(sSF + kNvSfBytes, msfb, bar_cluster, 0, 16 * ((ti.g * p.nt_w + ti.nb) * p.kb_total + kb));

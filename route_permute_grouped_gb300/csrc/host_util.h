@@ -81,6 +81,11 @@ inline size_t mx_sfa_bytes(long long R, int E, int K) {
 inline size_t nv_weight_sf_bytes(int E, int K, int N) {
   return static_cast<size_t>(E) * ((N + kNvTileN - 1) / kNvTileN) * (K / kNvKB) * 2 * kNvSfBytes;
 }
+// gate/up weights [W1 | W3] (K = H, 2F columns) in the gate/up GEMM's tiles
+// of 96 W1 + 96 W3 columns
+inline size_t nv_weight_sf_bytes_gu(int E, int K, int F) {
+  return static_cast<size_t>(E) * ((F + kMxTileF1 - 1) / kMxTileF1) * (K / kNvKB) * 2 * kNvSfBytes;
+}
 inline size_t nv_act_sf_bytes(long long R, int E, int K) {
   return 2 * static_cast<size_t>((R + 2 * kBM - 1) / (2 * kBM) + E) * (K / kNvKB) * kNvSfBytes;
 }
@@ -88,8 +93,7 @@ inline size_t nv_act_sf_bytes(long long R, int E, int K) {
 // the same shape whose elements count too)
 cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, float* out_g, cudaStream_t st,
                            const __nv_bfloat16* x2 = nullptr);
-cudaError_t launch_nv_swiglu_amax(const __nv_bfloat16* h, long long R, int F, __nv_bfloat16* a, float* g,
-                                  cudaStream_t st);
+cudaError_t launch_nv_scale_from_amax(float* g, int n, cudaStream_t st);
 cudaError_t launch_nv_quantize_rows(const __nv_bfloat16* x, long long M, int K, const float* g, uint8_t* q,
                                     uint8_t* s, cudaStream_t st);
 cudaError_t launch_nv_quantize_weights(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,

@@ -74,10 +74,14 @@ __global__ void __launch_bounds__(256) nv_quantize_rows_kernel(const __nv_bfloat
 // (B row b = n % 192 of the tile: block b / 128, row b % 128), tensor scale
 // g[e]; thread = one (e, n, kb16): 16 strided loads, coalesced over n.
 // Columns [split, N) come from a second weight w_hi (row stride N - split):
-// the gate/up weights W1 | W3 quantised as one tensor per expert.
+// the gate/up weights W1 | W3 quantised as one tensor per expert. With
+// gate_up set, the scales follow the gate/up GEMM's tiles instead: tile t
+// holds W1 columns 96 t .. as B rows 0..95 and W3 columns 96 t .. as B rows
+// 96..191 (ceil(split / 96) tiles).
 __global__ void __launch_bounds__(256) nv_quantize_weight_kernel(const __nv_bfloat16* __restrict__ w,
                                                                  const __nv_bfloat16* __restrict__ w_hi, int split,
-                                                                 int E, int K, int N, const float* __restrict__ g,
+                                                                 int gate_up, int E, int K, int N,
+                                                                 const float* __restrict__ g,
                                                                  uint8_t* __restrict__ wq, uint8_t* __restrict__ sf) {
   const int nkb16 = K / kNvBlock;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -97,9 +101,18 @@ __global__ void __launch_bounds__(256) nv_quantize_weight_kernel(const __nv_bflo
   const uint32_t sb = nv_quant16(v, g[e], c);
   *reinterpret_cast<uint2*>(wq + (static_cast<size_t>(e) * N + n) * (K / 2) + static_cast<size_t>(kb16) * 8) =
       make_uint2(c[0], c[1]);
-  const int ntiles = (N + kNvTileN - 1) / kNvTileN;
-  const int b = n % kNvTileN;
-  const size_t blk = (static_cast<size_t>(e) * ntiles + n / kNvTileN) * (K / kNvKB) + kb16 / 16;
+  int ntiles, tile, b;
+  if (gate_up) {
+    const int f = hi ? n - split : n;
+    ntiles = (split + kMxTileF1 - 1) / kMxTileF1;
+    tile = f / kMxTileF1;
+    b = f % kMxTileF1 + (hi ? kMxTileF1 : 0);
+  } else {
+    ntiles = (N + kNvTileN - 1) / kNvTileN;
+    tile = n / kNvTileN;
+    b = n % kNvTileN;
+  }
+  const size_t blk = (static_cast<size_t>(e) * ntiles + tile) * (K / kNvKB) + kb16 / 16;
   sf[blk * 2 * kNvSfBytes + (b >> 7) * kNvSfBytes + nv_sf_pos(b & 127, kb16 & 15)] = static_cast<uint8_t>(sb);
 }
 
@@ -199,55 +212,17 @@ cudaError_t launch_nv_quantize_rows(const __nv_bfloat16* x, long long M, int K, 
 
 cudaError_t launch_nv_quantize_weights(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,
                                        uint8_t* sf, cudaStream_t st, const __nv_bfloat16* w_hi, int split) {
-  cudaError_t e = cudaMemsetAsync(sf, 0, nv_weight_sf_bytes(E, K, N), st);
+  const bool gate_up = w_hi != nullptr;
+  cudaError_t e = cudaMemsetAsync(sf, 0, gate_up ? nv_weight_sf_bytes_gu(E, K, split) : nv_weight_sf_bytes(E, K, N), st);
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(E) * (K / kNvBlock) * N;
   nv_quantize_weight_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-      w, w_hi, w_hi != nullptr ? split : N, E, K, N, g, wq, sf);
+      w, w_hi, gate_up ? split : N, gate_up ? 1 : 0, E, K, N, g, wq, sf);
   return cudaGetLastError();
 }
 
-// a[r, f] = bf16(SiLU(h[r, f]) h[r, F + f]) from the gate/up GEMM's bf16 output
-// h [R, 2F], and the maximum |a| (bits, into *amax); thread = 8 columns
-__global__ void __launch_bounds__(256) nv_swiglu_amax_kernel(const __nv_bfloat16* __restrict__ h, long long R, int F,
-                                                             __nv_bfloat16* __restrict__ a, unsigned* __restrict__ amax) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int nv = F / 8;
-  float m = 0.0f;
-  if (i < R * nv) {
-    const long long r = i / nv;
-    const int c = static_cast<int>(i - r * nv) * 8;
-    const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(h + r * 2 * F + c));
-    const uint4 u4 = __ldg(reinterpret_cast<const uint4*>(h + r * 2 * F + F + c));
-    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
-    uint32_t ow[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float g0 = bf16_lo(gw[j]), g1 = bf16_hi(gw[j]);
-      const float a0 = g0 / (1.0f + expf(-g0)) * bf16_lo(uw[j]);
-      const float a1 = g1 / (1.0f + expf(-g1)) * bf16_hi(uw[j]);
-      ow[j] = pack_bf16x2(a0, a1);
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(ow[j])), fabsf(bf16_hi(ow[j]))));
-    }
-    *reinterpret_cast<uint4*>(a + r * F + c) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) atomicMax(amax, __float_as_uint(m));
-}
-
-cudaError_t launch_nv_swiglu_amax(const __nv_bfloat16* h, long long R, int F, __nv_bfloat16* a, float* g,
-                                  cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), st);
-  if (e != cudaSuccess) return e;
-  const long long n = R * (F / 8);
-  if (n > 0) {
-    nv_swiglu_amax_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(h, R, F, a,
-                                                                                  reinterpret_cast<unsigned*>(g));
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  nv_scale_from_amax_kernel<<<1, 32, 0, st>>>(g, 1);
+cudaError_t launch_nv_scale_from_amax(float* g, int n, cudaStream_t st) {
+  nv_scale_from_amax_kernel<<<(n + 255) / 256, 256, 0, st>>>(g, n);
   return cudaGetLastError();
 }
 
