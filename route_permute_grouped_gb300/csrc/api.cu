@@ -210,7 +210,7 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.a_q = take(R * F);
     L.sfa2 = take(mx_sfa_bytes(c.T * c.k, c.E, c.F));
   } else {
-    L.x_perm = take(2 * R * H);
+    if (!nv) L.x_perm = take(2 * R * H);  // the NVFP4 permute writes codes only
     L.a = take(2 * R * F);
   }
   if (nv) {
@@ -1054,7 +1054,6 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   int32_t* rows = at<int32_t>(ws, L.row_id_map);
   int32_t* counts = at<int32_t>(ws, L.counts);
   int32_t* offs = at<int32_t>(ws, L.offsets);
-  __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.x_perm);
   __nv_bfloat16* a = at<__nv_bfloat16>(ws, L.a);
   uint8_t* q = at<uint8_t>(ws, L.nv_q);
   uint8_t* sfq = at<uint8_t>(ws, L.nv_sf);
@@ -1065,12 +1064,11 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
                      nullptr, nullptr, at<float>(ws, L.logits_raw), st, s));
   stage_done(s, STAGE_ROUTER, 2);
-  MOE_CUDA(launch_permute(c, xb, idx, xp, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s));
-  stage_done(s, STAGE_PERMUTE, 2);
-  // the routed rows are copies of x's rows: the same tensor maximum
+  // the routed rows are copies of x's rows: the tensor maximum of x, then the
+  // permute quantises as it scatters
   MOE_CUDA(launch_nv_amax(xb, static_cast<long long>(c.T) * c.H, 1, gq, s));
-  MOE_CUDA(launch_nv_quantize_grouped(xp, static_cast<int>(R), c.H, c.E, offs, gq, q, sfq, s));
-  stage_done(s, STAGE_NV_QUANT, 3);
+  MOE_CUDA(launch_permute(c, xb, idx, nullptr, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s, q, sfq, gq));
+  stage_done(s, STAGE_PERMUTE, 4);
   // gate/up GEMM with SiLU * up and the maximum of a in its epilogue
   MOE_CUDA(cudaMemsetAsync(gq + 1, 0, sizeof(float), s));
   {

@@ -38,11 +38,13 @@ cudaError_t launch_router_select(const moe_config& c, const float* raw, int ld, 
 
 // permute.cu
 // With x_q != nullptr the permute writes MXFP8 rows (x_q [R, H] codes and the
-// tile-ready scales sfa, mx_sfa_bytes(R, E, H) bytes) instead of bf16 x_perm.
+// tile-ready scales sfa, mx_sfa_bytes(R, E, H) bytes) instead of bf16 x_perm;
+// with nv_g != nullptr too, NVFP4 rows with the tensor scale *nv_g (x_q
+// [R, H/2], nv_act_sf_bytes(R, E, H) bytes of scales).
 cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
                            __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
                            int32_t* lookback, DevStatus* st, cudaStream_t stream, uint8_t* x_q = nullptr,
-                           uint8_t* sfa = nullptr);
+                           uint8_t* sfa = nullptr, const float* nv_g = nullptr);
 
 size_t permute_lookback_ints(int T, int E);
 

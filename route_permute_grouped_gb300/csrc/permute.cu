@@ -7,6 +7,7 @@
 
 #include "host_util.h"
 #include "mx.cuh"
+#include "nv.cuh"
 
 namespace moe {
 
@@ -64,12 +65,18 @@ __device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
 // block j goes to scale block 2 P + h, P = the expert's first 256-row pair tile
 // + rel / 256, h = (rel / 128) % 2, k block j / 4 in sfa (row rel % 128, K
 // step j % 4): the blocks the CTA pairs of the expert GEMM read.
+//
+// NV (MX false, nv_g != nullptr): the rows are NVFP4 with the tensor scale
+// *nv_g: 16-element blocks quantised once per token, codes (two per byte) to
+// every destination row, scales to the same pair-tile blocks (2 KB per 128
+// rows and k block of 256).
 template <bool MX>
 __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx, int T, int H, int E, int k,
     const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out, int32_t* __restrict__ lookback,
     __nv_bfloat16* __restrict__ x_perm, int32_t* __restrict__ row_id_map, DevStatus* st,
-    unsigned long long limit_ns, int fault, uint8_t* __restrict__ x_q, uint8_t* __restrict__ sfa) {
+    unsigned long long limit_ns, int fault, uint8_t* __restrict__ x_q, uint8_t* __restrict__ sfa,
+    const float* __restrict__ nv_g) {
   __shared__ int s_ticket;
   __shared__ uint32_t s_mask[2][256];
   __shared__ int s_base[256];
@@ -175,6 +182,41 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
     }
   }
   __syncthreads();
+  if (MX && nv_g != nullptr) {
+    // NVFP4: lane l takes the 16-element blocks l, l+32, ... of the row
+    const float g = *nv_g;
+    const int nblk = H / kNvBlock, nkb = H / kNvKB;
+    for (int j = warp; j < kChunk; j += kScanThreads / 32) {
+      const int t = t0 + j;
+      if (t >= T) break;
+      for (int b = lane; b < nblk; b += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + b * kNvBlock);
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint4 w = __ldg(src + u);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            v[8 * u + 2 * q] = bf16_lo(ww[q]);
+            v[8 * u + 2 * q + 1] = bf16_hi(ww[q]);
+          }
+        }
+        uint32_t c[2];
+        const uint8_t sb = static_cast<uint8_t>(nv_quant16(v, g, c));
+        for (int i = 0; i < k; ++i) {
+          const int r = s_rows[j * k + i];
+          if (r < 0) continue;
+          *reinterpret_cast<uint2*>(x_q + static_cast<size_t>(r) * (H / 2) + b * 8) = make_uint2(c[0], c[1]);
+          const int e = s_exp[j * k + i];
+          const int rel = r - (e == 0 ? 0 : s_scan[e - 1]);
+          const int blk = 2 * ((e == 0 ? 0 : s_tscan[e - 1]) + rel / (2 * kBM)) + ((rel / kBM) & 1);
+          sfa[(static_cast<size_t>(blk) * nkb + b / 16) * kNvSfBytes + nv_sf_pos(rel % kBM, b & 15)] = sb;
+        }
+      }
+    }
+    return;
+  }
   if constexpr (MX) {
     // quantise and scatter: warp w takes tokens w, w+8, ...; lane l the
     // 32-element blocks l, l+32, ... of the row (64 contiguous bytes each)
@@ -241,7 +283,8 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
 
 cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const int32_t* topk_idx,
                            __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
-                           int32_t* lookback, DevStatus* st, cudaStream_t stream, uint8_t* x_q, uint8_t* sfa) {
+                           int32_t* lookback, DevStatus* st, cudaStream_t stream, uint8_t* x_q, uint8_t* sfa,
+                           const float* nv_g) {
   const int T = c.T, E = c.E, k = c.k;
   const int nchunks = (T + kChunk - 1) / kChunk;
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
@@ -258,15 +301,16 @@ cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const in
   if (x_q != nullptr) {
     // scale blocks of rows past an expert's count (the tail of its last m
     // tile) are not written by the scatter: zero scales
-    e = cudaMemsetAsync(sfa, 0, mx_sfa_bytes(T * k, E, c.H), stream);
+    e = cudaMemsetAsync(sfa, 0, nv_g != nullptr ? nv_act_sf_bytes(T * k, E, c.H) : mx_sfa_bytes(T * k, E, c.H),
+                        stream);
     if (e != cudaSuccess) return e;
     permute_scan_scatter_kernel<true><<<nchunks, kScanThreads, 0, stream>>>(
         x, topk_idx, T, c.H, E, k, counts, offsets, lookback, x_perm, row_id_map, st, wait_limit_ns(),
-        debug_fault(), x_q, sfa);
+        debug_fault(), x_q, sfa, nv_g);
   } else {
     permute_scan_scatter_kernel<false><<<nchunks, kScanThreads, 0, stream>>>(
         x, topk_idx, T, c.H, E, k, counts, offsets, lookback, x_perm, row_id_map, st, wait_limit_ns(),
-        debug_fault(), nullptr, nullptr);
+        debug_fault(), nullptr, nullptr, nullptr);
   }
   return cudaGetLastError();
 }
