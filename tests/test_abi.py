@@ -82,3 +82,36 @@ def test_binding_structs_match_the_library(lib):
     assert lib.moe_abi_struct_bytes(0) == ctypes.sizeof(ops.MoeConfig)
     assert lib.moe_abi_struct_bytes(1) == ctypes.sizeof(ops.MoeFwdSaved)
     assert lib.moe_abi_struct_bytes(2) == 0
+
+
+def test_low_precision_entry_points_check_on_the_host(lib):
+    # shapes the block-scaled GEMMs cannot take: sizes are 0, calls are
+    # rejected before any CUDA work (null pointers, bad shapes)
+    ok = ops.make_config(256, 256, 8, 2, 256)
+    bad_h = ops.make_config(256, 192, 8, 2, 256)      # H not a multiple of 128 / 256
+    bad_f = ops.make_config(256, 256, 8, 2, 192)      # F not a multiple of 128 (MXFP8) or 256 (NVFP4)
+    shared = ops.make_config(256, 256, 8, 2, 256, F_shared=64)
+    for i in range(4):
+        assert lib.moe_mx_weight_bytes(ctypes.byref(ok), i) > 0
+        assert lib.moe_mx_weight_bytes(ctypes.byref(bad_h), i) == 0
+        assert lib.moe_mx_weight_bytes(ctypes.byref(bad_f), i) == 0
+    assert lib.moe_mx_workspace_bytes(ctypes.byref(bad_h)) == 0
+    for i in range(6):
+        assert lib.moe_nv_layer_weight_bytes(ctypes.byref(ok), i) > 0
+        assert lib.moe_nv_layer_weight_bytes(ctypes.byref(bad_h), i) == 0
+        assert lib.moe_nv_layer_weight_bytes(ctypes.byref(shared), i) == 0   # no shared expert in the NVFP4 layer
+    assert lib.moe_nv_workspace_bytes_layer(ctypes.byref(bad_f)) == 0
+    assert lib.moe_nv_weight_bytes(4, 256, 8, 0) == 4 * 8 * 128
+    assert lib.moe_nv_weight_bytes(257, 256, 8, 0) == 0                      # more than 256 experts
+    assert lib.moe_nv_workspace_bytes(4, 10, 100) == 0                       # K not a multiple of 256
+    null = ctypes.c_void_p()
+    assert lib.moe_layer_fwd_mxfp8(ctypes.byref(ok), null, null, null, null, None, null, null, null, null, null, 0,
+                                   null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_fwd_nvfp4(ctypes.byref(ok), null, null, null, null, None, null, null, 0,
+                                   null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_nv_grouped_gemm(4, 100, 256, 64, null, null, null, null, null, null, null, 0,
+                                   null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_nv_grouped_gemm(4, 100, 200, 64, null, null, null, null, null, null, null, 0,
+                                   null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_mx_quantize(null, 10, 33, null, null, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_nv_quantize(null, 10, 32, null, null, null, null) == ops.MOE_ERR_INVALID_ARG
