@@ -29,10 +29,11 @@ from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import CONTRACT, permute_plan, route, silu, swiglu_expert
+from .moe_oracle import (CONTRACT, aux_loss, bf16_rne, permute_plan, route, router_backward, silu, silu_grad,
+                         softmax, swiglu_expert)
 
 __all__ = ["E4M3_MAX", "e4m3_round", "e4m3_encode", "e4m3_decode", "e8m0_exponent", "mx_quantize",
-           "mx_dequantize", "mx_roundtrip", "mx_layer_fwd"]
+           "mx_dequantize", "mx_roundtrip", "mx_layer_fwd", "mx_matmul_nt", "mx_layer_bwd"]
 
 E4M3_MAX = 448.0
 MX_BLOCK = 32
@@ -162,3 +163,113 @@ def mx_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
         acc = acc + rt["topk_gate"][tok, i:i + 1] * rows
     y[tok] = prec.r("y", acc)
     return {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": y, "y_perm_rows": yp}
+
+
+def mx_matmul_nt(A, B, quant=True):
+    """A [M, K] times B [N, K] transposed, both operands MXFP8 along their
+    shared K (the GEMM's contraction axis), products summed in fp64.
+    ``quant=False`` replaces the round trips by the identity."""
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    if quant:
+        A, B = mx_roundtrip(A, axis=1), mx_roundtrip(B, axis=1)
+    return A @ B.T
+
+
+def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
+                 topk_groups=1, gate_scale=1.0, aux_coeff=0.0, prec=CONTRACT, experts=None, tokens=None,
+                 force_balanced=False, quant=True):
+    """Forward and backward of the layer with MXFP8 data-gradient GEMMs, for
+    the loss <dO, y> + L_aux.
+
+    The report trains its Blackwell runs in MXFP8 without spelling out the
+    recipe; the reading here quantises every operand of the two data-gradient
+    GEMMs along that GEMM's own contraction axis (as the forward does) and
+    keeps the weight gradients in bf16 with fp32 accumulation:
+
+    forward, per expert e on its rows (as ``mx_layer_fwd``):
+      h1 = Q(x) Q(W1_e), h3 = Q(x) Q(W3_e)       (Q along H)
+      a = SiLU(h1) h3;  y_perm = Q(a) Q(W2_e)    (Q along F; stored per prec.y_perm)
+      saved: h1, h3 stored per prec.h13
+    backward:
+      dy_perm = g dO (per prec.dy_perm); dg = <dO, y_perm>
+      da  = bf16(Q(dy_perm) Q(W2_e)^T)           (Q along H: W2_e [F, H] row-wise)
+      dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)   (saved h13; stored per prec.dh13)
+      a'  = SiLU(h1) h3 from the saved h13       (stored per prec.a)
+      dW2_e = a'^T dy_perm
+      dx_perm = Q([dh1 | dh3]) Q([W1_e | W3_e])^T  (Q along 2F; per prec.dx_perm)
+      dW1_e = x^T dh1, dW3_e = x^T dh3
+      router backward, aux loss and dx = sum of dx_perm rows + dL W_r as in
+      the bf16 layer.
+    No shared expert. ``quant=False`` replaces every MXFP8 round trip by the
+    identity (and leaves da unrounded), which is the bf16 layer's backward
+    on the same stored tensors. Returns the same keys as the bf16 oracle's
+    ``layer_bwd`` (plus ``y``)."""
+    x = np.asarray(x, np.float64)
+    dO = np.asarray(dO, np.float64)
+    T, H = x.shape
+    w_r = np.asarray(w_r, np.float64)
+    E = w_r.shape[0]
+    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
+    idx, gate = rt["topk_idx"], rt["topk_gate"]
+    counts, offsets, row = permute_plan(idx, E)
+    Q = (lambda v, axis: mx_roundtrip(v, axis=axis)) if quant else (lambda v, axis: np.asarray(v, np.float64))
+    need_tok = np.zeros(T, bool)
+    if tokens is None:
+        need_tok[:] = True
+    else:
+        need_tok[np.asarray(tokens)] = True
+    exp_set = set(range(E)) if experts is None else set(int(e) for e in experts)
+    F = np.asarray(W1[0]).shape[1]
+    dgate = np.full((T, k), np.nan)
+    dx = np.zeros((T, H))
+    y = np.zeros((T, H))
+    dW1 = {e: np.zeros((H, F)) for e in exp_set}
+    dW3 = {e: np.zeros((H, F)) for e in exp_set}
+    dW2 = {e: np.zeros((F, H)) for e in exp_set}
+    for e in range(E):
+        tt, ii = np.nonzero(idx == e)                 # rows of expert e, ascending t
+        if len(tt) == 0:
+            continue
+        want = need_tok[tt] if e not in exp_set else np.ones(len(tt), bool)
+        if not want.any():
+            continue
+        tt, ii = tt[want], ii[want]
+        W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+        xr = x[tt]
+        xq = Q(xr, 1)
+        h1 = xq @ Q(W1e, 0)
+        h3 = xq @ Q(W3e, 0)
+        out = prec.r("y_perm", Q(silu(h1) * h3, 1) @ Q(W2e, 0))
+        gsel = gate[tt, ii]
+        y[tt] += gsel[:, None] * out
+        h1s, h3s = prec.r("h13", h1), prec.r("h13", h3)
+        dyr = prec.r("dy_perm", gsel[:, None] * dO[tt])
+        dgate[tt, ii] = np.sum(dO[tt] * out, axis=1)
+        da = mx_matmul_nt(dyr, W2e, quant)            # contraction over H
+        if quant:
+            da = bf16_rne(da)
+        dh1 = prec.r("dh13", da * h3s * silu_grad(h1s))
+        dh3 = prec.r("dh13", da * silu(h1s))
+        a_w = prec.r("a", silu(h1s) * h3s)
+        dxr = prec.r("dx_perm", mx_matmul_nt(np.concatenate([dh1, dh3], axis=1),
+                                             np.concatenate([W1e, W3e], axis=1), quant))  # over 2F
+        np.add.at(dx, tt, dxr)
+        if e in exp_set:
+            dW1[e] += xr.T @ dh1
+            dW3[e] += xr.T @ dh3
+            dW2[e] += a_w.T @ dyr
+    res = {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": y,
+           "dgate": dgate, "dW1": dW1, "dW3": dW3, "dW2": dW2}
+    lg = rt["logits"][need_tok]
+    aux = aux_coeff if score == "softmax" else 0.0
+    dL = router_backward(lg, idx[need_tok], gate[need_tok], dgate[need_tok], score, gate_scale, counts, k, aux,
+                         T_total=T)
+    if aux:
+        res["aux_loss"] = aux_loss(softmax(rt["logits"]), counts, k, aux)
+    dx[need_tok] += dL @ w_r
+    res["dlogits"] = dL
+    res["dx"] = np.where(need_tok[:, None], prec.r("dx", dx), np.nan)
+    if tokens is None:
+        res["dW_r"] = dL.T @ x
+    return res

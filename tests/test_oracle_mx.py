@@ -1,7 +1,11 @@
 """Pins of the MXFP8 oracle (CPU): the E4M3 code table, round-to-nearest-even
 checked against torch's float8_e4m3fn conversion, saturation, the E8M0 scale
-rule on hand-computed blocks, the quantisation error bound, and the MXFP8
-layer forward against its definitions on inputs where quantisation is exact."""
+rule on hand-computed blocks, the quantisation error bound, the MXFP8
+layer forward against its definitions on inputs where quantisation is exact,
+and the MXFP8 training backward: its GEMM helper exact on operands that are
+representable along the contraction axis only, and with the quantisers
+replaced by the identity the bf16 layer's backward (itself pinned by finite
+differences)."""
 import numpy as np
 import pytest
 import torch
@@ -115,6 +119,72 @@ def test_mx_layer_close_to_bf16_layer():
     assert 1e-3 < rel < 0.1  # FP8 error: present, and of FP8 size
 
 
+def _k_exact_operand(rng, M, K):
+    """[M, K]: integers in [-7, 7] times a power of two that is constant over
+    each 32-element block of a row but differs by 2^20 between neighbouring
+    rows, so every block along K is MXFP8-exact while blocks along M are not."""
+    ints = rng.integers(-7, 8, (M, K)).astype(np.float64)
+    ints[:, ::32] = 7.0                                      # every block holds its maximum
+    row_exp = np.where(np.arange(M) % 2 == 0, 0, -20)[:, None]
+    blk_exp = rng.integers(-3, 4, (M, K // 32)).repeat(32, axis=1)
+    return ints * np.ldexp(1.0, row_exp + blk_exp)
+
+
+def test_mx_matmul_nt_exact_along_the_contraction_axis():
+    rng = np.random.default_rng(31)
+    A = _k_exact_operand(rng, 64, 128)
+    B = _k_exact_operand(rng, 96, 128)
+    for V in (A, B):
+        assert np.array_equal(O.mx_roundtrip(V, axis=1), V)
+        assert not np.array_equal(O.mx_roundtrip(V, axis=0), V)  # the other axis would round
+    np.testing.assert_array_equal(O.mx_matmul_nt(A, B), A @ B.T)
+    np.testing.assert_array_equal(O.mx_matmul_nt(A, B, quant=False), A @ B.T)
+
+
+def _train_case(seed, T=24, H=64, E=4, k=2, F=64):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0, 1, (T, H))
+    w_r = rng.normal(0, 0.4, (E, H))
+    W1 = rng.normal(0, H ** -0.5, (E, H, F))
+    W3 = rng.normal(0, H ** -0.5, (E, H, F))
+    W2 = rng.normal(0, F ** -0.5, (E, F, H))
+    dO = rng.normal(0, 1, (T, H))
+    return x, w_r, W1, W3, W2, dO, k
+
+
+def test_mx_layer_bwd_without_quantisation_is_the_bf16_backward():
+    x, w_r, W1, W3, W2, dO, k = _train_case(3)
+    got = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, aux_coeff=1e-2, prec=O.EXACT, quant=False)
+    ref = O.layer_bwd(x, w_r, W1, W3, W2, dO, k, aux_coeff=1e-2, prec=O.EXACT)
+    for key in ("dx", "dW_r", "dgate"):
+        np.testing.assert_allclose(got[key], ref[key], rtol=1e-11, atol=1e-12, err_msg=key)
+    for key in ("dW1", "dW3", "dW2"):
+        for e in ref[key]:
+            np.testing.assert_allclose(got[key][e], ref[key][e], rtol=1e-11, atol=1e-12, err_msg=f"{key}[{e}]")
+    assert got["aux_loss"] == pytest.approx(ref["aux_loss"], rel=1e-14)
+    y = O.layer_fwd(x, w_r, W1, W3, W2, k, prec=O.EXACT)["y"]
+    np.testing.assert_allclose(got["y"], y, rtol=1e-11, atol=1e-12)
+
+
+def test_mx_layer_bwd_forward_is_the_mx_forward():
+    x, w_r, W1, W3, W2, dO, k = _train_case(4, H=128, F=96)
+    got = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    ref = O.mx_layer_fwd(x, w_r, W1, W3, W2, k)
+    np.testing.assert_allclose(got["y"], ref["y"], rtol=1e-12, atol=1e-12)
+
+
+def test_mx_layer_bwd_close_to_bf16_backward():
+    x, w_r, W1, W3, W2, dO, k = _train_case(5, T=64, H=128, E=8, F=96)
+    got = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    ref = O.layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    for key in ("dx", "dW_r"):
+        rel = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert 1e-3 < rel < 0.1, (key, rel)  # FP8 error: present, and of FP8 size
+    num = sum(np.sum((got["dW1"][e] - ref["dW1"][e]) ** 2) for e in ref["dW1"])
+    den = sum(np.sum(ref["dW1"][e] ** 2) for e in ref["dW1"])
+    assert 1e-3 < np.sqrt(num / den) < 0.1
+
+
 # planted mistakes: each must fail at least one pin above
 def _round_half_away(v):
     v = np.asarray(v, np.float64)
@@ -140,14 +210,36 @@ def _scale_ceil(amax):
     return np.where(amax > 0, s, -127).astype(np.int64)
 
 
+def _matmul_wrong_axis(A, B, quant=True):
+    import oracle.mx_oracle as MX
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    if quant:
+        A, B = MX.mx_roundtrip(A, axis=0), MX.mx_roundtrip(B, axis=0)
+    return A @ B.T
+
+
+def _matmul_transposed_operand(A, B, quant=True):
+    import oracle.mx_oracle as MX
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    if quant:
+        A, B = MX.mx_roundtrip(A, axis=1), MX.mx_roundtrip(B, axis=1)
+    return A @ B[::-1].T if B.shape[0] > 1 else A @ B.T
+
+
 MX_MUTATIONS = [
     ("e4m3_round", _round_half_away, [test_e4m3_rounding_matches_torch]),
     ("e4m3_round", _no_saturation, [test_e4m3_saturation]),
     ("e8m0_exponent", _scale_ceil, [test_e8m0_scale_rule_hand_blocks]),
+    ("mx_matmul_nt", _matmul_wrong_axis, [test_mx_matmul_nt_exact_along_the_contraction_axis]),
+    ("mx_matmul_nt", _matmul_transposed_operand,
+     [test_mx_matmul_nt_exact_along_the_contraction_axis, test_mx_layer_bwd_without_quantisation_is_the_bf16_backward]),
 ]
 
 
-@pytest.mark.parametrize("name,fn,pins", MX_MUTATIONS, ids=["half_away", "no_saturation", "scale_ceil"])
+@pytest.mark.parametrize("name,fn,pins", MX_MUTATIONS,
+                         ids=["half_away", "no_saturation", "scale_ceil", "matmul_wrong_axis", "matmul_row_order"])
 def test_planted_mx_mistake_is_caught(monkeypatch, name, fn, pins):
     import oracle.mx_oracle as MX
     monkeypatch.setattr(MX, name, fn)
