@@ -458,6 +458,69 @@ def run_ours(args, ls, rank, world, local_rank):
               "peak_source": f"{peaks['source']} bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"}
         del mxw, wsm, ym
 
+    # ---------------- the MXFP8 training step: forward saving for the
+    # backward, backward with MXFP8 data-gradient GEMMs (weights quantised
+    # once, outside the timed region; the gradient buffers of the bf16 step
+    # reused)
+    mxt = None
+    if training and not args.no_mxfp8 and ls.H % 128 == 0 and ls.F % 128 == 0 and not ls.F_shared:
+        mxw = ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"])
+        mxbw = ops.mx_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+        wst = ops.mx_train_workspace(cfg, dev)
+        svm = ops.alloc_saved_mxfp8(cfg, dev)
+        ym = torch.empty_like(y)
+
+        def step_mx():
+            ops.layer_fwd_mxfp8_train(cfg, d["x"], d["router_w"], mxw, svm, d["expert_bias"], d["logit_bias"],
+                                      ws=wst, y=ym)
+            ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, svm, ws=wst, grads=grads)
+
+        for _ in range(max(3, args.warmup)):
+            step_mx()
+        barrier()
+        cap_t = args.steps * 40 + 64
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ops.profile_start(cap_t)
+        t0.record()
+        for _ in range(args.steps):
+            step_mx()
+        t1.record()
+        torch.cuda.synchronize()
+        ops.profile_stop()
+        assert ops.device_status(wst) == 0
+        ms_mxt = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+        st_mx = {}
+        for name, t in ops.profile_read(cap_t):
+            st_mx.setdefault(name, []).append(t)
+        peak8 = 2 * peaks["bf16_tflops_sustained"]
+        R = ls.T * ls.k
+        tk = {}
+        for name, fl, pk in (("ffn1_gate_up", 2 * R * ls.H * 2 * ls.F, peak8), ("ffn2_down", 2 * R * ls.F * ls.H, peak8),
+                             ("mx_dgrad_down", 2 * R * ls.H * ls.F, peak8),
+                             ("mx_dgrad_gate_up", 2 * R * 2 * ls.F * ls.H, peak8),
+                             ("wgrad_down", 2 * R * ls.F * ls.H, peaks["bf16_tflops_sustained"]),
+                             ("wgrad_gate_up", 2 * R * ls.H * 2 * ls.F, peaks["bf16_tflops_sustained"])):
+            if name in st_mx:
+                avg = sum(st_mx[name]) / len(st_mx[name])
+                ach = fl / (avg * 1e-3) / 1e12
+                tk[name] = {"ms": round(avg, 4), "bound": "tensor", "achieved_tflops": round(ach, 1),
+                            "frac": round(ach / pk, 4)}
+        # algorithmic bytes of the two element-wise MXFP8 kernels
+        for name, nbytes in (("mx_quantize_dy", 3 * R * ls.H), ("mx_swiglu_bwd", 14 * R * ls.F)):
+            if name in st_mx:
+                avg = sum(st_mx[name]) / len(st_mx[name])
+                gbs = nbytes / (avg * 1e-3) / 1e9
+                tk[name] = {"ms": round(avg, 4), "bound": "hbm", "achieved_gbs": round(gbs, 1),
+                            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        for name in ("router", "permute", "combine", "combine_bwd", "router_bwd_elem", "permute_bwd"):
+            if name in st_mx:
+                tk[name] = {"ms": round(sum(st_mx[name]) / len(st_mx[name]), 4)}
+        mxt = {"value": round(job_throughput(layer_flops(ls, True), ms_mxt, world), 2), "unit": "TFLOPS",
+               "ms_per_step": round(ms_mxt, 4),
+               "dtype": "mxfp8 forward and data-gradient GEMMs, bf16 weight gradients (fp32 out)",
+               "vs_bf16_step": round(ms / ms_mxt, 3), "kernels": tk, "peak_fp8_tflops": round(peak8, 1)}
+        del mxw, mxbw, wst, svm, ym
+
     # ---------------- the NVFP4 grouped expert GEMM on the down projection's
     # shape: rows grouped by expert as the forward grouped them (its offsets),
     # the layer's W2 (quantised beforehand), activations quantised per call
@@ -666,7 +729,7 @@ def run_ours(args, ls, rank, world, local_rank):
             "tokens_per_s": round(world * ls.T / (ms * 1e-3), 1),
             "fwd": {"value": round(fwd_value, 2), "unit": "TFLOPS", "ms_per_step": round(ms_fwd, 4),
                     "tokens_per_s": round(world * ls.T / (ms_fwd * 1e-3), 1)},
-            "graph": graph, "mxfp8_fwd": mx, "nvfp4_grouped_gemm": nv, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "graph": graph, "mxfp8_fwd": mx, "mxfp8_train": mxt, "nvfp4_grouped_gemm": nv, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)

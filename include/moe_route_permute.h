@@ -277,6 +277,70 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
                         void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * MXFP8 training step: the forward above saving what the backward needs, and
+ * a backward whose two data-gradient GEMMs run on MXFP8 operands, each
+ * quantised along that GEMM's contraction axis (the report's Blackwell
+ * training runs use MXFP8, figures & tables page, Table 11 and Fig. 30; the
+ * split of the recipe is this library's reading):
+ *   da      = bf16(Q(dy_perm) Q(W2_e)^T)            (blocks along H)
+ *   dh1     = da h3 SiLU'(h1), dh3 = da SiLU(h1)    (saved bf16 h13; bf16)
+ *   dx_perm = bf16(Q([dh1 | dh3]) Q([W1_e | W3_e])^T)  (blocks along 2F)
+ * with the weight gradients in bf16 on the tensor cores (fp32 out):
+ * dW2_e = a_e^T dy_perm_e with a = bf16(SiLU(h1) h3) recomputed from the
+ * saved h13, dW1_e | dW3_e = x_perm_e^T [dh1 | dh3]. Routing, combine, their
+ * backward and the router backward are those of the bf16 layer. Requires H
+ * and F multiples of 128 and F_shared == 0.
+ * ------------------------------------------------------------------------- */
+
+/* The weights of the two data-gradient GEMMs, device buffers owned by the
+ * caller (sizes from moe_mx_bwd_weight_bytes), written by
+ * moe_mx_quantize_bwd_weights:
+ *   w2h  [E][F][H]  E4M3: W2[e] quantised along H (K = H contiguous);
+ *   w13f [E][H][2F] E4M3: row h = W1[e][h][:] then W3[e][h][:], quantised
+ *                   along F (K = 2F contiguous);
+ *   sf2h, sf13f: their E8M0 scales in the tile-ready layout of moe_mx_weights
+ *   (192-row tiles: F rows for w2h, H rows for w13f; w13f's k blocks
+ *   0 .. F/128 - 1 hold W1, the rest W3). */
+typedef struct {
+  uint8_t* w2h;
+  uint8_t* sf2h;
+  uint8_t* w13f;
+  uint8_t* sf13f;
+} moe_mx_bwd_weights;
+
+/* Bytes of the moe_mx_bwd_weights buffers: which = 0 w2h, 1 sf2h, 2 w13f,
+ * 3 sf13f (0 for an invalid config or shape). */
+size_t moe_mx_bwd_weight_bytes(const moe_config* cfg, int which);
+
+/* Quantise W1, W3 [E,H,F] (blocks along F) and W2 [E,F,H] (blocks along H)
+ * into *w. Enqueues on `stream`. */
+int moe_mx_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3,
+                                const moe_bf16* W2, const moe_mx_bwd_weights* w, void* stream);
+
+/* Workspace bytes of moe_layer_fwd_mxfp8_train and moe_layer_bwd_mxfp8 (one
+ * workspace serves both; 0 for an unsupported config). */
+size_t moe_mx_train_workspace_bytes(const moe_config* cfg);
+
+/* Training forward of the MXFP8 layer: the computation of
+ * moe_layer_fwd_mxfp8 (no shared expert) that also fills *saved: topk_idx,
+ * topk_gate, logits, row_id_map, counts, offsets, x_perm (bf16 rows, for the
+ * weight gradient), h13 (bf16 h1 | h3 from the gate/up GEMM's fp32
+ * accumulators), y_perm, aux_partials (when aux_coeff != 0). saved->a is
+ * not used. Every saved buffer is required (MOE_ERR_INVALID_ARG otherwise). */
+int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                              const float* expert_bias, const float* logit_bias, const moe_mx_weights* w,
+                              void* y, const moe_fwd_saved* saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the MXFP8 training step for the loss <dO, y> + L_aux, given the
+ * forward's saved tensors (the workspace need not hold the forward's): outputs as moe_layer_bwd
+ * (dx, dW_router, dW1, dW3, dW2 fp32, aux_loss_out). */
+int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x,
+                        const moe_bf16* router_w, const moe_mx_bwd_weights* w,
+                        const moe_fwd_saved* saved, void* dx, float* dW_router, float* dW1,
+                        float* dW3, float* dW2, float* aux_loss_out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
  * NVFP4 grouped expert GEMM. The report lists NVFP4 among its precisions
  * (summary page, "Modeling" and "Key Terms") without defining it; the format
  * here is NVIDIA's NVFP4: E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6,

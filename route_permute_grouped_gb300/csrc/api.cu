@@ -43,6 +43,7 @@ enum StageTag : int {
   STAGE_COMBINE_BWD = 10, STAGE_ROUTER_BWD = 11, STAGE_DGRAD2 = 12, STAGE_WGRAD2 = 13, STAGE_DGRAD1 = 14,
   STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
   STAGE_NV_QUANT = 20, STAGE_NV_GEMM = 21,
+  STAGE_MX_QUANT = 22, STAGE_MX_SWIGLU_BWD = 23, STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
 };
 // MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
 // report the first stage whose kernels failed (debugging aid, off by default).
@@ -172,6 +173,8 @@ struct WsLayout {
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
+  // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales, da bf16
+  size_t dy_q, sfa_dy, da, dh_q, sfa_dh;
   // NVFP4 forward: codes and scales of the current GEMM's activations
   // (x_perm, then a), their two tensor scales
   size_t nv_q, nv_sf, nv_g;
@@ -209,6 +212,14 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.sfa1 = take(mx_sfa_bytes(c.T * c.k, c.E, c.H));
     L.a_q = take(R * F);
     L.sfa2 = take(mx_sfa_bytes(c.T * c.k, c.E, c.F));
+    if (training) {
+      L.a = take(2 * R * F);  // a recomputed from h13 for the down weight gradient
+      L.dy_q = take(R * H);
+      L.sfa_dy = take(mx_sfa_bytes(c.T * c.k, c.E, c.H));
+      L.da = take(2 * R * F);
+      L.dh_q = take(2 * R * F);
+      L.sfa_dh = take(mx_sfa_bytes(c.T * c.k, c.E, 2 * c.F));
+    }
   } else {
     if (!nv) L.x_perm = take(2 * R * H);  // the NVFP4 permute writes codes only
     L.a = take(2 * R * F);
@@ -376,7 +387,7 @@ static int check_mx_shape(const moe_config& c) {
 // as rows of 256 bytes (A: 2 per block, B: 4 per tile's pair of blocks).
 static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const uint8_t* x_q, const uint8_t* sfa1,
                       const moe_mx_weights& w, uint8_t* a_q, uint8_t* sfa2, void* y, bool y_fp32, DevStatus* st,
-                      cudaStream_t s) {
+                      cudaStream_t s, __nv_bfloat16* h13 = nullptr) {
   GemmParams p = base_params(c, st);
   p.F = c.F;
   p.ngroups = c.E;
@@ -387,6 +398,7 @@ static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const 
   p.nt_w = mx_ntiles1(c);
   p.kb_total = c.H / kMxKB;
   p.out0 = a_q;
+  p.out1 = h13;  // training: bf16 h1 | h3 saved for the backward
   p.sfa_out = sfa2;
   CUtensorMap ma, mb, msa, msb;
   if (!make_map_u8(&ma, x_q, c.H, R, kMxKB, kBM)) return MOE_ERR_CUDA;
@@ -415,6 +427,32 @@ static int run_ffn_mx(const moe_config& c, const int32_t* offsets, int R, const 
   MOE_CUDA(launch_gemm(KIND_FFN2_MX, q, ma2, mb2, msa2, num_sms(), s, &oy, &msb2));
   stage_done(s, STAGE_FFN2, 1);
   return MOE_OK;
+}
+
+// Grouped MXFP8 GEMM y [R, N] bf16 = Q(A) Q(W_e)^T (the down projection's
+// kernel kind with N and K as given): A codes [R, K] with the activations'
+// tile-ready scales (mx_sfa_bytes(R, E, K)), W codes [E][N][K] with the
+// weights' tile-ready scales (tiles of 192 B rows, sfw_bytes in all).
+static int run_gemm_mx(const moe_config& c, const int32_t* offsets, int R, int K, int N, const uint8_t* aq,
+                       const uint8_t* sfa, const uint8_t* wq, const uint8_t* sfw, size_t sfw_bytes,
+                       __nv_bfloat16* y, DevStatus* st, cudaStream_t s) {
+  GemmParams q = base_params(c, st);
+  q.H = N;
+  q.ngroups = c.E;
+  q.offsets = offsets;
+  q.M_total = R;
+  q.bn = kMxBN;
+  q.n_tiles = (N + kMxTileN2 - 1) / kMxTileN2;
+  q.nt_w = q.n_tiles;
+  q.kb_total = K / kMxKB;
+  q.out0 = y;
+  CUtensorMap ma, mb, msa, msb, oy;
+  if (!make_map_u8(&ma, aq, K, R, kMxKB, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb, wq, K, static_cast<uint64_t>(c.E) * N, kMxKB, kMxBN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msa, sfa, 256, mx_sfa_bytes(R, c.E, K) / 256, 256, 2, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb, sfw, 256, sfw_bytes / 256, 256, 4, false)) return MOE_ERR_CUDA;
+  if (!make_map_store(&oy, y, N, R, false)) return MOE_ERR_CUDA;
+  return cuda_status(launch_gemm(KIND_FFN2_MX, q, ma, mb, msa, num_sms(), s, &oy, &msb));
 }
 
 // NVFP4 grouped GEMM on quantised activations: y [R, N] bf16 = g_x g_e (Q(x) Q(W_e))
@@ -639,24 +677,15 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
   return MOE_OK;
 }
 
-int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
-                  const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved, void* dx,
-                  float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws,
-                  size_t ws_bytes, void* stream) {
-  MOE_TRY(check_cfg(cfg));
-  const moe_config& c = *cfg;
-  if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
-    return MOE_ERR_INVALID_ARG;
-  if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
-      !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
-    return MOE_ERR_INVALID_ARG;
-  if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+// The layer backward after the checks. mx != nullptr: the backward of the
+// MXFP8 training step (the data-gradient GEMMs on MXFP8 operands with the
+// weights in mx; W1, W3, W2 unused; the SwiGLU backward in its own kernel).
+static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
+                          const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved,
+                          void* dx, float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out,
+                          void* ws, const WsLayout& L, const moe_mx_bwd_weights* mx, cudaStream_t s) {
   // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
-  const bool recompute = saved->a == nullptr;
-  const WsLayout L = ws_layout(c, true);
-  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool recompute = mx == nullptr && saved->a == nullptr;
   DevStatus* st = at<DevStatus>(ws, 0);
   const int R = c.T * c.k;
   const int Ep = padded_experts(c.E);
@@ -675,7 +704,8 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
   stage_done(s, STAGE_COMBINE_BWD, 1);
   const int n_part = (c.F + 255) / 256;
   float* dg_part = at<float>(ws, L.dg_part);
-  __nv_bfloat16* a_used = recompute ? at<__nv_bfloat16>(ws, L.a) : reinterpret_cast<__nv_bfloat16*>(saved->a);
+  __nv_bfloat16* a_used =
+      (recompute || mx != nullptr) ? at<__nv_bfloat16>(ws, L.a) : reinterpret_cast<__nv_bfloat16*>(saved->a);
   if (recompute) {
     // 3'. da = dy_perm W2_e^T: SwiGLU backward -> dh13, recomputed a -> workspace,
     //     gate-gradient partials <da, a> per row and 256-column tile
@@ -697,7 +727,23 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
                              n_part, saved->row_id_map, saved->counts, Ep, dL_hl, s));
   stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
-  if (!recompute) {
+  if (mx != nullptr) {
+    // MXFP8: dy_perm -> E4M3 rows (blocks along H); da = Q(dy_perm) Q(W2_e)^T
+    // in bf16; the SwiGLU backward -> dh13 bf16, a (for dW2) and the E4M3
+    // rows of dh13 (blocks along 2F)
+    uint8_t* dy_q = at<uint8_t>(ws, L.dy_q);
+    uint8_t* sfa_dy = at<uint8_t>(ws, L.sfa_dy);
+    __nv_bfloat16* da = at<__nv_bfloat16>(ws, L.da);
+    MOE_CUDA(launch_mx_quantize_grouped(dy_perm, R, c.H, c.E, saved->offsets, dy_q, sfa_dy, s));
+    stage_done(s, STAGE_MX_QUANT, 1);
+    MOE_TRY(run_gemm_mx(c, saved->offsets, R, c.H, c.F, dy_q, sfa_dy, mx->w2h, mx->sf2h, mx_sf2h_bytes(c), da, st,
+                        s));
+    stage_done(s, STAGE_MX_DGRAD2, 1);
+    MOE_CUDA(launch_mx_swiglu_bwd(da, reinterpret_cast<const __nv_bfloat16*>(saved->h13), R, c.F, c.E,
+                                  saved->offsets, dh13, a_used, at<uint8_t>(ws, L.dh_q), at<uint8_t>(ws, L.sfa_dh),
+                                  s));
+    stage_done(s, STAGE_MX_SWIGLU_BWD, 1);
+  } else if (!recompute) {
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
     p.n_tiles = (c.F + 255) / 256; p.kb_total = c.H / kBK;
@@ -728,7 +774,11 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     stage_done(s, STAGE_WGRAD2, 1);
   }
   // 5. dx_perm = dh13 [W1_e | W3_e]^T
-  {
+  if (mx != nullptr) {
+    MOE_TRY(run_gemm_mx(c, saved->offsets, R, 2 * c.F, c.H, at<uint8_t>(ws, L.dh_q), at<uint8_t>(ws, L.sfa_dh),
+                        mx->w13f, mx->sf13f, mx_sf13f_bytes(c), dx_perm, st, s));
+    stage_done(s, STAGE_MX_DGRAD1, 1);
+  } else {
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
     p.n_tiles = (c.H + 255) / 256; p.kb_total = 2 * c.F / kBK;
@@ -803,6 +853,25 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
     stage_done(s, STAGE_AUX, 1);
   }
   return MOE_OK;
+}
+
+int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
+                  const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved, void* dx,
+                  float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws,
+                  size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
+      !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return layer_bwd_core(c, dO, x, router_w, W1, W3, W2, saved, dx, dW_router, dW1, dW3, dW2, aux_loss_out, ws, L,
+                        nullptr, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -893,6 +962,100 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
   stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 training step
+// ---------------------------------------------------------------------------
+size_t moe_mx_bwd_weight_bytes(const moe_config* cfg, int which) {
+  if (check_cfg(cfg) != MOE_OK || check_mx_shape(*cfg) != MOE_OK) return 0;
+  const moe_config& c = *cfg;
+  switch (which) {
+    case 0: return static_cast<size_t>(c.E) * c.F * c.H;
+    case 1: return mx_sf2h_bytes(c);
+    case 2: return 2ull * c.E * c.H * c.F;
+    case 3: return mx_sf13f_bytes(c);
+    default: return 0;
+  }
+}
+
+int moe_mx_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                                const moe_mx_bwd_weights* w, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_mx_shape(*cfg));
+  if (!W1 || !W3 || !W2 || !w || !w->w2h || !w->sf2h || !w->w13f || !w->sf13f) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w2h) || !aligned16(w->w13f))
+    return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_mx_quantize_bwd_weights(*cfg, reinterpret_cast<const __nv_bfloat16*>(W1),
+                                          reinterpret_cast<const __nv_bfloat16*>(W3),
+                                          reinterpret_cast<const __nv_bfloat16*>(W2), w->w2h, w->sf2h, w->w13f,
+                                          w->sf13f, static_cast<cudaStream_t>(stream)));
+  count_launches(3);
+  return MOE_OK;
+}
+
+size_t moe_mx_train_workspace_bytes(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK || check_mx_shape(*cfg) != MOE_OK || cfg->F_shared != 0) return 0;
+  return ws_layout(*cfg, true, true).total;
+}
+
+static bool mx_saved_ok(const moe_config& c, const moe_fwd_saved* sv) {
+  return sv && sv->topk_idx && sv->topk_gate && sv->logits && sv->row_id_map && sv->counts && sv->offsets &&
+         sv->x_perm && sv->h13 && sv->y_perm && (c.aux_coeff == 0.0f || sv->aux_partials) &&
+         aligned16(sv->x_perm) && aligned16(sv->h13) && aligned16(sv->y_perm);
+}
+
+int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                              const float* expert_bias, const float* logit_bias, const moe_mx_weights* w, void* y,
+                              const moe_fwd_saved* saved, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_mx_shape(c));
+  if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2 || !y || !ws || !mx_saved_ok(c, saved))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
+      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, true, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  const moe_fwd_saved& sv = *saved;
+  uint8_t* x_q = at<uint8_t>(ws, L.x_q);
+  uint8_t* sfa1 = at<uint8_t>(ws, L.sfa1);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  prof_mark(s, STAGE_BEGIN);
+  MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, sv.topk_idx,
+                     sv.topk_gate, sv.logits, c.aux_coeff != 0.0f ? sv.aux_partials : nullptr,
+                     at<float>(ws, L.logits_raw), st, s));
+  stage_done(s, STAGE_ROUTER, 2);
+  MOE_CUDA(launch_permute(c, xb, sv.topk_idx, reinterpret_cast<__nv_bfloat16*>(sv.x_perm), sv.row_id_map, sv.counts,
+                          sv.offsets, at<int32_t>(ws, L.lookback), st, s, x_q, sfa1));
+  stage_done(s, STAGE_PERMUTE, 2);
+  MOE_TRY(run_ffn_mx(c, sv.offsets, c.T * c.k, x_q, sfa1, *w, at<uint8_t>(ws, L.a_q), at<uint8_t>(ws, L.sfa2),
+                     sv.y_perm, c.inter_fp32 != 0, st, s, reinterpret_cast<__nv_bfloat16*>(sv.h13)));
+  MOE_CUDA(launch_combine(c, sv.y_perm, sv.row_id_map, sv.topk_gate, nullptr, y, s));
+  stage_done(s, STAGE_COMBINE, 1);
+  return MOE_OK;
+}
+
+int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
+                        const moe_mx_bwd_weights* w, const moe_fwd_saved* saved, void* dx, float* dW_router,
+                        float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws, size_t ws_bytes,
+                        void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_mx_shape(c));
+  if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!dO || !x || !router_w || !w || !w->w2h || !w->sf2h || !w->w13f || !w->sf13f || !mx_saved_ok(c, saved) ||
+      !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dO) || !aligned16(w->w2h) || !aligned16(w->w13f) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, true, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return layer_bwd_core(c, dO, x, router_w, nullptr, nullptr, nullptr, saved, dx, dW_router, dW1, dW3, dW2,
+                        aux_loss_out, ws, L, w, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

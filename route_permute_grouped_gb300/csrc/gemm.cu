@@ -204,6 +204,16 @@ __device__ __forceinline__ void epi_ffn1_mx(const GemmParams& p, const TileInfo&
     uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out0) + static_cast<size_t>(row) * p.F + col);
     d[0] = make_uint4(w[0], w[1], w[2], w[3]);
     d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    if (p.out1 != nullptr) {  // training: the pre-activations h1, h3 in bf16
+      __nv_bfloat16* h13 = reinterpret_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(row) * 2 * p.F + col;
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v1[j]);
+      store_bf16x32(h13, f);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v3[j]);
+      store_bf16x32(h13 + p.F, f);
+    }
   }
   const int fb = col / 32;
   p.sfa_out[(static_cast<size_t>(2 * ti.mt + rank) * (p.F / kMxKB) + fb / 4) * kMxSfBytes + mx_sf_pos(r, fb & 3)] =

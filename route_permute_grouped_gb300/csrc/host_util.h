@@ -79,6 +79,15 @@ inline size_t mx_sf2_bytes(const moe_config& c) {
 inline size_t mx_sfa_bytes(long long R, int E, int K) {
   return 2 * static_cast<size_t>((R + 2 * kBM - 1) / (2 * kBM) + E) * (K / kMxKB) * kMxSfBytes;
 }
+// weights of the MXFP8 data-gradient GEMMs: W2 along H (B rows F in tiles of
+// 192) and W1 | W3 along F (one K = 2F operand, B rows H in tiles of 192)
+inline int mx_ntiles_f(const moe_config& c) { return (c.F + kMxTileN2 - 1) / kMxTileN2; }
+inline size_t mx_sf2h_bytes(const moe_config& c) {
+  return static_cast<size_t>(c.E) * mx_ntiles_f(c) * (c.H / kMxKB) * 2 * kMxSfBytes;
+}
+inline size_t mx_sf13f_bytes(const moe_config& c) {
+  return static_cast<size_t>(c.E) * mx_ntiles2(c) * (2 * c.F / kMxKB) * 2 * kMxSfBytes;
+}
 // nv.cu: NVFP4 quantisers and the sizes of the tile-ready scale buffers
 inline size_t nv_weight_sf_bytes(int E, int K, int N) {
   return static_cast<size_t>(E) * ((N + kNvTileN - 1) / kNvTileN) * (K / kNvKB) * 2 * kNvSfBytes;
@@ -108,5 +117,13 @@ cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, 
 cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
                                        const __nv_bfloat16* W2, uint8_t* w13q, uint8_t* sf13, uint8_t* w2q,
                                        uint8_t* sf2, cudaStream_t st);
+cudaError_t launch_mx_quantize_bwd_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
+                                           const __nv_bfloat16* W2, uint8_t* w2h, uint8_t* sf2h, uint8_t* w13f,
+                                           uint8_t* sf13f, cudaStream_t st);
+cudaError_t launch_mx_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
+                                       uint8_t* xq, uint8_t* sf, cudaStream_t st);
+cudaError_t launch_mx_swiglu_bwd(const __nv_bfloat16* da, const __nv_bfloat16* h13, int R, int F, int E,
+                                 const int32_t* offsets, __nv_bfloat16* dh13, __nv_bfloat16* a, uint8_t* dq,
+                                 uint8_t* sf, cudaStream_t st);
 
 }  // namespace moe

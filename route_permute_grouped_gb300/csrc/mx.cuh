@@ -73,4 +73,50 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&
   return sb;
 }
 
+// First 256-row CTA-pair tile of each expert in the grouped GEMMs' schedule:
+// s_pt[e] = sum over e' < e of ceil(rows_e' / 256), from the row offsets
+// s_off[0..E] (E <= 256). Run by one whole warp: lane l sums experts
+// 8 l .. 8 l + 7, then a warp scan; s_pt[E] is the total.
+__device__ __forceinline__ void pair_tile_prefix_warp(const int* s_off, int* s_pt, int E, int lane) {
+  int t[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = 8 * lane + j;
+    t[j] = e < E ? (s_off[e + 1] - s_off[e] + 255) / 256 : 0;
+    sum += t[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = 8 * lane + j;
+    if (e <= E) s_pt[e] = run;
+    run += t[j];
+  }
+}
+
+// expert e with s_off[e] <= row < s_off[e + 1] (binary search over E experts)
+__device__ __forceinline__ int expert_of_row(const int* s_off, int E, int row) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_off[mid] <= row) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Byte offset of the scale of row `rel` (relative to its expert's first row)
+// and 32-element block `b` (of nkb k blocks of 128) in the activations'
+// tile-ready scale blocks: block 2 P + h, P = pt_first + rel / 256 (the
+// row's CTA-pair tile), h = (rel / 128) % 2 (its CTA of the pair).
+__device__ __forceinline__ size_t mx_act_sf_offset(int pt_first, int rel, int b, int nkb) {
+  const int blk = 2 * (pt_first + rel / 256) + ((rel / 128) & 1);
+  return (static_cast<size_t>(blk) * nkb + b / 4) * kMxSfBytes + mx_sf_pos(rel % 128, b & 3);
+}
+
 }  // namespace moe

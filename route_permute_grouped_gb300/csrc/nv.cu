@@ -130,42 +130,14 @@ __global__ void __launch_bounds__(256) nv_quantize_grouped_kernel(const __nv_bfl
   __shared__ int s_pt[kMaxGroups + 1];  // first pair tile of each expert
   for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
   __syncthreads();
-  if (threadIdx.x < 32) {
-    // exclusive prefix of the experts' pair tiles: lane l sums experts
-    // 8 l .. 8 l + 7, then a warp scan
-    const int lane = threadIdx.x;
-    int t[8], sum = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = 8 * lane + j;
-      t[j] = e < E ? (s_off[e + 1] - s_off[e] + 2 * kBM - 1) / (2 * kBM) : 0;
-      sum += t[j];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    int run = incl - sum;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = 8 * lane + j;
-      if (e <= E) s_pt[e] = run;
-      run += t[j];
-    }
-  }
+  if (threadIdx.x < 32) pair_tile_prefix_warp(s_off, s_pt, E, threadIdx.x);
   __syncthreads();
   const int nb = K / kNvBlock;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<long long>(R) * nb) return;
   const int row = static_cast<int>(i / nb);
   const int b = static_cast<int>(i - static_cast<long long>(row) * nb);
-  int lo = 0, hi = E;  // expert e with s_off[e] <= row < s_off[e+1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_off[mid] <= row) lo = mid; else hi = mid;
-  }
+  const int lo = expert_of_row(s_off, E, row);
   const int rel = row - s_off[lo];
   float v[16];
   load_bf16x16(x + static_cast<size_t>(row) * K + b * kNvBlock, v);

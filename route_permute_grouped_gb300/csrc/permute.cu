@@ -64,7 +64,8 @@ __device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
 // destination row of x_q; the scale of row r (rel = r - offset of its expert),
 // block j goes to scale block 2 P + h, P = the expert's first 256-row pair tile
 // + rel / 256, h = (rel / 128) % 2, k block j / 4 in sfa (row rel % 128, K
-// step j % 4): the blocks the CTA pairs of the expert GEMM read.
+// step j % 4): the blocks the CTA pairs of the expert GEMM read. With x_perm
+// non-null (training) the bf16 rows are scattered as well.
 //
 // NV (MX false, nv_g != nullptr): the rows are NVFP4 with the tensor scale
 // *nv_g: 16-element blocks quantised once per token, codes (two per byte) to
@@ -227,10 +228,11 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
       for (int b = lane; b < nblk; b += 32) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + b * kMxBlock);
         float v[32];
+        uint4 raw[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 w = __ldg(src + u);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          raw[u] = __ldg(src + u);
+          const uint32_t ww[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             v[8 * u + 2 * q] = bf16_lo(ww[q]);
@@ -245,6 +247,11 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
           uint4* dst = reinterpret_cast<uint4*>(x_q + static_cast<size_t>(r) * H + b * kMxBlock);
           dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
           dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+          if (x_perm != nullptr) {  // training: the bf16 rows too (weight gradient)
+            uint4* dp = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H + b * kMxBlock);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dp[u] = raw[u];
+          }
           const int e = s_exp[j * k + i];
           const int rel = r - (e == 0 ? 0 : s_scan[e - 1]);
           const int blk = 2 * ((e == 0 ? 0 : s_tscan[e - 1]) + rel / (2 * kBM)) + ((rel / kBM) & 1);

@@ -99,6 +99,17 @@ def lib():
                                           vp, c_size_t, vp]
         for n in ("moe_mx_quantize_weights", "moe_mx_quantize", "moe_layer_fwd_mxfp8"):
             getattr(L, n).restype = c_int
+        L.moe_mx_bwd_weight_bytes.restype = c_size_t
+        L.moe_mx_bwd_weight_bytes.argtypes = [POINTER(MoeConfig), c_int]
+        L.moe_mx_train_workspace_bytes.restype = c_size_t
+        L.moe_mx_train_workspace_bytes.argtypes = [POINTER(MoeConfig)]
+        L.moe_mx_quantize_bwd_weights.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeMxBwdWeights), vp]
+        L.moe_layer_fwd_mxfp8_train.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, POINTER(MoeMxWeights), vp,
+                                                POINTER(MoeFwdSaved), vp, c_size_t, vp]
+        L.moe_layer_bwd_mxfp8.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeMxBwdWeights),
+                                          POINTER(MoeFwdSaved), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+        for n in ("moe_mx_quantize_bwd_weights", "moe_layer_fwd_mxfp8_train", "moe_layer_bwd_mxfp8"):
+            getattr(L, n).restype = c_int
         L.moe_nv_weight_bytes.restype = c_size_t
         L.moe_nv_weight_bytes.argtypes = [c_int, c_int, c_int, c_int]
         L.moe_nv_workspace_bytes.restype = c_size_t
@@ -121,7 +132,8 @@ def lib():
     return _lib
 
 
-STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
+STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 22: "mx_quantize_dy", 23: "mx_swiglu_bwd", 24: "mx_dgrad_down",
+               25: "mx_dgrad_gate_up", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
                17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss"}
@@ -395,6 +407,79 @@ def layer_fwd_mxfp8(cfg, x, router_w, mxw, expert_bias=None, logit_bias=None, Ws
                                    ws.numel(), _stream())
     _check(st, "moe_layer_fwd_mxfp8")
     return y
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 training step (forward saving, backward with MXFP8 data gradients)
+# ---------------------------------------------------------------------------
+class MoeMxBwdWeights(ctypes.Structure):
+    """Mirror of moe_mx_bwd_weights (four device pointers)."""
+    _fields_ = [("w2h", c_void_p), ("sf2h", c_void_p), ("w13f", c_void_p), ("sf13f", c_void_p)]
+
+
+MX_BWD_WEIGHT_FIELDS = ("w2h", "sf2h", "w13f", "sf13f")
+
+
+def mx_quantize_bwd_weights(cfg, W1, W3, W2):
+    """Weights of the MXFP8 data-gradient GEMMs as new uint8 device tensors:
+    w2h [E,F,H] (W2 along H), w13f [E,H,2F] (W1 | W3 along F), sf2h, sf13f."""
+    dev = W1.device
+    out = {}
+    for i, n in enumerate(MX_BWD_WEIGHT_FIELDS):
+        nb = int(lib().moe_mx_bwd_weight_bytes(ctypes.byref(cfg), i))
+        if nb == 0:
+            raise MoeError(2, "moe_mx_bwd_weight_bytes")
+        out[n] = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out["w2h"] = out["w2h"].view(cfg.E, cfg.F, cfg.H)
+    out["w13f"] = out["w13f"].view(cfg.E, cfg.H, 2 * cfg.F)
+    w = MoeMxBwdWeights(*[out[n].data_ptr() for n in MX_BWD_WEIGHT_FIELDS])
+    _check(lib().moe_mx_quantize_bwd_weights(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2), ctypes.byref(w), _stream()),
+           "moe_mx_quantize_bwd_weights")
+    return out
+
+
+def mx_train_workspace(cfg, device="cuda"):
+    n = int(lib().moe_mx_train_workspace_bytes(ctypes.byref(cfg)))
+    if n == 0:
+        raise MoeError(2, "moe_mx_train_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def alloc_saved_mxfp8(cfg, device="cuda"):
+    """Saved tensors of the MXFP8 training forward (``a`` is not kept: the
+    backward recomputes it from ``h13``)."""
+    sv = alloc_saved(cfg, device)
+    sv["a"] = None
+    return sv
+
+
+def layer_fwd_mxfp8_train(cfg, x, router_w, mxw, saved, expert_bias=None, logit_bias=None, ws=None, y=None):
+    """Training forward of the MXFP8 layer (``saved`` from alloc_saved_mxfp8)."""
+    dev = x.device
+    if y is None:
+        y = torch.empty((cfg.T, cfg.H), dtype=_out_dtype(cfg), device=dev)
+    ws = mx_train_workspace(cfg, dev) if ws is None else ws
+    st = lib().moe_layer_fwd_mxfp8_train(ctypes.byref(cfg), _p(x), _p(router_w), _p(expert_bias), _p(logit_bias),
+                                         ctypes.byref(_mx_struct(mxw)), _p(y), ctypes.byref(_saved_struct(saved)),
+                                         _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_fwd_mxfp8_train")
+    return y
+
+
+def layer_bwd_mxfp8(cfg, dO, x, router_w, mxbw, saved, ws=None, grads=None):
+    """Backward of the MXFP8 training step (``mxbw`` from
+    mx_quantize_bwd_weights); gradients as layer_bwd."""
+    dev = x.device
+    g = alloc_grads(cfg, dev) if grads is None else grads
+    ws = mx_train_workspace(cfg, dev) if ws is None else ws
+    w = MoeMxBwdWeights(*[mxbw[n].data_ptr() for n in MX_BWD_WEIGHT_FIELDS])
+    st = lib().moe_layer_bwd_mxfp8(ctypes.byref(cfg), _p(dO), _p(x), _p(router_w), ctypes.byref(w),
+                                   ctypes.byref(_saved_struct(saved)), _p(g["dx"]), _p(g["dW_r"]), _p(g["dW1"]),
+                                   _p(g["dW3"]), _p(g["dW2"]), _p(g["aux_loss"]), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_bwd_mxfp8")
+    return g
 
 
 # ---------------------------------------------------------------------------

@@ -96,6 +96,13 @@ def test_low_precision_entry_points_check_on_the_host(lib):
         assert lib.moe_mx_weight_bytes(ctypes.byref(bad_h), i) == 0
         assert lib.moe_mx_weight_bytes(ctypes.byref(bad_f), i) == 0
     assert lib.moe_mx_workspace_bytes(ctypes.byref(bad_h)) == 0
+    for i in range(4):
+        assert lib.moe_mx_bwd_weight_bytes(ctypes.byref(ok), i) > 0
+        assert lib.moe_mx_bwd_weight_bytes(ctypes.byref(bad_f), i) == 0
+    assert lib.moe_mx_bwd_weight_bytes(ctypes.byref(ok), 0) == 8 * 256 * 256
+    assert lib.moe_mx_train_workspace_bytes(ctypes.byref(ok)) > lib.moe_mx_workspace_bytes(ctypes.byref(ok))
+    assert lib.moe_mx_train_workspace_bytes(ctypes.byref(shared)) == 0      # no shared expert in training
+    assert lib.moe_mx_train_workspace_bytes(ctypes.byref(bad_h)) == 0
     for i in range(6):
         assert lib.moe_nv_layer_weight_bytes(ctypes.byref(ok), i) > 0
         assert lib.moe_nv_layer_weight_bytes(ctypes.byref(bad_h), i) == 0
@@ -113,5 +120,13 @@ def test_low_precision_entry_points_check_on_the_host(lib):
                                    null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_nv_grouped_gemm(4, 100, 200, 64, null, null, null, null, null, null, null, 0,
                                    null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_layer_fwd_mxfp8_train(ctypes.byref(ok), null, null, null, null, None, null, None, null, 0,
+                                         null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_fwd_mxfp8_train(ctypes.byref(shared), null, null, null, null, None, null, None, null, 0,
+                                         null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_layer_bwd_mxfp8(ctypes.byref(ok), null, null, null, None, None, null, null, null, null, null,
+                                   null, null, 0, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_quantize_bwd_weights(ctypes.byref(bad_h), null, null, null, None,
+                                           null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
     assert lib.moe_mx_quantize(null, 10, 33, null, null, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_nv_quantize(null, 10, 32, null, null, null, null) == ops.MOE_ERR_INVALID_ARG
