@@ -282,7 +282,7 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
  * quantised along that GEMM's contraction axis (the report's Blackwell
  * training runs use MXFP8, figures & tables page, Table 11 and Fig. 30; the
  * split of the recipe is this library's reading):
- *   da      = bf16(Q(dy_perm) Q(W2_e)^T)            (blocks along H)
+ *   da      = Q(dy_perm) Q(W2_e)^T                  (blocks along H; fp32, not stored)
  *   dh1     = da h3 SiLU'(h1), dh3 = da SiLU(h1)    (saved bf16 h13; bf16)
  *   dx_perm = bf16(Q([dh1 | dh3]) Q([W1_e | W3_e])^T)  (blocks along 2F)
  * with the weight gradients in bf16 on the tensor cores (fp32 out):

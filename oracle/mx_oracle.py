@@ -29,7 +29,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import (CONTRACT, aux_loss, bf16_rne, permute_plan, route, router_backward, silu, silu_grad,
+from .moe_oracle import (CONTRACT, aux_loss, permute_plan, route, router_backward, silu, silu_grad,
                          softmax, swiglu_expert)
 
 __all__ = ["E4M3_MAX", "e4m3_round", "e4m3_encode", "e4m3_decode", "e8m0_exponent", "mx_quantize",
@@ -193,7 +193,8 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
       saved: h1, h3 stored per prec.h13
     backward:
       dy_perm = g dO (per prec.dy_perm); dg = <dO, y_perm>
-      da  = bf16(Q(dy_perm) Q(W2_e)^T)           (Q along H: W2_e [F, H] row-wise)
+      da  = Q(dy_perm) Q(W2_e)^T                 (Q along H: W2_e [F, H] row-wise; not
+                                                  stored, so not rounded, as in the bf16 layer)
       dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)   (saved h13; stored per prec.dh13)
       a'  = SiLU(h1) h3 from the saved h13       (stored per prec.a)
       dW2_e = a'^T dy_perm
@@ -202,8 +203,7 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
       router backward, aux loss and dx = sum of dx_perm rows + dL W_r as in
       the bf16 layer.
     No shared expert. ``quant=False`` replaces every MXFP8 round trip by the
-    identity (and leaves da unrounded), which is the bf16 layer's backward
-    on the same stored tensors. Returns the same keys as the bf16 oracle's
+    identity, which is the bf16 layer's backward on the same stored tensors. Returns the same keys as the bf16 oracle's
     ``layer_bwd`` (plus ``y``)."""
     x = np.asarray(x, np.float64)
     dO = np.asarray(dO, np.float64)
@@ -247,8 +247,6 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
         dyr = prec.r("dy_perm", gsel[:, None] * dO[tt])
         dgate[tt, ii] = np.sum(dO[tt] * out, axis=1)
         da = mx_matmul_nt(dyr, W2e, quant)            # contraction over H
-        if quant:
-            da = bf16_rne(da)
         dh1 = prec.r("dh13", da * h3s * silu_grad(h1s))
         dh3 = prec.r("dh13", da * silu(h1s))
         a_w = prec.r("a", silu(h1s) * h3s)
