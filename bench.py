@@ -496,7 +496,7 @@ def run_ours(args, ls, rank, world, local_rank):
         R = ls.T * ls.k
         tk = {}
         for name, fl, pk in (("ffn1_gate_up", 2 * R * ls.H * 2 * ls.F, peak8), ("ffn2_down", 2 * R * ls.F * ls.H, peak8),
-                             ("mx_dgrad_down", 2 * R * ls.H * ls.F, peak8),
+                             ("mx_dgrad_down_swiglu", 2 * R * ls.H * ls.F, peak8),
                              ("mx_dgrad_gate_up", 2 * R * 2 * ls.F * ls.H, peak8),
                              ("wgrad_down", 2 * R * ls.F * ls.H, peaks["bf16_tflops_sustained"]),
                              ("wgrad_gate_up", 2 * R * ls.H * 2 * ls.F, peaks["bf16_tflops_sustained"])):
@@ -505,13 +505,6 @@ def run_ours(args, ls, rank, world, local_rank):
                 ach = fl / (avg * 1e-3) / 1e12
                 tk[name] = {"ms": round(avg, 4), "bound": "tensor", "achieved_tflops": round(ach, 1),
                             "frac": round(ach / pk, 4)}
-        # algorithmic bytes of the two element-wise MXFP8 kernels
-        for name, nbytes in (("mx_quantize_dy", 3 * R * ls.H), ("mx_swiglu_bwd", 14 * R * ls.F)):
-            if name in st_mx:
-                avg = sum(st_mx[name]) / len(st_mx[name])
-                gbs = nbytes / (avg * 1e-3) / 1e9
-                tk[name] = {"ms": round(avg, 4), "bound": "hbm", "achieved_gbs": round(gbs, 1),
-                            "frac": round(gbs / peaks["hbm_gbs"], 4)}
         for name in ("router", "permute", "combine", "combine_bwd", "router_bwd_elem", "permute_bwd"):
             if name in st_mx:
                 tk[name] = {"ms": round(sum(st_mx[name]) / len(st_mx[name]), 4)}

@@ -43,7 +43,7 @@ enum StageTag : int {
   STAGE_COMBINE_BWD = 10, STAGE_ROUTER_BWD = 11, STAGE_DGRAD2 = 12, STAGE_WGRAD2 = 13, STAGE_DGRAD1 = 14,
   STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
   STAGE_NV_QUANT = 20, STAGE_NV_GEMM = 21,
-  STAGE_MX_QUANT = 22, STAGE_MX_SWIGLU_BWD = 23, STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
+  STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
 };
 // MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
 // report the first stage whose kernels failed (debugging aid, off by default).
@@ -173,8 +173,8 @@ struct WsLayout {
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
-  // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales, da bf16
-  size_t dy_q, sfa_dy, da, dh_q, sfa_dh;
+  // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales
+  size_t dy_q, sfa_dy, dh_q, sfa_dh;
   // NVFP4 forward: codes and scales of the current GEMM's activations
   // (x_perm, then a), their two tensor scales
   size_t nv_q, nv_sf, nv_g;
@@ -216,7 +216,6 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
       L.a = take(2 * R * F);  // a recomputed from h13 for the down weight gradient
       L.dy_q = take(R * H);
       L.sfa_dy = take(mx_sfa_bytes(c.T * c.k, c.E, c.H));
-      L.da = take(2 * R * F);
       L.dh_q = take(2 * R * F);
       L.sfa_dh = take(mx_sfa_bytes(c.T * c.k, c.E, 2 * c.F));
     }
@@ -453,6 +452,35 @@ static int run_gemm_mx(const moe_config& c, const int32_t* offsets, int R, int K
   if (!make_map_u8(&msb, sfw, 256, sfw_bytes / 256, 256, 4, false)) return MOE_ERR_CUDA;
   if (!make_map_store(&oy, y, N, R, false)) return MOE_ERR_CUDA;
   return cuda_status(launch_gemm(KIND_FFN2_MX, q, ma, mb, msa, num_sms(), s, &oy, &msb));
+}
+
+// MXFP8 data gradient of the down projection with the SwiGLU backward in its
+// epilogue: da = Q(dy_perm) Q(W2_e)^T (K = H, N = F) -> dh13, a (bf16) and the
+// MXFP8 rows of dh13 with their tile-ready scales (K = 2F)
+static int run_dgrad2_mx(const moe_config& c, const int32_t* offsets, int R, const uint8_t* dy_q,
+                         const uint8_t* sfa_dy, const moe_mx_bwd_weights& w, const __nv_bfloat16* h13,
+                         __nv_bfloat16* dh13, __nv_bfloat16* a, uint8_t* dh_q, uint8_t* sfa_dh, DevStatus* st,
+                         cudaStream_t s) {
+  GemmParams q = base_params(c, st);
+  q.H = c.F;  // N of this GEMM
+  q.ngroups = c.E;
+  q.offsets = offsets;
+  q.M_total = R;
+  q.bn = kMxBN;
+  q.n_tiles = mx_ntiles_f(c);
+  q.nt_w = q.n_tiles;
+  q.kb_total = c.H / kMxKB;
+  q.in_aux = h13;
+  q.out0 = dh13;
+  q.out1 = a;
+  q.q_out = dh_q;
+  q.sfa_out = sfa_dh;
+  CUtensorMap ma, mb, msa, msb;
+  if (!make_map_u8(&ma, dy_q, c.H, R, kMxKB, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb, w.w2h, c.H, static_cast<uint64_t>(c.E) * c.F, kMxKB, kMxBN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msa, sfa_dy, 256, mx_sfa_bytes(R, c.E, c.H) / 256, 256, 2, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb, w.sf2h, 256, mx_sf2h_bytes(c) / 256, 256, 4, false)) return MOE_ERR_CUDA;
+  return cuda_status(launch_gemm(KIND_DGRAD2_MX, q, ma, mb, msa, num_sms(), s, nullptr, &msb));
 }
 
 // NVFP4 grouped GEMM on quantised activations: y [R, N] bf16 = g_x g_e (Q(x) Q(W_e))
@@ -698,9 +726,11 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   float* dwr_part = at<float>(ws, L.dwr_part);
 
   prof_mark(s, STAGE_BEGIN);
-  // 1. combine backward (memory-saving: dy_perm only)
+  // 1. combine backward (memory-saving: dy_perm only; MXFP8: dy_perm also
+  //    quantised, blocks of 32 along H)
   MOE_CUDA(launch_combine_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), saved->y_perm, saved->row_id_map,
-                              saved->topk_gate, dy_perm, dgate, s));
+                              saved->topk_gate, dy_perm, dgate, s, mx ? at<uint8_t>(ws, L.dy_q) : nullptr,
+                              mx ? at<uint8_t>(ws, L.sfa_dy) : nullptr, saved->offsets, saved->topk_idx));
   stage_done(s, STAGE_COMBINE_BWD, 1);
   const int n_part = (c.F + 255) / 256;
   float* dg_part = at<float>(ws, L.dg_part);
@@ -728,21 +758,13 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
   if (mx != nullptr) {
-    // MXFP8: dy_perm -> E4M3 rows (blocks along H); da = Q(dy_perm) Q(W2_e)^T
-    // in bf16; the SwiGLU backward -> dh13 bf16, a (for dW2) and the E4M3
-    // rows of dh13 (blocks along 2F)
-    uint8_t* dy_q = at<uint8_t>(ws, L.dy_q);
-    uint8_t* sfa_dy = at<uint8_t>(ws, L.sfa_dy);
-    __nv_bfloat16* da = at<__nv_bfloat16>(ws, L.da);
-    MOE_CUDA(launch_mx_quantize_grouped(dy_perm, R, c.H, c.E, saved->offsets, dy_q, sfa_dy, s));
-    stage_done(s, STAGE_MX_QUANT, 1);
-    MOE_TRY(run_gemm_mx(c, saved->offsets, R, c.H, c.F, dy_q, sfa_dy, mx->w2h, mx->sf2h, mx_sf2h_bytes(c), da, st,
-                        s));
+    // MXFP8: da = Q(dy_perm) Q(W2_e)^T with the SwiGLU backward in the GEMM's
+    // epilogue -> dh13 bf16, a (for dW2) and the E4M3 rows of dh13 (blocks
+    // along 2F)
+    MOE_TRY(run_dgrad2_mx(c, saved->offsets, R, at<uint8_t>(ws, L.dy_q), at<uint8_t>(ws, L.sfa_dy), *mx,
+                          reinterpret_cast<const __nv_bfloat16*>(saved->h13), dh13, a_used, at<uint8_t>(ws, L.dh_q),
+                          at<uint8_t>(ws, L.sfa_dh), st, s));
     stage_done(s, STAGE_MX_DGRAD2, 1);
-    MOE_CUDA(launch_mx_swiglu_bwd(da, reinterpret_cast<const __nv_bfloat16*>(saved->h13), R, c.F, c.E,
-                                  saved->offsets, dh13, a_used, at<uint8_t>(ws, L.dh_q), at<uint8_t>(ws, L.sfa_dh),
-                                  s));
-    stage_done(s, STAGE_MX_SWIGLU_BWD, 1);
   } else if (!recompute) {
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;

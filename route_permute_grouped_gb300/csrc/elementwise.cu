@@ -3,6 +3,7 @@
 // element-wise backward, the auxiliary-loss value and the split-K reduction.
 // One warp per token, 16-byte vectors along H, fp32 arithmetic.
 #include "host_util.h"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -88,19 +89,35 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // of a position are loaded before any store is issued, so the loads of the k
 // rows are in flight together. DG = false (memory-saving backward, no y_perm):
 // dy_perm only; the gate gradient comes from the down-projection dgrad.
-template <bool YP32, int KMAX, bool DG = true>
+// MXQ (the MXFP8 training step): the bf16 dy_perm rows are also quantised
+// (blocks of 32 along H, one block per four lanes) into codes mq [R, H] and
+// scales in the activations' tile-ready layout (msf), the row's expert and
+// its offset from topk_idx and offsets.
+template <bool YP32, int KMAX, bool DG = true, bool MXQ = false>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     combine_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ y_perm,
                        const int32_t* __restrict__ row_id_map, const float* __restrict__ gate,
-                       __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dgate, int T, int H, int k) {
+                       __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dgate, int T, int H, int k,
+                       uint8_t* __restrict__ mq = nullptr, uint8_t* __restrict__ msf = nullptr,
+                       const int32_t* __restrict__ offsets = nullptr, const int32_t* __restrict__ topk_idx = nullptr,
+                       int E = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
+  __shared__ int s_off[MXQ ? kMaxGroups + 1 : 1];
+  __shared__ int s_pt[MXQ ? kMaxGroups + 1 : 1];
+  if constexpr (MXQ) {
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
+    __syncthreads();
+    if (warp == 0) pair_tile_prefix_warp(s_off, s_pt, E, lane);
+    __syncthreads();
+  }
   if (t >= T) return;
-  int my_r = 0;
+  int my_r = 0, my_e = 0;
   float my_g = 0.0f;
   if (lane < k) {
     my_r = row_id_map[static_cast<size_t>(t) * k + lane];
     my_g = gate[static_cast<size_t>(t) * k + lane];
+    if (MXQ) my_e = topk_idx[static_cast<size_t>(t) * k + lane];
   }
   float dot[KMAX];
   int rows[KMAX];
@@ -131,6 +148,41 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
         }
         dot[i] += s;
         Vec8<false>::store(dy_perm, static_cast<size_t>(rows[i]) * H + v * 8, o);
+      }
+    }
+  }
+  if constexpr (MXQ) {
+    // second pass: the MXFP8 rows of dy_perm, from the same products g dO
+    // (the dO row is re-read from cache) rounded to bf16 as stored above; a
+    // block of 32 spans four lanes
+    const unsigned gmask = 0xFu << (lane & ~3);
+    const int nkb = H / kMxKB;
+#pragma unroll 1
+    for (int i = 0; i < k; ++i) {
+      const int r = __shfl_sync(0xffffffffu, my_r, i);
+      const float gi = __shfl_sync(0xffffffffu, my_g, i);
+      const int e = __shfl_sync(0xffffffffu, my_e, i);
+      const size_t sf0 = mx_act_sf_offset(s_pt[e], r - s_off[e], 0, nkb);
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float d[8], o[8];
+        Vec8<false>::load(dO, static_cast<size_t>(t) * H + v * 8, d);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o[j] = __bfloat162float(__float2bfloat16_rn(gi * d[j]));
+          amax = fmaxf(amax, fabsf(o[j]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+        const uint32_t sb = mx_scale_byte(amax);
+        uint32_t w[2];
+        mx_codes8(o, sb, w);
+        *reinterpret_cast<uint2*>(mq + static_cast<size_t>(r) * H + v * 8) = make_uint2(w[0], w[1]);
+        if ((lane & 3) == 0) {
+          const int b = v / 4;
+          msf[sf0 + (b / 4) * kMxSfBytes + (b & 3)] = static_cast<uint8_t>(sb);
+        }
       }
     }
   }
@@ -323,9 +375,22 @@ cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_pe
 
 cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
-                               cudaStream_t st) {
+                               cudaStream_t st, uint8_t* mq, uint8_t* msf, const int32_t* offsets,
+                               const int32_t* topk_idx) {
   const int b = blocks_for(c.T);
   const int th = kWarpsPerBlock * 32;
+  if (mq != nullptr) {  // MXFP8 training step: dy_perm quantised as it is written
+    cudaError_t e = cudaMemsetAsync(msf, 0, mx_sfa_bytes(static_cast<long long>(c.T) * c.k, c.E, c.H), st);
+    if (e != cudaSuccess) return e;
+    if (c.inter_fp32) {
+      if (c.k <= 8) combine_bwd_kernel<true, 8, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
+      else combine_bwd_kernel<true, 16, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
+    } else {
+      if (c.k <= 8) combine_bwd_kernel<false, 8, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
+      else combine_bwd_kernel<false, 16, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
+    }
+    return cudaGetLastError();
+  }
   if (y_perm == nullptr) {  // memory-saving backward: dy_perm only
     if (c.k <= 8) combine_bwd_kernel<false, 8, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k);
     else combine_bwd_kernel<false, 16, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k);

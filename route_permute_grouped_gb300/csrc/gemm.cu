@@ -220,6 +220,74 @@ __device__ __forceinline__ void epi_ffn1_mx(const GemmParams& p, const TileInfo&
       static_cast<uint8_t>(sb);
 }
 
+// DGRAD2_MX, thread = row r of this CTA's 128 rows of the pair tile, 64-column
+// part `part` (0..2) of the tile's 192 F columns (p.H = F here): da from the
+// accumulator and the row's saved bf16 h1, h3 give
+//   dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1) -> dh13 (bf16, out0 [rows, 2F])
+//   a = SiLU(h1) h3                          -> out1 (bf16, [rows, F])
+// and the MXFP8 codes of the bf16 dh1 and dh3 blocks -> q_out [rows, 2F], their
+// scales in the gate/up data gradient's A layout (sfa_out, K = 2F: dh1 block
+// f / 32, dh3 block F / 32 + f / 32). Rows past the expert's end load nothing
+// and store no codes; their scale bytes stay in this expert's own blocks.
+// one 32-column block of dh13 (columns c2.. of [0, 2F)) of DGRAD2_MX's row
+__device__ __forceinline__ void dgrad2_mx_out(const GemmParams& p, const float (&d)[32], int c2, size_t sblk, int r,
+                                              int step, size_t rb, bool valid, __nv_bfloat16* dh13) {
+  uint32_t w[8];
+  const uint32_t sb = mx_quant32(d, w);
+  p.sfa_out[(sblk + c2 / kMxKB) * kMxSfBytes + mx_sf_pos(r, step)] = static_cast<uint8_t>(sb);
+  if (valid) {
+    uint4* q = reinterpret_cast<uint4*>(p.q_out + rb + c2);
+    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    store_bf16x32(dh13 + rb + c2, d);
+  }
+}
+__device__ __forceinline__ void epi_dgrad2_mx(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r,
+                                              int rank, int part) {
+  const int F = p.H;
+  const int row = ti.m0 + r;
+  const bool valid = row < ti.m_end;
+  const int nkb = 2 * F / kMxKB;
+  const size_t sblk = static_cast<size_t>(2 * ti.mt + rank) * nkb;
+  const __nv_bfloat16* h13 = reinterpret_cast<const __nv_bfloat16*>(p.in_aux);
+  __nv_bfloat16* dh13 = reinterpret_cast<__nv_bfloat16*>(p.out0);
+  __nv_bfloat16* aout = reinterpret_cast<__nv_bfloat16*>(p.out1);
+  const size_t rb = static_cast<size_t>(row) * 2 * F;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    const int c = 2 * part + h;  // 32-column block of the tile
+    const int col = ti.n0 + 32 * c;
+    if (col >= F) break;  // uniform: the last tile of a ragged F
+    float g[32], u[32], v[32];
+    // the saved h1, h3 first: their loads are in flight during the TMEM load
+    if (valid) {
+      load_bf16x32(h13 + rb + col, u);
+      load_bf16x32(h13 + rb + F + col, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) u[j] = v[j] = 0.0f;
+    }
+    tmem_ld32f(tacc + 32 * c, g);
+    // in place: g <- dh1, u <- dh3, v <- a
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float s = 1.0f / (1.0f + __expf(-u[j]));
+      const float si = u[j] * s;
+      const float d1 = g[j] * v[j] * (s * (1.0f + u[j] * (1.0f - s)));
+      const float d3 = g[j] * si;
+      v[j] = si * v[j];
+      g[j] = __bfloat162float(__float2bfloat16_rn(d1));
+      u[j] = __bfloat162float(__float2bfloat16_rn(d3));
+    }
+    if (valid) store_bf16x32(aout + static_cast<size_t>(row) * F + col, v);
+    // dh1 (columns col..) then dh3 (F + col..): codes from the bf16 values,
+    // the scale, the bf16 values
+    const int step = (col / kMxBlock) & 3;
+    dgrad2_mx_out(p, g, col, sblk, r, step, rb, valid, dh13);
+    dgrad2_mx_out(p, u, F + col, sblk, r, step, rb, valid, dh13);
+  }
+}
+
 // DGRAD2: accumulator = da for F columns n0..n0+255; SwiGLU backward with the
 // saved bf16 pre-activations h1 (columns [0,F) of h13) and h3 ([F,2F)):
 //   dh1 = da * h3 * SiLU'(h1),  dh3 = da * SiLU(h1).
@@ -716,6 +784,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         } else if (any_rows) {
           epi_store(ti, tacc, r, kMxBN / 32, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
         }
+      } else if constexpr (KIND == KIND_DGRAD2_MX) {
+        epi_dgrad2_mx(p, ti, tacc, r, rank, part);
       } else if constexpr (KIND == KIND_FFN1_NV) {
         epi_ffn1_nv(p, ti, tacc, r, part);
       } else if constexpr (KIND == KIND_GEMM_NV) {
@@ -838,6 +908,7 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
     case KIND_ROUTER_DW: return launch_kind<KIND_ROUTER_DW>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN1_MX: return launch_kind<KIND_FFN1_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN2_MX: return launch_kind<KIND_FFN2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_DGRAD2_MX: return launch_kind<KIND_DGRAD2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_GEMM_NV: return launch_kind<KIND_GEMM_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN1_NV: return launch_kind<KIND_FFN1_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;

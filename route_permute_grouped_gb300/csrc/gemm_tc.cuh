@@ -54,6 +54,9 @@ enum GemmKind : int {
   KIND_GEMM_NV = 11,   // NVFP4 grouped expert GEMM: y = g_x g_e Q(x_e) Q(W_e), bf16 out; 256 x 192 pair tiles
   KIND_FFN1_NV = 12,   // NVFP4 gate/up: h = g_x g_e Q(x_perm) Q([W1_e | W3_e]) -> a = bf16(SiLU(h1) h3) and max |a|;
                        // 256 x (96 gate + 96 up) pair tiles
+  KIND_DGRAD2_MX = 13, // MXFP8 down-projection data gradient: da = Q(dy_perm) Q(W2_e)^T -> SwiGLU backward ->
+                       // dh13 and a (bf16) and dh13 as MXFP8 (codes + the gate/up data gradient's scales);
+                       // 256 x 192 pair tiles
 };
 
 constexpr int kBM = 128;
@@ -96,7 +99,7 @@ struct KindTraits {
   // MXFP8 kinds: CTA pairs on 256 x 192 tiles; a CTA's stage holds 128 k
   // elements (one byte each) of its 128 A rows (16 KB) and 96 B rows (12 KB),
   // its A scale block (0.5 KB) and the tile's B scale blocks (1 KB)
-  static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX);
+  static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX || KIND == KIND_DGRAD2_MX);
   // NVFP4: like MXFP8 with 256-element k blocks (128 bytes of codes per row)
   // and four scale blocks per operand block (2 KB of A, 4 KB of B scales)
   static constexpr bool kNv = (KIND == KIND_GEMM_NV || KIND == KIND_FFN1_NV);
@@ -114,11 +117,16 @@ struct KindTraits {
   // FFN1_MX runs twelve (three per TMEM lane quadrant, one 32-column block of
   // the 96 SwiGLU columns each): its tiles are short (K / 128 blocks of
   // 128) and its epilogue (SiLU, quantisation) long
-  static constexpr int kEpiWarps = (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV) ? 12 : 4;
+  // DGRAD2_MX runs twelve (three per quadrant, 64 of the tile's 192 columns
+  // each) for the same reasons
+  static constexpr int kEpiWarps =
+      (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX) ? 12 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
   static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (kPair ? 6 : 4);
   static constexpr int kOutWarpBytes =
-      (KIND == KIND_DGRAD2R) ? 3 * 4096 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV) ? 0 : 2 * 4096;  // staging
+      (KIND == KIND_DGRAD2R) ? 3 * 4096
+      : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX) ? 0
+                                                                                : 2 * 4096;  // staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
@@ -146,6 +154,7 @@ struct GemmParams {
   void* out1;            // FFN1: h13 save (nullable); WGRAD mode 1: dW3
   const void* in_aux;    // DGRAD2, DGRAD2R: h13 (saved pre-activations)
   float* dg_part;        // DGRAD2R: gate-gradient partials [rows, n_part] (DGRAD2R also stores a in out1)
+  uint8_t* q_out;        // DGRAD2_MX: MXFP8 codes of dh13 [rows, 2F] (scales in sfa_out)
   int n_part;            // DGRAD2R: 256-column tiles of F
   int out_fp32;          // FFN2: y_perm fp32
   // MXFP8 kinds: the activations' scale blocks are read through a tensor map;

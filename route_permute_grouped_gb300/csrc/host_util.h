@@ -51,9 +51,12 @@ size_t permute_lookback_ints(int T, int E);
 // elementwise.cu
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_id_map,
                            const float* gate, const void* shared, void* y, cudaStream_t st);
+// mq != nullptr (MXFP8 training step): also the MXFP8 rows of dy_perm (codes
+// mq [R, H], tile-ready scales msf; offsets and topk_idx locate each row)
 cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
-                               cudaStream_t st);
+                               cudaStream_t st, uint8_t* mq = nullptr, uint8_t* msf = nullptr,
+                               const int32_t* offsets = nullptr, const int32_t* topk_idx = nullptr);
 cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
                                  const float* extra, void* dx, cudaStream_t st);
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx,
@@ -120,10 +123,4 @@ cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16*
 cudaError_t launch_mx_quantize_bwd_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
                                            const __nv_bfloat16* W2, uint8_t* w2h, uint8_t* sf2h, uint8_t* w13f,
                                            uint8_t* sf13f, cudaStream_t st);
-cudaError_t launch_mx_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
-                                       uint8_t* xq, uint8_t* sf, cudaStream_t st);
-cudaError_t launch_mx_swiglu_bwd(const __nv_bfloat16* da, const __nv_bfloat16* h13, int R, int F, int E,
-                                 const int32_t* offsets, __nv_bfloat16* dh13, __nv_bfloat16* a, uint8_t* dq,
-                                 uint8_t* sf, cudaStream_t st);
-
 }  // namespace moe

@@ -128,23 +128,6 @@ __device__ __forceinline__ void st_codes32(uint8_t* dst, const uint32_t (&c)[8])
   d[0] = make_uint4(c[0], c[1], c[2], c[3]);
   d[1] = make_uint4(c[4], c[5], c[6], c[7]);
 }
-// 32 fp32 rounded to bf16 (RNE): stored as 64 bytes, and the rounded values
-// written back into v
-__device__ __forceinline__ void st_bf16x32_round(__nv_bfloat16* dst, float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      w[j] = pack_bf16x2(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]);
-      v[8 * q + 2 * j] = bf16_lo(w[j]);
-      v[8 * q + 2 * j + 1] = bf16_hi(w[j]);
-    }
-    d[q] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 // Weight rows with K contiguous (row n of expert e at w + e * w_estride +
 // n * ldw) -> codes at wq + e * wq_estride + n * ldq + 128 kb_off + 32 kb32
 // and the scale of (n, kb32) in expert e's tile-ready blocks (sf +
@@ -170,86 +153,6 @@ __global__ void __launch_bounds__(256) mx_quantize_weight_rows_kernel(
   const size_t blk = static_cast<size_t>(n / tile_n) * nkb_row + kb_off + kb32 / 4;
   sf[e * sf_estride + blk * 2 * kMxSfBytes + (b >> 7) * kMxSfBytes + mx_sf_pos(b & 127, kb32 & 3)] =
       static_cast<uint8_t>(sb);
-}
-
-// Rows of x [R, K] grouped by expert (offsets[0..E]) -> codes xq [R, K] and
-// the activations' tile-ready scales (mx_act_sf_offset); thread = one
-// 32-element block. Scales of rows past an expert's count keep what the
-// caller put there (zero).
-__global__ void __launch_bounds__(256) mx_quantize_grouped_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
-                                                                  int E, const int32_t* __restrict__ offsets,
-                                                                  uint8_t* __restrict__ xq, uint8_t* __restrict__ sf) {
-  __shared__ int s_off[kMaxGroups + 1];
-  __shared__ int s_pt[kMaxGroups + 1];
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
-  __syncthreads();
-  if (threadIdx.x < 32) pair_tile_prefix_warp(s_off, s_pt, E, threadIdx.x);
-  __syncthreads();
-  const int nb = K / kMxBlock;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<long long>(R) * nb) return;
-  const int row = static_cast<int>(i / nb);
-  const int b = static_cast<int>(i - static_cast<long long>(row) * nb);
-  const int e = expert_of_row(s_off, E, row);
-  float v[32];
-  ld_bf16x32(x + static_cast<size_t>(row) * K + b * kMxBlock, v);
-  uint32_t c[8];
-  const uint32_t sb = mx_quant32(v, c);
-  st_codes32(xq + static_cast<size_t>(row) * K + b * kMxBlock, c);
-  sf[mx_act_sf_offset(s_pt[e], row - s_off[e], b, K / kMxKB)] = static_cast<uint8_t>(sb);
-}
-
-// SwiGLU backward of the MXFP8 training step, per routed row (grouped by
-// expert): from da [R, F] and the saved pre-activations h13 [R, 2F] (h1 in
-// columns [0, F), h3 in [F, 2F)),
-//   dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)  -> dh13 [R, 2F] bf16
-//   a = bf16(SiLU(h1) h3)                      -> a [R, F] (for the weight gradient)
-// and the MXFP8 rows of the bf16 dh13 (blocks of 32 along 2F) -> dq [R, 2F]
-// with the activations' tile-ready scales for K = 2F. Thread = one row and
-// 32-column block b of F: the dh1 block b and the dh3 block F / 32 + b.
-__global__ void __launch_bounds__(256) mx_swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ da,
-                                                            const __nv_bfloat16* __restrict__ h13, int R, int F, int E,
-                                                            const int32_t* __restrict__ offsets,
-                                                            __nv_bfloat16* __restrict__ dh13,
-                                                            __nv_bfloat16* __restrict__ a, uint8_t* __restrict__ dq,
-                                                            uint8_t* __restrict__ sf) {
-  __shared__ int s_off[kMaxGroups + 1];
-  __shared__ int s_pt[kMaxGroups + 1];
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
-  __syncthreads();
-  if (threadIdx.x < 32) pair_tile_prefix_warp(s_off, s_pt, E, threadIdx.x);
-  __syncthreads();
-  const int nb = F / kMxBlock;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<long long>(R) * nb) return;
-  const int row = static_cast<int>(i / nb);
-  const int b = static_cast<int>(i - static_cast<long long>(row) * nb);
-  const size_t rb = static_cast<size_t>(row) * 2 * F;
-  float g[32], h1[32], h3[32], d1[32], d3[32], av[32];
-  ld_bf16x32(da + static_cast<size_t>(row) * F + b * kMxBlock, g);
-  ld_bf16x32(h13 + rb + b * kMxBlock, h1);
-  ld_bf16x32(h13 + rb + F + b * kMxBlock, h3);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float s = 1.0f / (1.0f + __expf(-h1[j]));
-    const float si = h1[j] * s;
-    d1[j] = g[j] * h3[j] * (s * (1.0f + h1[j] * (1.0f - s)));
-    d3[j] = g[j] * si;
-    av[j] = si * h3[j];
-  }
-  st_bf16x32_round(dh13 + rb + b * kMxBlock, d1);
-  st_bf16x32_round(dh13 + rb + F + b * kMxBlock, d3);
-  st_bf16x32_round(a + static_cast<size_t>(row) * F + b * kMxBlock, av);
-  const int e = expert_of_row(s_off, E, row);
-  const int rel = row - s_off[e];
-  const int nkb = 2 * F / kMxKB;
-  uint32_t c[8];
-  uint32_t sb = mx_quant32(d1, c);  // from the bf16 values just stored
-  st_codes32(dq + rb + b * kMxBlock, c);
-  sf[mx_act_sf_offset(s_pt[e], rel, b, nkb)] = static_cast<uint8_t>(sb);
-  sb = mx_quant32(d3, c);
-  st_codes32(dq + rb + F + b * kMxBlock, c);
-  sf[mx_act_sf_offset(s_pt[e], rel, nb + b, nkb)] = static_cast<uint8_t>(sb);
 }
 
 // Weights of the two data-gradient GEMMs: W2 [E, F, H] quantised along H
@@ -281,26 +184,6 @@ cudaError_t launch_mx_quantize_bwd_weights(const moe_config& c, const __nv_bfloa
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
-}
-
-cudaError_t launch_mx_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
-                                       uint8_t* xq, uint8_t* sf, cudaStream_t st) {
-  cudaError_t err = cudaMemsetAsync(sf, 0, mx_sfa_bytes(R, E, K), st);
-  if (err != cudaSuccess || R == 0) return err;
-  const long long n = static_cast<long long>(R) * (K / kMxBlock);
-  mx_quantize_grouped_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(x, R, K, E, offsets, xq, sf);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_mx_swiglu_bwd(const __nv_bfloat16* da, const __nv_bfloat16* h13, int R, int F, int E,
-                                 const int32_t* offsets, __nv_bfloat16* dh13, __nv_bfloat16* a, uint8_t* dq,
-                                 uint8_t* sf, cudaStream_t st) {
-  cudaError_t err = cudaMemsetAsync(sf, 0, mx_sfa_bytes(R, E, 2 * F), st);
-  if (err != cudaSuccess || R == 0) return err;
-  const long long n = static_cast<long long>(R) * (F / kMxBlock);
-  mx_swiglu_bwd_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(da, h13, R, F, E, offsets, dh13, a,
-                                                                               dq, sf);
-  return cudaGetLastError();
 }
 
 }  // namespace moe

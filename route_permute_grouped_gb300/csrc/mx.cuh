@@ -57,6 +57,15 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// E4M3 codes of 8 elements of a block whose scale byte is sb (w[0] holds
+// elements 0..3, low byte first)
+__device__ __forceinline__ void mx_codes8(const float (&v)[8], uint32_t sb, uint32_t (&w)[2]) {
+  const float inv = __uint_as_float((254u - sb) << 23);  // 1 / X, as in mx_quant32
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    w[j] = cvt_e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv) | (cvt_e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv) << 16);
+}
+
 // Quantise one 32-element block: codes in w[0..7] (byte j of the block at
 // byte j of w), returns the scale byte.
 __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&w)[8]) {

@@ -228,11 +228,10 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
       for (int b = lane; b < nblk; b += 32) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + b * kMxBlock);
         float v[32];
-        uint4 raw[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          raw[u] = __ldg(src + u);
-          const uint32_t ww[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+          const uint4 w = __ldg(src + u);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             v[8 * u + 2 * q] = bf16_lo(ww[q]);
@@ -247,15 +246,22 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
           uint4* dst = reinterpret_cast<uint4*>(x_q + static_cast<size_t>(r) * H + b * kMxBlock);
           dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
           dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-          if (x_perm != nullptr) {  // training: the bf16 rows too (weight gradient)
-            uint4* dp = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H + b * kMxBlock);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) dp[u] = raw[u];
-          }
           const int e = s_exp[j * k + i];
           const int rel = r - (e == 0 ? 0 : s_scan[e - 1]);
           const int blk = 2 * ((e == 0 ? 0 : s_tscan[e - 1]) + rel / (2 * kBM)) + ((rel / kBM) & 1);
           sfa[(static_cast<size_t>(blk) * nkb + b / 4) * kMxSfBytes + mx_sf_pos(rel % kBM, b & 3)] = sb;
+        }
+      }
+      if (x_perm != nullptr) {
+        // training: the bf16 rows too (weight gradient), 16-byte vectors,
+        // lane l taking vectors l, l + 32, ... (the row is in cache)
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+        for (int vv = lane; vv < H / 8; vv += 32) {
+          const uint4 w = __ldg(src + vv);
+          for (int i = 0; i < k; ++i) {
+            const int r = s_rows[j * k + i];
+            if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H)[vv] = w;
+          }
         }
       }
     }

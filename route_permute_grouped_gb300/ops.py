@@ -132,7 +132,7 @@ def lib():
     return _lib
 
 
-STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 22: "mx_quantize_dy", 23: "mx_swiglu_bwd", 24: "mx_dgrad_down",
+STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 24: "mx_dgrad_down_swiglu",
                25: "mx_dgrad_gate_up", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
