@@ -3,14 +3,16 @@ configuration the benchmark times, checked on sampled outputs the oracle
 computes one by one: the MXFP8 layer on the Qwen3 expert shape (H=4096,
 F=1536, top-8; 32 experts, T=4096) for 48 sampled tokens, and the NVFP4
 grouped GEMM on the down projection's full shape (131072 x 1536 x 4096, 128
-experts) for the rows of three experts."""
+experts) for the rows of three experts, and the MXFP8 training step on the
+full Qwen3 training workload (T=16384, E=128) for one token's output and input
+gradient and one expert's weight gradients."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import assert_close, f64
+from tests._util import TIE_MARGIN, assert_close, compare_topk, f64, wgrad_atol
 
 pytestmark = pytest.mark.gpu
 
@@ -57,3 +59,52 @@ def test_nvfp4_grouped_gemm_full_shape_sampled():
         We = O.nv_roundtrip(f64(W[e]).astype(np.float32), axis=0)
         ref = O.bf16_rne(xq @ We)
         assert_close(f"y rows of expert {e}", f64(y[lo:hi]), ref, atol=max(2e-2, 2.0 ** -7 * float(np.abs(ref).max())))
+
+
+class _PerExpert:
+    """W[e] as an fp64 array, converted from the device tensor on demand."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        return f64(self.t[e])
+
+
+def test_mxfp8_train_qwen3_full_sampled():
+    ls = synth.shape("qwen3_train")
+    d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
+    cfg = ops.config_from_shape(ls, out_fp32=True)
+    mxw = ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"])
+    mxbw = ops.mx_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+    ws = ops.mx_train_workspace(cfg)
+    saved = ops.alloc_saved_mxfp8(cfg)
+    y = ops.layer_fwd_mxfp8_train(cfg, d["x"], d["router_w"], mxw, saved, ws=ws)
+    g = ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, saved, ws=ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    x, w_r, dO = f64(d["x"]), f64(d["router_w"]), f64(d["dO"])
+    k = ls.k
+    rt = O.route(x, w_r, k)
+    zs = -np.sort(-rt["z"], axis=1)
+    ties = np.nonzero(zs[:, k - 1] - zs[:, k] < TIE_MARGIN)[0]
+    ok = np.ones(ls.T, bool)
+    ok[ties] = False
+    # selected sets exact outside near-ties (slot order where the scores are separated)
+    compare_topk(saved["topk_idx"].cpu().numpy(), rt["topk_idx"], rt["z"], k)
+    # experts a near-tie token could move to or from are not sampled
+    near = set()
+    for t in ties:
+        near.update(int(e) for e in np.argsort(-rt["z"][t], kind="stable")[k - 1:k + 1])
+    counts = np.bincount(rt["topk_idx"].reshape(-1), minlength=ls.E)
+    cand = [e for e in np.argsort(counts, kind="stable") if int(e) not in near]
+    e0 = int(cand[len(cand) // 2])
+    t0 = int(np.random.default_rng(7).choice(np.nonzero(ok)[0]))
+    ref = O.mx_layer_bwd(x, w_r, _PerExpert(d["W1"]), _PerExpert(d["W3"]), _PerExpert(d["W2"]), dO, k,
+                         aux_coeff=ls.aux_coeff, prec=O.Precision(y=False, dx=False), experts=[e0], tokens=[t0])
+    assert_close("y (sampled token)", f64(y)[t0], ref["y"][t0])
+    assert_close("dx (sampled token)", f64(g["dx"])[t0], ref["dx"][t0], atol=wgrad_atol(ref["dx"][t0]))
+    for key in ("dW1", "dW3", "dW2"):
+        want = ref[key][e0]
+        assert_close(f"{key} (expert {e0}, {counts[e0]} rows)", f64(g[key][e0]), want, atol=wgrad_atol(want))
+    assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))
