@@ -33,7 +33,7 @@ from .moe_oracle import (CONTRACT, aux_loss, permute_plan, route, router_backwar
                          softmax, swiglu_expert)
 
 __all__ = ["E4M3_MAX", "e4m3_round", "e4m3_encode", "e4m3_decode", "e8m0_exponent", "mx_quantize",
-           "mx_dequantize", "mx_roundtrip", "mx_layer_fwd", "mx_matmul_nt", "mx_layer_bwd"]
+           "mx_dequantize", "mx_roundtrip", "mx_layer_fwd", "mx_matmul_nt", "mx_matmul_tn", "mx_layer_bwd"]
 
 E4M3_MAX = 448.0
 MX_BLOCK = 32
@@ -176,16 +176,33 @@ def mx_matmul_nt(A, B, quant=True):
     return A @ B.T
 
 
+def mx_matmul_tn(A, B, quant=True):
+    """A [K, M] transposed times B [K, N], both operands MXFP8 along their
+    shared K (axis 0, the GEMM's contraction axis) in blocks of 32 from row 0;
+    a last partial block is quantised as if zero-padded to 32 rows (zeros
+    change neither a block's maximum nor the products). Products summed in
+    fp64. ``quant=False`` replaces the round trips by the identity."""
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    if quant:
+        K = A.shape[0]
+        pad = (-K) % MX_BLOCK
+        A = mx_roundtrip(np.concatenate([A, np.zeros((pad, A.shape[1]))]), axis=0)[:K]
+        B = mx_roundtrip(np.concatenate([B, np.zeros((pad, B.shape[1]))]), axis=0)[:K]
+    return A.T @ B
+
+
 def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
                  topk_groups=1, gate_scale=1.0, aux_coeff=0.0, prec=CONTRACT, experts=None, tokens=None,
-                 force_balanced=False, quant=True):
-    """Forward and backward of the layer with MXFP8 data-gradient GEMMs, for
-    the loss <dO, y> + L_aux.
+                 force_balanced=False, quant=True, wgrad="mxfp8"):
+    """Forward and backward of the layer with MXFP8 expert GEMMs, for the
+    loss <dO, y> + L_aux.
 
     The report trains its Blackwell runs in MXFP8 without spelling out the
-    recipe; the reading here quantises every operand of the two data-gradient
-    GEMMs along that GEMM's own contraction axis (as the forward does) and
-    keeps the weight gradients in bf16 with fp32 accumulation:
+    recipe; the reading here quantises both operands of every expert GEMM
+    along that GEMM's own contraction axis, as the forward does: along H or
+    F for the data gradients, along the expert's tokens for the weight
+    gradients (``wgrad="bf16"`` keeps those in bf16):
 
     forward, per expert e on its rows (as ``mx_layer_fwd``):
       h1 = Q(x) Q(W1_e), h3 = Q(x) Q(W3_e)       (Q along H)
@@ -197,9 +214,10 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
                                                   stored, so not rounded, as in the bf16 layer)
       dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)   (saved h13; stored per prec.dh13)
       a'  = SiLU(h1) h3 from the saved h13       (stored per prec.a)
-      dW2_e = a'^T dy_perm
+      dW2_e = Q(a')^T Q(dy_perm)                 (Q along the expert's tokens)
       dx_perm = Q([dh1 | dh3]) Q([W1_e | W3_e])^T  (Q along 2F; per prec.dx_perm)
-      dW1_e = x^T dh1, dW3_e = x^T dh3
+      dW1_e = Q(x)^T Q(dh1), dW3_e = Q(x)^T Q(dh3)  (Q along the expert's tokens;
+                                                 x = the bf16 rows of x_perm)
       router backward, aux loss and dx = sum of dx_perm rows + dL W_r as in
       the bf16 layer.
     No shared expert. ``quant=False`` replaces every MXFP8 round trip by the
@@ -254,9 +272,10 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
                                              np.concatenate([W1e, W3e], axis=1), quant))  # over 2F
         np.add.at(dx, tt, dxr)
         if e in exp_set:
-            dW1[e] += xr.T @ dh1
-            dW3[e] += xr.T @ dh3
-            dW2[e] += a_w.T @ dyr
+            wq = quant and wgrad == "mxfp8"
+            dW1[e] += mx_matmul_tn(xr, dh1, wq)
+            dW3[e] += mx_matmul_tn(xr, dh3, wq)
+            dW2[e] += mx_matmul_tn(a_w, dyr, wq)
     res = {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": y,
            "dgate": dgate, "dW1": dW1, "dW3": dW3, "dW2": dW2}
     lg = rt["logits"][need_tok]

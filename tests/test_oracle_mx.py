@@ -141,6 +141,45 @@ def test_mx_matmul_nt_exact_along_the_contraction_axis():
     np.testing.assert_array_equal(O.mx_matmul_nt(A, B, quant=False), A @ B.T)
 
 
+def _token_exact_operand(rng, K, M):
+    """[K, M]: integers in [-7, 7] times 2^(b + c), b alternating 0 / -16 over
+    the 32-row blocks counted from row 0 and c alternating 0 / -20 over the
+    columns, each block's first row holding its maximum: exact in MXFP8 along
+    axis 0 in blocks aligned at row 0 (a misaligned block mixes exponents 16
+    apart and rounds the small ones), not along axis 1."""
+    ints = rng.integers(-7, 8, (K, M)).astype(np.float64)
+    ints[::32] = 7.0
+    blk = np.where((np.arange(K) // 32) % 2 == 0, 0, -16)[:, None]
+    col = np.where(np.arange(M) % 2 == 0, 0, -20)[None, :]
+    return ints * np.ldexp(1.0, blk + col)
+
+
+def test_mx_matmul_tn_exact_along_tokens_with_a_ragged_last_block():
+    # [K, M] operands exact along axis 0 in blocks of 32 from row 0 (the last
+    # block has 16 rows), not along axis 1
+    rng = np.random.default_rng(32)
+    A = _token_exact_operand(rng, 80, 64)
+    B = _token_exact_operand(rng, 80, 96)
+    for V in (A, B):
+        pad = np.concatenate([V, np.zeros((16, V.shape[1]))])
+        assert np.array_equal(O.mx_roundtrip(pad, axis=0)[:80], V)
+        assert not np.array_equal(O.mx_roundtrip(V, axis=1), V)
+    np.testing.assert_array_equal(O.mx_matmul_tn(A, B), A.T @ B)
+    np.testing.assert_array_equal(O.mx_matmul_tn(A, B, quant=False), A.T @ B)
+
+
+def test_mx_weight_gradients_quantised_along_tokens():
+    x, w_r, W1, W3, W2, dO, k = _train_case(6, T=64, H=128, E=4, F=96)
+    q = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    b = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, wgrad="bf16")
+    np.testing.assert_array_equal(q["dx"], b["dx"])          # the switch touches the weight gradients only
+    np.testing.assert_array_equal(q["dW_r"], b["dW_r"])
+    for key in ("dW1", "dW3", "dW2"):
+        num = sum(np.sum((q[key][e] - b[key][e]) ** 2) for e in b[key])
+        den = sum(np.sum(b[key][e] ** 2) for e in b[key])
+        assert 1e-3 < np.sqrt(num / den) < 0.1, key          # FP8 error: present, and of FP8 size
+
+
 def _train_case(seed, T=24, H=64, E=4, k=2, F=64):
     rng = np.random.default_rng(seed)
     x = rng.normal(0, 1, (T, H))
@@ -228,6 +267,27 @@ def _matmul_transposed_operand(A, B, quant=True):
     return A @ B[::-1].T if B.shape[0] > 1 else A @ B.T
 
 
+def _matmul_tn_wrong_axis(A, B, quant=True):
+    import oracle.mx_oracle as MX
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    if quant:
+        A, B = MX.mx_roundtrip(A, axis=1), MX.mx_roundtrip(B, axis=1)
+    return A.T @ B
+
+
+def _matmul_tn_pad_in_front(A, B, quant=True):
+    import oracle.mx_oracle as MX
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    if quant:
+        K = A.shape[0]
+        pad = (-K) % 32
+        A = MX.mx_roundtrip(np.concatenate([np.zeros((pad, A.shape[1])), A]), axis=0)[pad:]
+        B = MX.mx_roundtrip(np.concatenate([np.zeros((pad, B.shape[1])), B]), axis=0)[pad:]
+    return A.T @ B
+
+
 MX_MUTATIONS = [
     ("e4m3_round", _round_half_away, [test_e4m3_rounding_matches_torch]),
     ("e4m3_round", _no_saturation, [test_e4m3_saturation]),
@@ -235,11 +295,14 @@ MX_MUTATIONS = [
     ("mx_matmul_nt", _matmul_wrong_axis, [test_mx_matmul_nt_exact_along_the_contraction_axis]),
     ("mx_matmul_nt", _matmul_transposed_operand,
      [test_mx_matmul_nt_exact_along_the_contraction_axis, test_mx_layer_bwd_without_quantisation_is_the_bf16_backward]),
+    ("mx_matmul_tn", _matmul_tn_wrong_axis, [test_mx_matmul_tn_exact_along_tokens_with_a_ragged_last_block]),
+    ("mx_matmul_tn", _matmul_tn_pad_in_front, [test_mx_matmul_tn_exact_along_tokens_with_a_ragged_last_block]),
 ]
 
 
 @pytest.mark.parametrize("name,fn,pins", MX_MUTATIONS,
-                         ids=["half_away", "no_saturation", "scale_ceil", "matmul_wrong_axis", "matmul_row_order"])
+                         ids=["half_away", "no_saturation", "scale_ceil", "matmul_wrong_axis", "matmul_row_order",
+                              "matmul_tn_wrong_axis", "matmul_tn_pad_in_front"])
 def test_planted_mx_mistake_is_caught(monkeypatch, name, fn, pins):
     import oracle.mx_oracle as MX
     monkeypatch.setattr(MX, name, fn)
