@@ -501,17 +501,58 @@ def run_ours(args, ls, rank, world, local_rank):
                              ("wgrad_down", 2 * R * ls.F * ls.H, peaks["bf16_tflops_sustained"]),
                              ("wgrad_gate_up", 2 * R * ls.H * 2 * ls.F, peaks["bf16_tflops_sustained"])):
             if name in st_mx:
-                avg = sum(st_mx[name]) / len(st_mx[name])
+                # per step (the gate/up weight gradient is two launches: dW1, dW3)
+                avg = sum(st_mx[name]) / args.steps
                 ach = fl / (avg * 1e-3) / 1e12
                 tk[name] = {"ms": round(avg, 4), "bound": "tensor", "achieved_tflops": round(ach, 1),
                             "frac": round(ach / pk, 4)}
         for name in ("router", "permute", "combine", "combine_bwd", "router_bwd_elem", "permute_bwd"):
             if name in st_mx:
-                tk[name] = {"ms": round(sum(st_mx[name]) / len(st_mx[name]), 4)}
+                tk[name] = {"ms": round(sum(st_mx[name]) / args.steps, 4)}
+        # the same step with the weight gradients in MXFP8 too (operands
+        # quantised along each expert's tokens)
+        def step_mxw():
+            ops.layer_fwd_mxfp8_train(cfg, d["x"], d["router_w"], mxw, svm, d["expert_bias"], d["logit_bias"],
+                                      ws=wst, y=ym)
+            ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, svm, ws=wst, grads=grads, mx_wgrad=True)
+
+        for _ in range(max(3, args.warmup)):
+            step_mxw()
+        barrier()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ops.profile_start(cap_t)
+        w0.record()
+        for _ in range(args.steps):
+            step_mxw()
+        w1.record()
+        torch.cuda.synchronize()
+        ops.profile_stop()
+        assert ops.device_status(wst) == 0
+        ms_mxw = max_over_ranks(w0.elapsed_time(w1) / args.steps, world, dev)
+        st_w = {}
+        for name, t in ops.profile_read(cap_t):
+            st_w.setdefault(name, []).append(t)
+        wk = {}
+        for name, fl in (("wgrad_down", 2 * R * ls.F * ls.H), ("wgrad_gate_up", 2 * R * ls.H * 2 * ls.F)):
+            if name in st_w:
+                avg = sum(st_w[name]) / args.steps
+                ach = fl / (avg * 1e-3) / 1e12
+                wk[name] = {"ms": round(avg, 4), "bound": "tensor", "achieved_tflops": round(ach, 1),
+                            "frac": round(ach / peak8, 4)}
+        if "mx_quantize_tokens" in st_w:
+            # a, dy_perm, x_perm, dh1, dh3 read (bf16), their padded transposed codes written
+            avg = sum(st_w["mx_quantize_tokens"]) / args.steps
+            nbytes = 3 * R * (2 * ls.H + 3 * ls.F)
+            gbs = nbytes / (avg * 1e-3) / 1e9
+            wk["mx_quantize_tokens"] = {"ms": round(avg, 4), "bound": "hbm", "achieved_gbs": round(gbs, 1),
+                                        "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        mxt_w = {"value": round(job_throughput(layer_flops(ls, True), ms_mxw, world), 2), "unit": "TFLOPS",
+                 "ms_per_step": round(ms_mxw, 4), "vs_bf16_step": round(ms / ms_mxw, 3), "kernels": wk}
         mxt = {"value": round(job_throughput(layer_flops(ls, True), ms_mxt, world), 2), "unit": "TFLOPS",
                "ms_per_step": round(ms_mxt, 4),
                "dtype": "mxfp8 forward and data-gradient GEMMs, bf16 weight gradients (fp32 out)",
-               "vs_bf16_step": round(ms / ms_mxt, 3), "kernels": tk, "peak_fp8_tflops": round(peak8, 1)}
+               "vs_bf16_step": round(ms / ms_mxt, 3), "kernels": tk, "peak_fp8_tflops": round(peak8, 1),
+               "mxfp8_weight_gradients": mxt_w}
         del mxw, mxbw, wst, svm, ym
 
     # ---------------- the NVFP4 grouped expert GEMM on the down projection's

@@ -285,11 +285,14 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
  *   da      = Q(dy_perm) Q(W2_e)^T                  (blocks along H; fp32, not stored)
  *   dh1     = da h3 SiLU'(h1), dh3 = da SiLU(h1)    (saved bf16 h13; bf16)
  *   dx_perm = bf16(Q([dh1 | dh3]) Q([W1_e | W3_e])^T)  (blocks along 2F)
- * with the weight gradients in bf16 on the tensor cores (fp32 out):
- * dW2_e = a_e^T dy_perm_e with a = bf16(SiLU(h1) h3) recomputed from the
- * saved h13, dW1_e | dW3_e = x_perm_e^T [dh1 | dh3]. Routing, combine, their
- * backward and the router backward are those of the bf16 layer. Requires H
- * and F multiples of 128 and F_shared == 0.
+ * and the weight gradients (fp32 out) dW2_e = a_e^T dy_perm_e, with
+ * a = bf16(SiLU(h1) h3) recomputed from the saved h13, and
+ * dW1_e | dW3_e = x_perm_e^T [dh1 | dh3]: in bf16 on the tensor cores, or with
+ * mx_wgrad set as MXFP8 GEMMs whose operands are quantised along each
+ * expert's tokens (blocks of 32 from the expert's first row, a last partial
+ * block zero-padded). Routing, combine, their backward and the router
+ * backward are those of the bf16 layer. Requires H and F multiples of 128
+ * and F_shared == 0.
  * ------------------------------------------------------------------------- */
 
 /* The weights of the two data-gradient GEMMs, device buffers owned by the
@@ -333,12 +336,13 @@ int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const mo
 
 /* Backward of the MXFP8 training step for the loss <dO, y> + L_aux, given the
  * forward's saved tensors (the workspace need not hold the forward's): outputs as moe_layer_bwd
- * (dx, dW_router, dW1, dW3, dW2 fp32, aux_loss_out). */
+ * (dx, dW_router, dW1, dW3, dW2 fp32, aux_loss_out). mx_wgrad != 0: MXFP8
+ * weight gradients (see above), else bf16. */
 int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x,
                         const moe_bf16* router_w, const moe_mx_bwd_weights* w,
                         const moe_fwd_saved* saved, void* dx, float* dW_router, float* dW1,
-                        float* dW3, float* dW2, float* aux_loss_out, void* ws, size_t ws_bytes,
-                        void* stream);
+                        float* dW3, float* dW2, float* aux_loss_out, int mx_wgrad, void* ws,
+                        size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * NVFP4 grouped expert GEMM. The report lists NVFP4 among its precisions

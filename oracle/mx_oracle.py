@@ -194,15 +194,15 @@ def mx_matmul_tn(A, B, quant=True):
 
 def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
                  topk_groups=1, gate_scale=1.0, aux_coeff=0.0, prec=CONTRACT, experts=None, tokens=None,
-                 force_balanced=False, quant=True, wgrad="mxfp8"):
+                 force_balanced=False, quant=True, wgrad="bf16"):
     """Forward and backward of the layer with MXFP8 expert GEMMs, for the
     loss <dO, y> + L_aux.
 
     The report trains its Blackwell runs in MXFP8 without spelling out the
-    recipe; the reading here quantises both operands of every expert GEMM
+    recipe; the reading here quantises both operands of each MXFP8 GEMM
     along that GEMM's own contraction axis, as the forward does: along H or
     F for the data gradients, along the expert's tokens for the weight
-    gradients (``wgrad="bf16"`` keeps those in bf16):
+    gradients, which are bf16 unless ``wgrad="mxfp8"``:
 
     forward, per expert e on its rows (as ``mx_layer_fwd``):
       h1 = Q(x) Q(W1_e), h3 = Q(x) Q(W3_e)       (Q along H)
@@ -214,15 +214,15 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
                                                   stored, so not rounded, as in the bf16 layer)
       dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)   (saved h13; stored per prec.dh13)
       a'  = SiLU(h1) h3 from the saved h13       (stored per prec.a)
-      dW2_e = Q(a')^T Q(dy_perm)                 (Q along the expert's tokens)
+      dW2_e = Q(a')^T Q(dy_perm)                 (Q along the expert's tokens; wgrad="mxfp8")
       dx_perm = Q([dh1 | dh3]) Q([W1_e | W3_e])^T  (Q along 2F; per prec.dx_perm)
-      dW1_e = Q(x)^T Q(dh1), dW3_e = Q(x)^T Q(dh3)  (Q along the expert's tokens;
-                                                 x = the bf16 rows of x_perm)
+      dW1_e = Q(x)^T Q(dh1), dW3_e = Q(x)^T Q(dh3)  (Q along the expert's tokens, wgrad="mxfp8";
+                                                 x = the bf16 rows of x_perm; Q = identity for "bf16")
       router backward, aux loss and dx = sum of dx_perm rows + dL W_r as in
       the bf16 layer.
     No shared expert. ``quant=False`` replaces every MXFP8 round trip by the
     identity, which is the bf16 layer's backward on the same stored tensors. Returns the same keys as the bf16 oracle's
-    ``layer_bwd`` (plus ``y``)."""
+    ``layer_bwd`` (plus ``y``, and ``wg_amax``: per expert the largest magnitude of each weight-gradient operand)."""
     x = np.asarray(x, np.float64)
     dO = np.asarray(dO, np.float64)
     T, H = x.shape
@@ -245,6 +245,7 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
     dW1 = {e: np.zeros((H, F)) for e in exp_set}
     dW3 = {e: np.zeros((H, F)) for e in exp_set}
     dW2 = {e: np.zeros((F, H)) for e in exp_set}
+    wg_amax = {}  # per expert: the largest magnitude of each weight-gradient operand
     for e in range(E):
         tt, ii = np.nonzero(idx == e)                 # rows of expert e, ascending t
         if len(tt) == 0:
@@ -276,8 +277,10 @@ def mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
             dW1[e] += mx_matmul_tn(xr, dh1, wq)
             dW3[e] += mx_matmul_tn(xr, dh3, wq)
             dW2[e] += mx_matmul_tn(a_w, dyr, wq)
+            wg_amax[e] = {n: float(np.abs(v).max()) for n, v in (("x", xr), ("dh1", dh1), ("dh3", dh3), ("a", a_w),
+                                                                    ("dy", dyr))}
     res = {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": y,
-           "dgate": dgate, "dW1": dW1, "dW3": dW3, "dW2": dW2}
+           "dgate": dgate, "dW1": dW1, "dW3": dW3, "dW2": dW2, "wg_amax": wg_amax}
     lg = rt["logits"][need_tok]
     aux = aux_coeff if score == "softmax" else 0.0
     dL = router_backward(lg, idx[need_tok], gate[need_tok], dgate[need_tok], score, gate_scale, counts, k, aux,

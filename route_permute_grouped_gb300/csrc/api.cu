@@ -43,7 +43,7 @@ enum StageTag : int {
   STAGE_COMBINE_BWD = 10, STAGE_ROUTER_BWD = 11, STAGE_DGRAD2 = 12, STAGE_WGRAD2 = 13, STAGE_DGRAD1 = 14,
   STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
   STAGE_NV_QUANT = 20, STAGE_NV_GEMM = 21,
-  STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
+  STAGE_MX_QUANT_TOK = 22, STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
 };
 // MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
 // report the first stage whose kernels failed (debugging aid, off by default).
@@ -173,8 +173,10 @@ struct WsLayout {
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
-  // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales
-  size_t dy_q, sfa_dy, dh_q, sfa_dh;
+  // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales; the
+  // transposed token-axis operands of the weight gradients (A, B) with their
+  // scales and the padded token offsets
+  size_t dy_q, sfa_dy, dh_q, sfa_dh, tok_a, sf_a, tok_b, sf_b, pad_off;
   // NVFP4 forward: codes and scales of the current GEMM's activations
   // (x_perm, then a), their two tensor scales
   size_t nv_q, nv_sf, nv_g;
@@ -218,6 +220,15 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
       L.sfa_dy = take(mx_sfa_bytes(c.T * c.k, c.E, c.H));
       L.dh_q = take(2 * R * F);
       L.sfa_dh = take(mx_sfa_bytes(c.T * c.k, c.E, 2 * c.F));
+      const int kbt = mx_wg_kbt(static_cast<long long>(R), c.E);
+      const size_t ldk = static_cast<size_t>(kbt) * kMxKB;
+      const int CA = c.H > c.F ? c.H : c.F;  // A: a (F rows) or x_perm (H rows)
+      const int CB = c.H > c.F ? c.H : c.F;  // B: dy_perm (H rows), dh1 or dh3 (F rows)
+      L.tok_a = take(static_cast<size_t>(CA) * ldk);
+      L.sf_a = take(mx_tok_sf_bytes(CA, 128, kbt));
+      L.tok_b = take(static_cast<size_t>(CB) * ldk);
+      L.sf_b = take(mx_tok_sf_bytes(CB, kMxBN, kbt));
+      L.pad_off = take(sizeof(int32_t) * (E + 1));
     }
   } else {
     if (!nv) L.x_perm = take(2 * R * H);  // the NVFP4 permute writes codes only
@@ -483,6 +494,44 @@ static int run_dgrad2_mx(const moe_config& c, const int32_t* offsets, int R, con
   return cuda_status(launch_gemm(KIND_DGRAD2_MX, q, ma, mb, msa, num_sms(), s, nullptr, &msb));
 }
 
+// MXFP8 weight gradient out [E][M][N] fp32 = Q(A_e)^T Q(B_e) over each expert's
+// tokens: X_A [R, M] (row stride lda) and X_B [R, N] (row stride ldb), bf16
+// rows grouped by expert, are quantised along the tokens into the transposed
+// operands (A: 128-row scale tiles, B: 192-row tiles; the padded token offsets
+// become the GEMM's group offsets), then one ragged-K block-scaled GEMM
+static int run_wgrad_mx(const moe_config& c, const int32_t* offsets, int R, const __nv_bfloat16* XA, int M, int lda,
+                        const __nv_bfloat16* XB, int N, int ldb, float* out, void* ws, const WsLayout& L,
+                        DevStatus* st, cudaStream_t s, bool quantise_a = true) {
+  const int kbt = mx_wg_kbt(static_cast<long long>(R), c.E);
+  const uint64_t ldk = static_cast<uint64_t>(kbt) * kMxKB;
+  uint8_t* ta = at<uint8_t>(ws, L.tok_a);
+  uint8_t* sa = at<uint8_t>(ws, L.sf_a);
+  uint8_t* tb = at<uint8_t>(ws, L.tok_b);
+  uint8_t* sb = at<uint8_t>(ws, L.sf_b);
+  int32_t* pad = at<int32_t>(ws, L.pad_off);
+  if (quantise_a) MOE_CUDA(launch_mx_quantize_tokens(XA, R, M, lda, c.E, offsets, ta, sa, 128, pad, s));
+  MOE_CUDA(launch_mx_quantize_tokens(XB, R, N, ldb, c.E, offsets, tb, sb, kMxBN, pad, s));
+  stage_done(s, STAGE_MX_QUANT_TOK, quantise_a ? 2 : 1);
+  GemmParams p = base_params(c, st);
+  p.ngroups = c.E;
+  p.offsets = pad;
+  p.wg_M = M; p.wg_N = N; p.wg_mode = 0;
+  p.m_tiles_fixed = (M + 255) / 256;
+  p.n_tiles = (N + kMxBN - 1) / kMxBN;
+  p.bn = kMxBN;
+  p.kb_total = kbt;
+  p.out0 = out;
+  CUtensorMap ma, mb, msa, msb, mo;
+  if (!make_map_u8(&ma, ta, ldk, static_cast<uint64_t>(M), kMxKB, kBM)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&mb, tb, ldk, static_cast<uint64_t>(N), kMxKB, kMxBN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msa, sa, 256, mx_tok_sf_bytes(M, 128, kbt) / 256, 256, 2, false)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&msb, sb, 256, mx_tok_sf_bytes(N, kMxBN, kbt) / 256, 256, 4, false)) return MOE_ERR_CUDA;
+  if (!make_map_f32_3d(&mo, out, N, M, c.E)) return MOE_ERR_CUDA;
+  const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
+  return cuda_status(launch_gemm(KIND_WGRAD_MX, p, ma, mb, msa,
+                                 static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s, &mo, &msb));
+}
+
 // NVFP4 grouped GEMM on quantised activations: y [R, N] bf16 = g_x g_e (Q(x) Q(W_e))
 static int run_gemm_nv(int E, long long R, int K, int N, const int32_t* offsets, const uint8_t* xq,
                        const uint8_t* sfx, const float* gx, const uint8_t* wq, const uint8_t* sf, const float* g,
@@ -707,11 +756,13 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
 
 // The layer backward after the checks. mx != nullptr: the backward of the
 // MXFP8 training step (the data-gradient GEMMs on MXFP8 operands with the
-// weights in mx; W1, W3, W2 unused; the SwiGLU backward in its own kernel).
+// weights in mx; W1, W3, W2 unused); with mx_wgrad the weight gradients too
+// (operands quantised along each expert's tokens).
 static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
                           const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved,
                           void* dx, float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out,
-                          void* ws, const WsLayout& L, const moe_mx_bwd_weights* mx, cudaStream_t s) {
+                          void* ws, const WsLayout& L, const moe_mx_bwd_weights* mx, cudaStream_t s,
+                          bool mx_wgrad = false) {
   // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
   const bool recompute = mx == nullptr && saved->a == nullptr;
   DevStatus* st = at<DevStatus>(ws, 0);
@@ -779,7 +830,11 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     stage_done(s, STAGE_DGRAD2, 1);
   }
   // 4. dW2_e = a_e^T dy_perm_e
-  {
+  if (mx != nullptr && mx_wgrad) {
+    // MXFP8: both operands quantised along the expert's tokens
+    MOE_TRY(run_wgrad_mx(c, saved->offsets, R, a_used, c.F, c.F, dy_perm, c.H, c.H, dW2, ws, L, st, s));
+    stage_done(s, STAGE_WGRAD2, 1);
+  } else {
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets;
     p.wg_M = c.F; p.wg_N = c.H; p.wg_mode = 0;
@@ -815,7 +870,15 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     stage_done(s, STAGE_DGRAD1, 1);
   }
   // 6. dW1_e | dW3_e = x_perm_e^T dh13_e
-  {
+  if (mx != nullptr && mx_wgrad) {
+    // MXFP8: dW1 from dh1 (columns [0, F) of dh13), then dW3 from dh3 with
+    // the quantised x_perm kept
+    const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(saved->x_perm);
+    MOE_TRY(run_wgrad_mx(c, saved->offsets, R, xp, c.H, c.H, dh13, c.F, 2 * c.F, dW1, ws, L, st, s));
+    stage_done(s, STAGE_WGRAD13, 1);
+    MOE_TRY(run_wgrad_mx(c, saved->offsets, R, xp, c.H, c.H, dh13 + c.F, c.F, 2 * c.F, dW3, ws, L, st, s, false));
+    stage_done(s, STAGE_WGRAD13, 1);
+  } else {
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets;
     p.wg_M = c.H; p.wg_N = 2 * c.F; p.wg_mode = 1;
@@ -1064,8 +1127,8 @@ int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const mo
 
 int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
                         const moe_mx_bwd_weights* w, const moe_fwd_saved* saved, void* dx, float* dW_router,
-                        float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws, size_t ws_bytes,
-                        void* stream) {
+                        float* dW1, float* dW3, float* dW2, float* aux_loss_out, int mx_wgrad, void* ws,
+                        size_t ws_bytes, void* stream) {
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(check_mx_shape(c));
@@ -1077,7 +1140,7 @@ int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf1
   const WsLayout L = ws_layout(c, true, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return layer_bwd_core(c, dO, x, router_w, nullptr, nullptr, nullptr, saved, dx, dW_router, dW1, dW3, dW2,
-                        aux_loss_out, ws, L, w, static_cast<cudaStream_t>(stream));
+                        aux_loss_out, ws, L, w, static_cast<cudaStream_t>(stream), mx_wgrad != 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -184,14 +184,15 @@ __device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc,
   }
 }
 
-// Weight gradient: 32 fp32 columns per box, into dW1 (n < F) or dW3 (n >= F)
-// in mode 1, into dW2 in mode 0; 3-D maps {N, M, experts}.
+// Weight gradient: 32 fp32 columns per box (boxes c_begin .. c_end - 1 of the
+// tile), into dW1 (n < F) or dW3 (n >= F) in mode 1, into dW2 in mode 0; 3-D
+// maps {N, M, experts}.
 __device__ __forceinline__ void epi_wgrad_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
                                               int row0, Stager& st, const CUtensorMap* mo0,
-                                              const CUtensorMap* mo1) {
+                                              const CUtensorMap* mo1, int c_begin = 0, int c_end = 8) {
   const bool zero = ti.nkb == 0;
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     const int n = ti.n0 + c * 32;
     if (n >= p.wg_N) break;
     float f[32];

@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         s_off[g] = o;
       }
       if (g < ng) {
-        if constexpr (KIND == KIND_WGRAD || KIND == KIND_ROUTER_DW) {
+        if constexpr (KIND == KIND_WGRAD || KIND == KIND_WGRAD_MX || KIND == KIND_ROUTER_DW) {
           c = p.m_tiles_fixed * p.n_tiles;
         } else {
           int lo, hi;
@@ -784,6 +784,9 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         } else if (any_rows) {
           epi_store(ti, tacc, r, kMxBN / 32, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
         }
+      } else if constexpr (KIND == KIND_WGRAD_MX) {
+        // 3-D output maps clip rows past M per expert; six 32-column boxes
+        epi_wgrad_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1, 0, kMxBN / 32);
       } else if constexpr (KIND == KIND_DGRAD2_MX) {
         epi_dgrad2_mx(p, ti, tacc, r, rank, part);
       } else if constexpr (KIND == KIND_FFN1_NV) {
@@ -909,6 +912,7 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
     case KIND_FFN1_MX: return launch_kind<KIND_FFN1_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN2_MX: return launch_kind<KIND_FFN2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_DGRAD2_MX: return launch_kind<KIND_DGRAD2_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
+    case KIND_WGRAD_MX: return launch_kind<KIND_WGRAD_MX>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_GEMM_NV: return launch_kind<KIND_GEMM_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     case KIND_FFN1_NV: return launch_kind<KIND_FFN1_NV>(p, ma, mb0, mb1, mo0, mo1, grid, st);
     default: return cudaErrorInvalidValue;

@@ -57,6 +57,9 @@ enum GemmKind : int {
   KIND_DGRAD2_MX = 13, // MXFP8 down-projection data gradient: da = Q(dy_perm) Q(W2_e)^T -> SwiGLU backward ->
                        // dh13 and a (bf16) and dh13 as MXFP8 (codes + the gate/up data gradient's scales);
                        // 256 x 192 pair tiles
+  KIND_WGRAD_MX = 14,  // MXFP8 weight gradient dW_e = Q(X_e)^T Q(Y_e) over the expert's tokens (K-major
+                       // transposed operands, k blocks of 128 padded tokens per expert), fp32 out;
+                       // 256 x 192 pair tiles
 };
 
 constexpr int kBM = 128;
@@ -99,7 +102,8 @@ struct KindTraits {
   // MXFP8 kinds: CTA pairs on 256 x 192 tiles; a CTA's stage holds 128 k
   // elements (one byte each) of its 128 A rows (16 KB) and 96 B rows (12 KB),
   // its A scale block (0.5 KB) and the tile's B scale blocks (1 KB)
-  static constexpr bool kMx = (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX || KIND == KIND_DGRAD2_MX);
+  static constexpr bool kMx =
+      (KIND == KIND_FFN1_MX || KIND == KIND_FFN2_MX || KIND == KIND_DGRAD2_MX || KIND == KIND_WGRAD_MX);
   // NVFP4: like MXFP8 with 256-element k blocks (128 bytes of codes per row)
   // and four scale blocks per operand block (2 KB of A, 4 KB of B scales)
   static constexpr bool kNv = (KIND == KIND_GEMM_NV || KIND == KIND_FFN1_NV);
@@ -131,7 +135,7 @@ struct KindTraits {
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R || kMx || kNv);
+                                        KIND == KIND_DGRAD1 || KIND == KIND_DGRAD2R || (kMx && KIND != KIND_WGRAD_MX) || kNv);
 };
 
 struct GemmParams {
@@ -213,6 +217,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     ti.krow_end = s_off[lo + 1];
     ti.kb0 = 0;
     ti.nkb = (ti.krow_end - ti.krow0 + kBK - 1) / kBK;
+  } else if constexpr (KIND == KIND_WGRAD_MX) {
+    // fixed M per expert; K = the expert's padded tokens (group offsets are
+    // padded token offsets, multiples of 128), whole k blocks from kb0
+    ti.mt = mb;
+    ti.m0 = mb * KindTraits<KIND>::kTileM + rank * kBM;
+    ti.m_end = p.wg_M;
+    ti.kb0 = s_off[lo] / kMxKB;
+    ti.nkb = (s_off[lo + 1] - s_off[lo]) / kMxKB;
+    ti.krow0 = 0;
+    ti.krow_end = 0;
   } else {  // ROUTER_DW: group = split
     ti.m0 = mb * kBM;
     ti.m_end = p.E;
@@ -267,19 +281,25 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
     // 128 k elements (bytes) of this CTA's 128 A rows and its 96 B rows, its A
     // scale block (block 2 * pair tile + rank of the activations' scales: map
     // mb1, 256-byte rows) and the tile's two B scale blocks (map msfb)
-    const int kc = kb * kMxKB;
+    // WGRAD_MX: k block kb0 + kb of the padded token axis shared by all
+    // experts (its operands and scales carry no expert index)
+    const int kbg = (KIND == KIND_WGRAD_MX) ? ti.kb0 + kb : kb;
+    const int kc = kbg * kMxKB;
     tma_load_2d_pair(sA, ma, bar_cluster, kc, ti.m0);
     if constexpr (KIND == KIND_FFN1_MX) {
       // W1 rows n0.. (even CTA) or W3 rows n0.. (odd CTA) of expert g
       tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * 2 * p.F + rank * p.F + ti.n0);
+    } else if constexpr (KIND == KIND_WGRAD_MX) {
+      // rows n0 + 96 rank .. of the transposed B operand
+      tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.n0 + rank * (kMxBN / 2));
     } else {
       // W2 rows (H index) n0 + 96 rank .. of expert g
       tma_load_2d_pair(sB, mb0, bar_cluster, kc, ti.g * p.H + ti.n0 + rank * (kMxBN / 2));
     }
     uint8_t* sSF = sA + kMxSfOff;
-    const int ablk = (2 * ti.mt + rank) * p.kb_total + kb;
+    const int ablk = (2 * ti.mt + rank) * p.kb_total + kbg;
     tma_load_2d_pair(sSF, mb1, bar_cluster, 0, 2 * ablk);
-    const int bblk = (ti.g * p.nt_w + ti.nb) * p.kb_total + kb;
+    const int bblk = ((KIND == KIND_WGRAD_MX) ? ti.nb : ti.g * p.nt_w + ti.nb) * p.kb_total + kbg;
     tma_load_2d_pair(sSF + kMxSfBytes, msfb, bar_cluster, 0, 4 * bblk);
     return;
   }

@@ -91,6 +91,14 @@ inline size_t mx_sf2h_bytes(const moe_config& c) {
 inline size_t mx_sf13f_bytes(const moe_config& c) {
   return static_cast<size_t>(c.E) * mx_ntiles2(c) * (2 * c.F / kMxKB) * 2 * kMxSfBytes;
 }
+// operands of the MXFP8 weight gradients: the tokens of each expert padded to
+// whole k blocks of 128, kbt = k blocks of the padded axis (at most
+// ceil((R + 127 E) / 128)); scale bytes of a transposed operand of C rows in
+// tiles of tile_rows
+inline int mx_wg_kbt(long long R, int E) { return static_cast<int>((R + 127ll * E + kMxKB - 1) / kMxKB); }
+inline size_t mx_tok_sf_bytes(int C, int tile_rows, int kbt) {
+  return static_cast<size_t>((C + tile_rows - 1) / tile_rows) * kbt * ((tile_rows + 127) / 128) * kMxSfBytes;
+}
 // nv.cu: NVFP4 quantisers and the sizes of the tile-ready scale buffers
 inline size_t nv_weight_sf_bytes(int E, int K, int N) {
   return static_cast<size_t>(E) * ((N + kNvTileN - 1) / kNvTileN) * (K / kNvKB) * 2 * kNvSfBytes;
@@ -120,6 +128,8 @@ cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, 
 cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
                                        const __nv_bfloat16* W2, uint8_t* w13q, uint8_t* sf13, uint8_t* w2q,
                                        uint8_t* sf2, cudaStream_t st);
+cudaError_t launch_mx_quantize_tokens(const __nv_bfloat16* X, int R, int C, int ldx, int E, const int32_t* offsets,
+                                      uint8_t* XT, uint8_t* sf, int tile_rows, int32_t* pad_off, cudaStream_t st);
 cudaError_t launch_mx_quantize_bwd_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
                                            const __nv_bfloat16* W2, uint8_t* w2h, uint8_t* sf2h, uint8_t* w13f,
                                            uint8_t* sf13f, cudaStream_t st);

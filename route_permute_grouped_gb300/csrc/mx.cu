@@ -155,6 +155,78 @@ __global__ void __launch_bounds__(256) mx_quantize_weight_rows_kernel(
       static_cast<uint8_t>(sb);
 }
 
+// The transposed MXFP8 operand of a weight-gradient GEMM, whose K runs over
+// each expert's tokens: rows of X [R, C] bf16 (row stride ldx) grouped by
+// expert (offsets[0..E]) -> XT [C][ldk] E4M3 codes, column p of XT = padded token position p (expert
+// e's rows at P_e .. P_e + count_e - 1, zeros up to P_{e+1}; P_e = 128 * sum
+// over e' < e of ceil(count_e' / 128), so every 128-position k block lies in
+// one expert), blocks of 32 positions along a row of XT sharing one E8M0
+// scale. Scales in the tile-ready layout of an MXFP8 operand with tile_rows
+// rows per tile (128: an A operand, 192: a B operand): the scale of (row c,
+// block g) at byte ((c / tile_rows * kbt + g / 4) * nblk + (c % tile_rows) /
+// 128) * 512 + pos((c % tile_rows) % 128, g % 4), nblk = ceil(tile_rows / 128),
+// kbt = k blocks of the padded axis. Block (x, y) = positions 32 x .. 32 x + 31
+// and columns 256 y ..: the 32 x 256 bf16 tile is staged in shared memory with
+// 16-byte loads (one 512-byte row per warp load), then thread t quantises
+// column t from it (one 32-byte store). Block (0, 0) also writes P[0..E].
+__global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __nv_bfloat16* __restrict__ X, int C, int ldx,
+                                                                 int E, const int32_t* __restrict__ offsets,
+                                                                 uint8_t* __restrict__ XT, size_t ldk,
+                                                                 uint8_t* __restrict__ sf, int tile_rows, int kbt,
+                                                                 int32_t* __restrict__ pad_off) {
+  __shared__ int s_off[kMaxGroups + 1];
+  __shared__ int s_kb[kMaxGroups + 1];  // 128-position k blocks before each expert
+  __shared__ __align__(16) __nv_bfloat16 s_x[32][256];
+  const int tid = threadIdx.x;
+  for (int i = tid; i <= E; i += blockDim.x) s_off[i] = offsets[i];
+  __syncthreads();
+  if (tid < 32) tile_prefix_warp(s_off, s_kb, E, tid, kMxKB);
+  __syncthreads();
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = tid; i <= E; i += blockDim.x) pad_off[i] = kMxKB * s_kb[i];
+  const int g = blockIdx.x;  // 32-position block
+  const int pos = kMxBlock * g;
+  if (pos >= kMxKB * s_kb[E]) return;  // uniform over the block
+  const int e = expert_of_row(s_kb, E, pos / kMxKB);
+  const int j0 = pos - kMxKB * s_kb[e];
+  const int cnt = s_off[e + 1] - s_off[e];
+  const int c0 = 256 * blockIdx.y;
+  // stage: warp w loads rows w, w + 8, w + 16, w + 24; lane l columns 8 l ..
+  const int w = tid >> 5, l = tid & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = w + 8 * i;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j0 + r < cnt && c0 + 8 * l < C)
+      v = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(s_off[e] + j0 + r) * ldx + c0 + 8 * l));
+    *reinterpret_cast<uint4*>(&s_x[r][8 * l]) = v;
+  }
+  __syncthreads();
+  const int c = c0 + tid;
+  if (c >= C) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(s_x[i][tid]);
+  uint32_t q[8];
+  const uint32_t sb = mx_quant32(v, q);
+  st_codes32(XT + static_cast<size_t>(c) * ldk + pos, q);
+  const int b = c % tile_rows;
+  const int nblk = (tile_rows + 127) / 128;
+  sf[((static_cast<size_t>(c / tile_rows) * kbt + g / 4) * nblk + (b >> 7)) * kMxSfBytes + mx_sf_pos(b & 127, g & 3)] =
+      static_cast<uint8_t>(sb);
+}
+
+cudaError_t launch_mx_quantize_tokens(const __nv_bfloat16* X, int R, int C, int ldx, int E, const int32_t* offsets,
+                                      uint8_t* XT, uint8_t* sf, int tile_rows, int32_t* pad_off, cudaStream_t st) {
+  const int kbt = mx_wg_kbt(R, E);
+  cudaError_t err = cudaMemsetAsync(sf, 0, mx_tok_sf_bytes(C, tile_rows, kbt), st);
+  if (err != cudaSuccess) return err;
+  const dim3 grid(static_cast<unsigned>(kbt * (kMxKB / kMxBlock)), static_cast<unsigned>((C + 255) / 256));
+  mx_quantize_tokens_kernel<<<grid, 256, 0, st>>>(X, C, ldx, E, offsets, XT, static_cast<size_t>(kbt) * kMxKB, sf,
+                                                   tile_rows, kbt, pad_off);
+  return cudaGetLastError();
+}
+
 // Weights of the two data-gradient GEMMs: W2 [E, F, H] quantised along H
 // (B rows = F, tiles of 192) -> w2h [E][F][H], sf2h; W1 | W3 [E, H, F]
 // quantised along F into one K = 2F operand (B rows = H, tiles of 192; W1 in

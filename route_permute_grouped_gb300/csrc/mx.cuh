@@ -82,16 +82,16 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&
   return sb;
 }
 
-// First 256-row CTA-pair tile of each expert in the grouped GEMMs' schedule:
-// s_pt[e] = sum over e' < e of ceil(rows_e' / 256), from the row offsets
-// s_off[0..E] (E <= 256). Run by one whole warp: lane l sums experts
-// 8 l .. 8 l + 7, then a warp scan; s_pt[E] is the total.
-__device__ __forceinline__ void pair_tile_prefix_warp(const int* s_off, int* s_pt, int E, int lane) {
+// Tiles of `rows` rows before each expert: s_pt[e] = sum over e' < e of
+// ceil(count_e' / rows), from the row offsets s_off[0..E] (E <= 256). Run by
+// one whole warp: lane l sums experts 8 l .. 8 l + 7, then a warp scan;
+// s_pt[E] is the total.
+__device__ __forceinline__ void tile_prefix_warp(const int* s_off, int* s_pt, int E, int lane, int rows) {
   int t[8], sum = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int e = 8 * lane + j;
-    t[j] = e < E ? (s_off[e + 1] - s_off[e] + 255) / 256 : 0;
+    t[j] = e < E ? (s_off[e + 1] - s_off[e] + rows - 1) / rows : 0;
     sum += t[j];
   }
   int incl = sum;
@@ -107,6 +107,11 @@ __device__ __forceinline__ void pair_tile_prefix_warp(const int* s_off, int* s_p
     if (e <= E) s_pt[e] = run;
     run += t[j];
   }
+}
+
+// First 256-row CTA-pair tile of each expert in the grouped GEMMs' schedule
+__device__ __forceinline__ void pair_tile_prefix_warp(const int* s_off, int* s_pt, int E, int lane) {
+  tile_prefix_warp(s_off, s_pt, E, lane, 256);
 }
 
 // expert e with s_off[e] <= row < s_off[e + 1] (binary search over E experts)

@@ -107,7 +107,7 @@ def lib():
         L.moe_layer_fwd_mxfp8_train.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, POINTER(MoeMxWeights), vp,
                                                 POINTER(MoeFwdSaved), vp, c_size_t, vp]
         L.moe_layer_bwd_mxfp8.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeMxBwdWeights),
-                                          POINTER(MoeFwdSaved), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+                                          POINTER(MoeFwdSaved), vp, vp, vp, vp, vp, vp, c_int, vp, c_size_t, vp]
         for n in ("moe_mx_quantize_bwd_weights", "moe_layer_fwd_mxfp8_train", "moe_layer_bwd_mxfp8"):
             getattr(L, n).restype = c_int
         L.moe_nv_weight_bytes.restype = c_size_t
@@ -132,7 +132,7 @@ def lib():
     return _lib
 
 
-STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 24: "mx_dgrad_down_swiglu",
+STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 22: "mx_quantize_tokens", 24: "mx_dgrad_down_swiglu",
                25: "mx_dgrad_gate_up", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
@@ -468,16 +468,18 @@ def layer_fwd_mxfp8_train(cfg, x, router_w, mxw, saved, expert_bias=None, logit_
     return y
 
 
-def layer_bwd_mxfp8(cfg, dO, x, router_w, mxbw, saved, ws=None, grads=None):
+def layer_bwd_mxfp8(cfg, dO, x, router_w, mxbw, saved, ws=None, grads=None, mx_wgrad=False):
     """Backward of the MXFP8 training step (``mxbw`` from
-    mx_quantize_bwd_weights); gradients as layer_bwd."""
+    mx_quantize_bwd_weights); gradients as layer_bwd. ``mx_wgrad``: the weight
+    gradients in MXFP8 too (operands quantised along each expert's tokens)."""
     dev = x.device
     g = alloc_grads(cfg, dev) if grads is None else grads
     ws = mx_train_workspace(cfg, dev) if ws is None else ws
     w = MoeMxBwdWeights(*[mxbw[n].data_ptr() for n in MX_BWD_WEIGHT_FIELDS])
     st = lib().moe_layer_bwd_mxfp8(ctypes.byref(cfg), _p(dO), _p(x), _p(router_w), ctypes.byref(w),
                                    ctypes.byref(_saved_struct(saved)), _p(g["dx"]), _p(g["dW_r"]), _p(g["dW1"]),
-                                   _p(g["dW3"]), _p(g["dW2"]), _p(g["aux_loss"]), _p(ws), ws.numel(), _stream())
+                                   _p(g["dW3"]), _p(g["dW2"]), _p(g["aux_loss"]), int(bool(mx_wgrad)), _p(ws),
+                                   ws.numel(), _stream())
     _check(st, "moe_layer_bwd_mxfp8")
     return g
 

@@ -29,6 +29,18 @@ def wgrad_atol(want):
     return max(MAX_ABS, 2.0 ** -7 * float(np.abs(np.asarray(want, np.float64)).max()))
 
 
+def mx_wgrad_atol(want, amax_a, amax_b):
+    """Max-abs bound of an MXFP8 weight gradient Q(A)^T Q(B) (both operands
+    quantised along the tokens). An operand's E4M3 code is decided from a bf16
+    value that fp32 and fp64 accumulation can put on either side of a rounding
+    boundary (see wgrad_atol); such a flip moves the code by one E4M3 step, at
+    most 2^-3 of the block's largest magnitude, and every entry of the
+    gradient's row or column through that element by at most the step times
+    the other operand's magnitude. The bound admits two flips on one entry:
+    2 * 2^-3 * max|A| * max|B|, and never less than the bf16 bound."""
+    return max(wgrad_atol(want), 2.0 ** -2 * float(amax_a) * float(amax_b))
+
+
 def rel_l2(got, ref):
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     den = np.linalg.norm(ref)

@@ -125,7 +125,7 @@ def test_low_precision_entry_points_check_on_the_host(lib):
     assert lib.moe_layer_fwd_mxfp8_train(ctypes.byref(shared), null, null, null, null, None, null, None, null, 0,
                                          null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
     assert lib.moe_layer_bwd_mxfp8(ctypes.byref(ok), null, null, null, None, None, null, null, null, null, null,
-                                   null, null, 0, null) == ops.MOE_ERR_INVALID_ARG
+                                   null, 1, null, 0, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_mx_quantize_bwd_weights(ctypes.byref(bad_h), null, null, null, None,
                                            null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
     assert lib.moe_mx_quantize(null, 10, 33, null, null, null) == ops.MOE_ERR_INVALID_ARG

@@ -4,15 +4,16 @@ computes one by one: the MXFP8 layer on the Qwen3 expert shape (H=4096,
 F=1536, top-8; 32 experts, T=4096) for 48 sampled tokens, and the NVFP4
 grouped GEMM on the down projection's full shape (131072 x 1536 x 4096, 128
 experts) for the rows of three experts, and the MXFP8 training step on the
-full Qwen3 training workload (T=16384, E=128) for one token's output and input
-gradient and one expert's weight gradients."""
+full Qwen3 training workload (T=16384, E=128), with bf16 and with MXFP8
+weight gradients, for one token's output and input gradient and one expert's
+weight gradients."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import TIE_MARGIN, assert_close, compare_topk, f64, wgrad_atol
+from tests._util import TIE_MARGIN, assert_close, compare_topk, f64, mx_wgrad_atol, wgrad_atol
 
 pytestmark = pytest.mark.gpu
 
@@ -71,7 +72,8 @@ class _PerExpert:
         return f64(self.t[e])
 
 
-def test_mxfp8_train_qwen3_full_sampled():
+@pytest.mark.parametrize("wgrad", ["bf16", "mxfp8"])
+def test_mxfp8_train_qwen3_full_sampled(wgrad):
     ls = synth.shape("qwen3_train")
     d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
     cfg = ops.config_from_shape(ls, out_fp32=True)
@@ -80,7 +82,7 @@ def test_mxfp8_train_qwen3_full_sampled():
     ws = ops.mx_train_workspace(cfg)
     saved = ops.alloc_saved_mxfp8(cfg)
     y = ops.layer_fwd_mxfp8_train(cfg, d["x"], d["router_w"], mxw, saved, ws=ws)
-    g = ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, saved, ws=ws)
+    g = ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, saved, ws=ws, mx_wgrad=wgrad == "mxfp8")
     torch.cuda.synchronize()
     assert ops.device_status(ws) == 0
     x, w_r, dO = f64(d["x"]), f64(d["router_w"]), f64(d["dO"])
@@ -101,10 +103,13 @@ def test_mxfp8_train_qwen3_full_sampled():
     e0 = int(cand[len(cand) // 2])
     t0 = int(np.random.default_rng(7).choice(np.nonzero(ok)[0]))
     ref = O.mx_layer_bwd(x, w_r, _PerExpert(d["W1"]), _PerExpert(d["W3"]), _PerExpert(d["W2"]), dO, k,
-                         aux_coeff=ls.aux_coeff, prec=O.Precision(y=False, dx=False), experts=[e0], tokens=[t0])
+                         aux_coeff=ls.aux_coeff, prec=O.Precision(y=False, dx=False), experts=[e0], tokens=[t0],
+                         wgrad=wgrad)
     assert_close("y (sampled token)", f64(y)[t0], ref["y"][t0])
     assert_close("dx (sampled token)", f64(g["dx"])[t0], ref["dx"][t0], atol=wgrad_atol(ref["dx"][t0]))
-    for key in ("dW1", "dW3", "dW2"):
+    am = ref["wg_amax"][e0]
+    for key, (oa, ob) in (("dW1", ("x", "dh1")), ("dW3", ("x", "dh3")), ("dW2", ("a", "dy"))):
         want = ref[key][e0]
-        assert_close(f"{key} (expert {e0}, {counts[e0]} rows)", f64(g[key][e0]), want, atol=wgrad_atol(want))
+        atol = mx_wgrad_atol(want, am[oa], am[ob]) if wgrad == "mxfp8" else wgrad_atol(want)
+        assert_close(f"{key} (expert {e0}, {counts[e0]} rows)", f64(g[key][e0]), want, atol=atol)
     assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))

@@ -1,16 +1,17 @@
 """MXFP8 training step (GPU) against the MXFP8 oracle: the weights of the two
 data-gradient GEMMs quantised bit for bit (codes and tile-ready scales), and
 the forward output and every gradient (dx, dW_router, dW1, dW3, dW2, aux
-loss) of the training step within the layer's tolerance, on shapes with
-several tiles, ragged N tiles of the data-gradient GEMMs and zero-token
-experts."""
+loss) of the training step within the layer's tolerance, with bf16 and with
+MXFP8 weight gradients, on shapes with several tiles, ragged N tiles of the
+data-gradient GEMMs, experts whose token count is not a multiple of 32 and
+zero-token experts."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import assert_close, f64, rel_l2, wgrad_atol
+from tests._util import assert_close, f64, mx_wgrad_atol, rel_l2, wgrad_atol
 from tests.test_mx_gpu import _decode_tile_scales
 
 pytestmark = pytest.mark.gpu
@@ -59,29 +60,30 @@ TRAIN_SHAPES = {
 }
 
 
-def _train(ls, d, cfg):
+def _train(ls, d, cfg, mx_wgrad=False):
     mxw = ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"])
     mxbw = ops.mx_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
     ws = ops.mx_train_workspace(cfg)
     saved = ops.alloc_saved_mxfp8(cfg)
     y = ops.layer_fwd_mxfp8_train(cfg, d["x"], d["router_w"], mxw, saved, d["expert_bias"], d["logit_bias"], ws=ws)
-    g = ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, saved, ws=ws)
+    g = ops.layer_bwd_mxfp8(cfg, d["dO"], d["x"], d["router_w"], mxbw, saved, ws=ws, mx_wgrad=mx_wgrad)
     torch.cuda.synchronize()
     assert ops.device_status(ws) == 0
     return y, g, saved
 
 
+@pytest.mark.parametrize("wgrad", ["bf16", "mxfp8"])
 @pytest.mark.parametrize("name", list(TRAIN_SHAPES))
-def test_layer_train_mxfp8(name):
+def test_layer_train_mxfp8(name, wgrad):
     ls = TRAIN_SHAPES[name]
     d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
     aux = 1e-2
     cfg = ops.config_from_shape(ls, aux_coeff=aux, out_fp32=True)
-    y, g, saved = _train(ls, d, cfg)
+    y, g, saved = _train(ls, d, cfg, mx_wgrad=wgrad == "mxfp8")
     n = {k_: (None if v is None else f64(v)) for k_, v in d.items()}
     ref = O.mx_layer_bwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], n["dO"], ls.k, ls.score,
                          n["expert_bias"], n["logit_bias"], ls.n_groups, ls.topk_groups, ls.gate_scale,
-                         aux_coeff=aux, prec=O.Precision(y=False, dx=False))
+                         aux_coeff=aux, prec=O.Precision(y=False, dx=False), wgrad=wgrad)
     assert np.array_equal(saved["topk_idx"].cpu().numpy(), ref["topk_idx"]), "routing differs (tie)"
     assert np.array_equal(saved["counts"].cpu().numpy(), ref["counts"])
     assert_close("y", f64(y), ref["y"])
@@ -90,10 +92,20 @@ def test_layer_train_mxfp8(name):
              "dW1": (f64(g["dW1"]), np.stack([ref["dW1"][e] for e in range(E)])),
              "dW3": (f64(g["dW3"]), np.stack([ref["dW3"][e] for e in range(E)])),
              "dW2": (f64(g["dW2"]), np.stack([ref["dW2"][e] for e in range(E)]))}
+    # MXFP8 weight gradients (operands quantised along the tokens): the bound
+    # of a flipped code, from the largest operand magnitudes over the experts
+    ops_of = {"dW1": ("x", "dh1"), "dW3": ("x", "dh3"), "dW2": ("a", "dy")}
     for key, (got, want) in pairs.items():
-        # bf16-stored activations (da, dh13, a, dy_perm) can round to the other
-        # neighbour where fp32 and fp64 accumulation straddle a boundary
-        assert_close(key, got, want, atol=wgrad_atol(want))
+        if key in ops_of and wgrad == "mxfp8":
+            am = ref["wg_amax"]
+            a_max = max(am[e][ops_of[key][0]] for e in am)
+            b_max = max(am[e][ops_of[key][1]] for e in am)
+            atol = mx_wgrad_atol(want, a_max, b_max)
+        else:
+            # bf16-stored activations (dh13, a, dy_perm) can round to the other
+            # neighbour where fp32 and fp64 accumulation straddle a boundary
+            atol = wgrad_atol(want)
+        assert_close(key, got, want, atol=atol)
     if ls.skew:
         empty = np.nonzero(ref["counts"] == 0)[0]
         assert len(empty) > 0

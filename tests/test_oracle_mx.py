@@ -170,7 +170,7 @@ def test_mx_matmul_tn_exact_along_tokens_with_a_ragged_last_block():
 
 def test_mx_weight_gradients_quantised_along_tokens():
     x, w_r, W1, W3, W2, dO, k = _train_case(6, T=64, H=128, E=4, F=96)
-    q = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    q = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, wgrad="mxfp8")
     b = O.mx_layer_bwd(x, w_r, W1, W3, W2, dO, k, wgrad="bf16")
     np.testing.assert_array_equal(q["dx"], b["dx"])          # the switch touches the weight gradients only
     np.testing.assert_array_equal(q["dW_r"], b["dW_r"])
