@@ -170,7 +170,7 @@ struct WsLayout {
   // forward intermediates (inference, or standalone grouped FFN without a_save)
   size_t logits_raw, topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
   // backward
-  size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part;
+  size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part, tmap_slots;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
   // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales; the
@@ -190,6 +190,11 @@ static int router_dw_splits(int T) {
   if (2 * kbh < s) s = 2 * kbh;
   return s < 1 ? 1 : s;
 }
+
+// the weight-gradient kernels' per-CTA tensor-map slots (two of 128 bytes),
+// for grids of up to kMaxGemmCtas CTAs
+constexpr size_t kTmapSlotBytes = 256;
+constexpr int kMaxGemmCtas = 1024;
 
 static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, bool nv = false) {
   WsLayout L{};
@@ -254,6 +259,7 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.dL_hl = take(2 * T * 2 * Ep);
     L.dx_r = take(4 * T * H);
     L.dwr_part = take(4 * static_cast<size_t>(router_dw_splits(c.T)) * E * H);
+    L.tmap_slots = take(kTmapSlotBytes * kMaxGemmCtas);  // weight gradients: per-CTA A-map slots
   }
   L.total = o;
   return L;
@@ -765,6 +771,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
                           bool mx_wgrad = false) {
   // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
   const bool recompute = mx == nullptr && saved->a == nullptr;
+  if (num_sms() > kMaxGemmCtas) return MOE_ERR_UNSUPPORTED_SHAPE;  // the tensor-map slots of the weight gradients
   DevStatus* st = at<DevStatus>(ws, 0);
   const int R = c.T * c.k;
   const int Ep = padded_experts(c.E);
@@ -838,6 +845,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets;
     p.wg_M = c.F; p.wg_N = c.H; p.wg_mode = 0;
+    p.tmap_slots = at<uint8_t>(ws, L.tmap_slots);
     p.m_tiles_fixed = (c.F + 255) / 256; p.n_tiles = (c.H + 255) / 256;  // CTA-pair tiles of 256 rows
     p.out0 = dW2;
     CUtensorMap ma, mb;
@@ -882,6 +890,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     GemmParams p = base_params(c, st);
     p.ngroups = c.E; p.offsets = saved->offsets;
     p.wg_M = c.H; p.wg_N = 2 * c.F; p.wg_mode = 1;
+    p.tmap_slots = at<uint8_t>(ws, L.tmap_slots);
     p.m_tiles_fixed = (c.H + 255) / 256; p.n_tiles = (2 * c.F + 255) / 256;  // CTA-pair tiles of 256 rows
     p.out0 = dW1; p.out1 = dW3;
     CUtensorMap ma, mb;

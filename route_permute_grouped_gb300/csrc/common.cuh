@@ -102,6 +102,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Copy a 2-D tensor map into `slot` (128 bytes of global memory, 128-byte
+// aligned) with its outer extent (dimension 1) set to `rows`, and make the copy
+// visible to the TMA unit: generic-proxy writes, then the tensormap-proxy
+// release and acquire fences. Loads through the copy read zeros at rows >= rows.
+__device__ __forceinline__ void tmap_set_rows(const CUtensorMap* src, uint8_t* slot, int rows) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* g = reinterpret_cast<uint4*>(slot);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = s[i];
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(slot), "r"(rows) : "memory");
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(slot) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"

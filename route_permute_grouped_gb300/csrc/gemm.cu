@@ -18,7 +18,7 @@ struct SmemLayout {
   static constexpr int kOutOff = KindTraits<KIND>::kStages * KindTraits<KIND>::kStageBytesK;
   static constexpr int kOutBytes = KindTraits<KIND>::kEpiWarps * KindTraits<KIND>::kOutWarpBytes;
   static constexpr int kBarOff = kOutOff + kOutBytes;
-  static constexpr int kNumBars = 3 * KindTraits<KIND>::kMaxStages + 5;  // full, empty, peer, tfull[2],
+  static constexpr int kNumBars = 2 * KindTraits<KIND>::kMaxStages + 5;  // full, empty, tfull[2],
                                                                         // tempty[2], drain
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
@@ -359,8 +359,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
   uint8_t* smem = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
   uint64_t* empty = full + NSTMAX;
-  uint64_t* peer = empty + NSTMAX;  // WGRAD pairs: the odd CTA's ragged k block is ready
-  uint64_t* tfull = peer + NSTMAX;
+  uint64_t* tfull = empty + NSTMAX;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
@@ -374,7 +373,6 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     for (int s = 0; s < NST; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
-      mbar_init(peer + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
@@ -455,6 +453,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued_phase[NSTMAX];
+      int rag_slot = 0;  // WGRAD: the tensor-map slot of the last partial k block
 #pragma unroll
       for (int s = 0; s < NSTMAX; ++s) issued_phase[s] = -1;
       bool ok = true;
@@ -464,24 +463,30 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
           if constexpr (PAIR) {
             uint8_t* sA = smem + stage * SBYTES;
-            const bool ragged = KIND == KIND_WGRAD && ti.krow_end - (ti.krow0 + kb * kBK) < kBK;
             // router: every pair reads the same router weight; start each pair at
             // a different k block (the sum runs over all k blocks either way)
             const int kbp = (KIND == KIND_ROUTER) ? (kb + tile_first * 5) % ti.nkb : kb;
-            if (ragged) {
-              // WGRAD's partial last k block: each CTA's share completes on
-              // its own barrier, so that each can zero its rows past the
-              // expert before the MMA (the odd CTA then relays)
-              mbar_arrive_expect_tx(full + stage, TR::kStageBytesK);
-              issue_loads_pair<KIND>(p, ti, kb, rank, sA, sA + kABytes, 0u, &ma, &mb0, &mb1, full + stage);
-            } else {
-              // both CTAs' shares complete on the even CTA's barrier, which
-              // expects them; a share may land before the expectation (the
-              // transaction count goes below zero meanwhile)
-              if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
-              issue_loads_pair<KIND>(p, ti, kbp, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), &ma,
-                                     &mb0, &mb1, nullptr, &mo1);
+            const CUtensorMap* amap = &ma;
+            if constexpr (KIND == KIND_WGRAD) {
+              if (ti.krow_end - (ti.krow0 + kb * kBK) < kBK) {
+                // the expert's last, partial k block: A comes through a copy
+                // of its map whose row extent ends at the expert's last row,
+                // so the TMA reads zeros past it and those rows contribute
+                // nothing whatever B holds there. Two slots per CTA, used in
+                // turn: a slot is rewritten a whole tile after its last load
+                // landed.
+                rag_slot ^= 1;
+                uint8_t* slot = p.tmap_slots + (static_cast<size_t>(blockIdx.x) * 2 + rag_slot) * 128;
+                tmap_set_rows(&ma, slot, ti.krow_end);
+                amap = reinterpret_cast<const CUtensorMap*>(slot);
+              }
             }
+            // both CTAs' shares complete on the even CTA's barrier, which
+            // expects them; a share may land before the expectation (the
+            // transaction count goes below zero meanwhile)
+            if (leader) mbar_arrive_expect_tx(full + stage, stage_tx_bytes<KIND>(p));
+            issue_loads_pair<KIND>(p, ti, kbp, rank, sA, sA + kABytes, mapa_shared(smem_u32(full + stage), 0), amap,
+                                   &mb0, &mb1, &mo1);
             issued_phase[stage] = static_cast<int>(phase);
             if (++stage == NST) { stage = 0; phase ^= 1u; }
             continue;
@@ -534,36 +539,6 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    uint32_t rag_bits = 0;  // WGRAD pairs: phase of each stage's ragged-block barrier
-    if (PAIR && KIND == KIND_WGRAD && !leader) {
-      // the odd CTA of a WGRAD pair: for each ragged k block, wait for this
-      // CTA's share, zero its A rows past the expert, and tell the even CTA
-      const uint32_t peer_even = mapa_shared(smem_u32(peer), 0);
-      for (int tile = tile_first; tile < ntiles && ok; tile += tile_step) {
-        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
-        for (int kb = 0; kb < ti.nkb; ++kb) {
-          const int valid = ti.krow_end - (ti.krow0 + kb * kBK);
-          if (valid < kBK) {
-            if (!mbar_wait_bounded(full + stage, (rag_bits >> stage) & 1u, s_abort, lim, p.status, 5)) {
-              ok = false;
-              break;
-            }
-            rag_bits ^= 1u << stage;
-            uint8_t* sA = smem + stage * SBYTES;
-#pragma unroll
-            for (int box = 0; box < 2; ++box) {
-              uint8_t* base = sA + box * 8192 + ((lane & 7) << 4);
-              for (int rr = valid + (lane >> 3); rr < kBK; rr += 4)
-                *reinterpret_cast<uint4*>(base + rr * 128) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(peer_even + 8u * static_cast<uint32_t>(stage));
-          }
-          if (++stage == NST) stage = 0;
-        }
-      }
-    }
     // pairs: only the even CTA issues MMAs; its peer's MMA warp holds the
     // tensor memory allocation and waits at the end
     for (int tile = tile_first; tile < ntiles && ok && leader; tile += tile_step) {
@@ -673,42 +648,6 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       for (int kb = 0; kb < ((TR::kMx || TR::kNv) ? 0 : ti.nkb); ++kb) {
         if (!mbar_wait_bounded(full + stage, phase, s_abort, lim, p.status, 3)) { ok = false; break; }
         tc_fence_after();
-        if constexpr (KIND == KIND_WGRAD) {
-          uint8_t* sA = smem + stage * SBYTES;
-          // ragged K: the rows of the last k block past the expert's rows hold
-          // the next expert's data (or TMA zero fill). Zeroing them in the A
-          // operand (two 64-row boxes of 128-byte rows) makes their products
-          // zero whatever B holds there (finite values). Lane l clears 16-byte
-          // chunk l&7 of rows valid + l/8, valid + l/8 + 4, ...
-          const int valid = ti.krow_end - (ti.krow0 + kb * kBK);
-          if (valid < kBK) {
-#pragma unroll
-            for (int box = 0; box < 2; ++box) {
-              uint8_t* base = sA + box * 8192 + ((lane & 7) << 4);
-              for (int rr = valid + (lane >> 3); rr < kBK; rr += 4)
-                *reinterpret_cast<uint4*>(base + rr * 128) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            if constexpr (PAIR) {
-              // the odd CTA's share of this block is zeroed likewise: wait for
-              // its relay (cluster-scope acquire)
-              const uint32_t par = (rag_bits >> stage) & 1u;
-              rag_bits ^= 1u << stage;
-              const uint64_t t0 = globaltimer();
-              bool got = mbar_try_wait_cluster(peer + stage, par);
-              while (!got && !*s_abort) {
-                got = mbar_try_wait_cluster(peer + stage, par);
-                if (!got && globaltimer() - t0 > lim) {
-                  *s_abort = 1;
-                  set_status(p.status, MOE_ERR_DEVICE_TIMEOUT, 6);
-                }
-              }
-              if (!got) { ok = false; break; }
-              tc_fence_after();
-            }
-          }
-          __syncwarp();
-        }
         if (lane == 0) {
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;

@@ -159,6 +159,7 @@ struct GemmParams {
   const void* in_aux;    // DGRAD2, DGRAD2R: h13 (saved pre-activations)
   float* dg_part;        // DGRAD2R: gate-gradient partials [rows, n_part] (DGRAD2R also stores a in out1)
   uint8_t* q_out;        // DGRAD2_MX: MXFP8 codes of dh13 [rows, 2F] (scales in sfa_out)
+  uint8_t* tmap_slots;   // WGRAD: two 128-byte global slots per CTA for the A map of a partial k block
   int n_part;            // DGRAD2R: 256-column tiles of F
   int out_fp32;          // FFN2: y_perm fp32
   // MXFP8 kinds: the activations' scale blocks are read through a tensor map;
@@ -252,13 +253,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
 // (FFN1: the W1 (even CTA) or W3 (odd CTA) columns of the tile; FFN2: columns
 // n0 + 128 rank ..; DGRAD2 / DGRAD1: B rows n0 + 128 rank .., boxes of 128
 // rows; WGRAD: A columns m0 .. m0 + 127 and B columns n0 + 128 rank .. of the
-// expert's rows kb*64 ..), completing on the even CTA's barrier `bar_cluster`,
-// or (WGRAD, `local_bar` != nullptr) on this CTA's own barrier.
+// expert's rows kb*64 .., A through the map `ma` given), completing on the even
+// CTA's barrier `bar_cluster`.
 template <int KIND>
 __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const TileInfo& ti, int kb, int rank,
                                                  uint8_t* sA, uint8_t* sB, uint32_t bar_cluster, const CUtensorMap* ma,
                                                  const CUtensorMap* mb0, const CUtensorMap* mb1,
-                                                 uint64_t* local_bar = nullptr, const CUtensorMap* msfb = nullptr) {
+                                                 const CUtensorMap* msfb = nullptr) {
   if constexpr (KindTraits<KIND>::kNv) {
     // 256 k elements (128 bytes) of this CTA's 128 A rows and its 96 B rows
     // (rows n0 + 96 rank .. of expert g's [N] weight rows), its A scale block
@@ -313,17 +314,10 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
   if constexpr (KIND == KIND_WGRAD) {
     const int r = ti.krow0 + kk;
     const int n = ti.n0 + 128 * rank;
-    if (local_bar != nullptr) {
-      tma_load_2d(sA, ma, local_bar, ti.m0, r);
-      tma_load_2d(sA + 8192, ma, local_bar, ti.m0 + 64, r);
-      tma_load_2d(sB, mb0, local_bar, n, r);
-      tma_load_2d(sB + 8192, mb0, local_bar, n + 64, r);
-    } else {
-      tma_load_2d_pair(sA, ma, bar_cluster, ti.m0, r);
-      tma_load_2d_pair(sA + 8192, ma, bar_cluster, ti.m0 + 64, r);
-      tma_load_2d_pair(sB, mb0, bar_cluster, n, r);
-      tma_load_2d_pair(sB + 8192, mb0, bar_cluster, n + 64, r);
-    }
+    tma_load_2d_pair(sA, ma, bar_cluster, ti.m0, r);
+    tma_load_2d_pair(sA + 8192, ma, bar_cluster, ti.m0 + 64, r);
+    tma_load_2d_pair(sB, mb0, bar_cluster, n, r);
+    tma_load_2d_pair(sB + 8192, mb0, bar_cluster, n + 64, r);
     return;
   }
   tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
