@@ -191,10 +191,8 @@ static int router_dw_splits(int T) {
   return s < 1 ? 1 : s;
 }
 
-// the weight-gradient kernels' per-CTA tensor-map slots (two of 128 bytes),
-// for grids of up to kMaxGemmCtas CTAs
-constexpr size_t kTmapSlotBytes = 256;
-constexpr int kMaxGemmCtas = 1024;
+// the weight-gradient kernels' per-expert tensor-map copies (128 bytes each)
+constexpr size_t kTmapSlotBytes = 128;
 
 static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, bool nv = false) {
   WsLayout L{};
@@ -259,7 +257,7 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.dL_hl = take(2 * T * 2 * Ep);
     L.dx_r = take(4 * T * H);
     L.dwr_part = take(4 * static_cast<size_t>(router_dw_splits(c.T)) * E * H);
-    L.tmap_slots = take(kTmapSlotBytes * kMaxGemmCtas);  // weight gradients: per-CTA A-map slots
+    L.tmap_slots = take(kTmapSlotBytes * E);  // weight gradients: per-expert A-map copies
   }
   L.total = o;
   return L;
@@ -771,7 +769,6 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
                           bool mx_wgrad = false) {
   // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
   const bool recompute = mx == nullptr && saved->a == nullptr;
-  if (num_sms() > kMaxGemmCtas) return MOE_ERR_UNSUPPORTED_SHAPE;  // the tensor-map slots of the weight gradients
   DevStatus* st = at<DevStatus>(ws, 0);
   const int R = c.T * c.k;
   const int Ep = padded_experts(c.E);
@@ -854,9 +851,10 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     CUtensorMap mo;
     if (!make_map_f32_3d(&mo, dW2, c.H, c.F, c.E)) return MOE_ERR_CUDA;
     const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_tmap_rows(ma, saved->offsets, c.E, p.tmap_slots, s));
     MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s,
                          &mo, &mo));
-    stage_done(s, STAGE_WGRAD2, 1);
+    stage_done(s, STAGE_WGRAD2, 2);
   }
   // 5. dx_perm = dh13 [W1_e | W3_e]^T
   if (mx != nullptr) {
@@ -900,9 +898,10 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     if (!make_map_f32_3d(&mo1, dW1, c.F, c.H, c.E) || !make_map_f32_3d(&mo3, dW3, c.F, c.H, c.E))
       return MOE_ERR_CUDA;
     const long long tiles = static_cast<long long>(c.E) * p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_tmap_rows(ma, saved->offsets, c.E, p.tmap_slots, s));
     MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s,
                          &mo1, &mo3));
-    stage_done(s, STAGE_WGRAD13, 1);
+    stage_done(s, STAGE_WGRAD13, 2);
   }
   // 7. router part of dx: dx_r = dL W_r (fp32)
   {

@@ -453,7 +453,6 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued_phase[NSTMAX];
-      int rag_slot = 0;  // WGRAD: the tensor-map slot of the last partial k block
 #pragma unroll
       for (int s = 0; s < NSTMAX; ++s) issued_phase[s] = -1;
       bool ok = true;
@@ -469,15 +468,13 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
             const CUtensorMap* amap = &ma;
             if constexpr (KIND == KIND_WGRAD) {
               if (ti.krow_end - (ti.krow0 + kb * kBK) < kBK) {
-                // the expert's last, partial k block: A comes through a copy
-                // of its map whose row extent ends at the expert's last row,
-                // so the TMA reads zeros past it and those rows contribute
-                // nothing whatever B holds there. Two slots per CTA, used in
-                // turn: a slot is rewritten a whole tile after its last load
-                // landed.
-                rag_slot ^= 1;
-                uint8_t* slot = p.tmap_slots + (static_cast<size_t>(blockIdx.x) * 2 + rag_slot) * 128;
-                tmap_set_rows(&ma, slot, ti.krow_end);
+                // the expert's last, partial k block: A comes through the
+                // expert's copy of its map (written before this launch by
+                // tmap_rows_kernel), whose row extent ends at the expert's
+                // last row, so the TMA reads zeros past it and those rows
+                // contribute nothing whatever B holds there
+                const uint8_t* slot = p.tmap_slots + static_cast<size_t>(ti.g) * 128;
+                asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(slot) : "memory");
                 amap = reinterpret_cast<const CUtensorMap*>(slot);
               }
             }
@@ -830,6 +827,22 @@ static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const
   }
   cfg.gridDim = dim3(grid);
   return cudaLaunchKernelEx(&cfg, kern, p, ma, mb0, mb1, mo0, mo1);
+}
+
+// Per-expert copies of the weight gradients' A tensor map: maps[e] (128 bytes)
+// = tmpl with its row extent set to expert e's end row offsets[e + 1],
+// released to the TMA unit (the GEMM launched next acquires each copy before
+// its first use).
+__global__ void tmap_rows_kernel(const __grid_constant__ CUtensorMap tmpl, const int32_t* __restrict__ offsets, int E,
+                                 uint8_t* __restrict__ maps) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  tmap_set_rows(&tmpl, maps + static_cast<size_t>(e) * 128, offsets[e + 1]);
+}
+
+cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st) {
+  tmap_rows_kernel<<<(E + 127) / 128, 128, 0, st>>>(tmpl, offsets, E, maps);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,

@@ -159,7 +159,7 @@ struct GemmParams {
   const void* in_aux;    // DGRAD2, DGRAD2R: h13 (saved pre-activations)
   float* dg_part;        // DGRAD2R: gate-gradient partials [rows, n_part] (DGRAD2R also stores a in out1)
   uint8_t* q_out;        // DGRAD2_MX: MXFP8 codes of dh13 [rows, 2F] (scales in sfa_out)
-  uint8_t* tmap_slots;   // WGRAD: two 128-byte global slots per CTA for the A map of a partial k block
+  uint8_t* tmap_slots;   // WGRAD: per-expert copies of the A map (128 bytes each) for the partial k blocks
   int n_part;            // DGRAD2R: 256-column tiles of F
   int out_fp32;          // FFN2: y_perm fp32
   // MXFP8 kinds: the activations' scale blocks are read through a tensor map;

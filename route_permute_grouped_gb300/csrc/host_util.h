@@ -128,6 +128,9 @@ cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, 
 cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
                                        const __nv_bfloat16* W2, uint8_t* w13q, uint8_t* sf13, uint8_t* w2q,
                                        uint8_t* sf2, cudaStream_t st);
+// gemm.cu: per-expert copies of a 2-D tensor map with the row extent set to
+// each expert's end row (for the weight gradients' partial k blocks)
+cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st);
 cudaError_t launch_mx_quantize_tokens(const __nv_bfloat16* X, int R, int C, int ldx, int E, const int32_t* offsets,
                                       uint8_t* XT, uint8_t* sf, int tile_rows, int32_t* pad_off, cudaStream_t st);
 cudaError_t launch_mx_quantize_bwd_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,
