@@ -293,6 +293,12 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
  * block zero-padded). Routing, combine, their backward and the router
  * backward are those of the bf16 layer. Requires H and F multiples of 128
  * and F_shared == 0.
+ * Every call below enqueues on `stream` and returns without a host sync; it
+ * returns MOE_ERR_INVALID_ARG for a null or misaligned pointer,
+ * MOE_ERR_UNSUPPORTED_SHAPE for a shape outside the above,
+ * MOE_ERR_WORKSPACE_TOO_SMALL for ws_bytes below moe_mx_train_workspace_bytes
+ * (which includes the buffers of the MXFP8 weight gradients), before any CUDA
+ * work; device-detected errors go to the workspace's status word.
  * ------------------------------------------------------------------------- */
 
 /* The weights of the two data-gradient GEMMs, device buffers owned by the
