@@ -37,7 +37,7 @@ rounding off (used by the finite-difference pins).
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, replace
+from dataclasses import dataclass
 
 import numpy as np
 

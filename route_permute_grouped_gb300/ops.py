@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_float, c_int, c_int32, c_longlong, c_size_t, c_void_p
+from ctypes import POINTER, c_float, c_int, c_longlong, c_size_t, c_void_p
 
 import torch
 

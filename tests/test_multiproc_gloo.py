@@ -2,12 +2,10 @@
 2: every rank runs its own replica (no collective on the data path); the step
 time is the maximum over ranks and the job value counts the work of every rank.
 The reference arm prints from rank 0 only."""
-import json
 import os
 import subprocess
 import sys
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp

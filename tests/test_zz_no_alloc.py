@@ -5,7 +5,6 @@ calls in a row (the second call must not see the first call's leftovers).
 Collected last so that a failure here never hides another test's result."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
