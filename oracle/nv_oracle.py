@@ -35,7 +35,8 @@ from .moe_oracle import bf16_rne, permute_plan, route, silu
 from .mx_oracle import e4m3_encode, e4m3_round
 
 __all__ = ["E2M1_MAX", "e2m1_round", "e2m1_encode", "e2m1_decode", "nv_tensor_scale", "nv_quantize",
-           "nv_dequantize", "nv_roundtrip", "nv_grouped_gemm", "nv_layer_fwd"]
+           "nv_dequantize", "nv_roundtrip", "nv_grouped_gemm", "routed_rows_roundtrip", "gate_up_store",
+           "activation_roundtrip", "nv_layer_fwd"]
 
 E2M1_MAX = 6.0
 NV_BLOCK = 16
@@ -137,6 +138,30 @@ def nv_grouped_gemm(x, offsets, W, out_bf16=True):
     return bf16_rne(y) if out_bf16 else y
 
 
+def routed_rows_roundtrip(rows, offsets):
+    """NVFP4 round trip of the routed rows x_perm [R,H] as ONE tensor: one fp32
+    tensor scale from the maximum over every routed row (whatever its expert),
+    16-element blocks along H (the gate/up GEMM's K)."""
+    rows = np.asarray(rows, np.float32)
+    g = nv_tensor_scale(np.abs(rows).max() if rows.size else 0.0)
+    return nv_roundtrip(rows, axis=1, g=g)
+
+
+def gate_up_store(h):
+    """The gate/up GEMM's output as the layer stores it: bf16 (round to nearest
+    even), before the activation is formed from it."""
+    return bf16_rne(h)
+
+
+def activation_roundtrip(a, offsets):
+    """NVFP4 round trip of the SwiGLU activation a [R,F] as ONE tensor over all
+    routed rows (one tensor scale), 16-element blocks along F (the down GEMM's
+    K)."""
+    a = np.asarray(a, np.float32)
+    g = nv_tensor_scale(np.abs(a).max() if a.size else 0.0)
+    return nv_roundtrip(a, axis=1, g=g)
+
+
 def nv_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
                  topk_groups=1, gate_scale=1.0, tokens=None, force_balanced=False):
     """Forward of the layer with NVFP4 expert GEMMs.
@@ -145,11 +170,12 @@ def nv_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
     form one tensor; expert e's [W1_e | W3_e] (H x 2F, blocks along H) one
     tensor and W2_e (blocks along F) another. Per expert:
       h  = bf16(Q(x_e) Q([W1_e | W3_e]))        (the gate/up GEMM, stored bf16)
-      a  = bf16(SiLU(h1) h3)                    (stored bf16)
+      a  = bf16(SiLU(h1) h3)                    (from the stored h; stored bf16)
       out = bf16(Q(a_e) Q(W2_e))                (a quantised as one tensor over all rows)
-    with Q = ``nv_roundtrip``. The tensor scale of a comes from the maximum of
-    a over every routed row, so a is formed for all rows; ``tokens`` restricts
-    the combine."""
+    with Q = ``nv_roundtrip`` (steps: ``routed_rows_roundtrip``,
+    ``gate_up_store``, ``activation_roundtrip``). The tensor scale of a comes
+    from the maximum of a over every routed row, so a is formed for all rows;
+    ``tokens`` restricts the combine."""
     x = np.asarray(x, np.float64)
     T, H = x.shape
     rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
@@ -158,8 +184,7 @@ def nv_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
     R = T * k
     x_perm = np.zeros((R, H), np.float32)
     x_perm[row.reshape(-1)] = np.repeat(x.astype(np.float32), k, axis=0)
-    gx = nv_tensor_scale(np.abs(x_perm).max() if R else 0.0)
-    xq = nv_roundtrip(x_perm, axis=1, g=gx)
+    xq = routed_rows_roundtrip(x_perm, offsets)
     F = np.asarray(W1[0]).shape[1]
     a = np.zeros((R, F))
     for e in range(E):
@@ -167,10 +192,9 @@ def nv_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
         if hi == lo:
             continue
         W13 = np.concatenate([np.asarray(W1[e], np.float32), np.asarray(W3[e], np.float32)], axis=1)
-        h = bf16_rne(xq[lo:hi] @ nv_roundtrip(W13, axis=0))
+        h = gate_up_store(xq[lo:hi] @ nv_roundtrip(W13, axis=0))
         a[lo:hi] = bf16_rne(silu(h[:, :F]) * h[:, F:])
-    ga = nv_tensor_scale(np.abs(a).max() if R else 0.0)
-    aq = nv_roundtrip(a.astype(np.float32), axis=1, g=ga)
+    aq = activation_roundtrip(a, offsets)
     y_perm = np.zeros((R, H))
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])

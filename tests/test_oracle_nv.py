@@ -1,7 +1,9 @@
 """Pins of the NVFP4 oracle (CPU): the E2M1 code table and its ties, the
 E4M3 block-scale and fp32 tensor-scale rules on hand-computed blocks, the
 quantisation error bound, the grouped GEMM on inputs where quantisation is
-exact, and planted mistakes that the pins must catch."""
+exact, the layer forward on inputs where every NVFP4 quantisation is exact
+(it then reduces to the plain bf16 layer), and planted mistakes that the pins
+must catch."""
 import numpy as np
 import pytest
 
@@ -132,3 +134,122 @@ def test_nv_layer_routing_and_fp4_closeness():
     # the tokens argument restricts the combine only
     sub = O.nv_layer_fwd(x, w_r, W1, W3, W2, k, tokens=np.array([3, 7]))
     np.testing.assert_array_equal(sub["y"][[3, 7]], out["y"][[3, 7]])
+
+
+# ---------------------------------------------------------------------------
+# The NVFP4 layer on exact inputs.
+#
+# Every operand below is an E2M1 value times a power of two per 16-element
+# block (the block's largest magnitude being 6 or 7.5 times that power), and
+# each tensor's maximum sits alone in its block with 2688 = 6 * 448 times a
+# power of two, so every tensor scale is a power of two and every block scale
+# an E4M3 value: quantising x_perm, [W1_e | W3_e], a and W2_e changes nothing.
+# The gate pre-activation of one entry carries a part below half a bf16 ulp
+# (64 + 7/32), which the stored bf16 h drops. The NVFP4 layer must then equal
+# the plain bf16 layer (a and y_perm rounded to bf16) run on weights without
+# that part.
+#
+# Layout: T = 32 tokens, H = 80 (blocks of 16: 0..3 signal, 4 routing), F = 32,
+# E = 2, k = 1; tokens 0..15 go to expert 0, 16..31 to expert 1.
+# ---------------------------------------------------------------------------
+def _exact_layer():
+    T, H, F, E = 32, 80, 32, 2
+    A, B, D, C, Z, C2 = 0, 1, 2, 16, 17, 18
+    x = np.zeros((T, H))
+    x[:, 0] = 4.0                      # shared feature: h1 = 4 * 16 = 64 everywhere
+    x[:, 14] = 6.0                     # block-0 maximum of every row (its weight rows are zero)
+    x[:16, 64] = 6.0                   # routing feature of expert 0
+    x[16:, 65] = 6.0                   # routing feature of expert 1
+    x[A, 1] = 6.0                      # private features
+    x[A, 16], x[A, 30] = 0.5, 6.0
+    x[A, 32], x[A, 46] = -1.0, 6.0
+    x[B, 2] = 1.0
+    x[B, 20] = 7.5                     # alone in its block: a block of the 1.25 * 2^j family
+    x[D, 4] = 6.0
+    x[C, 3] = 1.0
+    x[C2, 5] = 1.0
+    x[Z, 48] = 10.5                    # the tensor maximum of x: 2688 * 2^-8, alone in its block
+    w_r = np.zeros((E, H))
+    w_r[0, 64] = 1.0
+    w_r[1, 65] = 1.0
+    W1 = np.zeros((E, H, F))
+    W3 = np.zeros((E, H, F))
+    W2 = np.zeros((E, F, H))
+    for e in range(E):
+        W1[e, 0, :] = 16.0             # x feature 0 (4) * 16 = 64
+        W1[e, 15, :] = 24.0            # block maximum 6 * 4 (x is 0 on row 15)
+        W1[e, 49, 1] = 42.0            # tensor maximum of [W1_e | W3_e]: 2688 * 2^-6, alone
+        W2[e, 15, :79] = 0.375         # block maxima of W2 (a is 0 on columns 15 and 31)
+        W2[e, 31, :79] = 0.375
+        W2[e, 14, 79] = 2.625          # tensor maximum of W2_e: 2688 * 2^-10, alone
+    rng = np.random.default_rng(21)
+    vals = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]) * 2.0 ** -4
+    for e in range(E):
+        for rows in (slice(0, 14), slice(16, 30)):
+            W2[e, rows, :79] = rng.choice(vals, (14, 79)) * rng.choice([-1.0, 1.0], (14, 79))
+    # the entry (A, f=0): h1 = 64 + 0.5 * 0.5 - 1 * 2^-5 = 64.21875, stored as 64
+    W1[0, 16, 0], W1[0, 31, 0] = 0.5, 6.0
+    W1[0, 32, 0], W1[0, 47, 0] = 2.0 ** -5, 6.0 * 2.0 ** -5
+    # expert 0's up projection: h3(A,0) = 6 * 0.25 - 0.5 * 0.375 = 1.3125 (a = 84,
+    # the tensor maximum of a: 2688 * 2^-5); h3(B,0) = 0.25 (a = 16), h3(B,1) =
+    # 0.375 (a = 24); token D: h3 = 6 * 2^-6 +- 0.5 * 2^-11, the two bf16 ties
+    # around 0.09375, both stored as 0.09375 (a = 6)
+    W3[0, 1, 0], W3[0, 2, 0], W3[0, 15, 0] = 0.25, 0.25, 3.0
+    W3[0, 16, 0], W3[0, 31, 0] = -0.375, 1.5
+    W3[0, 2, 1], W3[0, 15, 1] = 0.375, 1.5
+    for f, sgn in ((16, 1.0), (17, -1.0)):
+        W3[0, 4, f], W3[0, 15, f] = 2.0 ** -6, 6.0 * 2.0 ** -6
+        W3[0, 17, f], W3[0, 31, f] = sgn * 2.0 ** -11, 6.0 * 2.0 ** -11
+    # expert 1: h3(C,0) = 0.09375 (a = 6); h3(C2,2) = 0.1171875 (a = 7.5, alone
+    # in its block: the 1.25 * 2^j family)
+    W3[1, 3, 0], W3[1, 15, 0] = 0.09375, 0.375
+    W3[1, 5, 2], W3[1, 15, 2] = 0.1171875, 0.46875
+    plain_W1 = W1.copy()
+    plain_W1[0, 16, 0] = 0.0           # the part of h1(A,0) below half a bf16 ulp
+    plain_W1[0, 32, 0] = 0.0
+    return x, w_r, W1, W3, W2, plain_W1
+
+
+def test_nv_layer_exact_inputs_reduce_to_plain_layer():
+    x, w_r, W1, W3, W2, plain_W1 = _exact_layer()
+    out = O.nv_layer_fwd(x, w_r, W1, W3, W2, 1)
+    # the quantisations are exact: x_perm, [W1_e | W3_e] and W2_e round-trip unchanged
+    xp = np.zeros_like(x)
+    xp[out["row_id_map"][:, 0]] = x
+    assert np.array_equal(O.routed_rows_roundtrip(xp, out["offsets"]), xp)
+    for e in range(2):
+        W13 = np.concatenate([W1[e], W3[e]], axis=1)
+        assert np.array_equal(O.nv_roundtrip(W13, axis=0), W13)
+        assert np.array_equal(O.nv_roundtrip(W2[e], axis=0), W2[e])
+    ref = O.layer_fwd(x, w_r, plain_W1, W3, W2, 1, prec=O.CONTRACT)
+    assert np.array_equal(out["topk_idx"], ref["topk_idx"]) and np.array_equal(out["row_id_map"], ref["row_id_map"])
+    assert np.array_equal(out["counts"], [16, 16])
+    np.testing.assert_allclose(out["y"], ref["y"], rtol=1e-12, atol=1e-12)
+    # the output is not trivially zero and carries every designed activation
+    assert np.count_nonzero(np.abs(ref["y"]) > 1.0) > 100
+
+
+def _per_expert_rows(rows, offsets):
+    out = np.zeros(np.shape(rows))
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            out[lo:hi] = O.nv_roundtrip(np.asarray(rows[lo:hi], np.float32), axis=1)
+    return out
+
+
+def _act_wrong_axis(a, offsets):
+    return O.nv_roundtrip(np.asarray(a, np.float32), axis=0)
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("routed_rows_roundtrip", _per_expert_rows),     # a tensor scale per expert for x_perm
+    ("gate_up_store", lambda h: np.asarray(h)),      # h not rounded to bf16 before SiLU
+    ("activation_roundtrip", _per_expert_rows),      # a tensor scale per expert for a
+    ("activation_roundtrip", _act_wrong_axis),       # a quantised along the rows, not along F
+], ids=["x_scale_per_expert", "h_unrounded", "a_scale_per_expert", "a_wrong_axis"])
+def test_planted_nv_layer_mistake_is_caught(monkeypatch, name, fn):
+    import oracle.nv_oracle as NV
+    monkeypatch.setattr(NV, name, fn)
+    with pytest.raises(AssertionError):
+        test_nv_layer_exact_inputs_reduce_to_plain_layer()
