@@ -166,11 +166,18 @@ int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_id
  * cudaMemsetAsync on `stream` and launches the permute kernels. All calls
  * share the one array, so calls that overlap on the GPU (other streams or
  * threads) race and give wrong results; serialise them. Device-side errors
- * of this entry point are not reported (moe_get_device_status reads a
- * workspace, which this call does not have). */
+ * (an index outside [0,E) skipped, a bounded wait that ran out) go to the
+ * status word of that array, which each call clears first:
+ * moe_noalloc_get_device_status reads the most recent call's. */
 int moe_permute_noalloc(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx,
                         moe_bf16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
                         void* stream);
+
+/* Synchronises `stream`, returns in *status_out the device-side status of the
+ * most recent moe_permute_noalloc call on the current device (MOE_OK if none;
+ * MOE_ERR_DEVICE_INDEX, MOE_ERR_DEVICE_TIMEOUT as for moe_permute) and
+ * clears it. Allocates nothing; for tests and debugging. */
+int moe_noalloc_get_device_status(void* stream, int* status_out);
 
 /* Grouped SwiGLU experts (summary page, "Key Terms", Grouped GEMM and
  * "System Modules", Experts; figures & tables page, Table 4): for each expert
@@ -463,6 +470,17 @@ void moe_profile_start(int capacity);
 void moe_profile_stop(void);
 int moe_profile_read(int* tags, float* ms, int max);
 unsigned long long moe_debug_launch_count(void);
+
+/* Test hook: byte offset, inside a workspace of moe_workspace_bytes(cfg,
+ * training), of an intermediate the layer keeps there, so that tests can read
+ * the bf16 operands the backward's GEMMs consumed: which = 0 dy_perm [R,H]
+ * (g * dO per routed row), 1 dh13 [R,2F] (dh1 in columns [0,F), dh3 in
+ * [F,2F)), 2 a [R,F] (the activation of the memory-saving mode), 3 dx_perm
+ * [R,H], all bf16, rows grouped by expert as x_perm. Valid until the next call
+ * that uses the workspace. Returns (size_t)-1 for an invalid config, an
+ * unknown `which`, or a buffer the workspace does not hold (training == 0 and
+ * which != 2). */
+size_t moe_debug_workspace_offset(const moe_config* cfg, int training, int which);
 
 #ifdef __cplusplus
 }

@@ -63,6 +63,7 @@ static void stage_done(cudaStream_t s, int tag, int launches) {
     fprintf(stderr, "moe: stage %d done: %s\n", tag, cudaGetErrorString(e));
   }
 }
+void record_stage(cudaStream_t s, int tag, int launches) { stage_done(s, tag, launches); }
 unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
 int debug_fault() { return g_fault; }
 
@@ -298,6 +299,7 @@ static int cuda_status(cudaError_t e) {
   fprintf(stderr, "moe: CUDA error %s\n", cudaGetErrorString(e));
   return MOE_ERR_CUDA;
 }
+int status_from_cuda(cudaError_t e) { return cuda_status(e); }
 
 static GemmParams base_params(const moe_config& c, DevStatus* st) {
   GemmParams p;
@@ -627,6 +629,19 @@ int moe_profile_read(int* tags, float* ms, int max) {
 }
 
 unsigned long long moe_debug_launch_count(void) { return g_launches; }
+
+size_t moe_debug_workspace_offset(const moe_config* cfg, int training, int which) {
+  if (check_cfg(cfg) != MOE_OK) return static_cast<size_t>(-1);
+  const WsLayout L = ws_layout(*cfg, training != 0);
+  if (training == 0 && which != 2) return static_cast<size_t>(-1);
+  switch (which) {
+    case 0: return L.dy_perm;
+    case 1: return L.dh13;
+    case 2: return L.a;
+    case 3: return L.dx_perm;
+    default: return static_cast<size_t>(-1);
+  }
+}
 
 int moe_get_device_status(void* ws, void* stream, int* status_out) {
   if (ws == nullptr || status_out == nullptr) return MOE_ERR_INVALID_ARG;

@@ -18,6 +18,11 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
                    uint32_t box_inner, uint32_t box_outer);
 
 int num_sms();
+// Bookkeeping every entry point does after enqueueing a stage: launch counter,
+// profiling event (tag as in moe_profile_start), debug synchronisation.
+void record_stage(cudaStream_t s, int tag, int launches);
+// MOE_OK for cudaSuccess, else MOE_ERR_CUDA with the CUDA message on stderr.
+int status_from_cuda(cudaError_t e);
 unsigned long long wait_limit_ns();
 int debug_fault();
 

@@ -89,6 +89,8 @@ def lib():
         L.moe_profile_read.restype = c_int
         L.moe_debug_launch_count.argtypes = []
         L.moe_debug_launch_count.restype = ctypes.c_ulonglong
+        L.moe_debug_workspace_offset.argtypes = [POINTER(MoeConfig), c_int, c_int]
+        L.moe_debug_workspace_offset.restype = c_size_t
         L.moe_mx_weight_bytes.restype = c_size_t
         L.moe_mx_weight_bytes.argtypes = [POINTER(MoeConfig), c_int]
         L.moe_mx_workspace_bytes.restype = c_size_t
@@ -159,6 +161,20 @@ def profile_read(max_events: int):
 
 def launch_count() -> int:
     return int(lib().moe_debug_launch_count())
+
+
+WS_TENSORS = {"dy_perm": 0, "dh13": 1, "a": 2, "dx_perm": 3}
+
+
+def workspace_tensor(ws, cfg, training, name):
+    """Test hook: a bf16 view of an intermediate the layer keeps in the
+    workspace (dy_perm [R,H], dh13 [R,2F], a [R,F], dx_perm [R,H])."""
+    off = int(lib().moe_debug_workspace_offset(ctypes.byref(cfg), int(training), WS_TENSORS[name]))
+    if off == ctypes.c_size_t(-1).value:
+        raise MoeError(1, "moe_debug_workspace_offset")
+    R = cfg.T * cfg.k
+    cols = {"dy_perm": cfg.H, "dh13": 2 * cfg.F, "a": cfg.F, "dx_perm": cfg.H}[name]
+    return ws[off:off + 2 * R * cols].view(torch.bfloat16).view(R, cols)
 
 
 def _p(t):

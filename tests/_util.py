@@ -90,3 +90,21 @@ def compare_topk(got_idx, ref_idx, z, k, margin=TIE_MARGIN):
         if sep:
             assert np.array_equal(g, r), f"token {t}: slot order {g} want {r}"
     return int(excl.sum())
+
+
+# Error of CUDA outputs against the fully unrounded fp64 oracle (oracle.EXACT:
+# no bf16 rounding of any stored intermediate). Reported for information next
+# to the contract comparison (which rounds where the layer stores bf16); never
+# asserted. Collected here, printed in pytest's terminal summary.
+EXACT_REPORT = []
+
+
+def report_exact(name, got, exact):
+    """Record rel-L2 and max-abs of `got` against the unrounded oracle value."""
+    got, exact = np.asarray(got, np.float64), np.asarray(exact, np.float64)
+    ok = np.isfinite(exact)
+    if not ok.any():
+        return
+    r = rel_l2(got[ok], exact[ok])
+    m = float(np.max(np.abs(got[ok] - exact[ok])))
+    EXACT_REPORT.append((name, r, m))

@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Error of the CUDA outputs against the fully unrounded fp64 oracle
+    (information only; the asserted comparison rounds where the layer stores
+    bf16)."""
+    try:
+        from tests._util import EXACT_REPORT
+    except Exception:  # pragma: no cover
+        return
+    if not EXACT_REPORT:
+        return
+    tr = terminalreporter
+    tr.section("error against the unrounded fp64 oracle (information)")
+    for name, r, m in EXACT_REPORT:
+        tr.write_line(f"{name:60s} rel_l2 {r:.3e}  max_abs {m:.3e}")

@@ -2,7 +2,10 @@
 largest supported router (E = 256 experts, k = 16, 8-wide per-lane candidate
 lists, the 16-slot combine paths), a single token, and the smallest dimensions
 (H = F = 64, E = 2, k = 1). Forward and backward, every output compared in
-full (no sampling); tokens within the tie margin are excused as elsewhere."""
+full (no sampling) at the layer's bar (dx at max-abs 2e-2; weight gradients
+with the bf16-flip allowance of tests/_util.wgrad_atol); tokens within the tie
+margin are excused as elsewhere, and the gradients that depend on them are
+left out."""
 import numpy as np
 import pytest
 import torch
@@ -50,13 +53,30 @@ def test_edge_layer(name):
     assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=ls.E))
     keep = topk_margin(ref["z"], ls.k) >= 1e-6
     assert_close("y", f64(y)[keep], fw["y"][keep])
-    if excused:
-        return  # a tie changes the expert rows, so the gradients are not comparable
+    # A token within the tie margin may route differently on the two sides;
+    # every gradient is compared where it does not depend on such a token:
+    # dx on tokens whose selection agrees (the counts enter only through the
+    # aux-loss term, alpha E / (T k T) per differing assignment), the expert
+    # weight gradients of experts that receive the same tokens, and the router
+    # weight gradient rows of experts all of whose tokens agree on their
+    # whole selection.
     E = ls.E
-    pairs = {"dx": (f64(g["dx"]), ref["dx"]), "dW_r": (f64(g["dW_r"]), ref["dW_r"]),
-             "dW1": (f64(g["dW1"]), np.stack([ref["dW1"][e] for e in range(E)])),
-             "dW3": (f64(g["dW3"]), np.stack([ref["dW3"][e] for e in range(E)])),
-             "dW2": (f64(g["dW2"]), np.stack([ref["dW2"][e] for e in range(E)]))}
-    for key, (got, want) in pairs.items():
+    same_tok = np.all(np.sort(idx, 1) == np.sort(ref["topk_idx"], 1), axis=1)
+    assert same_tok.sum() >= ls.T - excused
+    got_dx = f64(g["dx"])
+    assert_close("dx", got_dx[same_tok], ref["dx"][same_tok])
+    same_e = [e for e in range(E)
+              if np.array_equal(np.nonzero((idx == e).any(1))[0], np.nonzero((ref["topk_idx"] == e).any(1))[0])]
+    for key in ("dW1", "dW3", "dW2"):
+        got = f64(g[key])[same_e]
+        want = np.stack([ref[key][e] for e in same_e])
         assert_close(key, got, want, atol=wgrad_atol(want))
-    assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))
+    clean_e = [e for e in same_e if same_tok[(idx == e).any(1)].all()]
+    if excused == 0:
+        assert len(clean_e) == E
+    if clean_e:
+        want = ref["dW_r"][clean_e]
+        assert_close("dW_r", f64(g["dW_r"])[clean_e], want, atol=wgrad_atol(want))
+    # a token routed differently moves up to 2k fractions f_e by 1/(T k) each
+    assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= (1e-5 * max(1.0, abs(ref["aux_loss"]))
+                                                                 + 2 * aux * E * excused / ls.T)

@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import assert_close, compare_topk, f64, topk_margin, wgrad_atol
+from tests._util import assert_close, compare_topk, f64, report_exact, topk_margin, wgrad_atol
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -85,8 +85,10 @@ def test_full_forward(name, ntok, out_fp32):
     assert ops.device_status(ws) == 0
     rt, keep = _check_routing(ls, d, saved)
     if ls.skew:
+        # Zipf-skewed popularity: a dominant expert and experts with no token
         counts = saved["counts"].cpu().numpy()
         assert counts.max() > 8 * counts.mean()
+        assert (counts == 0).sum() >= 1
     rng = np.random.default_rng(7)
     tok = _sample(rng, keep, ntok)
     prec = O.Precision(y_perm=not ls.inter_fp32, shared=not ls.inter_fp32, y=not out_fp32)
@@ -96,6 +98,11 @@ def test_full_forward(name, ntok, out_fp32):
                       None if d["logit_bias"] is None else f64(d["logit_bias"]),
                       ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=prec, tokens=tok)
     assert_close("y", f64(y[torch.from_numpy(tok).cuda()]), ref["y"][tok])
+    ex = O.layer_fwd(f64(d["x"]), f64(d["router_w"]), _getter(d), None, None, ls.k, ls.score,
+                     None if d["expert_bias"] is None else f64(d["expert_bias"]),
+                     None if d["logit_bias"] is None else f64(d["logit_bias"]),
+                     ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=O.EXACT, tokens=tok)
+    report_exact(f"full_forward[{name}] y ({len(tok)} tokens)", f64(y[torch.from_numpy(tok).cuda()]), ex["y"][tok])
     # gates of the sampled tokens
     assert_close("gates", f64(saved["topk_gate"])[tok], ref["topk_gate"][tok])
 
@@ -114,6 +121,8 @@ def test_full_training_step(name):
     assert ops.device_status(ws) == 0
     rt, keep = _check_routing(ls, d, saved)
     counts = saved["counts"].cpu().numpy()
+    if ls.skew:
+        assert counts.max() > 8 * counts.mean() and (counts == 0).sum() >= 1
     rng = np.random.default_rng(11)
     gidx = saved["topk_idx"].cpu().numpy()
     # an expert's weight gradient is comparable when the GPU and the oracle route
@@ -139,6 +148,13 @@ def test_full_training_step(name):
         for key in ("dW1", "dW3", "dW2"):
             want = ref[key][e]
             assert_close(f"{key}[{e}]", f64(g[key][e]), want, atol=wgrad_atol(want))
+    ex = O.layer_bwd(x, f64(d["router_w"]), _getter(d), None, None, f64(d["dO"]), ls.k, ls.score, None, lb,
+                     aux_coeff=ls.aux_coeff, prec=O.EXACT, experts=experts, tokens=tok)
+    report_exact(f"full_training_step[{name}] dx ({len(tok)} tokens)", f64(g["dx"][torch.from_numpy(tok).cuda()]),
+                 ex["dx"][tok])
+    for e in experts:
+        for key in ("dW1", "dW3", "dW2"):
+            report_exact(f"full_training_step[{name}] {key}[{e}] ({int(counts[e])} rows)", f64(g[key][e]), ex[key][e])
     # router weight gradient, row of one expert: dL[t,e] for every token. Tokens
     # routed to e need their gate gradients (all k expert outputs); the others
     # only carry the aux-loss part, which depends on their softmax and the counts.

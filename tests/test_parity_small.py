@@ -8,7 +8,7 @@ import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import MAX_ABS, assert_close, compare_topk, f64, rel_l2, wgrad_atol
+from tests._util import MAX_ABS, assert_close, compare_topk, f64, rel_l2, report_exact, wgrad_atol
 
 pytestmark = pytest.mark.gpu
 
@@ -172,6 +172,7 @@ def test_layer_fwd(name, out_fp32):
     keep = topk_margin(rt["z"], ls.k) >= 1e-6
     assert keep.sum() >= 0.99 * ls.T
     assert_close("y", f64(y)[keep], ref["y"][keep])
+    report_exact(f"layer_fwd[{name}, out_fp32={out_fp32}] y", f64(y)[keep], _layer_ref(ls, n, O.EXACT)["y"][keep])
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "e128_k8", "skew", "k1"])
@@ -204,4 +205,10 @@ def test_layer_bwd(name):
         # are larger
         atol = wgrad_atol(want) if (key != "dx" or name in FLIP_BOUND_SHAPES) else MAX_ABS
         assert_close(key, got, want, atol=atol)
+    ex = O.layer_bwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], n["dO"], ls.k, ls.score, n["expert_bias"],
+                     n["logit_bias"], ls.n_groups, ls.topk_groups, ls.gate_scale, aux_coeff=aux, prec=O.EXACT)
+    for key in ("dx", "dW_r"):
+        report_exact(f"layer_bwd[{name}] {key}", pairs[key][0], ex[key])
+    for key in ("dW1", "dW3", "dW2"):
+        report_exact(f"layer_bwd[{name}] {key}", pairs[key][0], np.stack([ex[key][e] for e in range(E)]))
     assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))
