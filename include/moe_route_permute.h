@@ -98,7 +98,10 @@ typedef struct {
  * backward, given the same NULLs, recomputes a = bf16(SiLU(h1) h3) from h13 in
  * the epilogue of the down-projection dgrad and takes the gate gradient there
  * as <da, a> / g (da = dy_perm W2^T, dy_perm = g dO; 0 where g = 0), which
- * equals <dO, y_perm> in exact arithmetic. Saves 2 R (F + H) bytes (bf16). */
+ * equals <dO, y_perm> in exact arithmetic. Saves 2 R (F + H) bytes (bf16).
+ * With a shared expert (F_shared > 0; figures & tables page, Fig. 40):
+ * h13_shared [T,2Fs] bf16 (x Ws1 in columns [0,Fs), x Ws3 in [Fs,2Fs)) and
+ * a_shared [T,Fs] bf16 (SiLU(h1) * h3) are required; otherwise unused. */
 typedef struct {
   int32_t* topk_idx;
   float* topk_gate;
@@ -111,6 +114,8 @@ typedef struct {
   moe_bf16* a;
   void* y_perm;
   float* aux_partials;
+  moe_bf16* h13_shared;
+  moe_bf16* a_shared;
 } moe_fwd_saved;
 
 /* Bytes of device workspace the calls below need (training != 0: the
@@ -218,14 +223,21 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
  * forward; top-k selection and counts carry no gradient). dO [T,H] bf16.
  * Outputs: dx [T,H] (bf16, fp32 if out_fp32); dW_router [E,H], dW1, dW3
  * [E,H,F], dW2 [E,F,H] fp32 (overwritten, zero for experts with no tokens);
- * aux_loss_out (1 fp32, may be NULL; written when aux_coeff != 0). Supported
- * for F_shared == 0. With saved->a and saved->y_perm NULL it runs the
- * memory-saving backward (see moe_fwd_saved); the workspace must be the
- * training size either way. */
+ * aux_loss_out (1 fp32, may be NULL; written when aux_coeff != 0).
+ * Shared expert (F_shared > 0; figures & tables page, Fig. 40: it processes
+ * every token and is added ungated, so its output gradient is dO): Ws1, Ws3
+ * [H,Fs], Ws2 [Fs,H] bf16 as in the forward, saved->h13_shared and
+ * saved->a_shared from the training forward, and the outputs dWs1, dWs3
+ * [H,Fs], dWs2 [Fs,H] fp32; its input gradient is added to dx. All six are
+ * ignored (may be NULL) when F_shared == 0. With saved->a and saved->y_perm
+ * NULL it runs the memory-saving backward of the routed experts (see
+ * moe_fwd_saved); the workspace must be the training size either way. */
 int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x,
                   const moe_bf16* router_w, const moe_bf16* W1, const moe_bf16* W3,
-                  const moe_bf16* W2, const moe_fwd_saved* saved,
+                  const moe_bf16* W2, const moe_bf16* Ws1, const moe_bf16* Ws3,
+                  const moe_bf16* Ws2, const moe_fwd_saved* saved,
                   void* dx, float* dW_router, float* dW1, float* dW3, float* dW2,
+                  float* dWs1, float* dWs3, float* dWs2,
                   float* aux_loss_out, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
@@ -461,7 +473,9 @@ void moe_debug_set_fault(int fault);
  * 7 combine, 10 combine backward, 11 router backward (element-wise), 12 down
  * projection data gradient + SwiGLU backward, 13 down projection weight
  * gradient, 14 gate/up data gradient, 15 gate/up weight gradient, 16 router
- * data gradient, 17 permute backward, 18 router weight gradient, 19 aux loss).
+ * data gradient, 17 permute backward, 18 router weight gradient, 19 aux loss,
+ * 26-29 the shared expert's down data gradient + SwiGLU backward, down weight
+ * gradient, gate/up data gradient, gate/up weight gradient).
  * moe_profile_stop() stops recording. moe_profile_read() waits for the events
  * and returns their number; ms[i] is the time from event i-1 to event i
  * (0 for call starts). moe_debug_launch_count() returns the number of kernels

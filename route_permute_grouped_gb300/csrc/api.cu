@@ -44,6 +44,7 @@ enum StageTag : int {
   STAGE_WGRAD13 = 15, STAGE_ROUTER_DX = 16, STAGE_UNPERMUTE = 17, STAGE_ROUTER_DW = 18, STAGE_AUX = 19,
   STAGE_NV_QUANT = 20, STAGE_NV_GEMM = 21,
   STAGE_MX_QUANT_TOK = 22, STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
+  STAGE_SHARED_DGRAD2 = 26, STAGE_SHARED_WGRAD2 = 27, STAGE_SHARED_DGRAD1 = 28, STAGE_SHARED_WGRAD13 = 29,
 };
 // MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
 // report the first stage whose kernels failed (debugging aid, off by default).
@@ -172,6 +173,8 @@ struct WsLayout {
   size_t logits_raw, topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
   // backward
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part, tmap_slots;
+  // backward of the shared expert: dh13 [T, 2Fs] and its input gradient [T, H] (bf16)
+  size_t dh13_s, dx_s;
   // MXFP8 forward: E4M3 rows of x_perm and a, and their tile-ready scales
   size_t x_q, sfa1, a_q, sfa2;
   // MXFP8 backward: E4M3 rows of dy_perm and dh13 with their scales; the
@@ -258,7 +261,11 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.dL_hl = take(2 * T * 2 * Ep);
     L.dx_r = take(4 * T * H);
     L.dwr_part = take(4 * static_cast<size_t>(router_dw_splits(c.T)) * E * H);
-    L.tmap_slots = take(kTmapSlotBytes * E);  // weight gradients: per-expert A-map copies
+    L.tmap_slots = take(kTmapSlotBytes * (E + 1));  // weight gradients: per-expert A-map copies (+ shared)
+    if (c.F_shared) {
+      L.dh13_s = take(2 * T * 2 * static_cast<size_t>(c.F_shared));
+      L.dx_s = take(2 * T * H);
+    }
   }
   L.total = o;
   return L;
@@ -738,6 +745,7 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
         !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
       return MOE_ERR_INVALID_ARG;
     if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+    if (c.F_shared && (!saved->h13_shared || !saved->a_shared)) return MOE_ERR_INVALID_ARG;
     idx = saved->topk_idx; gate = saved->topk_gate; logits = saved->logits; rows = saved->row_id_map;
     counts = saved->counts; offs = saved->offsets;
     xp = reinterpret_cast<__nv_bfloat16*>(saved->x_perm);
@@ -763,10 +771,14 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
                   c.inter_fp32 != 0, st, s, STAGE_FFN1, STAGE_FFN2));
   void* shared = nullptr;
   if (c.F_shared) {
+    // training: the shared expert's pre-activations and activation are saved
+    // for the backward
     shared = at<void>(ws, L.s_out);
+    __nv_bfloat16* h13s = saved ? reinterpret_cast<__nv_bfloat16*>(saved->h13_shared) : nullptr;
+    __nv_bfloat16* as = saved ? reinterpret_cast<__nv_bfloat16*>(saved->a_shared) : at<__nv_bfloat16>(ws, L.as);
     MOE_TRY(run_ffn(c, c.F_shared, 1, nullptr, c.T, xb, reinterpret_cast<const __nv_bfloat16*>(Ws1),
-                    reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), nullptr,
-                    at<__nv_bfloat16>(ws, L.as), shared, c.inter_fp32 != 0, st, s, STAGE_SHARED1, STAGE_SHARED2));
+                    reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), h13s, as,
+                    shared, c.inter_fp32 != 0, st, s, STAGE_SHARED1, STAGE_SHARED2));
   }
   MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
   stage_done(s, STAGE_COMBINE, 1);
@@ -777,11 +789,90 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
 // MXFP8 training step (the data-gradient GEMMs on MXFP8 operands with the
 // weights in mx; W1, W3, W2 unused); with mx_wgrad the weight gradients too
 // (operands quantised along each expert's tokens).
+// Backward of the shared expert S(x) = (SiLU(x Ws1) * (x Ws3)) Ws2, added
+// ungated to every token (figures & tables page, Fig. 40): its output gradient
+// is dO itself. Four GEMMs over the T tokens as one group:
+//   da_s = dO Ws2^T -> SwiGLU backward with the saved h13_s -> dh13_s  (bf16)
+//   dWs2 = a_s^T dO                                                    (fp32)
+//   dx_s = dh13_s [Ws1 | Ws3]^T                                        (bf16)
+//   dWs1 | dWs3 = x^T dh13_s                                           (fp32)
+// dx_s is added to dx by the permute backward.
+static int shared_bwd(const moe_config& c, const __nv_bfloat16* dO, const __nv_bfloat16* x,
+                      const __nv_bfloat16* Ws1, const __nv_bfloat16* Ws3, const __nv_bfloat16* Ws2,
+                      const moe_fwd_saved* saved, float* dWs1, float* dWs3, float* dWs2, void* ws, const WsLayout& L,
+                      cudaStream_t s) {
+  DevStatus* st = at<DevStatus>(ws, 0);
+  const int Fs = c.F_shared;
+  __nv_bfloat16* dh13s = at<__nv_bfloat16>(ws, L.dh13_s);
+  __nv_bfloat16* dxs = at<__nv_bfloat16>(ws, L.dx_s);
+  uint8_t* slot = at<uint8_t>(ws, L.tmap_slots) + kTmapSlotBytes * c.E;  // after the routed experts' copies
+  {
+    GemmParams p = base_params(c, st);
+    p.F = Fs; p.ngroups = 1; p.offsets = nullptr; p.M_total = c.T;
+    p.n_tiles = (Fs + 255) / 256; p.kb_total = c.H / kBK;
+    p.out0 = dh13s; p.in_aux = saved->h13_shared;
+    CUtensorMap ma, mb, od;
+    MOE_MAP(&ma, dO, c.H, c.T, 2ull * c.H, 64, 128);
+    MOE_MAP(&mb, Ws2, c.H, Fs, 2ull * c.H, 64, 128);  // CTA pairs: 128 rows each
+    if (!make_map_store(&od, dh13s, 2ull * Fs, c.T, false)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_DGRAD2, p, ma, mb, mb, num_sms(), s, &od));
+    stage_done(s, STAGE_SHARED_DGRAD2, 1);
+  }
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = 1; p.offsets = nullptr; p.M_total = c.T;
+    p.wg_M = Fs; p.wg_N = c.H; p.wg_mode = 0;
+    p.tmap_slots = slot;
+    p.m_tiles_fixed = (Fs + 255) / 256; p.n_tiles = (c.H + 255) / 256;
+    p.out0 = dWs2;
+    CUtensorMap ma, mb, mo;
+    MOE_MAP(&ma, saved->a_shared, Fs, c.T, 2ull * Fs, 64, 64);
+    MOE_MAP(&mb, dO, c.H, c.T, 2ull * c.H, 64, 64);
+    if (!make_map_f32_3d(&mo, dWs2, c.H, Fs, 1)) return MOE_ERR_CUDA;
+    const int tiles = p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_tmap_rows(ma, nullptr, 1, slot, s, c.T));
+    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s, &mo, &mo));
+    stage_done(s, STAGE_SHARED_WGRAD2, 2);
+  }
+  {
+    GemmParams p = base_params(c, st);
+    p.F = Fs; p.ngroups = 1; p.offsets = nullptr; p.M_total = c.T;
+    p.n_tiles = (c.H + 255) / 256; p.kb_total = 2 * Fs / kBK;
+    p.out0 = dxs;
+    CUtensorMap ma, m1, m3, od;
+    MOE_MAP(&ma, dh13s, 2ull * Fs, c.T, 4ull * Fs, 64, 128);
+    MOE_MAP(&m1, Ws1, Fs, c.H, 2ull * Fs, 64, 128);  // CTA pairs: 128 rows each
+    MOE_MAP(&m3, Ws3, Fs, c.H, 2ull * Fs, 64, 128);
+    if (!make_map_store(&od, dxs, c.H, c.T, false)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s, &od));
+    stage_done(s, STAGE_SHARED_DGRAD1, 1);
+  }
+  {
+    GemmParams p = base_params(c, st);
+    p.ngroups = 1; p.offsets = nullptr; p.M_total = c.T;
+    p.wg_M = c.H; p.wg_N = 2 * Fs; p.wg_mode = 1;
+    p.tmap_slots = slot;
+    p.m_tiles_fixed = (c.H + 255) / 256; p.n_tiles = (2 * Fs + 255) / 256;
+    p.out0 = dWs1; p.out1 = dWs3;
+    CUtensorMap ma, mb, mo1, mo3;
+    MOE_MAP(&ma, x, c.H, c.T, 2ull * c.H, 64, 64);
+    MOE_MAP(&mb, dh13s, 2ull * Fs, c.T, 4ull * Fs, 64, 64);
+    if (!make_map_f32_3d(&mo1, dWs1, Fs, c.H, 1) || !make_map_f32_3d(&mo3, dWs3, Fs, c.H, 1)) return MOE_ERR_CUDA;
+    const int tiles = p.m_tiles_fixed * p.n_tiles;
+    MOE_CUDA(launch_tmap_rows(ma, nullptr, 1, slot, s, c.T));
+    MOE_CUDA(launch_gemm(KIND_WGRAD, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s, &mo1, &mo3));
+    stage_done(s, STAGE_SHARED_WGRAD13, 2);
+  }
+  return MOE_OK;
+}
+
 static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
                           const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved,
                           void* dx, float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out,
                           void* ws, const WsLayout& L, const moe_mx_bwd_weights* mx, cudaStream_t s,
-                          bool mx_wgrad = false) {
+                          bool mx_wgrad = false, const moe_bf16* Ws1 = nullptr, const moe_bf16* Ws3 = nullptr,
+                          const moe_bf16* Ws2 = nullptr, float* dWs1 = nullptr, float* dWs3 = nullptr,
+                          float* dWs2 = nullptr) {
   // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
   const bool recompute = mx == nullptr && saved->a == nullptr;
   DevStatus* st = at<DevStatus>(ws, 0);
@@ -933,8 +1024,16 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     MOE_CUDA(launch_gemm(KIND_ROUTER_DX, p, ma, mb, mb, tiles < num_sms() ? tiles : num_sms(), s, &od));
     stage_done(s, STAGE_ROUTER_DX, 1);
   }
-  // 8. dx = sum_i dx_perm[row(t,i)] + dx_r
-  MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s));
+  // 7'. the shared expert's backward (its input gradient dx_s in the workspace)
+  const bool shared = c.F_shared != 0 && mx == nullptr;
+  if (shared) {
+    MOE_TRY(shared_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), reinterpret_cast<const __nv_bfloat16*>(x),
+                       reinterpret_cast<const __nv_bfloat16*>(Ws1), reinterpret_cast<const __nv_bfloat16*>(Ws3),
+                       reinterpret_cast<const __nv_bfloat16*>(Ws2), saved, dWs1, dWs3, dWs2, ws, L, s));
+  }
+  // 8. dx = sum_i dx_perm[row(t,i)] + dx_r (+ dx_s)
+  MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s,
+                                shared ? at<__nv_bfloat16>(ws, L.dx_s) : nullptr));
   stage_done(s, STAGE_UNPERMUTE, 1);
   // 9. dW_r = dL^T x, split over K, then reduced in split order
   {
@@ -964,22 +1063,30 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
 }
 
 int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
-                  const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_fwd_saved* saved, void* dx,
-                  float* dW_router, float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws,
-                  size_t ws_bytes, void* stream) {
+                  const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, const moe_bf16* Ws1,
+                  const moe_bf16* Ws3, const moe_bf16* Ws2, const moe_fwd_saved* saved, void* dx, float* dW_router,
+                  float* dW1, float* dW3, float* dW2, float* dWs1, float* dWs3, float* dWs2, float* aux_loss_out,
+                  void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
-  if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
     return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dO) || !aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
       !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
     return MOE_ERR_INVALID_ARG;
   if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
+  if (c.F_shared != 0) {
+    if (!Ws1 || !Ws3 || !Ws2 || !dWs1 || !dWs3 || !dWs2 || !saved->h13_shared || !saved->a_shared)
+      return MOE_ERR_INVALID_ARG;
+    if (!aligned16(Ws1) || !aligned16(Ws3) || !aligned16(Ws2) || !aligned16(dWs1) || !aligned16(dWs3) ||
+        !aligned16(dWs2) || !aligned16(saved->h13_shared) || !aligned16(saved->a_shared))
+      return MOE_ERR_INVALID_ARG;
+  }
   const WsLayout L = ws_layout(c, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return layer_bwd_core(c, dO, x, router_w, W1, W3, W2, saved, dx, dW_router, dW1, dW3, dW2, aux_loss_out, ws, L,
-                        nullptr, static_cast<cudaStream_t>(stream));
+                        nullptr, static_cast<cudaStream_t>(stream), false, Ws1, Ws3, Ws2, dWs1, dWs3, dWs2);
 }
 
 // ---------------------------------------------------------------------------

@@ -830,18 +830,19 @@ static cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& ma, const
 }
 
 // Per-expert copies of the weight gradients' A tensor map: maps[e] (128 bytes)
-// = tmpl with its row extent set to expert e's end row offsets[e + 1],
-// released to the TMA unit (the GEMM launched next acquires each copy before
-// its first use).
+// = tmpl with its row extent set to expert e's end row offsets[e + 1] (one
+// group of `rows` rows when offsets == nullptr), released to the TMA unit (the
+// GEMM launched next acquires each copy before its first use).
 __global__ void tmap_rows_kernel(const __grid_constant__ CUtensorMap tmpl, const int32_t* __restrict__ offsets, int E,
-                                 uint8_t* __restrict__ maps) {
+                                 int rows, uint8_t* __restrict__ maps) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
-  tmap_set_rows(&tmpl, maps + static_cast<size_t>(e) * 128, offsets[e + 1]);
+  tmap_set_rows(&tmpl, maps + static_cast<size_t>(e) * 128, offsets != nullptr ? offsets[e + 1] : rows);
 }
 
-cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st) {
-  tmap_rows_kernel<<<(E + 127) / 128, 128, 0, st>>>(tmpl, offsets, E, maps);
+cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st,
+                             int rows) {
+  tmap_rows_kernel<<<(E + 127) / 128, 128, 0, st>>>(tmpl, offsets, E, rows, maps);
   return cudaGetLastError();
 }
 

@@ -62,8 +62,10 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq = nullptr, uint8_t* msf = nullptr,
                                const int32_t* offsets = nullptr, const int32_t* topk_idx = nullptr);
+// dx = sum_i dx_perm[row(t,i)] + extra (fp32, nullable) + add_bf16 (bf16, nullable)
 cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
-                                 const float* extra, void* dx, cudaStream_t st);
+                                 const float* extra, void* dx, cudaStream_t st,
+                                 const __nv_bfloat16* add_bf16 = nullptr);
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx,
                               const float* gate, const float* dgate, const float* dg_part, int n_part,
                               const int32_t* row_id_map, const int32_t* counts, int Ep, __nv_bfloat16* dL_hl,
@@ -134,8 +136,10 @@ cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16*
                                        const __nv_bfloat16* W2, uint8_t* w13q, uint8_t* sf13, uint8_t* w2q,
                                        uint8_t* sf2, cudaStream_t st);
 // gemm.cu: per-expert copies of a 2-D tensor map with the row extent set to
-// each expert's end row (for the weight gradients' partial k blocks)
-cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st);
+// each expert's end row (for the weight gradients' partial k blocks); one copy
+// ending at `rows` when offsets == nullptr
+cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st,
+                             int rows = 0);
 cudaError_t launch_mx_quantize_tokens(const __nv_bfloat16* X, int R, int C, int ldx, int E, const int32_t* offsets,
                                       uint8_t* XT, uint8_t* sf, int tile_rows, int32_t* pad_off, cudaStream_t st);
 cudaError_t launch_mx_quantize_bwd_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,

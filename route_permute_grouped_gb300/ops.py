@@ -37,7 +37,8 @@ class MoeConfig(ctypes.Structure):
 
 class MoeFwdSaved(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("topk_idx", "topk_gate", "logits", "row_id_map", "counts", "offsets",
-                                        "x_perm", "h13", "a", "y_perm", "aux_partials")]
+                                        "x_perm", "h13", "a", "y_perm", "aux_partials", "h13_shared",
+                                        "a_shared")]
 
 
 _lib = None
@@ -69,8 +70,8 @@ def lib():
         L.moe_unpermute_combine.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp]
         L.moe_layer_fwd.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                     POINTER(MoeFwdSaved), vp, c_size_t, vp]
-        L.moe_layer_bwd.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, POINTER(MoeFwdSaved), vp, vp, vp,
-                                    vp, vp, vp, vp, c_size_t, vp]
+        L.moe_layer_bwd.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, vp, vp, vp, vp, vp, POINTER(MoeFwdSaved),
+                                    vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
         L.moe_get_device_status.argtypes = [vp, vp, POINTER(c_int)]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_status_string.argtypes = [c_int]
@@ -135,7 +136,8 @@ def lib():
 
 
 STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 22: "mx_quantize_tokens", 24: "mx_dgrad_down_swiglu",
-               25: "mx_dgrad_gate_up", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
+               25: "mx_dgrad_gate_up", 26: "shared_dgrad_down_swiglu", 27: "shared_wgrad_down",
+               28: "shared_dgrad_gate_up", 29: "shared_wgrad_gate_up", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
                17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss"}
@@ -311,6 +313,8 @@ def alloc_saved(cfg, device="cuda", recompute=False):
         "a": None if recompute else torch.empty((R, F), dtype=bf, device=device),
         "y_perm": None if recompute else torch.empty((R, H), dtype=_inter_dtype(cfg), device=device),
         "aux_partials": torch.empty((4 * ((T + 127) // 128), E), dtype=f32, device=device) if cfg.aux_coeff else None,
+        "h13_shared": torch.empty((T, 2 * cfg.F_shared), dtype=bf, device=device) if cfg.F_shared else None,
+        "a_shared": torch.empty((T, cfg.F_shared), dtype=bf, device=device) if cfg.F_shared else None,
     }
 
 
@@ -334,7 +338,7 @@ def layer_fwd(cfg, x, router_w, W1, W3, W2, expert_bias=None, logit_bias=None, W
 
 
 def alloc_grads(cfg, device="cuda"):
-    T, H, E, F = cfg.T, cfg.H, cfg.E, cfg.F
+    T, H, E, F, Fs = cfg.T, cfg.H, cfg.E, cfg.F, cfg.F_shared
     f32 = torch.float32
     return {
         "dx": torch.empty((T, H), dtype=_out_dtype(cfg), device=device),
@@ -342,17 +346,24 @@ def alloc_grads(cfg, device="cuda"):
         "dW1": torch.empty((E, H, F), dtype=f32, device=device),
         "dW3": torch.empty((E, H, F), dtype=f32, device=device),
         "dW2": torch.empty((E, F, H), dtype=f32, device=device),
+        "dWs1": torch.empty((H, Fs), dtype=f32, device=device) if Fs else None,
+        "dWs3": torch.empty((H, Fs), dtype=f32, device=device) if Fs else None,
+        "dWs2": torch.empty((Fs, H), dtype=f32, device=device) if Fs else None,
         "aux_loss": torch.zeros(1, dtype=f32, device=device),
     }
 
 
-def layer_bwd(cfg, dO, x, router_w, W1, W3, W2, saved, ws=None, grads=None):
+def layer_bwd(cfg, dO, x, router_w, W1, W3, W2, saved, ws=None, grads=None, Ws=None):
+    """Whole layer backward (``Ws``: the shared expert's weights when
+    cfg.F_shared > 0; its gradients land in grads dWs1, dWs3, dWs2)."""
     dev = x.device
     g = alloc_grads(cfg, dev) if grads is None else grads
     ws = workspace(cfg, True, dev) if ws is None else ws
     sv = _saved_struct(saved)
-    st = lib().moe_layer_bwd(ctypes.byref(cfg), _p(dO), _p(x), _p(router_w), _p(W1), _p(W3), _p(W2),
-                             ctypes.byref(sv), _p(g["dx"]), _p(g["dW_r"]), _p(g["dW1"]), _p(g["dW3"]), _p(g["dW2"]),
+    Ws1, Ws3, Ws2 = Ws if Ws is not None else (None, None, None)
+    st = lib().moe_layer_bwd(ctypes.byref(cfg), _p(dO), _p(x), _p(router_w), _p(W1), _p(W3), _p(W2), _p(Ws1),
+                             _p(Ws3), _p(Ws2), ctypes.byref(sv), _p(g["dx"]), _p(g["dW_r"]), _p(g["dW1"]),
+                             _p(g["dW3"]), _p(g["dW2"]), _p(g.get("dWs1")), _p(g.get("dWs3")), _p(g.get("dWs2")),
                              _p(g["aux_loss"]), _p(ws), ws.numel(), _stream())
     _check(st, "moe_layer_bwd")
     return g

@@ -75,6 +75,16 @@ def test_host_rejects_null_and_small_workspace(lib):
                              None, fake, 16, None) == 3
     misaligned = ctypes.c_void_p(256 + 8)
     assert lib.moe_permute(ctypes.byref(cfg), misaligned, fake, fake, fake, fake, fake, fake, 1 << 30, None) == 1
+    # the backward of a layer with a shared expert needs its weights, its saved
+    # tensors and its gradient buffers
+    sh = ops.make_config(256, 128, 8, 2, 256, F_shared=64)
+    sv = ops.MoeFwdSaved(*([256] * 11 + [None, None]))
+    args = [fake] * 6
+    assert lib.moe_layer_bwd(ctypes.byref(sh), *args, None, None, None, ctypes.byref(sv), fake, fake, fake, fake,
+                             fake, None, None, None, None, fake, 1 << 40, None) == 1
+    sv_full = ops.MoeFwdSaved(*([256] * 13))
+    assert lib.moe_layer_bwd(ctypes.byref(sh), *args, fake, fake, fake, ctypes.byref(sv_full), fake, fake, fake,
+                             fake, fake, fake, fake, fake, None, fake, 16, None) == 3
 
 
 def test_binding_structs_match_the_library(lib):

@@ -254,3 +254,46 @@ def test_full_training_step_modes(mode):
                                ls.aux_coeff, T_total=ls.T)
     dwr_e = part["dlogits"][:, e] @ x[te] + dL_aux[:, e] @ x[others]
     assert_close(f"dW_r[{e}]", f64(g["dW_r"][e]), dwr_e, atol=wgrad_atol(dwr_e))
+
+
+def test_full_training_step_shared_expert():
+    """The DeepSeek-V3-shaped layer (256 experts, sigmoid with group limit,
+    one shared expert F=2048) through forward and backward: the shared
+    expert's weight gradients (they depend on every token, not on routing) on
+    sampled rows, dx on sampled tokens, two routed experts' weight
+    gradients."""
+    ls = synth.shape("dsv3")
+    d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
+    cfg = ops.config_from_shape(ls, out_fp32=True)
+    ws = ops.workspace(cfg, True)
+    saved = ops.alloc_saved(cfg)
+    Ws = (d["Ws1"], d["Ws3"], d["Ws2"])
+    ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"], Ws,
+                  saved=saved, ws=ws)
+    g = ops.layer_bwd(cfg, d["dO"], d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws, Ws=Ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    rt, keep = _check_routing(ls, d, saved)
+    gidx = saved["topk_idx"].cpu().numpy()
+    rng = np.random.default_rng(17)
+    same = [e for e in range(ls.E)
+            if np.array_equal(np.nonzero((gidx == e).any(1))[0], np.nonzero((rt["topk_idx"] == e).any(1))[0])]
+    experts = sorted(rng.choice(same, size=2, replace=False).tolist())
+    tok = _sample(rng, keep, 64)
+    x = f64(d["x"])
+    Wsn = tuple(f64(w) for w in Ws)
+    prec = O.Precision(y_perm=False, shared=False, y=False, dx=False)
+    ref = O.layer_bwd(x, f64(d["router_w"]), _getter(d), None, None, f64(d["dO"]), ls.k, ls.score,
+                      f64(d["expert_bias"]), None, ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=prec,
+                      experts=experts, tokens=tok)
+    assert_close("dx", f64(g["dx"][torch.from_numpy(tok).cuda()]), ref["dx"][tok])
+    for e in experts:
+        for key in ("dW1", "dW3", "dW2"):
+            want = ref[key][e]
+            assert_close(f"{key}[{e}]", f64(g[key][e]), want, atol=wgrad_atol(want))
+    rows_h = np.sort(rng.choice(ls.H, size=256, replace=False))
+    rows_f = np.sort(rng.choice(ls.F_shared, size=128, replace=False))
+    for key, rows in (("dWs1", rows_h), ("dWs3", rows_h), ("dWs2", rows_f)):
+        want = ref[key][rows]
+        assert_close(f"{key} ({len(rows)} rows)", f64(g[key][torch.from_numpy(rows).cuda()]), want,
+                     atol=wgrad_atol(ref[key]))

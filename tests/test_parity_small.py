@@ -212,3 +212,51 @@ def test_layer_bwd(name):
     for key in ("dW1", "dW3", "dW2"):
         report_exact(f"layer_bwd[{name}] {key}", pairs[key][0], np.stack([ex[key][e] for e in range(E)]))
     assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))
+
+
+SHARED_SHAPES = {
+    "dsv3_small": SHAPES["dsv3_small"],
+    "softmax_shared": synth.shape("tiny", T=300, H=192, E=8, k=2, F=128, F_shared=128),
+}
+
+
+@pytest.mark.parametrize("name", list(SHARED_SHAPES))
+def test_layer_bwd_shared_expert(name):
+    """The backward of a layer with a shared expert (figures & tables page,
+    Fig. 40): the shared expert's weight gradients (independent of routing)
+    in full, and the routed gradients and dx where the routing agrees with
+    the oracle's (tokens within the selection tie margin may differ)."""
+    ls = SHARED_SHAPES[name]
+    d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
+    cfg = ops.config_from_shape(ls, out_fp32=True)
+    ws = ops.workspace(cfg, True)
+    saved = ops.alloc_saved(cfg)
+    Ws = (d["Ws1"], d["Ws3"], d["Ws2"])
+    ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"], Ws,
+                  saved=saved, ws=ws)
+    g = ops.layer_bwd(cfg, d["dO"], d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws, Ws=Ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    n = _np(d)
+    Wsn = (n["Ws1"], n["Ws3"], n["Ws2"])
+    prec = O.Precision(y_perm=not ls.inter_fp32, shared=not ls.inter_fp32, y=False, dx=False)
+    ref = O.layer_bwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], n["dO"], ls.k, ls.score, n["expert_bias"],
+                      n["logit_bias"], ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=prec)
+    ex = O.layer_bwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], n["dO"], ls.k, ls.score, n["expert_bias"],
+                     n["logit_bias"], ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=O.EXACT)
+    for key in ("dWs1", "dWs3", "dWs2"):
+        assert_close(key, f64(g[key]), ref[key], atol=wgrad_atol(ref[key]))
+        report_exact(f"layer_bwd_shared[{name}] {key}", f64(g[key]), ex[key])
+    idx = saved["topk_idx"].cpu().numpy()
+    excused = compare_topk(idx, ref["topk_idx"], ref["z"], ls.k)
+    same_tok = np.all(np.sort(idx, 1) == np.sort(ref["topk_idx"], 1), axis=1)
+    assert same_tok.sum() >= ls.T - excused
+    atol_dx = wgrad_atol(ref["dx"]) if name in FLIP_BOUND_SHAPES else MAX_ABS
+    assert_close("dx", f64(g["dx"])[same_tok], ref["dx"][same_tok], atol=atol_dx)
+    report_exact(f"layer_bwd_shared[{name}] dx", f64(g["dx"])[same_tok], ex["dx"][same_tok])
+    same_e = [e for e in range(ls.E)
+              if np.array_equal(np.nonzero((idx == e).any(1))[0], np.nonzero((ref["topk_idx"] == e).any(1))[0])]
+    assert len(same_e) >= ls.E // 2
+    for key in ("dW1", "dW3", "dW2"):
+        want = np.stack([ref[key][e] for e in same_e])
+        assert_close(key, f64(g[key])[same_e], want, atol=wgrad_atol(want))
