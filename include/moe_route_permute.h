@@ -64,7 +64,9 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
  *                alpha * E * sum_e (c_e / (T k)) * mean_t p[t,e] (training);
  *   out_fp32     y (forward) and dx (backward) written as fp32 instead of bf16;
  *   inter_fp32   expert outputs y_perm and the shared-expert output kept in
- *                fp32 instead of bf16;
+ *                fp32 instead of bf16, and in the backward the input
+ *                gradients of the routed rows (dx_perm) and of the shared
+ *                expert likewise;
  *   force_balanced  force-balanced routing (throughput page, Table 11, where
  *                every benchmark configuration uses it): slot i of token t goes
  *                to expert (t k + i) mod E instead of the top-k, so each expert
@@ -490,7 +492,8 @@ unsigned long long moe_debug_launch_count(void);
  * the bf16 operands the backward's GEMMs consumed: which = 0 dy_perm [R,H]
  * (g * dO per routed row), 1 dh13 [R,2F] (dh1 in columns [0,F), dh3 in
  * [F,2F)), 2 a [R,F] (the activation of the memory-saving mode), 3 dx_perm
- * [R,H], all bf16, rows grouped by expert as x_perm. Valid until the next call
+ * [R,H], all bf16 (dx_perm fp32 with inter_fp32), rows grouped by expert as
+ * x_perm. Valid until the next call
  * that uses the workspace. Returns (size_t)-1 for an invalid config, an
  * unknown `which`, or a buffer the workspace does not hold (training == 0 and
  * which != 2). */

@@ -257,14 +257,14 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     L.dgate = take(4 * T * k);
     L.dg_part = take(4 * R * ((F + 255) / 256));  // memory-saving backward: gate-gradient partials
     L.dh13 = take(2 * R * 2 * F);
-    L.dx_perm = take(2 * R * H);
+    L.dx_perm = take(inter * R * H);  // fp32 with inter_fp32 (the bf16 backward)
     L.dL_hl = take(2 * T * 2 * Ep);
     L.dx_r = take(4 * T * H);
     L.dwr_part = take(4 * static_cast<size_t>(router_dw_splits(c.T)) * E * H);
     L.tmap_slots = take(kTmapSlotBytes * (E + 1));  // weight gradients: per-expert A-map copies (+ shared)
     if (c.F_shared) {
       L.dh13_s = take(2 * T * 2 * static_cast<size_t>(c.F_shared));
-      L.dx_s = take(2 * T * H);
+      L.dx_s = take(inter * T * H);
     }
   }
   L.total = o;
@@ -794,7 +794,7 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
 // is dO itself. Four GEMMs over the T tokens as one group:
 //   da_s = dO Ws2^T -> SwiGLU backward with the saved h13_s -> dh13_s  (bf16)
 //   dWs2 = a_s^T dO                                                    (fp32)
-//   dx_s = dh13_s [Ws1 | Ws3]^T                                        (bf16)
+//   dx_s = dh13_s [Ws1 | Ws3]^T                          (bf16, fp32 with inter_fp32)
 //   dWs1 | dWs3 = x^T dh13_s                                           (fp32)
 // dx_s is added to dx by the permute backward.
 static int shared_bwd(const moe_config& c, const __nv_bfloat16* dO, const __nv_bfloat16* x,
@@ -804,7 +804,7 @@ static int shared_bwd(const moe_config& c, const __nv_bfloat16* dO, const __nv_b
   DevStatus* st = at<DevStatus>(ws, 0);
   const int Fs = c.F_shared;
   __nv_bfloat16* dh13s = at<__nv_bfloat16>(ws, L.dh13_s);
-  __nv_bfloat16* dxs = at<__nv_bfloat16>(ws, L.dx_s);
+  void* dxs = at<void>(ws, L.dx_s);
   uint8_t* slot = at<uint8_t>(ws, L.tmap_slots) + kTmapSlotBytes * c.E;  // after the routed experts' copies
   {
     GemmParams p = base_params(c, st);
@@ -839,11 +839,12 @@ static int shared_bwd(const moe_config& c, const __nv_bfloat16* dO, const __nv_b
     p.F = Fs; p.ngroups = 1; p.offsets = nullptr; p.M_total = c.T;
     p.n_tiles = (c.H + 255) / 256; p.kb_total = 2 * Fs / kBK;
     p.out0 = dxs;
+    p.out_fp32 = c.inter_fp32;
     CUtensorMap ma, m1, m3, od;
     MOE_MAP(&ma, dh13s, 2ull * Fs, c.T, 4ull * Fs, 64, 128);
     MOE_MAP(&m1, Ws1, Fs, c.H, 2ull * Fs, 64, 128);  // CTA pairs: 128 rows each
     MOE_MAP(&m3, Ws3, Fs, c.H, 2ull * Fs, 64, 128);
-    if (!make_map_store(&od, dxs, c.H, c.T, false)) return MOE_ERR_CUDA;
+    if (!make_map_store(&od, dxs, c.H, c.T, c.inter_fp32 != 0)) return MOE_ERR_CUDA;
     MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s, &od));
     stage_done(s, STAGE_SHARED_DGRAD1, 1);
   }
@@ -882,6 +883,10 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   float* dgate = at<float>(ws, L.dgate);
   __nv_bfloat16* dh13 = at<__nv_bfloat16>(ws, L.dh13);
   __nv_bfloat16* dx_perm = at<__nv_bfloat16>(ws, L.dx_perm);
+  // the bf16 backward keeps the per-row input gradients in fp32 with
+  // inter_fp32 (layers whose activations reach magnitudes where one bf16
+  // rounding exceeds the accuracy bar); the MXFP8 backward stores them in bf16
+  const bool dxp32 = mx == nullptr && c.inter_fp32 != 0;
   __nv_bfloat16* dL_hl = at<__nv_bfloat16>(ws, L.dL_hl);
   float* dx_r = at<float>(ws, L.dx_r);
   float* dwr_part = at<float>(ws, L.dwr_part);
@@ -972,12 +977,13 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     p.ngroups = c.E; p.offsets = saved->offsets; p.M_total = R;
     p.n_tiles = (c.H + 255) / 256; p.kb_total = 2 * c.F / kBK;
     p.out0 = dx_perm;
+    p.out_fp32 = dxp32;
     CUtensorMap ma, m1, m3;
     MOE_MAP(&ma, dh13, 2ull * c.F, R, 4ull * c.F, 64, 128);
     MOE_MAP(&m1, W1, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 128);  // CTA pairs: 128 rows each
     MOE_MAP(&m3, W3, c.F, static_cast<uint64_t>(c.E) * c.H, 2ull * c.F, 64, 128);
     CUtensorMap od;
-    if (!make_map_store(&od, dx_perm, c.H, R, false)) return MOE_ERR_CUDA;
+    if (!make_map_store(&od, dx_perm, c.H, R, dxp32)) return MOE_ERR_CUDA;
     MOE_CUDA(launch_gemm(KIND_DGRAD1, p, ma, m1, m3, num_sms(), s, &od));
     stage_done(s, STAGE_DGRAD1, 1);
   }
@@ -1033,7 +1039,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   }
   // 8. dx = sum_i dx_perm[row(t,i)] + dx_r (+ dx_s)
   MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s,
-                                shared ? at<__nv_bfloat16>(ws, L.dx_s) : nullptr));
+                                shared ? at<void>(ws, L.dx_s) : nullptr, dxp32));
   stage_done(s, STAGE_UNPERMUTE, 1);
   // 9. dW_r = dL^T x, split over K, then reduced in split order
   {

@@ -38,13 +38,14 @@ constexpr int kWarpsPerBlock = 8;
 
 // y[t] = shared[t] + sum_i g[t,i] * y_perm[row[t,i]]  (fp32, slot order).
 // With gate == nullptr the weights are 1 (permute backward) and `extra` (fp32,
-// nullable) is added instead of `shared`; `add_bf16` (nullable, bf16 [T,H]) is
-// added last (the permute backward: the shared expert's input gradient).
+// nullable) is added instead of `shared`; `add` (nullable, [T,H], the storage
+// type of y_perm) is added last (the permute backward: the shared expert's
+// input gradient).
 template <bool YP32, bool SH32, bool OUT32>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     gather_sum_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ row_id_map,
                       const float* __restrict__ gate, const void* __restrict__ shared, void* __restrict__ y, int T,
-                      int H, int k, const __nv_bfloat16* __restrict__ add_bf16 = nullptr) {
+                      int H, int k, const void* __restrict__ add = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   if (t >= T) return;
@@ -81,9 +82,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         for (int j = 0; j < 8; ++j) acc[j] = fmaf(gs[i], f[j], acc[j]);
       }
     }
-    if (add_bf16 != nullptr) {
+    if (add != nullptr) {
       float f[8];
-      Vec8<false>::load(add_bf16, static_cast<size_t>(t) * H + v * 8, f);
+      Vec8<YP32>::load(add, static_cast<size_t>(t) * H + v * 8, f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] += f[j];
     }
@@ -370,15 +371,19 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
-                                 const float* extra, void* dx, cudaStream_t st, const __nv_bfloat16* add_bf16) {
+cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const int32_t* row_id_map,
+                                 const float* extra, void* dx, cudaStream_t st, const void* add, bool rows_fp32) {
   const int b = blocks_for(c.T);
-  if (c.out_fp32)
-    gather_sum_kernel<false, true, true><<<b, kWarpsPerBlock * 32, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx,
-                                                                             c.T, c.H, c.k, add_bf16);
+  const dim3 g(b), blk(kWarpsPerBlock * 32);
+  if (rows_fp32 && c.out_fp32)
+    gather_sum_kernel<true, true, true><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add);
+  else if (rows_fp32)
+    gather_sum_kernel<true, true, false><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add);
+  else if (c.out_fp32)
+    gather_sum_kernel<false, true, true><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add);
   else
-    gather_sum_kernel<false, true, false><<<b, kWarpsPerBlock * 32, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx,
-                                                                              c.T, c.H, c.k, add_bf16);
+    gather_sum_kernel<false, true, false><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k,
+                                                             add);
   return cudaGetLastError();
 }
 

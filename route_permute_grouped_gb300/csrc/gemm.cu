@@ -742,8 +742,12 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0, 2 * part, 2 * part + 2);
         else if (any_rows) epi_dgrad2(p, ti, tacc, r, false, 4 * part, 4 * part + 4);
       } else if constexpr (KIND == KIND_DGRAD1) {
-        if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
-        else if (any_rows) epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, false, 0);
+        if (full_rows) {
+          if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0);
+          else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
+        } else if (any_rows) {
+          epi_store(ti, tacc, r, 8, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
+        }
       } else if constexpr (KIND == KIND_WGRAD) {
         // 3-D output maps clip rows past M per expert
         epi_wgrad_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);

@@ -161,7 +161,7 @@ struct GemmParams {
   uint8_t* q_out;        // DGRAD2_MX: MXFP8 codes of dh13 [rows, 2F] (scales in sfa_out)
   uint8_t* tmap_slots;   // WGRAD: per-expert copies of the A map (128 bytes each) for the partial k blocks
   int n_part;            // DGRAD2R: 256-column tiles of F
-  int out_fp32;          // FFN2: y_perm fp32
+  int out_fp32;          // FFN2: y_perm fp32; DGRAD1: dx_perm fp32
   // MXFP8 kinds: the activations' scale blocks are read through a tensor map;
   // FFN1_MX writes the down GEMM's A scale blocks to sfa_out; nt_w = n tiles
   // per expert of the weight scales (the weight scales: map msfb)

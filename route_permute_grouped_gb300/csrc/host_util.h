@@ -62,10 +62,11 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq = nullptr, uint8_t* msf = nullptr,
                                const int32_t* offsets = nullptr, const int32_t* topk_idx = nullptr);
-// dx = sum_i dx_perm[row(t,i)] + extra (fp32, nullable) + add_bf16 (bf16, nullable)
-cudaError_t launch_unpermute_sum(const moe_config& c, const __nv_bfloat16* dx_perm, const int32_t* row_id_map,
-                                 const float* extra, void* dx, cudaStream_t st,
-                                 const __nv_bfloat16* add_bf16 = nullptr);
+// dx = sum_i dx_perm[row(t,i)] + extra (fp32, nullable) + add ([T,H], nullable);
+// dx_perm and add are fp32 with rows_fp32, else bf16
+cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const int32_t* row_id_map,
+                                 const float* extra, void* dx, cudaStream_t st, const void* add = nullptr,
+                                 bool rows_fp32 = false);
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx,
                               const float* gate, const float* dgate, const float* dg_part, int n_part,
                               const int32_t* row_id_map, const int32_t* counts, int Ep, __nv_bfloat16* dL_hl,

@@ -169,14 +169,17 @@ WS_TENSORS = {"dy_perm": 0, "dh13": 1, "a": 2, "dx_perm": 3}
 
 
 def workspace_tensor(ws, cfg, training, name):
-    """Test hook: a bf16 view of an intermediate the layer keeps in the
-    workspace (dy_perm [R,H], dh13 [R,2F], a [R,F], dx_perm [R,H])."""
+    """Test hook: a view of an intermediate the layer keeps in the workspace
+    (bf16 dy_perm [R,H], dh13 [R,2F], a [R,F]; dx_perm [R,H], fp32 with
+    inter_fp32)."""
     off = int(lib().moe_debug_workspace_offset(ctypes.byref(cfg), int(training), WS_TENSORS[name]))
     if off == ctypes.c_size_t(-1).value:
         raise MoeError(1, "moe_debug_workspace_offset")
     R = cfg.T * cfg.k
     cols = {"dy_perm": cfg.H, "dh13": 2 * cfg.F, "a": cfg.F, "dx_perm": cfg.H}[name]
-    return ws[off:off + 2 * R * cols].view(torch.bfloat16).view(R, cols)
+    dt = torch.float32 if (name == "dx_perm" and cfg.inter_fp32) else torch.bfloat16
+    nb = R * cols * (4 if dt == torch.float32 else 2)
+    return ws[off:off + nb].view(dt).view(R, cols)
 
 
 def _p(t):

@@ -282,7 +282,7 @@ def test_full_training_step_shared_expert():
     tok = _sample(rng, keep, 64)
     x = f64(d["x"])
     Wsn = tuple(f64(w) for w in Ws)
-    prec = O.Precision(y_perm=False, shared=False, y=False, dx=False)
+    prec = O.Precision(y_perm=False, shared=False, dx_perm=False, y=False, dx=False)
     ref = O.layer_bwd(x, f64(d["router_w"]), _getter(d), None, None, f64(d["dO"]), ls.k, ls.score,
                       f64(d["expert_bias"]), None, ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=prec,
                       experts=experts, tokens=tok)

@@ -239,7 +239,8 @@ def test_layer_bwd_shared_expert(name):
     assert ops.device_status(ws) == 0
     n = _np(d)
     Wsn = (n["Ws1"], n["Ws3"], n["Ws2"])
-    prec = O.Precision(y_perm=not ls.inter_fp32, shared=not ls.inter_fp32, y=False, dx=False)
+    prec = O.Precision(y_perm=not ls.inter_fp32, shared=not ls.inter_fp32, dx_perm=not ls.inter_fp32, y=False,
+                       dx=False)
     ref = O.layer_bwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], n["dO"], ls.k, ls.score, n["expert_bias"],
                       n["logit_bias"], ls.n_groups, ls.topk_groups, ls.gate_scale, Ws=Wsn, prec=prec)
     ex = O.layer_bwd(n["x"], n["router_w"], n["W1"], n["W3"], n["W2"], n["dO"], ls.k, ls.score, n["expert_bias"],
