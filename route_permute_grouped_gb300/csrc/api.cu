@@ -170,7 +170,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t status, lookback;
   // forward intermediates (inference, or standalone grouped FFN without a_save)
-  size_t logits_raw, topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
+  size_t topk_idx, topk_gate, row_id_map, counts, offsets, x_perm, a, y_perm, as, s_out;
   // backward
   size_t dy_perm, dgate, dh13, dx_perm, dL_hl, dx_r, dwr_part, dg_part, tmap_slots;
   // backward of the shared expert: dh13 [T, 2Fs] and its input gradient [T, H] (bf16)
@@ -210,7 +210,6 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
   };
   L.status = take(sizeof(DevStatus));
   L.lookback = take(sizeof(int32_t) * permute_lookback_ints(c.T, c.E));
-  L.logits_raw = take(4 * T * (((E + 31) / 32) * 32));
   L.topk_idx = take(4 * T * k);
   L.topk_gate = take(4 * T * k);
   L.row_id_map = take(4 * T * k);
@@ -334,8 +333,10 @@ static GemmParams base_params(const moe_config& c, DevStatus* st) {
 // stages
 // ---------------------------------------------------------------------------
 static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* w_r, const float* eb,
-                      const float* lb, int32_t* idx, float* gate, float* logits, float* aux, float* raw,
-                      DevStatus* st, cudaStream_t s) {
+                      const float* lb, int32_t* idx, float* gate, float* logits, float* aux, DevStatus* st,
+                      cudaStream_t s) {
+  // logits GEMM with the score, selection and gates in its epilogue: the
+  // 128-row tiles of x against the whole router weight (E <= 256 columns)
   GemmParams p = base_params(c, st);
   p.bn = ((c.E + 31) / 32) * 32;
   p.n_tiles = 1;
@@ -343,15 +344,26 @@ static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bf
   p.M_total = c.T;
   p.kb_total = c.H / kBK;
   p.offsets = nullptr;
-  CUtensorMap ma, mb, mo;
+  const bool softmax = c.score == MOE_SCORE_SOFTMAX;
+  // a group limit ranks groups by sums of scores, which logits do not order
+  const bool grouped = !c.force_balanced && c.n_groups > 1 && c.topk_groups < c.n_groups;
+  p.r_mode = !softmax ? RSEL_SIGMOID : ((eb == nullptr && !grouped) ? RSEL_LOGIT : RSEL_SOFTMAX);
+  p.r_lbias = lb;
+  p.r_ebias = eb;
+  p.r_idx = idx;
+  p.r_gate = gate;
+  p.r_logits = logits;
+  p.r_aux = softmax ? aux : nullptr;
+  p.r_groups = c.n_groups;
+  p.r_topk_groups = c.topk_groups;
+  p.r_force = c.force_balanced;
+  p.r_gate_scale = c.gate_scale;
+  CUtensorMap ma, mb;
   MOE_MAP(&ma, x, c.H, c.T, 2ull * c.H, 64, 128);
   MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn / 2);  // CTA pairs: bn/2 router rows each
-  // raw logits [T, bn] fp32 (columns >= E are zero: router rows past E read as zero)
-  if (!make_map_store(&mo, raw, p.bn, c.T, true)) return MOE_ERR_CUDA;
   const int tiles = (c.T + kBM - 1) / kBM;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  MOE_CUDA(launch_gemm(KIND_ROUTER, p, ma, mb, mb, grid, s, &mo));
-  return cuda_status(launch_router_select(c, raw, p.bn, eb, lb, idx, gate, logits, aux, s));
+  return cuda_status(launch_gemm(KIND_ROUTER, p, ma, mb, mb, grid, s));
 }
 
 // grouped (offsets != nullptr, rows of x_rows grouped by expert) or single-group
@@ -671,9 +683,9 @@ int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* ro
   if (ws_bytes < ws_layout(c, false).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   MOE_TRY(run_router(c, reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(router_w),
                      expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials,
-                     at<float>(ws, ws_layout(c, false).logits_raw), at<DevStatus>(ws, 0),
+                     at<DevStatus>(ws, 0),
                      static_cast<cudaStream_t>(stream)));
-  stage_done(static_cast<cudaStream_t>(stream), STAGE_ROUTER, 2);
+  stage_done(static_cast<cudaStream_t>(stream), STAGE_ROUTER, 1);
   return MOE_OK;
 }
 
@@ -762,8 +774,8 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   prof_mark(s, STAGE_BEGIN);
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
-                     logits, aux, at<float>(ws, L.logits_raw), st, s));
-  stage_done(s, STAGE_ROUTER, 2);
+                     logits, aux, st, s));
+  stage_done(s, STAGE_ROUTER, 1);
   MOE_CUDA(launch_permute(c, xb, idx, xp, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s));
   stage_done(s, STAGE_PERMUTE, 2);
   MOE_TRY(run_ffn(c, c.F, c.E, offs, c.T * c.k, xp, reinterpret_cast<const __nv_bfloat16*>(W1),
@@ -1168,8 +1180,8 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   prof_mark(s, STAGE_BEGIN);
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
-                     nullptr, nullptr, at<float>(ws, L.logits_raw), st, s));
-  stage_done(s, STAGE_ROUTER, 2);
+                     nullptr, nullptr, st, s));
+  stage_done(s, STAGE_ROUTER, 1);
   MOE_CUDA(launch_permute(c, xb, idx, nullptr, rows, counts, offs, at<int32_t>(ws, L.lookback), st, s, x_q, sfa1));
   stage_done(s, STAGE_PERMUTE, 2);
   MOE_TRY(run_ffn_mx(c, offs, c.T * c.k, x_q, sfa1, *w, a_q, sfa2, yp, c.inter_fp32 != 0, st, s));
@@ -1249,8 +1261,8 @@ int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const mo
   prof_mark(s, STAGE_BEGIN);
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, sv.topk_idx,
                      sv.topk_gate, sv.logits, c.aux_coeff != 0.0f ? sv.aux_partials : nullptr,
-                     at<float>(ws, L.logits_raw), st, s));
-  stage_done(s, STAGE_ROUTER, 2);
+                     st, s));
+  stage_done(s, STAGE_ROUTER, 1);
   MOE_CUDA(launch_permute(c, xb, sv.topk_idx, reinterpret_cast<__nv_bfloat16*>(sv.x_perm), sv.row_id_map, sv.counts,
                           sv.offsets, at<int32_t>(ws, L.lookback), st, s, x_q, sfa1));
   stage_done(s, STAGE_PERMUTE, 2);
@@ -1446,8 +1458,8 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   prof_mark(s, STAGE_BEGIN);
   MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, idx, gate,
-                     nullptr, nullptr, at<float>(ws, L.logits_raw), st, s));
-  stage_done(s, STAGE_ROUTER, 2);
+                     nullptr, nullptr, st, s));
+  stage_done(s, STAGE_ROUTER, 1);
   // the routed rows are copies of x's rows: the tensor maximum of x, then the
   // permute quantises as it scatters
   MOE_CUDA(launch_nv_amax(xb, static_cast<long long>(c.T) * c.H, 1, gq, s));

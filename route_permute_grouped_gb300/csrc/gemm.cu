@@ -5,6 +5,7 @@
 #include "epilogue.cuh"
 #include "gemm_tc.cuh"
 #include "host_util.h"
+#include "router_sel.cuh"
 
 namespace moe {
 
@@ -28,6 +29,7 @@ struct SmemLayout {
   // entry): the 128-byte-swizzled tiles and staging boxes need that alignment
   static constexpr int kDynBytes = kBytes;
   static_assert(kDynBytes <= 232448, "shared memory per CTA");
+  static_assert(KIND != KIND_ROUTER || kOutBytes >= kRouterSmemBytes, "router epilogue scratch");
 };
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
@@ -668,8 +670,12 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         else mbar_arrive(tfull + acc);
       }
       __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if constexpr (KIND == KIND_ROUTER) {
+        acc_phase ^= 1u;  // one accumulator: the columns past it hold the epilogue's selection values
+      } else {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
     }
     // drain every MMA issued by this CTA before the TMEM is released
     if (leader) {
@@ -691,6 +697,15 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     Stager st{smem + SL::kOutOff + (warp - 2) * TR::kOutWarpBytes, 0u};
     // pairs: the odd CTA's epilogue frees the even CTA's accumulator slot
     const uint32_t tempty_even = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
+    if constexpr (KIND == KIND_ROUTER) {
+      // the logit and expert biases, zero-padded to 256 experts, for every tile
+      RouterSmem rsm(smem + SL::kOutOff);
+      for (int i = static_cast<int>(threadIdx.x) - 64; i < 256; i += kRouterRows) {
+        rsm.lb[i] = (p.r_lbias != nullptr && i < p.E) ? p.r_lbias[i] : 0.0f;
+        rsm.eb[i] = (p.r_ebias != nullptr && i < p.E) ? p.r_ebias[i] : 0.0f;
+      }
+      named_bar_sync(1, kRouterRows);
+    }
     for (int tile = tile_first; tile < ntiles; tile += tile_step) {
       const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
       // this warp's 32 rows: a full block leaves through TMA boxes; a block
@@ -733,8 +748,12 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0, kNvTileN / 64, alpha);
         else if (any_rows) epi_store(ti, tacc, r, kNvTileN / 32, p.H, p.H, p.out0, false, 0, alpha);
       } else if constexpr (KIND == KIND_ROUTER) {
-        // raw fp32 logits [T, bn]; the map's row extent T clips the tail
-        epi_store_tma<true, false>(ti, tacc, lane, row0, p.bn, st, &mo0);
+        // score, selection, gates (and aux statistics, logits) per token
+        const RouterSmem rsm(smem + SL::kOutOff);
+        const int tid = q * 32 + lane;
+        const uint32_t tz = tmem_base + kRouterZCol + (static_cast<uint32_t>(q * 32) << 16);
+        if (p.k <= 8) router_select_row<8>(p, tacc, tz, ti.m0 + tid, tid, lane, ti.m0 / 32 + q, rsm);
+        else router_select_row<16>(p, tacc, tz, ti.m0 + tid, tid, lane, ti.m0 / 32 + q, rsm);
       } else if constexpr (KIND == KIND_DGRAD2R) {
         if (full_rows) epi_dgrad2r_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
         else if (any_rows) epi_dgrad2(p, ti, tacc, r, true, 0, 8);
@@ -763,8 +782,12 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         if (PAIR && !leader) mbar_arrive_cluster(tempty_even + 8u * acc);
         else mbar_arrive(tempty + acc);
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if constexpr (KIND == KIND_ROUTER) {
+        acc_phase ^= 1u;
+      } else {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
     }
     st.drain(lane);  // this warp's stores are complete
   }

@@ -40,7 +40,7 @@ namespace moe {
 enum GemmKind : int {
   KIND_FFN1 = 0,       // h = x_perm [W1_e | W3_e]  -> a = SiLU(h1) h3 (+ h13 save)
   KIND_FFN2 = 1,       // y_perm = a W2_e
-  KIND_ROUTER = 2,     // raw fp32 router logits L = x W_r^T (selection: router.cu)
+  KIND_ROUTER = 2,     // router: logits L = x W_r^T, score, selection and gates in the epilogue (router_sel.cuh)
   KIND_DGRAD2 = 3,     // da = dy_perm W2_e^T -> SwiGLU backward -> dh13
   KIND_DGRAD1 = 4,     // dx_perm = dh13 [W1_e | W3_e]^T
   KIND_WGRAD = 5,      // dW_e = X_e^T Y_e over the expert's rows (ragged K)
@@ -61,6 +61,11 @@ enum GemmKind : int {
                        // transposed operands, k blocks of 128 padded tokens per expert), fp32 out;
                        // 256 x 192 pair tiles
 };
+
+// Score modes of the router's selection (router_sel.cuh): selection on the
+// logits (softmax, no expert bias, no group limit), on softmax probabilities
+// (+ expert bias), or on sigmoid scores (+ expert bias).
+enum RouterSelMode : int { RSEL_LOGIT = 0, RSEL_SOFTMAX = 1, RSEL_SIGMOID = 2 };
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -170,6 +175,16 @@ struct GemmParams {
   const float* nv_ga;    // GEMM_NV: tensor scale of the activations (one value)
   const float* nv_gb;    // GEMM_NV: tensor scales of the experts' weights [ngroups]
   unsigned* nv_amax;     // FFN1_NV: running max |a| (fp32 bits)
+  // ROUTER: the selection in the epilogue (router_sel.cuh)
+  const float* r_lbias;  // logit bias [E] (added to the logits), nullable
+  const float* r_ebias;  // expert bias [E] (selection only), nullable
+  int32_t* r_idx;        // topk_idx [T, k]
+  float* r_gate;         // topk_gate [T, k]
+  float* r_logits;       // biased logits [T, E], nullable
+  float* r_aux;          // softmax column sums per 32-token slice [4 ceil(T/128), E], nullable
+  int r_mode;            // RouterSelMode
+  int r_groups, r_topk_groups, r_force;
+  float r_gate_scale;
   // status
   DevStatus* status;
   unsigned long long wait_limit_ns;

@@ -36,11 +36,6 @@ cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, co
                         const CUtensorMap& mb1, int grid, cudaStream_t st, const CUtensorMap* out0 = nullptr,
                         const CUtensorMap* out1 = nullptr);
 
-// router.cu: top-k selection from the raw fp32 logits [T, ld] of the router GEMM
-cudaError_t launch_router_select(const moe_config& c, const float* raw, int ld, const float* expert_bias,
-                                 const float* logit_bias, int32_t* topk_idx, float* topk_gate, float* logits_out,
-                                 float* aux_partials, cudaStream_t st);
-
 // permute.cu
 // With x_q != nullptr the permute writes MXFP8 rows (x_q [R, H] codes and the
 // tile-ready scales sfa, mx_sfa_bytes(R, E, H) bytes) instead of bf16 x_perm;
