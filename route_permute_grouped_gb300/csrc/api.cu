@@ -676,6 +676,7 @@ int moe_get_device_status(void* ws, void* stream, int* status_out) {
 int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w, const float* expert_bias,
                     const float* logit_bias, int32_t* topk_idx, float* topk_gate, float* logits_out,
                     float* aux_partials, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_router_topk");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x || !router_w || !topk_idx || !topk_gate || !ws) return MOE_ERR_INVALID_ARG;
@@ -691,6 +692,7 @@ int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* ro
 
 int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_idx, moe_bf16* x_perm,
                 int32_t* row_id_map, int32_t* counts, int32_t* offsets, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_permute");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x || !topk_idx || !x_perm || !row_id_map || !counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
@@ -707,6 +709,7 @@ int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_id
 int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const int32_t* offsets,
                            const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, moe_bf16* h13_save,
                            moe_bf16* a_save, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_grouped_swiglu_ffn");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x_perm || !offsets || !W1 || !W3 || !W2 || !y_perm || !ws) return MOE_ERR_INVALID_ARG;
@@ -724,6 +727,7 @@ int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const 
 
 int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_id_map,
                           const float* topk_gate, const void* shared_out, void* y, void* stream) {
+  NvtxRange nvtx("moe_unpermute_combine");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!y_perm || !row_id_map || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
@@ -737,6 +741,7 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
                   const float* logit_bias, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
                   const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2, void* y, const moe_fwd_saved* saved,
                   void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_fwd");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x || !router_w || !W1 || !W3 || !W2 || !y || !ws) return MOE_ERR_INVALID_ARG;
@@ -1085,6 +1090,7 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
                   const moe_bf16* Ws3, const moe_bf16* Ws2, const moe_fwd_saved* saved, void* dx, float* dW_router,
                   float* dW1, float* dW3, float* dW2, float* dWs1, float* dWs3, float* dWs2, float* aux_loss_out,
                   void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_bwd");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
@@ -1124,6 +1130,7 @@ size_t moe_mx_weight_bytes(const moe_config* cfg, int which) {
 
 int moe_mx_quantize_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
                             const moe_mx_weights* w, void* stream) {
+  NvtxRange nvtx("moe_mx_quantize_weights");
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_mx_shape(*cfg));
   if (!W1 || !W3 || !W2 || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2) return MOE_ERR_INVALID_ARG;
@@ -1138,6 +1145,7 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_bf16* W1, const moe
 }
 
 int moe_mx_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, void* stream) {
+  NvtxRange nvtx("moe_mx_quantize");
   if (!x || !q || !scales || M < 0 || K < kMxBlock || K % kMxBlock != 0) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   MOE_CUDA(launch_mx_quantize_rows(reinterpret_cast<const __nv_bfloat16*>(x), M, K, q, scales,
@@ -1155,6 +1163,7 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
                         const float* expert_bias, const float* logit_bias, const moe_mx_weights* w,
                         const moe_bf16* Ws1, const moe_bf16* Ws3, const moe_bf16* Ws2, void* y, void* ws,
                         size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_fwd_mxfp8");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(check_mx_shape(c));
@@ -1214,6 +1223,7 @@ size_t moe_mx_bwd_weight_bytes(const moe_config* cfg, int which) {
 
 int moe_mx_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
                                 const moe_mx_bwd_weights* w, void* stream) {
+  NvtxRange nvtx("moe_mx_quantize_bwd_weights");
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_mx_shape(*cfg));
   if (!W1 || !W3 || !W2 || !w || !w->w2h || !w->sf2h || !w->w13f || !w->sf13f) return MOE_ERR_INVALID_ARG;
@@ -1241,6 +1251,7 @@ static bool mx_saved_ok(const moe_config& c, const moe_fwd_saved* sv) {
 int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
                               const float* expert_bias, const float* logit_bias, const moe_mx_weights* w, void* y,
                               const moe_fwd_saved* saved, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_fwd_mxfp8_train");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(check_mx_shape(c));
@@ -1277,6 +1288,7 @@ int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf1
                         const moe_mx_bwd_weights* w, const moe_fwd_saved* saved, void* dx, float* dW_router,
                         float* dW1, float* dW3, float* dW2, float* aux_loss_out, int mx_wgrad, void* ws,
                         size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_bwd_mxfp8");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(check_mx_shape(c));
@@ -1312,6 +1324,7 @@ size_t moe_nv_weight_bytes(int E, int K, int N, int which) {
 
 int moe_nv_quantize_weights(int E, int K, int N, const moe_bf16* W, uint8_t* wq, uint8_t* sf, float* g,
                             void* stream) {
+  NvtxRange nvtx("moe_nv_quantize_weights");
   MOE_TRY(check_nv_shape(E, 0, K, N));
   if (!W || !wq || !sf || !g || !aligned16(W) || !aligned16(wq) || !aligned16(sf)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1323,6 +1336,7 @@ int moe_nv_quantize_weights(int E, int K, int N, const moe_bf16* W, uint8_t* wq,
 }
 
 int moe_nv_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, float* g, void* stream) {
+  NvtxRange nvtx("moe_nv_quantize");
   if (!x || !q || !scales || !g || M < 1 || K < kNvBlock || K % kNvBlock != 0) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || (M * K) % 8 != 0) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1360,6 +1374,7 @@ size_t moe_nv_workspace_bytes(int E, long long R, int K) {
 int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, const int32_t* offsets,
                         const uint8_t* wq, const uint8_t* sf, const float* g, moe_bf16* y, void* ws,
                         size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_nv_grouped_gemm");
   MOE_TRY(check_nv_shape(E, R, K, N));
   if (!x || !offsets || !wq || !sf || !g || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(wq) || !aligned16(sf) || !aligned16(y) || !aligned16(ws))
@@ -1401,6 +1416,7 @@ size_t moe_nv_layer_weight_bytes(const moe_config* cfg, int which) {
 
 int moe_nv_quantize_layer_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
                                   const moe_nv_weights* w, void* stream) {
+  NvtxRange nvtx("moe_nv_quantize_layer_weights");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(check_nv_layer_shape(c));
@@ -1432,6 +1448,7 @@ size_t moe_nv_workspace_bytes_layer(const moe_config* cfg) {
 int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
                         const float* expert_bias, const float* logit_bias, const moe_nv_weights* w, void* y, void* ws,
                         size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_fwd_nvfp4");
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(check_nv_layer_shape(c));

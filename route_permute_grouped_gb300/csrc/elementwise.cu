@@ -361,6 +361,7 @@ static int blocks_for(int T) { return (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
 
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_id_map, const float* gate,
                            const void* shared, void* y, cudaStream_t st) {
+  NvtxRange nvtx("moe.combine");
   const int b = blocks_for(c.T);
   const bool yp = c.inter_fp32 != 0, out = c.out_fp32 != 0;
   // the shared output has the storage type of y_perm
@@ -373,6 +374,7 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_
 
 cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const int32_t* row_id_map,
                                  const float* extra, void* dx, cudaStream_t st, const void* add, bool rows_fp32) {
+  NvtxRange nvtx("moe.permute_backward");
   const int b = blocks_for(c.T);
   const dim3 g(b), blk(kWarpsPerBlock * 32);
   if (rows_fp32 && c.out_fp32)
@@ -391,6 +393,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq, uint8_t* msf, const int32_t* offsets,
                                const int32_t* topk_idx) {
+  NvtxRange nvtx("moe.combine_backward");
   const int b = blocks_for(c.T);
   const int th = kWarpsPerBlock * 32;
   if (mq != nullptr) {  // MXFP8 training step: dy_perm quantised as it is written
@@ -421,6 +424,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx, const float* gate,
                               const float* dgate, const float* dg_part, int n_part, const int32_t* row_id_map,
                               const int32_t* counts, int Ep, __nv_bfloat16* dL_hl, cudaStream_t st) {
+  NvtxRange nvtx("moe.router_backward");
   router_bwd_kernel<<<blocks_for(c.T), kWarpsPerBlock * 32, 0, st>>>(logits, topk_idx, gate, dgate, dg_part, n_part,
                                                                      row_id_map, counts, c.T, c.E, c.k, c.score,
                                                                      c.gate_scale, c.aux_coeff, Ep, dL_hl);
@@ -429,11 +433,13 @@ cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const in
 
 cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
                             cudaStream_t st) {
+  NvtxRange nvtx("moe.aux_loss");
   aux_loss_kernel<<<1, 1024, 0, st>>>(aux_partials, 4 * ((c.T + 127) / 128), counts, c.T, c.E, c.k, c.aux_coeff, out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, float* out, cudaStream_t st) {
+  NvtxRange nvtx("moe.router_weight_gradient_reduce");
   const size_t n4 = (n + 3) / 4;
   const int blocks = static_cast<int>((n4 + 255) / 256);
   split_reduce_kernel<<<blocks, 256, 0, st>>>(partials, splits, n, out);

@@ -869,13 +869,36 @@ __global__ void tmap_rows_kernel(const __grid_constant__ CUtensorMap tmpl, const
 
 cudaError_t launch_tmap_rows(const CUtensorMap& tmpl, const int32_t* offsets, int E, uint8_t* maps, cudaStream_t st,
                              int rows) {
+  NvtxRange nvtx("moe.weight_gradient_maps");
   tmap_rows_kernel<<<(E + 127) / 128, 128, 0, st>>>(tmpl, offsets, E, rows, maps);
   return cudaGetLastError();
+}
+
+static const char* gemm_range_name(int kind) {
+  switch (kind) {
+    case KIND_FFN1: return "moe.gemm.gate_up_swiglu";
+    case KIND_FFN2: return "moe.gemm.down";
+    case KIND_ROUTER: return "moe.router";
+    case KIND_DGRAD2: return "moe.gemm.dgrad_down_swiglu_bwd";
+    case KIND_DGRAD2R: return "moe.gemm.dgrad_down_swiglu_bwd_recompute";
+    case KIND_DGRAD1: return "moe.gemm.dgrad_gate_up";
+    case KIND_WGRAD: return "moe.gemm.weight_gradient";
+    case KIND_ROUTER_DX: return "moe.router_dgrad";
+    case KIND_ROUTER_DW: return "moe.router_wgrad";
+    case KIND_FFN1_MX: return "moe.gemm.mxfp8_gate_up_swiglu";
+    case KIND_FFN2_MX: return "moe.gemm.mxfp8_down";
+    case KIND_DGRAD2_MX: return "moe.gemm.mxfp8_dgrad_down_swiglu_bwd";
+    case KIND_WGRAD_MX: return "moe.gemm.mxfp8_weight_gradient";
+    case KIND_GEMM_NV: return "moe.gemm.nvfp4";
+    case KIND_FFN1_NV: return "moe.gemm.nvfp4_gate_up_swiglu";
+    default: return "moe.gemm";
+  }
 }
 
 cudaError_t launch_gemm(int kind, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb0,
                         const CUtensorMap& mb1, int grid, cudaStream_t st, const CUtensorMap* out0,
                         const CUtensorMap* out1) {
+  NvtxRange nvtx(gemm_range_name(kind));
   static const CUtensorMap kNone = {};
   const CUtensorMap& mo0 = out0 ? *out0 : kNone;
   const CUtensorMap& mo1 = out1 ? *out1 : kNone;

@@ -4,12 +4,24 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
 
 #include "gemm_tc.cuh"
 
 namespace moe {
+
+// NVTX range for the lifetime of the object (header-only NVTX3: a no-op unless
+// a profiler attaches). Every entry point opens one named after itself and
+// every kernel launch one named after its stage, so timelines of Nsight tools
+// show the layer's stages and ncu can filter launches by range.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // 2-D bf16 tensor map over a row-major [outer, inner] array with row pitch
 // `row_bytes`, box {box_inner, box_outer}, 128-byte swizzle, zero fill outside

@@ -298,6 +298,7 @@ cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const in
                            __nv_bfloat16* x_perm, int32_t* row_id_map, int32_t* counts, int32_t* offsets,
                            int32_t* lookback, DevStatus* st, cudaStream_t stream, uint8_t* x_q, uint8_t* sfa,
                            const float* nv_g) {
+  NvtxRange nvtx(x_q == nullptr ? "moe.permute" : "moe.permute_quantize");
   const int T = c.T, E = c.E, k = c.k;
   const int nchunks = (T + kChunk - 1) / kChunk;
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);

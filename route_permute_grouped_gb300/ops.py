@@ -343,17 +343,19 @@ def layer_fwd(cfg, x, router_w, W1, W3, W2, expert_bias=None, logit_bias=None, W
 def alloc_grads(cfg, device="cuda"):
     T, H, E, F, Fs = cfg.T, cfg.H, cfg.E, cfg.F, cfg.F_shared
     f32 = torch.float32
-    return {
+    g = {
         "dx": torch.empty((T, H), dtype=_out_dtype(cfg), device=device),
         "dW_r": torch.empty((E, H), dtype=f32, device=device),
         "dW1": torch.empty((E, H, F), dtype=f32, device=device),
         "dW3": torch.empty((E, H, F), dtype=f32, device=device),
         "dW2": torch.empty((E, F, H), dtype=f32, device=device),
-        "dWs1": torch.empty((H, Fs), dtype=f32, device=device) if Fs else None,
-        "dWs3": torch.empty((H, Fs), dtype=f32, device=device) if Fs else None,
-        "dWs2": torch.empty((Fs, H), dtype=f32, device=device) if Fs else None,
         "aux_loss": torch.zeros(1, dtype=f32, device=device),
     }
+    if Fs:  # the shared expert's weight gradients
+        g["dWs1"] = torch.empty((H, Fs), dtype=f32, device=device)
+        g["dWs3"] = torch.empty((H, Fs), dtype=f32, device=device)
+        g["dWs2"] = torch.empty((Fs, H), dtype=f32, device=device)
+    return g
 
 
 def layer_bwd(cfg, dO, x, router_w, W1, W3, W2, saved, ws=None, grads=None, Ws=None):
