@@ -231,6 +231,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 TMEM lanes x 64 consecutive 32-bit columns (shape 16x256b, 8 repeats).
+// Thread t receives, for repeat j (columns 8j .. 8j+7 of the block):
+//   r[4j], r[4j+1]     lane (t / 4),     columns 8j + 2 (t % 4) and + 1;
+//   r[4j+2], r[4j+3]   lane (t / 4) + 8, the same columns
+// (measured on the GB300 with an in-bounds probe before use). taddr carries
+// the first of the 16 lanes in bits 31:16.
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : MOE_TMEM_LD32_REGS(r)
+      : "r"(taddr));
+}
 // 32 consecutive 32-bit columns of this thread's TMEM lane (the store form of
 // tmem_ld32), and the wait for this thread's TMEM stores.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

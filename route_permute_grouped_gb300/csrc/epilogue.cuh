@@ -214,6 +214,54 @@ __device__ __forceinline__ void epi_wgrad_tma(const GemmParams& p, const TileInf
   }
 }
 
+// WGRAD (bf16 operands), fp32 output stored straight from tensor memory: the
+// warp of lane quadrant q reads its 32 rows in two 16-lane halves and 64-column
+// blocks with the 16x256b shape, so each store instruction of the warp writes
+// 32 contiguous bytes (one full sector) in each of 8 rows; no shared-memory
+// staging. Rows past wg_M are skipped (the tile's rows of the next m tile do
+// not exist); a tile with no k blocks (an expert with no rows) stores zeros.
+// Mode 0: out0 = dW [E][wg_M][wg_N]; mode 1: columns [0, wg_N/2) go to out0 and
+// [wg_N/2, wg_N) to out1, each [E][wg_M][wg_N/2].
+__device__ __forceinline__ void st_f32x2(float* dst, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(dst), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const TileInfo& ti, uint32_t tacc_q, int q,
+                                                 int lane) {
+  const bool zero = ti.nkb == 0;
+  const int half_n = p.wg_N / 2;
+  const int ld = p.wg_mode == 1 ? half_n : p.wg_N;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    const int ra = ti.m0 + 32 * q + 16 * h + (lane >> 2);  // rows ra and ra + 8
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      const int n = ti.n0 + 64 * cb;
+      if (n >= p.wg_N) break;  // uniform
+      uint32_t r[32];
+      if (!zero) {
+        tmem_ld16x256b_x8(tacc_q + (static_cast<uint32_t>(16 * h) << 16) + 64 * cb, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0u;
+      }
+      float* out = reinterpret_cast<float*>(p.out0);
+      int col = n;
+      if (p.wg_mode == 1 && n >= half_n) {
+        out = reinterpret_cast<float*>(p.out1);
+        col = n - half_n;
+      }
+      const size_t base_a = (static_cast<size_t>(ti.g) * p.wg_M + ra) * ld + col + 2 * (lane & 3);
+      const size_t base_b = base_a + static_cast<size_t>(8) * ld;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (ra < p.wg_M) st_f32x2(out + base_a + 8 * j, r[4 * j], r[4 * j + 1]);
+        if (ra + 8 < p.wg_M) st_f32x2(out + base_b + 8 * j, r[4 * j + 2], r[4 * j + 3]);
+      }
+    }
+  }
+}
+
 // DGRAD2, rows all inside the expert: dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1).
 // Per 64-column chunk each thread reads its row's 64 values of the saved h1
 // and h3 with vector loads (not through the TMA unit, whose queue holds the

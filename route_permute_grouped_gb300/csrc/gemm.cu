@@ -769,7 +769,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         }
       } else if constexpr (KIND == KIND_WGRAD) {
         // 3-D output maps clip rows past M per expert
-        epi_wgrad_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
+        epi_wgrad_direct(p, ti, tacc, q, lane);
       } else if constexpr (KIND == KIND_ROUTER_DX) {
         // the map's row extent is T: rows past it are clipped
         epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0);

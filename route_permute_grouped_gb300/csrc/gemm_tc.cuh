@@ -131,11 +131,14 @@ struct KindTraits {
   static constexpr int kEpiWarps =
       (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX) ? 12 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
-  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (kPair ? 6 : 4);
+  // WGRAD stores its fp32 output straight from tensor memory (no staging
+  // boxes), which leaves room for a seventh stage
+  static constexpr int kStages =
+      (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (KIND == KIND_WGRAD ? 7 : (kPair ? 6 : 4));
   static constexpr int kOutWarpBytes =
       (KIND == KIND_DGRAD2R) ? 3 * 4096
-      : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX) ? 0
-                                                                                : 2 * 4096;  // staging
+      : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX || KIND == KIND_WGRAD) ? 0
+                                                                                                       : 2 * 4096;  // staging
   // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
