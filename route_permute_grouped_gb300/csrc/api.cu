@@ -335,8 +335,8 @@ static GemmParams base_params(const moe_config& c, DevStatus* st) {
 static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* w_r, const float* eb,
                       const float* lb, int32_t* idx, float* gate, float* logits, float* aux, DevStatus* st,
                       cudaStream_t s) {
-  // logits GEMM with the score, selection and gates in its epilogue: the
-  // 128-row tiles of x against the whole router weight (E <= 256 columns)
+  // logits GEMM with the score, selection and gates in its epilogue: one CTA
+  // per 128-row tile of x against the whole router weight (E <= 256 columns)
   GemmParams p = base_params(c, st);
   p.bn = ((c.E + 31) / 32) * 32;
   p.n_tiles = 1;
@@ -360,7 +360,7 @@ static int run_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bf
   p.r_gate_scale = c.gate_scale;
   CUtensorMap ma, mb;
   MOE_MAP(&ma, x, c.H, c.T, 2ull * c.H, 64, 128);
-  MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn / 2);  // CTA pairs: bn/2 router rows each
+  MOE_MAP(&mb, w_r, c.H, c.E, 2ull * c.H, 64, p.bn);  // rows past E read as zero
   const int tiles = (c.T + kBM - 1) / kBM;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return cuda_status(launch_gemm(KIND_ROUTER, p, ma, mb, mb, grid, s));

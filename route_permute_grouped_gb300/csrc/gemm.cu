@@ -690,7 +690,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant of this warp
-    const int part = (warp - 2) >> 2;  // DGRAD2: which half of the tile's columns
+    const int part = (warp - 2) >> 2;  // DGRAD2, ROUTER: which half of the tile's columns
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -700,11 +700,11 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     if constexpr (KIND == KIND_ROUTER) {
       // the logit and expert biases, zero-padded to 256 experts, for every tile
       RouterSmem rsm(smem + SL::kOutOff);
-      for (int i = static_cast<int>(threadIdx.x) - 64; i < 256; i += kRouterRows) {
+      for (int i = static_cast<int>(threadIdx.x) - 64; i < 256; i += 32 * TR::kEpiWarps) {
         rsm.lb[i] = (p.r_lbias != nullptr && i < p.E) ? p.r_lbias[i] : 0.0f;
         rsm.eb[i] = (p.r_ebias != nullptr && i < p.E) ? p.r_ebias[i] : 0.0f;
       }
-      named_bar_sync(1, kRouterRows);
+      named_bar_sync(1, 32 * TR::kEpiWarps);
     }
     for (int tile = tile_first; tile < ntiles; tile += tile_step) {
       const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
@@ -752,8 +752,11 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         const RouterSmem rsm(smem + SL::kOutOff);
         const int tid = q * 32 + lane;
         const uint32_t tz = tmem_base + kRouterZCol + (static_cast<uint32_t>(q * 32) << 16);
-        if (p.k <= 8) router_select_row<8>(p, tacc, tz, ti.m0 + tid, tid, lane, ti.m0 / 32 + q, rsm);
-        else router_select_row<16>(p, tacc, tz, ti.m0 + tid, tid, lane, ti.m0 / 32 + q, rsm);
+        const int row = ti.m0 + tid, slice = ti.m0 / 32 + q;
+        if (p.r_mode == RSEL_LOGIT) router_select_mode<RSEL_LOGIT>(p, tacc, tz, row, tid, lane, q, part, slice, rsm);
+        else if (p.r_mode == RSEL_SOFTMAX)
+          router_select_mode<RSEL_SOFTMAX>(p, tacc, tz, row, tid, lane, q, part, slice, rsm);
+        else router_select_mode<RSEL_SIGMOID>(p, tacc, tz, row, tid, lane, q, part, slice, rsm);
       } else if constexpr (KIND == KIND_DGRAD2R) {
         if (full_rows) epi_dgrad2r_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
         else if (any_rows) epi_dgrad2(p, ti, tacc, r, true, 0, 8);

@@ -113,8 +113,7 @@ struct KindTraits {
   // and four scale blocks per operand block (2 KB of A, 4 KB of B scales)
   static constexpr bool kNv = (KIND == KIND_GEMM_NV || KIND == KIND_FFN1_NV);
   static constexpr bool kPair = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
-                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R ||
-                                 KIND == KIND_ROUTER || kMx || kNv);
+                                 KIND == KIND_DGRAD1 || KIND == KIND_WGRAD || KIND == KIND_DGRAD2R || kMx || kNv);
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
@@ -128,8 +127,11 @@ struct KindTraits {
   // 128) and its epilogue (SiLU, quantisation) long
   // DGRAD2_MX runs twelve (three per quadrant, 64 of the tile's 192 columns
   // each) for the same reasons
+  // ROUTER runs eight (two per quadrant, each on half of a token's experts):
+  // its selection follows the tile's main loop with nothing to overlap it
   static constexpr int kEpiWarps =
-      (KIND == KIND_DGRAD2) ? 8 : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX) ? 12 : 4;
+      (KIND == KIND_DGRAD2 || KIND == KIND_ROUTER) ? 8
+      : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX) ? 12 : 4;
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
   // WGRAD stores its fp32 output straight from tensor memory (no staging
   // boxes), which leaves room for a seventh stage
@@ -137,9 +139,10 @@ struct KindTraits {
       (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (KIND == KIND_WGRAD ? 7 : (kPair ? 6 : 4));
   static constexpr int kOutWarpBytes =
       (KIND == KIND_DGRAD2R) ? 3 * 4096
+      : (KIND == KIND_ROUTER) ? 4096  // selection scratch, 32 KB in all
       : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX || KIND == KIND_WGRAD) ? 0
                                                                                                        : 2 * 4096;  // staging
-  // the router's B half is bn/2 x 64 (bn <= 256): its stages are packed at
+  // the router's B is bn x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
   static constexpr int kMaxStages = (KIND == KIND_ROUTER) ? 8 : kStages;
   static constexpr bool kGroupedRows = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD2 ||
@@ -423,10 +426,10 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 // wait until every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// router stage stride (a CTA-pair share: 128 x 64 of x and bn/2 x 64 of the
-// router weight; a multiple of 1024 bytes: bn is a multiple of 32) and the
-// number of such stages in the ring
-__host__ __device__ __forceinline__ int router_stage_bytes(int bn) { return kABytes + (bn / 2) * 128; }
+// router stage stride (128 x 64 of x and bn x 64 of the router weight; a
+// multiple of 1024 bytes: bn is a multiple of 32) and the number of such
+// stages in the ring
+__host__ __device__ __forceinline__ int router_stage_bytes(int bn) { return kABytes + bn * 128; }
 __host__ __device__ __forceinline__ int router_stages(int bn) {
   const int n = kRingBytes / router_stage_bytes(bn);
   return n < 8 ? n : 8;
@@ -436,7 +439,7 @@ template <int KIND>
 __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
   if constexpr (KindTraits<KIND>::kNv) return 2 * kNvStageTx;                    // both CTAs' shares
   else if constexpr (KindTraits<KIND>::kMx) return 2 * kMxStageTx;               // both CTAs' shares
-  else if constexpr (KIND == KIND_ROUTER) return 2 * router_stage_bytes(p.bn);   // both CTAs' shares
+  else if constexpr (KIND == KIND_ROUTER) return router_stage_bytes(p.bn);
   else if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
   else return kABytes + kBBytesMax;
 }
