@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--force-balanced", action="store_true", help="force-balanced routing (cyclic assignment)")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
     ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 grouped GEMM timing")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements (Mixtral, Qwen3, skewed Qwen3, DeepSeek-V3 shapes)")
     ap.add_argument("--recompute", action="store_true",
                     help="memory-saving training step (a and y_perm not kept; recomputed in the backward)")
     return ap.parse_args()
@@ -107,6 +109,83 @@ def stage_model(ls, training):
 
 TENSOR_STAGES = {"router", "ffn1_gate_up", "ffn2_down", "shared_gate_up", "shared_down", "dgrad_down_swiglu",
                  "wgrad_down", "dgrad_gate_up", "wgrad_gate_up", "router_dgrad", "router_wgrad"}
+
+
+def kernel_table(stages, model, peaks):
+    """Per stage: average ms per launch, launches, share of the stage time and
+    the fraction of its roofline. A contraction whose arithmetic intensity
+    (FLOP per algorithmic byte) is below the ridge point of the two measured
+    peaks is bounded by HBM. Returns (table, {stage: [total ms, launches]})."""
+    ridge = peaks["bf16_tflops_sustained"] * 1e3 / peaks["hbm_gbs"]  # FLOP per byte
+    agg = {}
+    for name, t in stages:
+        a = agg.setdefault(name, [0.0, 0])
+        a[0] += t
+        a[1] += 1
+    kernels = {}
+    for name, (tot, n) in agg.items():
+        avg = tot / n
+        fl, by = model.get(name, (0, 0))
+        ent = {"ms": round(avg, 4), "launches": n, "share": None}
+        if name in TENSOR_STAGES and fl and (not by or fl / by >= ridge):
+            ach = fl / (avg * 1e-3) / 1e12
+            ent.update(bound="tensor", achieved_tflops=round(ach, 1),
+                       frac=round(ach / peaks["bf16_tflops_sustained"], 4))
+        elif by:
+            ach = by / (avg * 1e-3) / 1e9
+            ent.update(bound="hbm", achieved_gbs=round(ach, 1), frac=round(ach / peaks["hbm_gbs"], 4))
+            if fl:
+                ent["achieved_tflops"] = round(fl / (avg * 1e-3) / 1e12, 1)
+        kernels[name] = ent
+    total_stage = sum(v[0] for v in agg.values())
+    for name in kernels:
+        kernels[name]["share"] = round(agg[name][0] / total_stage, 4) if total_stage else None
+    return kernels, agg
+
+
+_READ_CEILING = {}
+
+
+def read_ceiling_gbs(nbytes, dev, reps=7):
+    """Median rate of one moe_read_ceiling launch over `nbytes` (cold L2: a
+    buffer larger than L2 is written before each launch): the rate at which a
+    single kernel that reads that many bytes can stream them, launch ramp-up and
+    tail included. The router reads x once; its fraction of this ceiling says
+    how close it comes to a plain read of the same size."""
+    import torch
+
+    from route_permute_grouped_gb300 import ops
+
+    nbytes = int(nbytes) // 16 * 16
+    if nbytes in _READ_CEILING:
+        return _READ_CEILING[nbytes]
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    sink = torch.zeros(4096, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(reps + 1):
+        flush.fill_(i & 0xff)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ops.read_ceiling(buf, sink)
+        b.record()
+        torch.cuda.synchronize()
+        if i:
+            ts.append(a.elapsed_time(b))
+    ts.sort()
+    gbs = nbytes / (ts[len(ts) // 2] * 1e-3) / 1e9
+    del buf, flush, sink
+    _READ_CEILING[nbytes] = round(gbs, 1)
+    return _READ_CEILING[nbytes]
+
+
+def add_read_ceiling(kernels, model, dev):
+    """The router's row gains the single-launch read ceiling of its bytes."""
+    if "router" in kernels and kernels["router"].get("achieved_gbs"):
+        rc = read_ceiling_gbs(model["router"][1], dev)
+        kernels["router"]["read_ceiling_gbs"] = rc
+        kernels["router"]["frac_of_read_ceiling"] = round(kernels["router"]["achieved_gbs"] / rc, 4)
 
 
 def load_peaks():
@@ -190,11 +269,11 @@ class Clocks:
 # ----------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline / reference arm)
 # ----------------------------------------------------------------------------
-def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024):
+def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024, max_rows=None):
     """Prepare a bounded sample of the same workload for the fp64 oracle: the
-    rows of `n_experts` seeded experts (forward + backward of those experts) and
-    the router over `n_router_tokens` tokens. Returns (fn, flops, description):
-    fn() runs the sample once."""
+    rows of `n_experts` seeded experts (at most `max_rows` each; forward +
+    backward of those experts) and the router over `n_router_tokens` tokens.
+    Returns (fn, flops, description): fn() runs the sample once."""
     import numpy as np
     import torch
 
@@ -212,6 +291,8 @@ def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024):
     rows_total = 0
     for e in experts:
         tt, ii = np.nonzero(rt["topk_idx"] == e)
+        if max_rows is not None:
+            tt, ii = tt[:max_rows], ii[:max_rows]
         W = (f64(d["W1"][e]), f64(d["W3"][e]), f64(d["W2"][e]))
         xr = x[tt]
         dO = f64(d["dO"][torch.from_numpy(tt).to(d["dO"].device)]) if d["dO"] is not None else None
@@ -220,8 +301,10 @@ def oracle_sample(ls, d, seed, n_experts=4, n_router_tokens=1024):
     xs = x[:n_router_tokens]
     training = ls.aux_coeff > 0 or d["dO"] is not None
 
+    eb = None if d["expert_bias"] is None else f64(d["expert_bias"])
+
     def fn():
-        O.route(xs, w_r, ls.k, ls.score, None, lb, ls.n_groups, ls.topk_groups, ls.gate_scale,
+        O.route(xs, w_r, ls.k, ls.score, eb, lb, ls.n_groups, ls.topk_groups, ls.gate_scale,
                 force_balanced=ls.force_balanced)
         for xr, W, g, dO in data:
             h1, h3, a, out = O.swiglu_expert(xr, *W)
@@ -617,32 +700,8 @@ def run_ours(args, ls, rank, world, local_rank):
 
     # ---------------- per-stage table and roofline of the dominant kernel
     model = stage_model(ls, training)
-    ridge = peaks["bf16_tflops_sustained"] * 1e3 / peaks["hbm_gbs"]  # FLOP per byte
-    agg = {}
-    for name, t in stages:
-        a = agg.setdefault(name, [0.0, 0])
-        a[0] += t
-        a[1] += 1
-    kernels = {}
-    for name, (tot, n) in agg.items():
-        avg = tot / n
-        fl, by = model.get(name, (0, 0))
-        ent = {"ms": round(avg, 4), "launches": n, "share": None}
-        # a contraction whose arithmetic intensity (FLOP per algorithmic byte)
-        # is below the ridge point of the two measured peaks is bounded by HBM
-        if name in TENSOR_STAGES and fl and (not by or fl / by >= ridge):
-            ach = fl / (avg * 1e-3) / 1e12
-            ent.update(bound="tensor", achieved_tflops=round(ach, 1),
-                       frac=round(ach / peaks["bf16_tflops_sustained"], 4))
-        elif by:
-            ach = by / (avg * 1e-3) / 1e9
-            ent.update(bound="hbm", achieved_gbs=round(ach, 1), frac=round(ach / peaks["hbm_gbs"], 4))
-            if fl:
-                ent["achieved_tflops"] = round(fl / (avg * 1e-3) / 1e12, 1)
-        kernels[name] = ent
-    total_stage = sum(v[0] for v in agg.values())
-    for name in kernels:
-        kernels[name]["share"] = round(agg[name][0] / total_stage, 4) if total_stage else None
+    kernels, agg = kernel_table(stages, model, peaks)
+    add_read_ceiling(kernels, model, dev)
     dom = max(agg, key=lambda n: agg[n][0])
     dk = kernels[dom]
     fl, by = model[dom]
@@ -754,6 +813,13 @@ def run_ours(args, ls, rank, world, local_rank):
         cpu = {"value": round(tflops, 6), "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
                "sample": desc + f"; {reps} repetitions, {dt:.2f} s each"}
 
+    # ---------------- every layer configuration, each as its own measurement
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        for name in CONFIG_LINES:
+            configs[name] = measure_config(name, args, rank, world, dev, peaks)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -763,9 +829,97 @@ def run_ours(args, ls, rank, world, local_rank):
             "fwd": {"value": round(fwd_value, 2), "unit": "TFLOPS", "ms_per_step": round(ms_fwd, 4),
                     "tokens_per_s": round(world * ls.T / (ms_fwd * 1e-3), 1)},
             "graph": graph, "mxfp8_fwd": mx, "mxfp8_train": mxt, "nvfp4_grouped_gemm": nv, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clk,
+            "gpu_launches": launches, "clocks": clk, "configs": configs,
         }
         print(json.dumps(line), flush=True)
+
+
+# The layer configurations each measured as a sub-object of the one bench line
+# (their shapes are route_permute_grouped_gb300.synth's): the Mixtral-8x7B-,
+# Qwen3-235B- (balanced and Zipf-skewed) and DeepSeek-V3-shaped forwards and
+# the skewed Qwen3 training step.
+CONFIG_LINES = ("mixtral", "qwen3", "qwen3_skew", "qwen3_skew_train", "dsv3")
+
+
+def measure_config(name, args, rank, world, dev, peaks):
+    """One layer configuration: the step (forward, or forward + backward for a
+    training workload) timed with CUDA events over inputs larger than L2,
+    per-stage roofline fractions, the expert-count histogram summary, and the
+    fp64 oracle on a bounded sample of the same workload (rank 0, N = 1)."""
+    import numpy as np
+    import torch
+
+    from route_permute_grouped_gb300 import ops, synth
+
+    ls = synth.shape(name)
+    training = ls.aux_coeff > 0
+    d = synth.make_layer(ls, seed=args.seed + rank, device=dev, training=training)
+    cfg = ops.config_from_shape(ls)
+    ws = ops.workspace(cfg, training, dev)
+    saved = ops.alloc_saved(cfg, dev) if training else None
+    grads = ops.alloc_grads(cfg, dev) if training else None
+    y = torch.empty((ls.T, ls.H), dtype=torch.float32 if cfg.out_fp32 else torch.bfloat16, device=dev)
+    Ws = (d["Ws1"], d["Ws3"], d["Ws2"]) if ls.F_shared else None
+
+    def step():
+        ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"], Ws,
+                      saved=saved, ws=ws, y=y)
+        if training:
+            ops.layer_bwd(cfg, d["dO"], d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws,
+                          grads=grads, Ws=Ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if ops.device_status(ws) != 0:
+        raise RuntimeError(f"{name}: device status after warm-up")
+    steps = max(3, min(args.steps, 10))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    cap = steps * 40 + 64
+    ops.profile_start(cap)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ops.profile_stop()
+    assert ops.device_status(ws) == 0
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
+    kernels, agg = kernel_table(ops.profile_read(cap), stage_model(ls, training), peaks)
+    add_read_ceiling(kernels, stage_model(ls, training), dev)
+    # the expert-count histogram of this routing (one training-style forward
+    # keeps the counts)
+    sv = saved if saved is not None else ops.alloc_saved(cfg, dev)
+    wsc = ws if training else ops.workspace(cfg, True, dev)
+    ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"], Ws,
+                  saved=sv, ws=wsc)
+    counts = sv["counts"].cpu().numpy()
+    out = {"workload": workload_config(ls)["workload"], "value": round(job_throughput(layer_flops(ls, training), ms,
+                                                                                      world), 2),
+           "unit": "TFLOPS", "ms_per_step": round(ms, 4), "steps": steps,
+           "tokens_per_s": round(world * ls.T / (ms * 1e-3), 1), "dtype": "bf16",
+           "expert_counts": {"min": int(counts.min()), "max": int(counts.max()), "mean": round(float(counts.mean()), 1),
+                             "zero_token_experts": int((counts == 0).sum())},
+           "kernels": kernels}
+    if ls.skew:
+        # the skewed regime's defining property: a dominant expert and
+        # experts that receive no token
+        assert counts.max() > 8 * counts.mean() and (counts == 0).sum() >= 1, out["expert_counts"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fn, fl_s, desc = oracle_sample(ls, d, args.seed, n_experts=2, n_router_tokens=512, max_rows=256)
+        t0 = time.perf_counter()
+        fn()
+        one = time.perf_counter() - t0
+        reps = max(1, min(10, int(3.0 / max(one, 1e-3))))
+        tflops, dt = time_oracle(fn, fl_s, reps)
+        out["cpu_baseline"] = {"value": round(tflops, 6), "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
+                               "sample": desc + f" (at most 256 rows per expert); {reps} repetitions, {dt:.2f} s each"}
+    del d, ws, saved, grads, y, sv, wsc
+    torch.cuda.empty_cache()
+    return out
 
 
 def gemm_source_sha():

@@ -477,7 +477,7 @@ void moe_debug_set_fault(int fault);
  * gradient, 14 gate/up data gradient, 15 gate/up weight gradient, 16 router
  * data gradient, 17 permute backward, 18 router weight gradient, 19 aux loss,
  * 26-29 the shared expert's down data gradient + SwiGLU backward, down weight
- * gradient, gate/up data gradient, gate/up weight gradient).
+ * gradient, gate/up data gradient, gate/up weight gradient; 30 moe_read_ceiling).
  * moe_profile_stop() stops recording. moe_profile_read() waits for the events
  * and returns their number; ms[i] is the time from event i-1 to event i
  * (0 for call starts). moe_debug_launch_count() returns the number of kernels
@@ -486,6 +486,17 @@ void moe_profile_start(int capacity);
 void moe_profile_stop(void);
 int moe_profile_read(int* tags, float* ms, int max);
 unsigned long long moe_debug_launch_count(void);
+
+/* Measurement helper, not a step of the layer: reads the `bytes` bytes at
+ * `buf` (device memory, 16-byte aligned, bytes a multiple of 16) once, with
+ * coalesced 16-byte loads from a grid of four 512-thread CTAs per SM, and
+ * stores nothing unless the data hashes to one fixed word (then one word per
+ * CTA into `sink`, device memory of at least 16 * SMs bytes). One launch timed
+ * alone (cold L2) gives the rate at which a single kernel reading that many
+ * bytes can stream them: the practical ceiling of a read-bound kernel of that
+ * size, below the long-copy peak by the launch's ramp-up and tail. Returns
+ * MOE_ERR_INVALID_ARG for a null or misaligned pointer or size. */
+int moe_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream);
 
 /* Test hook: byte offset, inside a workspace of moe_workspace_bytes(cfg,
  * training), of an intermediate the layer keeps there, so that tests can read

@@ -188,10 +188,12 @@ struct WsLayout {
 };
 
 static int padded_experts(int E) { return ((E + 63) / 64) * 64; }
+// K splits of the router weight gradient (at most 16, at most one per token
+// block); the workspace holds this many partials, a launch may use fewer
 static int router_dw_splits(int T) {
   const int kbh = (T + kBK - 1) / kBK;
   int s = 16;
-  if (2 * kbh < s) s = 2 * kbh;
+  if (kbh < s) s = kbh;
   return s < 1 ? 1 : s;
 }
 
@@ -1058,14 +1060,19 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s,
                                 shared ? at<void>(ws, L.dx_s) : nullptr, dxp32));
   stage_done(s, STAGE_UNPERMUTE, 1);
-  // 9. dW_r = dL^T x, split over K, then reduced in split order
+  // 9. dW_r = dL^T x (each token block: dL's hi and lo parts against one box
+  // of x), split over the token blocks, then reduced in split order; as many
+  // splits as keep one wave of tiles on the SMs
   {
-    const int splits = router_dw_splits(c.T);
-    const int total_kb = 2 * ((c.T + kBK - 1) / kBK);
+    const int m_tiles = (c.E + 127) / 128, n_tiles = (c.H + 255) / 256;
+    int splits = num_sms() / (m_tiles * n_tiles);
+    if (splits > router_dw_splits(c.T)) splits = router_dw_splits(c.T);
+    if (splits < 1) splits = 1;
+    const int total_kb = (c.T + kBK - 1) / kBK;
     GemmParams p = base_params(c, st);
     p.ngroups = splits; p.offsets = nullptr; p.splits = splits;
     p.kb_total = (total_kb + splits - 1) / splits;
-    p.m_tiles_fixed = (c.E + 127) / 128; p.n_tiles = (c.H + 255) / 256; p.Ep = Ep;
+    p.m_tiles_fixed = m_tiles; p.n_tiles = n_tiles; p.Ep = Ep;
     p.out0 = dwr_part;
     CUtensorMap ma, mb;
     MOE_MAP(&ma, dL_hl, 2ull * Ep, c.T, 4ull * Ep, 64, 64);

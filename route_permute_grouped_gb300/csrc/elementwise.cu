@@ -226,6 +226,11 @@ __device__ __forceinline__ float slot_dgate(const float* dgate, const float* dg_
   const float g = gate[slot];
   return g != 0.0f ? s / g : 0.0f;
 }
+// One warp per token; lane j holds experts j, j + 32, ... (NJ of them, NJ * 32
+// >= Ep): every load of the token (its slots, the logits, the counts) is
+// issued before any arithmetic, the softmax of the aux term is formed once in
+// registers, and each lane writes its columns of hi and lo.
+template <int NJ>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                       const float* __restrict__ gate, const float* __restrict__ dgate,
@@ -235,47 +240,61 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   if (t >= T) return;
-  int my_e = -1;
-  float my_dl = 0.0f;
+  const bool aux = (score == MOE_SCORE_SOFTMAX) && aux_coeff != 0.0f;
   const float* Lrow = logits + static_cast<size_t>(t) * E;
+  // loads
+  int my_e = -1;
+  float g_or_L = 0.0f, dg = 0.0f;
+  if (lane < k) {
+    const size_t slot = static_cast<size_t>(t) * k + lane;
+    my_e = topk_idx[slot];
+    dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, slot);
+    g_or_L = score == MOE_SCORE_SOFTMAX ? gate[slot] : Lrow[my_e];
+  }
+  float v[NJ];
+  float cnt[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = (aux && e < E) ? Lrow[e] : -INFINITY;
+    cnt[j] = (aux && e < E) ? static_cast<float>(counts[e]) : 0.0f;
+  }
+  // the gate term of the selected slots
+  float my_dl;
   if (score == MOE_SCORE_SOFTMAX) {
-    float q = 0.0f, dg = 0.0f;
-    if (lane < k) {
-      my_e = topk_idx[static_cast<size_t>(t) * k + lane];
-      q = gate[static_cast<size_t>(t) * k + lane] / gate_scale;
-      dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, static_cast<size_t>(t) * k + lane);
-    }
+    const float q = lane < k ? g_or_L / gate_scale : 0.0f;
     float inner = q * dg;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, o);
     my_dl = gate_scale * q * (dg - inner);
   } else {
-    float s = 0.0f, dg = 0.0f;
-    if (lane < k) {
-      my_e = topk_idx[static_cast<size_t>(t) * k + lane];
-      s = 1.0f / (1.0f + __expf(-Lrow[my_e]));
-      dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, static_cast<size_t>(t) * k + lane);
-    }
-    float S = s, inner = dg * s;
+    const float sg = lane < k ? 1.0f / (1.0f + __expf(-g_or_L)) : 0.0f;
+    float S = sg, inner = dg * sg;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       S += __shfl_xor_sync(0xffffffffu, S, o);
       inner += __shfl_xor_sync(0xffffffffu, inner, o);
     }
     const float ds = (gate_scale / S) * (dg - inner / S);
-    my_dl = ds * s * (1.0f - s);
+    my_dl = ds * sg * (1.0f - sg);
   }
-  const bool aux = (score == MOE_SCORE_SOFTMAX) && aux_coeff != 0.0f;
-  float mx = -INFINITY, sum = 0.0f, pdp = 0.0f;
-  const float dp_scale = aux_coeff * static_cast<float>(E) / (static_cast<float>(T) * k * static_cast<float>(T));
+  // the aux term: p (dp - <p, dp>), dp_e = alpha E counts_e / (T k T)
+  float d[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) d[j] = 0.0f;
   if (aux) {
-    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, Lrow[e]);
+    const float dp_scale = aux_coeff * static_cast<float>(E) / (static_cast<float>(T) * k * static_cast<float>(T));
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) mx = fmaxf(mx, v[j]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    for (int e = lane; e < E; e += 32) {
-      const float ex = __expf(Lrow[e] - mx);
-      sum += ex;
-      pdp += ex * (dp_scale * static_cast<float>(counts[e]));
+    float sum = 0.0f, pdp = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      v[j] = __expf(v[j] - mx);  // 0 past E
+      sum += v[j];
+      pdp += v[j] * (dp_scale * cnt[j]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -283,64 +302,113 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       pdp += __shfl_xor_sync(0xffffffffu, pdp, o);
     }
     pdp /= sum;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const float p = v[j] / sum;
+      d[j] = p * (dp_scale * cnt[j] - pdp);
+    }
+  }
+  // scatter the selected slots' terms to their experts' lanes
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (i < k) {
+      const int e = __shfl_sync(0xffffffffu, my_e, i);
+      const float x = __shfl_sync(0xffffffffu, my_dl, i);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        if (e == lane + 32 * j) d[j] += x;
+    }
   }
   __nv_bfloat16* out = dL_hl + static_cast<size_t>(t) * 2 * Ep;
-  int sel_e[16];
-  float sel_d[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {  // all lanes, before any divergence
-    sel_e[i] = __shfl_sync(0xffffffffu, my_e, i < k ? i : 0);
-    sel_d[i] = __shfl_sync(0xffffffffu, my_dl, i < k ? i : 0);
-  }
-  for (int e = lane; e < Ep; e += 32) {
-    float d = 0.0f;
-    if (e < E) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (i < k && sel_e[i] == e) d += sel_d[i];
-      if (aux) {
-        const float p = __expf(Lrow[e] - mx) / sum;
-        d += p * (dp_scale * static_cast<float>(counts[e]) - pdp);
-      }
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    if (e < Ep) {
+      const float dd = e < E ? d[j] : 0.0f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(dd);
+      out[e] = hi;
+      out[Ep + e] = __float2bfloat16_rn(dd - __bfloat162float(hi));
     }
-    const __nv_bfloat16 hi = __float2bfloat16_rn(d);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(d - __bfloat162float(hi));
-    out[e] = hi;
-    out[Ep + e] = lo;
   }
 }
 
 // aux loss value: alpha * E * sum_e (c_e / (T k)) * (sum_rows partial[row][e] / T).
-// One block of 1024 threads: thread (part, e) sums every fourth row of column
-// e (coalesced over e), the four parts and then the experts are combined in a
-// fixed order.
+// One block of 1024 threads. With E a multiple of 4 (rows 16-byte aligned),
+// thread (g, c) (c fastest over the E/4 float4 columns, RG = the largest power
+// of two <= 1024 / (E/4) row groups) adds rows g, g + RG, ... of its four
+// columns; the loads of a thread are independent of one another (unrolled, in
+// flight together), the row groups are combined by a halving tree in shared
+// memory. Otherwise thread (g, e) adds rows of one column in four independent
+// accumulators. Then the experts are combined by a halving tree: a fixed order
+// throughout.
 __global__ void __launch_bounds__(1024) aux_loss_kernel(const float* __restrict__ partials, int nrows,
                                                         const int32_t* __restrict__ counts, int T, int E, int k,
                                                         float aux_coeff, float* __restrict__ out) {
-  __shared__ float s_part[4][256];
+  __shared__ float s_part[4096];
   __shared__ float s[256];
-  const int e = threadIdx.x & 255, part = threadIdx.x >> 8;
-  float P = 0.0f;
-  if (e < E) {
-#pragma unroll 8
-    for (int i = part; i < nrows; i += 4) P += partials[static_cast<size_t>(i) * E + e];
-  }
-  s_part[part][e] = P;
-  __syncthreads();
-  if (threadIdx.x < 256) {
-    float v = 0.0f;
-    if (e < E) {
-      const float Pe = (s_part[0][e] + s_part[1][e]) + (s_part[2][e] + s_part[3][e]);
-      v = (static_cast<float>(counts[e]) / (static_cast<float>(T) * k)) * (Pe / static_cast<float>(T));
+  const int tid = static_cast<int>(threadIdx.x);
+  if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(partials) & 15) == 0) {
+    const int C4 = E >> 2;
+    int RG = 1;
+    while (2 * RG * C4 <= 1024) RG *= 2;
+    const int c = tid % C4, g = tid / C4;
+    if (g < RG) {
+      const float4* p4 = reinterpret_cast<const float4*>(partials);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+      for (int i = g; i < nrows; i += RG) {
+        const float4 v = __ldg(p4 + static_cast<size_t>(i) * C4 + c);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      float* dst = s_part + g * E + 4 * c;
+      dst[0] = acc.x; dst[1] = acc.y; dst[2] = acc.z; dst[3] = acc.w;
     }
-    s[e] = v;
+    __syncthreads();
+    for (int st = RG / 2; st >= 1; st >>= 1) {
+      for (int i = tid; i < st * E; i += 1024) s_part[i] += s_part[i + st * E];
+      __syncthreads();
+    }
+  } else {
+    const int Eb = (E + 31) & ~31;
+    const int G = 1024 / Eb;
+    const int e = tid % Eb, g = tid / Eb;
+    float P = 0.0f;
+    if (g < G && e < E) {
+      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+      int i = g;
+      for (; i + 3 * G < nrows; i += 4 * G) {
+        a0 += partials[static_cast<size_t>(i) * E + e];
+        a1 += partials[static_cast<size_t>(i + G) * E + e];
+        a2 += partials[static_cast<size_t>(i + 2 * G) * E + e];
+        a3 += partials[static_cast<size_t>(i + 3 * G) * E + e];
+      }
+      for (; i < nrows; i += G) a0 += partials[static_cast<size_t>(i) * E + e];
+      P = (a0 + a1) + (a2 + a3);
+    }
+    s_part[tid] = P;
+    __syncthreads();
+    if (tid < E) {
+      float Pe = 0.0f;
+      for (int gg = 0; gg < G; ++gg) Pe += s_part[gg * Eb + tid];
+      s_part[2048 + tid] = Pe;
+    }
+    __syncthreads();
+    if (tid < E) s_part[tid] = s_part[2048 + tid];
+    __syncthreads();
+  }
+  // s_part[e] = sum over the rows of column e
+  if (tid < 256) {
+    float v = 0.0f;
+    if (tid < E)
+      v = (static_cast<float>(counts[tid]) / (static_cast<float>(T) * k)) * (s_part[tid] / static_cast<float>(T));
+    s[tid] = v;
   }
   __syncthreads();
   for (int d = 128; d > 0; d >>= 1) {
-    if (threadIdx.x < d) s[threadIdx.x] += s[threadIdx.x + d];
+    if (tid < d) s[tid] += s[tid + d];
     __syncthreads();
   }
-  if (threadIdx.x == 0) *out = aux_coeff * static_cast<float>(E) * s[0];
+  if (tid == 0) *out = aux_coeff * static_cast<float>(E) * s[0];
 }
 
 // out[i] = sum_s partials[s][i], s in order.
@@ -425,9 +493,15 @@ cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const in
                               const float* dgate, const float* dg_part, int n_part, const int32_t* row_id_map,
                               const int32_t* counts, int Ep, __nv_bfloat16* dL_hl, cudaStream_t st) {
   NvtxRange nvtx("moe.router_backward");
-  router_bwd_kernel<<<blocks_for(c.T), kWarpsPerBlock * 32, 0, st>>>(logits, topk_idx, gate, dgate, dg_part, n_part,
-                                                                     row_id_map, counts, c.T, c.E, c.k, c.score,
-                                                                     c.gate_scale, c.aux_coeff, Ep, dL_hl);
+  const dim3 g(blocks_for(c.T)), b(kWarpsPerBlock * 32);
+#define MOE_ROUTER_BWD(NJ)                                                                                  \
+  router_bwd_kernel<NJ><<<g, b, 0, st>>>(logits, topk_idx, gate, dgate, dg_part, n_part, row_id_map, counts, \
+                                         c.T, c.E, c.k, c.score, c.gate_scale, c.aux_coeff, Ep, dL_hl)
+  // Ep (a multiple of 64, <= 256) columns over 32 lanes
+  if (Ep <= 64) MOE_ROUTER_BWD(2);
+  else if (Ep <= 128) MOE_ROUTER_BWD(4);
+  else MOE_ROUTER_BWD(8);
+#undef MOE_ROUTER_BWD
   return cudaGetLastError();
 }
 
@@ -447,3 +521,36 @@ cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, flo
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Read ceiling (measurement helper): a grid-stride pass of 16-byte loads over
+// a buffer, four loads in flight per thread, nothing stored unless the data
+// hashes to a fixed word (so the loads cannot be dropped).
+// ---------------------------------------------------------------------------
+namespace moe {
+__global__ void __launch_bounds__(512) read_ceiling_kernel(const uint4* __restrict__ p, size_t n16, unsigned* sink) {
+  unsigned acc = 0;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldg(p + i), b = __ldg(p + i + stride), c = __ldg(p + i + 2 * stride),
+                d = __ldg(p + i + 3 * stride);
+    acc += a.x ^ b.y ^ c.z ^ d.w;
+  }
+  for (; i < n16; i += stride) acc += __ldg(p + i).x;
+  if (acc == 0x9e3779b9u) sink[blockIdx.x] = acc;
+}
+}  // namespace moe
+
+extern "C" int moe_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream) {
+  using namespace moe;
+  if (buf == nullptr || sink == nullptr || (reinterpret_cast<uintptr_t>(buf) & 15) != 0 || (bytes & 15) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (bytes == 0) return MOE_OK;
+  NvtxRange nvtx("moe.read_ceiling");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  read_ceiling_kernel<<<4 * num_sms(), 512, 0, st>>>(static_cast<const uint4*>(buf), bytes / 16, sink);
+  const int rc = status_from_cuda(cudaGetLastError());
+  record_stage(st, 30, 1);
+  return rc;
+}

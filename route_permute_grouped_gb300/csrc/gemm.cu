@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
           // different k block so the CTAs do not all hit the same L2 lines
           // at once (the sum runs over all k blocks either way)
           const int kbl = (KIND == KIND_ROUTER) ? (kb + static_cast<int>(blockIdx.x) * 5) % ti.nkb : kb;
-          issue_loads<KIND>(p, ti, kbl, sA, sA + kABytes, full + stage, &ma, &mb0, &mb1);
+          issue_loads<KIND>(p, ti, kbl, sA, sA + TR::kBOff, full + stage, &ma, &mb0, &mb1);
           issued_phase[stage] = static_cast<int>(phase);
           if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     // 16-deep k step (K-major: 32 bytes; MN-major: 16 rows of 128 bytes)
     const uint32_t d_hi = sdesc_hi_sw128(1024);
     const uint32_t a_lo0 = sdesc_lo(smem_u32(smem), TR::A_MN ? 8192u : 16u);
-    const uint32_t b_lo0 = sdesc_lo(smem_u32(smem) + kABytes, TR::B_MN ? 8192u : 16u);
+    const uint32_t b_lo0 = sdesc_lo(smem_u32(smem) + TR::kBOff, TR::B_MN ? 8192u : 16u);
     constexpr uint32_t kAStep = TR::A_MN ? (2048u >> 4) : (32u >> 4);
     constexpr uint32_t kBStep = TR::B_MN ? (2048u >> 4) : (32u >> 4);
     const uint32_t stage_lo = static_cast<uint32_t>(SBYTES) >> 4;
@@ -656,6 +656,12 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
               umma2_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
             else
               umma_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (KIND == KIND_ROUTER_DW) {
+            // the lo part of dL against the same box of x
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16_w(d_tmem, a_lo + (kABytes >> 4) + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, 1u);
           }
           if constexpr (PAIR) umma2_commit_mc(empty + stage, 3);  // frees the stage in both CTAs
           else umma_commit(empty + stage);

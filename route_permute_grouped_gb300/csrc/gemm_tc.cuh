@@ -117,8 +117,14 @@ struct KindTraits {
   static constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of one (pair) tile
   // stage ring of kRingBytes: single-CTA stages of kStageBytes; pair stages of
   // 16 KB of A + 16 KB of B
-  static constexpr int kStageBytesK =
-      kNv ? kNvStageBytes : kMx ? kMxStageBytes : kPair ? (kABytes + kBBytesMax / 2) : kStageBytes;
+  // ROUTER_DW: both bf16 parts of dL (hi, lo) with one box of x, so x is
+  // read once for the two products
+  static constexpr int kStageBytesK = kNv ? kNvStageBytes
+                                      : kMx ? kMxStageBytes
+                                      : kPair ? (kABytes + kBBytesMax / 2)
+                                      : (KIND == KIND_ROUTER_DW) ? (2 * kABytes + kBBytesMax) : kStageBytes;
+  // offset of B in a stage
+  static constexpr int kBOff = (KIND == KIND_ROUTER_DW) ? 2 * kABytes : kABytes;
   // DGRAD2 runs eight epilogue warps (two per TMEM lane quadrant, each taking
   // half of the tile's columns) to hide the latency of its loads of the saved
   // pre-activations; it and DGRAD2R (third staging box) give up one stage
@@ -135,8 +141,11 @@ struct KindTraits {
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
   // WGRAD stores its fp32 output straight from tensor memory (no staging
   // boxes), which leaves room for a seventh stage
-  static constexpr int kStages =
-      (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5 : (KIND == KIND_WGRAD ? 7 : (kPair ? 6 : 4));
+  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5
+                                 : (KIND == KIND_WGRAD)                            ? 7
+                                 : kPair                                           ? 6
+                                 : (KIND == KIND_ROUTER_DW)                        ? 3
+                                                                                   : 4;
   static constexpr int kOutWarpBytes =
       (KIND == KIND_DGRAD2R) ? 3 * 4096
       : (KIND == KIND_ROUTER) ? 4096  // selection scratch, 32 KB in all
@@ -249,10 +258,10 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     ti.nkb = (s_off[lo + 1] - s_off[lo]) / kMxKB;
     ti.krow0 = 0;
     ti.krow_end = 0;
-  } else {  // ROUTER_DW: group = split
+  } else {  // ROUTER_DW: group = split of the token blocks
     ti.m0 = mb * kBM;
     ti.m_end = p.E;
-    int total = 2 * ((p.T + kBK - 1) / kBK);
+    int total = (p.T + kBK - 1) / kBK;
     int per = p.kb_total;
     ti.kb0 = lo * per;
     ti.nkb = min(per, total - ti.kb0);
@@ -326,12 +335,6 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
     return;
   }
   const int kk = kb * kBK;
-  if constexpr (KIND == KIND_ROUTER) {
-    // 128 token rows of x; router-weight rows rank * bn/2 .. (box of bn/2 rows)
-    tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
-    tma_load_2d_pair(sB, mb0, bar_cluster, kk, rank * (p.bn / 2));
-    return;
-  }
   if constexpr (KIND == KIND_WGRAD) {
     const int r = ti.krow0 + kk;
     const int n = ti.n0 + 128 * rank;
@@ -380,8 +383,11 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
 #pragma unroll
     for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, brow);
   } else if constexpr (KIND == KIND_ROUTER) {
-    tma_load_2d(sA, ma, bar, kk, ti.m0);
-    tma_load_2d(sB, mb0, bar, kk, 0);
+    // x is read once here: its lines go first when L2 needs room, so that
+    // streaming it does not push other kernels' data (or their dirty lines)
+    // out; the router weight, read by every CTA, stays
+    tma_load_2d_hint(sA, ma, bar, kk, ti.m0, l2_policy_evict_first());
+    tma_load_2d_hint(sB, mb0, bar, kk, 0, l2_policy_evict_last());
   } else if constexpr (KIND == KIND_DGRAD2) {
     tma_load_2d(sA, ma, bar, kk, ti.m0);
     tma_load_2d(sB, mb0, bar, kk, ti.g * p.F + ti.n0);
@@ -400,16 +406,29 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     const int erow = kk % p.Ep;
 #pragma unroll
     for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, erow);
-  } else {  // ROUTER_DW
-    const int half = (p.T + kBK - 1) / kBK;
-    const int kbg = ti.kb0 + kb;
-    const int is_lo = kbg >= half ? 1 : 0;
-    const int trow = (kbg - is_lo * half) * kBK;
-    const int col = ti.m0 + is_lo * p.Ep;
-    tma_load_2d(sA, ma, bar, col, trow);
-    tma_load_2d(sA + 8192, ma, bar, col + 64, trow);
+  } else {  // ROUTER_DW: token block kb0 + kb; dL hi at sA, lo at sA + kABytes
+    const int trow = (ti.kb0 + kb) * kBK;
+    const int col = ti.m0;
+    if (p.Ep <= kBM) {
+      // one tile of experts: each box of x is read by one CTA; x goes first
+      // when L2 needs room, dL (re-read by every tile of H) stays
+      const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, trow);
+      for (int part = 0; part < 2; ++part) {
+        tma_load_2d_hint(sA + part * kABytes, ma, bar, col + part * p.Ep, trow, keep);
+        tma_load_2d_hint(sA + part * kABytes + 8192, ma, bar, col + part * p.Ep + 64, trow, keep);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tma_load_2d_hint(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, trow, stream);
+    } else {
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        tma_load_2d(sA + part * kABytes, ma, bar, col + part * p.Ep, trow);
+        tma_load_2d(sA + part * kABytes + 8192, ma, bar, col + part * p.Ep + 64, trow);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mb0, bar, ti.n0 + 64 * j, trow);
+    }
   }
 }
 
@@ -441,7 +460,7 @@ __device__ __forceinline__ uint32_t stage_tx_bytes(const GemmParams& p) {
   else if constexpr (KindTraits<KIND>::kMx) return 2 * kMxStageTx;               // both CTAs' shares
   else if constexpr (KIND == KIND_ROUTER) return router_stage_bytes(p.bn);
   else if constexpr (KindTraits<KIND>::kPair) return 2 * KindTraits<KIND>::kStageBytesK;  // both CTAs' shares
-  else return kABytes + kBBytesMax;
+  else return KindTraits<KIND>::kStageBytesK;
 }
 
 }  // namespace moe

@@ -140,3 +140,15 @@ def test_low_precision_entry_points_check_on_the_host(lib):
                                            null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
     assert lib.moe_mx_quantize(null, 10, 33, null, null, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_nv_quantize(null, 10, 32, null, null, null, null) == ops.MOE_ERR_INVALID_ARG
+
+
+def test_read_ceiling_checks_on_the_host(lib):
+    # the measurement helper rejects null and misaligned arguments before any
+    # CUDA work
+    null = ctypes.c_void_p()
+    some = ctypes.c_void_p(4096)
+    assert lib.moe_read_ceiling(null, 1024, some, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_read_ceiling(some, 1024, null, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_read_ceiling(ctypes.c_void_p(4100), 1024, some, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_read_ceiling(some, 1000, some, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_read_ceiling(some, 0, some, null) == ops.MOE_OK
