@@ -24,7 +24,11 @@ struct SmemLayout {
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;  // u32 TMEM base, int abort flag
   static constexpr int kCumOff = kTmemSlot + 16;
   static constexpr int kOffOff = kCumOff + (kMaxGroups + 1) * 4;
-  static constexpr int kBytes = kOffOff + (kMaxGroups + 1) * 4;
+  // WGRAD: the experts in descending order of their rows (one byte each)
+  static constexpr int kOrderOff = kOffOff + (kMaxGroups + 1) * 4;
+  // WGRAD: 1 when the tiles are walked long / short alternately (skewed rows)
+  static constexpr int kSkewOff = kOrderOff + kMaxGroups;
+  static constexpr int kBytes = kSkewOff + 4;
   // the dynamic shared memory starts 1024-byte aligned (checked at kernel
   // entry): the 128-byte-swizzled tiles and staging boxes need that alignment
   static constexpr int kDynBytes = kBytes;
@@ -333,6 +337,37 @@ __device__ __forceinline__ void epi_dgrad2(const GemmParams& p, const TileInfo& 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// Order in which a CTA (pair) walks the tiles. Weight gradients: every expert
+// has the same number of tiles, but a tile's k blocks are the expert's rows,
+// so with skewed routing a hot expert's tiles are long (tensor-bound) and a
+// cold expert's short (bound by its fp32 output). When the routing is skewed
+// (`skew`: the largest expert above four times the mean rows), position
+// v = k P + c of CTA c (P CTAs, k-th tile of each) takes the next tile from the
+// front of the experts sorted by rows (descending) when k + c is even and from
+// the back otherwise, so every CTA alternates long and short tiles and at any
+// moment about half the CTAs compute while the others write. A bijection onto
+// [0, ntiles): the front and back take disjoint ranges. Balanced routing keeps
+// the expert-major order (one expert's operands hot in L2 at a time, measured
+// faster there); other kinds: as is.
+template <int KIND>
+__device__ __forceinline__ int schedule_tile(int v, int P, int ntiles, const GemmParams& p, const uint8_t* s_order,
+                                             int skew) {
+  if constexpr (KIND == KIND_WGRAD) {
+    if (!skew) return v;
+    const int k = v / P, c = v - k * P;
+    // front positions before v: rows 0..k-1 hold ceil(P/2) (k' even) or
+    // floor(P/2) (k' odd) each; row k those c' < c with c' + k even
+    const int front_rows = ((k + 1) / 2) * ((P + 1) / 2) + (k / 2) * (P / 2);
+    const int front_before = front_rows + ((k & 1) == 0 ? (c + 1) / 2 : c / 2);
+    const int j = ((k + c) & 1) == 0 ? front_before : ntiles - 1 - (v - front_before);
+    const int tpg = p.m_tiles_fixed * p.n_tiles;
+    const int e = j / tpg;
+    return static_cast<int>(s_order[e]) * tpg + (j - e * tpg);
+  } else {
+    return v;
+  }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap ma,
@@ -368,6 +403,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SL::kTmemSlot + 4);
   int* s_cum = reinterpret_cast<int*>(smem + SL::kCumOff);
   int* s_off = reinterpret_cast<int*>(smem + SL::kOffOff);
+  uint8_t* s_order = smem + SL::kOrderOff;
+  int* s_skew = reinterpret_cast<int*>(smem + SL::kSkewOff);
 
   const int warp = warp_id(), lane = lane_id();
 
@@ -436,6 +473,25 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       if (g <= ng) s_cum[g] = run;
       run += cnt[i];
     }
+    if constexpr (KIND == KIND_WGRAD) {
+      // rank of each expert by its rows (descending, lower index first), and
+      // whether the largest expert has more than four times the mean rows
+      __syncwarp();
+      int mx = 0;
+      for (int g = lane; g < ng; g += 32) {
+        const int rg = s_off[g + 1] - s_off[g];
+        mx = max(mx, rg);
+        int rank = 0;
+        for (int h = 0; h < ng; ++h) {
+          const int rh = s_off[h + 1] - s_off[h];
+          rank += (rh > rg || (rh == rg && h < g)) ? 1 : 0;
+        }
+        s_order[rank] = static_cast<uint8_t>(g);
+      }
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+      if (lane == 0) *s_skew = (static_cast<long long>(mx) * ng > 4ll * (s_off[ng] - s_off[0])) ? 1 : 0;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -444,6 +500,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int ntiles = s_cum[p.ngroups];
+  const int skew = KIND == KIND_WGRAD ? *s_skew : 0;
   const uint64_t lim = p.wait_limit_ns;
 
   if (warp == 0) {
@@ -459,7 +516,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       for (int s = 0; s < NSTMAX; ++s) issued_phase[s] = -1;
       bool ok = true;
       for (int tile = tile_first; tile < ntiles && ok; tile += tile_step) {
-        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
+        const int t = schedule_tile<KIND>(tile, tile_step, ntiles, p, s_order, skew);
+        const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, t, rank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, s_abort, lim, p.status, 1)) { ok = false; break; }
           if constexpr (PAIR) {
@@ -541,7 +599,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     // pairs: only the even CTA issues MMAs; its peer's MMA warp holds the
     // tensor memory allocation and waits at the end
     for (int tile = tile_first; tile < ntiles && ok && leader; tile += tile_step) {
-      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
+      const int t = schedule_tile<KIND>(tile, tile_step, ntiles, p, s_order, skew);
+      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, t, rank);
       if constexpr (PAIR) {
         // the accumulator is free once the epilogue warps of both CTAs are done
         // with it (the odd CTA's arrive from across the cluster)
@@ -713,7 +772,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       named_bar_sync(1, 32 * TR::kEpiWarps);
     }
     for (int tile = tile_first; tile < ntiles; tile += tile_step) {
-      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, tile, rank);
+      const int t = schedule_tile<KIND>(tile, tile_step, ntiles, p, s_order, skew);
+      const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, t, rank);
       // this warp's 32 rows: a full block leaves through TMA boxes; a block
       // that crosses the end of the expert's rows uses masked per-thread stores
       const int row0 = ti.m0 + 32 * q;

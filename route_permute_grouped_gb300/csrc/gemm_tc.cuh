@@ -338,10 +338,13 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
   if constexpr (KIND == KIND_WGRAD) {
     const int r = ti.krow0 + kk;
     const int n = ti.n0 + 128 * rank;
-    tma_load_2d_pair(sA, ma, bar_cluster, ti.m0, r);
-    tma_load_2d_pair(sA + 8192, ma, bar_cluster, ti.m0 + 64, r);
-    tma_load_2d_pair(sB, mb0, bar_cluster, n, r);
-    tma_load_2d_pair(sB + 8192, mb0, bar_cluster, n + 64, r);
+    // the operands are re-read by the expert's other tiles while the fp32
+    // output streams through L2: they stay, the output goes first
+    const uint64_t keep = l2_policy_evict_last();
+    tma_load_2d_pair_hint(sA, ma, bar_cluster, ti.m0, r, keep);
+    tma_load_2d_pair_hint(sA + 8192, ma, bar_cluster, ti.m0 + 64, r, keep);
+    tma_load_2d_pair_hint(sB, mb0, bar_cluster, n, r, keep);
+    tma_load_2d_pair_hint(sB + 8192, mb0, bar_cluster, n + 64, r, keep);
     return;
   }
   tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
