@@ -228,9 +228,20 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     if (s_cum[mid] <= tile) lo = mid; else hi = mid;
   }
   ti.g = lo;
-  int local = tile - s_cum[lo];
-  int mb = local / p.n_tiles;
-  int nb = local - mb * p.n_tiles;
+  const int local = tile - s_cum[lo];
+  int mb, nb;
+  if constexpr (KindTraits<KIND>::kGroupedRows) {
+    // n-major inside an expert: its m tiles of one n tile are consecutive, so
+    // CTA pairs that start together share that n tile's weight block in L2
+    // (m-major, an expert whose tiles straddle two rounds of the persistent
+    // CTAs read the weight blocks of the later round from DRAM again)
+    const int me = (s_cum[lo + 1] - s_cum[lo]) / p.n_tiles;
+    nb = local / me;
+    mb = local - nb * me;
+  } else {
+    mb = local / p.n_tiles;
+    nb = local - mb * p.n_tiles;
+  }
   ti.mt = s_cum[lo] / p.n_tiles + mb;
   ti.nb = nb;
   if constexpr (KindTraits<KIND>::kGroupedRows || KIND == KIND_ROUTER || KIND == KIND_ROUTER_DX) {
