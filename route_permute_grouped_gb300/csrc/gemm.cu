@@ -848,8 +848,16 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (PAIR && !leader) mbar_arrive_cluster(tempty_even + 8u * acc);
-        else mbar_arrive(tempty + acc);
+        if constexpr (KIND == KIND_WGRAD) {
+          // the tile's TMEM loads are complete (tcgen05.wait::ld in every
+          // lane before the warp sync): release the accumulator without
+          // waiting for this warp's fp32 stores to drain
+          if (PAIR && !leader) mbar_arrive_cluster_relaxed(tempty_even + 8u * acc);
+          else mbar_arrive_relaxed(tempty + acc);
+        } else {
+          if (PAIR && !leader) mbar_arrive_cluster(tempty_even + 8u * acc);
+          else mbar_arrive(tempty + acc);
+        }
       }
       if constexpr (KIND == KIND_ROUTER) {
         acc_phase ^= 1u;
