@@ -180,12 +180,51 @@ def read_ceiling_gbs(nbytes, dev, reps=7):
     return _READ_CEILING[nbytes]
 
 
-def add_read_ceiling(kernels, model, dev):
-    """The router's row gains the single-launch read ceiling of its bytes."""
+_WRITE_CEILING = {}
+
+
+def write_ceiling_gbs(dev, nbytes=1 << 30, reps=5):
+    """Median rate of one moe_write_ceiling launch filling `nbytes` (8x the
+    L2): the rate at which HBM absorbs a stream of writes, below the copy
+    peak's read + write figure."""
+    import torch
+
+    from route_permute_grouped_gb300 import ops
+
+    if nbytes in _WRITE_CEILING:
+        return _WRITE_CEILING[nbytes]
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ops.write_ceiling(buf, i)
+        b.record()
+        torch.cuda.synchronize()
+        if i:
+            ts.append(a.elapsed_time(b))
+    ts.sort()
+    del buf
+    _WRITE_CEILING[nbytes] = round(nbytes / (ts[len(ts) // 2] * 1e-3) / 1e9, 1)
+    return _WRITE_CEILING[nbytes]
+
+
+def add_read_ceiling(kernels, model, dev, ls=None):
+    """The router's row gains the single-launch read ceiling of its bytes;
+    the weight gradients' rows the rate of their fp32 output against the
+    measured write ceiling (their output is 6.4 + 3.2 GB per Qwen3 step)."""
     if "router" in kernels and kernels["router"].get("achieved_gbs"):
         rc = read_ceiling_gbs(model["router"][1], dev)
         kernels["router"]["read_ceiling_gbs"] = rc
         kernels["router"]["frac_of_read_ceiling"] = round(kernels["router"]["achieved_gbs"] / rc, 4)
+    if ls is not None and any(n in kernels for n in ("wgrad_gate_up", "wgrad_down")):
+        wc = write_ceiling_gbs(dev)
+        out = {"wgrad_gate_up": 8 * ls.E * ls.H * ls.F, "wgrad_down": 4 * ls.E * ls.F * ls.H}
+        for name, nb in out.items():
+            if name in kernels:
+                gbs = nb / (kernels[name]["ms"] * 1e-3) / 1e9
+                kernels[name].update(output_gbs=round(gbs, 1), write_ceiling_gbs=wc,
+                                     frac_of_write_ceiling=round(gbs / wc, 4))
 
 
 def load_peaks():
@@ -701,7 +740,7 @@ def run_ours(args, ls, rank, world, local_rank):
     # ---------------- per-stage table and roofline of the dominant kernel
     model = stage_model(ls, training)
     kernels, agg = kernel_table(stages, model, peaks)
-    add_read_ceiling(kernels, model, dev)
+    add_read_ceiling(kernels, model, dev, ls)
     dom = max(agg, key=lambda n: agg[n][0])
     dk = kernels[dom]
     fl, by = model[dom]
@@ -889,7 +928,7 @@ def measure_config(name, args, rank, world, dev, peaks):
     assert ops.device_status(ws) == 0
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
     kernels, agg = kernel_table(ops.profile_read(cap), stage_model(ls, training), peaks)
-    add_read_ceiling(kernels, stage_model(ls, training), dev)
+    add_read_ceiling(kernels, stage_model(ls, training), dev, ls)
     # the expert-count histogram of this routing (one training-style forward
     # keeps the counts)
     sv = saved if saved is not None else ops.alloc_saved(cfg, dev)

@@ -477,7 +477,8 @@ void moe_debug_set_fault(int fault);
  * gradient, 14 gate/up data gradient, 15 gate/up weight gradient, 16 router
  * data gradient, 17 permute backward, 18 router weight gradient, 19 aux loss,
  * 26-29 the shared expert's down data gradient + SwiGLU backward, down weight
- * gradient, gate/up data gradient, gate/up weight gradient; 30 moe_read_ceiling).
+ * gradient, gate/up data gradient, gate/up weight gradient; 30 moe_read_ceiling, 31
+ * moe_write_ceiling).
  * moe_profile_stop() stops recording. moe_profile_read() waits for the events
  * and returns their number; ms[i] is the time from event i-1 to event i
  * (0 for call starts). moe_debug_launch_count() returns the number of kernels
@@ -497,6 +498,15 @@ unsigned long long moe_debug_launch_count(void);
  * size, below the long-copy peak by the launch's ramp-up and tail. Returns
  * MOE_ERR_INVALID_ARG for a null or misaligned pointer or size. */
 int moe_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream);
+
+/* Measurement helper, not a step of the layer: fills the `bytes` bytes at
+ * `buf` (device memory, 16-byte aligned, bytes a multiple of 16) with the
+ * 32-bit `word`, 16-byte stores from a grid of four 512-thread CTAs per SM. One
+ * launch over a buffer much larger than L2, timed alone, gives the rate at
+ * which HBM absorbs writes: the bound of a kernel whose time goes to storing
+ * its output (the fp32 weight gradients). Returns MOE_ERR_INVALID_ARG for a
+ * null or misaligned pointer or size. */
+int moe_write_ceiling(void* buf, size_t bytes, unsigned word, void* stream);
 
 /* Test hook: byte offset, inside a workspace of moe_workspace_bytes(cfg,
  * training), of an intermediate the layer keeps there, so that tests can read

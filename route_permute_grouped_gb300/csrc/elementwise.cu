@@ -542,6 +542,26 @@ __global__ void __launch_bounds__(512) read_ceiling_kernel(const uint4* __restri
 }
 }  // namespace moe
 
+namespace moe {
+__global__ void __launch_bounds__(512) write_ceiling_kernel(uint4* __restrict__ p, size_t n16, uint32_t word) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const uint4 v = make_uint4(word, word, word, word);
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) p[i] = v;
+}
+}  // namespace moe
+
+extern "C" int moe_write_ceiling(void* buf, size_t bytes, unsigned word, void* stream) {
+  using namespace moe;
+  if (buf == nullptr || (reinterpret_cast<uintptr_t>(buf) & 15) != 0 || (bytes & 15) != 0) return MOE_ERR_INVALID_ARG;
+  if (bytes == 0) return MOE_OK;
+  NvtxRange nvtx("moe.write_ceiling");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  write_ceiling_kernel<<<4 * num_sms(), 512, 0, st>>>(static_cast<uint4*>(buf), bytes / 16, word);
+  const int rc = status_from_cuda(cudaGetLastError());
+  record_stage(st, 31, 1);
+  return rc;
+}
+
 extern "C" int moe_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream) {
   using namespace moe;
   if (buf == nullptr || sink == nullptr || (reinterpret_cast<uintptr_t>(buf) & 15) != 0 || (bytes & 15) != 0)

@@ -92,6 +92,8 @@ def lib():
         L.moe_debug_launch_count.restype = ctypes.c_ulonglong
         L.moe_read_ceiling.argtypes = [vp, c_size_t, vp, vp]
         L.moe_read_ceiling.restype = c_int
+        L.moe_write_ceiling.argtypes = [vp, c_size_t, ctypes.c_uint, vp]
+        L.moe_write_ceiling.restype = c_int
         L.moe_debug_workspace_offset.argtypes = [POINTER(MoeConfig), c_int, c_int]
         L.moe_debug_workspace_offset.restype = c_size_t
         L.moe_mx_weight_bytes.restype = c_size_t
@@ -142,7 +144,8 @@ STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 22: "mx_quantize_tokens", 24: "
                28: "shared_dgrad_gate_up", 29: "shared_wgrad_gate_up", 1: "router", 2: "permute", 3: "ffn1_gate_up", 4: "ffn2_down", 5: "shared_gate_up",
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
-               17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss", 30: "read_ceiling"}
+               17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss", 30: "read_ceiling",
+               31: "write_ceiling"}
 
 
 def profile_start(capacity: int) -> None:
@@ -169,6 +172,14 @@ def read_ceiling(buf: torch.Tensor, sink: torch.Tensor) -> None:
     assert buf.is_cuda and buf.is_contiguous() and sink.is_cuda
     nbytes = buf.numel() * buf.element_size() // 16 * 16
     _check(lib().moe_read_ceiling(_p(buf), nbytes, _p(sink), _stream()), "moe_read_ceiling")
+
+
+def write_ceiling(buf: torch.Tensor, word: int = 0) -> None:
+    """moe_write_ceiling over the bytes of a contiguous CUDA tensor (a
+    measurement helper: one write-only pass; time it with events)."""
+    assert buf.is_cuda and buf.is_contiguous()
+    nbytes = buf.numel() * buf.element_size() // 16 * 16
+    _check(lib().moe_write_ceiling(_p(buf), nbytes, int(word) & 0xFFFFFFFF, _stream()), "moe_write_ceiling")
 
 
 def launch_count() -> int:

@@ -143,7 +143,7 @@ def test_low_precision_entry_points_check_on_the_host(lib):
 
 
 def test_read_ceiling_checks_on_the_host(lib):
-    # the measurement helper rejects null and misaligned arguments before any
+    # the measurement helpers reject null and misaligned arguments before any
     # CUDA work
     null = ctypes.c_void_p()
     some = ctypes.c_void_p(4096)
@@ -152,3 +152,7 @@ def test_read_ceiling_checks_on_the_host(lib):
     assert lib.moe_read_ceiling(ctypes.c_void_p(4100), 1024, some, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_read_ceiling(some, 1000, some, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_read_ceiling(some, 0, some, null) == ops.MOE_OK
+    assert lib.moe_write_ceiling(null, 1024, 0, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_write_ceiling(ctypes.c_void_p(4100), 1024, 0, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_write_ceiling(some, 1000, 0, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_write_ceiling(some, 0, 0, null) == ops.MOE_OK
