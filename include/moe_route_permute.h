@@ -204,7 +204,9 @@ int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const 
  * figures & tables page, Fig. 40 for the shared expert):
  *   y[t] = sum_{i=0..k-1} topk_gate[t,i] * y_perm[row_id_map[t,i]] (+ shared_out[t]),
  * reduced in fp32 in slot order. y_perm and shared_out are bf16 (fp32 if
- * inter_fp32); y [T,H] is bf16 (fp32 if out_fp32). shared_out may be NULL. */
+ * inter_fp32); y [T,H] is bf16 (fp32 if out_fp32). shared_out may be NULL. A
+ * row index of -1 in row_id_map (a slot moe_permute dropped for an expert
+ * index outside [0,E)) contributes nothing. */
 int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_id_map,
                           const float* topk_gate, const void* shared_out, void* y, void* stream);
 
@@ -487,6 +489,17 @@ void moe_profile_start(int capacity);
 void moe_profile_stop(void);
 int moe_profile_read(int* tags, float* ms, int max);
 unsigned long long moe_debug_launch_count(void);
+
+/* 1 when this library is the bounds-check build (compiled with
+ * -DMOE_BOUNDS_CHECK): its element-wise kernels (combine, combine backward,
+ * permute backward, router backward) range-check every row index they read
+ * from row_id_map against [-1, T*k) and every expert index from topk_idx
+ * against [0, E); an index outside records MOE_ERR_DEVICE_INDEX in the
+ * workspace status word (read by moe_get_device_status; the standalone
+ * moe_unpermute_combine has none and only skips it) and is skipped instead of
+ * read. 0 for the default build, which skips the row index -1 (a slot
+ * moe_permute dropped) and trusts the rest. */
+int moe_bounds_checked(void);
 
 /* Measurement helper, not a step of the layer: reads the `bytes` bytes at
  * `buf` (device memory, 16-byte aligned, bytes a multiple of 16) once, with

@@ -638,6 +638,8 @@ void moe_profile_start(int capacity) {
 
 void moe_profile_stop(void) { g_prof.on = false; }
 
+int moe_bounds_checked(void) { return kBoundsCheck ? 1 : 0; }
+
 int moe_profile_read(int* tags, float* ms, int max) {
   const int n = g_prof.n < max ? g_prof.n : max;
   for (int i = 0; i < n; ++i) {
@@ -799,7 +801,7 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
                     reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), h13s, as,
                     shared, c.inter_fp32 != 0, st, s, STAGE_SHARED1, STAGE_SHARED2));
   }
-  MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
+  MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s, st));
   stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
 }
@@ -915,7 +917,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   //    quantised, blocks of 32 along H)
   MOE_CUDA(launch_combine_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), saved->y_perm, saved->row_id_map,
                               saved->topk_gate, dy_perm, dgate, s, mx ? at<uint8_t>(ws, L.dy_q) : nullptr,
-                              mx ? at<uint8_t>(ws, L.sfa_dy) : nullptr, saved->offsets, saved->topk_idx));
+                              mx ? at<uint8_t>(ws, L.sfa_dy) : nullptr, saved->offsets, saved->topk_idx, st));
   stage_done(s, STAGE_COMBINE_BWD, 1);
   const int n_part = (c.F + 255) / 256;
   float* dg_part = at<float>(ws, L.dg_part);
@@ -939,7 +941,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   }
   // 2. router backward (element-wise): dL as bf16 hi/lo
   MOE_CUDA(launch_router_bwd(c, saved->logits, saved->topk_idx, saved->topk_gate, dgate, recompute ? dg_part : nullptr,
-                             n_part, saved->row_id_map, saved->counts, Ep, dL_hl, s));
+                             n_part, saved->row_id_map, saved->counts, Ep, dL_hl, s, st));
   stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
   if (mx != nullptr) {
@@ -1058,7 +1060,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   }
   // 8. dx = sum_i dx_perm[row(t,i)] + dx_r (+ dx_s)
   MOE_CUDA(launch_unpermute_sum(c, dx_perm, saved->row_id_map, dx_r, dx, s,
-                                shared ? at<void>(ws, L.dx_s) : nullptr, dxp32));
+                                shared ? at<void>(ws, L.dx_s) : nullptr, dxp32, st));
   stage_done(s, STAGE_UNPERMUTE, 1);
   // 9. dW_r = dL^T x (each token block: dL's hi and lo parts against one box
   // of x), split over the token blocks, then reduced in split order; as many
@@ -1208,7 +1210,7 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
                     reinterpret_cast<const __nv_bfloat16*>(Ws3), reinterpret_cast<const __nv_bfloat16*>(Ws2), nullptr,
                     at<__nv_bfloat16>(ws, L.as), shared, c.inter_fp32 != 0, st, s, STAGE_SHARED1, STAGE_SHARED2));
   }
-  MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s));
+  MOE_CUDA(launch_combine(c, yp, rows, gate, shared, y, s, st));
   stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
 }
@@ -1286,7 +1288,7 @@ int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const mo
   stage_done(s, STAGE_PERMUTE, 2);
   MOE_TRY(run_ffn_mx(c, sv.offsets, c.T * c.k, x_q, sfa1, *w, at<uint8_t>(ws, L.a_q), at<uint8_t>(ws, L.sfa2),
                      sv.y_perm, c.inter_fp32 != 0, st, s, reinterpret_cast<__nv_bfloat16*>(sv.h13)));
-  MOE_CUDA(launch_combine(c, sv.y_perm, sv.row_id_map, sv.topk_gate, nullptr, y, s));
+  MOE_CUDA(launch_combine(c, sv.y_perm, sv.row_id_map, sv.topk_gate, nullptr, y, s, st));
   stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
 }
@@ -1520,7 +1522,7 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_TRY(run_gemm_nv(c.E, R, c.F, c.H, offs, q, sfq, gq + 1, w->w2, w->sf2, w->g2,
                       reinterpret_cast<__nv_bfloat16*>(yp), st, s));
   stage_done(s, STAGE_FFN2, 1);
-  MOE_CUDA(launch_combine(c, yp, rows, gate, nullptr, y, s));
+  MOE_CUDA(launch_combine(c, yp, rows, gate, nullptr, y, s, st));
   stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
 }

@@ -27,6 +27,27 @@ __device__ __forceinline__ void set_status(DevStatus* st, int code, int where = 
   }
 }
 
+// The bounds-check build (compiled with -DMOE_BOUNDS_CHECK) range-checks the
+// indices the element-wise kernels read from row_id_map and topk_idx.
+#ifdef MOE_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+// A row index read from row_id_map: -1 marks a slot the permute dropped (its
+// expert index was out of range), which contributes nothing; the bounds-check
+// build also rejects anything outside [-1, nrows), recording
+// MOE_ERR_DEVICE_INDEX (at `where`), and skips it.
+__device__ __forceinline__ bool row_valid(long long r, long long nrows, DevStatus* st, int where) {
+  if constexpr (kBoundsCheck) {
+    if (r < -1 || r >= nrows) {
+      set_status(st, MOE_ERR_DEVICE_INDEX, where);
+      return false;
+    }
+  }
+  return r >= 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -45,14 +45,15 @@ template <bool YP32, bool SH32, bool OUT32>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     gather_sum_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ row_id_map,
                       const float* __restrict__ gate, const void* __restrict__ shared, void* __restrict__ y, int T,
-                      int H, int k, const void* __restrict__ add = nullptr) {
+                      int H, int k, const void* __restrict__ add = nullptr, DevStatus* st = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   if (t >= T) return;
-  int my_r = 0;
+  int my_r = -1;
   float my_g = 1.0f;
   if (lane < k) {
     my_r = row_id_map[static_cast<size_t>(t) * k + lane];
+    if (!row_valid(my_r, static_cast<long long>(T) * k, st, 21)) my_r = -1;  // a dropped slot adds nothing
     if (gate != nullptr) my_g = gate[static_cast<size_t>(t) * k + lane];
   }
   // every lane takes all k (row, gate) pairs before the H loop, whose trip
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      if (i < k) {
+      if (i < k && rows[i] >= 0) {
         float f[8];
         Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f);
 #pragma unroll
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
                        __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dgate, int T, int H, int k,
                        uint8_t* __restrict__ mq = nullptr, uint8_t* __restrict__ msf = nullptr,
                        const int32_t* __restrict__ offsets = nullptr, const int32_t* __restrict__ topk_idx = nullptr,
-                       int E = 0) {
+                       int E = 0, DevStatus* st = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   __shared__ int s_off[MXQ ? kMaxGroups + 1 : 1];
@@ -120,12 +121,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     __syncthreads();
   }
   if (t >= T) return;
-  int my_r = 0, my_e = 0;
+  int my_r = -1, my_e = 0;
   float my_g = 0.0f;
   if (lane < k) {
     my_r = row_id_map[static_cast<size_t>(t) * k + lane];
+    if (!row_valid(my_r, static_cast<long long>(T) * k, st, 22)) my_r = -1;  // a dropped slot: no row
     my_g = gate[static_cast<size_t>(t) * k + lane];
     if (MXQ) my_e = topk_idx[static_cast<size_t>(t) * k + lane];
+    if (MXQ && (my_e < 0 || my_e >= E)) my_r = -1;
   }
   float dot[KMAX];
   int rows[KMAX];
@@ -143,10 +146,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     float f[KMAX][8];
 #pragma unroll
     for (int i = 0; i < KMAX; ++i)
-      if (DG && i < k) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f[i]);
+      if (DG && i < k && rows[i] >= 0) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f[i]);
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
-      if (i < k) {
+      if (i < k && rows[i] >= 0) {
         float o[8];
         float s = 0.0f;
 #pragma unroll
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
       const int r = __shfl_sync(0xffffffffu, my_r, i);
       const float gi = __shfl_sync(0xffffffffu, my_g, i);
       const int e = __shfl_sync(0xffffffffu, my_e, i);
+      if (r < 0) continue;  // warp-uniform
       const size_t sf0 = mx_act_sf_offset(s_pt[e], r - s_off[e], 0, nkb);
 #pragma unroll 4
       for (int v = lane; v < nvec; v += 32) {
@@ -218,9 +222,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
 // Memory-saving backward (dg_part != nullptr): the gate gradient of slot i is
 // (sum over the n_part tile partials of its permuted row) / g, 0 where g = 0.
 __device__ __forceinline__ float slot_dgate(const float* dgate, const float* dg_part, int n_part,
-                                            const int32_t* row_id_map, const float* gate, size_t slot) {
+                                            const int32_t* row_id_map, const float* gate, size_t slot, long long R,
+                                            DevStatus* st) {
   if (dg_part == nullptr) return dgate[slot];
-  const float* pr = dg_part + static_cast<size_t>(row_id_map[slot]) * n_part;
+  const int r = row_id_map[slot];
+  if (!row_valid(r, R, st, 23)) return 0.0f;  // a dropped slot
+  const float* pr = dg_part + static_cast<size_t>(r) * n_part;
   float s = 0.0f;
   for (int j = 0; j < n_part; ++j) s += pr[j];
   const float g = gate[slot];
@@ -236,20 +243,25 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                       const float* __restrict__ gate, const float* __restrict__ dgate,
                       const float* __restrict__ dg_part, int n_part, const int32_t* __restrict__ row_id_map,
                       const int32_t* __restrict__ counts, int T, int E, int k, int score, float gate_scale,
-                      float aux_coeff, int Ep, __nv_bfloat16* __restrict__ dL_hl) {
+                      float aux_coeff, int Ep, __nv_bfloat16* __restrict__ dL_hl, DevStatus* st) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   if (t >= T) return;
   const bool aux = (score == MOE_SCORE_SOFTMAX) && aux_coeff != 0.0f;
   const float* Lrow = logits + static_cast<size_t>(t) * E;
-  // loads
+  // loads; a slot whose expert index is out of range contributes nothing
   int my_e = -1;
   float g_or_L = 0.0f, dg = 0.0f;
   if (lane < k) {
     const size_t slot = static_cast<size_t>(t) * k + lane;
     my_e = topk_idx[slot];
-    dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, slot);
-    g_or_L = score == MOE_SCORE_SOFTMAX ? gate[slot] : Lrow[my_e];
+    if (my_e < 0 || my_e >= E) {
+      if (kBoundsCheck) set_status(st, MOE_ERR_DEVICE_INDEX, 24);
+      my_e = -1;
+    } else {
+      dg = slot_dgate(dgate, dg_part, n_part, row_id_map, gate, slot, static_cast<long long>(T) * k, st);
+      g_or_L = score == MOE_SCORE_SOFTMAX ? gate[slot] : Lrow[my_e];
+    }
   }
   float v[NJ];
   float cnt[NJ];
@@ -262,13 +274,13 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   // the gate term of the selected slots
   float my_dl;
   if (score == MOE_SCORE_SOFTMAX) {
-    const float q = lane < k ? g_or_L / gate_scale : 0.0f;
+    const float q = (lane < k && my_e >= 0) ? g_or_L / gate_scale : 0.0f;
     float inner = q * dg;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, o);
     my_dl = gate_scale * q * (dg - inner);
   } else {
-    const float sg = lane < k ? 1.0f / (1.0f + __expf(-g_or_L)) : 0.0f;
+    const float sg = (lane < k && my_e >= 0) ? 1.0f / (1.0f + __expf(-g_or_L)) : 0.0f;
     float S = sg, inner = dg * sg;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -428,39 +440,40 @@ __global__ void split_reduce_kernel(const float* __restrict__ partials, int spli
 static int blocks_for(int T) { return (T + kWarpsPerBlock - 1) / kWarpsPerBlock; }
 
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_id_map, const float* gate,
-                           const void* shared, void* y, cudaStream_t st) {
+                           const void* shared, void* y, cudaStream_t st, DevStatus* ds) {
   NvtxRange nvtx("moe.combine");
   const int b = blocks_for(c.T);
   const bool yp = c.inter_fp32 != 0, out = c.out_fp32 != 0;
   // the shared output has the storage type of y_perm
-  if (yp && out) gather_sum_kernel<true, true, true><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
-  else if (yp) gather_sum_kernel<true, true, false><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
-  else if (out) gather_sum_kernel<false, false, true><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
-  else gather_sum_kernel<false, false, false><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k);
+  if (yp && out) gather_sum_kernel<true, true, true><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k, nullptr, ds);
+  else if (yp) gather_sum_kernel<true, true, false><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k, nullptr, ds);
+  else if (out) gather_sum_kernel<false, false, true><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k, nullptr, ds);
+  else gather_sum_kernel<false, false, false><<<b, kWarpsPerBlock * 32, 0, st>>>(y_perm, row_id_map, gate, shared, y, c.T, c.H, c.k, nullptr, ds);
   return cudaGetLastError();
 }
 
 cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const int32_t* row_id_map,
-                                 const float* extra, void* dx, cudaStream_t st, const void* add, bool rows_fp32) {
+                                 const float* extra, void* dx, cudaStream_t st, const void* add, bool rows_fp32,
+                                 DevStatus* ds) {
   NvtxRange nvtx("moe.permute_backward");
   const int b = blocks_for(c.T);
   const dim3 g(b), blk(kWarpsPerBlock * 32);
   if (rows_fp32 && c.out_fp32)
-    gather_sum_kernel<true, true, true><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add);
+    gather_sum_kernel<true, true, true><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add, ds);
   else if (rows_fp32)
-    gather_sum_kernel<true, true, false><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add);
+    gather_sum_kernel<true, true, false><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add, ds);
   else if (c.out_fp32)
-    gather_sum_kernel<false, true, true><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add);
+    gather_sum_kernel<false, true, true><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k, add, ds);
   else
     gather_sum_kernel<false, true, false><<<g, blk, 0, st>>>(dx_perm, row_id_map, nullptr, extra, dx, c.T, c.H, c.k,
-                                                             add);
+                                                             add, ds);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq, uint8_t* msf, const int32_t* offsets,
-                               const int32_t* topk_idx) {
+                               const int32_t* topk_idx, DevStatus* ds) {
   NvtxRange nvtx("moe.combine_backward");
   const int b = blocks_for(c.T);
   const int th = kWarpsPerBlock * 32;
@@ -468,35 +481,36 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
     cudaError_t e = cudaMemsetAsync(msf, 0, mx_sfa_bytes(static_cast<long long>(c.T) * c.k, c.E, c.H), st);
     if (e != cudaSuccess) return e;
     if (c.inter_fp32) {
-      if (c.k <= 8) combine_bwd_kernel<true, 8, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
-      else combine_bwd_kernel<true, 16, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
+      if (c.k <= 8) combine_bwd_kernel<true, 8, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E, ds);
+      else combine_bwd_kernel<true, 16, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E, ds);
     } else {
-      if (c.k <= 8) combine_bwd_kernel<false, 8, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
-      else combine_bwd_kernel<false, 16, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E);
+      if (c.k <= 8) combine_bwd_kernel<false, 8, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E, ds);
+      else combine_bwd_kernel<false, 16, true, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, mq, msf, offsets, topk_idx, c.E, ds);
     }
     return cudaGetLastError();
   }
   if (y_perm == nullptr) {  // memory-saving backward: dy_perm only
-    if (c.k <= 8) combine_bwd_kernel<false, 8, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k);
-    else combine_bwd_kernel<false, 16, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k);
+    if (c.k <= 8) combine_bwd_kernel<false, 8, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
+    else combine_bwd_kernel<false, 16, false><<<b, th, 0, st>>>(dO, nullptr, row_id_map, gate, dy_perm, nullptr, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
   } else if (c.inter_fp32) {
-    if (c.k <= 8) combine_bwd_kernel<true, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
-    else combine_bwd_kernel<true, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+    if (c.k <= 8) combine_bwd_kernel<true, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
+    else combine_bwd_kernel<true, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
   } else {
-    if (c.k <= 8) combine_bwd_kernel<false, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
-    else combine_bwd_kernel<false, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k);
+    if (c.k <= 8) combine_bwd_kernel<false, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
+    else combine_bwd_kernel<false, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx, const float* gate,
                               const float* dgate, const float* dg_part, int n_part, const int32_t* row_id_map,
-                              const int32_t* counts, int Ep, __nv_bfloat16* dL_hl, cudaStream_t st) {
+                              const int32_t* counts, int Ep, __nv_bfloat16* dL_hl, cudaStream_t st,
+                              DevStatus* ds) {
   NvtxRange nvtx("moe.router_backward");
   const dim3 g(blocks_for(c.T)), b(kWarpsPerBlock * 32);
 #define MOE_ROUTER_BWD(NJ)                                                                                  \
   router_bwd_kernel<NJ><<<g, b, 0, st>>>(logits, topk_idx, gate, dgate, dg_part, n_part, row_id_map, counts, \
-                                         c.T, c.E, c.k, c.score, c.gate_scale, c.aux_coeff, Ep, dL_hl)
+                                         c.T, c.E, c.k, c.score, c.gate_scale, c.aux_coeff, Ep, dL_hl, ds)
   // Ep (a multiple of 64, <= 256) columns over 32 lanes
   if (Ep <= 64) MOE_ROUTER_BWD(2);
   else if (Ep <= 128) MOE_ROUTER_BWD(4);

@@ -61,23 +61,26 @@ cudaError_t launch_permute(const moe_config& c, const __nv_bfloat16* x, const in
 size_t permute_lookback_ints(int T, int E);
 
 // elementwise.cu
+// ds: the status word that a dropped-slot or (bounds-check build) out-of-range
+// index read from row_id_map / topk_idx is recorded in; nullable
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_id_map,
-                           const float* gate, const void* shared, void* y, cudaStream_t st);
+                           const float* gate, const void* shared, void* y, cudaStream_t st, DevStatus* ds = nullptr);
 // mq != nullptr (MXFP8 training step): also the MXFP8 rows of dy_perm (codes
 // mq [R, H], tile-ready scales msf; offsets and topk_idx locate each row)
 cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq = nullptr, uint8_t* msf = nullptr,
-                               const int32_t* offsets = nullptr, const int32_t* topk_idx = nullptr);
+                               const int32_t* offsets = nullptr, const int32_t* topk_idx = nullptr,
+                               DevStatus* ds = nullptr);
 // dx = sum_i dx_perm[row(t,i)] + extra (fp32, nullable) + add ([T,H], nullable);
 // dx_perm and add are fp32 with rows_fp32, else bf16
 cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const int32_t* row_id_map,
                                  const float* extra, void* dx, cudaStream_t st, const void* add = nullptr,
-                                 bool rows_fp32 = false);
+                                 bool rows_fp32 = false, DevStatus* ds = nullptr);
 cudaError_t launch_router_bwd(const moe_config& c, const float* logits, const int32_t* topk_idx,
                               const float* gate, const float* dgate, const float* dg_part, int n_part,
                               const int32_t* row_id_map, const int32_t* counts, int Ep, __nv_bfloat16* dL_hl,
-                              cudaStream_t st);
+                              cudaStream_t st, DevStatus* ds = nullptr);
 cudaError_t launch_aux_loss(const moe_config& c, const float* aux_partials, const int32_t* counts, float* out,
                             cudaStream_t st);
 cudaError_t launch_split_reduce(const float* partials, int splits, size_t n, float* out, cudaStream_t st);

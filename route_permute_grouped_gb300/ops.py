@@ -45,14 +45,16 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library this process loads: the bounds-check build when the
+    environment sets MOE_BOUNDS_CHECK=1, else the default build."""
+    return _build.LIB_CHECKED if os.environ.get("MOE_BOUNDS_CHECK") == "1" else _build.LIB
 
 
 def lib():
     """The loaded library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        path = _build.LIB
+        path = library_path()
         if not os.path.exists(path):
             raise RuntimeError(f"CUDA library {path} is missing: run route_permute_grouped_gb300.build.build()")
         L = ctypes.CDLL(path)
@@ -90,6 +92,8 @@ def lib():
         L.moe_profile_read.restype = c_int
         L.moe_debug_launch_count.argtypes = []
         L.moe_debug_launch_count.restype = ctypes.c_ulonglong
+        L.moe_bounds_checked.argtypes = []
+        L.moe_bounds_checked.restype = c_int
         L.moe_read_ceiling.argtypes = [vp, c_size_t, vp, vp]
         L.moe_read_ceiling.restype = c_int
         L.moe_write_ceiling.argtypes = [vp, c_size_t, ctypes.c_uint, vp]

@@ -156,3 +156,7 @@ def test_read_ceiling_checks_on_the_host(lib):
     assert lib.moe_write_ceiling(ctypes.c_void_p(4100), 1024, 0, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_write_ceiling(some, 1000, 0, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_write_ceiling(some, 0, 0, null) == ops.MOE_OK
+
+
+def test_default_build_is_not_the_bounds_check_build(lib):
+    assert lib.moe_bounds_checked() == 0

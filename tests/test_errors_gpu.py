@@ -63,3 +63,32 @@ def test_bounded_wait_runs_out_and_context_survives():
     _, _, r_ref = O.permute_plan(idx.cpu().numpy(), cfg.E)
     assert np.array_equal(rows.cpu().numpy(), r_ref)
     torch.cuda.synchronize()
+
+
+def test_combine_skips_slots_the_permute_dropped():
+    # moe_permute marks a slot whose expert index is out of range with row -1;
+    # the combine then adds only the token's other slots (no read at row -1)
+    cfg, idx, x = _inputs()
+    bad = idx.clone()
+    bad[5, 1] = cfg.E
+    ws = ops.workspace(cfg)
+    _, rows, _, _ = ops.permute(cfg, x, bad, ws)
+    assert ops.device_status(ws) == DEVICE_INDEX
+    R = cfg.T * cfg.k
+    g = torch.Generator(device="cuda").manual_seed(3)
+    y_perm = torch.randn((R, cfg.H), generator=g, device="cuda").to(torch.bfloat16)
+    gate = torch.rand((cfg.T, cfg.k), generator=g, device="cuda")
+    y = ops.unpermute_combine(cfg, y_perm, rows, gate)
+    torch.cuda.synchronize()
+    r = rows.cpu().numpy()
+    yp = y_perm.float().cpu().numpy().astype(np.float64)
+    gt = gate.cpu().numpy().astype(np.float64)
+    ref = np.zeros((cfg.T, cfg.H))
+    for t in range(cfg.T):
+        for i in range(cfg.k):
+            if r[t, i] >= 0:
+                ref[t] += gt[t, i] * yp[r[t, i]]
+    got = y.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(got - ref)) <= 2e-2 * max(1.0, float(np.abs(ref).max()))
+    assert np.allclose(got[5], (gt[5, 0] * yp[r[5, 0]]), rtol=1e-2, atol=1e-2)
