@@ -206,7 +206,7 @@ int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const 
  * reduced in fp32 in slot order. y_perm and shared_out are bf16 (fp32 if
  * inter_fp32); y [T,H] is bf16 (fp32 if out_fp32). shared_out may be NULL. A
  * row index of -1 in row_id_map (a slot moe_permute dropped for an expert
- * index outside [0,E)) contributes nothing. */
+ * index outside [0,E)) is weighted 0 (row 0 of y_perm is read in its place). */
 int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_id_map,
                           const float* topk_gate, const void* shared_out, void* y, void* stream);
 

@@ -49,12 +49,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   if (t >= T) return;
-  int my_r = -1;
+  int my_r = 0;
   float my_g = 1.0f;
   if (lane < k) {
     my_r = row_id_map[static_cast<size_t>(t) * k + lane];
-    if (!row_valid(my_r, static_cast<long long>(T) * k, st, 21)) my_r = -1;  // a dropped slot adds nothing
     if (gate != nullptr) my_g = gate[static_cast<size_t>(t) * k + lane];
+    if (!row_valid(my_r, static_cast<long long>(T) * k, st, 21)) {
+      my_r = 0;  // a dropped slot: row 0 read with weight 0
+      my_g = 0.0f;
+    }
   }
   // every lane takes all k (row, gate) pairs before the H loop, whose trip
   // count differs between lanes when H/8 is not a multiple of 32
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      if (i < k && rows[i] >= 0) {
+      if (i < k) {
         float f[8];
         Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f);
 #pragma unroll
@@ -145,11 +148,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     Vec8<false>::load(dO, static_cast<size_t>(t) * H + v * 8, d);
     float f[KMAX][8];
 #pragma unroll
-    for (int i = 0; i < KMAX; ++i)
-      if (DG && i < k && rows[i] >= 0) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i]) * H + v * 8, f[i]);
+    for (int i = 0; i < KMAX; ++i)  // a dropped slot (row -1) loads row 0; its results are discarded
+      if (DG && i < k) Vec8<YP32>::load(y_perm, static_cast<size_t>(rows[i] >= 0 ? rows[i] : 0) * H + v * 8, f[i]);
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
-      if (i < k && rows[i] >= 0) {
+      if (i < k) {
         float o[8];
         float s = 0.0f;
 #pragma unroll
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
           o[j] = gs[i] * d[j];
         }
         dot[i] += s;
-        Vec8<false>::store(dy_perm, static_cast<size_t>(rows[i]) * H + v * 8, o);
+        if (rows[i] >= 0) Vec8<false>::store(dy_perm, static_cast<size_t>(rows[i]) * H + v * 8, o);
       }
     }
   }
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
       float s = dot[i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) dgate[static_cast<size_t>(t) * k + i] = s;
+      if (lane == 0) dgate[static_cast<size_t>(t) * k + i] = rows[i] >= 0 ? s : 0.0f;
     }
   }
 }
