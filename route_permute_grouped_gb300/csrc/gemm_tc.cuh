@@ -230,11 +230,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
   ti.g = lo;
   const int local = tile - s_cum[lo];
   int mb, nb;
-  if constexpr (KindTraits<KIND>::kGroupedRows) {
-    // n-major inside an expert: its m tiles of one n tile are consecutive, so
-    // CTA pairs that start together share that n tile's weight block in L2
-    // (m-major, an expert whose tiles straddle two rounds of the persistent
-    // CTAs read the weight blocks of the later round from DRAM again)
+  if constexpr (KindTraits<KIND>::kGroupedRows && !KindTraits<KIND>::kMx && !KindTraits<KIND>::kNv) {
+    // bf16 kinds: n-major inside an expert: its m tiles of one n tile are
+    // consecutive, so CTA pairs that start together share that n tile's weight
+    // block in L2 (m-major, an expert whose tiles straddle two rounds of the
+    // persistent CTAs read the weight blocks of the later round from DRAM
+    // again). The MXFP8 and NVFP4 kinds, whose weight blocks are half or a
+    // quarter the bytes, measured 1% faster m-major and keep it.
     const int me = (s_cum[lo + 1] - s_cum[lo]) / p.n_tiles;
     nb = local / me;
     mb = local - nb * me;
