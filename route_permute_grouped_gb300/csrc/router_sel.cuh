@@ -213,9 +213,15 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
     inv = (valid && tot > 0.0f) ? 1.0f / tot : 0.0f;
   }
 
-  // pass 2: selection values (parked unless they are the logits); aux sums
+  // pass 2: selection values (parked unless they are the logits); aux sums;
+  // with a group limit whose groups lie inside this part's chunks, the part
+  // also scores its own groups here (top-2 sum each) as the values pass by
   const int nslices = 4 * ((p.T + 127) >> 7);
+  const int gsz = grouped ? E / p.r_groups : 1;
+  const bool own_groups = grouped && (32 * cpp) % gsz == 0;
   if (MODE != RSEL_LOGIT || want_aux) {
+    int og = (32 * c0) / gsz, ocnt = 0;
+    float ob1 = -INFINITY, ob2 = -INFINITY;
     for (int c = c0; c < c1; ++c) {
       float v[32], z[32], pr[32];
       rs_ld(tacc + 32 * c, v);
@@ -233,6 +239,25 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
         pr[j] = e < E ? pe : 0.0f;
       }
       if (MODE != RSEL_LOGIT && !force) rs_st(tz + 32 * c, z);
+      if (own_groups) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (32 * c + j < E) {
+            if (z[j] > ob1) {
+              ob2 = ob1;
+              ob1 = z[j];
+            } else if (z[j] > ob2) {
+              ob2 = z[j];
+            }
+            if (++ocnt == gsz) {
+              sm.gs[og * kRouterRows + tid] = gsz >= 2 ? ob1 + ob2 : ob1;
+              ++og;
+              ocnt = 0;
+              ob1 = ob2 = -INFINITY;
+            }
+          }
+        }
+      }
       if (want_aux) {
         const float col = lane_column_sums(pr, lane);
         if (32 * c + lane < E && slice < nslices) p.r_aux[static_cast<size_t>(slice) * E + 32 * c + lane] = col;
@@ -293,11 +318,10 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
   }
 
   if (grouped) {
-    // part 0 scores every group (a group's experts are contiguous) and keeps
-    // the best topk_groups; each part then masks its own chunks
-    named_bar_sync(bar, 64);  // both parts' values are parked
-    if (part == 0) {
-      const int gsz = E / p.r_groups;
+    uint32_t kp = 0u;  // kept groups of this row
+    named_bar_sync(bar, 64);  // both parts' values are parked (and own group scores written)
+    if (!own_groups && part == 0) {
+      // groups straddle the parts: part 0 scores every group from the parked values
       int g = 0, cnt = 0;
       float b1 = -INFINITY, b2 = -INFINITY;
       for (int c = 0; c < nch; ++c) {
@@ -321,25 +345,24 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
           }
         }
       }
-      uint32_t kp = 0u;
-      for (int s = 0; s < p.r_topk_groups; ++s) {
-        int bi = -1;
-        float best = -INFINITY;
-        for (int gg = 0; gg < p.r_groups; ++gg) {
-          if ((kp >> gg) & 1u) continue;
-          const float v = sm.gs[gg * kRouterRows + tid];
-          if (bi < 0 || v > best) {
-            best = v;
-            bi = gg;
-          }
-        }
-        kp |= 1u << bi;
-      }
-      sm.keep[tid] = kp;
     }
-    named_bar_sync(bar, 64);
-    const uint32_t kp = sm.keep[tid];
-    const int gsz = E / p.r_groups;
+    if (!own_groups) named_bar_sync(bar, 64);
+    // the best topk_groups groups (a lower group wins ties), by both parts
+    // from the shared scores
+    for (int sg = 0; sg < p.r_topk_groups; ++sg) {
+      int bi = -1;
+      float best = -INFINITY;
+      for (int gg = 0; gg < p.r_groups; ++gg) {
+        if ((kp >> gg) & 1u) continue;
+        const float v = sm.gs[gg * kRouterRows + tid];
+        if (bi < 0 || v > best) {
+          best = v;
+          bi = gg;
+        }
+      }
+      kp |= 1u << bi;
+    }
+    // each part masks its own parked chunks
     for (int c = c0; c < c1; ++c) {
       float z[32];
       rs_ld(tz + 32 * c, z);
@@ -356,6 +379,7 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
       }
       rs_st(tz + 32 * c, z);
     }
+    named_bar_sync(bar, 64);  // both parts are done reading the group scores
   }
 
   // pass 3: the KM largest values of the part's chunks; both lists merged
