@@ -167,8 +167,10 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
   const int other = (part ^ 1) * kRouterRows + tid;
 
   // pass 1: biased logits (out to logits_out), softmax statistics of the part
+  // (skipped when there is neither)
   float m = -INFINITY, S = 0.0f;
-  for (int c = c0; c < c1; ++c) {
+  const bool pass1 = need_p || p.r_logits != nullptr;
+  for (int c = c0; pass1 && c < c1; ++c) {
     float v[32];
     rs_ld(tacc + 32 * c, v);
     float cm = -INFINITY;
@@ -317,8 +319,9 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
     return;
   }
 
+  uint32_t kp = 0xffffffffu;  // kept groups of this row
   if (grouped) {
-    uint32_t kp = 0u;  // kept groups of this row
+    kp = 0u;
     named_bar_sync(bar, 64);  // both parts' values are parked (and own group scores written)
     if (!own_groups && part == 0) {
       // groups straddle the parts: part 0 scores every group from the parked values
@@ -362,8 +365,9 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
       }
       kp |= 1u << bi;
     }
-    // each part masks its own parked chunks
-    for (int c = c0; c < c1; ++c) {
+    // each part masks its own parked chunks (groups of whole chunks are
+    // masked per chunk where the passes below load them instead)
+    for (int c = c0; c < c1 && gsz % 32 != 0; ++c) {
       float z[32];
       rs_ld(tz + 32 * c, z);
       int g = (32 * c) / gsz, cnt = (32 * c) % gsz;
@@ -389,6 +393,10 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
   for (int c = c0; c < c1; ++c) {
     float z[32];
     chunk_z<MODE>(tacc, tz, c, E, sm, z);
+    if (grouped && gsz % 32 == 0 && !((kp >> ((32 * c) / gsz)) & 1u)) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = -INFINITY;
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) topk_insert<KM>(b, z[j]);
   }
@@ -407,6 +415,10 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
   for (int c = c0; c < c1; ++c) {
     float z[32];
     chunk_z<MODE>(tacc, tz, c, E, sm, z);
+    if (grouped && gsz % 32 == 0 && !((kp >> ((32 * c) / gsz)) & 1u)) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = -INFINITY;
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       ngt += z[j] > t ? 1 : 0;
@@ -427,6 +439,10 @@ __device__ __forceinline__ void router_select_part(const GemmParams& p, uint32_t
   for (int c = c0; c < c1; ++c) {
     float z[32], v[32];
     chunk_z<MODE>(tacc, tz, c, E, sm, z);
+    if (grouped && gsz % 32 == 0 && !((kp >> ((32 * c) / gsz)) & 1u)) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = -INFINITY;
+    }
     if constexpr (MODE == RSEL_LOGIT) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = z[j];
