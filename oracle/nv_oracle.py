@@ -31,12 +31,14 @@ from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import bf16_rne, permute_plan, route, silu
+from .moe_oracle import (CONTRACT, aux_loss, bf16_rne, permute_plan, route, router_backward, silu, silu_grad,
+                         softmax)
 from .mx_oracle import e4m3_encode, e4m3_round
 
 __all__ = ["E2M1_MAX", "e2m1_round", "e2m1_encode", "e2m1_decode", "nv_tensor_scale", "nv_quantize",
            "nv_dequantize", "nv_roundtrip", "nv_grouped_gemm", "routed_rows_roundtrip", "gate_up_store",
-           "activation_roundtrip", "nv_layer_fwd"]
+           "activation_roundtrip", "nv_layer_fwd", "output_grad_roundtrip", "swiglu_grad_roundtrip",
+           "dgrad_weight_roundtrip", "nv_layer_bwd"]
 
 E2M1_MAX = 6.0
 NV_BLOCK = 16
@@ -208,3 +210,139 @@ def nv_layer_fwd(x, w_r, W1, W3, W2, k, score="softmax", expert_bias=None, logit
         acc = acc + rt["topk_gate"][tok, i:i + 1] * y_perm[row[tok, i]]
     y[tok] = acc
     return {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": y}
+
+
+# ----------------------------------------------------------------------------
+# Training step with NVFP4 data-gradient GEMMs
+# ----------------------------------------------------------------------------
+def output_grad_roundtrip(dy, offsets):
+    """NVFP4 round trip of dy_perm [R,H] (the down data gradient's activation
+    operand) as ONE tensor over all routed rows, 16-element blocks along H."""
+    dy = np.asarray(dy, np.float32)
+    g = nv_tensor_scale(np.abs(dy).max() if dy.size else 0.0)
+    return nv_roundtrip(dy, axis=1, g=g)
+
+
+def swiglu_grad_roundtrip(dh, offsets):
+    """NVFP4 round trip of [dh1 | dh3] [R,2F] (the gate/up data gradient's
+    activation operand) as ONE tensor over all routed rows, 16-element blocks
+    along 2F."""
+    dh = np.asarray(dh, np.float32)
+    g = nv_tensor_scale(np.abs(dh).max() if dh.size else 0.0)
+    return nv_roundtrip(dh, axis=1, g=g)
+
+
+def dgrad_weight_roundtrip(W):
+    """NVFP4 round trip of one expert's weight as the data-gradient GEMM reads
+    it: W [N, K] row-wise (16-element blocks along K, the GEMM's contraction
+    axis), the expert's matrix a tensor of its own (W2_e [F, H] along H;
+    [W1_e | W3_e] [H, 2F] along 2F)."""
+    return nv_roundtrip(np.asarray(W, np.float32), axis=1)
+
+
+def nv_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, logit_bias=None, n_groups=1,
+                 topk_groups=1, gate_scale=1.0, aux_coeff=0.0, prec=CONTRACT, force_balanced=False, quant=True):
+    """Forward and backward of the layer with NVFP4 expert GEMMs, for the loss
+    <dO, y> + L_aux.
+
+    The report trains in NVFP4 (summary page, "Modeling"; Key Terms) without
+    giving a recipe. The reading here follows the NVFP4 forward
+    (``nv_layer_fwd``): each data-gradient GEMM quantises both operands along
+    its own contraction axis, the operand made of routed rows as ONE tensor
+    over all of them (one fp32 tensor scale), each expert's weight as a tensor
+    of its own; the weight gradients stay bf16 x bf16 (fp32 out). In row space
+    (rows ordered by expert as the permute lays them out):
+
+      forward  h = Q(x_perm) Q([W1_e | W3_e])         (Q along H; stored per prec.h13)
+               a = SiLU(h1) h3                          (from the stored h; per prec.a)
+               y_perm = Q(a) Q(W2_e)                    (Q along F; per prec.y_perm)
+      backward dy_perm = g dO (per prec.dy_perm); dg = <dO, y_perm>
+               da = Q(dy_perm) Q(W2_e)^T                (Q along H, W2_e [F,H] row-wise; not rounded)
+               dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1) (stored h; per prec.dh13)
+               dx_perm = Q([dh1 | dh3]) Q([W1_e | W3_e])^T   (Q along 2F; per prec.dx_perm)
+               dW2_e = a_e^T dy_perm_e, dW1_e = x_e^T dh1_e, dW3_e = x_e^T dh3_e (fp64 sums)
+               router backward, aux loss and dx = sum of the token's dx_perm rows + dL W_r as in
+               the bf16 layer
+
+    Round trips: ``routed_rows_roundtrip`` (x_perm), ``activation_roundtrip``
+    (a), ``output_grad_roundtrip`` (dy_perm), ``swiglu_grad_roundtrip``
+    ([dh1 | dh3]), ``nv_roundtrip`` along axis 0 for the forward weights and
+    ``dgrad_weight_roundtrip`` for the backward ones. ``quant=False`` makes
+    every round trip the identity: the bf16 layer's backward on the same
+    stored tensors. No shared expert. Returns the keys of the bf16 oracle's
+    ``layer_bwd`` for the whole layer (dW1, dW3, dW2 as dicts over every
+    expert) and, for the pins, the row-space tensors "dy_perm", "da",
+    "dh13" and "dx_perm"."""
+    x = np.asarray(x, np.float64)
+    dO = np.asarray(dO, np.float64)
+    T, H = x.shape
+    w_r = np.asarray(w_r, np.float64)
+    E = w_r.shape[0]
+    F = np.asarray(W1[0]).shape[1]
+    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
+    idx, gate = rt["topk_idx"], rt["topk_gate"]
+    counts, offsets, row = permute_plan(idx, E)
+    R = T * k
+    flat = row.reshape(-1)
+    x_perm = np.zeros((R, H))
+    x_perm[flat] = np.repeat(x, k, axis=0)
+    g_perm = np.zeros(R)
+    g_perm[flat] = gate.reshape(-1)
+    dO_perm = np.zeros((R, H))
+    dO_perm[flat] = np.repeat(dO, k, axis=0)
+    ident = lambda v, *a: np.asarray(v, np.float64)  # noqa: E731
+    rows_q = routed_rows_roundtrip if quant else ident
+    act_q = activation_roundtrip if quant else ident
+    dy_q = output_grad_roundtrip if quant else ident
+    dh_q = swiglu_grad_roundtrip if quant else ident
+    fw_q = (lambda W: nv_roundtrip(np.asarray(W, np.float32), axis=0)) if quant else ident
+    bw_q = dgrad_weight_roundtrip if quant else ident
+    segs = [(e, int(offsets[e]), int(offsets[e + 1])) for e in range(E) if offsets[e + 1] > offsets[e]]
+    W13 = {e: np.concatenate([np.asarray(W1[e], np.float64), np.asarray(W3[e], np.float64)], axis=1)
+           for e, _, _ in segs}
+    # forward
+    xq = rows_q(x_perm, offsets)
+    h = np.zeros((R, 2 * F))
+    for e, lo, hi in segs:
+        h[lo:hi] = prec.r("h13", xq[lo:hi] @ fw_q(W13[e]))
+    h1, h3 = h[:, :F], h[:, F:]
+    a = prec.r("a", silu(h1) * h3)
+    aq = act_q(a, offsets)
+    y_perm = np.zeros((R, H))
+    for e, lo, hi in segs:
+        y_perm[lo:hi] = prec.r("y_perm", aq[lo:hi] @ fw_q(np.asarray(W2[e], np.float64)))
+    y = np.zeros((T, H))
+    for i in range(k):
+        y += gate[:, i:i + 1] * y_perm[row[:, i]]
+    # backward
+    dy = prec.r("dy_perm", g_perm[:, None] * dO_perm)
+    dgate = np.einsum("th,tih->ti", dO, y_perm[row])
+    dyq = dy_q(dy, offsets)
+    da = np.zeros((R, F))
+    for e, lo, hi in segs:
+        da[lo:hi] = dyq[lo:hi] @ bw_q(np.asarray(W2[e], np.float64)).T
+    dh1 = prec.r("dh13", da * h3 * silu_grad(h1))
+    dh3 = prec.r("dh13", da * silu(h1))
+    dh = np.concatenate([dh1, dh3], axis=1)
+    dhq = dh_q(dh, offsets)
+    dx_perm = np.zeros((R, H))
+    for e, lo, hi in segs:
+        dx_perm[lo:hi] = prec.r("dx_perm", dhq[lo:hi] @ bw_q(W13[e]).T)
+    dW1 = {e: np.zeros((H, F)) for e in range(E)}
+    dW3 = {e: np.zeros((H, F)) for e in range(E)}
+    dW2 = {e: np.zeros((F, H)) for e in range(E)}
+    for e, lo, hi in segs:
+        dW1[e] = x_perm[lo:hi].T @ dh1[lo:hi]
+        dW3[e] = x_perm[lo:hi].T @ dh3[lo:hi]
+        dW2[e] = a[lo:hi].T @ dy[lo:hi]
+    aux = aux_coeff if score == "softmax" else 0.0
+    dL = router_backward(rt["logits"], idx, gate, dgate, score, gate_scale, counts, k, aux, T_total=T)
+    dx = dL @ w_r
+    for i in range(k):
+        dx += dx_perm[row[:, i]]
+    res = {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": prec.r("y", y), "dgate": dgate,
+           "dW1": dW1, "dW3": dW3, "dW2": dW2, "dlogits": dL, "dx": prec.r("dx", dx), "dW_r": dL.T @ x,
+           "dy_perm": dy, "da": da, "dh13": dh, "dx_perm": dx_perm}
+    if aux:
+        res["aux_loss"] = aux_loss(softmax(rt["logits"]), counts, k, aux)
+    return res

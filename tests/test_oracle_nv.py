@@ -253,3 +253,114 @@ def test_planted_nv_layer_mistake_is_caught(monkeypatch, name, fn):
     monkeypatch.setattr(NV, name, fn)
     with pytest.raises(AssertionError):
         test_nv_layer_exact_inputs_reduce_to_plain_layer()
+
+
+# ---------------------------------------------------------------------------
+# The NVFP4 training step (forward and backward with NVFP4 data gradients).
+# ---------------------------------------------------------------------------
+def _nv_train_case(seed, T=48, H=64, E=4, k=2, F=32):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0, 1, (T, H))
+    w_r = rng.normal(0, 0.4, (E, H))
+    W1 = rng.normal(0, H ** -0.5, (E, H, F))
+    W3 = rng.normal(0, H ** -0.5, (E, H, F))
+    W2 = rng.normal(0, F ** -0.5, (E, F, H))
+    dO = rng.normal(0, 1, (T, H))
+    return x, w_r, W1, W3, W2, dO, k
+
+
+def test_nv_layer_bwd_without_quantisation_is_the_bf16_backward():
+    # every round trip the identity: the plain backward (terms, signs, transposes)
+    x, w_r, W1, W3, W2, dO, k = _nv_train_case(3)
+    got = O.nv_layer_bwd(x, w_r, W1, W3, W2, dO, k, aux_coeff=1e-2, prec=O.EXACT, quant=False)
+    ref = O.layer_bwd(x, w_r, W1, W3, W2, dO, k, aux_coeff=1e-2, prec=O.EXACT)
+    for key in ("dx", "dW_r", "dgate"):
+        np.testing.assert_allclose(got[key], ref[key], rtol=1e-11, atol=1e-12, err_msg=key)
+    y = O.layer_fwd(x, w_r, W1, W3, W2, k, prec=O.EXACT)["y"]
+    np.testing.assert_allclose(got["y"], y, rtol=1e-11, atol=1e-12)
+    for key in ("dW1", "dW3", "dW2"):
+        for e in ref[key]:
+            np.testing.assert_allclose(got[key][e], ref[key][e], rtol=1e-11, atol=1e-12, err_msg=f"{key}[{e}]")
+    assert got["aux_loss"] == pytest.approx(ref["aux_loss"], rel=1e-14)
+
+
+def test_nv_layer_bwd_forward_is_the_nv_forward():
+    x, w_r, W1, W3, W2, dO, k = _nv_train_case(4)
+    got = O.nv_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    ref = O.nv_layer_fwd(x, w_r, W1, W3, W2, k)
+    np.testing.assert_array_equal(got["y"], ref["y"])
+
+
+def test_nv_data_gradients_are_the_pinned_grouped_gemm():
+    # each data-gradient GEMM is the (exact-input pinned) grouped NVFP4 GEMM
+    # on the operands the backward defines: dy_perm against W2_e^T [H, F]
+    # (blocks along H), [dh1 | dh3] against [W1_e | W3_e]^T [2F, H] (blocks
+    # along 2F); the routed-row operand one tensor over all rows
+    x, w_r, W1, W3, W2, dO, k = _nv_train_case(5)
+    W2 = W2 * np.array([1.0, 8.0, 0.125, 1.0])[:, None, None]      # experts of different magnitudes
+    dO = dO * np.exp(np.random.default_rng(6).normal(0, 1, (dO.shape[0], 1)))
+    out = O.nv_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    off = out["offsets"]
+    E = len(off) - 1
+    da = O.nv_grouped_gemm(out["dy_perm"], off, [W2[e].T for e in range(E)], out_bf16=False)
+    np.testing.assert_allclose(out["da"], da, rtol=1e-12, atol=1e-12)
+    W13t = [np.concatenate([W1[e], W3[e]], axis=1).T for e in range(E)]
+    dxp = O.nv_grouped_gemm(out["dh13"], off, W13t)
+    np.testing.assert_allclose(out["dx_perm"], dxp, rtol=1e-12, atol=1e-12)
+    # and quantisation is present: the data gradients are not the plain products
+    plain = np.zeros_like(out["da"])
+    for e in range(E):
+        plain[off[e]:off[e + 1]] = out["dy_perm"][off[e]:off[e + 1]] @ W2[e].T
+    assert np.linalg.norm(out["da"] - plain) > 1e-2 * np.linalg.norm(plain)
+
+
+def test_nv_backward_tensor_scales_span_all_rows():
+    # one tensor scale over every routed row: an expert whose rows are 2^-24
+    # times the others' sits below the smallest E4M3 block scale and its
+    # quantised rows are zero (a scale per expert would keep them)
+    x, w_r, W1, W3, W2, dO, k = _nv_train_case(7, k=1)
+    rt = O.route(x, w_r, 1)
+    e_small = int(rt["topk_idx"][0, 0])
+    tok = rt["topk_idx"][:, 0] == e_small
+    # (a) dO of the expert's tokens tiny: dy_perm's blocks vanish, so does da
+    # (and dh13, dx_perm), while the bf16 weight gradient dW2 = a^T dy is not zero
+    dO_s = dO.copy()
+    dO_s[tok] *= 2.0 ** -24
+    out = O.nv_layer_bwd(x, w_r, W1, W3, W2, dO_s, 1)
+    lo, hi = int(out["offsets"][e_small]), int(out["offsets"][e_small + 1])
+    assert hi > lo
+    assert not out["da"][lo:hi].any() and not out["dx_perm"][lo:hi].any()
+    assert np.abs(out["dW2"][e_small]).max() > 0
+    assert np.abs(np.delete(out["da"], np.s_[lo:hi], axis=0)).max() > 0.1
+    # (b) the expert's W2_e tiny: dy_perm is as usual (its own weight tensor
+    # scale keeps Q(W2_e)), da is 2^-24 small, [dh1 | dh3]'s global scale zeroes
+    # those rows: dx_perm vanishes, the bf16 weight gradient dW1 does not
+    W2_s = W2.copy()
+    W2_s[e_small] *= 2.0 ** -24
+    out = O.nv_layer_bwd(x, w_r, W1, W3, W2_s, dO, 1)
+    assert np.abs(out["da"][lo:hi]).max() > 0
+    assert not out["dx_perm"][lo:hi].any()
+    assert np.abs(out["dW1"][e_small]).max() > 0
+
+
+def _rows_per_expert(v, offsets):
+    out = np.zeros(np.shape(v))
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            out[lo:hi] = O.nv_roundtrip(np.asarray(v[lo:hi], np.float32), axis=1)
+    return out
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("output_grad_roundtrip", _rows_per_expert),                      # dy_perm: a scale per expert
+    ("swiglu_grad_roundtrip", _rows_per_expert),                      # dh13: a scale per expert
+    ("dgrad_weight_roundtrip", lambda W: O.nv_roundtrip(np.asarray(W, np.float32), axis=0)),  # weight along N
+    ("output_grad_roundtrip", lambda v, off: O.nv_roundtrip(np.asarray(v, np.float32), axis=0)),  # along rows
+], ids=["dy_scale_per_expert", "dh_scale_per_expert", "weight_wrong_axis", "dy_wrong_axis"])
+def test_planted_nv_bwd_mistake_is_caught(monkeypatch, name, fn):
+    import oracle.nv_oracle as NV
+    monkeypatch.setattr(NV, name, fn)
+    with pytest.raises(AssertionError):
+        test_nv_data_gradients_are_the_pinned_grouped_gemm()
+        test_nv_backward_tensor_scales_span_all_rows()
