@@ -448,6 +448,61 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
                         const float* expert_bias, const float* logit_bias, const moe_nv_weights* w, void* y, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * NVFP4 training step. The report trains in NVFP4 (summary page, "Modeling";
+ * "Key Terms") without giving a recipe; the reading here follows the NVFP4
+ * forward: each data-gradient GEMM quantises both operands along its own
+ * contraction axis, the operand made of routed rows as ONE tensor (one tensor
+ * scale over every routed row), each expert's weight as a tensor of its own;
+ * the weight gradients stay bf16 x bf16 with fp32 output.
+ * ------------------------------------------------------------------------- */
+
+/* The data gradients' quantised weights (device buffers owned by the caller,
+ * sizes from moe_nv_bwd_weight_bytes, which = 0..5 in field order): w2h /
+ * sf2h / g2h are W2_e [F, H] row-wise along H (codes [E][F][H/2]; scales in
+ * the layout of moe_nv_quantize_weights with K = H, N = F); w13f / sf13f /
+ * g13f are [W1_e | W3_e] [H, 2F] row-wise along 2F, one tensor per expert
+ * (codes [E][H][F]: W1's F columns then W3's; K = 2F, N = H). */
+typedef struct {
+  uint8_t* w2h;
+  uint8_t* sf2h;
+  float* g2h;
+  uint8_t* w13f;
+  uint8_t* sf13f;
+  float* g13f;
+} moe_nv_bwd_weights;
+
+size_t moe_nv_bwd_weight_bytes(const moe_config* cfg, int which);
+
+/* Quantise W1, W3 [E,H,F] and W2 [E,F,H] bf16 into *w (the data gradients'
+ * weights). */
+int moe_nv_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                                const moe_nv_bwd_weights* w, void* stream);
+
+/* Workspace bytes of moe_layer_fwd_nvfp4_train / moe_layer_bwd_nvfp4 (one
+ * workspace serves both). 0 for an unsupported shape. */
+size_t moe_nv_train_workspace_bytes(const moe_config* cfg);
+
+/* NVFP4 layer forward that keeps what the backward needs: as
+ * moe_layer_fwd_nvfp4, with the router's logits (and aux partials when
+ * aux_coeff != 0), routing, x_perm (bf16 rows), h13 (the stored bf16 gate/up
+ * output), a and y_perm (bf16) written to *saved (all of them required). */
+int moe_layer_fwd_nvfp4_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                              const float* expert_bias, const float* logit_bias, const moe_nv_weights* w, void* y,
+                              const moe_fwd_saved* saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the NVFP4 layer for the loss <dO, y> + L_aux (outputs as in
+ * moe_layer_bwd, no shared expert): dy_perm = g dO (bf16); da = Q(dy_perm)
+ * Q(W2_e)^T (fp32, blocks along H); dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1)
+ * (bf16); dx_perm = Q([dh1 | dh3]) Q([W1_e | W3_e])^T (bf16, blocks along
+ * 2F); dW2 = a^T dy_perm, dW1 | dW3 = x_perm^T [dh1 | dh3] (bf16 operands,
+ * fp32); the router backward and dx as in moe_layer_bwd. `saved` is the one
+ * moe_layer_fwd_nvfp4_train filled, `ws` the same workspace. */
+int moe_layer_bwd_nvfp4(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
+                        const moe_nv_bwd_weights* w, const moe_fwd_saved* saved, void* dx, float* dW_router,
+                        float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws, size_t ws_bytes,
+                        void* stream);
+
 /* Synchronises `stream`, returns in *status_out the first device-side error
  * recorded in `ws` since the last read (MOE_OK if none) and clears it. For
  * tests and debugging; the hot path never calls it. */
@@ -478,9 +533,13 @@ void moe_debug_set_fault(int fault);
  * projection data gradient + SwiGLU backward, 13 down projection weight
  * gradient, 14 gate/up data gradient, 15 gate/up weight gradient, 16 router
  * data gradient, 17 permute backward, 18 router weight gradient, 19 aux loss,
- * 26-29 the shared expert's down data gradient + SwiGLU backward, down weight
- * gradient, gate/up data gradient, gate/up weight gradient; 30 moe_read_ceiling, 31
- * moe_write_ceiling).
+ * 20 NVFP4 quantisation of a GEMM's activations, 21 NVFP4 grouped GEMM, 22
+ * MXFP8 token-axis quantisation, 24 MXFP8 down data gradient + SwiGLU
+ * backward, 25 MXFP8 gate/up data gradient, 26-29 the shared expert's down
+ * data gradient + SwiGLU backward, down weight gradient, gate/up data
+ * gradient, gate/up weight gradient; 30 moe_read_ceiling, 31
+ * moe_write_ceiling; 32 NVFP4 down data gradient (da), 33 NVFP4 SwiGLU
+ * backward, 34 NVFP4 gate/up data gradient).
  * moe_profile_stop() stops recording. moe_profile_read() waits for the events
  * and returns their number; ms[i] is the time from event i-1 to event i
  * (0 for call starts). moe_debug_launch_count() returns the number of kernels

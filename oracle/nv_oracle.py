@@ -271,8 +271,8 @@ def nv_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
     every round trip the identity: the bf16 layer's backward on the same
     stored tensors. No shared expert. Returns the keys of the bf16 oracle's
     ``layer_bwd`` for the whole layer (dW1, dW3, dW2 as dicts over every
-    expert) and, for the pins, the row-space tensors "dy_perm", "da",
-    "dh13" and "dx_perm"."""
+    expert) and, for the pins and tolerances, the row-space tensors "h13",
+    "dy_perm", "da", "dh13" and "dx_perm"."""
     x = np.asarray(x, np.float64)
     dO = np.asarray(dO, np.float64)
     T, H = x.shape
@@ -342,7 +342,7 @@ def nv_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
         dx += dx_perm[row[:, i]]
     res = {**rt, "counts": counts, "offsets": offsets, "row_id_map": row, "y": prec.r("y", y), "dgate": dgate,
            "dW1": dW1, "dW3": dW3, "dW2": dW2, "dlogits": dL, "dx": prec.r("dx", dx), "dW_r": dL.T @ x,
-           "dy_perm": dy, "da": da, "dh13": dh, "dx_perm": dx_perm}
+           "h13": h, "dy_perm": dy, "da": da, "dh13": dh, "dx_perm": dx_perm}
     if aux:
         res["aux_loss"] = aux_loss(softmax(rt["logits"]), counts, k, aux)
     return res

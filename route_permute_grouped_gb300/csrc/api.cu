@@ -45,6 +45,7 @@ enum StageTag : int {
   STAGE_NV_QUANT = 20, STAGE_NV_GEMM = 21,
   STAGE_MX_QUANT_TOK = 22, STAGE_MX_DGRAD2 = 24, STAGE_MX_DGRAD1 = 25,
   STAGE_SHARED_DGRAD2 = 26, STAGE_SHARED_WGRAD2 = 27, STAGE_SHARED_DGRAD1 = 28, STAGE_SHARED_WGRAD13 = 29,
+  STAGE_NV_DGRAD2 = 32, STAGE_NV_SWIGLU_BWD = 33, STAGE_NV_DGRAD1 = 34,
 };
 // MOE_DEBUG_SYNC=1 in the environment: synchronise after every stage and
 // report the first stage whose kernels failed (debugging aid, off by default).
@@ -181,9 +182,10 @@ struct WsLayout {
   // transposed token-axis operands of the weight gradients (A, B) with their
   // scales and the padded token offsets
   size_t dy_q, sfa_dy, dh_q, sfa_dh, tok_a, sf_a, tok_b, sf_b, pad_off;
-  // NVFP4 forward: codes and scales of the current GEMM's activations
-  // (x_perm, then a), their two tensor scales
-  size_t nv_q, nv_sf, nv_g;
+  // NVFP4: codes and scales of the current GEMM's activations (x_perm, then
+  // a; training: then dy_perm, then dh13), their tensor scales (x, a, dy,
+  // dh13); training: da (fp32)
+  size_t nv_q, nv_sf, nv_g, nv_da;
   size_t total;
 };
 
@@ -240,14 +242,16 @@ static WsLayout ws_layout(const moe_config& c, bool training, bool mx = false, b
     }
   } else {
     if (!nv) L.x_perm = take(2 * R * H);  // the NVFP4 permute writes codes only
-    L.a = take(2 * R * F);
+    if (!(nv && training)) L.a = take(2 * R * F);  // NVFP4 training: a lives in the saved buffers
   }
   if (nv) {
-    L.nv_q = take(R * (H > F ? H : F) / 2);
-    const size_t sx = nv_act_sf_bytes(static_cast<long long>(R), c.E, c.H);
-    const size_t sa = nv_act_sf_bytes(static_cast<long long>(R), c.E, c.F);
-    L.nv_sf = take(sx > sa ? sx : sa);
-    L.nv_g = take(2 * sizeof(float));
+    // the widest activation operand: x_perm or a (H or F columns); training
+    // also dh13 (2F)
+    const size_t kq = training ? (H > 2 * F ? H : 2 * F) : (H > F ? H : F);
+    L.nv_q = take(R * kq / 2);
+    L.nv_sf = take(nv_act_sf_bytes(static_cast<long long>(R), c.E, static_cast<int>(kq)));
+    L.nv_g = take(4 * sizeof(float));
+    if (training) L.nv_da = take(4 * R * F);
   }
   L.y_perm = take(inter * R * H);
   L.as = c.F_shared ? take(2 * T * c.F_shared) : 0;
@@ -559,10 +563,11 @@ static int run_wgrad_mx(const moe_config& c, const int32_t* offsets, int R, cons
                                  static_cast<int>(tiles < num_sms() ? tiles : num_sms()), s, &mo, &msb));
 }
 
-// NVFP4 grouped GEMM on quantised activations: y [R, N] bf16 = g_x g_e (Q(x) Q(W_e))
+// NVFP4 grouped GEMM on quantised activations: y [R, N] = g_x g_e (Q(x) Q(W_e)),
+// bf16 (fp32 with out_fp32)
 static int run_gemm_nv(int E, long long R, int K, int N, const int32_t* offsets, const uint8_t* xq,
                        const uint8_t* sfx, const float* gx, const uint8_t* wq, const uint8_t* sf, const float* g,
-                       __nv_bfloat16* y, DevStatus* st, cudaStream_t s) {
+                       void* y, DevStatus* st, cudaStream_t s, bool out_fp32 = false) {
   moe_config c{};
   c.T = 1; c.H = N; c.E = E; c.k = 1; c.F = K;
   GemmParams p = base_params(c, st);
@@ -575,6 +580,7 @@ static int run_gemm_nv(int E, long long R, int K, int N, const int32_t* offsets,
   p.nt_w = p.n_tiles;
   p.kb_total = K / kNvKB;
   p.out0 = y;
+  p.out_fp32 = out_fp32 ? 1 : 0;
   p.nv_ga = gx;
   p.nv_gb = g;
   CUtensorMap ma, mb, msa, msb, oy;
@@ -582,7 +588,7 @@ static int run_gemm_nv(int E, long long R, int K, int N, const int32_t* offsets,
   if (!make_map_u8(&mb, wq, K / 2, static_cast<uint64_t>(E) * N, 128, kNvTileN / 2)) return MOE_ERR_CUDA;
   if (!make_map_u8(&msa, sfx, 256, nv_act_sf_bytes(R, E, K) / 256, 256, 8, false)) return MOE_ERR_CUDA;
   if (!make_map_u8(&msb, sf, 256, nv_weight_sf_bytes(E, K, N) / 256, 256, 16, false)) return MOE_ERR_CUDA;
-  if (!make_map_store(&oy, y, N, R, false)) return MOE_ERR_CUDA;
+  if (!make_map_store(&oy, y, N, R, out_fp32)) return MOE_ERR_CUDA;
   return cuda_status(launch_gemm(KIND_GEMM_NV, p, ma, mb, msa, num_sms(), s, &oy, &msb));
 }
 
@@ -894,7 +900,7 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
                           void* ws, const WsLayout& L, const moe_mx_bwd_weights* mx, cudaStream_t s,
                           bool mx_wgrad = false, const moe_bf16* Ws1 = nullptr, const moe_bf16* Ws3 = nullptr,
                           const moe_bf16* Ws2 = nullptr, float* dWs1 = nullptr, float* dWs3 = nullptr,
-                          float* dWs2 = nullptr) {
+                          float* dWs2 = nullptr, const moe_nv_bwd_weights* nv = nullptr) {
   // memory-saving backward: a recomputed from h13, gate gradient from the dgrad
   const bool recompute = mx == nullptr && saved->a == nullptr;
   DevStatus* st = at<DevStatus>(ws, 0);
@@ -944,7 +950,27 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
                              n_part, saved->row_id_map, saved->counts, Ep, dL_hl, s, st));
   stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
-  if (mx != nullptr) {
+  if (nv != nullptr) {
+    // NVFP4: dy_perm quantised as one tensor (blocks along H); da = Q(dy_perm)
+    // Q(W2_e)^T in fp32; the SwiGLU backward -> dh13 (bf16) and its maximum;
+    // dh13 quantised as one tensor (blocks along 2F) for step 5
+    uint8_t* q = at<uint8_t>(ws, L.nv_q);
+    uint8_t* sfq = at<uint8_t>(ws, L.nv_sf);
+    float* gq = at<float>(ws, L.nv_g);
+    float* da = at<float>(ws, L.nv_da);
+    const int32_t* n_rows = saved->offsets + c.E;
+    MOE_CUDA(launch_nv_amax_rows(dy_perm, R, c.H, n_rows, gq + 2, s));
+    MOE_CUDA(launch_nv_quantize_grouped(dy_perm, R, c.H, c.E, saved->offsets, gq + 2, q, sfq, s));
+    stage_done(s, STAGE_NV_QUANT, 3);
+    MOE_TRY(run_gemm_nv(c.E, R, c.H, c.F, saved->offsets, q, sfq, gq + 2, nv->w2h, nv->sf2h, nv->g2h, da, st, s,
+                        true));
+    stage_done(s, STAGE_NV_DGRAD2, 1);
+    MOE_CUDA(launch_nv_swiglu_bwd(da, reinterpret_cast<const __nv_bfloat16*>(saved->h13), R, c.F, n_rows, dh13,
+                                  gq + 3, s));
+    stage_done(s, STAGE_NV_SWIGLU_BWD, 2);
+    MOE_CUDA(launch_nv_quantize_grouped(dh13, R, 2 * c.F, c.E, saved->offsets, gq + 3, q, sfq, s));
+    stage_done(s, STAGE_NV_QUANT, 1);
+  } else if (mx != nullptr) {
     // MXFP8: da = Q(dy_perm) Q(W2_e)^T with the SwiGLU backward in the GEMM's
     // epilogue -> dh13 bf16, a (for dW2) and the E4M3 rows of dh13 (blocks
     // along 2F)
@@ -989,7 +1015,11 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     stage_done(s, STAGE_WGRAD2, 2);
   }
   // 5. dx_perm = dh13 [W1_e | W3_e]^T
-  if (mx != nullptr) {
+  if (nv != nullptr) {
+    MOE_TRY(run_gemm_nv(c.E, R, 2 * c.F, c.H, saved->offsets, at<uint8_t>(ws, L.nv_q), at<uint8_t>(ws, L.nv_sf),
+                        at<float>(ws, L.nv_g) + 3, nv->w13f, nv->sf13f, nv->g13f, dx_perm, st, s));
+    stage_done(s, STAGE_NV_DGRAD1, 1);
+  } else if (mx != nullptr) {
     MOE_TRY(run_gemm_mx(c, saved->offsets, R, 2 * c.F, c.H, at<uint8_t>(ws, L.dh_q), at<uint8_t>(ws, L.sfa_dh),
                         mx->w13f, mx->sf13f, mx_sf13f_bytes(c), dx_perm, st, s));
     stage_done(s, STAGE_MX_DGRAD1, 1);
@@ -1518,13 +1548,156 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_CUDA(launch_nv_scale_from_amax(gq + 1, 1, s));
   stage_done(s, STAGE_FFN1, 2);
   MOE_CUDA(launch_nv_quantize_grouped(a, static_cast<int>(R), c.F, c.E, offs, gq + 1, q, sfq, s));
-  stage_done(s, STAGE_NV_QUANT, 3);
+  stage_done(s, STAGE_NV_QUANT, 1);
   MOE_TRY(run_gemm_nv(c.E, R, c.F, c.H, offs, q, sfq, gq + 1, w->w2, w->sf2, w->g2,
                       reinterpret_cast<__nv_bfloat16*>(yp), st, s));
   stage_done(s, STAGE_FFN2, 1);
   MOE_CUDA(launch_combine(c, yp, rows, gate, nullptr, y, s, st));
   stage_done(s, STAGE_COMBINE, 1);
   return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 training step
+// ---------------------------------------------------------------------------
+size_t moe_nv_bwd_weight_bytes(const moe_config* cfg, int which) {
+  if (check_cfg(cfg) != MOE_OK || check_nv_layer_shape(*cfg) != MOE_OK) return 0;
+  const moe_config& c = *cfg;
+  switch (which) {
+    case 0: return moe_nv_weight_bytes(c.E, c.H, c.F, 0);      // W2_e rows along H: K = H, N = F
+    case 1: return moe_nv_weight_bytes(c.E, c.H, c.F, 1);
+    case 2: return moe_nv_weight_bytes(c.E, c.H, c.F, 2);
+    case 3: return moe_nv_weight_bytes(c.E, 2 * c.F, c.H, 0);  // [W1_e | W3_e] rows along 2F: K = 2F, N = H
+    case 4: return moe_nv_weight_bytes(c.E, 2 * c.F, c.H, 1);
+    case 5: return moe_nv_weight_bytes(c.E, 2 * c.F, c.H, 2);
+    default: return 0;
+  }
+}
+
+int moe_nv_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                                const moe_nv_bwd_weights* w, void* stream) {
+  NvtxRange nvtx("moe_nv_quantize_bwd_weights");
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_nv_layer_shape(c));
+  if (!W1 || !W3 || !W2 || !w || !w->w2h || !w->sf2h || !w->g2h || !w->w13f || !w->sf13f || !w->g13f)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w2h) || !aligned16(w->sf2h) ||
+      !aligned16(w->w13f) || !aligned16(w->sf13f))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* w1 = reinterpret_cast<const __nv_bfloat16*>(W1);
+  const __nv_bfloat16* w3 = reinterpret_cast<const __nv_bfloat16*>(W3);
+  const __nv_bfloat16* w2 = reinterpret_cast<const __nv_bfloat16*>(W2);
+  // W2_e [F, H] row-wise along H, one tensor per expert
+  MOE_CUDA(launch_nv_amax(w2, static_cast<long long>(c.F) * c.H, c.E, w->g2h, s));
+  MOE_CUDA(launch_nv_quantize_weight_rows(w2, c.E, c.H, c.F, w->g2h, w->w2h, w->sf2h, s));
+  // [W1_e | W3_e] [H, 2F] row-wise along 2F, one tensor per expert
+  MOE_CUDA(launch_nv_amax(w1, static_cast<long long>(c.H) * c.F, c.E, w->g13f, s, w3));
+  MOE_CUDA(launch_nv_quantize_weight_rows(w1, c.E, 2 * c.F, c.H, w->g13f, w->w13f, w->sf13f, s, w3, c.F));
+  count_launches(7);
+  return MOE_OK;
+}
+
+size_t moe_nv_train_workspace_bytes(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK || check_nv_layer_shape(*cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg, true, false, true).total;
+}
+
+static bool nv_saved_ok(const moe_config& c, const moe_fwd_saved* sv) {
+  return sv && sv->topk_idx && sv->topk_gate && sv->logits && sv->row_id_map && sv->counts && sv->offsets &&
+         sv->x_perm && sv->h13 && sv->a && sv->y_perm && (c.aux_coeff == 0.0f || sv->aux_partials) &&
+         aligned16(sv->x_perm) && aligned16(sv->h13) && aligned16(sv->a) && aligned16(sv->y_perm);
+}
+
+int moe_layer_fwd_nvfp4_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
+                              const float* expert_bias, const float* logit_bias, const moe_nv_weights* w, void* y,
+                              const moe_fwd_saved* saved, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("moe_layer_fwd_nvfp4_train");
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_nv_layer_shape(c));
+  if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->g13 || !w->w2 || !w->sf2 || !w->g2 || !y || !ws ||
+      !nv_saved_ok(c, saved))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
+      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, true, false, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  const moe_fwd_saved& sv = *saved;
+  const long long R = static_cast<long long>(c.T) * c.k;
+  uint8_t* q = at<uint8_t>(ws, L.nv_q);
+  uint8_t* sfq = at<uint8_t>(ws, L.nv_sf);
+  float* gq = at<float>(ws, L.nv_g);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  prof_mark(s, STAGE_BEGIN);
+  MOE_TRY(run_router(c, xb, reinterpret_cast<const __nv_bfloat16*>(router_w), expert_bias, logit_bias, sv.topk_idx,
+                     sv.topk_gate, sv.logits, c.aux_coeff != 0.0f ? sv.aux_partials : nullptr, st, s));
+  stage_done(s, STAGE_ROUTER, 1);
+  // the permute quantises the routed rows (x's tensor scale) and scatters
+  // their bf16 copies for the weight gradient
+  MOE_CUDA(launch_nv_amax(xb, static_cast<long long>(c.T) * c.H, 1, gq, s));
+  MOE_CUDA(launch_permute(c, xb, sv.topk_idx, reinterpret_cast<__nv_bfloat16*>(sv.x_perm), sv.row_id_map, sv.counts,
+                          sv.offsets, at<int32_t>(ws, L.lookback), st, s, q, sfq, gq));
+  stage_done(s, STAGE_PERMUTE, 4);
+  MOE_CUDA(cudaMemsetAsync(gq + 1, 0, sizeof(float), s));
+  {
+    GemmParams p = base_params(c, st);
+    p.F = c.F;
+    p.ngroups = c.E;
+    p.offsets = sv.offsets;
+    p.M_total = static_cast<int>(R);
+    p.bn = kNvTileN;
+    p.n_tiles = (c.F + kMxTileF1 - 1) / kMxTileF1;
+    p.nt_w = p.n_tiles;
+    p.kb_total = c.H / kNvKB;
+    p.out0 = sv.a;
+    p.out1 = sv.h13;
+    p.nv_ga = gq;
+    p.nv_gb = w->g13;
+    p.nv_amax = reinterpret_cast<unsigned*>(gq + 1);
+    CUtensorMap ma, mb, msa, msb;
+    if (!make_map_u8(&ma, q, c.H / 2, R, 128, kBM)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&mb, w->w13, c.H / 2, 2ull * c.E * c.F, 128, kMxTileF1)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&msa, sfq, 256, nv_act_sf_bytes(R, c.E, c.H) / 256, 256, 8, false)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&msb, w->sf13, 256, nv_weight_sf_bytes_gu(c.E, c.H, c.F) / 256, 256, 16, false))
+      return MOE_ERR_CUDA;
+    MOE_CUDA(launch_gemm(KIND_FFN1_NV, p, ma, mb, msa, num_sms(), s, nullptr, &msb));
+  }
+  MOE_CUDA(launch_nv_scale_from_amax(gq + 1, 1, s));
+  stage_done(s, STAGE_FFN1, 2);
+  MOE_CUDA(launch_nv_quantize_grouped(reinterpret_cast<const __nv_bfloat16*>(sv.a), static_cast<int>(R), c.F, c.E,
+                                      sv.offsets, gq + 1, q, sfq, s));
+  stage_done(s, STAGE_NV_QUANT, 1);
+  MOE_TRY(run_gemm_nv(c.E, R, c.F, c.H, sv.offsets, q, sfq, gq + 1, w->w2, w->sf2, w->g2, sv.y_perm, st, s));
+  stage_done(s, STAGE_FFN2, 1);
+  MOE_CUDA(launch_combine(c, sv.y_perm, sv.row_id_map, sv.topk_gate, nullptr, y, s, st));
+  stage_done(s, STAGE_COMBINE, 1);
+  return MOE_OK;
+}
+
+int moe_layer_bwd_nvfp4(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, const moe_bf16* router_w,
+                        const moe_nv_bwd_weights* w, const moe_fwd_saved* saved, void* dx, float* dW_router,
+                        float* dW1, float* dW3, float* dW2, float* aux_loss_out, void* ws, size_t ws_bytes,
+                        void* stream) {
+  NvtxRange nvtx("moe_layer_bwd_nvfp4");
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_nv_layer_shape(c));
+  if (!dO || !x || !router_w || !w || !w->w2h || !w->sf2h || !w->g2h || !w->w13f || !w->sf13f || !w->g13f ||
+      !nv_saved_ok(c, saved) || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dO) || !aligned16(x) || !aligned16(router_w) || !aligned16(w->w2h) || !aligned16(w->w13f) ||
+      !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, true, false, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return layer_bwd_core(c, dO, x, router_w, nullptr, nullptr, nullptr, saved, dx, dW_router, dW1, dW3, dW2,
+                        aux_loss_out, ws, L, nullptr, static_cast<cudaStream_t>(stream), false, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, nullptr, w);
 }
 
 }  // extern "C"

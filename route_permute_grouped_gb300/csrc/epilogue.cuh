@@ -152,6 +152,10 @@ __device__ __forceinline__ void epi_store_tma(const TileInfo& ti, uint32_t tacc,
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = 0.0f;
       }
+      if (alpha != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] *= alpha;
+      }
       uint8_t* buf = st.next(lane);
       stage_f32x32(buf, lane, f);
       if (THREE_D) st.commit3d(lane, map, buf, col, row0, ti.g);

@@ -145,8 +145,9 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
 // NVFP4 gate/up epilogue, thread = row r of this CTA's 128 rows of the pair
 // tile, block b (0..2) of the tile's 96 F columns: h = bf16(g_x g_e acc) for
 // the gate (columns 32 b..) and up (96 + 32 b..) halves, a = bf16(SiLU(h1) h3)
-// stored to a[row, col..] (rows of this expert only), and max |a| of the
-// warp's rows into *nv_amax.
+// stored to a[row, col..] (rows of this expert only), h stored to out1
+// [rows, 2F] when set (training), and max |a| of the warp's rows into
+// *nv_amax.
 __device__ __forceinline__ void epi_ffn1_nv(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r, int b) {
   const int col = ti.n0 + 32 * b;
   if (col >= p.F) return;  // uniform: the last tile of a ragged F
@@ -175,6 +176,16 @@ __device__ __forceinline__ void epi_ffn1_nv(const GemmParams& p, const TileInfo&
     uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(row) * p.F + col);
 #pragma unroll
     for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    if (p.out1 != nullptr) {  // training: the stored h1, h3 (bf16) for the backward
+      __nv_bfloat16* h13 = reinterpret_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(row) * 2 * p.F + col;
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = alpha * __uint_as_float(v1[j]);
+      store_bf16x32(h13, f);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = alpha * __uint_as_float(v3[j]);
+      store_bf16x32(h13 + p.F, f);
+    }
   } else {
     m = 0.0f;
   }
@@ -810,9 +821,14 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         epi_ffn1_nv(p, ti, tacc, r, part);
       } else if constexpr (KIND == KIND_GEMM_NV) {
         // y = g_x g_e (sum of the block-scaled products)
+        // (fp32 out: the data gradient da of the NVFP4 training step)
         const float alpha = __ldg(p.nv_ga) * __ldg(p.nv_gb + ti.g);
-        if (full_rows) epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0, kNvTileN / 64, alpha);
-        else if (any_rows) epi_store(ti, tacc, r, kNvTileN / 32, p.H, p.H, p.out0, false, 0, alpha);
+        if (full_rows) {
+          if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0, kNvTileN / 64, alpha);
+          else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0, kNvTileN / 64, alpha);
+        } else if (any_rows) {
+          epi_store(ti, tacc, r, kNvTileN / 32, p.H, p.H, p.out0, p.out_fp32 != 0, 0, alpha);
+        }
       } else if constexpr (KIND == KIND_ROUTER) {
         // score, selection, gates (and aux statistics, logits) per token
         const RouterSmem rsm(smem + SL::kOutOff);

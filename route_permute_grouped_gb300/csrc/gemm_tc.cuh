@@ -51,7 +51,7 @@ enum GemmKind : int {
   KIND_FFN1_MX = 9,    // MXFP8 gate/up: h = Q(x_perm) [Q(W1_e) | Q(W3_e)] -> a = SiLU(h1) h3, stored as MXFP8
                        // (codes + the down GEMM's tile-ready scales); 256 x (96 gate + 96 up) pair tiles
   KIND_FFN2_MX = 10,   // MXFP8 down: y_perm = Q(a) Q(W2_e), bf16 out; 256 x 192 pair tiles
-  KIND_GEMM_NV = 11,   // NVFP4 grouped expert GEMM: y = g_x g_e Q(x_e) Q(W_e), bf16 out; 256 x 192 pair tiles
+  KIND_GEMM_NV = 11,   // NVFP4 grouped expert GEMM: y = g_x g_e Q(x_e) Q(W_e), bf16 or fp32 out; 256 x 192 pair tiles
   KIND_FFN1_NV = 12,   // NVFP4 gate/up: h = g_x g_e Q(x_perm) Q([W1_e | W3_e]) -> a = bf16(SiLU(h1) h3) and max |a|;
                        // 256 x (96 gate + 96 up) pair tiles
   KIND_DGRAD2_MX = 13, // MXFP8 down-projection data gradient: da = Q(dy_perm) Q(W2_e)^T -> SwiGLU backward ->

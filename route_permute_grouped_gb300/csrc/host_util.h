@@ -141,6 +141,19 @@ cudaError_t launch_nv_quantize_weights(const __nv_bfloat16* w, int E, int K, int
                                        int split = 0);
 cudaError_t launch_nv_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
                                        const float* g, uint8_t* xq, uint8_t* sf, cudaStream_t st);
+// tensor scale of the first *n_rows rows (cols elements each, at most
+// max_rows) of x, into *out
+cudaError_t launch_nv_amax_rows(const __nv_bfloat16* x, long long max_rows, int cols, const int32_t* n_rows,
+                                float* out, cudaStream_t st);
+// row-major weights W[E][N][K] (columns [split, K) from w_hi [E][N][K - split])
+// -> K-major codes and tile-ready scales as launch_nv_quantize_weights' plain layout
+cudaError_t launch_nv_quantize_weight_rows(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,
+                                           uint8_t* sf, cudaStream_t st, const __nv_bfloat16* w_hi = nullptr,
+                                           int split = 0);
+// dh13 = SwiGLU backward of da (fp32 [R, F]) on the saved h13 (first *n_rows
+// rows), its tensor scale into *g
+cudaError_t launch_nv_swiglu_bwd(const float* da, const __nv_bfloat16* h13, int R, int F, const int32_t* n_rows,
+                                 __nv_bfloat16* dh13, float* g, cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,
                                     cudaStream_t st);
 cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16* W1, const __nv_bfloat16* W3,

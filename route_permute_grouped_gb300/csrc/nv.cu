@@ -1,18 +1,27 @@
 // NVFP4 quantisers (see nv.cuh for the format and the scale layout): tensor
-// maxima, row-major blocks of a bf16 matrix, expert weights transposed to
-// K-major codes with tile-ready scales, and the grouped rows of an expert
-// GEMM's activations with tile-ready scales per 256-row pair tile.
+// maxima, row-major blocks of a bf16 matrix, expert weights (transposed, or
+// row-wise for the data gradients) to K-major codes with tile-ready scales,
+// and the grouped rows of an expert GEMM's activations with tile-ready scales
+// per 256-row pair tile; and the SwiGLU backward of the NVFP4 training step.
 #include "host_util.h"
 #include "nv.cuh"
 
 namespace moe {
 
 // out[grp] = bits of max |x| over group grp's n_per elements (non-negative
-// fp32 values order like their bit patterns); 8 elements per 16-byte load
+// fp32 values order like their bit patterns); 8 elements per 16-byte load.
+// With lim_rows set (one group), only the first *lim_rows rows of `cols`
+// elements count.
 __global__ void __launch_bounds__(256) nv_amax_kernel(const __nv_bfloat16* __restrict__ x, long long n_per,
-                                                      unsigned* __restrict__ out) {
+                                                      unsigned* __restrict__ out,
+                                                      const int32_t* __restrict__ lim_rows = nullptr,
+                                                      long long cols = 0) {
   const uint4* base = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.y) * n_per);
-  const long long nv = n_per / 8;
+  long long nv = n_per / 8;
+  if (lim_rows != nullptr) {
+    const long long lim = static_cast<long long>(max(__ldg(lim_rows), 0)) * cols / 8;
+    nv = lim < nv ? lim : nv;
+  }
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   float m = 0.0f;
   // four independent 16-byte loads in flight per thread
@@ -149,6 +158,94 @@ __global__ void __launch_bounds__(256) nv_quantize_grouped_kernel(const __nv_bfl
       static_cast<uint8_t>(sb);
 }
 
+// Weights stored row-major W[E][N][K] (row n of expert e holds the K
+// elements of one GEMM output column; columns [split, K) come from a second
+// weight w_hi [E][N][K - split]) -> codes wq[E][N][K/2] and the scales in the
+// tile-ready layout of nv_quantize_weight_kernel (B row b = n % 192 of tile
+// n / 192), tensor scale g[e]; thread = one (e, n, kb16): two 16-byte loads,
+// consecutive threads on consecutive blocks of a row. The data gradients read
+// their weights this way: W2_e [F, H] along H, [W1_e | W3_e] [H, 2F] along 2F.
+__global__ void __launch_bounds__(256) nv_quantize_weight_rows_kernel(const __nv_bfloat16* __restrict__ w,
+                                                                      const __nv_bfloat16* __restrict__ w_hi,
+                                                                      int split, int E, int K, int N,
+                                                                      const float* __restrict__ g,
+                                                                      uint8_t* __restrict__ wq,
+                                                                      uint8_t* __restrict__ sf) {
+  const int nkb16 = K / kNvBlock;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(E) * N * nkb16) return;
+  const int kb16 = static_cast<int>(i % nkb16);
+  const long long r = i / nkb16;
+  const int n = static_cast<int>(r % N);
+  const int e = static_cast<int>(r / N);
+  const int k0 = kb16 * kNvBlock;
+  const bool hi = k0 >= split;
+  const int ld = hi ? K - split : split;
+  const __nv_bfloat16* src =
+      (hi ? w_hi : w) + (static_cast<size_t>(e) * N + n) * static_cast<size_t>(ld) + (hi ? k0 - split : k0);
+  float v[16];
+  load_bf16x16(src, v);
+  uint32_t c[2];
+  const uint32_t sb = nv_quant16(v, g[e], c);
+  *reinterpret_cast<uint2*>(wq + (static_cast<size_t>(e) * N + n) * (K / 2) + static_cast<size_t>(kb16) * 8) =
+      make_uint2(c[0], c[1]);
+  const int ntiles = (N + kNvTileN - 1) / kNvTileN;
+  const int tile = n / kNvTileN, b = n % kNvTileN;
+  const size_t blk = (static_cast<size_t>(e) * ntiles + tile) * (K / kNvKB) + kb16 / 16;
+  sf[blk * 2 * kNvSfBytes + (b >> 7) * kNvSfBytes + nv_sf_pos(b & 127, kb16 & 15)] = static_cast<uint8_t>(sb);
+}
+
+// SwiGLU backward of the NVFP4 training step; thread = 8 columns f.. of row r
+// (rows below *n_rows, the routed rows): da fp32 [R, F] and the saved bf16
+// pre-activations h13 [R, 2F] (h1 | h3) give dh1 = da h3 SiLU'(h1) and
+// dh3 = da SiLU(h1), stored bf16 to dh13 [R, 2F] (h1's columns then h3's), and
+// the largest magnitude of the stored values into *amax_bits.
+__global__ void __launch_bounds__(256) nv_swiglu_bwd_kernel(const float* __restrict__ da,
+                                                            const __nv_bfloat16* __restrict__ h13, int R, int F,
+                                                            const int32_t* __restrict__ n_rows,
+                                                            __nv_bfloat16* __restrict__ dh13,
+                                                            unsigned* __restrict__ amax_bits) {
+  const int nv = F / 8;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int rows = min(R, max(__ldg(n_rows), 0));
+  float m = 0.0f;
+  if (i < static_cast<long long>(rows) * nv) {
+    const long long r = i / nv;
+    const int c = static_cast<int>(i - r * nv) * 8;
+    const float4* dp = reinterpret_cast<const float4*>(da + r * F + c);
+    const float4 d0 = __ldg(dp), d1 = __ldg(dp + 1);
+    const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    const __nv_bfloat16* hr = h13 + r * 2 * F;
+    const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(hr + c));
+    const uint4 v3 = __ldg(reinterpret_cast<const uint4*>(hr + F + c));
+    const uint32_t a1[4] = {v1.x, v1.y, v1.z, v1.w};
+    const uint32_t a3[4] = {v3.x, v3.y, v3.z, v3.w};
+    uint32_t o1[4], o3[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float d1v[2], d3v[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float x1 = u ? bf16_hi(a1[q]) : bf16_lo(a1[q]);
+        const float x3 = u ? bf16_hi(a3[q]) : bf16_lo(a3[q]);
+        const float s = 1.0f / (1.0f + __expf(-x1));
+        d1v[u] = d[2 * q + u] * x3 * (s * (1.0f + x1 * (1.0f - s)));
+        d3v[u] = d[2 * q + u] * x1 * s;
+      }
+      o1[q] = pack_bf16x2(d1v[0], d1v[1]);
+      o3[q] = pack_bf16x2(d3v[0], d3v[1]);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(o1[q])), fabsf(bf16_hi(o1[q]))),
+                         fmaxf(fabsf(bf16_lo(o3[q])), fabsf(bf16_hi(o3[q])))));
+    }
+    __nv_bfloat16* orow = dh13 + r * 2 * F;
+    *reinterpret_cast<uint4*>(orow + c) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    *reinterpret_cast<uint4*>(orow + F + c) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(amax_bits, __float_as_uint(m));
+}
+
 cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, float* out_bits, cudaStream_t st,
                            const __nv_bfloat16* x2) {
   cudaError_t e = cudaMemsetAsync(out_bits, 0, sizeof(float) * groups, st);
@@ -171,6 +268,46 @@ cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   nv_scale_from_amax_kernel<<<(groups + 255) / 256, 256, 0, st>>>(out_bits, groups);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_amax_rows(const __nv_bfloat16* x, long long max_rows, int cols, const int32_t* n_rows,
+                                float* out, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  long long blocks = (max_rows * cols / 8 + 255) / 256;
+  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+  if (blocks < 1) blocks = 1;
+  nv_amax_kernel<<<dim3(static_cast<unsigned>(blocks), 1), 256, 0, st>>>(x, max_rows * cols,
+                                                                       reinterpret_cast<unsigned*>(out), n_rows, cols);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  nv_scale_from_amax_kernel<<<1, 32, 0, st>>>(out, 1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_quantize_weight_rows(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,
+                                           uint8_t* sf, cudaStream_t st, const __nv_bfloat16* w_hi, int split) {
+  cudaError_t e = cudaMemsetAsync(sf, 0, nv_weight_sf_bytes(E, K, N), st);
+  if (e != cudaSuccess) return e;
+  const long long n = static_cast<long long>(E) * N * (K / kNvBlock);
+  nv_quantize_weight_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+      w, w_hi, w_hi != nullptr ? split : K, E, K, N, g, wq, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_swiglu_bwd(const float* da, const __nv_bfloat16* h13, int R, int F, const int32_t* n_rows,
+                                 __nv_bfloat16* dh13, float* g, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const long long n = static_cast<long long>(R) * (F / 8);
+  if (n > 0) {
+    nv_swiglu_bwd_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(da, h13, R, F, n_rows, dh13,
+                                                                                reinterpret_cast<unsigned*>(g));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  nv_scale_from_amax_kernel<<<1, 32, 0, st>>>(g, 1);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,22 @@ __device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
   *reinterpret_cast<volatile int32_t*>(p) = static_cast<int32_t>(v);
 }
 
+// training scatter with quantised rows: the bf16 copies of token t's row too
+// (for the weight gradient), 16-byte vectors, lane l taking vectors l, l + 32,
+// ... (the row is in cache); rows[i] < 0: slot dropped
+__device__ __forceinline__ void scatter_row_bf16(const __nv_bfloat16* __restrict__ x,
+                                                 __nv_bfloat16* __restrict__ x_perm, int t, int H, const int* rows,
+                                                 int k, int lane) {
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  for (int vv = lane; vv < H / 8; vv += 32) {
+    const uint4 w = __ldg(src + vv);
+    for (int i = 0; i < k; ++i) {
+      const int r = rows[i];
+      if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H)[vv] = w;
+    }
+  }
+}
+
 // One CTA per chunk of 64 tokens, chunks taken in ticket order (so every
 // earlier chunk has started when a CTA looks back). For expert e the row of
 // (t,i) is offsets[e] + (rows of e in earlier chunks) + (rank of t among this
@@ -67,10 +83,10 @@ __device__ __forceinline__ void st_volatile_u32(int32_t* p, uint32_t v) {
 // step j % 4): the blocks the CTA pairs of the expert GEMM read. With x_perm
 // non-null (training) the bf16 rows are scattered as well.
 //
-// NV (MX false, nv_g != nullptr): the rows are NVFP4 with the tensor scale
-// *nv_g: 16-element blocks quantised once per token, codes (two per byte) to
-// every destination row, scales to the same pair-tile blocks (2 KB per 128
-// rows and k block of 256).
+// NV (the MX instance with nv_g != nullptr): the rows are NVFP4 with the
+// tensor scale *nv_g: 16-element blocks quantised once per token, codes (two
+// per byte) to every destination row, scales to the same pair-tile blocks (2 KB
+// per 128 rows and k block of 256); the bf16 rows too with x_perm non-null.
 template <bool MX>
 __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx, int T, int H, int E, int k,
@@ -215,6 +231,7 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
           sfa[(static_cast<size_t>(blk) * nkb + b / 16) * kNvSfBytes + nv_sf_pos(rel % kBM, b & 15)] = sb;
         }
       }
+      if (x_perm != nullptr) scatter_row_bf16(x, x_perm, t, H, s_rows + j * k, k, lane);
     }
     return;
   }
@@ -252,18 +269,7 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_scatter_kernel(
           sfa[(static_cast<size_t>(blk) * nkb + b / 4) * kMxSfBytes + mx_sf_pos(rel % kBM, b & 3)] = sb;
         }
       }
-      if (x_perm != nullptr) {
-        // training: the bf16 rows too (weight gradient), 16-byte vectors,
-        // lane l taking vectors l, l + 32, ... (the row is in cache)
-        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-        for (int vv = lane; vv < H / 8; vv += 32) {
-          const uint4 w = __ldg(src + vv);
-          for (int i = 0; i < k; ++i) {
-            const int r = s_rows[j * k + i];
-            if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H)[vv] = w;
-          }
-        }
-      }
+      if (x_perm != nullptr) scatter_row_bf16(x, x_perm, t, H, s_rows + j * k, k, lane);
     }
     return;
   }

@@ -139,6 +139,17 @@ def lib():
                                           c_size_t, vp]
         for n in ("moe_nv_quantize_layer_weights", "moe_layer_fwd_nvfp4"):
             getattr(L, n).restype = c_int
+        L.moe_nv_bwd_weight_bytes.restype = c_size_t
+        L.moe_nv_bwd_weight_bytes.argtypes = [POINTER(MoeConfig), c_int]
+        L.moe_nv_train_workspace_bytes.restype = c_size_t
+        L.moe_nv_train_workspace_bytes.argtypes = [POINTER(MoeConfig)]
+        L.moe_nv_quantize_bwd_weights.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeNvBwdWeights), vp]
+        L.moe_layer_fwd_nvfp4_train.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, POINTER(MoeNvWeights), vp,
+                                                POINTER(MoeFwdSaved), vp, c_size_t, vp]
+        L.moe_layer_bwd_nvfp4.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeNvBwdWeights),
+                                          POINTER(MoeFwdSaved), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+        for n in ("moe_nv_quantize_bwd_weights", "moe_layer_fwd_nvfp4_train", "moe_layer_bwd_nvfp4"):
+            getattr(L, n).restype = c_int
         _lib = L
     return _lib
 
@@ -149,7 +160,7 @@ STAGE_NAMES = {20: "nv_quantize", 21: "nv_gemm", 22: "mx_quantize_tokens", 24: "
                6: "shared_down", 7: "combine", 10: "combine_bwd", 11: "router_bwd_elem", 12: "dgrad_down_swiglu",
                13: "wgrad_down", 14: "dgrad_gate_up", 15: "wgrad_gate_up", 16: "router_dgrad",
                17: "permute_bwd", 18: "router_wgrad", 19: "aux_loss", 30: "read_ceiling",
-               31: "write_ceiling"}
+               31: "write_ceiling", 32: "nv_dgrad_down", 33: "nv_swiglu_bwd", 34: "nv_dgrad_gate_up"}
 
 
 def profile_start(capacity: int) -> None:
@@ -632,3 +643,67 @@ def layer_fwd_nvfp4(cfg, x, router_w, nvw, expert_bias=None, logit_bias=None, ws
                                    ctypes.byref(_nv_struct(nvw)), _p(y), _p(ws), ws.numel(), _stream())
     _check(st, "moe_layer_fwd_nvfp4")
     return y
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 training step (forward saving, backward with NVFP4 data gradients)
+# ---------------------------------------------------------------------------
+class MoeNvBwdWeights(ctypes.Structure):
+    """Mirror of moe_nv_bwd_weights (six device pointers)."""
+    _fields_ = [(n, c_void_p) for n in ("w2h", "sf2h", "g2h", "w13f", "sf13f", "g13f")]
+
+
+def nv_quantize_bwd_weights(cfg, W1, W3, W2):
+    """Weights of the NVFP4 data-gradient GEMMs as new device tensors: w2h
+    [E,F,H/2] (W2 along H), w13f [E,H,F] (W1 | W3 along 2F; codes two per
+    byte), their tile-ready scales sf2h, sf13f and tensor scales g2h, g13f [E]."""
+    out = {}
+    for i, (n, _) in enumerate(MoeNvBwdWeights._fields_):
+        nb = int(lib().moe_nv_bwd_weight_bytes(ctypes.byref(cfg), i))
+        if nb == 0:
+            raise MoeError(2, "moe_nv_bwd_weight_bytes")
+        dt = torch.float32 if n.startswith("g") else torch.uint8
+        out[n] = torch.empty(nb // (4 if dt == torch.float32 else 1), dtype=dt, device=W1.device)
+    out["w2h"] = out["w2h"].view(cfg.E, cfg.F, cfg.H // 2)
+    out["w13f"] = out["w13f"].view(cfg.E, cfg.H, cfg.F)
+    w = MoeNvBwdWeights(*[out[n].data_ptr() for n, _ in MoeNvBwdWeights._fields_])
+    _check(lib().moe_nv_quantize_bwd_weights(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2), ctypes.byref(w), _stream()),
+           "moe_nv_quantize_bwd_weights")
+    return out
+
+
+def nv_train_workspace(cfg, device="cuda"):
+    n = int(lib().moe_nv_train_workspace_bytes(ctypes.byref(cfg)))
+    if n == 0:
+        raise MoeError(2, "moe_nv_train_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def layer_fwd_nvfp4_train(cfg, x, router_w, nvw, saved, expert_bias=None, logit_bias=None, ws=None, y=None):
+    """Training forward of the NVFP4 layer (``nvw`` from
+    nv_quantize_layer_weights, ``saved`` from alloc_saved)."""
+    dev = x.device
+    if y is None:
+        y = torch.empty((cfg.T, cfg.H), dtype=_out_dtype(cfg), device=dev)
+    ws = nv_train_workspace(cfg, dev) if ws is None else ws
+    st = lib().moe_layer_fwd_nvfp4_train(ctypes.byref(cfg), _p(x), _p(router_w), _p(expert_bias), _p(logit_bias),
+                                         ctypes.byref(_nv_struct(nvw)), _p(y), ctypes.byref(_saved_struct(saved)),
+                                         _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_fwd_nvfp4_train")
+    return y
+
+
+def layer_bwd_nvfp4(cfg, dO, x, router_w, nvbw, saved, ws=None, grads=None):
+    """Backward of the NVFP4 training step (``nvbw`` from
+    nv_quantize_bwd_weights); gradients as layer_bwd."""
+    dev = x.device
+    g = alloc_grads(cfg, dev) if grads is None else grads
+    ws = nv_train_workspace(cfg, dev) if ws is None else ws
+    w = MoeNvBwdWeights(*[nvbw[n].data_ptr() for n, _ in MoeNvBwdWeights._fields_])
+    st = lib().moe_layer_bwd_nvfp4(ctypes.byref(cfg), _p(dO), _p(x), _p(router_w), ctypes.byref(w),
+                                   ctypes.byref(_saved_struct(saved)), _p(g["dx"]), _p(g["dW_r"]), _p(g["dW1"]),
+                                   _p(g["dW3"]), _p(g["dW2"]), _p(g["aux_loss"]), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_bwd_nvfp4")
+    return g

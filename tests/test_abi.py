@@ -140,6 +140,24 @@ def test_low_precision_entry_points_check_on_the_host(lib):
                                            null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
     assert lib.moe_mx_quantize(null, 10, 33, null, null, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_nv_quantize(null, 10, 32, null, null, null, null) == ops.MOE_ERR_INVALID_ARG
+    # the NVFP4 training step
+    for i in range(6):
+        assert lib.moe_nv_bwd_weight_bytes(ctypes.byref(ok), i) > 0
+        assert lib.moe_nv_bwd_weight_bytes(ctypes.byref(bad_f), i) == 0
+        assert lib.moe_nv_bwd_weight_bytes(ctypes.byref(shared), i) == 0
+    assert lib.moe_nv_bwd_weight_bytes(ctypes.byref(ok), 0) == 8 * 256 * 128      # W2 rows along H: [E][F][H/2]
+    assert lib.moe_nv_bwd_weight_bytes(ctypes.byref(ok), 3) == 8 * 256 * 256      # [W1 | W3] along 2F: [E][H][F]
+    assert lib.moe_nv_bwd_weight_bytes(ctypes.byref(ok), 5) == 4 * 8
+    assert lib.moe_nv_train_workspace_bytes(ctypes.byref(ok)) > lib.moe_nv_workspace_bytes_layer(ctypes.byref(ok))
+    assert lib.moe_nv_train_workspace_bytes(ctypes.byref(shared)) == 0
+    assert lib.moe_layer_fwd_nvfp4_train(ctypes.byref(ok), null, null, null, null, None, null, None, null, 0,
+                                         null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_fwd_nvfp4_train(ctypes.byref(bad_f), null, null, null, null, None, null, None, null, 0,
+                                         null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_layer_bwd_nvfp4(ctypes.byref(ok), null, null, null, None, None, null, null, null, null, null,
+                                   null, null, 0, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_nv_quantize_bwd_weights(ctypes.byref(bad_h), null, null, null, None,
+                                           null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
 
 
 def test_read_ceiling_checks_on_the_host(lib):
