@@ -736,6 +736,65 @@ def run_ours(args, ls, rank, world, local_rank):
         nv["layer_fwd"] = {"value": round(job_throughput(layer_flops(ls, False), ms_nl, world), 2), "unit": "TFLOPS",
                            "ms_per_step": round(ms_nl, 4), "vs_bf16_fwd": round(ms_fwd / ms_nl, 3)}
         del nlw, yl
+        # the NVFP4 training step: forward saving for the backward, backward
+        # with NVFP4 data-gradient GEMMs (weights quantised once, outside the
+        # timed region; bf16 weight gradients into the bf16 step's buffers)
+        if not ls.F_shared:
+            nlw = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
+            nbw = ops.nv_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+            wsn = ops.nv_train_workspace(cfg, dev)
+            svn = ops.alloc_saved(cfg, dev)
+            yl = torch.empty_like(y)
+
+            def step_nv():
+                ops.layer_fwd_nvfp4_train(cfg, d["x"], d["router_w"], nlw, svn, d["expert_bias"], d["logit_bias"],
+                                          ws=wsn, y=yl)
+                ops.layer_bwd_nvfp4(cfg, d["dO"], d["x"], d["router_w"], nbw, svn, ws=wsn, grads=grads)
+
+            for _ in range(max(3, args.warmup)):
+                step_nv()
+            barrier()
+            cap_n = args.steps * 48 + 64
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ops.profile_start(cap_n)
+            s0.record()
+            for _ in range(args.steps):
+                step_nv()
+            s1.record()
+            torch.cuda.synchronize()
+            ops.profile_stop()
+            assert ops.device_status(wsn) == 0
+            ms_nt = max_over_ranks(s0.elapsed_time(s1) / args.steps, world, dev)
+            st_nt = {}
+            for name, t in ops.profile_read(cap_n):
+                st_nt.setdefault(name, []).append(t)
+            nk = {}
+            for name, fl, pk in (("ffn1_gate_up", 2 * R * ls.H * 2 * ls.F, peak4),
+                                 ("ffn2_down", 2 * R * ls.F * ls.H, peak4),
+                                 ("nv_dgrad_down", 2 * R * ls.H * ls.F, peak4),
+                                 ("nv_dgrad_gate_up", 2 * R * 2 * ls.F * ls.H, peak4),
+                                 ("wgrad_down", 2 * R * ls.F * ls.H, peaks["bf16_tflops_sustained"]),
+                                 ("wgrad_gate_up", 2 * R * ls.H * 2 * ls.F, peaks["bf16_tflops_sustained"])):
+                if name in st_nt:
+                    avg = sum(st_nt[name]) / args.steps
+                    ach = fl / (avg * 1e-3) / 1e12
+                    nk[name] = {"ms": round(avg, 4), "bound": "tensor", "achieved_tflops": round(ach, 1),
+                                "frac": round(ach / pk, 4)}
+            if "nv_swiglu_bwd" in st_nt:
+                # da fp32 and h13 read, dh13 written (bf16)
+                avg = sum(st_nt["nv_swiglu_bwd"]) / args.steps
+                gbs = 12 * R * ls.F / (avg * 1e-3) / 1e9
+                nk["nv_swiglu_bwd"] = {"ms": round(avg, 4), "bound": "hbm", "achieved_gbs": round(gbs, 1),
+                                       "frac": round(gbs / peaks["hbm_gbs"], 4)}
+            for name in ("nv_quantize", "router", "permute", "combine", "combine_bwd", "router_bwd_elem",
+                         "permute_bwd"):
+                if name in st_nt:
+                    nk[name] = {"ms": round(sum(st_nt[name]) / args.steps, 4)}
+            nv["train_step"] = {"value": round(job_throughput(layer_flops(ls, True), ms_nt, world), 2),
+                                "unit": "TFLOPS", "ms_per_step": round(ms_nt, 4), "vs_bf16_step": round(ms / ms_nt, 3),
+                                "dtype": "nvfp4 forward and data-gradient GEMMs, bf16 weight gradients (fp32 out)",
+                                "kernels": nk}
+            del nlw, nbw, wsn, svn, yl
 
     # ---------------- per-stage table and roofline of the dominant kernel
     model = stage_model(ls, training)

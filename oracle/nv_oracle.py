@@ -38,7 +38,7 @@ from .mx_oracle import e4m3_encode, e4m3_round
 __all__ = ["E2M1_MAX", "e2m1_round", "e2m1_encode", "e2m1_decode", "nv_tensor_scale", "nv_quantize",
            "nv_dequantize", "nv_roundtrip", "nv_grouped_gemm", "routed_rows_roundtrip", "gate_up_store",
            "activation_roundtrip", "nv_layer_fwd", "output_grad_roundtrip", "swiglu_grad_roundtrip",
-           "dgrad_weight_roundtrip", "nv_layer_bwd"]
+           "dgrad_weight_roundtrip", "nv_layer_bwd", "nv_expert_weight_grads"]
 
 E2M1_MAX = 6.0
 NV_BLOCK = 16
@@ -346,3 +346,53 @@ def nv_layer_bwd(x, w_r, W1, W3, W2, dO, k, score="softmax", expert_bias=None, l
     if aux:
         res["aux_loss"] = aux_loss(softmax(rt["logits"]), counts, k, aux)
     return res
+
+
+def nv_expert_weight_grads(x, w_r, W1, W3, W2, dO, k, experts, score="softmax", expert_bias=None, logit_bias=None,
+                           n_groups=1, topk_groups=1, gate_scale=1.0, prec=CONTRACT, force_balanced=False):
+    """dW1_e, dW3_e, dW2_e of ``nv_layer_bwd`` for the listed experts, from
+    those experts' rows alone (for layers too large for the whole step).
+
+    Of the tensor scales, the weight gradients depend on two, and both follow
+    from per-token maxima: x_perm's (every token is routed, so its maximum is
+    x's) and dy_perm's (the largest |g dO| is the largest gate of a token
+    times the largest |dO| of that token, maximised over tokens, then stored
+    per prec.dy_perm; rounding is monotone). Per expert e, on its rows:
+      h = Q(x_e) Q([W1_e | W3_e]) (per prec.h13), a = SiLU(h1) h3 (per prec.a),
+      dy = g dO (per prec.dy_perm), da = Q(dy) Q(W2_e)^T,
+      dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1) (per prec.dh13),
+      dW1_e = x_e^T dh1, dW3_e = x_e^T dh3, dW2_e = a^T dy.
+    Returns {"dW1": {e: ..}, "dW3": .., "dW2": .., "counts": counts}."""
+    x = np.asarray(x, np.float64)
+    dO = np.asarray(dO, np.float64)
+    w_r = np.asarray(w_r, np.float64)
+    E = w_r.shape[0]
+    rt = route(x, w_r, k, score, expert_bias, logit_bias, n_groups, topk_groups, gate_scale, force_balanced)
+    idx, gate = rt["topk_idx"], rt["topk_gate"]
+    counts = np.bincount(idx.ravel(), minlength=E)
+    g_x = nv_tensor_scale(np.abs(x).max() if x.size else 0.0)
+    dy_max = prec.r("dy_perm", np.max(np.abs(gate).max(axis=1) * np.abs(dO).max(axis=1)) if x.size else 0.0)
+    g_dy = nv_tensor_scale(dy_max)
+    out = {"dW1": {}, "dW3": {}, "dW2": {}, "counts": counts}
+    for e in experts:
+        e = int(e)
+        tt, ii = np.nonzero(idx == e)                       # the expert's rows, ascending t
+        F = np.asarray(W1[e]).shape[1]
+        if len(tt) == 0:
+            H = x.shape[1]
+            out["dW1"][e], out["dW3"][e], out["dW2"][e] = np.zeros((H, F)), np.zeros((H, F)), np.zeros((F, H))
+            continue
+        xr = x[tt]
+        W13 = np.concatenate([np.asarray(W1[e], np.float64), np.asarray(W3[e], np.float64)], axis=1)
+        h = prec.r("h13", nv_roundtrip(np.asarray(xr, np.float32), axis=1, g=g_x)
+                   @ nv_roundtrip(np.asarray(W13, np.float32), axis=0))
+        h1, h3 = h[:, :F], h[:, F:]
+        a = prec.r("a", silu(h1) * h3)
+        dy = prec.r("dy_perm", gate[tt, ii][:, None] * dO[tt])
+        da = nv_roundtrip(np.asarray(dy, np.float32), axis=1, g=g_dy) @ dgrad_weight_roundtrip(W2[e]).T
+        dh1 = prec.r("dh13", da * h3 * silu_grad(h1))
+        dh3 = prec.r("dh13", da * silu(h1))
+        out["dW1"][e] = xr.T @ dh1
+        out["dW3"][e] = xr.T @ dh3
+        out["dW2"][e] = a.T @ dy
+    return out

@@ -921,10 +921,13 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   prof_mark(s, STAGE_BEGIN);
   // 1. combine backward (memory-saving: dy_perm only; MXFP8: dy_perm also
   //    quantised, blocks of 32 along H)
+  //    NVFP4: with the largest |dy_perm| for its tensor scale
+  float* nv_dy_g = nv != nullptr ? at<float>(ws, L.nv_g) + 2 : nullptr;
   MOE_CUDA(launch_combine_bwd(c, reinterpret_cast<const __nv_bfloat16*>(dO), saved->y_perm, saved->row_id_map,
                               saved->topk_gate, dy_perm, dgate, s, mx ? at<uint8_t>(ws, L.dy_q) : nullptr,
-                              mx ? at<uint8_t>(ws, L.sfa_dy) : nullptr, saved->offsets, saved->topk_idx, st));
-  stage_done(s, STAGE_COMBINE_BWD, 1);
+                              mx ? at<uint8_t>(ws, L.sfa_dy) : nullptr, saved->offsets, saved->topk_idx, st, nv_dy_g));
+  if (nv != nullptr) MOE_CUDA(launch_nv_scale_from_amax(nv_dy_g, 1, s));
+  stage_done(s, STAGE_COMBINE_BWD, nv != nullptr ? 2 : 1);
   const int n_part = (c.F + 255) / 256;
   float* dg_part = at<float>(ws, L.dg_part);
   __nv_bfloat16* a_used =
@@ -951,7 +954,8 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
   stage_done(s, STAGE_ROUTER_BWD, 1);
   // 3. da = dy_perm W2_e^T with the SwiGLU backward epilogue -> dh13
   if (nv != nullptr) {
-    // NVFP4: dy_perm quantised as one tensor (blocks along H); da = Q(dy_perm)
+    // NVFP4: dy_perm quantised as one tensor (blocks along H, the tensor
+    // scale from the combine backward's maximum); da = Q(dy_perm)
     // Q(W2_e)^T in fp32; the SwiGLU backward -> dh13 (bf16) and its maximum;
     // dh13 quantised as one tensor (blocks along 2F) for step 5
     uint8_t* q = at<uint8_t>(ws, L.nv_q);
@@ -959,9 +963,8 @@ static int layer_bwd_core(const moe_config& c, const moe_bf16* dO, const moe_bf1
     float* gq = at<float>(ws, L.nv_g);
     float* da = at<float>(ws, L.nv_da);
     const int32_t* n_rows = saved->offsets + c.E;
-    MOE_CUDA(launch_nv_amax_rows(dy_perm, R, c.H, n_rows, gq + 2, s));
     MOE_CUDA(launch_nv_quantize_grouped(dy_perm, R, c.H, c.E, saved->offsets, gq + 2, q, sfq, s));
-    stage_done(s, STAGE_NV_QUANT, 3);
+    stage_done(s, STAGE_NV_QUANT, 1);
     MOE_TRY(run_gemm_nv(c.E, R, c.H, c.F, saved->offsets, q, sfq, gq + 2, nv->w2h, nv->sf2h, nv->g2h, da, st, s,
                         true));
     stage_done(s, STAGE_NV_DGRAD2, 1);

@@ -104,15 +104,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // MXQ (the MXFP8 training step): the bf16 dy_perm rows are also quantised
 // (blocks of 32 along H, one block per four lanes) into codes mq [R, H] and
 // scales in the activations' tile-ready layout (msf), the row's expert and
-// its offset from topk_idx and offsets.
-template <bool YP32, int KMAX, bool DG = true, bool MXQ = false>
+// its offset from topk_idx and offsets. AMAX (the NVFP4 training step): the
+// largest magnitude of the stored dy_perm values, as fp32 bits, maximised
+// into *amax_bits.
+template <bool YP32, int KMAX, bool DG = true, bool MXQ = false, bool AMAX = false>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     combine_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ y_perm,
                        const int32_t* __restrict__ row_id_map, const float* __restrict__ gate,
                        __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dgate, int T, int H, int k,
                        uint8_t* __restrict__ mq = nullptr, uint8_t* __restrict__ msf = nullptr,
                        const int32_t* __restrict__ offsets = nullptr, const int32_t* __restrict__ topk_idx = nullptr,
-                       int E = 0, DevStatus* st = nullptr) {
+                       int E = 0, DevStatus* st = nullptr, unsigned* __restrict__ amax_bits = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + warp;
   __shared__ int s_off[MXQ ? kMaxGroups + 1 : 1];
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
     gs[i] = __shfl_sync(0xffffffffu, my_g, i < k ? i : 0);
   }
   const int nvec = H / 8;
+  float am = 0.0f;  // AMAX: largest |g dO| this warp stores
   for (int v = lane; v < nvec; v += 32) {
     float d[8];
     Vec8<false>::load(dO, static_cast<size_t>(t) * H + v * 8, d);
@@ -161,9 +164,23 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, KMAX <= 8 ? 2 : 1)
           o[j] = gs[i] * d[j];
         }
         dot[i] += s;
-        if (rows[i] >= 0) Vec8<false>::store(dy_perm, static_cast<size_t>(rows[i]) * H + v * 8, o);
+        if (rows[i] >= 0) {
+          Vec8<false>::store(dy_perm, static_cast<size_t>(rows[i]) * H + v * 8, o);
+          if constexpr (AMAX) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(o[j]));
+          }
+        }
       }
     }
+  }
+  if constexpr (AMAX) {
+    // the maximum of the stored bf16 values is the bf16 rounding of the fp32
+    // maximum (rounding is monotone)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    am = __bfloat162float(__float2bfloat16_rn(am));
+    if (lane == 0 && am > 0.0f) atomicMax(amax_bits, __float_as_uint(am));
   }
   if constexpr (MXQ) {
     // second pass: the MXFP8 rows of dy_perm, from the same products g dO
@@ -476,10 +493,15 @@ cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const
 cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq, uint8_t* msf, const int32_t* offsets,
-                               const int32_t* topk_idx, DevStatus* ds) {
+                               const int32_t* topk_idx, DevStatus* ds, float* dy_amax) {
   NvtxRange nvtx("moe.combine_backward");
   const int b = blocks_for(c.T);
   const int th = kWarpsPerBlock * 32;
+  unsigned* am = reinterpret_cast<unsigned*>(dy_amax);
+  if (dy_amax != nullptr) {
+    cudaError_t e = cudaMemsetAsync(dy_amax, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
   if (mq != nullptr) {  // MXFP8 training step: dy_perm quantised as it is written
     cudaError_t e = cudaMemsetAsync(msf, 0, mx_sfa_bytes(static_cast<long long>(c.T) * c.k, c.E, c.H), st);
     if (e != cudaSuccess) return e;
@@ -498,6 +520,9 @@ cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, con
   } else if (c.inter_fp32) {
     if (c.k <= 8) combine_bwd_kernel<true, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
     else combine_bwd_kernel<true, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
+  } else if (am != nullptr) {  // NVFP4 training step: with the maximum of dy_perm
+    if (c.k <= 8) combine_bwd_kernel<false, 8, true, false, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds, am);
+    else combine_bwd_kernel<false, 16, true, false, true><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds, am);
   } else {
     if (c.k <= 8) combine_bwd_kernel<false, 8><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);
     else combine_bwd_kernel<false, 16><<<b, th, 0, st>>>(dO, y_perm, row_id_map, gate, dy_perm, dgate, c.T, c.H, c.k, nullptr, nullptr, nullptr, nullptr, c.E, ds);

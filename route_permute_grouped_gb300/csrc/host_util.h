@@ -67,11 +67,12 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_
                            const float* gate, const void* shared, void* y, cudaStream_t st, DevStatus* ds = nullptr);
 // mq != nullptr (MXFP8 training step): also the MXFP8 rows of dy_perm (codes
 // mq [R, H], tile-ready scales msf; offsets and topk_idx locate each row)
+// dy_amax (bf16 dy_perm only): the largest |dy_perm| stored, as fp32 bits
 cudaError_t launch_combine_bwd(const moe_config& c, const __nv_bfloat16* dO, const void* y_perm,
                                const int32_t* row_id_map, const float* gate, __nv_bfloat16* dy_perm, float* dgate,
                                cudaStream_t st, uint8_t* mq = nullptr, uint8_t* msf = nullptr,
                                const int32_t* offsets = nullptr, const int32_t* topk_idx = nullptr,
-                               DevStatus* ds = nullptr);
+                               DevStatus* ds = nullptr, float* dy_amax = nullptr);
 // dx = sum_i dx_perm[row(t,i)] + extra (fp32, nullable) + add ([T,H], nullable);
 // dx_perm and add are fp32 with rows_fp32, else bf16
 cudaError_t launch_unpermute_sum(const moe_config& c, const void* dx_perm, const int32_t* row_id_map,
@@ -141,10 +142,6 @@ cudaError_t launch_nv_quantize_weights(const __nv_bfloat16* w, int E, int K, int
                                        int split = 0);
 cudaError_t launch_nv_quantize_grouped(const __nv_bfloat16* x, int R, int K, int E, const int32_t* offsets,
                                        const float* g, uint8_t* xq, uint8_t* sf, cudaStream_t st);
-// tensor scale of the first *n_rows rows (cols elements each, at most
-// max_rows) of x, into *out
-cudaError_t launch_nv_amax_rows(const __nv_bfloat16* x, long long max_rows, int cols, const int32_t* n_rows,
-                                float* out, cudaStream_t st);
 // row-major weights W[E][N][K] (columns [split, K) from w_hi [E][N][K - split])
 // -> K-major codes and tile-ready scales as launch_nv_quantize_weights' plain layout
 cudaError_t launch_nv_quantize_weight_rows(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,

@@ -9,19 +9,11 @@
 namespace moe {
 
 // out[grp] = bits of max |x| over group grp's n_per elements (non-negative
-// fp32 values order like their bit patterns); 8 elements per 16-byte load.
-// With lim_rows set (one group), only the first *lim_rows rows of `cols`
-// elements count.
+// fp32 values order like their bit patterns); 8 elements per 16-byte load
 __global__ void __launch_bounds__(256) nv_amax_kernel(const __nv_bfloat16* __restrict__ x, long long n_per,
-                                                      unsigned* __restrict__ out,
-                                                      const int32_t* __restrict__ lim_rows = nullptr,
-                                                      long long cols = 0) {
+                                                      unsigned* __restrict__ out) {
   const uint4* base = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.y) * n_per);
-  long long nv = n_per / 8;
-  if (lim_rows != nullptr) {
-    const long long lim = static_cast<long long>(max(__ldg(lim_rows), 0)) * cols / 8;
-    nv = lim < nv ? lim : nv;
-  }
+  const long long nv = n_per / 8;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   float m = 0.0f;
   // four independent 16-byte loads in flight per thread
@@ -128,8 +120,9 @@ __global__ void __launch_bounds__(256) nv_quantize_weight_kernel(const __nv_bflo
 // Grouped rows of x [R, K] (expert e's rows offsets[e]..offsets[e+1]) ->
 // codes xq [R, K/2] and scale blocks 2 P + h per k block, P = the expert's
 // first 256-row pair tile + rel / 256, h = (rel / 128) % 2 (rel = row -
-// offsets[e]); thread = one 16-element block. Scales of rows past an expert's
-// count are left as they are (zeroed by the caller).
+// offsets[e]); thread = one 16-element block (grid-stride, so that each block
+// forms the experts' tile prefix once for many). Scales of rows past an
+// expert's count are left as they are (zeroed by the caller).
 __global__ void __launch_bounds__(256) nv_quantize_grouped_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
                                                                   int E, const int32_t* __restrict__ offsets,
                                                                   const float* __restrict__ g,
@@ -142,20 +135,23 @@ __global__ void __launch_bounds__(256) nv_quantize_grouped_kernel(const __nv_bfl
   if (threadIdx.x < 32) pair_tile_prefix_warp(s_off, s_pt, E, threadIdx.x);
   __syncthreads();
   const int nb = K / kNvBlock;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<long long>(R) * nb) return;
-  const int row = static_cast<int>(i / nb);
-  const int b = static_cast<int>(i - static_cast<long long>(row) * nb);
-  const int lo = expert_of_row(s_off, E, row);
-  const int rel = row - s_off[lo];
-  float v[16];
-  load_bf16x16(x + static_cast<size_t>(row) * K + b * kNvBlock, v);
-  uint32_t c[2];
-  const uint32_t sb = nv_quant16(v, *g, c);
-  *reinterpret_cast<uint2*>(xq + static_cast<size_t>(row) * (K / 2) + b * 8) = make_uint2(c[0], c[1]);
-  const int blk = 2 * (s_pt[lo] + rel / (2 * kBM)) + ((rel / kBM) & 1);
-  sf[(static_cast<size_t>(blk) * (K / kNvKB) + b / 16) * kNvSfBytes + nv_sf_pos(rel % kBM, b & 15)] =
-      static_cast<uint8_t>(sb);
+  const float gs = *g;
+  const long long n = static_cast<long long>(R) * nb;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(i / nb);
+    const int b = static_cast<int>(i - static_cast<long long>(row) * nb);
+    const int lo = expert_of_row(s_off, E, row);
+    const int rel = row - s_off[lo];
+    float v[16];
+    load_bf16x16(x + static_cast<size_t>(row) * K + b * kNvBlock, v);
+    uint32_t c[2];
+    const uint32_t sb = nv_quant16(v, gs, c);
+    *reinterpret_cast<uint2*>(xq + static_cast<size_t>(row) * (K / 2) + b * 8) = make_uint2(c[0], c[1]);
+    const int blk = 2 * (s_pt[lo] + rel / (2 * kBM)) + ((rel / kBM) & 1);
+    sf[(static_cast<size_t>(blk) * (K / kNvKB) + b / 16) * kNvSfBytes + nv_sf_pos(rel % kBM, b & 15)] =
+        static_cast<uint8_t>(sb);
+  }
 }
 
 // Weights stored row-major W[E][N][K] (row n of expert e holds the K
@@ -199,17 +195,19 @@ __global__ void __launch_bounds__(256) nv_quantize_weight_rows_kernel(const __nv
 // (rows below *n_rows, the routed rows): da fp32 [R, F] and the saved bf16
 // pre-activations h13 [R, 2F] (h1 | h3) give dh1 = da h3 SiLU'(h1) and
 // dh3 = da SiLU(h1), stored bf16 to dh13 [R, 2F] (h1's columns then h3's), and
-// the largest magnitude of the stored values into *amax_bits.
+// the largest magnitude of the stored values into *amax_bits. Grid-stride
+// (blockDim 256): one atomic per block.
 __global__ void __launch_bounds__(256) nv_swiglu_bwd_kernel(const float* __restrict__ da,
                                                             const __nv_bfloat16* __restrict__ h13, int R, int F,
                                                             const int32_t* __restrict__ n_rows,
                                                             __nv_bfloat16* __restrict__ dh13,
                                                             unsigned* __restrict__ amax_bits) {
   const int nv = F / 8;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int rows = min(R, max(__ldg(n_rows), 0));
+  const long long n = static_cast<long long>(rows) * nv;
   float m = 0.0f;
-  if (i < static_cast<long long>(rows) * nv) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long r = i / nv;
     const int c = static_cast<int>(i - r * nv) * 8;
     const float4* dp = reinterpret_cast<const float4*>(da + r * F + c);
@@ -241,9 +239,16 @@ __global__ void __launch_bounds__(256) nv_swiglu_bwd_kernel(const float* __restr
     *reinterpret_cast<uint4*>(orow + c) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
     *reinterpret_cast<uint4*>(orow + F + c) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
   }
+  // one atomic per block
+  __shared__ float s_m[8];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(amax_bits, __float_as_uint(m));
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, s_m[w]);
+    if (m > 0.0f) atomicMax(amax_bits, __float_as_uint(m));
+  }
 }
 
 cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, float* out_bits, cudaStream_t st,
@@ -271,21 +276,6 @@ cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_nv_amax_rows(const __nv_bfloat16* x, long long max_rows, int cols, const int32_t* n_rows,
-                                float* out, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), st);
-  if (e != cudaSuccess) return e;
-  long long blocks = (max_rows * cols / 8 + 255) / 256;
-  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
-  if (blocks < 1) blocks = 1;
-  nv_amax_kernel<<<dim3(static_cast<unsigned>(blocks), 1), 256, 0, st>>>(x, max_rows * cols,
-                                                                       reinterpret_cast<unsigned*>(out), n_rows, cols);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  nv_scale_from_amax_kernel<<<1, 32, 0, st>>>(out, 1);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_nv_quantize_weight_rows(const __nv_bfloat16* w, int E, int K, int N, const float* g, uint8_t* wq,
                                            uint8_t* sf, cudaStream_t st, const __nv_bfloat16* w_hi, int split) {
   cudaError_t e = cudaMemsetAsync(sf, 0, nv_weight_sf_bytes(E, K, N), st);
@@ -302,8 +292,10 @@ cudaError_t launch_nv_swiglu_bwd(const float* da, const __nv_bfloat16* h13, int 
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(R) * (F / 8);
   if (n > 0) {
-    nv_swiglu_bwd_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(da, h13, R, F, n_rows, dh13,
-                                                                                reinterpret_cast<unsigned*>(g));
+    long long blocks = (n + 255) / 256;
+    if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+    nv_swiglu_bwd_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(da, h13, R, F, n_rows, dh13,
+                                                                        reinterpret_cast<unsigned*>(g));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -341,7 +333,9 @@ cudaError_t launch_nv_quantize_grouped(const __nv_bfloat16* x, int R, int K, int
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(R) * (K / kNvBlock);
   if (n == 0) return cudaSuccess;
-  nv_quantize_grouped_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(x, R, K, E, offsets, g, xq, sf);
+  long long blocks = (n + 255) / 256;
+  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+  nv_quantize_grouped_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, R, K, E, offsets, g, xq, sf);
   return cudaGetLastError();
 }
 

@@ -41,25 +41,34 @@ def mx_wgrad_atol(want, amax_a, amax_b):
     return max(wgrad_atol(want), 2.0 ** -2 * float(amax_a) * float(amax_b))
 
 
-def assert_close_but_flips(name, got, ref, atol, flip_atol, max_slices=2, rel=REL_L2):
-    """assert_close for a result whose low-precision operand codes may differ
-    in rare places from the oracle's: a code is decided from a bf16 value that
-    the kernel (fp32) and the oracle (fp64) can round to different neighbours,
-    and a coarse code (E2M1) then moves by a whole step. Relative L2 <= rel
-    everywhere; entries beyond `atol` must lie in at most `max_slices` slices
-    along axis 0 (the experts or tokens one flipped code reaches) and stay
-    within `flip_atol`, the bound of one such flip."""
+def assert_close_but_flips(name, got, ref, atol, rank=2, rel=REL_L2):
+    """assert_close for weight gradients whose low-precision operand codes may
+    differ in rare places from the oracle's: a code is decided from a bf16
+    value that the kernel (fp32) and the oracle (fp64) can round to
+    neighbouring values, and a coarse code (E2M1) then moves by a whole step.
+    One flipped code of a routed row r changes that row of dh13 (or dy_perm),
+    so the gradient sum_r X[r]^T D[r] moves by one outer product: a rank-one
+    error. Relative L2 <= rel over everything; per matrix (the last two axes),
+    the error left after removing its `rank` largest singular components must
+    be within `atol` (the bf16 bound), i.e. up to `rank` flips are admitted."""
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     assert got.shape == ref.shape, f"{name}: shape {got.shape} vs {ref.shape}"
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     r = rel_l2(got, ref)
-    err = np.abs(got - ref)
-    m = float(err.max()) if got.size else 0.0
-    bad = np.nonzero((err > atol).reshape(err.shape[0], -1).any(axis=1))[0]
     assert r <= rel, f"{name}: rel_l2={r:.3e} (<= {rel})"
-    assert len(bad) <= max_slices and m <= max(atol, flip_atol), \
-        f"{name}: max_abs={m:.3e} (<= {atol}, flips {flip_atol:.3e}), slices beyond atol: {list(bad[:8])}"
-    return r, m
+    err = (got - ref).reshape((-1,) + got.shape[-2:])
+    flips = 0
+    m_left = 0.0
+    for i in range(err.shape[0]):
+        e = err[i]
+        if np.abs(e).max(initial=0.0) <= atol:
+            continue
+        u, sv, vt = np.linalg.svd(e, full_matrices=False)
+        left = e - (u[:, :rank] * sv[:rank]) @ vt[:rank]
+        m_left = max(m_left, float(np.abs(left).max()))
+        flips += 1
+        assert m_left <= atol, f"{name}[{i}]: max_abs beyond rank {rank}: {m_left:.3e} (<= {atol})"
+    return r, flips
 
 
 def rel_l2(got, ref):

@@ -6,14 +6,17 @@ grouped GEMM on the down projection's full shape (131072 x 1536 x 4096, 128
 experts) for the rows of three experts, and the MXFP8 training step on the
 full Qwen3 training workload (T=16384, E=128), with bf16 and with MXFP8
 weight gradients, for one token's output and input gradient and one expert's
-weight gradients."""
+weight gradients; and the NVFP4 training step on the same workload for two
+experts' weight gradients (its input gradient as a property against the bf16
+step)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
 from route_permute_grouped_gb300 import ops, synth
-from tests._util import TIE_MARGIN, assert_close, compare_topk, f64, mx_wgrad_atol, wgrad_atol
+from tests._util import (TIE_MARGIN, assert_close, assert_close_but_flips, compare_topk, f64, mx_wgrad_atol,
+                         wgrad_atol)
 
 pytestmark = pytest.mark.gpu
 
@@ -113,3 +116,54 @@ def test_mxfp8_train_qwen3_full_sampled(wgrad):
         atol = mx_wgrad_atol(want, am[oa], am[ob]) if wgrad == "mxfp8" else wgrad_atol(want)
         assert_close(f"{key} (expert {e0}, {counts[e0]} rows)", f64(g[key][e0]), want, atol=atol)
     assert abs(float(g["aux_loss"].item()) - ref["aux_loss"]) <= 1e-5 * max(1.0, abs(ref["aux_loss"]))
+
+
+def test_nvfp4_train_qwen3_full_sampled():
+    # the NVFP4 training step on the full Qwen3 training workload: two experts'
+    # weight gradients (the median and the largest row count among experts no
+    # near-tie token can enter or leave) against the per-expert NVFP4 oracle,
+    # whose tensor scales come from per-token maxima; the input gradient (whose
+    # dh13 tensor scale needs every row) against the bf16 step as a property:
+    # FP4-sized, not more
+    ls = synth.shape("qwen3_train")
+    d = synth.make_layer(ls, seed=1234, device="cuda", training=True)
+    cfg = ops.config_from_shape(ls, out_fp32=True)
+    nvw = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
+    nvbw = ops.nv_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+    ws = ops.nv_train_workspace(cfg)
+    saved = ops.alloc_saved(cfg)
+    ops.layer_fwd_nvfp4_train(cfg, d["x"], d["router_w"], nvw, saved, ws=ws)
+    g = ops.layer_bwd_nvfp4(cfg, d["dO"], d["x"], d["router_w"], nvbw, saved, ws=ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    del nvw, nvbw, ws
+    x, w_r, dO = f64(d["x"]), f64(d["router_w"]), f64(d["dO"])
+    k = ls.k
+    rt = O.route(x, w_r, k)
+    zs = -np.sort(-rt["z"], axis=1)
+    ties = np.nonzero(zs[:, k - 1] - zs[:, k] < TIE_MARGIN)[0]
+    compare_topk(saved["topk_idx"].cpu().numpy(), rt["topk_idx"], rt["z"], k)
+    near = set()
+    for t in ties:
+        near.update(int(e) for e in np.argsort(-rt["z"][t], kind="stable")[k - 1:k + 1])
+    counts = np.bincount(rt["topk_idx"].reshape(-1), minlength=ls.E)
+    cand = [int(e) for e in np.argsort(counts, kind="stable") if int(e) not in near]
+    sample = [cand[len(cand) // 2], cand[-1]]
+    ref = O.nv_expert_weight_grads(x, w_r, _PerExpert(d["W1"]), _PerExpert(d["W3"]), _PerExpert(d["W2"]), dO, k,
+                                   experts=sample, prec=O.Precision(y=False, dx=False))
+    for e in sample:
+        for key in ("dW1", "dW3", "dW2"):
+            want = ref[key][e]
+            # up to two flipped E2M1 codes of dy_perm (see assert_close_but_flips)
+            assert_close_but_flips(f"{key} (expert {e}, {counts[e]} rows)", f64(g[key][e]), want,
+                                   atol=wgrad_atol(want))
+    # the bf16 step on the same inputs (GPU): the NVFP4 input gradient differs
+    # from it by FP4 rounding of two chained GEMMs
+    ws16, sv16 = ops.workspace(cfg, True), ops.alloc_saved(cfg)
+    ops.layer_fwd(cfg, d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], saved=sv16, ws=ws16)
+    g16 = ops.layer_bwd(cfg, d["dO"], d["x"], d["router_w"], d["W1"], d["W3"], d["W2"], sv16, ws=ws16)
+    torch.cuda.synchronize()
+    dx, dx16 = g["dx"].float(), g16["dx"].float()
+    assert torch.isfinite(dx).all()
+    r = float((dx - dx16).norm() / dx16.norm())
+    assert 1e-2 < r < 0.5, r

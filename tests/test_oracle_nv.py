@@ -364,3 +364,17 @@ def test_planted_nv_bwd_mistake_is_caught(monkeypatch, name, fn):
     with pytest.raises(AssertionError):
         test_nv_data_gradients_are_the_pinned_grouped_gemm()
         test_nv_backward_tensor_scales_span_all_rows()
+
+
+@pytest.mark.parametrize("seed,k", [(8, 2), (9, 4)])
+def test_nv_expert_weight_grads_are_the_layer_backward(seed, k):
+    # the per-expert evaluation (tensor scales from per-token maxima) equals the
+    # whole backward on every expert
+    x, w_r, W1, W3, W2, dO, _ = _nv_train_case(seed, T=40, k=k)
+    dO = dO * np.exp(np.random.default_rng(seed).normal(0, 1, (dO.shape[0], 1)))
+    full = O.nv_layer_bwd(x, w_r, W1, W3, W2, dO, k)
+    part = O.nv_expert_weight_grads(x, w_r, W1, W3, W2, dO, k, experts=range(4))
+    assert np.array_equal(part["counts"], full["counts"])
+    for key in ("dW1", "dW3", "dW2"):
+        for e in range(4):
+            np.testing.assert_allclose(part[key][e], full[key][e], rtol=1e-12, atol=1e-12, err_msg=f"{key}[{e}]")
