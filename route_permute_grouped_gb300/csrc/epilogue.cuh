@@ -97,21 +97,22 @@ __device__ __forceinline__ void tmem_ld32_f(uint32_t taddr, float* f) {
 __device__ __forceinline__ float silu_fast(float z) { return z / (1.0f + __expf(-z)); }
 
 // FFN1, rows row0..row0+31 all inside the expert: a = SiLU(h1) h3 (and h1, h3
-// when saving) for the 128 F-columns n0.. of the tile, in 64-column boxes.
-__device__ __forceinline__ void epi_ffn1_tma(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane,
-                                             int row0, Stager& st, const CUtensorMap* map_a,
-                                             const CUtensorMap* map_h13) {
+// when saving) for the 64 * nch F-columns n0.. (h1 at TMEM columns 0.., h3 at
+// `up` ..), in 64-column boxes.
+__device__ __forceinline__ void epi_ffn1_tma(const GemmParams& p, int n0, uint32_t tacc, int lane, int row0,
+                                             Stager& st, const CUtensorMap* map_a, const CUtensorMap* map_h13,
+                                             int nch = 2, int up = 128) {
   const bool save = p.out1 != nullptr;
 #pragma unroll 1
-  for (int cc = 0; cc < 2; ++cc) {
-    const int col = ti.n0 + cc * 64;
+  for (int cc = 0; cc < nch; ++cc) {
+    const int col = n0 + cc * 64;
     if (col >= p.F) break;  // uniform over the warp
     uint8_t* buf = st.next(lane);
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float g[32], u[32];
       tmem_ld32_f(tacc + (cc * 2 + h) * 32, g);
-      tmem_ld32_f(tacc + 128 + (cc * 2 + h) * 32, u);
+      tmem_ld32_f(tacc + up + (cc * 2 + h) * 32, u);
 #pragma unroll
       for (int j = 0; j < 32; ++j) g[j] = silu_fast(g[j]) * u[j];
       stage_bf16x32(buf, lane, h, g);
@@ -124,7 +125,7 @@ __device__ __forceinline__ void epi_ffn1_tma(const GemmParams& p, const TileInfo
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           float v[32];
-          tmem_ld32_f(tacc + part * 128 + (cc * 2 + h) * 32, v);
+          tmem_ld32_f(tacc + part * up + (cc * 2 + h) * 32, v);
           stage_bf16x32(b, lane, h, v);
         }
         st.commit2d(lane, map_h13, b, part * p.F + col, row0);

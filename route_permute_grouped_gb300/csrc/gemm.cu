@@ -78,18 +78,19 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float* f) {
 }
 
 // FFN1: columns [0,128) of the accumulator hold h1 = x W1 for F columns
-// n0..n0+127, columns [128,256) hold h3 = x W3 for the same F columns.
-__device__ __forceinline__ void epi_ffn1(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int r) {
-  const int row = ti.m0 + r;
-  const bool valid = row < ti.m_end;
+// n0..n0+127, columns [128,256) hold h3 = x W3 for the same F columns (a half
+// tile: 64 columns each, h3 from column `up` = 64; nc = 2 chunks of 32).
+__device__ __forceinline__ void epi_ffn1(const GemmParams& p, int n0, int row, int m_end, uint32_t tacc,
+                                         int nc = 4, int up = 128) {
+  const bool valid = row < m_end;
   __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(p.out0);
   __nv_bfloat16* h13 = reinterpret_cast<__nv_bfloat16*>(p.out1);
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < nc; ++c) {
     float g[32], u[32];
     tmem_ld32f(tacc + c * 32, g);
-    tmem_ld32f(tacc + 128 + c * 32, u);
-    const int col = ti.n0 + c * 32;
+    tmem_ld32f(tacc + up + c * 32, u);
+    const int col = n0 + c * 32;
     if (valid && col < p.F) {
       float o[32];
 #pragma unroll
@@ -139,6 +140,23 @@ __device__ __forceinline__ void epi_store(const TileInfo& ti, uint32_t tacc, int
         }
       }
     }
+  }
+}
+
+// Plain store of a half tile (an M = 128 pair MMA): warp q's 32 rows row0..
+// (of the CTA's 64) hold output columns n0 + 128 (q / 2) .. at TMEM columns
+// 0..127 (lanes 64.. carry the odd CTA's B half).
+__device__ __forceinline__ void epi_store_half(const GemmParams& p, const TileInfo& ti, uint32_t tacc, int lane, int q,
+                                            int r, int row0, bool full_rows, bool any_rows, Stager& st,
+                                            const CUtensorMap* map) {
+  TileInfo tw = ti;
+  tw.n0 = ti.n0 + 128 * (q >> 1);
+  if (full_rows) {
+    if (p.out_fp32) epi_store_tma<true, false>(tw, tacc, lane, row0, p.H, st, map, 2);
+    else epi_store_tma<false, false>(tw, tacc, lane, row0, p.H, st, map, 2);
+  } else if (any_rows) {
+    tw.m0 = row0 - 32 * q;  // epi_store takes row = m0 + r, r = 32 q + lane
+    epi_store(tw, tacc, r, 4, p.H, p.H, p.out0, p.out_fp32 != 0, 0);
   }
 }
 
@@ -590,6 +608,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
     const uint32_t idesc = TR::kNv ? idesc_nvf4_f32(TR::kTileM, kNvTileN)
                            : TR::kMx ? idesc_mxf8_f32(TR::kTileM, kMxBN)
                                      : idesc_bf16_f32(TR::kTileM, p.bn, TR::A_MN, TR::B_MN);
+    // half tiles (kHalfTiles): M = 128 over the pair
+    const uint32_t idesc_half = idesc_bf16_f32(TR::kTileM / 2, p.bn, TR::A_MN, TR::B_MN);
     // MXFP8: descriptors of the stage's scale blocks (32 rows of 16 bytes,
     // no swizzle, 8-row groups 128 bytes apart) for the copies into TMEM
     const uint32_t sf_lo0 = sdesc_lo(smem_u32(smem) + (TR::kNv ? kNvSfOff : kMxSfOff), 128);
@@ -720,10 +740,11 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         if (lane == 0) {
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo;
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(stage) * stage_lo;
+          const uint32_t id = (kHalfTiles<KIND> && ti.half) ? idesc_half : idesc;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             if constexpr (PAIR)
-              umma2_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              umma2_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, id, (kb > 0 || kk > 0) ? 1u : 0u);
             else
               umma_bf16_w(d_tmem, a_lo + kk * kAStep, b_lo + kk * kBStep, d_hi, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
@@ -787,17 +808,29 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
       const TileInfo ti = decode_tile<KIND>(p, s_cum, s_off, t, rank);
       // this warp's 32 rows: a full block leaves through TMA boxes; a block
       // that crosses the end of the expert's rows uses masked per-thread stores
-      const int row0 = ti.m0 + 32 * q;
+      // a half tile: this warp's 32 of the CTA's 64 rows, and the columns of
+      // the B half its TMEM lanes hold (lanes 64.. : the odd CTA's half)
+      const bool half = kHalfTiles<KIND> && ti.half;
+      const int row0 = ti.m0 + 32 * (half ? (q & 1) : q);
       const bool full_rows = row0 + 32 <= ti.m_end;
       const bool any_rows = row0 < ti.m_end;
       if (!mbar_wait_bounded(tfull + acc, acc_phase, s_abort, lim, p.status, 4)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * kAccStride) + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (KIND == KIND_FFN1) {
-        if (full_rows) epi_ffn1_tma(p, ti, tacc, lane, row0, st, &mo0, &mo1);
-        else if (any_rows) epi_ffn1(p, ti, tacc, r);
+        if (half) {
+          // 64 F columns n0 + 64 (q / 2) ..: h1 at TMEM columns 0..63, h3 at 64..127
+          const int n0h = ti.n0 + 64 * (q >> 1);
+          if (full_rows) epi_ffn1_tma(p, n0h, tacc, lane, row0, st, &mo0, &mo1, 1, 64);
+          else if (any_rows) epi_ffn1(p, n0h, row0 + lane, ti.m_end, tacc, 2, 64);
+        } else {
+          if (full_rows) epi_ffn1_tma(p, ti.n0, tacc, lane, row0, st, &mo0, &mo1);
+          else if (any_rows) epi_ffn1(p, ti.n0, ti.m0 + r, ti.m_end, tacc);
+        }
       } else if constexpr (KIND == KIND_FFN2) {
-        if (full_rows) {
+        if (half) {
+          epi_store_half(p, ti, tacc, lane, q, r, row0, full_rows, any_rows, st, &mo0);
+        } else if (full_rows) {
           if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0);
           else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
         } else if (any_rows) {
@@ -846,7 +879,9 @@ __global__ void __launch_bounds__(KindTraits<KIND>::kThreadsK, 1)
         if (full_rows) epi_dgrad2_tma(p, ti, tacc, lane, row0, st, &mo0, 2 * part, 2 * part + 2);
         else if (any_rows) epi_dgrad2(p, ti, tacc, r, false, 4 * part, 4 * part + 4);
       } else if constexpr (KIND == KIND_DGRAD1) {
-        if (full_rows) {
+        if (half) {
+          epi_store_half(p, ti, tacc, lane, q, r, row0, full_rows, any_rows, st, &mo0);
+        } else if (full_rows) {
           if (p.out_fp32) epi_store_tma<true, false>(ti, tacc, lane, row0, p.H, st, &mo0);
           else epi_store_tma<false, false>(ti, tacc, lane, row0, p.H, st, &mo0);
         } else if (any_rows) {

@@ -216,7 +216,18 @@ struct TileInfo {
   int krow_end;
   int mt;      // grouped kinds: global m tile (tiles of all earlier groups + this group's)
   int nb;      // n tile within the group
+  int half;    // an expert's last m tile with at most 128 rows: an M = 128 pair MMA (64 rows per CTA)
 };
+
+// Kinds whose last m tile of an expert runs as an M = 128 pair MMA when it
+// holds at most 128 rows (the tail of a ragged expert then costs half the
+// tensor work). With cta_group::2 and M = 128 each CTA supplies 64 rows of A
+// and holds its 64 rows' accumulator twice over in tensor memory: lanes 0..63
+// with the N columns of the even CTA's B half, lanes 64..127 with the odd
+// CTA's, both at columns 0 .. N/2 - 1 (measured on the GB300 with an in-bounds
+// probe before use).
+template <int KIND>
+constexpr bool kHalfTiles = (KIND == KIND_FFN1 || KIND == KIND_FFN2 || KIND == KIND_DGRAD1);
 
 template <int KIND>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_cum, const int* s_off,
@@ -246,9 +257,15 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
   }
   ti.mt = s_cum[lo] / p.n_tiles + mb;
   ti.nb = nb;
+  ti.half = 0;
+  if constexpr (kHalfTiles<KIND>) {
+    const int me = (s_cum[lo + 1] - s_cum[lo]) / p.n_tiles;
+    ti.half = (mb == me - 1 && s_off[lo + 1] - s_off[lo] - mb * KindTraits<KIND>::kTileM <= kBM) ? 1 : 0;
+  }
   if constexpr (KindTraits<KIND>::kGroupedRows || KIND == KIND_ROUTER || KIND == KIND_ROUTER_DX) {
-    // a pair tile spans 256 rows: this CTA's 128 start at rank * 128
-    ti.m0 = s_off[lo] + mb * KindTraits<KIND>::kTileM + rank * kBM;
+    // a pair tile spans 256 rows: this CTA's 128 start at rank * 128 (a half
+    // tile's 64 at rank * 64)
+    ti.m0 = s_off[lo] + mb * KindTraits<KIND>::kTileM + rank * (ti.half ? kBM / 2 : kBM);
     ti.m_end = s_off[lo + 1];
     ti.kb0 = 0;
     ti.nkb = p.kb_total;
@@ -363,6 +380,13 @@ __device__ __forceinline__ void issue_loads_pair(const GemmParams& p, const Tile
   tma_load_2d_pair(sA, ma, bar_cluster, kk, ti.m0);
   if constexpr (KIND == KIND_FFN1) {
     const int brow = ti.g * p.H + kk;
+    if (ti.half) {
+      // half tile: this CTA's B half holds W1 and W3 columns n0 + 64 rank ..
+      // (64 each), so a row's gate and up values share a TMEM lane
+      tma_load_2d_pair(sB, mb0, bar_cluster, ti.n0 + 64 * rank, brow);
+      tma_load_2d_pair(sB + 8192, mb1, bar_cluster, ti.n0 + 64 * rank, brow);
+      return;
+    }
     const CUtensorMap* m = rank == 0 ? mb0 : mb1;
     tma_load_2d_pair(sB, m, bar_cluster, ti.n0, brow);
     tma_load_2d_pair(sB + 8192, m, bar_cluster, ti.n0 + 64, brow);
