@@ -505,6 +505,102 @@ def run_ours(args, ls, rank, world, local_rank):
     ms_fwd = f0.elapsed_time(f1) / args.steps
     ms_fwd = max_over_ranks(ms_fwd, world, dev)
 
+    # ---------------- end to end through the C ABI with host buffers (right after
+    # the device-timed steps, so that both see the GPU in the same state)
+    flops_step = layer_flops(ls, training)
+    e2e = None
+    if not args.no_e2e:
+        hx = d["x"].cpu().pin_memory()
+        hdO = d["dO"].cpu().pin_memory() if training else None
+        hy = torch.empty((ls.T, ls.H), dtype=torch.bfloat16).pin_memory()
+        hdx = torch.empty((ls.T, ls.H), dtype=torch.bfloat16).pin_memory() if training else None
+        haux = torch.empty(1, dtype=torch.float32).pin_memory()
+        # every step copies its inputs in from pinned host memory and its
+        # results out; the copies run on two copy streams, double-buffered on
+        # the device, so they overlap the neighbouring steps' compute. In a
+        # training step they run beside the backward's GEMMs (compute-bound):
+        # once step i's forward is done, step i-1's results go out and step
+        # i+1's inputs come in, away from the forward's memory-bound kernels
+        comp = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        xd = [torch.empty_like(d["x"]) for _ in range(2)]
+        dOd = [torch.empty_like(d["dO"]) for _ in range(2)] if training else None
+        ys = [y, torch.empty_like(y)]
+        gbuf = None
+        if training:
+            gbuf = [grads, dict(grads, dx=torch.empty_like(grads["dx"]), aux_loss=torch.zeros_like(grads["aux_loss"]))]
+        ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b on the device
+        ev_used = [torch.cuda.Event() for _ in range(2)]  # compute finished with inputs / outputs of b
+        ev_read = [torch.cuda.Event() for _ in range(2)]  # outputs of b copied to the host
+        ev_fwd = torch.cuda.Event()                       # the current step's forward is done
+
+        def issue_h2d(i, after=None):
+            b = i % 2
+            if after is not None:
+                s_in.wait_event(after)
+            with torch.cuda.stream(s_in):
+                xd[b].copy_(hx, non_blocking=True)
+                if training:
+                    dOd[b].copy_(hdO, non_blocking=True)
+                ev_in[b].record(s_in)
+
+        def issue_d2h(i, after):
+            b = i % 2
+            s_out.wait_event(after)
+            with torch.cuda.stream(s_out):
+                hy.copy_(ys[b], non_blocking=True)
+                if training:
+                    hdx.copy_(gbuf[b]["dx"], non_blocking=True)
+                    haux.copy_(gbuf[b]["aux_loss"], non_blocking=True)
+                ev_read[b].record(s_out)
+
+        def e2e_step(i, n):
+            b = i % 2
+            comp.wait_event(ev_in[b])
+            if i >= 2:
+                comp.wait_event(ev_read[b])
+            ops.layer_fwd(cfg, xd[b], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"],
+                          Ws, saved=saved, ws=ws, y=ys[b])
+            if training:
+                ev_fwd.record(comp)  # step i-1 is complete as well
+                if i >= 1:
+                    issue_d2h(i - 1, ev_fwd)
+                if i + 1 < n:
+                    issue_h2d(i + 1, ev_fwd)
+                ops.layer_bwd(cfg, dOd[b], xd[b], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws,
+                              grads=gbuf[b])
+            ev_used[b].record(comp)
+            if not training:
+                issue_d2h(i, ev_used[b])
+                if i + 2 < n:
+                    issue_h2d(i + 2, ev_used[b])
+
+        def e2e_run(n):
+            issue_h2d(0)
+            if n > 1 and not training:
+                issue_h2d(1)
+            for i in range(n):
+                e2e_step(i, n)
+            if training:
+                issue_d2h(n - 1, ev_used[(n - 1) % 2])
+            comp.wait_event(ev_read[(n - 1) % 2])  # the last results are on the host
+
+        e2e_run(2)
+        torch.cuda.synchronize()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(comp)
+        s_in.wait_stream(comp)  # the first copies start inside the timed region
+        e2e_run(args.steps)
+        g1.record(comp)
+        torch.cuda.synchronize()
+        ms_e2e = g0.elapsed_time(g1) / args.steps
+        ms_e2e = max_over_ranks(ms_e2e, world, dev)
+        h2d = hx.numel() * 2 + (hdO.numel() * 2 if training else 0)
+        d2h = hy.numel() * 2 + ((hdx.numel() * 2 + 4) if training else 0)
+        e2e = {"value": round(job_throughput(flops_step, ms_e2e, world), 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)}
+
     # ---------------- the same step captured once as a CUDA graph and replayed
     # (device-side offsets: no host synchronisation inside a step)
     graph = None
@@ -819,84 +915,6 @@ def run_ours(args, ls, rank, world, local_rank):
     flops_step = layer_flops(ls, training)
     value = job_throughput(flops_step, ms, world)
     fwd_value = job_throughput(layer_flops(ls, False), ms_fwd, world)
-
-    # ---------------- end to end through the C ABI with host buffers
-    e2e = None
-    if not args.no_e2e:
-        hx = d["x"].cpu().pin_memory()
-        hdO = d["dO"].cpu().pin_memory() if training else None
-        hy = torch.empty((ls.T, ls.H), dtype=torch.bfloat16).pin_memory()
-        hdx = torch.empty((ls.T, ls.H), dtype=torch.bfloat16).pin_memory() if training else None
-        haux = torch.empty(1, dtype=torch.float32).pin_memory()
-        # every step copies its inputs in from pinned host memory and its
-        # results out; the copies run on two copy streams, double-buffered on
-        # the device, so they overlap the neighbouring steps' compute
-        comp = torch.cuda.current_stream()
-        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        xd = [torch.empty_like(d["x"]) for _ in range(2)]
-        dOd = [torch.empty_like(d["dO"]) for _ in range(2)] if training else None
-        ys = [y, torch.empty_like(y)]
-        gbuf = None
-        if training:
-            gbuf = [grads, dict(grads, dx=torch.empty_like(grads["dx"]), aux_loss=torch.zeros_like(grads["aux_loss"]))]
-        ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b on the device
-        ev_used = [torch.cuda.Event() for _ in range(2)]  # compute finished with inputs / outputs of b
-        ev_read = [torch.cuda.Event() for _ in range(2)]  # outputs of b copied to the host
-
-        def issue_h2d(i):
-            b = i % 2
-            if i >= 2:
-                s_in.wait_event(ev_used[b])
-            with torch.cuda.stream(s_in):
-                xd[b].copy_(hx, non_blocking=True)
-                if training:
-                    dOd[b].copy_(hdO, non_blocking=True)
-                ev_in[b].record(s_in)
-
-        def e2e_step(i):
-            b = i % 2
-            comp.wait_event(ev_in[b])
-            if i >= 2:
-                comp.wait_event(ev_read[b])
-            ops.layer_fwd(cfg, xd[b], d["router_w"], d["W1"], d["W3"], d["W2"], d["expert_bias"], d["logit_bias"],
-                          Ws, saved=saved, ws=ws, y=ys[b])
-            if training:
-                ops.layer_bwd(cfg, dOd[b], xd[b], d["router_w"], d["W1"], d["W3"], d["W2"], saved, ws=ws,
-                              grads=gbuf[b])
-            ev_used[b].record(comp)
-            s_out.wait_event(ev_used[b])
-            with torch.cuda.stream(s_out):
-                hy.copy_(ys[b], non_blocking=True)
-                if training:
-                    hdx.copy_(gbuf[b]["dx"], non_blocking=True)
-                    haux.copy_(gbuf[b]["aux_loss"], non_blocking=True)
-                ev_read[b].record(s_out)
-
-        def e2e_run(n):
-            issue_h2d(0)
-            if n > 1:
-                issue_h2d(1)
-            for i in range(n):
-                e2e_step(i)
-                if i + 2 < n:
-                    issue_h2d(i + 2)
-            comp.wait_event(ev_read[(n - 1) % 2])  # the last results are on the host
-
-        e2e_run(2)
-        torch.cuda.synchronize()
-        barrier()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(comp)
-        s_in.wait_stream(comp)  # the first copies start inside the timed region
-        e2e_run(args.steps)
-        g1.record(comp)
-        torch.cuda.synchronize()
-        ms_e2e = g0.elapsed_time(g1) / args.steps
-        ms_e2e = max_over_ranks(ms_e2e, world, dev)
-        h2d = hx.numel() * 2 + (hdO.numel() * 2 if training else 0)
-        d2h = hy.numel() * 2 + ((hdx.numel() * 2 + 4) if training else 0)
-        e2e = {"value": round(job_throughput(flops_step, ms_e2e, world), 3), "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)}
 
     # ---------------- CPU baseline (rank 0, N = 1)
     cpu = None

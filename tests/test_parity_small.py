@@ -127,6 +127,30 @@ def test_grouped_swiglu_ffn(name):
     assert_close("y_perm", f64(y_perm), y_ref)
 
 
+def test_grouped_swiglu_ffn_tile_boundaries():
+    # expert row counts on every side of the tile boundaries: an expert's last
+    # m tile holding 1, 63, 64, 65, 127 or 128 rows runs as a half-height
+    # (M = 128) pair tile, 129..256 rows as a whole tile; an empty expert; F and
+    # H ragged against the 128- and 256-column tiles
+    counts = [1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 384, 385, 0, 512, 640]
+    E, H, F = len(counts), 384, 320
+    R = int(sum(counts))
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    g = torch.Generator().manual_seed(17)
+    xp = torch.randn((R, H), generator=g).to(torch.bfloat16)
+    W1 = (torch.randn((E, H, F), generator=g) * H ** -0.5).to(torch.bfloat16)
+    W3 = (torch.randn((E, H, F), generator=g) * H ** -0.5).to(torch.bfloat16)
+    W2 = (torch.randn((E, F, H), generator=g) * F ** -0.5).to(torch.bfloat16)
+    cfg = ops.make_config(R, H, E, 1, F)
+    y_perm, h13, a = ops.grouped_swiglu_ffn(cfg, xp.cuda(), torch.from_numpy(offs.astype(np.int32)).cuda(),
+                                            W1.cuda(), W3.cuda(), W2.cuda(), save=True)
+    torch.cuda.synchronize()
+    h13_ref, a_ref, y_ref = O.grouped_swiglu(f64(xp), offs, f64(W1), f64(W3), f64(W2))
+    assert_close("h13", f64(h13), h13_ref)
+    assert_close("a", f64(a), a_ref)
+    assert_close("y_perm", f64(y_perm), y_ref)
+
+
 @pytest.mark.parametrize("name", ["tiny", "e128_k8", "dsv3_small"])
 def test_unpermute_combine(name):
     ls, d = _inputs(name)
