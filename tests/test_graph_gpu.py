@@ -66,3 +66,46 @@ def test_training_step_graph_replay(name, force):
     torch.cuda.synchronize()
     for a, b in zip(replayed, _snapshot(y, grads)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("prec", ["mxfp8", "nvfp4"])
+def test_low_precision_training_step_graph_replay(prec):
+    # the MXFP8 and NVFP4 training steps keep their scales and tensor maxima
+    # on the device too: one step captures and replays bit for bit
+    ls = synth.shape("tiny", T=300, H=256, E=8, k=2, F=256)
+    d = synth.make_layer(ls, seed=5, device="cuda", training=True)
+    cfg = ops.config_from_shape(ls, aux_coeff=1e-2)
+    grads = ops.alloc_grads(cfg)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    if prec == "mxfp8":
+        wf = ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"])
+        wb = ops.mx_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+        ws, saved = ops.mx_train_workspace(cfg), ops.alloc_saved_mxfp8(cfg)
+        fwd, bwd = ops.layer_fwd_mxfp8_train, ops.layer_bwd_mxfp8
+    else:
+        wf = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
+        wb = ops.nv_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+        ws, saved = ops.nv_train_workspace(cfg), ops.alloc_saved(cfg)
+        fwd, bwd = ops.layer_fwd_nvfp4_train, ops.layer_bwd_nvfp4
+
+    def step():
+        fwd(cfg, d["x"], d["router_w"], wf, saved, d["expert_bias"], d["logit_bias"], ws=ws, y=y)
+        bwd(cfg, d["dO"], d["x"], d["router_w"], wb, saved, ws=ws, grads=grads)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = _snapshot(y, grads)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for a in (y, *grads.values()):
+        a.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    for a, b in zip(eager, _snapshot(y, grads)):
+        assert torch.equal(a, b)
