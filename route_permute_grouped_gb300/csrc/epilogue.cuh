@@ -270,8 +270,9 @@ __device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile
 // DGRAD2, rows all inside the expert: dh1 = da h3 SiLU'(h1), dh3 = da SiLU(h1).
 // Per 64-column chunk each thread reads its row's 64 values of the saved h1
 // and h3 with vector loads (not through the TMA unit, whose queue holds the
-// operand loads of the main loop), reads da from TMEM, writes dh1 and dh3 into
-// the warp's two staging boxes and stores them with the TMA.
+// operand loads of the main loop), reads da from TMEM, and the warp's one
+// staging box carries dh1 to a TMA store, then dh3 (held in registers
+// meanwhile).
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -298,8 +299,11 @@ __device__ __forceinline__ void epi_dgrad2_tma(const GemmParams& p, const TileIn
     float da0[32], da1[32];
     tmem_ld32_f(tacc + (cc * 2) * 32, da0);
     tmem_ld32_f(tacc + (cc * 2 + 1) * 32, da1);
-    uint8_t *b1, *b3;
-    st.both(lane, b1, b3);  // the previous boxes have left both buffers
+    // one 4 KB staging box per warp: dh1 leaves first, dh3 waits in registers
+    uint8_t* b1 = st.base;
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    uint32_t keep[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float* da = j < 4 ? da0 : da1;
@@ -323,13 +327,26 @@ __device__ __forceinline__ void epi_dgrad2_tma(const GemmParams& p, const TileIn
       }
       const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
       *reinterpret_cast<uint4*>(b1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-      *reinterpret_cast<uint4*>(b3 + off) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) keep[j][q] = o3[q];
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       tma_store_2d(map_out, b1, col, row0);
-      tma_store_2d(map_out, b3, p.F + col, row0);
+      bulk_commit();
+      bulk_wait_read0();
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
+      *reinterpret_cast<uint4*>(b1 + off) = make_uint4(keep[j][0], keep[j][1], keep[j][2], keep[j][3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map_out, b1, p.F + col, row0);
       bulk_commit();
     }
     st.n += 2;

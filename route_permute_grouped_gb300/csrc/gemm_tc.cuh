@@ -127,7 +127,9 @@ struct KindTraits {
   static constexpr int kBOff = (KIND == KIND_ROUTER_DW) ? 2 * kABytes : kABytes;
   // DGRAD2 runs eight epilogue warps (two per TMEM lane quadrant, each taking
   // half of the tile's columns) to hide the latency of its loads of the saved
-  // pre-activations; it and DGRAD2R (third staging box) give up one stage
+  // pre-activations, with one 4 KB staging box each (dh1 leaves before dh3
+  // is staged), which keeps six stages; DGRAD2R (third staging box) gives up
+  // one stage
   // FFN1_MX runs twelve (three per TMEM lane quadrant, one 32-column block of
   // the 96 SwiGLU columns each): its tiles are short (K / 128 blocks of
   // 128) and its epilogue (SiLU, quantisation) long
@@ -141,7 +143,7 @@ struct KindTraits {
   static constexpr int kThreadsK = 64 + 32 * kEpiWarps;
   // WGRAD stores its fp32 output straight from tensor memory (no staging
   // boxes), which leaves room for a seventh stage
-  static constexpr int kStages = (KIND == KIND_DGRAD2R || KIND == KIND_DGRAD2 || kNv) ? 5
+  static constexpr int kStages = (KIND == KIND_DGRAD2R || kNv) ? 5
                                  : (KIND == KIND_WGRAD)                            ? 7
                                  : kPair                                           ? 6
                                  : (KIND == KIND_ROUTER_DW)                        ? 3
@@ -150,6 +152,7 @@ struct KindTraits {
       (KIND == KIND_DGRAD2R) ? 3 * 4096
       : (KIND == KIND_ROUTER) ? 4096  // selection scratch, 32 KB in all
       : (KIND == KIND_FFN1_MX || KIND == KIND_FFN1_NV || KIND == KIND_DGRAD2_MX || KIND == KIND_WGRAD) ? 0
+      : (KIND == KIND_DGRAD2)                                                                           ? 4096
                                                                                                        : 2 * 4096;  // staging
   // the router's B is bn x 64 (bn <= 256): its stages are packed at
   // router_stage_bytes(bn) so narrow routers keep more k blocks in flight
