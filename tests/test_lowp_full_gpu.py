@@ -154,9 +154,11 @@ def test_nvfp4_train_qwen3_full_sampled():
     for e in sample:
         for key in ("dW1", "dW3", "dW2"):
             want = ref[key][e]
-            # up to two flipped E2M1 codes of dy_perm (see assert_close_but_flips)
+            # flipped E2M1 codes of dy_perm (see assert_close_but_flips): an
+            # expert of ~1000 rows x 4096 columns can see a few, each a rank-one
+            # error; a GEMM error would not be of low rank
             assert_close_but_flips(f"{key} (expert {e}, {counts[e]} rows)", f64(g[key][e]), want,
-                                   atol=wgrad_atol(want))
+                                   atol=wgrad_atol(want), rank=4)
     # the bf16 step on the same inputs (GPU): the NVFP4 input gradient differs
     # from it by FP4 rounding of two chained GEMMs
     ws16, sv16 = ops.workspace(cfg, True), ops.alloc_saved(cfg)
