@@ -45,6 +45,31 @@ def test_nv_quantize_rows_bit_exact():
     assert np.array_equal(_unpack(q.cpu().numpy()), rq)
 
 
+def test_nv_quantize_at_e2m1_boundaries():
+    # (1) exact ties: with the tensor maximum 2688 * 2^-4 alone in its block,
+    # g = 2^-4, and a block whose maximum is 6 * 2^(j-4) has the scale 2^j, so
+    # its elements B * 2^(j-4) divide to the E2M1 decision boundaries B exactly
+    # (ties to the even code); (2) 4M random elements under random block and
+    # row scales, where a few quotients fall within a few fp32 ulps of a
+    # boundary: every code and scale as the definition gives them
+    bnd = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    base = np.concatenate([[6.0], bnd, -bnd, [0.0]])
+    rows = [np.concatenate([[2688.0 * 2.0 ** -4], np.zeros(15)])]
+    for j in range(-6, 6):
+        rows.append(base * 2.0 ** (j - 4))
+    x1 = torch.from_numpy(np.stack(rows).reshape(1, -1).repeat(16, axis=0)).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(31)
+    x2 = (torch.randn((4096, 1024), generator=g) * torch.exp(torch.randn((4096, 64, 1), generator=g) * 2.0)
+          .repeat(1, 1, 16).reshape(4096, 1024)).to(torch.bfloat16)
+    for x in (x1, x2):
+        q, sc, gg = ops.nv_quantize(x.cuda())
+        torch.cuda.synchronize()
+        rq, rs, rg = O.nv_quantize(f64(x).astype(np.float32), axis=1)
+        assert gg.item() == float(rg)
+        assert np.array_equal(sc.cpu().numpy(), rs)
+        assert np.array_equal(_unpack(q.cpu().numpy()), rq)
+
+
 @pytest.mark.parametrize("E,K,N", [(3, 512, 200), (2, 256, 384)])
 def test_nv_weight_quantization_bit_exact(E, K, N):
     W = _bf16((E, K, N), K ** -0.5, 11)
