@@ -11,7 +11,9 @@
  * ---------------------------------------
  *  - All tensors are dense, row-major, in DEVICE memory of the current CUDA
  *    device, and allocated by the caller. The library allocates nothing on the
- *    GPU and keeps no per-call state. Pointers must be 16-byte aligned.
+ *    GPU and keeps no per-call state. Pointers must be 16-byte aligned
+ *    (every device pointer an entry point takes, the fields of the structs
+ *    it takes included, is checked: a misaligned one is MOE_ERR_INVALID_ARG).
  *  - bf16 tensors are passed as moe_bf16* (IEEE bfloat16 bit patterns).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call only enqueues work on `stream` and returns; nothing synchronises

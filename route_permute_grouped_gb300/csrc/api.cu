@@ -4,6 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -305,6 +306,19 @@ static int check_cfg(const moe_config* c) {
 int validate_config(const moe_config* c) { return check_cfg(c); }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Every device pointer an entry point takes must be 16-byte aligned: the
+// kernels reach them with 16-byte vector accesses and TMA copies, which fault
+// on a misaligned address. Null passes here (the null checks are separate).
+static bool all_aligned16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!aligned16(p)) return false;
+  return true;
+}
+static bool saved_aligned16(const moe_fwd_saved* sv) {
+  return sv == nullptr || all_aligned16({sv->topk_idx, sv->topk_gate, sv->logits, sv->row_id_map, sv->counts,
+                                         sv->offsets, sv->x_perm, sv->h13, sv->a, sv->y_perm, sv->aux_partials,
+                                         sv->h13_shared, sv->a_shared});
+}
 
 static int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
@@ -690,7 +704,8 @@ int moe_router_topk(const moe_config* cfg, const moe_bf16* x, const moe_bf16* ro
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x || !router_w || !topk_idx || !topk_gate || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({x, router_w, expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials, ws}))
+    return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_layout(c, false).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   MOE_TRY(run_router(c, reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(router_w),
                      expert_bias, logit_bias, topk_idx, topk_gate, logits_out, aux_partials,
@@ -706,7 +721,7 @@ int moe_permute(const moe_config* cfg, const moe_bf16* x, const int32_t* topk_id
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x || !topk_idx || !x_perm || !row_id_map || !counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({x, topk_idx, x_perm, row_id_map, counts, offsets, ws})) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, false);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   MOE_CUDA(launch_permute(c, reinterpret_cast<const __nv_bfloat16*>(x), topk_idx,
@@ -723,8 +738,7 @@ int moe_grouped_swiglu_ffn(const moe_config* cfg, const moe_bf16* x_perm, const 
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!x_perm || !offsets || !W1 || !W3 || !W2 || !y_perm || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x_perm) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(y_perm) ||
-      !aligned16(ws) || (h13_save && !aligned16(h13_save)) || (a_save && !aligned16(a_save)))
+  if (!all_aligned16({x_perm, offsets, W1, W3, W2, h13_save, a_save, y_perm, ws}))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, false);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -741,7 +755,7 @@ int moe_unpermute_combine(const moe_config* cfg, const void* y_perm, const int32
   MOE_TRY(check_cfg(cfg));
   const moe_config& c = *cfg;
   if (!y_perm || !row_id_map || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(y_perm) || !aligned16(y) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({y_perm, row_id_map, topk_gate, shared_out, y})) return MOE_ERR_INVALID_ARG;
   MOE_CUDA(launch_combine(c, y_perm, row_id_map, topk_gate, shared_out, y, static_cast<cudaStream_t>(stream)));
   stage_done(static_cast<cudaStream_t>(stream), STAGE_COMBINE, 1);
   return MOE_OK;
@@ -756,8 +770,8 @@ int moe_layer_fwd(const moe_config* cfg, const moe_bf16* x, const moe_bf16* rout
   const moe_config& c = *cfg;
   if (!x || !router_w || !W1 || !W3 || !W2 || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (c.F_shared && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) ||
-      !aligned16(y) || !aligned16(ws))
+  if (!all_aligned16({x, router_w, expert_bias, logit_bias, W1, W3, W2, Ws1, Ws3, Ws2, y, ws}) ||
+      !saved_aligned16(saved))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, false);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -1137,16 +1151,16 @@ int moe_layer_bwd(const moe_config* cfg, const moe_bf16* dO, const moe_bf16* x, 
   const moe_config& c = *cfg;
   if (!dO || !x || !router_w || !W1 || !W3 || !W2 || !saved || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dO) || !aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({dO, x, router_w, W1, W3, W2, Ws1, Ws3, Ws2, dx, dW_router, dW1, dW3, dW2, dWs1, dWs3, dWs2,
+                      aux_loss_out, ws}) ||
+      !saved_aligned16(saved))
+    return MOE_ERR_INVALID_ARG;
   if (!saved->topk_idx || !saved->topk_gate || !saved->logits || !saved->row_id_map || !saved->counts ||
       !saved->offsets || !saved->x_perm || !saved->h13 || (!saved->a) != (!saved->y_perm))
     return MOE_ERR_INVALID_ARG;
   if (c.aux_coeff != 0.0f && !saved->aux_partials) return MOE_ERR_INVALID_ARG;
   if (c.F_shared != 0) {
     if (!Ws1 || !Ws3 || !Ws2 || !dWs1 || !dWs3 || !dWs2 || !saved->h13_shared || !saved->a_shared)
-      return MOE_ERR_INVALID_ARG;
-    if (!aligned16(Ws1) || !aligned16(Ws3) || !aligned16(Ws2) || !aligned16(dWs1) || !aligned16(dWs3) ||
-        !aligned16(dWs2) || !aligned16(saved->h13_shared) || !aligned16(saved->a_shared))
       return MOE_ERR_INVALID_ARG;
   }
   const WsLayout L = ws_layout(c, true);
@@ -1176,7 +1190,7 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_bf16* W1, const moe
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_mx_shape(*cfg));
   if (!W1 || !W3 || !W2 || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w13) || !aligned16(w->w2))
+  if (!all_aligned16({W1, W3, W2, w->w13, w->sf13, w->w2, w->sf2}))
     return MOE_ERR_INVALID_ARG;
   MOE_CUDA(launch_mx_quantize_weights(*cfg, reinterpret_cast<const __nv_bfloat16*>(W1),
                                       reinterpret_cast<const __nv_bfloat16*>(W3),
@@ -1189,7 +1203,7 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_bf16* W1, const moe
 int moe_mx_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, void* stream) {
   NvtxRange nvtx("moe_mx_quantize");
   if (!x || !q || !scales || M < 0 || K < kMxBlock || K % kMxBlock != 0) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({x, q, scales})) return MOE_ERR_INVALID_ARG;
   MOE_CUDA(launch_mx_quantize_rows(reinterpret_cast<const __nv_bfloat16*>(x), M, K, q, scales,
                                    static_cast<cudaStream_t>(stream)));
   count_launches(M > 0 ? 1 : 0);
@@ -1211,8 +1225,8 @@ int moe_layer_fwd_mxfp8(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_TRY(check_mx_shape(c));
   if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2 || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (c.F_shared && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
-      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+  if (!all_aligned16({x, router_w, expert_bias, logit_bias, w->w13, w->sf13, w->w2, w->sf2, Ws1, Ws3, Ws2, y,
+                      ws}))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, false, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -1269,7 +1283,7 @@ int moe_mx_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_mx_shape(*cfg));
   if (!W1 || !W3 || !W2 || !w || !w->w2h || !w->sf2h || !w->w13f || !w->sf13f) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w2h) || !aligned16(w->w13f))
+  if (!all_aligned16({W1, W3, W2, w->w2h, w->sf2h, w->w13f, w->sf13f}))
     return MOE_ERR_INVALID_ARG;
   MOE_CUDA(launch_mx_quantize_bwd_weights(*cfg, reinterpret_cast<const __nv_bfloat16*>(W1),
                                           reinterpret_cast<const __nv_bfloat16*>(W3),
@@ -1287,7 +1301,7 @@ size_t moe_mx_train_workspace_bytes(const moe_config* cfg) {
 static bool mx_saved_ok(const moe_config& c, const moe_fwd_saved* sv) {
   return sv && sv->topk_idx && sv->topk_gate && sv->logits && sv->row_id_map && sv->counts && sv->offsets &&
          sv->x_perm && sv->h13 && sv->y_perm && (c.aux_coeff == 0.0f || sv->aux_partials) &&
-         aligned16(sv->x_perm) && aligned16(sv->h13) && aligned16(sv->y_perm);
+         saved_aligned16(sv);
 }
 
 int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
@@ -1300,8 +1314,7 @@ int moe_layer_fwd_mxfp8_train(const moe_config* cfg, const moe_bf16* x, const mo
   if (c.F_shared != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->w2 || !w->sf2 || !y || !ws || !mx_saved_ok(c, saved))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
-      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+  if (!all_aligned16({x, router_w, expert_bias, logit_bias, w->w13, w->sf13, w->w2, w->sf2, y, ws}))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, true, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -1338,7 +1351,9 @@ int moe_layer_bwd_mxfp8(const moe_config* cfg, const moe_bf16* dO, const moe_bf1
   if (!dO || !x || !router_w || !w || !w->w2h || !w->sf2h || !w->w13f || !w->sf13f || !mx_saved_ok(c, saved) ||
       !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dO) || !aligned16(w->w2h) || !aligned16(w->w13f) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({dO, x, router_w, w->w2h, w->sf2h, w->w13f, w->sf13f, dx, dW_router, dW1, dW3, dW2,
+                      aux_loss_out, ws}))
+    return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, true, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return layer_bwd_core(c, dO, x, router_w, nullptr, nullptr, nullptr, saved, dx, dW_router, dW1, dW3, dW2,
@@ -1368,7 +1383,7 @@ int moe_nv_quantize_weights(int E, int K, int N, const moe_bf16* W, uint8_t* wq,
                             void* stream) {
   NvtxRange nvtx("moe_nv_quantize_weights");
   MOE_TRY(check_nv_shape(E, 0, K, N));
-  if (!W || !wq || !sf || !g || !aligned16(W) || !aligned16(wq) || !aligned16(sf)) return MOE_ERR_INVALID_ARG;
+  if (!W || !wq || !sf || !g || !all_aligned16({W, wq, sf, g})) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(W);
   MOE_CUDA(launch_nv_amax(w, static_cast<long long>(K) * N, E, g, s));
@@ -1380,7 +1395,7 @@ int moe_nv_quantize_weights(int E, int K, int N, const moe_bf16* W, uint8_t* wq,
 int moe_nv_quantize(const moe_bf16* x, long long M, int K, uint8_t* q, uint8_t* scales, float* g, void* stream) {
   NvtxRange nvtx("moe_nv_quantize");
   if (!x || !q || !scales || !g || M < 1 || K < kNvBlock || K % kNvBlock != 0) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || (M * K) % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({x, q, scales, g}) || (M * K) % 8 != 0) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   MOE_CUDA(launch_nv_amax(xb, M * K, 1, g, s));
@@ -1419,7 +1434,7 @@ int moe_nv_grouped_gemm(int E, long long R, int K, int N, const moe_bf16* x, con
   NvtxRange nvtx("moe_nv_grouped_gemm");
   MOE_TRY(check_nv_shape(E, R, K, N));
   if (!x || !offsets || !wq || !sf || !g || !y || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(wq) || !aligned16(sf) || !aligned16(y) || !aligned16(ws))
+  if (!all_aligned16({x, offsets, wq, sf, g, y, ws}))
     return MOE_ERR_INVALID_ARG;
   const NvWs L = nv_ws_layout(E, R, K);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -1464,8 +1479,7 @@ int moe_nv_quantize_layer_weights(const moe_config* cfg, const moe_bf16* W1, con
   MOE_TRY(check_nv_layer_shape(c));
   if (!W1 || !W3 || !W2 || !w || !w->w13 || !w->sf13 || !w->g13 || !w->w2 || !w->sf2 || !w->g2)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w13) || !aligned16(w->sf13) ||
-      !aligned16(w->w2) || !aligned16(w->sf2))
+  if (!all_aligned16({W1, W3, W2, w->w13, w->sf13, w->g13, w->w2, w->sf2, w->g2}))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* w1 = reinterpret_cast<const __nv_bfloat16*>(W1);
@@ -1496,8 +1510,8 @@ int moe_layer_fwd_nvfp4(const moe_config* cfg, const moe_bf16* x, const moe_bf16
   MOE_TRY(check_nv_layer_shape(c));
   if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->g13 || !w->w2 || !w->sf2 || !w->g2 || !y || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
-      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+  if (!all_aligned16({x, router_w, expert_bias, logit_bias, w->w13, w->sf13, w->g13, w->w2, w->sf2, w->g2, y,
+                      ws}))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = nv_layer_ws(c);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -1585,8 +1599,7 @@ int moe_nv_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const
   MOE_TRY(check_nv_layer_shape(c));
   if (!W1 || !W3 || !W2 || !w || !w->w2h || !w->sf2h || !w->g2h || !w->w13f || !w->sf13f || !w->g13f)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(w->w2h) || !aligned16(w->sf2h) ||
-      !aligned16(w->w13f) || !aligned16(w->sf13f))
+  if (!all_aligned16({W1, W3, W2, w->w2h, w->sf2h, w->g2h, w->w13f, w->sf13f, w->g13f}))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* w1 = reinterpret_cast<const __nv_bfloat16*>(W1);
@@ -1610,7 +1623,7 @@ size_t moe_nv_train_workspace_bytes(const moe_config* cfg) {
 static bool nv_saved_ok(const moe_config& c, const moe_fwd_saved* sv) {
   return sv && sv->topk_idx && sv->topk_gate && sv->logits && sv->row_id_map && sv->counts && sv->offsets &&
          sv->x_perm && sv->h13 && sv->a && sv->y_perm && (c.aux_coeff == 0.0f || sv->aux_partials) &&
-         aligned16(sv->x_perm) && aligned16(sv->h13) && aligned16(sv->a) && aligned16(sv->y_perm);
+         saved_aligned16(sv);
 }
 
 int moe_layer_fwd_nvfp4_train(const moe_config* cfg, const moe_bf16* x, const moe_bf16* router_w,
@@ -1623,8 +1636,8 @@ int moe_layer_fwd_nvfp4_train(const moe_config* cfg, const moe_bf16* x, const mo
   if (!x || !router_w || !w || !w->w13 || !w->sf13 || !w->g13 || !w->w2 || !w->sf2 || !w->g2 || !y || !ws ||
       !nv_saved_ok(c, saved))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(y) || !aligned16(ws) || !aligned16(w->w13) ||
-      !aligned16(w->sf13) || !aligned16(w->w2) || !aligned16(w->sf2))
+  if (!all_aligned16({x, router_w, expert_bias, logit_bias, w->w13, w->sf13, w->g13, w->w2, w->sf2, w->g2, y,
+                      ws}))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, true, false, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -1693,8 +1706,8 @@ int moe_layer_bwd_nvfp4(const moe_config* cfg, const moe_bf16* dO, const moe_bf1
   if (!dO || !x || !router_w || !w || !w->w2h || !w->sf2h || !w->g2h || !w->w13f || !w->sf13f || !w->g13f ||
       !nv_saved_ok(c, saved) || !dx || !dW_router || !dW1 || !dW3 || !dW2 || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dO) || !aligned16(x) || !aligned16(router_w) || !aligned16(w->w2h) || !aligned16(w->w13f) ||
-      !aligned16(ws))
+  if (!all_aligned16({dO, x, router_w, w->w2h, w->sf2h, w->g2h, w->w13f, w->sf13f, w->g13f, dx, dW_router, dW1,
+                      dW3, dW2, aux_loss_out, ws}))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c, true, false, true);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;

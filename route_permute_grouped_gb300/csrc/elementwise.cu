@@ -606,7 +606,8 @@ extern "C" int moe_write_ceiling(void* buf, size_t bytes, unsigned word, void* s
 
 extern "C" int moe_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream) {
   using namespace moe;
-  if (buf == nullptr || sink == nullptr || (reinterpret_cast<uintptr_t>(buf) & 15) != 0 || (bytes & 15) != 0)
+  if (buf == nullptr || sink == nullptr || (reinterpret_cast<uintptr_t>(buf) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(sink) & 15) != 0 || (bytes & 15) != 0)
     return MOE_ERR_INVALID_ARG;
   if (bytes == 0) return MOE_OK;
   NvtxRange nvtx("moe.read_ceiling");

@@ -3,6 +3,7 @@
 // expert-contiguous rows (dropless; rows of one expert in token order).
 #include <stdio.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "host_util.h"
@@ -395,8 +396,10 @@ extern "C" int moe_permute_noalloc(const moe_config* cfg, const moe_bf16* x, con
   if (v != MOE_OK) return v;
   const moe_config& c = *cfg;
   if (!x || !topk_idx || !x_perm || !row_id_map || !counts || !offsets) return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
-    return MOE_ERR_INVALID_ARG;
+  for (const void* ptr : {static_cast<const void*>(x), static_cast<const void*>(topk_idx),
+                          static_cast<const void*>(x_perm), static_cast<const void*>(row_id_map),
+                          static_cast<const void*>(counts), static_cast<const void*>(offsets)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return MOE_ERR_INVALID_ARG;
   const size_t flags = static_cast<size_t>((c.T + kChunk - 1) / kChunk) * c.E;
   if (flags > kNoAllocMaxFlags) {
     fprintf(stderr,

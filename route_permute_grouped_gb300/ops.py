@@ -18,6 +18,10 @@ from . import build as _build
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
 MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_WORKSPACE_TOO_SMALL = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_DEVICE_INDEX = 6
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "workspace too small",
                 4: "CUDA error", 5: "device: bounded wait ran out", 6: "device: index out of range"}
 SCORE = {"softmax": 0, "sigmoid": 1}

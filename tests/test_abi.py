@@ -169,6 +169,7 @@ def test_read_ceiling_checks_on_the_host(lib):
     assert lib.moe_read_ceiling(some, 1024, null, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_read_ceiling(ctypes.c_void_p(4100), 1024, some, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_read_ceiling(some, 1000, some, null) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_read_ceiling(some, 1024, ctypes.c_void_p(4100), null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_read_ceiling(some, 0, some, null) == ops.MOE_OK
     assert lib.moe_write_ceiling(null, 1024, 0, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_write_ceiling(ctypes.c_void_p(4100), 1024, 0, null) == ops.MOE_ERR_INVALID_ARG
@@ -178,3 +179,87 @@ def test_read_ceiling_checks_on_the_host(lib):
 
 def test_default_build_is_not_the_bounds_check_build(lib):
     assert lib.moe_bounds_checked() == 0
+
+
+def _misaligned_each(call, n_ptrs, structs=()):
+    """Run `call(ptrs, structs)` with every pointer 16-byte aligned, then with
+    one pointer (or one field of one struct) moved by 8 bytes at a time; yield
+    (what was moved, status)."""
+    good, bad = 4096, 4096 + 8
+    ptrs = [ctypes.c_void_p(good) for _ in range(n_ptrs)]
+    mk = [lambda S=S: S(*([good] * len(S._fields_))) for S in structs]
+    yield "none", call(ptrs, [m() for m in mk])
+    for i in range(n_ptrs):
+        p = list(ptrs)
+        p[i] = ctypes.c_void_p(bad)
+        yield f"pointer {i}", call(p, [m() for m in mk])
+    for j, S in enumerate(structs):
+        for name, _ in S._fields_:
+            st = [m() for m in mk]
+            setattr(st[j], name, bad)
+            yield f"{S.__name__}.{name}", call(ptrs, st)
+
+
+def test_every_device_pointer_is_checked_for_alignment(lib):
+    """The header's convention (every device pointer 16-byte aligned; the
+    kernels reach them with 16-byte vector accesses and TMA copies) is checked
+    on each pointer an entry point takes, saved-tensor and weight-struct
+    fields included, before anything is enqueued. The workspace size given is
+    too small, so a pointer the check missed would show as
+    MOE_ERR_WORKSPACE_TOO_SMALL, never as a launch."""
+    small = 16
+    shared = ops.make_config(256, 256, 8, 2, 256, F_shared=64, aux_coeff=0.01)
+    plain = ops.make_config(256, 256, 8, 2, 256, aux_coeff=0.01)
+    B = ctypes.byref
+    cases = {
+        "moe_router_topk": (9, (), lambda p, s: lib.moe_router_topk(B(plain), *p, small, None)),
+        "moe_permute": (7, (), lambda p, s: lib.moe_permute(B(plain), *p, small, None)),
+        "moe_grouped_swiglu_ffn": (9, (), lambda p, s: lib.moe_grouped_swiglu_ffn(B(plain), *p, small, None)),
+        "moe_layer_fwd": (12, (ops.MoeFwdSaved,), lambda p, s: lib.moe_layer_fwd(
+            B(shared), *p[:11], B(s[0]), p[11], small, None)),
+        "moe_layer_bwd": (19, (ops.MoeFwdSaved,), lambda p, s: lib.moe_layer_bwd(
+            B(shared), *p[:9], B(s[0]), *p[9:19], small, None)),
+        "moe_layer_fwd_mxfp8": (9, (ops.MoeMxWeights,), lambda p, s: lib.moe_layer_fwd_mxfp8(
+            B(shared), *p[:4], B(s[0]), *p[4:9], small, None)),
+        "moe_layer_fwd_mxfp8_train": (6, (ops.MoeMxWeights, ops.MoeFwdSaved), lambda p, s: (
+            lib.moe_layer_fwd_mxfp8_train(B(plain), *p[:4], B(s[0]), p[4], B(s[1]), p[5], small, None))),
+        "moe_layer_bwd_mxfp8": (10, (ops.MoeMxBwdWeights, ops.MoeFwdSaved), lambda p, s: lib.moe_layer_bwd_mxfp8(
+            B(plain), *p[:3], B(s[0]), B(s[1]), *p[3:9], 0, p[9], small, None)),
+        "moe_layer_fwd_nvfp4": (6, (ops.MoeNvWeights,), lambda p, s: lib.moe_layer_fwd_nvfp4(
+            B(plain), *p[:4], B(s[0]), p[4], p[5], small, None)),
+        "moe_layer_fwd_nvfp4_train": (6, (ops.MoeNvWeights, ops.MoeFwdSaved), lambda p, s: (
+            lib.moe_layer_fwd_nvfp4_train(B(plain), *p[:4], B(s[0]), p[4], B(s[1]), p[5], small, None))),
+        "moe_layer_bwd_nvfp4": (10, (ops.MoeNvBwdWeights, ops.MoeFwdSaved), lambda p, s: lib.moe_layer_bwd_nvfp4(
+            B(plain), *p[:3], B(s[0]), B(s[1]), *p[3:10], small, None)),
+        "moe_nv_grouped_gemm": (7, (), lambda p, s: lib.moe_nv_grouped_gemm(4, 100, 256, 64, *p, small, None)),
+    }
+    for fn, (n, structs, call) in cases.items():
+        for what, st in _misaligned_each(call, n, structs):
+            want = ops.MOE_ERR_WORKSPACE_TOO_SMALL if what == "none" else ops.MOE_ERR_INVALID_ARG
+            assert st == want, f"{fn}: {what} misaligned -> {st}"
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="entry points without a workspace would launch if a check were missing")
+def test_alignment_of_entry_points_without_a_workspace(lib):
+    plain = ops.make_config(256, 256, 8, 2, 256)
+    B = ctypes.byref
+    cases = {
+        "moe_unpermute_combine": (5, (), lambda p, s: lib.moe_unpermute_combine(B(plain), *p, None)),
+        "moe_permute_noalloc": (6, (), lambda p, s: lib.moe_permute_noalloc(B(plain), *p, None)),
+        "moe_mx_quantize": (3, (), lambda p, s: lib.moe_mx_quantize(p[0], 64, 256, p[1], p[2], None)),
+        "moe_nv_quantize": (4, (), lambda p, s: lib.moe_nv_quantize(p[0], 64, 256, *p[1:4], None)),
+        "moe_nv_quantize_weights": (4, (), lambda p, s: lib.moe_nv_quantize_weights(4, 256, 64, *p, None)),
+        "moe_mx_quantize_weights": (3, (ops.MoeMxWeights,), lambda p, s: lib.moe_mx_quantize_weights(
+            B(plain), *p, B(s[0]), None)),
+        "moe_mx_quantize_bwd_weights": (3, (ops.MoeMxBwdWeights,), lambda p, s: lib.moe_mx_quantize_bwd_weights(
+            B(plain), *p, B(s[0]), None)),
+        "moe_nv_quantize_layer_weights": (3, (ops.MoeNvWeights,), lambda p, s: lib.moe_nv_quantize_layer_weights(
+            B(plain), *p, B(s[0]), None)),
+        "moe_nv_quantize_bwd_weights": (3, (ops.MoeNvBwdWeights,), lambda p, s: lib.moe_nv_quantize_bwd_weights(
+            B(plain), *p, B(s[0]), None)),
+    }
+    for fn, (n, structs, call) in cases.items():
+        for what, st in _misaligned_each(call, n, structs):
+            if what != "none":
+                assert st == ops.MOE_ERR_INVALID_ARG, f"{fn}: {what} misaligned -> {st}"
