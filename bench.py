@@ -146,6 +146,22 @@ def kernel_table(stages, model, peaks):
 _READ_CEILING = {}
 
 
+def device_ms(fn, reps=3):
+    """Average device time of `fn()` over `reps` calls: CUDA events on the
+    current stream, after one untimed call."""
+    import torch
+
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def read_ceiling_gbs(nbytes, dev, reps=7):
     """Median rate of one moe_read_ceiling launch over `nbytes` (cold L2: a
     buffer larger than L2 is written before each launch): the rate at which a
@@ -601,6 +617,37 @@ def run_ours(args, ls, rank, world, local_rank):
         e2e = {"value": round(job_throughput(flops_step, ms_e2e, world), 3), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)}
 
+        # the host link alone, after the end-to-end run: one step's input
+        # copies, its output copies, and both at once (an end-to-end step is no
+        # shorter than the last, whatever the overlap)
+        def link_ms(inputs, outputs, reps=3):
+            torch.cuda.synchronize()
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(comp)
+            s_in.wait_stream(comp)
+            s_out.wait_stream(comp)
+            for _ in range(reps):
+                if inputs:
+                    with torch.cuda.stream(s_in):
+                        xd[0].copy_(hx, non_blocking=True)
+                        if training:
+                            dOd[0].copy_(hdO, non_blocking=True)
+                if outputs:
+                    with torch.cuda.stream(s_out):
+                        hy.copy_(ys[0], non_blocking=True)
+                        if training:
+                            hdx.copy_(gbuf[0]["dx"], non_blocking=True)
+            comp.wait_stream(s_in)
+            comp.wait_stream(s_out)
+            c1.record(comp)
+            torch.cuda.synchronize()
+            return c0.elapsed_time(c1) / reps
+
+        ms_in, ms_out, ms_both = link_ms(True, False), link_ms(False, True), link_ms(True, True)
+        e2e["host_link"] = {"h2d_gbs": round(h2d / (ms_in * 1e-3) / 1e9, 1),
+                            "d2h_gbs": round(d2h / (ms_out * 1e-3) / 1e9, 1),
+                            "copies_alone_ms": round(ms_both, 4)}
+
     # ---------------- the same step captured once as a CUDA graph and replayed
     # (device-side offsets: no host synchronisation inside a step)
     graph = None
@@ -765,8 +812,14 @@ def run_ours(args, ls, rank, world, local_rank):
                                         "frac": round(gbs / peaks["hbm_gbs"], 4)}
         mxt_w = {"value": round(job_throughput(layer_flops(ls, True), ms_mxw, world), 2), "unit": "TFLOPS",
                  "ms_per_step": round(ms_mxw, 4), "vs_bf16_step": round(ms / ms_mxw, 3), "kernels": wk}
+        # the weight copies (forward and data-gradient operands) that a
+        # training loop refreshes once per optimizer step: not in ms_per_step
+        wq_mx = max_over_ranks(device_ms(lambda: (ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"]),
+                                                  ops.mx_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"]))),
+                               world, dev)
         mxt = {"value": round(job_throughput(layer_flops(ls, True), ms_mxt, world), 2), "unit": "TFLOPS",
-               "ms_per_step": round(ms_mxt, 4),
+               "ms_per_step": round(ms_mxt, 4), "weight_quant_ms": round(wq_mx, 4),
+               "ms_per_step_with_weight_quant": round(ms_mxt + wq_mx, 4),
                "dtype": "mxfp8 forward and data-gradient GEMMs, bf16 weight gradients (fp32 out)",
                "vs_bf16_step": round(ms / ms_mxt, 3), "kernels": tk, "peak_fp8_tflops": round(peak8, 1),
                "mxfp8_weight_gradients": mxt_w}
@@ -886,8 +939,15 @@ def run_ours(args, ls, rank, world, local_rank):
                          "permute_bwd"):
                 if name in st_nt:
                     nk[name] = {"ms": round(sum(st_nt[name]) / args.steps, 4)}
+            # the weight copies a training loop refreshes once per optimizer
+            # step (maxima, then codes): not in ms_per_step
+            wq_nv = max_over_ranks(device_ms(lambda: (ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"]),
+                                                      ops.nv_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"]))),
+                                   world, dev)
             nv["train_step"] = {"value": round(job_throughput(layer_flops(ls, True), ms_nt, world), 2),
                                 "unit": "TFLOPS", "ms_per_step": round(ms_nt, 4), "vs_bf16_step": round(ms / ms_nt, 3),
+                                "weight_quant_ms": round(wq_nv, 4),
+                                "ms_per_step_with_weight_quant": round(ms_nt + wq_nv, 4),
                                 "dtype": "nvfp4 forward and data-gradient GEMMs, bf16 weight gradients (fp32 out)",
                                 "kernels": nk}
             del nlw, nbw, wsn, svn, yl

@@ -255,19 +255,20 @@ cudaError_t launch_nv_amax(const __nv_bfloat16* x, long long n_per, int groups, 
                            const __nv_bfloat16* x2) {
   cudaError_t e = cudaMemsetAsync(out_bits, 0, sizeof(float) * groups, st);
   if (e != cudaSuccess) return e;
+  // about eight 256-thread blocks per SM over all groups together (one wave;
+  // each thread keeps four 16-byte loads in flight), at most one 16-byte load
+  // per thread of a group
+  long long blocks = (n_per / 8 + 255) / 256;
+  const long long cap = (8ll * num_sms() + groups - 1) / groups;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
   if (x2 != nullptr) {
     // the maxima cover a second tensor of the same shape too
-    long long b2 = (n_per / 8 + 255) / 256;
-    if (b2 > 8 * num_sms()) b2 = 8 * num_sms();
-    if (b2 < 1) b2 = 1;
-    nv_amax_kernel<<<dim3(static_cast<unsigned>(b2), groups), 256, 0, st>>>(x2, n_per,
-                                                                            reinterpret_cast<unsigned*>(out_bits));
+    nv_amax_kernel<<<dim3(static_cast<unsigned>(blocks), groups), 256, 0, st>>>(x2, n_per,
+                                                                                reinterpret_cast<unsigned*>(out_bits));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  long long blocks = (n_per / 8 + 255) / 256;
-  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
-  if (blocks < 1) blocks = 1;
   nv_amax_kernel<<<dim3(static_cast<unsigned>(blocks), groups), 256, 0, st>>>(x, n_per,
                                                                               reinterpret_cast<unsigned*>(out_bits));
   e = cudaGetLastError();
