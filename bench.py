@@ -940,9 +940,9 @@ def run_ours(args, ls, rank, world, local_rank):
                 if name in st_nt:
                     nk[name] = {"ms": round(sum(st_nt[name]) / args.steps, 4)}
             # the weight copies a training loop refreshes once per optimizer
-            # step (maxima, then codes): not in ms_per_step
-            wq_nv = max_over_ranks(device_ms(lambda: (ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"]),
-                                                      ops.nv_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"]))),
+            # step (one call: the per-expert maxima once, then both copies'
+            # codes): not in ms_per_step
+            wq_nv = max_over_ranks(device_ms(lambda: ops.nv_quantize_train_weights(cfg, d["W1"], d["W3"], d["W2"])),
                                    world, dev)
             nv["train_step"] = {"value": round(job_throughput(layer_flops(ls, True), ms_nt, world), 2),
                                 "unit": "TFLOPS", "ms_per_step": round(ms_nt, 4), "vs_bf16_step": round(ms / ms_nt, 3),

@@ -481,6 +481,18 @@ size_t moe_nv_bwd_weight_bytes(const moe_config* cfg, int which);
 int moe_nv_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
                                 const moe_nv_bwd_weights* w, void* stream);
 
+/* Both weight copies of the NVFP4 training step in one call, as a training
+ * loop refreshes them once per optimizer step: the same codes, scales and
+ * tensor scales as moe_nv_quantize_layer_weights into *fw and
+ * moe_nv_quantize_bwd_weights into *bw, with each per-expert maximum taken once
+ * (the two copies quantise the same per-expert tensors, so g13f = g13 and
+ * g2h = g2). Buffers as those two calls take them. Returns MOE_ERR_INVALID_ARG
+ * for a null or misaligned pointer, MOE_ERR_UNSUPPORTED_SHAPE where the NVFP4
+ * layer does not apply. */
+int moe_nv_quantize_train_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3,
+                                  const moe_bf16* W2, const moe_nv_weights* fw, const moe_nv_bwd_weights* bw,
+                                  void* stream);
+
 /* Workspace bytes of moe_layer_fwd_nvfp4_train / moe_layer_bwd_nvfp4 (one
  * workspace serves both). 0 for an unsupported shape. */
 size_t moe_nv_train_workspace_bytes(const moe_config* cfg);

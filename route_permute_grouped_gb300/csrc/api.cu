@@ -1615,6 +1615,39 @@ int moe_nv_quantize_bwd_weights(const moe_config* cfg, const moe_bf16* W1, const
   return MOE_OK;
 }
 
+int moe_nv_quantize_train_weights(const moe_config* cfg, const moe_bf16* W1, const moe_bf16* W3,
+                                  const moe_bf16* W2, const moe_nv_weights* fw, const moe_nv_bwd_weights* bw,
+                                  void* stream) {
+  NvtxRange nvtx("moe_nv_quantize_train_weights");
+  MOE_TRY(check_cfg(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(check_nv_layer_shape(c));
+  if (!W1 || !W3 || !W2 || !fw || !fw->w13 || !fw->sf13 || !fw->g13 || !fw->w2 || !fw->sf2 || !fw->g2 || !bw ||
+      !bw->w2h || !bw->sf2h || !bw->g2h || !bw->w13f || !bw->sf13f || !bw->g13f)
+    return MOE_ERR_INVALID_ARG;
+  if (!all_aligned16({W1, W3, W2, fw->w13, fw->sf13, fw->g13, fw->w2, fw->sf2, fw->g2, bw->w2h, bw->sf2h, bw->g2h,
+                      bw->w13f, bw->sf13f, bw->g13f}))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* w1 = reinterpret_cast<const __nv_bfloat16*>(W1);
+  const __nv_bfloat16* w3 = reinterpret_cast<const __nv_bfloat16*>(W3);
+  const __nv_bfloat16* w2 = reinterpret_cast<const __nv_bfloat16*>(W2);
+  // both copies quantise the same per-expert tensors ([W1_e | W3_e] and
+  // W2_e), so they share one tensor scale each: the maxima are taken once
+  MOE_CUDA(launch_nv_amax(w1, static_cast<long long>(c.H) * c.F, c.E, fw->g13, s, w3));
+  MOE_CUDA(launch_nv_amax(w2, static_cast<long long>(c.F) * c.H, c.E, fw->g2, s));
+  MOE_CUDA(cudaMemcpyAsync(bw->g13f, fw->g13, sizeof(float) * c.E, cudaMemcpyDeviceToDevice, s));
+  MOE_CUDA(cudaMemcpyAsync(bw->g2h, fw->g2, sizeof(float) * c.E, cudaMemcpyDeviceToDevice, s));
+  // forward operands: codes along H (gate/up) and F (down)
+  MOE_CUDA(launch_nv_quantize_weights(w1, c.E, c.H, 2 * c.F, fw->g13, fw->w13, fw->sf13, s, w3, c.F));
+  MOE_CUDA(launch_nv_quantize_weights(w2, c.E, c.F, c.H, fw->g2, fw->w2, fw->sf2, s));
+  // data-gradient operands: W2_e row-wise along H, [W1_e | W3_e] row-wise along 2F
+  MOE_CUDA(launch_nv_quantize_weight_rows(w2, c.E, c.H, c.F, bw->g2h, bw->w2h, bw->sf2h, s));
+  MOE_CUDA(launch_nv_quantize_weight_rows(w1, c.E, 2 * c.F, c.H, bw->g13f, bw->w13f, bw->sf13f, s, w3, c.F));
+  count_launches(9);
+  return MOE_OK;
+}
+
 size_t moe_nv_train_workspace_bytes(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK || check_nv_layer_shape(*cfg) != MOE_OK) return 0;
   return ws_layout(*cfg, true, false, true).total;

@@ -148,11 +148,14 @@ def lib():
         L.moe_nv_train_workspace_bytes.restype = c_size_t
         L.moe_nv_train_workspace_bytes.argtypes = [POINTER(MoeConfig)]
         L.moe_nv_quantize_bwd_weights.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeNvBwdWeights), vp]
+        L.moe_nv_quantize_train_weights.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeNvWeights),
+                                                    POINTER(MoeNvBwdWeights), vp]
         L.moe_layer_fwd_nvfp4_train.argtypes = [POINTER(MoeConfig), vp, vp, vp, vp, POINTER(MoeNvWeights), vp,
                                                 POINTER(MoeFwdSaved), vp, c_size_t, vp]
         L.moe_layer_bwd_nvfp4.argtypes = [POINTER(MoeConfig), vp, vp, vp, POINTER(MoeNvBwdWeights),
                                           POINTER(MoeFwdSaved), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
-        for n in ("moe_nv_quantize_bwd_weights", "moe_layer_fwd_nvfp4_train", "moe_layer_bwd_nvfp4"):
+        for n in ("moe_nv_quantize_bwd_weights", "moe_nv_quantize_train_weights", "moe_layer_fwd_nvfp4_train",
+                  "moe_layer_bwd_nvfp4"):
             getattr(L, n).restype = c_int
         _lib = L
     return _lib
@@ -674,6 +677,32 @@ def nv_quantize_bwd_weights(cfg, W1, W3, W2):
     _check(lib().moe_nv_quantize_bwd_weights(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2), ctypes.byref(w), _stream()),
            "moe_nv_quantize_bwd_weights")
     return out
+
+
+def _nv_alloc(cfg, size_fn, fields, device):
+    out = {}
+    for i, (n, _) in enumerate(fields):
+        nb = int(size_fn(ctypes.byref(cfg), i))
+        if nb == 0:
+            raise MoeError(2, size_fn.__name__)
+        dt = torch.float32 if n.startswith("g") else torch.uint8
+        out[n] = torch.empty(nb // (4 if dt == torch.float32 else 1), dtype=dt, device=device)
+    return out
+
+
+def nv_quantize_train_weights(cfg, W1, W3, W2):
+    """Both weight copies of the NVFP4 training step in one call (the maxima
+    taken once): the dicts nv_quantize_layer_weights and
+    nv_quantize_bwd_weights return."""
+    fw = _nv_alloc(cfg, lib().moe_nv_layer_weight_bytes, MoeNvWeights._fields_, W1.device)
+    bw = _nv_alloc(cfg, lib().moe_nv_bwd_weight_bytes, MoeNvBwdWeights._fields_, W1.device)
+    bw["w2h"] = bw["w2h"].view(cfg.E, cfg.F, cfg.H // 2)
+    bw["w13f"] = bw["w13f"].view(cfg.E, cfg.H, cfg.F)
+    b = MoeNvBwdWeights(*[bw[n].data_ptr() for n, _ in MoeNvBwdWeights._fields_])
+    _check(lib().moe_nv_quantize_train_weights(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2),
+                                               ctypes.byref(_nv_struct(fw)), ctypes.byref(b), _stream()),
+           "moe_nv_quantize_train_weights")
+    return fw, bw
 
 
 def nv_train_workspace(cfg, device="cuda"):

@@ -158,6 +158,10 @@ def test_low_precision_entry_points_check_on_the_host(lib):
                                    null, null, 0, null) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_nv_quantize_bwd_weights(ctypes.byref(bad_h), null, null, null, None,
                                            null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_nv_quantize_train_weights(ctypes.byref(bad_h), null, null, null, None, None,
+                                             null) == ops.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_nv_quantize_train_weights(ctypes.byref(ok), null, null, null, None, None,
+                                             null) == ops.MOE_ERR_INVALID_ARG
 
 
 def test_read_ceiling_checks_on_the_host(lib):
@@ -258,6 +262,9 @@ def test_alignment_of_entry_points_without_a_workspace(lib):
             B(plain), *p, B(s[0]), None)),
         "moe_nv_quantize_bwd_weights": (3, (ops.MoeNvBwdWeights,), lambda p, s: lib.moe_nv_quantize_bwd_weights(
             B(plain), *p, B(s[0]), None)),
+        "moe_nv_quantize_train_weights": (3, (ops.MoeNvWeights, ops.MoeNvBwdWeights),
+                                          lambda p, s: lib.moe_nv_quantize_train_weights(B(plain), *p, B(s[0]),
+                                                                                         B(s[1]), None)),
     }
     for fn, (n, structs, call) in cases.items():
         for what, st in _misaligned_each(call, n, structs):

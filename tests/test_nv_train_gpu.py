@@ -62,6 +62,25 @@ def test_nv_bwd_weight_quantization_bit_exact(E, H, F):
         assert np.array_equal(w13f[e], q) and np.array_equal(s13[e], s) and w["g13f"][e].item() == float(g), e
 
 
+@pytest.mark.parametrize("E,H,F", [(3, 256, 512), (130, 256, 256)])
+def test_nv_train_weights_in_one_call_are_the_two_copies(E, H, F):
+    """The combined refresh takes each per-expert maximum once; its codes,
+    scales and tensor scales are those of the two separate calls, byte for
+    byte (the separate calls being pinned to the oracle above and by the
+    forward's weight test)."""
+    ls = synth.shape("tiny", T=64, H=H, E=E, k=2, F=F)
+    d = synth.make_layer(ls, seed=8, device="cuda", training=False)
+    cfg = ops.config_from_shape(ls)
+    fw_ref = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
+    bw_ref = ops.nv_quantize_bwd_weights(cfg, d["W1"], d["W3"], d["W2"])
+    fw, bw = ops.nv_quantize_train_weights(cfg, d["W1"], d["W3"], d["W2"])
+    torch.cuda.synchronize()
+    for got, ref in ((fw, fw_ref), (bw, bw_ref)):
+        assert set(got) == set(ref)
+        for n in ref:
+            assert torch.equal(got[n].view(torch.uint8).reshape(-1), ref[n].view(torch.uint8).reshape(-1)), n
+
+
 TRAIN_SHAPES = {
     "tiny": synth.shape("tiny", T=300, H=256, E=8, k=2, F=256),
     # ragged N tiles in both data-gradient GEMMs (F = 512 = 2 x 192 + 128,
