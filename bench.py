@@ -162,6 +162,72 @@ def device_ms(fn, reps=3):
     return e0.elapsed_time(e1) / reps
 
 
+def library_gemm_rate(mm, n, reps_seconds, what):
+    """Best of 10 launches (burst) and back to back for `reps_seconds`
+    (sustained) of the library GEMM `mm()` of size n^3, as TFLOP/s; None where
+    the call is unavailable."""
+    import torch
+
+    try:
+        mm()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(10):
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        reps = max(10, int(reps_seconds * 1e3 / best))
+        e0.record()
+        for _ in range(reps):
+            mm()
+        e1.record()
+        torch.cuda.synchronize()
+        sus = e0.elapsed_time(e1) / reps
+        fl = 2.0 * n ** 3
+        return {"burst_tflops": round(fl / (best * 1e-3) / 1e12, 1),
+                "sustained_tflops": round(fl / (sus * 1e-3) / 1e12, 1),
+                "how": f"{what} {n}^3, best of 10 and {reps} back to back"}
+    except Exception as ex:  # the library GEMM is missing on this build
+        print(f"{what}: not measured: {ex}", file=sys.stderr)
+        return None
+
+
+def measured_fp8_peak(dev, seconds=2.0):
+    """Rate of a dense FP8 GEMM from the vendor library (torch._scaled_mm:
+    e4m3 x e4m3, per-tensor scales, bf16 out), measured the way the bf16 peaks
+    beside it were."""
+    import torch
+
+    n = 8192
+    g = torch.Generator(device=dev).manual_seed(11)
+    a = (0.5 * torch.randn((n, n), generator=g, device=dev)).to(torch.float8_e4m3fn)
+    b = (0.5 * torch.randn((n, n), generator=g, device=dev)).to(torch.float8_e4m3fn)
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    return library_gemm_rate(lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16),
+                             n, seconds, "torch._scaled_mm e4m3")
+
+
+def measured_fp4_peak(dev, seconds=2.0):
+    """Rate of a dense NVFP4 GEMM from the vendor library (torch._scaled_mm:
+    e2m1 x e2m1 with an e4m3 scale per 16 elements, bf16 out); None where the
+    library or this torch build does not offer it."""
+    import torch
+
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        return None
+    n = 8192
+    g = torch.Generator(device=dev).manual_seed(12)
+    a = torch.randint(0, 256, (n, n // 2), generator=g, dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+    b = torch.randint(0, 256, (n, n // 2), generator=g, dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+    sa = torch.ones(n * (n // 16), device=dev).to(torch.float8_e4m3fn)
+    sb = torch.ones(n * (n // 16), device=dev).to(torch.float8_e4m3fn)
+    return library_gemm_rate(lambda: torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16),
+                             n, seconds, "torch._scaled_mm nvfp4")
+
+
 def read_ceiling_gbs(nbytes, dev, reps=7):
     """Median rate of one moe_read_ceiling launch over `nbytes` (cold L2: a
     buffer larger than L2 is written before each launch): the rate at which a
@@ -677,6 +743,16 @@ def run_ours(args, ls, rank, world, local_rank):
     # would be)
     peaks = load_peaks()
     mx = None
+    # FP8 dense peak: the vendor FP8 GEMM's sustained rate measured in this
+    # run, else the measured sustained bf16 peak times the nominal fp8 : bf16
+    # ratio of the tensor cores (2)
+    fp8_meas = measured_fp8_peak(dev) if not args.no_mxfp8 and ls.H % 128 == 0 and ls.F % 128 == 0 else None
+    if fp8_meas is not None:
+        peak8 = fp8_meas["sustained_tflops"]
+        peak8_src = "measured in this run: " + fp8_meas["how"] + " (sustained)"
+    else:
+        peak8 = 2 * peaks["bf16_tflops_sustained"]
+        peak8_src = f"{peaks['source']} bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"
     if not args.no_mxfp8 and ls.H % 128 == 0 and ls.F % 128 == 0:
         mxw = ops.mx_quantize_weights(cfg, d["W1"], d["W3"], d["W2"])
         wsm = ops.mx_workspace(cfg, dev)
@@ -702,9 +778,6 @@ def run_ours(args, ls, rank, world, local_rank):
         mx_stages = {}
         for name, t in ops.profile_read(args.steps * 8 + 8):
             mx_stages.setdefault(name, []).append(t)
-        # FP8 dense peak: the measured sustained bf16 peak times the nominal
-        # fp8 : bf16 ratio of the tensor cores (2)
-        peak8 = 2 * peaks["bf16_tflops_sustained"]
         R = ls.T * ls.k
         mk = {}
         for name, fl in (("ffn1_gate_up", 2 * R * ls.H * 2 * ls.F), ("ffn2_down", 2 * R * ls.F * ls.H)):
@@ -719,7 +792,8 @@ def run_ours(args, ls, rank, world, local_rank):
         mx = {"value": round(job_throughput(layer_flops(ls, False), ms_mx, world), 2), "unit": "TFLOPS",
               "ms_per_step": round(ms_mx, 4), "dtype": "mxfp8 (e4m3, e8m0 scale per 32 along K)",
               "vs_bf16_fwd": round(ms_fwd / ms_mx, 3), "kernels": mk, "peak_fp8_tflops": round(peak8, 1),
-              "peak_source": f"{peaks['source']} bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"}
+              "peak_source": peak8_src, "fp8_gemm_measured": fp8_meas,
+              "peak_fp8_nominal_ratio_tflops": round(2 * peaks["bf16_tflops_sustained"], 1)}
         del mxw, wsm, ym
 
     # ---------------- the MXFP8 training step: forward saving for the
@@ -756,7 +830,6 @@ def run_ours(args, ls, rank, world, local_rank):
         st_mx = {}
         for name, t in ops.profile_read(cap_t):
             st_mx.setdefault(name, []).append(t)
-        peak8 = 2 * peaks["bf16_tflops_sustained"]
         R = ls.T * ls.k
         tk = {}
         for name, fl, pk in (("ffn1_gate_up", 2 * R * ls.H * 2 * ls.F, peak8), ("ffn2_down", 2 * R * ls.F * ls.H, peak8),
@@ -822,7 +895,7 @@ def run_ours(args, ls, rank, world, local_rank):
                "ms_per_step_with_weight_quant": round(ms_mxt + wq_mx, 4),
                "dtype": "mxfp8 forward and data-gradient GEMMs, bf16 weight gradients (fp32 out)",
                "vs_bf16_step": round(ms / ms_mxt, 3), "kernels": tk, "peak_fp8_tflops": round(peak8, 1),
-               "mxfp8_weight_gradients": mxt_w}
+               "peak_source": peak8_src, "mxfp8_weight_gradients": mxt_w}
         del mxw, mxbw, wst, svm, ym
 
     # ---------------- the NVFP4 grouped expert GEMM on the down projection's
@@ -858,7 +931,16 @@ def run_ours(args, ls, rank, world, local_rank):
         for name, t in ops.profile_read(args.steps * 4 + 4):
             st_nv.setdefault(name, []).append(t)
         fl = 2 * R * ls.F * ls.H
-        peak4 = 6 * peaks["bf16_tflops_sustained"]
+        # FP4 dense peak: the vendor NVFP4 GEMM's sustained rate measured in
+        # this run, else the measured sustained bf16 peak times the nominal
+        # fp4 : bf16 ratio (13.5 / 2.25)
+        fp4_meas = measured_fp4_peak(dev)
+        if fp4_meas is not None:
+            peak4 = fp4_meas["sustained_tflops"]
+            peak4_src = "measured in this run: " + fp4_meas["how"] + " (sustained)"
+        else:
+            peak4 = 6 * peaks["bf16_tflops_sustained"]
+            peak4_src = f"{peaks['source']} bf16_tflops_sustained x 6 (nominal fp4:bf16 ratio 13.5/2.25)"
         g_ms = sum(st_nv.get("nv_gemm", [0])) / max(1, len(st_nv.get("nv_gemm", [0])))
         q_ms = sum(st_nv.get("nv_quantize", [0])) / max(1, len(st_nv.get("nv_quantize", [0])))
         nv = {"shape": f"grouped {R} x {ls.F} x {ls.H} (down projection, {ls.E} experts)",
@@ -867,7 +949,8 @@ def run_ours(args, ls, rank, world, local_rank):
               "gemm": {"bound": "tensor", "achieved_tflops": round(fl / (g_ms * 1e-3) / 1e12, 1) if g_ms else None,
                        "frac": round(fl / (g_ms * 1e-3) / 1e12 / peak4, 4) if g_ms else None},
               "dtype": "nvfp4 (e2m1, e4m3 scale per 16 along K, fp32 tensor scale)", "peak_fp4_tflops": round(peak4, 1),
-              "peak_source": f"{peaks['source']} bf16_tflops_sustained x 6 (nominal fp4:bf16 ratio 13.5/2.25)"}
+              "peak_source": peak4_src, "fp4_gemm_measured": fp4_meas,
+              "peak_fp4_nominal_ratio_tflops": round(6 * peaks["bf16_tflops_sustained"], 1)}
         del nvw, a_in, wsn, yn
         # the layer forward with NVFP4 expert GEMMs (same inputs)
         nlw = ops.nv_quantize_layer_weights(cfg, d["W1"], d["W3"], d["W2"])
