@@ -41,35 +41,76 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const __nv_bfloat
 // (sf + e * sf_estride): tile n / tile_n, k block kb32 / 4, B row of the tile
 // b = n % tile_n + row_off (row_off: 0 for W1 and W2, tile_n for W3, whose
 // rows follow W1's in a gate/up tile); every (tile, k block) owns two 512-byte
-// blocks (B rows 0..127, 128..255). Thread = one (e, n, kb32): 32 strided
-// loads (coalesced over n across the warp), one 32-byte store.
+// blocks (B rows 0..127, 128..255). Block = one (e, 128-element k block, 64
+// columns): the 128 x 64 bf16 tile is staged in shared memory with 16-byte
+// loads (whole 128-byte rows), thread = one (column, 32-element block) (a warp:
+// 32 consecutive columns of one block) quantises from shared memory into a
+// staged 64 x 128-byte code tile, which leaves in whole 128-byte lines. N is a
+// multiple of 8, K of 128.
+constexpr int kMxWqCols = 64;
 __global__ void __launch_bounds__(256) mx_quantize_weight_kernel(const __nv_bfloat16* __restrict__ w, int E, int K,
                                                                  int N, uint8_t* __restrict__ wq, size_t wq_estride,
                                                                  uint8_t* __restrict__ sf, size_t sf_estride,
                                                                  int tile_n, int row_off) {
-  const int nkb32 = K / kMxBlock;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(E) * nkb32 * N;
-  if (i >= total) return;
-  const int n = static_cast<int>(i % N);
-  const long long r = i / N;
-  const int kb32 = static_cast<int>(r % nkb32);
-  const int e = static_cast<int>(r / nkb32);
-  const __nv_bfloat16* src = w + (static_cast<size_t>(e) * K + static_cast<size_t>(kb32) * kMxBlock) * N + n;
-  float v[32];
+  __shared__ __align__(16) __nv_bfloat16 tile[kMxKB][kMxWqCols + 8];  // 144-byte rows
+  __shared__ __align__(16) uint8_t codes[kMxWqCols][kMxKB + 16];      // 144-byte rows
+  const int nkb = K / kMxKB;
+  const int nnb = (N + kMxWqCols - 1) / kMxWqCols;
+  long long bid = blockIdx.x;
+  const int kb = static_cast<int>(bid % nkb);
+  bid /= nkb;
+  const int nb = static_cast<int>(bid % nnb);
+  const int e = static_cast<int>(bid / nnb);
+  if (e >= E) return;
+  const int n0 = nb * kMxWqCols;
+  const int ncols = min(kMxWqCols, N - n0);
+  const __nv_bfloat16* src = w + (static_cast<size_t>(e) * K + static_cast<size_t>(kb) * kMxKB) * N + n0;
+  const int t = threadIdx.x;
+  {
+    // 128 rows x 8 chunks of 16 bytes: thread t takes chunk t % 8 of rows t / 8 + 32 i
+    const int c = t & 7;
+    if (8 * c < ncols) {
+      uint4 v[4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(src[static_cast<size_t>(j) * N]);
-  uint32_t c[8];
-  const uint32_t sb = mx_quant32(v, c);
-  uint4* dst = reinterpret_cast<uint4*>(wq + e * wq_estride + static_cast<size_t>(n) * K +
-                                        static_cast<size_t>(kb32) * kMxBlock);
-  dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-  dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-  const int tile = n / tile_n;
-  const int b = n % tile_n + row_off;  // B row of the tile
-  const size_t blk = static_cast<size_t>(tile) * (K / kMxKB) + kb32 / 4;
-  sf[e * sf_estride + blk * 2 * kMxSfBytes + (b >> 7) * kMxSfBytes + mx_sf_pos(b & 127, kb32 & 3)] =
-      static_cast<uint8_t>(sb);
+      for (int i = 0; i < 4; ++i)
+        v[i] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>((t >> 3) + 32 * i) * N) + c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(&tile[(t >> 3) + 32 * i][8 * c]) = v[i];
+    }
+  }
+  __syncthreads();
+  const int col = t & 63, blk = t >> 6;  // column of the tile, 32-element block of the k block
+  if (col < ncols) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(tile[32 * blk + j][col]);
+    uint32_t c[8];
+    const uint32_t sb = mx_quant32(v, c);
+    uint4* d = reinterpret_cast<uint4*>(&codes[col][32 * blk]);
+    d[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    d[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    const int n = n0 + col;
+    const int kb32 = 4 * kb + blk;
+    const int tl = n / tile_n;
+    const int b = n % tile_n + row_off;  // B row of the tile
+    const size_t sblk = static_cast<size_t>(tl) * (K / kMxKB) + kb32 / 4;
+    sf[e * sf_estride + sblk * 2 * kMxSfBytes + (b >> 7) * kMxSfBytes + mx_sf_pos(b & 127, kb32 & 3)] =
+        static_cast<uint8_t>(sb);
+  }
+  __syncthreads();
+  // 64 code rows of 128 bytes: thread t stores 16-byte pieces t % 8 of rows t / 8 and t / 8 + 32
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = (t >> 3) + 32 * i;
+    if (r < ncols)
+      reinterpret_cast<uint4*>(wq + e * wq_estride + static_cast<size_t>(n0 + r) * K +
+                               static_cast<size_t>(kb) * kMxKB)[t & 7] =
+          *reinterpret_cast<const uint4*>(&codes[r][16 * (t & 7)]);
+  }
+}
+
+static unsigned mx_weight_blocks(int E, int K, int N) {
+  return static_cast<unsigned>(static_cast<long long>(E) * (K / kMxKB) * ((N + kMxWqCols - 1) / kMxWqCols));
 }
 
 cudaError_t launch_mx_quantize_rows(const __nv_bfloat16* x, long long M, int K, uint8_t* q, uint8_t* s,
@@ -93,18 +134,16 @@ cudaError_t launch_mx_quantize_weights(const moe_config& c, const __nv_bfloat16*
   err = cudaMemsetAsync(sf2, 0, mx_sf2_bytes(c), st);
   if (err != cudaSuccess) return err;
   // W1 and W3 of expert e land in w13q[e][0] and w13q[e][1]
-  const long long n1 = static_cast<long long>(E) * (H / kMxBlock) * F;
   const size_t sf13_e = static_cast<size_t>(nt1) * (H / kMxKB) * 2 * kMxSfBytes;
   for (int which = 0; which < 2; ++which) {
-    mx_quantize_weight_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, st>>>(
+    mx_quantize_weight_kernel<<<mx_weight_blocks(E, H, F), 256, 0, st>>>(
         which == 0 ? W1 : W3, E, H, F, w13q + static_cast<size_t>(which) * F * H, 2ull * F * H, sf13, sf13_e,
         kMxTileF1, which * kMxTileF1);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  const long long n2 = static_cast<long long>(E) * (F / kMxBlock) * H;
   const size_t sf2_e = static_cast<size_t>(nt2) * (F / kMxKB) * 2 * kMxSfBytes;
-  mx_quantize_weight_kernel<<<static_cast<unsigned>((n2 + 255) / 256), 256, 0, st>>>(
+  mx_quantize_weight_kernel<<<mx_weight_blocks(E, F, H), 256, 0, st>>>(
       W2, E, F, H, w2q, static_cast<size_t>(H) * F, sf2, sf2_e, kMxTileN2, 0);
   return cudaGetLastError();
 }
