@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay timing")
+    ap.add_argument("--no-lib-peaks", action="store_true",
+                    help="skip the vendor library's FP8/NVFP4 GEMM rates (low-precision fractions then take the "
+                         "nominal ratios to the measured bf16 peak)")
     ap.add_argument("--force-balanced", action="store_true", help="force-balanced routing (cyclic assignment)")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
     ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 grouped GEMM timing")
@@ -746,7 +749,8 @@ def run_ours(args, ls, rank, world, local_rank):
     # FP8 dense peak: the vendor FP8 GEMM's sustained rate measured in this
     # run, else the measured sustained bf16 peak times the nominal fp8 : bf16
     # ratio of the tensor cores (2)
-    fp8_meas = measured_fp8_peak(dev) if not args.no_mxfp8 and ls.H % 128 == 0 and ls.F % 128 == 0 else None
+    fp8_meas = (measured_fp8_peak(dev) if not args.no_mxfp8 and not args.no_lib_peaks and ls.H % 128 == 0
+                and ls.F % 128 == 0 else None)
     if fp8_meas is not None:
         peak8 = fp8_meas["sustained_tflops"]
         peak8_src = "measured in this run: " + fp8_meas["how"] + " (sustained)"
@@ -934,7 +938,7 @@ def run_ours(args, ls, rank, world, local_rank):
         # FP4 dense peak: the vendor NVFP4 GEMM's sustained rate measured in
         # this run, else the measured sustained bf16 peak times the nominal
         # fp4 : bf16 ratio (13.5 / 2.25)
-        fp4_meas = measured_fp4_peak(dev)
+        fp4_meas = None if args.no_lib_peaks else measured_fp4_peak(dev)
         if fp4_meas is not None:
             peak4 = fp4_meas["sustained_tflops"]
             peak4_src = "measured in this run: " + fp4_meas["how"] + " (sustained)"
